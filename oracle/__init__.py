@@ -1,0 +1,354 @@
+"""Plain CPU oracle of the FP8 FFN sublayer -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product (``realtime_transformer_gb300``
+and its CUDA library) never imports, links or calls it, and the two share no
+code: this package wraps ``frt_oracle.c`` (plain fp32 C, bit-level E4M3/BF16)
+through ctypes and loops over layers in Python.
+
+Every function cites the passage it restates (page title, section):
+  * agentlenshq "flashrt-project/FlashRT" summary, "Main ideas": fused
+    residual-norm-quantise, FP8 per-tensor calibration, cosine > 0.999.
+  * itsolotime FlashRT article, 5.2 (FusedGateUp + Quant), 7.1 (FP8 path),
+    7.2 (per-layer FFN loop).
+  * "FlashRT docs/architecture.md", 6 "Calibration Framework" and "What
+    happens when you call model.predict".
+
+Arrays are numpy: BF16 tensors travel as ``uint16`` bit patterns, E4M3 tensors
+as ``uint8`` codes, scales as Python floats (fp32 values).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from dataclasses import dataclass
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "frt_oracle.c")
+_LIB = os.path.join(_HERE, "libfrt_oracle.so")
+
+ACT_GEGLU_TANH = 0
+ACT_SWIGLU = 1
+EPS = 1e-6  # reading: the pages never state the RMSNorm epsilon
+
+
+def build(force: bool = False) -> str:
+    """Compile frt_oracle.c with gcc (fp contraction off, OpenMP on)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + ".tmp%d" % os.getpid()
+        cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-ffp-contract=off", "-fno-fast-math",
+               "-fPIC", "-shared", "-fvisibility=hidden", "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        build()
+        L = ctypes.CDLL(_LIB)
+        P = ctypes.c_void_p
+        i32, i64, f32, u8, u16 = ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_uint8, ctypes.c_uint16
+        sig = {
+            "orc_e4m3_decode": (f32, [u8]),
+            "orc_e4m3_encode": (u8, [f32]),
+            "orc_bf16_encode": (u16, [f32]),
+            "orc_bf16_decode": (f32, [u16]),
+            "orc_e4m3_encode_array": (None, [P, i64, P]),
+            "orc_bf16_encode_array": (None, [P, i64, P]),
+            "orc_scale_from_amax": (f32, [f32]),
+            "orc_amax_bf16": (f32, [P, i64]),
+            "orc_amax_f32": (f32, [P, i64]),
+            "orc_quantize_bf16": (None, [P, i64, f32, P]),
+            "orc_quantize_f32": (None, [P, i64, f32, P]),
+            "orc_quantize_weight": (f32, [P, i64, P]),
+            "orc_residual_rmsnorm": (None, [i32, i32, f32, P, P, P, P, P]),
+            "orc_gemm_e4m3": (None, [i32, i32, i32, P, P, P]),
+            "orc_gelu_tanh": (f32, [f32]),
+            "orc_silu": (f32, [f32]),
+            "orc_gated_act": (None, [i32, i32, i32, P, P]),
+            "orc_ffn_layer": (i32, [i32, i32, i32, i32, f32, P, P, P, P, P, f32, f32, f32, f32, P, P, P, P, P]),
+            "orc_calibrate_layer": (i32, [i32, i32, i32, i32, f32, i32, P, P, P, P, P, f32, f32,
+                                          ctypes.POINTER(f32), ctypes.POINTER(f32), P]),
+            "orc_ref_layer_f32": (i32, [i32, i32, i32, i32, f32, P, P, P, P, P, P, P]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _p(a: np.ndarray | None):
+    if a is None:
+        return None
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _u16(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.uint16)
+
+
+def _u8(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.uint8)
+
+
+# --------------------------------------------------------------------------
+# Number formats
+# --------------------------------------------------------------------------
+
+def e4m3_decode(codes) -> np.ndarray:
+    """E4M3 codes -> fp32 values (OCP E4M3 'fn' definition)."""
+    c = _u8(codes)
+    table = np.array([lib().orc_e4m3_decode(i) for i in range(256)], dtype=np.float32)
+    return table[c]
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """fp32 -> E4M3 codes, round to nearest even, saturating to +-448."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint8)
+    lib().orc_e4m3_encode_array(_p(x), x.size, _p(out))
+    return out
+
+
+def bf16_encode(x) -> np.ndarray:
+    """fp32 -> BF16 bit patterns, round to nearest even."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint16)
+    lib().orc_bf16_encode_array(_p(x), x.size, _p(out))
+    return out
+
+
+def bf16_decode(b) -> np.ndarray:
+    b = _u16(b)
+    return (b.astype(np.uint32) << 16).view(np.float32)
+
+
+def scale_from_amax(amax: float) -> float:
+    return float(lib().orc_scale_from_amax(amax))
+
+
+def recip(s: float) -> float:
+    """fp32 reciprocal 1/s, the multiplier every quantisation uses."""
+    return float(np.float32(1.0) / np.float32(s))
+
+
+# --------------------------------------------------------------------------
+# Steps
+# --------------------------------------------------------------------------
+
+def quantize_weight(w_bf16) -> tuple[np.ndarray, float]:
+    """Step A0: per-tensor E4M3 weight quantisation -> (codes, scale)."""
+    w = _u16(w_bf16)
+    q = np.empty(w.shape, dtype=np.uint8)
+    s = lib().orc_quantize_weight(_p(w), w.size, _p(q))
+    return q, float(s)
+
+
+def quantize_layer_weights(w_gate, w_up, w_down):
+    """Step A0 for one layer: one scale over [W_gate; W_up], one for W_down."""
+    w_gu = np.concatenate([_u16(w_gate), _u16(w_up)], axis=0)
+    q_gu, s_gu = quantize_weight(w_gu)
+    q_d, s_d = quantize_weight(w_down)
+    return q_gu, s_gu, q_d, s_d
+
+
+def residual_rmsnorm(r, h, w_norm, eps: float = EPS):
+    """Step A1 before quantisation -> (r' BF16 bits, y fp32)."""
+    r = _u16(r)
+    M, d = r.shape
+    hh = _u16(h) if h is not None else None
+    w = _u16(w_norm)
+    rp = np.empty((M, d), dtype=np.uint16)
+    y = np.empty((M, d), dtype=np.float32)
+    lib().orc_residual_rmsnorm(M, d, eps, _p(r), _p(hh), _p(w), _p(rp), _p(y))
+    return rp, y
+
+
+def quantize_f32(x, inv_s: float) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    q = np.empty(x.shape, dtype=np.uint8)
+    lib().orc_quantize_f32(_p(x), x.size, inv_s, _p(q))
+    return q
+
+
+def amax_f32(x) -> float:
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    return float(lib().orc_amax_f32(_p(x), x.size))
+
+
+def gemm_e4m3(A, B) -> np.ndarray:
+    """acc = dec(A) dec(B)^T in fp32, k ascending; A [M,K], B [N,K] codes."""
+    A = _u8(A)
+    B = _u8(B)
+    M, K = A.shape
+    N, K2 = B.shape
+    assert K == K2
+    acc = np.empty((M, N), dtype=np.float32)
+    lib().orc_gemm_e4m3(M, N, K, _p(A), _p(B), _p(acc))
+    return acc
+
+
+def gelu_tanh(g: float) -> float:
+    return float(lib().orc_gelu_tanh(g))
+
+
+def silu(g: float) -> float:
+    return float(lib().orc_silu(g))
+
+
+def gated_act(gu_bf16, act: int) -> np.ndarray:
+    """Step A3 before quantisation: a = act(g) * u from the BF16 [M, 2ff] GEMM output."""
+    gu = _u16(gu_bf16)
+    M, two_ff = gu.shape
+    ff = two_ff // 2
+    a = np.empty((M, ff), dtype=np.float32)
+    lib().orc_gated_act(M, ff, act, _p(gu), _p(a))
+    return a
+
+
+@dataclass
+class LayerTrace:
+    out: np.ndarray       # [M,d] BF16 bits
+    r_prime: np.ndarray   # [M,d] BF16 bits
+    q_x: np.ndarray       # [M,d] E4M3 codes
+    gu: np.ndarray        # [M,2ff] BF16 bits
+    q_h: np.ndarray       # [M,ff] E4M3 codes
+
+
+def ffn_layer(r, h, w_norm, q_gu, q_down, s_x, s_h, s_gu, s_d, act: int, eps: float = EPS,
+              trace: bool = False):
+    """Steps A1..A4 of one layer with fixed scales -> out (or a LayerTrace)."""
+    r = _u16(r)
+    M, d = r.shape
+    q_gu = _u8(q_gu)
+    q_down = _u8(q_down)
+    ff = q_down.shape[1]
+    assert q_gu.shape == (2 * ff, d) and q_down.shape == (d, ff)
+    hh = _u16(h) if h is not None else None
+    out = np.empty((M, d), dtype=np.uint16)
+    if trace:
+        rp = np.empty((M, d), dtype=np.uint16)
+        qx = np.empty((M, d), dtype=np.uint8)
+        gu = np.empty((M, 2 * ff), dtype=np.uint16)
+        qh = np.empty((M, ff), dtype=np.uint8)
+    else:
+        rp = qx = gu = qh = None
+    rc = lib().orc_ffn_layer(M, d, ff, act, eps, _p(r), _p(hh), _p(_u16(w_norm)), _p(q_gu), _p(q_down),
+                             s_x, s_h, s_gu, s_d, _p(out), _p(rp), _p(qx), _p(gu), _p(qh))
+    if rc != 0:
+        raise MemoryError("oracle layer allocation failed")
+    if trace:
+        return LayerTrace(out, rp, qx, gu, qh)
+    return out
+
+
+def calibrate_layer(r_batches, h_batches, w_norm, q_gu, q_down, s_gu, s_d, act: int, eps: float = EPS):
+    """Step A6 for one layer: progressive amax over the calibration batches.
+
+    Returns (s_x, s_h, next_residuals)."""
+    rb = [_u16(r) for r in r_batches]
+    M, d = rb[0].shape
+    ff = _u8(q_down).shape[1]
+    nb = len(rb)
+    hb = [_u16(h) for h in h_batches] if h_batches is not None else None
+    outs = [np.empty((M, d), dtype=np.uint16) for _ in range(nb)]
+    P = ctypes.c_void_p
+    r_arr = (P * nb)(*[_p(a) for a in rb])
+    h_arr = (P * nb)(*[_p(a) for a in hb]) if hb is not None else None
+    o_arr = (P * nb)(*[_p(a) for a in outs])
+    sx = ctypes.c_float()
+    sh = ctypes.c_float()
+    rc = lib().orc_calibrate_layer(M, d, ff, act, eps, nb, ctypes.cast(r_arr, P),
+                                   ctypes.cast(h_arr, P) if h_arr is not None else None,
+                                   _p(_u16(w_norm)), _p(_u8(q_gu)), _p(_u8(q_down)), s_gu, s_d,
+                                   ctypes.byref(sx), ctypes.byref(sh), ctypes.cast(o_arr, P))
+    if rc != 0:
+        raise MemoryError("oracle calibration allocation failed")
+    return float(sx.value), float(sh.value), outs
+
+
+def ref_layer_f32(r, h, w_norm, w_gate, w_up, w_down, act: int, eps: float = EPS) -> np.ndarray:
+    """Unquantised fp32 layer (the baseline of the cosine > 0.999 claim)."""
+    r = np.ascontiguousarray(r, dtype=np.float32)
+    M, d = r.shape
+    ff = _u16(w_gate).shape[0]
+    hh = np.ascontiguousarray(h, dtype=np.float32) if h is not None else None
+    out = np.empty((M, d), dtype=np.float32)
+    rc = lib().orc_ref_layer_f32(M, d, ff, act, eps, _p(r), _p(hh), _p(_u16(w_norm)), _p(_u16(w_gate)),
+                                 _p(_u16(w_up)), _p(_u16(w_down)), _p(out))
+    if rc != 0:
+        raise MemoryError("oracle reference allocation failed")
+    return out
+
+
+# --------------------------------------------------------------------------
+# Stack (step A5 semantics: r_{l+1} = out_l, hidden added at layer 0 only)
+# --------------------------------------------------------------------------
+
+@dataclass
+class QuantLayer:
+    w_norm: np.ndarray
+    q_gu: np.ndarray
+    s_gu: float
+    q_down: np.ndarray
+    s_d: float
+
+
+def quantize_stack(layers) -> list[QuantLayer]:
+    """Step A0 over a list of dicts with w_norm, w_gate, w_up, w_down (BF16 bits)."""
+    out = []
+    for lw in layers:
+        q_gu, s_gu, q_d, s_d = quantize_layer_weights(lw["w_gate"], lw["w_up"], lw["w_down"])
+        out.append(QuantLayer(_u16(lw["w_norm"]), q_gu, s_gu, q_d, s_d))
+    return out
+
+
+def calibrate_stack(qlayers, r_batches, h_batches, act: int, eps: float = EPS):
+    """Step A6 over the stack -> (s_x[L], s_h[L])."""
+    s_x, s_h = [], []
+    rb = list(r_batches)
+    hb = list(h_batches) if h_batches is not None else None
+    for l, ql in enumerate(qlayers):
+        sx, sh, rb = calibrate_layer(rb, hb if l == 0 else None, ql.w_norm, ql.q_gu, ql.q_down,
+                                     ql.s_gu, ql.s_d, act, eps)
+        s_x.append(sx)
+        s_h.append(sh)
+    return s_x, s_h
+
+
+def stack_forward(qlayers, r, h, s_x, s_h, act: int, eps: float = EPS, trace: bool = False):
+    """Quantised forward through all layers -> final out (or per-layer traces)."""
+    cur = _u16(r)
+    traces = []
+    for l, ql in enumerate(qlayers):
+        res = ffn_layer(cur, h if l == 0 else None, ql.w_norm, ql.q_gu, ql.q_down, s_x[l], s_h[l],
+                        ql.s_gu, ql.s_d, act, eps, trace=trace)
+        if trace:
+            traces.append(res)
+            cur = res.out
+        else:
+            cur = res
+    return traces if trace else cur
+
+
+def ref_stack_f32(layers, r, h, act: int, eps: float = EPS) -> np.ndarray:
+    """fp32 unquantised forward through all layers (BF16 master weights)."""
+    cur = bf16_decode(r) if np.asarray(r).dtype == np.uint16 else np.asarray(r, dtype=np.float32)
+    hf = None
+    if h is not None:
+        hf = bf16_decode(h) if np.asarray(h).dtype == np.uint16 else np.asarray(h, dtype=np.float32)
+    for l, lw in enumerate(layers):
+        cur = ref_layer_f32(cur, hf if l == 0 else None, lw["w_norm"], lw["w_gate"], lw["w_up"],
+                            lw["w_down"], act, eps)
+    return cur

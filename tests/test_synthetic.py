@@ -1,0 +1,51 @@
+"""The seeded input recipe: shapes, determinism, outlier channels."""
+import math
+
+import torch
+
+import synthetic
+
+
+def test_shapes_and_dtypes():
+    wl = synthetic.WORKLOADS["tiny"]
+    w = synthetic.layer_weights(wl, 0)
+    assert w["w_norm"].shape == (256,) and w["w_gate"].shape == (1024, 256)
+    assert w["w_up"].shape == (1024, 256) and w["w_down"].shape == (256, 1024)
+    assert all(v.dtype == torch.bfloat16 for v in w.values())
+    r, h = synthetic.inputs(wl)
+    assert r.shape == (8, 256) and h.shape == (8, 256) and r.dtype == torch.bfloat16
+    assert len(synthetic.calibration_batches(wl)) == 4
+
+
+def test_deterministic_and_layers_independent():
+    wl = synthetic.WORKLOADS["tiny"].with_(L=3)
+    a = synthetic.layer_weights(wl, 1)
+    b = synthetic.layer_weights(wl, 1)
+    c = synthetic.layer_weights(wl, 2)
+    assert torch.equal(a["w_gate"], b["w_gate"])
+    assert not torch.equal(a["w_gate"], c["w_gate"])
+    assert not torch.equal(a["w_gate"], a["w_up"])
+
+
+def test_outlier_channels():
+    for name, wl in synthetic.WORKLOADS.items():
+        ch = synthetic.outlier_channels(wl)
+        if not wl.outliers:
+            assert ch == []
+            continue
+        assert len(ch) == math.ceil(0.001 * wl.d)
+        r, h = synthetic.inputs(wl, M=64)
+        rms = r.float().pow(2).mean(0).sqrt()
+        mask = torch.zeros(wl.d, dtype=torch.bool)
+        mask[ch] = True
+        assert rms[mask].min() > 10 and rms[~mask].max() < 2
+        (rc, hc), = synthetic.calibration_batches(wl, M=64)
+        assert rc.float().pow(2).mean(0).sqrt()[mask].min() > 10
+
+
+def test_distribution():
+    wl = synthetic.WORKLOADS["vla_action_expert"]
+    w = synthetic.layer_weights(wl, 0)
+    assert abs(w["w_gate"].float().std().item() - 0.02) < 1e-3
+    assert abs(w["w_norm"].float().mean().item() - 1.0) < 0.02
+    assert abs(w["w_norm"].float().std().item() - 0.1) < 0.01
