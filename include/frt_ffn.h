@@ -1,0 +1,191 @@
+/*
+ * frt_ffn.h -- C ABI of the GB300 (sm_103a) FP8 FFN sublayer library
+ * (libfrt_ffn.so).
+ *
+ * The library runs the FP8-quantised pre-norm transformer FFN sublayer,
+ * stacked n_layers deep, on one GPU:
+ *
+ *   A1  r' = bf16(r + h);  y = r' / sqrt(mean(r'^2) + eps) * w_norm;
+ *       q_x = E4M3(y / s_x)
+ *   A2  [g | u] = bf16((q_x . W_gu^T) * s_x * s_gu)         (FP8 GEMM)
+ *   A3  q_h = E4M3(act(g) * u / s_h)   act = GELU(tanh) or SiLU
+ *   A4  out = bf16(r' + (q_h . W_down^T) * s_h * s_down)    (FP8 GEMM)
+ *
+ * Passages (page title, section):
+ *   - agentlenshq "flashrt-project/FlashRT" summary, "Main ideas": kernels
+ *     for fused residual-norm-quantise and FP8 GEMM bundled into static CUDA
+ *     graphs; FP8 weights and activations with per-tensor calibration cached
+ *     as JSON.
+ *   - itsolotime FlashRT article, 4.1-4.2 (graph capture of a pointer-only
+ *     forward, Relaxed capture mode, no allocation during replay), 5.2
+ *     (FusedGateUp quantised as one tensor), 7.1 (FP8 path), 7.2 (the FFN
+ *     layer loop: norm, gate/up GEMM, gated activation + requantise, down
+ *     GEMM, residual add).
+ *   - "FlashRT docs/architecture.md": "exec/" (a C ABI execution contract of
+ *     Buffer / Graph / Plan), 6 "Calibration Framework" (amax per FP8 GEMM
+ *     input; alpha = act_scale x weight_scale baked as host scalars), 7
+ *     "CUDA Graph Capture" (pointer-only forward, no allocation in replay).
+ *
+ * Conventions for every call:
+ *   - Tensors are row-major and dense.  BF16 tensors are the 16-bit bfloat16
+ *     bit patterns; E4M3 tensors are OCP FP8 E4M3 ("fn") bytes.
+ *   - Device pointers are pointers into the current CUDA device's memory and
+ *     must be 16-byte aligned; host pointers are ordinary host memory.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
+ *     that take a stream enqueue work on it and return before the GPU has
+ *     finished, unless a call says it synchronises.
+ *   - No call throws.  Each returns an frt_status; on failure
+ *     frt_ffn_last_error() gives a message (per host thread).
+ *   - A plan is used from one host thread at a time.
+ */
+#ifndef FRT_FFN_H
+#define FRT_FFN_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct frt_ffn_plan *frt_ffn_plan_t;
+typedef void *frt_stream_t; /* cudaStream_t */
+
+typedef enum {
+    FRT_OK = 0,
+    FRT_ERR_INVALID_ARG = 1,    /* null/misaligned pointer, bad size or layer index */
+    FRT_ERR_UNSUPPORTED = 2,    /* shape outside what the kernels support, or wrong GPU */
+    FRT_ERR_OOM = 3,            /* a device allocation failed */
+    FRT_ERR_NOT_READY = 4,      /* weights not loaded or scales not calibrated/set */
+    FRT_ERR_SHAPE = 5,          /* M > M_max */
+    FRT_ERR_CAPTURE = 6,        /* stream capture failed, or no graph for this M */
+    FRT_ERR_STALE_GRAPH = 7,    /* scales changed after the graph was captured */
+    FRT_ERR_CUDA = 8,           /* a CUDA runtime call failed (message has the name) */
+    FRT_ERR_DEVICE_TIMEOUT = 9  /* a kernel gave up a bounded wait (see frt_ffn_device_status) */
+} frt_status;
+
+typedef enum { FRT_ACT_GEGLU_TANH = 0, FRT_ACT_SWIGLU = 1 } frt_act;
+
+/*
+ * Create a plan for a stack of n_layers FFN sublayers of model width d and
+ * hidden width ff, gated activation act, at most M_max tokens per call.
+ * Allocates, on the current device, the FP8 weight arena (layer-major,
+ * [W_gate; W_up] as one [2ff, d] matrix and W_down [d, ff] per layer, the
+ * flat concatenated buffers of the itsolotime article, 5.2 "FlatCat"), the
+ * BF16 norm weights, and all scratch sized by M_max.  Nothing is allocated
+ * later by forward, capture or replay.
+ * Requires: d % 128 == 0, ff % 128 == 0, 1 <= M_max <= 65536,
+ * 1 <= n_layers <= 4096, a compute-capability 10.3 device.
+ * Errors: INVALID_ARG, UNSUPPORTED, OOM, CUDA.  *out is NULL on failure.
+ */
+frt_status frt_ffn_plan_create(int d, int ff, int act, int M_max, int n_layers, frt_ffn_plan_t *out);
+
+/* Free the plan, its device memory and its captured graphs.  Synchronises
+ * the device first.  NULL is accepted. */
+frt_status frt_ffn_plan_destroy(frt_ffn_plan_t plan);
+
+/*
+ * Step A0 (itsolotime article, 5.2 FusedGateUp + Quant; "scale_into"):
+ * quantise one layer's BF16 master weights into the plan's E4M3 arena with
+ * per-tensor scales s_gu = amax([W_gate; W_up]) / 448 and
+ * s_down = amax(W_down) / 448 (an all-zero tensor gets scale 1).
+ * w_norm [d], w_gate [ff, d], w_up [ff, d], w_down [d, ff]: BF16, device,
+ * row-major (nn.Linear layout, so every GEMM operand is K-major).  The plan
+ * copies what it needs; the caller keeps ownership of its buffers.
+ * Synchronises `stream` (the scales are read back to the host).
+ * Errors: INVALID_ARG (null/misaligned pointer, layer out of range), CUDA.
+ */
+frt_status frt_ffn_load_weights(frt_ffn_plan_t plan, int layer, const void *w_norm, const void *w_gate,
+                                const void *w_up, const void *w_down, frt_stream_t stream);
+
+/*
+ * Step A6 ("FlashRT docs/architecture.md", 6 Calibration Framework: amax per
+ * FP8 GEMM input; "What happens when you call model.predict": run one
+ * forward and record amax).  Progressive, layer by layer: for layer l the
+ * amax of y over all batches gives s_x[l] = amax / 448; the batches are then
+ * quantised with it and run through the gate/up GEMM and activation, whose
+ * amax gives s_h[l]; the batches are finished with s_h[l] and become the
+ * inputs of layer l + 1.  residual[b] and hidden[b] (hidden may be NULL, or
+ * may hold NULL entries) are n_batches host arrays of device pointers to BF16
+ * [M, d]; hidden is added at layer 0 only.  Needs all layers' weights.
+ * Allocates temporary device memory for the batches' running residuals and
+ * frees it before returning; synchronises `stream`.  Marks captured graphs
+ * stale.  Errors: INVALID_ARG, NOT_READY, SHAPE, OOM, CUDA, DEVICE_TIMEOUT.
+ */
+frt_status frt_ffn_calibrate(frt_ffn_plan_t plan, const void *const *residual, const void *const *hidden,
+                             int n_batches, int M, frt_stream_t stream);
+
+/* Copy the scales to host arrays of n_layers floats each (any may be NULL).
+ * s_x, s_h are 0 until calibrated or set.  Errors: INVALID_ARG. */
+frt_status frt_ffn_get_scales(frt_ffn_plan_t plan, float *s_x, float *s_h, float *s_gu, float *s_down);
+
+/* Set the activation scales (e.g. from a calibration cache) from host arrays
+ * of n_layers positive finite floats.  Graphs captured before are stale: their
+ * alpha values are baked in ("FlashRT docs/architecture.md", 6).
+ * Errors: INVALID_ARG. */
+frt_status frt_ffn_set_scales(frt_ffn_plan_t plan, const float *s_x, const float *s_h);
+
+/*
+ * Eager forward through all layers (steps A1..A4 per layer, step A5's stack):
+ * residual_in [M, d] BF16 (device), hidden_in [M, d] BF16 or NULL (added at
+ * layer 0 only), out [M, d] BF16 (device; may alias residual_in).  0 <= M <=
+ * M_max; M == 0 does nothing.  Allocates nothing.
+ * Errors: INVALID_ARG, NOT_READY, SHAPE, CUDA (launch errors).  Errors inside
+ * kernels surface through frt_ffn_device_status.
+ */
+frt_status frt_ffn_forward(frt_ffn_plan_t plan, const void *residual_in, const void *hidden_in, void *out, int M,
+                           frt_stream_t stream);
+
+/*
+ * Capture the forward for token count M into a CUDA graph owned by the plan
+ * (itsolotime article, 4.1: cudaStreamBeginCapture in Relaxed mode on this
+ * stream only; 4.2: stable pointers, no allocation).  The pointers are baked
+ * into the graph; replay reads and writes the same buffers.  `stream` must be
+ * a non-default stream that is not capturing.  Replaces a graph already held
+ * for this M.  Errors: INVALID_ARG, NOT_READY, SHAPE, CAPTURE, CUDA.
+ */
+frt_status frt_ffn_graph_capture(frt_ffn_plan_t plan, const void *residual_in, const void *hidden_in, void *out,
+                                 int M, frt_stream_t stream);
+
+/* Launch the graph captured for M on `stream` (one cudaGraphLaunch).
+ * Errors: CAPTURE (no graph for M), STALE_GRAPH (scales changed since the
+ * capture), CUDA. */
+frt_status frt_ffn_graph_replay(frt_ffn_plan_t plan, int M, frt_stream_t stream);
+
+/*
+ * Test/diagnostic: run layer `layer` alone on residual_in (+ hidden_in if not
+ * NULL) and copy its intermediates to caller device buffers (each may be
+ * NULL): r_prime [M, d] BF16, q_x [M, d] E4M3, gu [M, 2ff] BF16 (g then u),
+ * q_h [M, ff] E4M3, out [M, d] BF16.  Runs the same kernels as the forward
+ * for this M.  Errors: as frt_ffn_forward.
+ */
+frt_status frt_ffn_debug_trace(frt_ffn_plan_t plan, int layer, const void *residual_in, const void *hidden_in,
+                               int M, void *r_prime, void *q_x, void *gu, void *q_h, void *out, frt_stream_t stream);
+
+/*
+ * Synchronise `stream` and report kernel-side failures: DEVICE_TIMEOUT if a
+ * kernel of this plan gave up a bounded wait since the last call (the flag is
+ * then cleared), else OK.  Errors: CUDA.
+ */
+frt_status frt_ffn_device_status(frt_ffn_plan_t plan, frt_stream_t stream);
+
+/*
+ * Test/diagnostic: the plan's FP8 GEMM kernels on caller buffers,
+ * C[m][n] = alpha * sum_k A[m][k] B[n][k] stored as fp32 (the contraction of
+ * steps A2/A4, itsolotime article 7.2).  A [M, K] and B [N, K] E4M3 (device,
+ * K-major, 16-byte aligned), C [M, N] fp32 (device).  path: 0 = pick as the
+ * forward does, 1 = weight-streaming (B rows on the MMA's 128-row side, the M
+ * tokens on its narrow side; M <= 64), 2 = tiled (128 x 256 or 128 x 128
+ * tiles).  splits: 0 = pick, else the split-K factor.  Uses the plan's
+ * split-K workspace and error word.  Requires K % 16 == 0, N % 128 == 0,
+ * 1 <= M <= 65536, 16 <= K.  Synchronises nothing.
+ * Errors: INVALID_ARG, UNSUPPORTED, CUDA.
+ */
+frt_status frt_fp8_gemm(frt_ffn_plan_t plan, const void *A, const void *B, void *C, int M, int N, int K,
+                        float alpha, int path, int splits, frt_stream_t stream);
+
+/* Message of the last failed call on this host thread ("" if none). */
+const char *frt_ffn_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FRT_FFN_H */

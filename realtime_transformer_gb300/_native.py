@@ -1,0 +1,145 @@
+"""ctypes binding of libfrt_ffn.so (include/frt_ffn.h).
+
+Argument marshalling only: every step of the FFN path runs in the CUDA
+library.  The functions keep the C names; a non-OK status raises FrtError
+with the library's message.  There is no fallback: if the library has not
+been built, loading raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfrt_ffn.so")
+
+FRT_OK = 0
+STATUS = {
+    0: "FRT_OK", 1: "FRT_ERR_INVALID_ARG", 2: "FRT_ERR_UNSUPPORTED", 3: "FRT_ERR_OOM", 4: "FRT_ERR_NOT_READY",
+    5: "FRT_ERR_SHAPE", 6: "FRT_ERR_CAPTURE", 7: "FRT_ERR_STALE_GRAPH", 8: "FRT_ERR_CUDA",
+    9: "FRT_ERR_DEVICE_TIMEOUT",
+}
+FRT_ACT_GEGLU_TANH = 0
+FRT_ACT_SWIGLU = 1
+
+# every symbol include/frt_ffn.h declares, with (restype, argtypes)
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+_FP = ctypes.POINTER(ctypes.c_float)
+SIGNATURES = {
+    "frt_ffn_plan_create": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(_P)]),
+    "frt_ffn_plan_destroy": (_I, [_P]),
+    "frt_ffn_load_weights": (_I, [_P, _I, _P, _P, _P, _P, _P]),
+    "frt_ffn_calibrate": (_I, [_P, ctypes.POINTER(_P), ctypes.POINTER(_P), _I, _I, _P]),
+    "frt_ffn_get_scales": (_I, [_P, _FP, _FP, _FP, _FP]),
+    "frt_ffn_set_scales": (_I, [_P, _FP, _FP]),
+    "frt_ffn_forward": (_I, [_P, _P, _P, _P, _I, _P]),
+    "frt_ffn_graph_capture": (_I, [_P, _P, _P, _P, _I, _P]),
+    "frt_ffn_graph_replay": (_I, [_P, _I, _P]),
+    "frt_ffn_debug_trace": (_I, [_P, _I, _P, _P, _I, _P, _P, _P, _P, _P, _P]),
+    "frt_ffn_device_status": (_I, [_P, _P]),
+    "frt_fp8_gemm": (_I, [_P, _P, _P, _P, _I, _I, _I, _F, _I, _I, _P]),
+    "frt_ffn_last_error": (ctypes.c_char_p, []),
+}
+
+
+class FrtError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__("%s: %s" % (STATUS.get(status, str(status)), message))
+        self.status = status
+        self.name = STATUS.get(status, str(status))
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libfrt_ffn.so (built by realtime_transformer_gb300.build)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError("libfrt_ffn.so is not built; run `python -m realtime_transformer_gb300.build` "
+                              "(or __graft_entry__.build())")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(status: int) -> None:
+    if status != FRT_OK:
+        msg = lib().frt_ffn_last_error()
+        raise FrtError(status, msg.decode() if msg else "")
+
+
+def _ptrs(values):
+    arr = (_P * len(values))(*[v if v else None for v in values])
+    return arr
+
+
+def frt_ffn_plan_create(d: int, ff: int, act: int, M_max: int, n_layers: int) -> int:
+    out = _P()
+    _check(lib().frt_ffn_plan_create(d, ff, act, M_max, n_layers, ctypes.byref(out)))
+    return out.value
+
+
+def frt_ffn_plan_destroy(plan: int) -> None:
+    _check(lib().frt_ffn_plan_destroy(plan))
+
+
+def frt_ffn_load_weights(plan, layer, w_norm, w_gate, w_up, w_down, stream) -> None:
+    _check(lib().frt_ffn_load_weights(plan, layer, w_norm, w_gate, w_up, w_down, stream))
+
+
+def frt_ffn_calibrate(plan, residual_ptrs, hidden_ptrs, M, stream) -> None:
+    n = len(residual_ptrs)
+    r = _ptrs(residual_ptrs)
+    h = _ptrs(hidden_ptrs) if hidden_ptrs is not None else None
+    _check(lib().frt_ffn_calibrate(plan, ctypes.cast(r, ctypes.POINTER(_P)),
+                                   ctypes.cast(h, ctypes.POINTER(_P)) if h is not None else None, n, M, stream))
+
+
+def frt_ffn_get_scales(plan, n_layers: int):
+    arrs = [(ctypes.c_float * n_layers)() for _ in range(4)]
+    _check(lib().frt_ffn_get_scales(plan, *[ctypes.cast(a, _FP) for a in arrs]))
+    return [list(a) for a in arrs]
+
+
+def frt_ffn_set_scales(plan, s_x, s_h) -> None:
+    n = len(s_x)
+    ax = (ctypes.c_float * n)(*s_x)
+    ah = (ctypes.c_float * n)(*s_h)
+    _check(lib().frt_ffn_set_scales(plan, ctypes.cast(ax, _FP), ctypes.cast(ah, _FP)))
+
+
+def frt_ffn_forward(plan, residual_in, hidden_in, out, M, stream) -> None:
+    _check(lib().frt_ffn_forward(plan, residual_in, hidden_in, out, M, stream))
+
+
+def frt_ffn_graph_capture(plan, residual_in, hidden_in, out, M, stream) -> None:
+    _check(lib().frt_ffn_graph_capture(plan, residual_in, hidden_in, out, M, stream))
+
+
+def frt_ffn_graph_replay(plan, M, stream) -> None:
+    _check(lib().frt_ffn_graph_replay(plan, M, stream))
+
+
+def frt_ffn_debug_trace(plan, layer, residual_in, hidden_in, M, r_prime, q_x, gu, q_h, out, stream) -> None:
+    _check(lib().frt_ffn_debug_trace(plan, layer, residual_in, hidden_in, M, r_prime, q_x, gu, q_h, out, stream))
+
+
+def frt_ffn_device_status(plan, stream) -> None:
+    _check(lib().frt_ffn_device_status(plan, stream))
+
+
+def frt_fp8_gemm(plan, A, B, C, M, N, K, alpha, path, splits, stream) -> None:
+    _check(lib().frt_fp8_gemm(plan, A, B, C, M, N, K, alpha, path, splits, stream))
+
+
+def frt_ffn_last_error() -> str:
+    msg = lib().frt_ffn_last_error()
+    return msg.decode() if msg else ""

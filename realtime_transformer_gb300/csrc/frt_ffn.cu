@@ -1,0 +1,653 @@
+// frt_ffn.cu -- the plan object behind the C ABI of include/frt_ffn.h.
+//
+// The plan owns everything the forward touches besides the caller's
+// input/output buffers: the E4M3 weight arena (layer-major, [W_gate; W_up]
+// then W_down per layer -- the flat concatenated buffers of the itsolotime
+// FlashRT article, 5.2 "FlatCat"), BF16 norm weights, per-layer scales, all
+// scratch sized by M_max, the split-K workspace, TMA descriptors, and the
+// CUDA graphs captured per token count ("FlashRT docs/architecture.md", 7
+// CUDA Graph Capture: pointer-only forward, no allocation during replay;
+// "exec/": a C ABI Buffer / Graph / Plan contract).
+//
+// Per layer the forward launches four kernels on the caller's stream, each
+// with a programmatic-dependent-launch edge to its predecessor:
+//   A1 norm_quant -> A2 FP8 gate/up GEMM -> A3 act_quant -> A4 FP8 down GEMM
+// (itsolotime article, 7.2: the FFN layer loop).
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <string>
+#include <utility>
+#include <vector>
+
+#include "frt_ffn.h"
+#include "frt_internal.h"
+
+#define FRT_API extern "C" __attribute__((visibility("default")))
+
+using namespace frt;
+
+namespace {
+
+constexpr float RMS_EPS = 1e-6f;     // reading: the pages never state the epsilon
+constexpr int SWAP_MAX_TOKENS = 64;  // weight-streaming GEMM path up to this many tokens
+constexpr int COUNTERS_PER_GEMM = 4096;
+constexpr int N_GEMM_SITES = 2;      // gate/up and down keep separate split-K counters
+
+thread_local std::string g_last_error;
+
+frt_status fail(frt_status st, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
+frt_status cuda_fail(cudaError_t e, const char *what) {
+    return fail(e == cudaErrorMemoryAllocation ? FRT_ERR_OOM : FRT_ERR_CUDA, "%s: %s (%s)", what,
+                cudaGetErrorString(e), cudaGetErrorName(e));
+}
+
+#define CK(call)                                   \
+    do {                                           \
+        cudaError_t e_ = (call);                   \
+        if (e_ != cudaSuccess)                     \
+            return cuda_fail(e_, #call);           \
+    } while (0)
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+float scale_from_amax(float amax) { return amax == 0.0f ? 1.0f : amax / 448.0f; }
+
+enum Buf { B_WGU = 0, B_WDOWN = 1, B_QX = 2, B_QH = 3 };
+
+struct GraphEntry {
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+    uint64_t version = 0;
+};
+
+}  // namespace
+
+struct frt_ffn_plan {
+    int d = 0, ff = 0, act = 0, M_max = 0, L = 0;
+    int dev = 0, num_sms = 0, M_alloc = 0;
+    uint8_t *w_gu = nullptr, *w_down = nullptr;
+    uint16_t *w_norm = nullptr;
+    std::vector<float> s_gu, s_d, s_x, s_h;
+    std::vector<char> loaded;
+    bool scales_ok = false;
+    uint64_t version = 1;
+    uint16_t *rbuf[2] = {nullptr, nullptr};
+    uint16_t *rprime = nullptr, *gu = nullptr;
+    uint8_t *qx = nullptr, *qh = nullptr;
+    float *ws = nullptr;
+    size_t ws_floats = 0;
+    int *counters = nullptr;
+    unsigned *amax = nullptr;  // [2]
+    int *err = nullptr;
+    std::map<std::pair<int, int>, CUtensorMap> tmaps;
+    std::map<int, GraphEntry> graphs;
+    int force_path = 0;        // 0 auto, 1 swap, 2 tiled (FRT_FFN_FORCE_PATH)
+};
+
+namespace {
+
+frt_status get_tmap(frt_ffn_plan *P, int buf, int box_rows, CUtensorMap *out) {
+    auto key = std::make_pair(buf, box_rows);
+    auto it = P->tmaps.find(key);
+    if (it != P->tmaps.end()) {
+        *out = it->second;
+        return FRT_OK;
+    }
+    CUtensorMap m;
+    cudaError_t e;
+    switch (buf) {
+    case B_WGU: e = encode_tmap_u8(&m, P->w_gu, (uint64_t)P->L * 2 * P->ff, P->d, box_rows); break;
+    case B_WDOWN: e = encode_tmap_u8(&m, P->w_down, (uint64_t)P->L * P->d, P->ff, box_rows); break;
+    case B_QX: e = encode_tmap_u8(&m, P->qx, P->M_alloc, P->d, box_rows); break;
+    default: e = encode_tmap_u8(&m, P->qh, P->M_alloc, P->ff, box_rows); break;
+    }
+    if (e != cudaSuccess)
+        return fail(FRT_ERR_CUDA, "cuTensorMapEncodeTiled failed for buffer %d box %d", buf, box_rows);
+    P->tmaps[key] = m;
+    *out = m;
+    return FRT_OK;
+}
+
+bool use_swap(const frt_ffn_plan *P, int M) {
+    if (P->force_path == 1)
+        return M <= SWAP_MAX_TOKENS;
+    if (P->force_path == 2)
+        return false;
+    return M <= SWAP_MAX_TOKENS;
+}
+
+// Fill a GEMM launch for one of the two sites of layer l.
+frt_status setup_gemm(frt_ffn_plan *P, GemmLaunch &g, int site, int l, int M) {
+    const bool swap = use_swap(P, M);
+    const int N = site == 0 ? 2 * P->ff : P->d;
+    const int K = site == 0 ? P->d : P->ff;
+    const int wbuf = site == 0 ? B_WGU : B_WDOWN;
+    const int xbuf = site == 0 ? B_QX : B_QH;
+    memset(&g.p, 0, sizeof g.p);
+    plan_gemm(g, swap, M, N, K, P->num_sms, 0);
+    frt_status st;
+    if (swap) {
+        if ((st = get_tmap(P, wbuf, 128, &g.tmP)) != FRT_OK) return st;
+        if ((st = get_tmap(P, xbuf, g.bn, &g.tmQ)) != FRT_OK) return st;
+        g.p.p_row0 = l * N;
+        g.p.q_row0 = 0;
+    } else {
+        if ((st = get_tmap(P, xbuf, 128, &g.tmP)) != FRT_OK) return st;
+        if ((st = get_tmap(P, wbuf, g.bn, &g.tmQ)) != FRT_OK) return st;
+        g.p.p_row0 = 0;
+        g.p.q_row0 = l * N;
+    }
+    if (gemm_ws_floats(g) > P->ws_floats || (g.p.splits > 1 && gemm_tiles(g) > COUNTERS_PER_GEMM))
+        return fail(FRT_ERR_UNSUPPORTED, "split-K workspace too small for M=%d site %d", M, site);
+    g.p.ws = P->ws;
+    g.p.counters = P->counters + site * COUNTERS_PER_GEMM;
+    g.p.err = P->err;
+    return FRT_OK;
+}
+
+// One layer: A1 -> A2 -> A3 -> A4.  `out` receives the layer output; when
+// hid != null, r' is materialised in P->rprime and used as A4's residual.
+frt_status run_layer(frt_ffn_plan *P, int l, const void *in, const void *hid, void *out, int M, cudaStream_t s,
+                     void *trace_rprime, void *trace_qx, void *trace_gu, void *trace_qh) {
+    const int d = P->d, ff = P->ff;
+    const float s_x = P->s_x[l], s_h = P->s_h[l];
+    const float inv_sx = 1.0f / s_x, inv_sh = 1.0f / s_h;
+    void *rp = hid ? (void *)P->rprime : nullptr;
+    CK(launch_norm_quant(in, hid, P->w_norm + (size_t)l * d, M, d, RMS_EPS, inv_sx, rp, P->qx, nullptr, false, s,
+                         true));
+    GemmLaunch g;
+    frt_status st = setup_gemm(P, g, 0, l, M);
+    if (st != FRT_OK)
+        return st;
+    g.p.epi = EPI_BF16;
+    g.p.alpha = s_x * P->s_gu[l];
+    g.p.out = P->gu;
+    g.p.ldo = 2 * ff;
+    CK(launch_gemm(g, s, true));
+    CK(launch_act_quant(P->gu, M, ff, P->act, inv_sh, P->qh, nullptr, false, s, true));
+    if (trace_gu)
+        CK(cudaMemcpyAsync(trace_gu, P->gu, (size_t)M * 2 * ff * 2, cudaMemcpyDeviceToDevice, s));
+    if (trace_qx)
+        CK(cudaMemcpyAsync(trace_qx, P->qx, (size_t)M * d, cudaMemcpyDeviceToDevice, s));
+    if (trace_qh)
+        CK(cudaMemcpyAsync(trace_qh, P->qh, (size_t)M * ff, cudaMemcpyDeviceToDevice, s));
+    if (trace_rprime)
+        CK(cudaMemcpyAsync(trace_rprime, hid ? (const void *)P->rprime : in, (size_t)M * d * 2,
+                           cudaMemcpyDeviceToDevice, s));
+    GemmLaunch g2;
+    st = setup_gemm(P, g2, 1, l, M);
+    if (st != FRT_OK)
+        return st;
+    g2.p.epi = EPI_RESID;
+    g2.p.alpha = s_h * P->s_d[l];
+    g2.p.out = out;
+    g2.p.ldo = d;
+    g2.p.resid = hid ? (const void *)P->rprime : in;
+    g2.p.ldr = d;
+    CK(launch_gemm(g2, s, true));
+    return FRT_OK;
+}
+
+frt_status run_stack(frt_ffn_plan *P, const void *r_in, const void *h_in, void *out, int M, cudaStream_t s) {
+    const void *cur = r_in;
+    for (int l = 0; l < P->L; ++l) {
+        void *dst = (l == P->L - 1) ? out : (void *)P->rbuf[l & 1];
+        frt_status st = run_layer(P, l, cur, l == 0 ? h_in : nullptr, dst, M, s, nullptr, nullptr, nullptr,
+                                  nullptr);
+        if (st != FRT_OK)
+            return st;
+        cur = dst;
+    }
+    return FRT_OK;
+}
+
+frt_status check_ready(frt_ffn_plan *P) {
+    for (int l = 0; l < P->L; ++l)
+        if (!P->loaded[l])
+            return fail(FRT_ERR_NOT_READY, "weights of layer %d not loaded", l);
+    if (!P->scales_ok)
+        return fail(FRT_ERR_NOT_READY, "activation scales not calibrated or set");
+    return FRT_OK;
+}
+
+frt_status check_io(frt_ffn_plan *P, const void *r, const void *h, const void *out, int M) {
+    if (!P)
+        return fail(FRT_ERR_INVALID_ARG, "null plan");
+    if (M < 0)
+        return fail(FRT_ERR_INVALID_ARG, "M must be >= 0 (got %d)", M);
+    if (M > P->M_max)
+        return fail(FRT_ERR_SHAPE, "M=%d exceeds M_max=%d", M, P->M_max);
+    if (M > 0 && (!r || !out))
+        return fail(FRT_ERR_INVALID_ARG, "residual_in and out must be non-null");
+    if (!aligned16(r) || !aligned16(h) || !aligned16(out))
+        return fail(FRT_ERR_INVALID_ARG, "device pointers must be 16-byte aligned");
+    return FRT_OK;
+}
+
+void free_plan(frt_ffn_plan *P) {
+    for (auto &kv : P->graphs) {
+        if (kv.second.exec) cudaGraphExecDestroy(kv.second.exec);
+        if (kv.second.graph) cudaGraphDestroy(kv.second.graph);
+    }
+    void *ptrs[] = {P->w_gu, P->w_down, P->w_norm, P->rbuf[0], P->rbuf[1], P->rprime, P->gu,
+                    P->qx,   P->qh,     P->ws,     P->counters, P->amax,  P->err};
+    for (void *p : ptrs)
+        if (p) cudaFree(p);
+    delete P;
+}
+
+}  // namespace
+
+// ===================================================================== ABI ==
+
+FRT_API const char *frt_ffn_last_error(void) { return g_last_error.c_str(); }
+
+FRT_API frt_status frt_ffn_plan_create(int d, int ff, int act, int M_max, int n_layers, frt_ffn_plan_t *out) {
+    if (!out)
+        return fail(FRT_ERR_INVALID_ARG, "out is null");
+    *out = nullptr;
+    if (d <= 0 || ff <= 0 || d % 128 || ff % 128)
+        return fail(FRT_ERR_INVALID_ARG, "d and ff must be positive multiples of 128 (d=%d ff=%d)", d, ff);
+    if (act != FRT_ACT_GEGLU_TANH && act != FRT_ACT_SWIGLU)
+        return fail(FRT_ERR_INVALID_ARG, "unknown activation %d", act);
+    if (M_max < 1 || M_max > 65536)
+        return fail(FRT_ERR_INVALID_ARG, "M_max must be in [1, 65536] (got %d)", M_max);
+    if (n_layers < 1 || n_layers > 4096)
+        return fail(FRT_ERR_INVALID_ARG, "n_layers must be in [1, 4096] (got %d)", n_layers);
+    int dev = 0;
+    CK(cudaGetDevice(&dev));
+    cudaDeviceProp prop;
+    CK(cudaGetDeviceProperties(&prop, dev));
+    if (prop.major != 10 || prop.minor != 3)
+        return fail(FRT_ERR_UNSUPPORTED, "needs a compute capability 10.3 GPU (found %d.%d, %s)", prop.major,
+                    prop.minor, prop.name);
+    frt_ffn_plan *P = new frt_ffn_plan();
+    P->d = d;
+    P->ff = ff;
+    P->act = act;
+    P->M_max = M_max;
+    P->L = n_layers;
+    P->dev = dev;
+    P->num_sms = prop.multiProcessorCount;
+    P->M_alloc = (M_max + 127) / 128 * 128;
+    P->s_gu.assign(n_layers, 0.f);
+    P->s_d.assign(n_layers, 0.f);
+    P->s_x.assign(n_layers, 0.f);
+    P->s_h.assign(n_layers, 0.f);
+    P->loaded.assign(n_layers, 0);
+    if (const char *fp = getenv("FRT_FFN_FORCE_PATH")) {
+        if (!strcmp(fp, "splitk") || !strcmp(fp, "swap")) P->force_path = 1;
+        if (!strcmp(fp, "tiled")) P->force_path = 2;
+    }
+    const size_t L = n_layers, D = d, F = ff, MA = P->M_alloc, MM = M_max;
+    P->ws_floats = (size_t)P->num_sms * 128 * 256;
+    struct A { void **p; size_t bytes; } allocs[] = {
+        {(void **)&P->w_gu, L * 2 * F * D},
+        {(void **)&P->w_down, L * D * F},
+        {(void **)&P->w_norm, L * D * 2},
+        {(void **)&P->rbuf[0], MM * D * 2},
+        {(void **)&P->rbuf[1], MM * D * 2},
+        {(void **)&P->rprime, MM * D * 2},
+        {(void **)&P->gu, MM * 2 * F * 2},
+        {(void **)&P->qx, MA * D},
+        {(void **)&P->qh, MA * F},
+        {(void **)&P->ws, P->ws_floats * 4},
+        {(void **)&P->counters, (size_t)N_GEMM_SITES * COUNTERS_PER_GEMM * 4},
+        {(void **)&P->amax, 2 * 4},
+        {(void **)&P->err, 4},
+    };
+    for (auto &a : allocs) {
+        cudaError_t e = cudaMalloc(a.p, a.bytes);
+        if (e != cudaSuccess) {
+            frt_status st = cuda_fail(e, "cudaMalloc");
+            free_plan(P);
+            return st;
+        }
+    }
+    // Padding rows of the activation tiles and every counter start at zero.
+    cudaError_t e = cudaSuccess;
+    if (e == cudaSuccess) e = cudaMemset(P->qx, 0, MA * D);
+    if (e == cudaSuccess) e = cudaMemset(P->qh, 0, MA * F);
+    if (e == cudaSuccess) e = cudaMemset(P->counters, 0, (size_t)N_GEMM_SITES * COUNTERS_PER_GEMM * 4);
+    if (e == cudaSuccess) e = cudaMemset(P->err, 0, 4);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        frt_status st = cuda_fail(e, "plan initialisation");
+        free_plan(P);
+        return st;
+    }
+    *out = P;
+    return FRT_OK;
+}
+
+FRT_API frt_status frt_ffn_plan_destroy(frt_ffn_plan_t P) {
+    if (!P)
+        return FRT_OK;
+    cudaDeviceSynchronize();
+    free_plan(P);
+    return FRT_OK;
+}
+
+FRT_API frt_status frt_ffn_load_weights(frt_ffn_plan_t P, int layer, const void *w_norm, const void *w_gate,
+                                        const void *w_up, const void *w_down, frt_stream_t stream) {
+    if (!P)
+        return fail(FRT_ERR_INVALID_ARG, "null plan");
+    if (layer < 0 || layer >= P->L)
+        return fail(FRT_ERR_INVALID_ARG, "layer %d out of range [0, %d)", layer, P->L);
+    if (!w_norm || !w_gate || !w_up || !w_down)
+        return fail(FRT_ERR_INVALID_ARG, "weight pointers must be non-null");
+    if (!aligned16(w_norm) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down))
+        return fail(FRT_ERR_INVALID_ARG, "weight pointers must be 16-byte aligned");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t D = P->d, F = P->ff;
+    uint8_t *gu_dst = P->w_gu + (size_t)layer * 2 * F * D;
+    uint8_t *d_dst = P->w_down + (size_t)layer * D * F;
+    CK(cudaMemcpyAsync(P->w_norm + (size_t)layer * D, w_norm, D * 2, cudaMemcpyDeviceToDevice, s));
+    // one scale for [W_gate; W_up], one for W_down
+    CK(cudaMemsetAsync(P->amax, 0, 8, s));
+    CK(launch_amax_bf16(w_gate, F * D, P->amax, s));
+    CK(launch_amax_bf16(w_up, F * D, P->amax, s));
+    CK(launch_amax_bf16(w_down, D * F, P->amax + 1, s));
+    unsigned h_amax[2];
+    CK(cudaMemcpyAsync(h_amax, P->amax, 8, cudaMemcpyDeviceToHost, s));
+    CK(cudaStreamSynchronize(s));
+    float a_gu, a_d;
+    memcpy(&a_gu, &h_amax[0], 4);
+    memcpy(&a_d, &h_amax[1], 4);
+    const float s_gu = scale_from_amax(a_gu), s_d = scale_from_amax(a_d);
+    CK(launch_quant_bf16(w_gate, F * D, 1.0f / s_gu, gu_dst, s));
+    CK(launch_quant_bf16(w_up, F * D, 1.0f / s_gu, gu_dst + F * D, s));
+    CK(launch_quant_bf16(w_down, D * F, 1.0f / s_d, d_dst, s));
+    CK(cudaStreamSynchronize(s));
+    P->s_gu[layer] = s_gu;
+    P->s_d[layer] = s_d;
+    P->loaded[layer] = 1;
+    P->version++;
+    return FRT_OK;
+}
+
+FRT_API frt_status frt_ffn_get_scales(frt_ffn_plan_t P, float *s_x, float *s_h, float *s_gu, float *s_down) {
+    if (!P)
+        return fail(FRT_ERR_INVALID_ARG, "null plan");
+    const size_t n = P->L * sizeof(float);
+    if (s_x) memcpy(s_x, P->s_x.data(), n);
+    if (s_h) memcpy(s_h, P->s_h.data(), n);
+    if (s_gu) memcpy(s_gu, P->s_gu.data(), n);
+    if (s_down) memcpy(s_down, P->s_d.data(), n);
+    return FRT_OK;
+}
+
+FRT_API frt_status frt_ffn_set_scales(frt_ffn_plan_t P, const float *s_x, const float *s_h) {
+    if (!P)
+        return fail(FRT_ERR_INVALID_ARG, "null plan");
+    if (!s_x || !s_h)
+        return fail(FRT_ERR_INVALID_ARG, "scale arrays must be non-null");
+    for (int l = 0; l < P->L; ++l)
+        if (!(s_x[l] > 0.f) || !(s_h[l] > 0.f) || !std::isfinite(s_x[l]) || !std::isfinite(s_h[l]))
+            return fail(FRT_ERR_INVALID_ARG, "scales of layer %d must be positive and finite", l);
+    P->s_x.assign(s_x, s_x + P->L);
+    P->s_h.assign(s_h, s_h + P->L);
+    P->scales_ok = true;
+    P->version++;
+    return FRT_OK;
+}
+
+FRT_API frt_status frt_ffn_calibrate(frt_ffn_plan_t P, const void *const *residual, const void *const *hidden,
+                                     int n_batches, int M, frt_stream_t stream) {
+    if (!P)
+        return fail(FRT_ERR_INVALID_ARG, "null plan");
+    if (!residual || n_batches < 1)
+        return fail(FRT_ERR_INVALID_ARG, "need at least one calibration batch");
+    if (M < 1)
+        return fail(FRT_ERR_INVALID_ARG, "calibration needs M >= 1");
+    if (M > P->M_max)
+        return fail(FRT_ERR_SHAPE, "M=%d exceeds M_max=%d", M, P->M_max);
+    for (int b = 0; b < n_batches; ++b) {
+        if (!residual[b] || !aligned16(residual[b]) || (hidden && !aligned16(hidden[b])))
+            return fail(FRT_ERR_INVALID_ARG, "batch %d: null or misaligned pointer", b);
+    }
+    for (int l = 0; l < P->L; ++l)
+        if (!P->loaded[l])
+            return fail(FRT_ERR_NOT_READY, "weights of layer %d not loaded", l);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int d = P->d, ff = P->ff;
+    const size_t row_bytes = (size_t)M * d * 2;
+    uint16_t *state = nullptr;
+    CK(cudaMalloc(&state, row_bytes * n_batches));
+    auto st_of = [&](int b) { return reinterpret_cast<uint16_t *>(reinterpret_cast<uint8_t *>(state) + row_bytes * b); };
+    std::vector<float> sx(P->L), sh(P->L);
+    frt_status result = FRT_OK;
+    auto run = [&]() -> frt_status {
+        unsigned h_amax;
+        for (int l = 0; l < P->L; ++l) {
+            const uint16_t *wn = P->w_norm + (size_t)l * d;
+            // 1. amax of the gate/up GEMM input over all batches
+            CK(cudaMemsetAsync(P->amax, 0, 8, s));
+            for (int b = 0; b < n_batches; ++b) {
+                const void *in = l == 0 ? residual[b] : (const void *)st_of(b);
+                const void *hid = (l == 0 && hidden) ? hidden[b] : nullptr;
+                CK(launch_norm_quant(in, hid, wn, M, d, RMS_EPS, 1.0f, nullptr, P->qx, P->amax, true, s, false));
+            }
+            CK(cudaMemcpyAsync(&h_amax, P->amax, 4, cudaMemcpyDeviceToHost, s));
+            CK(cudaStreamSynchronize(s));
+            float a;
+            memcpy(&a, &h_amax, 4);
+            sx[l] = scale_from_amax(a);
+            // 2. amax of the down GEMM input, r' of layer 0 kept in the batch state
+            for (int b = 0; b < n_batches; ++b) {
+                const void *in = l == 0 ? residual[b] : (const void *)st_of(b);
+                const void *hid = (l == 0 && hidden) ? hidden[b] : nullptr;
+                if (l == 0 && !hid)
+                    CK(cudaMemcpyAsync(st_of(b), residual[b], row_bytes, cudaMemcpyDeviceToDevice, s));
+                CK(launch_norm_quant(in, hid, wn, M, d, RMS_EPS, 1.0f / sx[l], hid ? (void *)st_of(b) : nullptr,
+                                     P->qx, nullptr, false, s, false));
+                GemmLaunch g;
+                frt_status st2 = setup_gemm(P, g, 0, l, M);
+                if (st2 != FRT_OK)
+                    return st2;
+                g.p.epi = EPI_BF16;
+                g.p.alpha = sx[l] * P->s_gu[l];
+                g.p.out = P->gu;
+                g.p.ldo = 2 * ff;
+                CK(launch_gemm(g, s, false));
+                CK(launch_act_quant(P->gu, M, ff, P->act, 1.0f, P->qh, P->amax + 1, true, s, false));
+            }
+            CK(cudaMemcpyAsync(&h_amax, P->amax + 1, 4, cudaMemcpyDeviceToHost, s));
+            CK(cudaStreamSynchronize(s));
+            memcpy(&a, &h_amax, 4);
+            sh[l] = scale_from_amax(a);
+            // 3. finish the layer for every batch with both scales
+            P->s_x[l] = sx[l];
+            P->s_h[l] = sh[l];
+            for (int b = 0; b < n_batches; ++b) {
+                frt_status st2 = run_layer(P, l, st_of(b), nullptr, st_of(b), M, s, nullptr, nullptr, nullptr,
+                                           nullptr);
+                if (st2 != FRT_OK)
+                    return st2;
+            }
+        }
+        CK(cudaStreamSynchronize(s));
+        return FRT_OK;
+    };
+    result = run();
+    cudaStreamSynchronize(s);
+    cudaFree(state);
+    if (result != FRT_OK) {
+        P->scales_ok = false;
+        return result;
+    }
+    int h_err = 0;
+    CK(cudaMemcpy(&h_err, P->err, 4, cudaMemcpyDeviceToHost));
+    if (h_err) {
+        CK(cudaMemset(P->err, 0, 4));
+        P->scales_ok = false;
+        return fail(FRT_ERR_DEVICE_TIMEOUT, "a kernel gave up a bounded wait during calibration");
+    }
+    P->s_x = sx;
+    P->s_h = sh;
+    P->scales_ok = true;
+    P->version++;
+    return FRT_OK;
+}
+
+FRT_API frt_status frt_ffn_forward(frt_ffn_plan_t P, const void *residual_in, const void *hidden_in, void *out,
+                                   int M, frt_stream_t stream) {
+    frt_status st = check_io(P, residual_in, hidden_in, out, M);
+    if (st != FRT_OK)
+        return st;
+    if ((st = check_ready(P)) != FRT_OK)
+        return st;
+    if (M == 0)
+        return FRT_OK;
+    return run_stack(P, residual_in, hidden_in, out, M, static_cast<cudaStream_t>(stream));
+}
+
+FRT_API frt_status frt_ffn_graph_capture(frt_ffn_plan_t P, const void *residual_in, const void *hidden_in,
+                                         void *out, int M, frt_stream_t stream) {
+    frt_status st = check_io(P, residual_in, hidden_in, out, M);
+    if (st != FRT_OK)
+        return st;
+    if ((st = check_ready(P)) != FRT_OK)
+        return st;
+    if (M == 0)
+        return fail(FRT_ERR_INVALID_ARG, "cannot capture M == 0");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (s == nullptr)
+        return fail(FRT_ERR_CAPTURE, "capture needs a non-default stream");
+    cudaStreamCaptureStatus cs;
+    CK(cudaStreamIsCapturing(s, &cs));
+    if (cs != cudaStreamCaptureStatusNone)
+        return fail(FRT_ERR_CAPTURE, "stream is already capturing");
+    // Encode every tensor map the capture needs before capturing.
+    for (int site = 0; site < 2; ++site) {
+        GemmLaunch g;
+        if ((st = setup_gemm(P, g, site, 0, M)) != FRT_OK)
+            return st;
+    }
+    CK(cudaStreamBeginCapture(s, cudaStreamCaptureModeRelaxed));
+    st = run_stack(P, residual_in, hidden_in, out, M, s);
+    cudaGraph_t graph = nullptr;
+    cudaError_t e = cudaStreamEndCapture(s, &graph);
+    if (st != FRT_OK) {
+        if (graph) cudaGraphDestroy(graph);
+        return st;
+    }
+    if (e != cudaSuccess || !graph)
+        return fail(FRT_ERR_CAPTURE, "cudaStreamEndCapture: %s", cudaGetErrorString(e));
+    cudaGraphExec_t exec = nullptr;
+    e = cudaGraphInstantiate(&exec, graph, 0);
+    if (e != cudaSuccess) {
+        cudaGraphDestroy(graph);
+        return fail(FRT_ERR_CAPTURE, "cudaGraphInstantiate: %s", cudaGetErrorString(e));
+    }
+    auto it = P->graphs.find(M);
+    if (it != P->graphs.end()) {
+        cudaGraphExecDestroy(it->second.exec);
+        cudaGraphDestroy(it->second.graph);
+    }
+    GraphEntry ge;
+    ge.graph = graph;
+    ge.exec = exec;
+    ge.version = P->version;
+    P->graphs[M] = ge;
+    return FRT_OK;
+}
+
+FRT_API frt_status frt_ffn_graph_replay(frt_ffn_plan_t P, int M, frt_stream_t stream) {
+    if (!P)
+        return fail(FRT_ERR_INVALID_ARG, "null plan");
+    auto it = P->graphs.find(M);
+    if (it == P->graphs.end())
+        return fail(FRT_ERR_CAPTURE, "no graph captured for M=%d", M);
+    if (it->second.version != P->version)
+        return fail(FRT_ERR_STALE_GRAPH, "scales or weights changed since the graph for M=%d was captured", M);
+    CK(cudaGraphLaunch(it->second.exec, static_cast<cudaStream_t>(stream)));
+    return FRT_OK;
+}
+
+FRT_API frt_status frt_ffn_debug_trace(frt_ffn_plan_t P, int layer, const void *residual_in, const void *hidden_in,
+                                       int M, void *r_prime, void *q_x, void *gu, void *q_h, void *out,
+                                       frt_stream_t stream) {
+    frt_status st = check_io(P, residual_in, hidden_in, out ? out : (void *)residual_in, M);
+    if (st != FRT_OK)
+        return st;
+    if (layer < 0 || layer >= P->L)
+        return fail(FRT_ERR_INVALID_ARG, "layer %d out of range", layer);
+    if (!P->loaded[layer] || !P->scales_ok)
+        return fail(FRT_ERR_NOT_READY, "layer %d not loaded or scales not set", layer);
+    if (!aligned16(r_prime) || !aligned16(q_x) || !aligned16(gu) || !aligned16(q_h))
+        return fail(FRT_ERR_INVALID_ARG, "trace buffers must be 16-byte aligned");
+    if (M == 0)
+        return FRT_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void *dst = out ? out : (void *)P->rbuf[0];
+    return run_layer(P, layer, residual_in, hidden_in, dst, M, s, r_prime, q_x, gu, q_h);
+}
+
+FRT_API frt_status frt_ffn_device_status(frt_ffn_plan_t P, frt_stream_t stream) {
+    if (!P)
+        return fail(FRT_ERR_INVALID_ARG, "null plan");
+    CK(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+    int h = 0;
+    CK(cudaMemcpy(&h, P->err, 4, cudaMemcpyDeviceToHost));
+    if (h) {
+        CK(cudaMemset(P->err, 0, 4));
+        CK(cudaDeviceSynchronize());
+        return fail(FRT_ERR_DEVICE_TIMEOUT, "a kernel gave up a bounded wait (code %d)", h);
+    }
+    return FRT_OK;
+}
+
+FRT_API frt_status frt_fp8_gemm(frt_ffn_plan_t P, const void *A, const void *B, void *C, int M, int N, int K,
+                                float alpha, int path, int splits, frt_stream_t stream) {
+    if (!P)
+        return fail(FRT_ERR_INVALID_ARG, "null plan");
+    if (!A || !B || !C || !aligned16(A) || !aligned16(B) || !aligned16(C))
+        return fail(FRT_ERR_INVALID_ARG, "A, B, C must be non-null and 16-byte aligned");
+    if (M < 1 || M > 65536 || N < 128 || N % 128 || K < 16 || K % 16)
+        return fail(FRT_ERR_INVALID_ARG, "need 1 <= M <= 65536, N % 128 == 0, K >= 16, K %% 16 == 0");
+    if (path < 0 || path > 2 || splits < 0)
+        return fail(FRT_ERR_INVALID_ARG, "bad path or splits");
+    const bool swap = path == 1 || (path == 0 && M <= SWAP_MAX_TOKENS);
+    if (swap && M > SWAP_MAX_TOKENS)
+        return fail(FRT_ERR_UNSUPPORTED, "the weight-streaming path takes at most %d tokens", SWAP_MAX_TOKENS);
+    GemmLaunch g;
+    memset(&g.p, 0, sizeof g.p);
+    plan_gemm(g, swap, M, N, K, P->num_sms, splits);
+    if (gemm_ws_floats(g) > P->ws_floats || (g.p.splits > 1 && gemm_tiles(g) > COUNTERS_PER_GEMM))
+        return fail(FRT_ERR_UNSUPPORTED, "split-K workspace too small");
+    cudaError_t e1, e2;
+    if (swap) {
+        e1 = encode_tmap_u8(&g.tmP, B, N, K, 128);
+        e2 = encode_tmap_u8(&g.tmQ, A, M, K, g.bn);
+    } else {
+        e1 = encode_tmap_u8(&g.tmP, A, M, K, 128);
+        e2 = encode_tmap_u8(&g.tmQ, B, N, K, g.bn);
+    }
+    if (e1 != cudaSuccess || e2 != cudaSuccess)
+        return fail(FRT_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+    g.p.epi = EPI_F32;
+    g.p.alpha = alpha;
+    g.p.out = C;
+    g.p.ldo = N;
+    g.p.ws = P->ws;
+    g.p.counters = P->counters;
+    g.p.err = P->err;
+    CK(launch_gemm(g, static_cast<cudaStream_t>(stream), false));
+    return FRT_OK;
+}

@@ -1,0 +1,95 @@
+// frt_internal.h -- declarations shared by the library's translation units
+// (plan / ABI, elementwise kernels, FP8 GEMM).  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace frt {
+
+enum Act : int { ACT_GEGLU_TANH = 0, ACT_SWIGLU = 1 };
+
+// GEMM epilogues.
+enum Epi : int {
+    EPI_BF16 = 0,   // out[m][n] = bf16(acc * alpha)
+    EPI_RESID = 1,  // out[m][n] = bf16(resid[m][n] + acc * alpha)
+    EPI_F32 = 2,    // out[m][n] = acc * alpha (fp32; diagnostics)
+};
+
+// One GEMM launch: C[token][feature] = epilogue(sum_k X[token][k] W[feature][k]).
+// The MMA's 128-row operand P and its narrow operand Q are either
+// (P = X tiles, Q = W tiles) -- the tiled path -- or (P = W tiles, Q = X tiles)
+// -- the weight-streaming path for few tokens ("swap").
+struct GemmParams {
+    int p_row0, q_row0;     // row offsets of the P and Q tiles in their tensor maps
+    int n_tiles_p, n_tiles_q;
+    int k_blocks;           // ceil(K / 128)
+    int splits;             // split-K factor (1 = none)
+    int kb_per_split;
+    int total_units;        // n_tiles_p * n_tiles_q * splits
+    int epi;                // Epi
+    float alpha;
+    void *out;
+    int ldo;                // elements
+    const void *resid;      // BF16, EPI_RESID only
+    int ldr;
+    int m_tok;              // valid token rows
+    int n_feat;             // valid feature columns
+    float *ws;              // split-K partials
+    int *counters;          // split-K arrival counters (zero between launches)
+    int *err;               // device error word
+};
+
+struct GemmLaunch {
+    CUtensorMap tmP, tmQ;
+    GemmParams p;
+    int bn;                 // MMA N (Q tile rows)
+    bool swap;
+    int grid;
+};
+
+// Host side --------------------------------------------------------------
+
+// Encode a 2-D E4M3 tensor map: rows x cols bytes, row stride `cols` bytes,
+// box of 128 bytes x box_rows rows, 128-byte swizzle.
+cudaError_t encode_tmap_u8(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows);
+
+// Choose tiling / split-K for a GEMM of m_tok tokens x n_feat features x K
+// and fill the launch (tensor maps excluded).  swap: weight-streaming path.
+void plan_gemm(GemmLaunch &g, bool swap, int m_tok, int n_feat, int K, int num_sms, int force_splits);
+size_t gemm_ws_floats(const GemmLaunch &g);
+int gemm_tiles(const GemmLaunch &g);
+cudaError_t launch_gemm(const GemmLaunch &g, cudaStream_t s, bool pdl);
+
+cudaError_t launch_amax_bf16(const void *x, size_t n, unsigned *amax_word, cudaStream_t s);
+cudaError_t launch_quant_bf16(const void *x, size_t n, float inv_s, uint8_t *q, cudaStream_t s);
+cudaError_t launch_norm_quant(const void *r, const void *h, const void *w, int M, int d, float eps, float inv_s,
+                              void *rprime, uint8_t *qx, unsigned *amax_word, bool measure, cudaStream_t s,
+                              bool pdl);
+cudaError_t launch_act_quant(const void *gu, int M, int ff, int act, float inv_s, uint8_t *qh,
+                             unsigned *amax_word, bool measure, cudaStream_t s, bool pdl);
+
+}  // namespace frt
+
+namespace frt {
+
+// cudaLaunchKernelEx with an optional programmatic-dependent-launch edge to
+// the previous work on the stream.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                             bool pdl, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
+}  // namespace frt

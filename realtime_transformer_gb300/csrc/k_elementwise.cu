@@ -1,0 +1,318 @@
+// k_elementwise.cu -- the memory-bound steps of the FP8 FFN sublayer:
+//   A0  per-tensor amax and E4M3 quantisation of BF16 weights
+//       (itsolotime FlashRT article, 5.2: FusedGateUp + Quant, scale_into);
+//   A1  residual add + RMSNorm + E4M3 quantise, one warp per row with
+//       128-bit loads and a warp-shuffle reduction (agentlenshq FlashRT
+//       summary, "Main ideas": fused residual-norm-quantise; itsolotime
+//       article, 3.3: rms_norm kernel row);
+//   A3  gated activation (GeGLU with tanh GELU, or SwiGLU) + E4M3
+//       requantise, 8 outputs per thread (itsolotime article, 7.2).
+// Each A1/A3 kernel has a measure mode for calibration that records the
+// per-tensor amax instead of writing codes ("FlashRT docs/architecture.md",
+// 6 Calibration Framework).
+//
+// Arithmetic follows the rounding points of the method exactly: every fp32
+// operation is rounded on its own (explicit __f*_rn intrinsics), the scale
+// is applied as a multiplication by its fp32 reciprocal, E4M3 conversion is
+// round-to-nearest-even with saturation (cvt.rn.satfinite).
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+#include "frt_internal.h"
+#include "frt_ptx.cuh"
+
+namespace frt {
+
+namespace {
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ void unpack8(const uint4 v, float (&f)[8]) {
+    f[0] = bf_lo(v.x); f[1] = bf_hi(v.x);
+    f[2] = bf_lo(v.y); f[3] = bf_hi(v.y);
+    f[4] = bf_lo(v.z); f[5] = bf_hi(v.z);
+    f[6] = bf_lo(v.w); f[7] = bf_hi(v.w);
+}
+
+__device__ __forceinline__ uint32_t bf16_bits(float x) {
+    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
+__device__ __forceinline__ uint4 pack8_bf16(const float (&f)[8]) {
+    uint4 v;
+    v.x = bf16_bits(f[0]) | (bf16_bits(f[1]) << 16);
+    v.y = bf16_bits(f[2]) | (bf16_bits(f[3]) << 16);
+    v.z = bf16_bits(f[4]) | (bf16_bits(f[5]) << 16);
+    v.w = bf16_bits(f[6]) | (bf16_bits(f[7]) << 16);
+    return v;
+}
+
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+    return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
+}
+
+__device__ __forceinline__ uint2 pack8_e4m3(const float (&f)[8]) {
+    uint2 v;
+    v.x = e4m3x2(f[0], f[1]) | (e4m3x2(f[2], f[3]) << 16);
+    v.y = e4m3x2(f[4], f[5]) | (e4m3x2(f[6], f[7]) << 16);
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// |x| of non-negative floats orders like its bit pattern.
+__device__ __forceinline__ void atomic_amax(unsigned *word, float v) {
+    atomicMax(word, __float_as_uint(v));
+}
+
+// GELU, tanh form: 0.5 g (1 + tanh(sqrt(2/pi) (g + 0.044715 g^3))).
+__device__ __forceinline__ float gelu_tanh(float g) {
+    const float k0 = 0.7978845608028654f;
+    const float k1 = 0.044715f;
+    float g3 = __fmul_rn(__fmul_rn(g, g), g);
+    float inner = __fmul_rn(k0, __fadd_rn(g, __fmul_rn(k1, g3)));
+    return __fmul_rn(__fmul_rn(0.5f, g), __fadd_rn(1.0f, tanhf(inner)));
+}
+
+// SiLU: g / (1 + exp(-g)).
+__device__ __forceinline__ float silu(float g) { return __fdiv_rn(g, __fadd_rn(1.0f, expf(-g))); }
+
+// ------------------------------------------------------------------- A0 --
+
+__global__ void k_amax_bf16(const uint4 *__restrict__ x, size_t nvec, const uint16_t *__restrict__ tail,
+                            int ntail, unsigned *amax_word) {
+    float m = 0.0f;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < nvec; i += (size_t)gridDim.x * blockDim.x) {
+        float f[8];
+        unpack8(__ldg(x + i), f);
+#pragma unroll
+        for (int j = 0; j < 8; j++)
+            m = fmaxf(m, fabsf(f[j]));
+    }
+    if (blockIdx.x == 0 && threadIdx.x < (unsigned)ntail)
+        m = fmaxf(m, fabsf(__uint_as_float((uint32_t)tail[threadIdx.x] << 16)));
+    m = warp_max(m);
+    if ((threadIdx.x & 31) == 0)
+        atomic_amax(amax_word, m);
+}
+
+__global__ void k_quant_bf16(const uint4 *__restrict__ x, size_t nvec, const uint16_t *__restrict__ tail,
+                             int ntail, float inv_s, uint2 *__restrict__ q, uint8_t *__restrict__ qtail) {
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < nvec; i += (size_t)gridDim.x * blockDim.x) {
+        float f[8];
+        unpack8(__ldg(x + i), f);
+#pragma unroll
+        for (int j = 0; j < 8; j++)
+            f[j] = __fmul_rn(f[j], inv_s);
+        q[i] = pack8_e4m3(f);
+    }
+    if (blockIdx.x == 0 && threadIdx.x < (unsigned)ntail) {
+        float v = __fmul_rn(__uint_as_float((uint32_t)tail[threadIdx.x] << 16), inv_s);
+        qtail[threadIdx.x] = (uint8_t)(e4m3x2(v, 0.0f) & 0xFF);
+    }
+}
+
+// ------------------------------------------------------------------- A1 --
+
+// One warp per row.  Pass 1: r' = bf16(r + h) (stored if rprime != null),
+// sum of squares.  Pass 2: y = (r' * inv) * w, then either amax (measure) or
+// q = E4M3(y * inv_s).  d % 8 == 0.
+template <bool MEASURE>
+__global__ void __launch_bounds__(256) k_norm_quant(const uint16_t *__restrict__ r, const uint16_t *__restrict__ h,
+                                                    const uint16_t *__restrict__ w, int M, int d, float eps,
+                                                    float inv_s, uint16_t *__restrict__ rprime,
+                                                    uint8_t *__restrict__ qx, unsigned *amax_word) {
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x & 31;
+    const int row = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
+    if (row >= M)
+        return;
+    const int nv = d >> 3;
+    const uint4 *rv = reinterpret_cast<const uint4 *>(r + (size_t)row * d);
+    const uint4 *hv = h ? reinterpret_cast<const uint4 *>(h + (size_t)row * d) : nullptr;
+    uint4 *rpv = rprime ? reinterpret_cast<uint4 *>(rprime + (size_t)row * d) : nullptr;
+    const uint4 *wv = reinterpret_cast<const uint4 *>(w);
+
+    float ss = 0.0f;
+    for (int v = lane; v < nv; v += 32) {
+        float x[8];
+        unpack8(rv[v], x);
+        if (hv) {
+            float hh[8];
+            unpack8(hv[v], hh);
+#pragma unroll
+            for (int j = 0; j < 8; j++)
+                x[j] = __bfloat162float(__float2bfloat16_rn(__fadd_rn(x[j], hh[j])));
+            if (rpv)
+                rpv[v] = pack8_bf16(x);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; j++)
+            ss = __fadd_rn(ss, __fmul_rn(x[j], x[j]));
+    }
+    ss = warp_sum(ss);
+    const float ms = __fdiv_rn(ss, (float)d);
+    const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+
+    float amax = 0.0f;
+    uint2 *qv = reinterpret_cast<uint2 *>(qx + (size_t)row * d);
+    for (int v = lane; v < nv; v += 32) {
+        float x[8], wf[8];
+        unpack8(rv[v], x);
+        if (hv) {
+            float hh[8];
+            unpack8(hv[v], hh);
+#pragma unroll
+            for (int j = 0; j < 8; j++)
+                x[j] = __bfloat162float(__float2bfloat16_rn(__fadd_rn(x[j], hh[j])));
+        }
+        unpack8(__ldg(wv + v), wf);
+#pragma unroll
+        for (int j = 0; j < 8; j++)
+            x[j] = __fmul_rn(__fmul_rn(x[j], inv), wf[j]);
+        if (MEASURE) {
+#pragma unroll
+            for (int j = 0; j < 8; j++)
+                amax = fmaxf(amax, fabsf(x[j]));
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; j++)
+                x[j] = __fmul_rn(x[j], inv_s);
+            qv[v] = pack8_e4m3(x);
+        }
+    }
+    if (MEASURE) {
+        amax = warp_max(amax);
+        if (lane == 0)
+            atomic_amax(amax_word, amax);
+    }
+}
+
+// ------------------------------------------------------------------- A3 --
+
+// gu rows are [g_0 .. g_{ff-1}, u_0 .. u_{ff-1}] (BF16); a = act(g) * u.
+template <int ACT, bool MEASURE>
+__global__ void __launch_bounds__(256) k_act_quant(const uint16_t *__restrict__ gu, int M, int ff, float inv_s,
+                                                   uint8_t *__restrict__ qh, unsigned *amax_word) {
+    pdl_wait();
+    pdl_trigger();
+    const int vpr = ff >> 3;  // 8-wide vectors per row
+    const size_t total = (size_t)M * vpr;
+    float amax = 0.0f;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+        const size_t row = i / vpr;
+        const int j0 = (int)(i - row * vpr) << 3;
+        const uint16_t *base = gu + row * (size_t)(2 * ff);
+        float g[8], u[8], a[8];
+        unpack8(*reinterpret_cast<const uint4 *>(base + j0), g);
+        unpack8(*reinterpret_cast<const uint4 *>(base + ff + j0), u);
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            const float ag = (ACT == ACT_SWIGLU) ? silu(g[j]) : gelu_tanh(g[j]);
+            a[j] = __fmul_rn(ag, u[j]);
+        }
+        if (MEASURE) {
+#pragma unroll
+            for (int j = 0; j < 8; j++)
+                amax = fmaxf(amax, fabsf(a[j]));
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; j++)
+                a[j] = __fmul_rn(a[j], inv_s);
+            *reinterpret_cast<uint2 *>(qh + row * (size_t)ff + j0) = pack8_e4m3(a);
+        }
+    }
+    if (MEASURE) {
+        amax = warp_max(amax);
+        if ((threadIdx.x & 31) == 0)
+            atomic_amax(amax_word, amax);
+    }
+}
+
+int sm_count() {
+    static int n = 0;
+    if (n == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0)
+            n = 1;
+    }
+    return n;
+}
+
+}  // namespace
+
+cudaError_t launch_amax_bf16(const void *x, size_t n, unsigned *amax_word, cudaStream_t s) {
+    const size_t nvec = n / 8;
+    const int ntail = (int)(n - nvec * 8);
+    const uint16_t *tail = static_cast<const uint16_t *>(x) + nvec * 8;
+    size_t blocks = (nvec + 255) / 256;
+    const size_t cap = (size_t)sm_count() * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks == 0) blocks = 1;
+    k_amax_bf16<<<(unsigned)blocks, 256, 0, s>>>(static_cast<const uint4 *>(x), nvec, tail, ntail, amax_word);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_bf16(const void *x, size_t n, float inv_s, uint8_t *q, cudaStream_t s) {
+    const size_t nvec = n / 8;
+    const int ntail = (int)(n - nvec * 8);
+    const uint16_t *tail = static_cast<const uint16_t *>(x) + nvec * 8;
+    size_t blocks = (nvec + 255) / 256;
+    const size_t cap = (size_t)sm_count() * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks == 0) blocks = 1;
+    k_quant_bf16<<<(unsigned)blocks, 256, 0, s>>>(static_cast<const uint4 *>(x), nvec, tail, ntail, inv_s,
+                                                   reinterpret_cast<uint2 *>(q), q + nvec * 8);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_norm_quant(const void *r, const void *h, const void *w, int M, int d, float eps, float inv_s,
+                              void *rprime, uint8_t *qx, unsigned *amax_word, bool measure, cudaStream_t s,
+                              bool pdl) {
+    const dim3 grid((unsigned)((M + 7) / 8)), block(256);
+    auto rr = static_cast<const uint16_t *>(r);
+    auto hh = static_cast<const uint16_t *>(h);
+    auto ww = static_cast<const uint16_t *>(w);
+    auto rp = static_cast<uint16_t *>(rprime);
+    if (measure)
+        return launch_ex(k_norm_quant<true>, grid, block, 0, s, pdl, rr, hh, ww, M, d, eps, inv_s, rp, qx,
+                         amax_word);
+    return launch_ex(k_norm_quant<false>, grid, block, 0, s, pdl, rr, hh, ww, M, d, eps, inv_s, rp, qx, amax_word);
+}
+
+cudaError_t launch_act_quant(const void *gu, int M, int ff, int act, float inv_s, uint8_t *qh,
+                             unsigned *amax_word, bool measure, cudaStream_t s, bool pdl) {
+    const size_t total = (size_t)M * (ff / 8);
+    size_t blocks = (total + 255) / 256;
+    const size_t cap = (size_t)sm_count() * 16;
+    if (blocks > cap) blocks = cap;
+    if (blocks == 0) blocks = 1;
+    const dim3 grid((unsigned)blocks), block(256);
+    auto g = static_cast<const uint16_t *>(gu);
+    if (act == ACT_SWIGLU) {
+        if (measure)
+            return launch_ex(k_act_quant<ACT_SWIGLU, true>, grid, block, 0, s, pdl, g, M, ff, inv_s, qh, amax_word);
+        return launch_ex(k_act_quant<ACT_SWIGLU, false>, grid, block, 0, s, pdl, g, M, ff, inv_s, qh, amax_word);
+    }
+    if (measure)
+        return launch_ex(k_act_quant<ACT_GEGLU_TANH, true>, grid, block, 0, s, pdl, g, M, ff, inv_s, qh, amax_word);
+    return launch_ex(k_act_quant<ACT_GEGLU_TANH, false>, grid, block, 0, s, pdl, g, M, ff, inv_s, qh, amax_word);
+}
+
+}  // namespace frt

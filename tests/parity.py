@@ -1,0 +1,90 @@
+"""Shared helpers of the GPU parity tests: the tolerance contract and the
+plumbing that hands the same seeded inputs to the CUDA path and the oracle.
+
+Contract (GPU vs oracle on the same inputs and the same scales):
+  * E4M3 activation codes identical on >= 99.9% of elements and never more
+    than one code step apart on the monotone code line (+0 and -0 equal);
+  * BF16 outputs: cosine >= 0.9999 and max |err| <= 2e-2 x RMS(oracle).
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import synthetic
+
+CODE_AGREE = 0.999
+COS_MIN = 0.9999
+ERR_RMS = 2e-2
+
+
+def code_ordinal(c):
+    c = np.asarray(c, np.int32)
+    mag = c & 0x7F
+    return np.where(c & 0x80, -mag, mag)
+
+
+def check_codes(got, ref, what=""):
+    got = np.asarray(got, np.uint8)
+    ref = np.asarray(ref, np.uint8)
+    assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    same = float(np.mean(code_ordinal(got) == code_ordinal(ref)))
+    step = int(np.abs(code_ordinal(got) - code_ordinal(ref)).max()) if got.size else 0
+    assert same >= CODE_AGREE, "%s: only %.5f of codes agree" % (what, same)
+    assert step <= 1, "%s: codes differ by %d steps" % (what, step)
+    return same
+
+
+def cosine(a, b):
+    a = np.asarray(a, np.float64).ravel()
+    b = np.asarray(b, np.float64).ravel()
+    return float(a @ b / np.sqrt((a @ a) * (b @ b)))
+
+
+def check_bf16(got_bits, ref_bits, what=""):
+    g = oracle.bf16_decode(got_bits).astype(np.float64)
+    r = oracle.bf16_decode(ref_bits).astype(np.float64)
+    assert g.shape == r.shape
+    c = cosine(g, r)
+    err = float(np.abs(g - r).max() / np.sqrt((r ** 2).mean()))
+    assert c >= COS_MIN, "%s: cosine %.7f" % (what, c)
+    assert err <= ERR_RMS, "%s: max|err|/rms %.4g" % (what, err)
+    return c, err
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    return synthetic.bf16_bits(t)
+
+
+def u8(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().numpy().astype(np.uint8)
+
+
+class Case:
+    """One workload: seeded weights/inputs, oracle-quantised weights and
+    oracle-calibrated scales, and a loaded GPU plan."""
+
+    def __init__(self, wl, device="cuda", gen_device="cpu", M_max=None, calib_rows=None):
+        from realtime_transformer_gb300.ffn import FFNPlan
+        self.wl = wl
+        self.dev = torch.device(device)
+        self.weights = [synthetic.layer_weights(wl, l, device=gen_device) for l in range(wl.L)]
+        self.r, self.h = synthetic.inputs(wl, device=gen_device)
+        self.calib = synthetic.calibration_batches(wl, device=gen_device)
+        self.q = oracle.quantize_stack([{k: bits(v) for k, v in w.items()} for w in self.weights])
+        rows = slice(None) if calib_rows is None else slice(0, calib_rows)
+        self.s_x, self.s_h = oracle.calibrate_stack(self.q, [bits(a[rows]) for a, _ in self.calib],
+                                                    [bits(b[rows]) for _, b in self.calib], wl.act_id)
+        self.plan = FFNPlan(wl.d, wl.ff, wl.act, M_max or wl.M, wl.L)
+        for l, w in enumerate(self.weights):
+            self.plan.load_weights(l, *(w[k].to(self.dev) for k in ("w_norm", "w_gate", "w_up", "w_down")))
+        self.plan.set_scales(self.s_x, self.s_h)
+
+    def oracle_forward(self, rows=None, trace=False):
+        r = bits(self.r) if rows is None else bits(self.r)[rows]
+        h = bits(self.h) if rows is None else bits(self.h)[rows]
+        return oracle.stack_forward(self.q, r, h, self.s_x, self.s_h, self.wl.act_id, trace=trace)
+
+    def close(self):
+        self.plan.close()

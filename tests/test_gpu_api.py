@@ -1,0 +1,92 @@
+"""Boundary behaviour of the C ABI on the GPU: status codes, stale graphs,
+empty and oversized inputs, misaligned pointers ("FlashRT
+docs/architecture.md", 7: pointer-only forward, graphs with baked alpha)."""
+import pytest
+import torch
+
+import synthetic
+from realtime_transformer_gb300 import _native as N
+from realtime_transformer_gb300.ffn import FFNPlan
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def loaded():
+    wl = synthetic.WORKLOADS["tiny"]
+    dev = torch.device("cuda")
+    plan = FFNPlan(wl.d, wl.ff, wl.act, 16, 1)
+    w = synthetic.layer_weights(wl, 0, device=dev)
+    plan.load_weights(0, w["w_norm"], w["w_gate"], w["w_up"], w["w_down"])
+    r, h = synthetic.inputs(wl, device=dev)
+    yield plan, r, h
+    plan.close()
+
+
+def status_of(fn, *a):
+    with pytest.raises(N.FrtError) as ei:
+        fn(*a)
+    return ei.value.name
+
+
+def test_forward_before_scales_is_not_ready(loaded):
+    plan, r, h = loaded
+    assert status_of(plan.forward, r, h) == "FRT_ERR_NOT_READY"
+
+
+def test_missing_weights_is_not_ready():
+    p = FFNPlan(256, 1024, "geglu_tanh", 8, 2)
+    p.set_scales([1.0, 1.0], [1.0, 1.0])
+    r = torch.zeros((8, 256), dtype=torch.bfloat16, device="cuda")
+    assert status_of(p.forward, r) == "FRT_ERR_NOT_READY"
+    p.close()
+
+
+def test_shape_and_argument_errors(loaded):
+    plan, r, h = loaded
+    plan.set_scales([0.01], [0.01])
+    big = torch.zeros((17, 256), dtype=torch.bfloat16, device="cuda")
+    assert status_of(plan.forward, big) == "FRT_ERR_SHAPE"
+    raw = torch.zeros(8 * 256 + 8, dtype=torch.bfloat16, device="cuda")
+    mis = raw[1:1 + 8 * 256].view(8, 256)
+    assert status_of(N.frt_ffn_forward, plan.handle, mis.data_ptr(), None, r.data_ptr(), 8, 0) == \
+        "FRT_ERR_INVALID_ARG"
+    assert status_of(N.frt_ffn_set_scales, plan.handle, [0.0], [1.0]) == "FRT_ERR_INVALID_ARG"
+    assert status_of(N.frt_ffn_load_weights, plan.handle, 3, r.data_ptr(), r.data_ptr(), r.data_ptr(),
+                     r.data_ptr(), 0) == "FRT_ERR_INVALID_ARG"
+
+
+def test_empty_input_is_a_no_op(loaded):
+    plan, r, h = loaded
+    plan.set_scales([0.01], [0.01])
+    N.frt_ffn_forward(plan.handle, r.data_ptr(), None, r.data_ptr(), 0, 0)
+    plan.device_status()
+
+
+def test_graph_replay_errors_and_staleness(loaded):
+    plan, r, h = loaded
+    plan.set_scales([0.02], [0.003])
+    assert status_of(plan.graph_replay, 5) == "FRT_ERR_CAPTURE"
+    out = torch.empty_like(r)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        plan.graph_capture(r, h, out, s)
+        plan.graph_replay(8, s)
+    s.synchronize()
+    ref = plan.forward(r, h)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+    plan.set_scales([0.02], [0.003])
+    assert status_of(plan.graph_replay, 8, s) == "FRT_ERR_STALE_GRAPH"
+    assert status_of(plan.graph_capture, r, h, out, 0) == "FRT_ERR_CAPTURE"
+
+
+def test_smaller_M_than_M_max_and_repeat_calls(loaded):
+    plan, r, h = loaded
+    plan.set_scales([0.02], [0.003])
+    full = plan.forward(r, h)
+    part = plan.forward(r[:3].contiguous(), h[:3].contiguous())
+    again = plan.forward(r, h)
+    torch.cuda.synchronize()
+    assert torch.equal(full[:3], part)
+    assert torch.equal(full, again)
