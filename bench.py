@@ -1,0 +1,401 @@
+#!/usr/bin/env python
+"""Benchmark of the FP8 FFN sublayer stack on GB300.
+
+One step = one graph replay of the whole stack (steps A1..A4 for every layer)
+over one batch of M tokens, inputs resident in HBM.  Prints one JSON line:
+tokens/s of the whole job, microseconds per layer, an end-to-end figure
+through the C ABI with host buffers, the roofline of the dominant kernel,
+the clocks seen during the timed region, and the CPU oracle's throughput.
+
+  python bench.py [--config vla_action_expert] [--steps K] [--warmup W]
+  python bench.py --impl reference ...   # the CPU oracle as the reference arm
+
+Multi-GPU (torchrun, one rank per GPU): replicas only -- every rank runs the
+same workload on its own GPU; timing is barrier-bracketed and the slowest
+rank's time counts.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import synthetic  # noqa: E402
+
+DEFAULT_CONFIG = "vla_action_expert"
+L2_FLUSH_BYTES = 2 * 129 * 1024 * 1024
+CLOCK_FIELDS = ["timestamp", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+                "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+                "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+STEP_NAMES = ["norm_quant", "gemm_gate_up_act", "gemm_down"]
+KERNEL_SOURCES = {"norm_quant": ["k_elementwise.cu"], "gemm_gate_up_act": ["k_gemm_fp8.cu", "frt_ptx.cuh"],
+                  "gemm_down": ["k_gemm_fp8.cu", "frt_ptx.cuh"]}
+
+
+# ----------------------------------------------------------------- helpers --
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            js = json.load(f)
+        return {"hbm_gbs": js["hbm_gbs"], "bf16_tflops": js["bf16_tflops"],
+                "bf16_tflops_sustained": js.get("bf16_tflops_sustained", js["bf16_tflops"]), "src": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "src": "fallback"}
+
+
+def kernel_bytes_flops(wl, M, step):
+    """Algorithmic bytes (minimum reads + writes) and FLOPs of one launch of
+    one step of one layer, for M tokens."""
+    d, ff = wl.d, wl.ff
+    if step == 0:   # residual (+ hidden at layer 0 is not timed here) in, norm weight in, q_x out
+        return 2 * M * d + 2 * d + M * d, 0
+    if step == 1:   # W_gu + q_x in, q_h out (gated activation in the epilogue)
+        return 2 * ff * d + M * d + M * ff, 2 * M * 2 * ff * d
+    return d * ff + M * ff + 2 * M * d + 2 * M * d, 2 * M * d * ff   # W_down + q_h + residual in, out
+
+
+def layer_algorithmic_bytes(wl, M):
+    """FP8 weights + BF16 residual in/out of one layer (intermediates excluded)."""
+    return 3 * wl.d * wl.ff + 2 * 2 * M * wl.d
+
+
+def source_hash(names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "realtime_transformer_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel, workload):
+    """dram read+write bytes per launch recorded from an ncu capture in
+    profiles/, if the kernel source has not changed since."""
+    path = os.path.join(ROOT, "profiles", "ncu_%s_%s.md" % (kernel, workload))
+    if not os.path.exists(path):
+        return None
+    rec = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and line.startswith("- "):
+                k, v = line[2:].split(":", 1)
+                rec[k.strip()] = v.strip().strip("`")
+    if rec.get("source_sha256_16") != source_hash(KERNEL_SOURCES[kernel]):
+        return None
+    try:
+        return int(float(rec["traffic_bytes_per_launch"]))
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        ident = None
+        try:
+            props = torch.cuda.get_device_properties(device_index)
+            uuid = getattr(props, "uuid", None)
+            if uuid is not None:
+                ident = "GPU-" + str(uuid) if not str(uuid).startswith("GPU-") else str(uuid)
+        except Exception:
+            ident = None
+        self.ident = ident
+        self.device_index = device_index
+
+    def start(self):
+        sel = ["-i", self.ident] if self.ident else []
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", *sel, "--query-gpu=" + ",".join(CLOCK_FIELDS),
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = [r.split(", ") for r in out.strip().splitlines() if r.count(",") >= len(CLOCK_FIELDS) - 1]
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def reduce_max(value: float, world: int, device) -> float:
+    if world <= 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# -------------------------------------------------------------- CPU oracle --
+
+def oracle_setup(wl, weights, calib, rows):
+    """Quantise and calibrate with the oracle (untimed)."""
+    import oracle
+    bits = synthetic.bf16_bits
+    q = oracle.quantize_stack([{k: bits(v) for k, v in w.items()} for w in weights])
+    s_x, s_h = oracle.calibrate_stack(q, [bits(a[:rows]) for a, _ in calib], [bits(b[:rows]) for _, b in calib],
+                                      wl.act_id)
+    return q, s_x, s_h
+
+
+def oracle_time(wl, q, s_x, s_h, r, h, rows, reps):
+    import oracle
+    bits = synthetic.bf16_bits
+    rb, hb = bits(r[:rows]), bits(h[:rows])
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.stack_forward(q, rb, hb, s_x, s_h, wl.act_id)
+    return time.perf_counter() - t0
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------- arms --
+
+def gen_workload(wl, device):
+    weights = [synthetic.layer_weights(wl, l, device=device) for l in range(wl.L)]
+    r, h = synthetic.inputs(wl, device=device)
+    calib = synthetic.calibration_batches(wl, device=device)
+    return weights, r, h, calib
+
+
+def run_reference(args, wl, world, rank):
+    """The CPU oracle, as it stands, on this host's cores."""
+    if rank != 0:
+        return None
+    gen_dev = "cuda" if torch.cuda.is_available() else "cpu"
+    weights, r, h, calib = gen_workload(wl, gen_dev)
+    rows_cal = min(wl.M, 64)
+    q, s_x, s_h = oracle_setup(wl, weights, calib, rows_cal)
+    t1 = oracle_time(wl, q, s_x, s_h, r, h, 1, 1)            # one token through the stack
+    budget = float(os.environ.get("FRT_REFERENCE_SECONDS", "120"))
+    rows = max(1, min(wl.M, int(budget / max(1e-9, t1 * max(1, args.steps + args.warmup)))))
+    oracle_time(wl, q, s_x, s_h, r, h, rows, args.warmup)
+    dt = oracle_time(wl, q, s_x, s_h, r, h, rows, args.steps)
+    value = rows * args.steps / dt
+    sample = "%d of %d tokens through all %d layers per step" % (rows, wl.M, wl.L)
+    line = {
+        "impl": "reference", "metric": "FP8 FFN stack tokens/s (graph-replayed, %s)" % wl.name, "value": value,
+        "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp32 (E4M3/BF16 emulated)", "data": "synthetic",
+        "config": config_of(wl),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    return line
+
+
+def config_of(wl):
+    return {"workload": wl.name, "M": wl.M, "d": wl.d, "ff": wl.ff, "act": wl.act, "layers": wl.L,
+            "weights": "E4M3 per-tensor", "residual": "BF16", "graph": "one CUDA graph per stack",
+            "l2": "flushed between timed steps (%d MiB write)" % (L2_FLUSH_BYTES >> 20), "parallelism": "replicas"}
+
+
+def run_ours(args, wl, world, rank, local):
+    from realtime_transformer_gb300.ffn import FFNPlan
+    from realtime_transformer_gb300 import _native as N
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    P = peaks()
+    weights, r, h, calib = gen_workload(wl, dev)
+    plan = FFNPlan(wl.d, wl.ff, wl.act, wl.M, wl.L)
+    for l, w in enumerate(weights):
+        plan.load_weights(l, w["w_norm"], w["w_gate"], w["w_up"], w["w_down"])
+    plan.calibrate([a for a, _ in calib], [b for _, b in calib])
+    out = torch.empty_like(r)
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        plan.graph_capture(r, h, out, stream)
+    torch.cuda.synchronize()
+
+    def timed(fn, n, warm):
+        for _ in range(warm):
+            with torch.cuda.stream(stream):
+                flush.zero_()
+                fn()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        with torch.cuda.stream(stream):
+            for e0, e1 in evs:
+                flush.zero_()
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+        torch.cuda.synchronize()
+        return [e0.elapsed_time(e1) for e0, e1 in evs]
+
+    replay = lambda: plan.graph_replay(wl.M, stream)
+
+    # warm-up, then exactly K timed steps between barriers
+    timed(replay, 0, args.warmup)
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    t_wall0 = time.perf_counter()
+    step_ms = timed(replay, args.steps, 0)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    clocks = sampler.stop()
+    barrier(world)
+    plan.device_status(stream)
+    total_s = sum(step_ms) / 1000.0
+    total_s = reduce_max(total_s, world, dev)
+    value = world * wl.M * args.steps / total_s
+    ms_step = 1000.0 * total_s / args.steps
+
+    # end to end through the public API: pinned host in, graph, host out
+    h_r = r.cpu().pin_memory()
+    h_h = h.cpu().pin_memory()
+    h_o = torch.empty_like(out, device="cpu").pin_memory()
+
+    def e2e_step():
+        r.copy_(h_r, non_blocking=True)
+        h.copy_(h_h, non_blocking=True)
+        plan.graph_replay(wl.M, stream)
+        h_o.copy_(out, non_blocking=True)
+
+    e2e_ms = timed(e2e_step, args.steps, args.warmup)
+    e2e_s = reduce_max(sum(e2e_ms) / 1000.0, world, dev)
+    h2d = h_r.numel() * 2 + h_h.numel() * 2
+    d2h = h_o.numel() * 2
+
+    # per-kernel timing (one layer's four kernels launched alone)
+    kern = {}
+    n_k = max(20, min(200, args.steps))
+    for step in range(len(STEP_NAMES)):
+        ms = timed(lambda s=step: N.frt_ffn_debug_step(plan.handle, 0, s, wl.M, stream.cuda_stream), n_k, 3)
+        kern[STEP_NAMES[step]] = statistics.mean(ms) * 1000.0
+    plan.device_status(stream)
+    dom = max(kern, key=kern.get)
+    dom_step = STEP_NAMES.index(dom)
+    nbytes, flops = kernel_bytes_flops(wl, wl.M, dom_step)
+    t_dom = kern[dom] * 1e-6
+    fp8_peak = 2.0 * P["bf16_tflops"]
+    ridge = fp8_peak * 1e12 / (P["hbm_gbs"] * 1e9)
+    tensor_bound = flops > 0 and flops / nbytes > ridge
+    if tensor_bound:
+        achieved = flops / t_dom / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
+                "frac": achieved / fp8_peak,
+                "peak_note": "FP8 dense = 2 x measured bf16 burst (%s; nominal fp8/bf16 ratio 2)" % P["src"]}
+    else:
+        achieved = nbytes / t_dom / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": P["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / P["hbm_gbs"], "peak_note": "%s HBM copy bandwidth" % P["src"]}
+    roof["kernel"] = dom
+    roof["us_per_launch"] = kern[dom]
+    roof["algorithmic_bytes"] = nbytes
+    roof["traffic"] = profiled_traffic(dom, wl.name)
+
+    layer_s = ms_step / 1000.0 / wl.L
+    step_roof = {"bound": "hbm", "achieved": layer_algorithmic_bytes(wl, wl.M) / layer_s / 1e9,
+                 "peak": P["hbm_gbs"], "unit": "GB/s"}
+    step_roof["frac"] = step_roof["achieved"] / P["hbm_gbs"]
+    step_roof["tflops"] = 6.0 * wl.M * wl.d * wl.ff / layer_s / 1e12
+
+    line = {
+        "metric": "FP8 FFN stack tokens/s (graph-replayed, %s)" % wl.name, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "us_per_layer": 1000.0 * ms_step / wl.L, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8_e4m3 (fp32 accumulate, bf16 residual)", "data": "synthetic", "config": config_of(wl),
+        "roofline": roof, "step_roofline": step_roof, "kernels_us": kern,
+        "e2e": {"value": world * wl.M * args.steps / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": 1000.0 * e2e_s / args.steps},
+        "gpu_launches": args.steps * wl.L * len(STEP_NAMES), "clocks": clocks, "wall_s_timed_region": t_wall,
+    }
+    plan.close()
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rows = min(wl.M, 64)
+        q, s_x, s_h = oracle_setup(wl, weights, calib, rows)
+        budget = float(os.environ.get("FRT_CPU_BASELINE_SECONDS", "15"))
+        t1 = oracle_time(wl, q, s_x, s_h, r.cpu(), h.cpu(), 1, 1)
+        rows = max(1, min(wl.M, int(budget / max(t1, 1e-9))))
+        dt = oracle_time(wl, q, s_x, s_h, r.cpu(), h.cpu(), rows, 1)
+        line["cpu_baseline"] = {"value": rows / dt, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+                                "sample": "%d of %d tokens through all %d layers, once" % (rows, wl.M, wl.L)}
+    return line
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(synthetic.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    wl = synthetic.WORKLOADS[args.config]
+    world, rank, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        line = run_reference(args, wl, world, rank)
+    else:
+        line = run_ours(args, wl, world, rank, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -36,7 +36,9 @@
  *     finished, unless a call says it synchronises.
  *   - No call throws.  Each returns an frt_status; on failure
  *     frt_ffn_last_error() gives a message (per host thread).
- *   - A plan is used from one host thread at a time.
+ *   - A plan is used from one host thread at a time, and its calls must not
+ *     run concurrently on different streams: they share the plan's scratch
+ *     buffers.  Order work on different streams with events.
  */
 #ifndef FRT_FFN_H
 #define FRT_FFN_H
@@ -158,6 +160,16 @@ frt_status frt_ffn_graph_replay(frt_ffn_plan_t plan, int M, frt_stream_t stream)
  */
 frt_status frt_ffn_debug_trace(frt_ffn_plan_t plan, int layer, const void *residual_in, const void *hidden_in,
                                int M, void *r_prime, void *q_x, void *gu, void *q_h, void *out, frt_stream_t stream);
+
+/*
+ * Diagnostics (timing single kernels): launch step `step` of layer `layer`
+ * alone, for M tokens, on the plan's own scratch buffers (whatever they hold):
+ * 0 = A1 residual+RMSNorm+quantise, 1 = A2 gate/up GEMM with A3 (gated
+ * activation + requantise) in its epilogue, 2 = A4 down GEMM + residual.  No
+ * programmatic dependency on earlier work.  Errors: INVALID_ARG, NOT_READY,
+ * SHAPE, CUDA.
+ */
+frt_status frt_ffn_debug_step(frt_ffn_plan_t plan, int layer, int step, int M, frt_stream_t stream);
 
 /*
  * Synchronise `stream` and report kernel-side failures: DEVICE_TIMEOUT if a

@@ -39,6 +39,7 @@ SIGNATURES = {
     "frt_ffn_graph_replay": (_I, [_P, _I, _P]),
     "frt_ffn_debug_trace": (_I, [_P, _I, _P, _P, _I, _P, _P, _P, _P, _P, _P]),
     "frt_ffn_device_status": (_I, [_P, _P]),
+    "frt_ffn_debug_step": (_I, [_P, _I, _I, _I, _P]),
     "frt_fp8_gemm": (_I, [_P, _P, _P, _P, _I, _I, _I, _F, _I, _I, _P]),
     "frt_ffn_last_error": (ctypes.c_char_p, []),
 }
@@ -130,6 +131,10 @@ def frt_ffn_graph_replay(plan, M, stream) -> None:
 
 def frt_ffn_debug_trace(plan, layer, residual_in, hidden_in, M, r_prime, q_x, gu, q_h, out, stream) -> None:
     _check(lib().frt_ffn_debug_trace(plan, layer, residual_in, hidden_in, M, r_prime, q_x, gu, q_h, out, stream))
+
+
+def frt_ffn_debug_step(plan, layer, step, M, stream) -> None:
+    _check(lib().frt_ffn_debug_step(plan, layer, step, M, stream))
 
 
 def frt_ffn_device_status(plan, stream) -> None:

@@ -9,10 +9,12 @@
 // CUDA Graph Capture: pointer-only forward, no allocation during replay;
 // "exec/": a C ABI Buffer / Graph / Plan contract).
 //
-// Per layer the forward launches four kernels on the caller's stream, each
+// Per layer the forward launches three kernels on the caller's stream, each
 // with a programmatic-dependent-launch edge to its predecessor:
-//   A1 norm_quant -> A2 FP8 gate/up GEMM -> A3 act_quant -> A4 FP8 down GEMM
-// (itsolotime article, 7.2: the FFN layer loop).
+//   A1 norm_quant -> A2+A3 FP8 gate/up GEMM with the gated activation and
+//   requantise in its epilogue -> A4 FP8 down GEMM with the residual add
+// (itsolotime article, 7.2: the FFN layer loop; the gate/up weights are
+// stored interleaved in 64-row blocks so one tile holds matching rows).
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -87,7 +89,7 @@ struct frt_ffn_plan {
     bool scales_ok = false;
     uint64_t version = 1;
     uint16_t *rbuf[2] = {nullptr, nullptr};
-    uint16_t *rprime = nullptr, *gu = nullptr;
+    uint16_t *rprime = nullptr;
     uint8_t *qx = nullptr, *qh = nullptr;
     float *ws = nullptr;
     size_t ws_floats = 0;
@@ -97,6 +99,8 @@ struct frt_ffn_plan {
     std::map<std::pair<int, int>, CUtensorMap> tmaps;
     std::map<int, GraphEntry> graphs;
     int force_path = 0;        // 0 auto, 1 swap, 2 tiled (FRT_FFN_FORCE_PATH)
+    bool pdl = true;           // programmatic dependent launch (FRT_FFN_NO_PDL=1 disables)
+    int max_splits = 0;        // cap on split-K (FRT_FFN_MAX_SPLITS; 0 = none)
 };
 
 namespace {
@@ -140,6 +144,8 @@ frt_status setup_gemm(frt_ffn_plan *P, GemmLaunch &g, int site, int l, int M) {
     const int xbuf = site == 0 ? B_QX : B_QH;
     memset(&g.p, 0, sizeof g.p);
     plan_gemm(g, swap, M, N, K, P->num_sms, 0);
+    if (P->max_splits > 0 && g.p.splits > P->max_splits)
+        plan_gemm(g, swap, M, N, K, P->num_sms, P->max_splits);
     frt_status st;
     if (swap) {
         if ((st = get_tmap(P, wbuf, 128, &g.tmP)) != FRT_OK) return st;
@@ -160,7 +166,37 @@ frt_status setup_gemm(frt_ffn_plan *P, GemmLaunch &g, int site, int l, int M) {
     return FRT_OK;
 }
 
-// One layer: A1 -> A2 -> A3 -> A4.  `out` receives the layer output; when
+// Gate/up GEMM of layer l with the gated epilogue (q_h, or its amax).
+frt_status setup_gate_up(frt_ffn_plan *P, GemmLaunch &g, int l, int M, int epi) {
+    frt_status st = setup_gemm(P, g, 0, l, M);
+    if (st != FRT_OK)
+        return st;
+    g.p.epi = epi;
+    g.p.alpha = P->s_x[l] * P->s_gu[l];
+    g.p.out = P->qh;
+    g.p.ldo = P->ff;
+    g.p.act = P->act;
+    g.p.ff = P->ff;
+    g.p.inv_s = 1.0f / P->s_h[l];
+    g.p.amax = P->amax + 1;
+    return FRT_OK;
+}
+
+// Down GEMM of layer l with the residual epilogue.
+frt_status setup_down(frt_ffn_plan *P, GemmLaunch &g, int l, int M, const void *resid, void *out) {
+    frt_status st = setup_gemm(P, g, 1, l, M);
+    if (st != FRT_OK)
+        return st;
+    g.p.epi = EPI_RESID;
+    g.p.alpha = P->s_h[l] * P->s_d[l];
+    g.p.out = out;
+    g.p.ldo = P->d;
+    g.p.resid = resid;
+    g.p.ldr = P->d;
+    return FRT_OK;
+}
+
+// One layer: A1 -> A2+A3 -> A4.  `out` receives the layer output; when
 // hid != null, r' is materialised in P->rprime and used as A4's residual.
 frt_status run_layer(frt_ffn_plan *P, int l, const void *in, const void *hid, void *out, int M, cudaStream_t s,
                      void *trace_rprime, void *trace_qx, void *trace_gu, void *trace_qh) {
@@ -168,20 +204,15 @@ frt_status run_layer(frt_ffn_plan *P, int l, const void *in, const void *hid, vo
     const float s_x = P->s_x[l], s_h = P->s_h[l];
     const float inv_sx = 1.0f / s_x, inv_sh = 1.0f / s_h;
     void *rp = hid ? (void *)P->rprime : nullptr;
+    const bool pdl = P->pdl;
     CK(launch_norm_quant(in, hid, P->w_norm + (size_t)l * d, M, d, RMS_EPS, inv_sx, rp, P->qx, nullptr, false, s,
-                         true));
+                         pdl));
     GemmLaunch g;
-    frt_status st = setup_gemm(P, g, 0, l, M);
+    frt_status st = setup_gate_up(P, g, l, M, EPI_GATED);
     if (st != FRT_OK)
         return st;
-    g.p.epi = EPI_BF16;
-    g.p.alpha = s_x * P->s_gu[l];
-    g.p.out = P->gu;
-    g.p.ldo = 2 * ff;
-    CK(launch_gemm(g, s, true));
-    CK(launch_act_quant(P->gu, M, ff, P->act, inv_sh, P->qh, nullptr, false, s, true));
-    if (trace_gu)
-        CK(cudaMemcpyAsync(trace_gu, P->gu, (size_t)M * 2 * ff * 2, cudaMemcpyDeviceToDevice, s));
+    g.p.dbg_gu = static_cast<uint16_t *>(trace_gu);
+    CK(launch_gemm(g, s, pdl));
     if (trace_qx)
         CK(cudaMemcpyAsync(trace_qx, P->qx, (size_t)M * d, cudaMemcpyDeviceToDevice, s));
     if (trace_qh)
@@ -190,16 +221,11 @@ frt_status run_layer(frt_ffn_plan *P, int l, const void *in, const void *hid, vo
         CK(cudaMemcpyAsync(trace_rprime, hid ? (const void *)P->rprime : in, (size_t)M * d * 2,
                            cudaMemcpyDeviceToDevice, s));
     GemmLaunch g2;
-    st = setup_gemm(P, g2, 1, l, M);
+    st = setup_down(P, g2, l, M, hid ? (const void *)P->rprime : in, out);
     if (st != FRT_OK)
         return st;
-    g2.p.epi = EPI_RESID;
-    g2.p.alpha = s_h * P->s_d[l];
-    g2.p.out = out;
-    g2.p.ldo = d;
-    g2.p.resid = hid ? (const void *)P->rprime : in;
-    g2.p.ldr = d;
-    CK(launch_gemm(g2, s, true));
+    CK(launch_gemm(g2, s, pdl));
+    (void)inv_sh;
     return FRT_OK;
 }
 
@@ -244,7 +270,7 @@ void free_plan(frt_ffn_plan *P) {
         if (kv.second.exec) cudaGraphExecDestroy(kv.second.exec);
         if (kv.second.graph) cudaGraphDestroy(kv.second.graph);
     }
-    void *ptrs[] = {P->w_gu, P->w_down, P->w_norm, P->rbuf[0], P->rbuf[1], P->rprime, P->gu,
+    void *ptrs[] = {P->w_gu, P->w_down, P->w_norm, P->rbuf[0], P->rbuf[1], P->rprime,
                     P->qx,   P->qh,     P->ws,     P->counters, P->amax,  P->err};
     for (void *p : ptrs)
         if (p) cudaFree(p);
@@ -294,6 +320,10 @@ FRT_API frt_status frt_ffn_plan_create(int d, int ff, int act, int M_max, int n_
         if (!strcmp(fp, "splitk") || !strcmp(fp, "swap")) P->force_path = 1;
         if (!strcmp(fp, "tiled")) P->force_path = 2;
     }
+    if (const char *np = getenv("FRT_FFN_NO_PDL"))
+        P->pdl = !(np[0] == '1');
+    if (const char *ms = getenv("FRT_FFN_MAX_SPLITS"))
+        P->max_splits = atoi(ms);
     const size_t L = n_layers, D = d, F = ff, MA = P->M_alloc, MM = M_max;
     P->ws_floats = (size_t)P->num_sms * 128 * 256;
     struct A { void **p; size_t bytes; } allocs[] = {
@@ -303,7 +333,6 @@ FRT_API frt_status frt_ffn_plan_create(int d, int ff, int act, int M_max, int n_
         {(void **)&P->rbuf[0], MM * D * 2},
         {(void **)&P->rbuf[1], MM * D * 2},
         {(void **)&P->rprime, MM * D * 2},
-        {(void **)&P->gu, MM * 2 * F * 2},
         {(void **)&P->qx, MA * D},
         {(void **)&P->qh, MA * F},
         {(void **)&P->ws, P->ws_floats * 4},
@@ -370,8 +399,7 @@ FRT_API frt_status frt_ffn_load_weights(frt_ffn_plan_t P, int layer, const void 
     memcpy(&a_gu, &h_amax[0], 4);
     memcpy(&a_d, &h_amax[1], 4);
     const float s_gu = scale_from_amax(a_gu), s_d = scale_from_amax(a_d);
-    CK(launch_quant_bf16(w_gate, F * D, 1.0f / s_gu, gu_dst, s));
-    CK(launch_quant_bf16(w_up, F * D, 1.0f / s_gu, gu_dst + F * D, s));
+    CK(launch_quant_gu_interleave(w_gate, w_up, (int)F, (int)D, 1.0f / s_gu, gu_dst, s));
     CK(launch_quant_bf16(w_down, D * F, 1.0f / s_d, d_dst, s));
     CK(cudaStreamSynchronize(s));
     P->s_gu[layer] = s_gu;
@@ -449,6 +477,7 @@ FRT_API frt_status frt_ffn_calibrate(frt_ffn_plan_t P, const void *const *residu
             memcpy(&a, &h_amax, 4);
             sx[l] = scale_from_amax(a);
             // 2. amax of the down GEMM input, r' of layer 0 kept in the batch state
+            CK(cudaMemsetAsync(P->amax + 1, 0, 4, s));
             for (int b = 0; b < n_batches; ++b) {
                 const void *in = l == 0 ? residual[b] : (const void *)st_of(b);
                 const void *hid = (l == 0 && hidden) ? hidden[b] : nullptr;
@@ -457,15 +486,12 @@ FRT_API frt_status frt_ffn_calibrate(frt_ffn_plan_t P, const void *const *residu
                 CK(launch_norm_quant(in, hid, wn, M, d, RMS_EPS, 1.0f / sx[l], hid ? (void *)st_of(b) : nullptr,
                                      P->qx, nullptr, false, s, false));
                 GemmLaunch g;
-                frt_status st2 = setup_gemm(P, g, 0, l, M);
+                P->s_x[l] = sx[l];
+                P->s_h[l] = 1.0f;
+                frt_status st2 = setup_gate_up(P, g, l, M, EPI_GATED_AMAX);
                 if (st2 != FRT_OK)
                     return st2;
-                g.p.epi = EPI_BF16;
-                g.p.alpha = sx[l] * P->s_gu[l];
-                g.p.out = P->gu;
-                g.p.ldo = 2 * ff;
                 CK(launch_gemm(g, s, false));
-                CK(launch_act_quant(P->gu, M, ff, P->act, 1.0f, P->qh, P->amax + 1, true, s, false));
             }
             CK(cudaMemcpyAsync(&h_amax, P->amax + 1, 4, cudaMemcpyDeviceToHost, s));
             CK(cudaStreamSynchronize(s));
@@ -597,6 +623,39 @@ FRT_API frt_status frt_ffn_debug_trace(frt_ffn_plan_t P, int layer, const void *
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     void *dst = out ? out : (void *)P->rbuf[0];
     return run_layer(P, layer, residual_in, hidden_in, dst, M, s, r_prime, q_x, gu, q_h);
+}
+
+FRT_API frt_status frt_ffn_debug_step(frt_ffn_plan_t P, int layer, int step, int M, frt_stream_t stream) {
+    if (!P)
+        return fail(FRT_ERR_INVALID_ARG, "null plan");
+    if (layer < 0 || layer >= P->L || step < 0 || step > 2 || M < 1)
+        return fail(FRT_ERR_INVALID_ARG, "bad layer, step or M");
+    if (M > P->M_max)
+        return fail(FRT_ERR_SHAPE, "M=%d exceeds M_max=%d", M, P->M_max);
+    if (!P->loaded[layer] || !P->scales_ok)
+        return fail(FRT_ERR_NOT_READY, "layer %d not loaded or scales not set", layer);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int d = P->d, ff = P->ff;
+    GemmLaunch g;
+    frt_status st;
+    switch (step) {
+    case 0:
+        CK(launch_norm_quant(P->rbuf[0], nullptr, P->w_norm + (size_t)layer * d, M, d, RMS_EPS, 1.0f / P->s_x[layer],
+                             nullptr, P->qx, nullptr, false, s, false));
+        break;
+    case 1:
+        if ((st = setup_gate_up(P, g, layer, M, EPI_GATED)) != FRT_OK)
+            return st;
+        CK(launch_gemm(g, s, false));
+        break;
+    default:
+        if ((st = setup_down(P, g, layer, M, P->rbuf[0], P->rbuf[1])) != FRT_OK)
+            return st;
+        CK(launch_gemm(g, s, false));
+        break;
+    }
+    (void)ff;
+    return FRT_OK;
 }
 
 FRT_API frt_status frt_ffn_device_status(frt_ffn_plan_t P, frt_stream_t stream) {

@@ -15,6 +15,8 @@ enum Epi : int {
     EPI_BF16 = 0,   // out[m][n] = bf16(acc * alpha)
     EPI_RESID = 1,  // out[m][n] = bf16(resid[m][n] + acc * alpha)
     EPI_F32 = 2,    // out[m][n] = acc * alpha (fp32; diagnostics)
+    EPI_GATED = 3,  // out = q_h[m][f] = E4M3(act(g) * u * inv_s), g/u = bf16(acc * alpha) (interleaved rows)
+    EPI_GATED_AMAX = 4,  // atomicMax(amax, |act(g) * u|) (calibration)
 };
 
 // One GEMM launch: C[token][feature] = epilogue(sum_k X[token][k] W[feature][k]).
@@ -39,6 +41,12 @@ struct GemmParams {
     float *ws;              // split-K partials
     int *counters;          // split-K arrival counters (zero between launches)
     int *err;               // device error word
+    // gated epilogues
+    int act;                // Act
+    int ff;                 // hidden width (feature count of q_h)
+    float inv_s;            // 1 / s_h
+    unsigned *amax;         // EPI_GATED_AMAX target
+    uint16_t *dbg_gu;       // optional: BF16 [g | u] [M, 2ff] (diagnostics)
 };
 
 struct GemmLaunch {
@@ -64,11 +72,11 @@ cudaError_t launch_gemm(const GemmLaunch &g, cudaStream_t s, bool pdl);
 
 cudaError_t launch_amax_bf16(const void *x, size_t n, unsigned *amax_word, cudaStream_t s);
 cudaError_t launch_quant_bf16(const void *x, size_t n, float inv_s, uint8_t *q, cudaStream_t s);
+cudaError_t launch_quant_gu_interleave(const void *gate, const void *up, int ff, int d, float inv_s, uint8_t *dst,
+                                      cudaStream_t s);
 cudaError_t launch_norm_quant(const void *r, const void *h, const void *w, int M, int d, float eps, float inv_s,
                               void *rprime, uint8_t *qx, unsigned *amax_word, bool measure, cudaStream_t s,
                               bool pdl);
-cudaError_t launch_act_quant(const void *gu, int M, int ff, int act, float inv_s, uint8_t *qh,
-                             unsigned *amax_word, bool measure, cudaStream_t s, bool pdl);
 
 }  // namespace frt
 

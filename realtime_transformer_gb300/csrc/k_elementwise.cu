@@ -5,11 +5,10 @@
 //       128-bit loads and a warp-shuffle reduction (agentlenshq FlashRT
 //       summary, "Main ideas": fused residual-norm-quantise; itsolotime
 //       article, 3.3: rms_norm kernel row);
-//   A3  gated activation (GeGLU with tanh GELU, or SwiGLU) + E4M3
-//       requantise, 8 outputs per thread (itsolotime article, 7.2).
-// Each A1/A3 kernel has a measure mode for calibration that records the
-// per-tensor amax instead of writing codes ("FlashRT docs/architecture.md",
-// 6 Calibration Framework).
+// (A3, the gated activation + requantise, runs in the gate/up GEMM's
+// epilogue, k_gemm_fp8.cu.)  The A1 kernel has a measure mode for
+// calibration that records the per-tensor amax instead of writing codes
+// ("FlashRT docs/architecture.md", 6 Calibration Framework).
 //
 // Arithmetic follows the rounding points of the method exactly: every fp32
 // operation is rounded on its own (explicit __f*_rn intrinsics), the scale
@@ -78,18 +77,6 @@ __device__ __forceinline__ void atomic_amax(unsigned *word, float v) {
     atomicMax(word, __float_as_uint(v));
 }
 
-// GELU, tanh form: 0.5 g (1 + tanh(sqrt(2/pi) (g + 0.044715 g^3))).
-__device__ __forceinline__ float gelu_tanh(float g) {
-    const float k0 = 0.7978845608028654f;
-    const float k1 = 0.044715f;
-    float g3 = __fmul_rn(__fmul_rn(g, g), g);
-    float inner = __fmul_rn(k0, __fadd_rn(g, __fmul_rn(k1, g3)));
-    return __fmul_rn(__fmul_rn(0.5f, g), __fadd_rn(1.0f, tanhf(inner)));
-}
-
-// SiLU: g / (1 + exp(-g)).
-__device__ __forceinline__ float silu(float g) { return __fdiv_rn(g, __fadd_rn(1.0f, expf(-g))); }
-
 // ------------------------------------------------------------------- A0 --
 
 __global__ void k_amax_bf16(const uint4 *__restrict__ x, size_t nvec, const uint16_t *__restrict__ tail,
@@ -122,6 +109,29 @@ __global__ void k_quant_bf16(const uint4 *__restrict__ x, size_t nvec, const uin
     if (blockIdx.x == 0 && threadIdx.x < (unsigned)ntail) {
         float v = __fmul_rn(__uint_as_float((uint32_t)tail[threadIdx.x] << 16), inv_s);
         qtail[threadIdx.x] = (uint8_t)(e4m3x2(v, 0.0f) & 0xFF);
+    }
+}
+
+// [W_gate; W_up] quantised into the interleaved arena layout: blocks of 128
+// rows, each 64 gate rows followed by the 64 up rows of the same features,
+// so that one GEMM tile holds matching gate and up rows.  d % 8 == 0,
+// ff % 64 == 0.
+__global__ void k_quant_gu_interleave(const uint16_t *__restrict__ gate, const uint16_t *__restrict__ up, int ff,
+                                      int d, float inv_s, uint8_t *__restrict__ dst) {
+    const size_t vpr = (size_t)d / 8;
+    const size_t total = (size_t)2 * ff * vpr;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+        const size_t row = i / vpr;
+        const size_t v = i - row * vpr;
+        const size_t within = row & 127;
+        const size_t srow = (row >> 7) * 64 + (within & 63);
+        const uint16_t *src = (within < 64 ? gate : up) + srow * d + v * 8;
+        float f[8];
+        unpack8(__ldg(reinterpret_cast<const uint4 *>(src)), f);
+#pragma unroll
+        for (int j = 0; j < 8; j++)
+            f[j] = __fmul_rn(f[j], inv_s);
+        *reinterpret_cast<uint2 *>(dst + row * d + v * 8) = pack8_e4m3(f);
     }
 }
 
@@ -202,47 +212,6 @@ __global__ void __launch_bounds__(256) k_norm_quant(const uint16_t *__restrict__
     }
 }
 
-// ------------------------------------------------------------------- A3 --
-
-// gu rows are [g_0 .. g_{ff-1}, u_0 .. u_{ff-1}] (BF16); a = act(g) * u.
-template <int ACT, bool MEASURE>
-__global__ void __launch_bounds__(256) k_act_quant(const uint16_t *__restrict__ gu, int M, int ff, float inv_s,
-                                                   uint8_t *__restrict__ qh, unsigned *amax_word) {
-    pdl_wait();
-    pdl_trigger();
-    const int vpr = ff >> 3;  // 8-wide vectors per row
-    const size_t total = (size_t)M * vpr;
-    float amax = 0.0f;
-    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
-        const size_t row = i / vpr;
-        const int j0 = (int)(i - row * vpr) << 3;
-        const uint16_t *base = gu + row * (size_t)(2 * ff);
-        float g[8], u[8], a[8];
-        unpack8(*reinterpret_cast<const uint4 *>(base + j0), g);
-        unpack8(*reinterpret_cast<const uint4 *>(base + ff + j0), u);
-#pragma unroll
-        for (int j = 0; j < 8; j++) {
-            const float ag = (ACT == ACT_SWIGLU) ? silu(g[j]) : gelu_tanh(g[j]);
-            a[j] = __fmul_rn(ag, u[j]);
-        }
-        if (MEASURE) {
-#pragma unroll
-            for (int j = 0; j < 8; j++)
-                amax = fmaxf(amax, fabsf(a[j]));
-        } else {
-#pragma unroll
-            for (int j = 0; j < 8; j++)
-                a[j] = __fmul_rn(a[j], inv_s);
-            *reinterpret_cast<uint2 *>(qh + row * (size_t)ff + j0) = pack8_e4m3(a);
-        }
-    }
-    if (MEASURE) {
-        amax = warp_max(amax);
-        if ((threadIdx.x & 31) == 0)
-            atomic_amax(amax_word, amax);
-    }
-}
-
 int sm_count() {
     static int n = 0;
     if (n == 0) {
@@ -282,6 +251,18 @@ cudaError_t launch_quant_bf16(const void *x, size_t n, float inv_s, uint8_t *q, 
     return cudaGetLastError();
 }
 
+cudaError_t launch_quant_gu_interleave(const void *gate, const void *up, int ff, int d, float inv_s, uint8_t *dst,
+                                      cudaStream_t s) {
+    const size_t total = (size_t)2 * ff * (d / 8);
+    size_t blocks = (total + 255) / 256;
+    const size_t cap = (size_t)sm_count() * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks == 0) blocks = 1;
+    k_quant_gu_interleave<<<(unsigned)blocks, 256, 0, s>>>(static_cast<const uint16_t *>(gate),
+                                                            static_cast<const uint16_t *>(up), ff, d, inv_s, dst);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_norm_quant(const void *r, const void *h, const void *w, int M, int d, float eps, float inv_s,
                               void *rprime, uint8_t *qx, unsigned *amax_word, bool measure, cudaStream_t s,
                               bool pdl) {
@@ -294,25 +275,6 @@ cudaError_t launch_norm_quant(const void *r, const void *h, const void *w, int M
         return launch_ex(k_norm_quant<true>, grid, block, 0, s, pdl, rr, hh, ww, M, d, eps, inv_s, rp, qx,
                          amax_word);
     return launch_ex(k_norm_quant<false>, grid, block, 0, s, pdl, rr, hh, ww, M, d, eps, inv_s, rp, qx, amax_word);
-}
-
-cudaError_t launch_act_quant(const void *gu, int M, int ff, int act, float inv_s, uint8_t *qh,
-                             unsigned *amax_word, bool measure, cudaStream_t s, bool pdl) {
-    const size_t total = (size_t)M * (ff / 8);
-    size_t blocks = (total + 255) / 256;
-    const size_t cap = (size_t)sm_count() * 16;
-    if (blocks > cap) blocks = cap;
-    if (blocks == 0) blocks = 1;
-    const dim3 grid((unsigned)blocks), block(256);
-    auto g = static_cast<const uint16_t *>(gu);
-    if (act == ACT_SWIGLU) {
-        if (measure)
-            return launch_ex(k_act_quant<ACT_SWIGLU, true>, grid, block, 0, s, pdl, g, M, ff, inv_s, qh, amax_word);
-        return launch_ex(k_act_quant<ACT_SWIGLU, false>, grid, block, 0, s, pdl, g, M, ff, inv_s, qh, amax_word);
-    }
-    if (measure)
-        return launch_ex(k_act_quant<ACT_GEGLU_TANH, true>, grid, block, 0, s, pdl, g, M, ff, inv_s, qh, amax_word);
-    return launch_ex(k_act_quant<ACT_GEGLU_TANH, false>, grid, block, 0, s, pdl, g, M, ff, inv_s, qh, amax_word);
 }
 
 }  // namespace frt

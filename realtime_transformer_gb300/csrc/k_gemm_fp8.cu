@@ -27,6 +27,7 @@
 // Every wait is bounded (frt_ptx.cuh); on a timeout the CTA drains its
 // in-flight copies and MMAs, frees TMEM and exits with the error word set.
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 
 #include <algorithm>
 
@@ -56,7 +57,8 @@ struct Cfg {
                                           : (2 * BN <= 256) ? 256
                                                             : 512;
     static constexpr int CH = BN < 32 ? 16 : 32;  // accumulator columns per tcgen05.ld
-    static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + 256;
+    static constexpr uint32_t XBUF_BYTES = 128 * (CH + 1) * 4;  // gate/up exchange (weight-streaming path)
+    static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + 256 + XBUF_BYTES;
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
     static_assert(Q_BYTES % 1024 == 0, "tiles must stay 1024-byte aligned");
 };
@@ -218,7 +220,41 @@ __device__ __forceinline__ void tmem_load_chunk(uint32_t taddr, float (&v)[CH]) 
         v[j] = __uint_as_float(r[j]);
 }
 
-// Store CH accumulator columns c .. c+CH-1 of P-row r of this unit's tile.
+// Accumulator columns c .. c+CH-1 of this thread's row: straight from TMEM,
+// or (split-K, last arriver) the sum of every split's partial in split order.
+template <int BN, int CH>
+__device__ __forceinline__ void fetch_chunk(bool from_ws, uint32_t tbase, const float *tile_ws, int splits, int r,
+                                            int c, float (&v)[CH]) {
+    if (!from_ws) {
+        tmem_load_chunk<CH>(tbase + c, v);
+        return;
+    }
+#pragma unroll
+    for (int j = 0; j < CH; ++j)
+        v[j] = 0.0f;
+    const float *src = tile_ws + (size_t)c * BM + r;
+    int sp = 0;
+#pragma unroll 1
+    for (; sp + 2 <= splits; sp += 2) {
+        float t0[CH], t1[CH];
+#pragma unroll
+        for (int j = 0; j < CH; ++j)
+            t0[j] = __ldcg(src + (size_t)sp * (BM * BN) + (size_t)j * BM);
+#pragma unroll
+        for (int j = 0; j < CH; ++j)
+            t1[j] = __ldcg(src + (size_t)(sp + 1) * (BM * BN) + (size_t)j * BM);
+#pragma unroll
+        for (int j = 0; j < CH; ++j)
+            v[j] = __fadd_rn(__fadd_rn(v[j], t0[j]), t1[j]);
+    }
+    if (sp < splits) {
+#pragma unroll
+        for (int j = 0; j < CH; ++j)
+            v[j] = __fadd_rn(v[j], __ldcg(src + (size_t)sp * (BM * BN) + (size_t)j * BM));
+    }
+}
+
+// Store CH accumulator columns c .. c+CH-1 of P-row r (plain epilogues).
 template <int BN, bool SWAP, int CH>
 __device__ __forceinline__ void store_chunk(const GemmParams &p, const Unit &w, int r, int c, const float (&v)[CH]) {
     if constexpr (!SWAP) {
@@ -239,6 +275,15 @@ __device__ __forceinline__ void store_chunk(const GemmParams &p, const Unit &w, 
             return;
         }
         uint16_t *o = static_cast<uint16_t *>(p.out) + (size_t)m * p.ldo + n0;
+        // residual vectors of the whole chunk first (out may alias resid)
+        uint4 rvs[CH / 8];
+#pragma unroll
+        for (int j = 0; j < CH; j += 8) {
+            rvs[j / 8] = make_uint4(0, 0, 0, 0);
+            if (p.epi == EPI_RESID && n0 + j < p.n_feat)
+                rvs[j / 8] = *reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.resid) +
+                                                             (size_t)m * p.ldr + n0 + j);
+        }
 #pragma unroll
         for (int j = 0; j < CH; j += 8) {
             if (n0 + j >= p.n_feat)
@@ -248,8 +293,7 @@ __device__ __forceinline__ void store_chunk(const GemmParams &p, const Unit &w, 
             for (int t = 0; t < 8; ++t)
                 f[t] = __fmul_rn(v[j + t], p.alpha);
             if (p.epi == EPI_RESID) {
-                const uint4 rv = *reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.resid) +
-                                                                 (size_t)m * p.ldr + n0 + j);
+                const uint4 rv = rvs[j / 8];
                 f[0] = __fadd_rn(bf_lo(rv.x), f[0]);
                 f[1] = __fadd_rn(bf_hi(rv.x), f[1]);
                 f[2] = __fadd_rn(bf_lo(rv.y), f[2]);
@@ -270,28 +314,205 @@ __device__ __forceinline__ void store_chunk(const GemmParams &p, const Unit &w, 
         const int n = w.tp * BM + r;  // feature
         if (n >= p.n_feat)
             return;
+        const int m0 = w.tq * BN + c;  // first token of the chunk
+        const int nv = min(CH, p.m_tok - m0);
+        if (nv <= 0)
+            return;
+        if (p.epi == EPI_F32) {
+#pragma unroll
+            for (int j = 0; j < CH; ++j)
+                if (j < nv)
+                    static_cast<float *>(p.out)[(size_t)(m0 + j) * p.ldo + n] = __fmul_rn(v[j], p.alpha);
+            return;
+        }
+        // Read every residual of the chunk before the first store: out may
+        // alias resid, and loads issued after stores would serialise.
+        float res[CH];
 #pragma unroll
         for (int j = 0; j < CH; ++j) {
-            const int m = w.tq * BN + c + j;  // token
-            if (m >= p.m_tok)
-                break;
-            float f = __fmul_rn(v[j], p.alpha);
-            if (p.epi == EPI_F32) {
-                static_cast<float *>(p.out)[(size_t)m * p.ldo + n] = f;
-            } else {
-                if (p.epi == EPI_RESID) {
-                    const uint16_t rb = static_cast<const uint16_t *>(p.resid)[(size_t)m * p.ldr + n];
-                    f = __fadd_rn(__uint_as_float((uint32_t)rb << 16), f);
-                }
-                static_cast<uint16_t *>(p.out)[(size_t)m * p.ldo + n] = (uint16_t)bf16_bits(f);
+            res[j] = 0.0f;
+            if (p.epi == EPI_RESID && j < nv)
+                res[j] = __uint_as_float((uint32_t)static_cast<const uint16_t *>(p.resid)[(size_t)(m0 + j) * p.ldr + n]
+                                         << 16);
+        }
+#pragma unroll
+        for (int j = 0; j < CH; ++j) {
+            if (j < nv) {
+                float f = __fmul_rn(v[j], p.alpha);
+                if (p.epi == EPI_RESID)
+                    f = __fadd_rn(res[j], f);
+                static_cast<uint16_t *>(p.out)[(size_t)(m0 + j) * p.ldo + n] = (uint16_t)bf16_bits(f);
             }
         }
     }
 }
 
+// --- gated epilogue (step A3 fused into the gate/up GEMM) -----------------
+// The weight arena holds [W_gate; W_up] interleaved in blocks of 64 rows
+// (64 gate rows, then the 64 up rows of the same features), so every tile
+// holds matching gate and up rows.  g and u are rounded to BF16 (where the
+// unfused method stores them), then a = act(g) * u and q_h = E4M3(a / s_h).
+
+__device__ __forceinline__ float round_bf16(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+
+// GELU, tanh form: 0.5 g (1 + tanh(sqrt(2/pi) (g + 0.044715 g^3))).
+__device__ __forceinline__ float gelu_tanh(float g) {
+    const float k0 = 0.7978845608028654f;
+    const float k1 = 0.044715f;
+    float g3 = __fmul_rn(__fmul_rn(g, g), g);
+    float inner = __fmul_rn(k0, __fadd_rn(g, __fmul_rn(k1, g3)));
+    return __fmul_rn(__fmul_rn(0.5f, g), __fadd_rn(1.0f, tanhf(inner)));
+}
+// SiLU: g / (1 + exp(-g)).
+__device__ __forceinline__ float silu(float g) { return __fdiv_rn(g, __fadd_rn(1.0f, expf(-g))); }
+
+__device__ __forceinline__ float gated(int act, float g, float u) {
+    return __fmul_rn(act == ACT_SWIGLU ? silu(g) : gelu_tanh(g), u);
+}
+
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+    return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
+}
+
+__device__ __forceinline__ void dbg_store_gu(const GemmParams &p, int m, int f, bool up, float val) {
+    if (p.dbg_gu)
+        p.dbg_gu[(size_t)m * 2 * p.ff + (up ? p.ff : 0) + f] = (uint16_t)bf16_bits(val);
+}
+
+// Weight-streaming path: TMEM lanes 0..63 are gate rows, 64..127 the up rows
+// of the same 64 features; columns are tokens.  Up values go through shared
+// memory to the gate threads.  Called by all 128 epilogue threads.
+template <int BN, int CH>
+__device__ __forceinline__ void gated_swap_chunk(const GemmParams &p, const Unit &w, int r, int c,
+                                                 const float (&v)[CH], float *xbuf, float &amax) {
+    const int m0 = w.tq * BN + c;  // first token of the chunk
+    {
+        const int f = w.tp * (BM / 2) + (r & 63);
+        const bool up = r >= 64;
+#pragma unroll
+        for (int j = 0; j < CH; ++j) {
+            const float gv = round_bf16(__fmul_rn(v[j], p.alpha));
+            xbuf[r * (CH + 1) + j] = gv;
+            if (m0 + j < p.m_tok)
+                dbg_store_gu(p, m0 + j, f, up, gv);
+        }
+    }
+    named_bar_sync(1, 128);
+    // thread t: feature t % 64, tokens of half t / 64 of the chunk
+    {
+        constexpr int HALF = CH / 2;
+        const int fl = r & 63;
+        const int f = w.tp * (BM / 2) + fl;
+        const int j0 = (r >> 6) * HALF;
+        uint8_t *qh = static_cast<uint8_t *>(p.out);
+        float a[HALF];
+#pragma unroll
+        for (int j = 0; j < HALF; ++j)
+            a[j] = gated(p.act, xbuf[fl * (CH + 1) + j0 + j], xbuf[(fl + 64) * (CH + 1) + j0 + j]);
+#pragma unroll
+        for (int j = 0; j < HALF; ++j) {
+            const int m = m0 + j0 + j;
+            if (m < p.m_tok) {
+                if (p.epi == EPI_GATED_AMAX)
+                    amax = fmaxf(amax, fabsf(a[j]));
+                else
+                    qh[(size_t)m * p.ldo + f] = (uint8_t)(e4m3x2(__fmul_rn(a[j], p.inv_s), 0.0f) & 0xFFu);
+            }
+        }
+    }
+    named_bar_sync(1, 128);
+}
+
+// Tiled path: TMEM lanes are tokens; columns [128q, 128q+64) are gate and
+// [128q+64, 128q+128) the up rows of the same 64 features.
+template <int CH>
+__device__ __forceinline__ void gated_tiled_chunk(const GemmParams &p, int m, int f0, const float (&g)[CH],
+                                                  const float (&u)[CH], float &amax) {
+    if (m >= p.m_tok)
+        return;
+    float a[CH];
+#pragma unroll
+    for (int j = 0; j < CH; ++j) {
+        const float gb = round_bf16(__fmul_rn(g[j], p.alpha));
+        const float ub = round_bf16(__fmul_rn(u[j], p.alpha));
+        dbg_store_gu(p, m, f0 + j, false, gb);
+        dbg_store_gu(p, m, f0 + j, true, ub);
+        a[j] = gated(p.act, gb, ub);
+    }
+    if (p.epi == EPI_GATED_AMAX) {
+#pragma unroll
+        for (int j = 0; j < CH; ++j)
+            amax = fmaxf(amax, fabsf(a[j]));
+        return;
+    }
+    uint8_t *q = static_cast<uint8_t *>(p.out) + (size_t)m * p.ldo + f0;
+#pragma unroll
+    for (int j = 0; j < CH; j += 16) {
+        uint4 ov;
+        ov.x = e4m3x2(__fmul_rn(a[j + 0], p.inv_s), __fmul_rn(a[j + 1], p.inv_s)) |
+               (e4m3x2(__fmul_rn(a[j + 2], p.inv_s), __fmul_rn(a[j + 3], p.inv_s)) << 16);
+        ov.y = e4m3x2(__fmul_rn(a[j + 4], p.inv_s), __fmul_rn(a[j + 5], p.inv_s)) |
+               (e4m3x2(__fmul_rn(a[j + 6], p.inv_s), __fmul_rn(a[j + 7], p.inv_s)) << 16);
+        ov.z = e4m3x2(__fmul_rn(a[j + 8], p.inv_s), __fmul_rn(a[j + 9], p.inv_s)) |
+               (e4m3x2(__fmul_rn(a[j + 10], p.inv_s), __fmul_rn(a[j + 11], p.inv_s)) << 16);
+        ov.w = e4m3x2(__fmul_rn(a[j + 12], p.inv_s), __fmul_rn(a[j + 13], p.inv_s)) |
+               (e4m3x2(__fmul_rn(a[j + 14], p.inv_s), __fmul_rn(a[j + 15], p.inv_s)) << 16);
+        *reinterpret_cast<uint4 *>(q + j) = ov;
+    }
+}
+
+__device__ __forceinline__ float warp_max_f(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// Consume one unit's accumulator (from TMEM or from the split-K workspace).
+template <int BN, bool SWAP>
+__device__ __forceinline__ void consume_unit(const GemmParams &p, const Unit &w, bool from_ws, uint32_t tbase,
+                                             const float *tile_ws, int ncols, float *xbuf) {
+    using C = Cfg<BN>;
+    constexpr int CH = C::CH;
+    const int r = threadIdx.x;
+    const bool gated_epi = p.epi == EPI_GATED || p.epi == EPI_GATED_AMAX;
+    float amax = 0.0f;
+    if (gated_epi && !SWAP) {
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 128) {
+#pragma unroll 1
+            for (int sub = 0; sub < 64; sub += CH) {
+                float g[CH], u[CH];
+                fetch_chunk<BN, CH>(from_ws, tbase, tile_ws, p.splits, r, c0 + sub, g);
+                fetch_chunk<BN, CH>(from_ws, tbase, tile_ws, p.splits, r, c0 + 64 + sub, u);
+                gated_tiled_chunk<CH>(p, w.tp * BM + r, w.tq * (BN / 2) + c0 / 2 + sub, g, u, amax);
+            }
+        }
+    } else {
+#pragma unroll 1
+        for (int c = 0; c < BN; c += CH) {
+            float v[CH];
+            if (from_ws && c >= ncols)
+                break;  // uniform: padding columns of the split-K partials
+            fetch_chunk<BN, CH>(from_ws, tbase, tile_ws, p.splits, r, c, v);
+            if (gated_epi) {
+                if constexpr (SWAP)
+                    gated_swap_chunk<BN, CH>(p, w, r, c, v, xbuf, amax);
+            } else {
+                store_chunk<BN, SWAP, CH>(p, w, r, c, v);
+            }
+        }
+    }
+    if (p.epi == EPI_GATED_AMAX) {
+        amax = warp_max_f(amax);
+        if ((threadIdx.x & 31) == 0)
+            atomicMax(p.amax, __float_as_uint(amax));
+    }
+}
+
 template <int BN, bool SWAP>
 __device__ void epilogue(const GemmParams &p, uint64_t *tfull, uint64_t *tempty, uint32_t tmem_base,
-                         volatile int *abort_f, volatile int *s_ok, volatile int *s_last) {
+                         volatile int *abort_f, volatile int *s_ok, volatile int *s_last, float *xbuf) {
     using C = Cfg<BN>;
     constexpr int CH = C::CH;
     const int warp = threadIdx.x >> 5;
@@ -311,48 +532,40 @@ __device__ void epilogue(const GemmParams &p, uint64_t *tfull, uint64_t *tempty,
         tc_fence_after();
         const uint32_t tbase = tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(abuf * BN);
         if (p.splits == 1) {
-#pragma unroll 1
-            for (int c = 0; c < BN; c += CH) {
-                float v[CH];
-                tmem_load_chunk<CH>(tbase + c, v);
-                store_chunk<BN, SWAP, CH>(p, w, r, c, v);
-            }
+            consume_unit<BN, SWAP>(p, w, false, tbase, nullptr, BN, xbuf);
             tc_fence_before();
             mbar_arrive(smem_u32(&tempty[abuf]));
         } else {
+            // Split-K: park this split's fp32 partial in the workspace
+            // ([column][row], so a warp's accesses are contiguous); the last
+            // split to arrive on the tile sums all partials in split order.
+            // Columns past the last valid token (weight-streaming path) are
+            // padding and are skipped.
+            const int ncols = SWAP ? min(BN, p.m_tok - w.tq * BN) : BN;
             float *mine = p.ws + ((size_t)w.tile * p.splits + w.split) * (size_t)(BM * BN);
 #pragma unroll 1
             for (int c = 0; c < BN; c += CH) {
                 float v[CH];
                 tmem_load_chunk<CH>(tbase + c, v);
+                if (c < ncols) {
 #pragma unroll
-                for (int j = 0; j < CH; ++j)
-                    mine[(size_t)(c + j) * BM + r] = v[j];
+                    for (int j = 0; j < CH; ++j)
+                        mine[(size_t)(c + j) * BM + r] = v[j];
+                }
             }
             tc_fence_before();
             mbar_arrive(smem_u32(&tempty[abuf]));
-            __threadfence();
             named_bar_sync(1, 128);
             if (threadIdx.x == 0) {
-                const int prev = atomicAdd(&p.counters[w.tile], 1);
+                // release: this CTA's partial (ordered before by the barrier);
+                // acquire: every other split's partial, for the last arriver
+                const int prev = atomic_add_acq_rel_gpu(&p.counters[w.tile], 1);
                 s_last[abuf] = (prev == p.splits - 1) ? 1 : 0;
             }
             named_bar_sync(1, 128);
             if (s_last[abuf]) {
-                __threadfence();
                 const float *tile_ws = p.ws + (size_t)w.tile * p.splits * (size_t)(BM * BN);
-#pragma unroll 1
-                for (int c = 0; c < BN; c += CH) {
-                    float v[CH];
-#pragma unroll
-                    for (int j = 0; j < CH; ++j) {
-                        float s = 0.0f;
-                        for (int sp = 0; sp < p.splits; ++sp)
-                            s = __fadd_rn(s, ld_cg_f32(tile_ws + (size_t)sp * (BM * BN) + (size_t)(c + j) * BM + r));
-                        v[j] = s;
-                    }
-                    store_chunk<BN, SWAP, CH>(p, w, r, c, v);
-                }
+                consume_unit<BN, SWAP>(p, w, true, tbase, tile_ws, ncols, xbuf);
                 if (threadIdx.x == 0)
                     p.counters[w.tile] = 0;  // ready for the next launch
             }
@@ -384,6 +597,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     volatile int *abort_f = reinterpret_cast<volatile int *>(tmem_holder + 1);
     volatile int *s_ok = abort_f + 1;    // [2]
     volatile int *s_last = s_ok + 2;     // [2]
+    float *xbuf = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(bars) + 256);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -415,7 +629,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     pdl_trigger();
 
     if (warp < 4) {
-        epilogue<BN, SWAP>(p, tfull, tempty, tmem_base, abort_f, s_ok, s_last);
+        epilogue<BN, SWAP>(p, tfull, tempty, tmem_base, abort_f, s_ok, s_last, xbuf);
     } else if (warp == 4) {
         if (lane == 0)
             producer<BN, SWAP>(&tmP, &tmQ, p, sP, sQ, full, empty, abort_f);

@@ -1,0 +1,53 @@
+"""Host logic of bench.py that needs no GPU: the max-over-ranks timing
+reduction and the barrier, on world_size 2 over gloo; the roofline byte
+accounting."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+import synthetic
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    bench.barrier(world)
+    m = bench.reduce_max(1.5 + rank, world, "cpu")
+    q.put((rank, m))
+    dist.destroy_process_group()
+
+
+def test_reduce_max_over_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(60)
+    got = dict(q.get(timeout=5) for _ in range(2))
+    assert got == {0: 2.5, 1: 2.5}
+
+
+def test_single_rank_needs_no_process_group():
+    assert bench.reduce_max(3.0, 1, "cpu") == 3.0
+
+
+def test_algorithmic_bytes():
+    wl = synthetic.WORKLOADS["vla_action_expert"]
+    b, f = bench.kernel_bytes_flops(wl, wl.M, 1)
+    assert b == 2 * 4096 * 1024 + 50 * 1024 + 50 * 4096 and f == 2 * 50 * 8192 * 1024
+    assert bench.layer_algorithmic_bytes(wl, wl.M) == 3 * 1024 * 4096 + 4 * 50 * 1024

@@ -1,14 +1,21 @@
 """Teacher-forced parity of one layer (steps A0..A4) against the oracle: both
-sides get the same layer input and the same scales; every intermediate is
-compared (itsolotime FlashRT article, 7.2; agentlenshq summary, "Main
-ideas": fused residual-norm-quantise)."""
+sides get the same layer input and the same scales, and every intermediate
+is compared (itsolotime FlashRT article, 7.2; agentlenshq summary, "Main
+ideas": fused residual-norm-quantise).
+
+GPU and oracle sum the RMSNorm mean square in different orders, so about one
+q_x element per call lands on the other side of an E4M3 rounding boundary
+(allowed: one code step).  Everything after q_x in that row is then a
+different, equally valid computation, so the gate/up output and q_h are held
+to the contract on rows whose q_x codes agree; the layer output is held to it
+on all rows."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
 import synthetic
-from parity import Case, bits, check_bf16, check_codes, u8
+from parity import Case, bits, check_bf16, check_codes, cosine, u8
 
 pytestmark = pytest.mark.gpu
 
@@ -39,22 +46,35 @@ def test_weight_scales_match_oracle_exactly(case):
         assert sc["s_down"][l] == np.float32(ql.s_d)
 
 
+def compare_layer(plan, layer, r_bits, h_bits, ql, s_x, s_h, act, dev, what=""):
+    """Run GPU layer `layer` and the oracle on the same input; check the contract."""
+    r = synthetic.from_bf16_bits(r_bits, dev)
+    h = synthetic.from_bf16_bits(h_bits, dev) if h_bits is not None else None
+    tr = plan.trace_layer(layer, r, h)
+    torch.cuda.synchronize()
+    plan.device_status()
+    ref = oracle.ffn_layer(r_bits, h_bits, ql.w_norm, ql.q_gu, ql.q_down, s_x, s_h, ql.s_gu, ql.s_d, act, trace=True)
+    assert np.array_equal(bits(tr["r_prime"]), ref.r_prime), "r' = bf16(r + h) must be bit-exact"
+    qx = u8(tr["q_x"])
+    agree_x = check_codes(qx, ref.q_x, what + " q_x")
+    rows = np.all(qx == ref.q_x, axis=1)
+    assert rows.mean() >= 0.5, what
+    gu = bits(tr["gu"])
+    check_bf16(gu[rows], ref.gu[rows], what + " gate/up (rows with identical q_x)")
+    assert cosine(oracle.bf16_decode(gu), oracle.bf16_decode(ref.gu)) >= 0.9999
+    agree_h = check_codes(u8(tr["q_h"])[rows], ref.q_h[rows], what + " q_h (rows with identical q_x)")
+    c, e = check_bf16(bits(tr["out"]), ref.out, what + " layer output")
+    return dict(q_x=agree_x, rows=float(rows.mean()), q_h=agree_h, cos=c, err=e, out=bits(tr["out"]),
+                ref_out=ref.out)
+
+
 @pytest.mark.parametrize("with_hidden", [True, False])
 def test_layer_intermediates_match_oracle(case, with_hidden):
     wl = case.wl
-    dev = case.dev
-    h = case.h if with_hidden else None
-    tr = case.plan.trace_layer(0, case.r.to(dev), h.to(dev) if h is not None else None)
-    torch.cuda.synchronize()
-    case.plan.device_status()
-    ql = case.q[0]
-    ref = oracle.ffn_layer(bits(case.r), bits(h) if h is not None else None, ql.w_norm, ql.q_gu, ql.q_down,
-                           case.s_x[0], case.s_h[0], ql.s_gu, ql.s_d, wl.act_id, trace=True)
-    assert np.array_equal(bits(tr["r_prime"]), ref.r_prime), "r' = bf16(r + h) must be bit-exact"
-    check_codes(u8(tr["q_x"]), ref.q_x, "q_x")
-    check_bf16(bits(tr["gu"]), ref.gu, "gate/up output")
-    check_codes(u8(tr["q_h"]), ref.q_h, "q_h")
-    check_bf16(bits(tr["out"]), ref.out, "layer output")
+    st = compare_layer(case.plan, 0, bits(case.r), bits(case.h) if with_hidden else None, case.q[0],
+                       case.s_x[0], case.s_h[0], wl.act_id, case.dev, wl.name)
+    print("%s hidden=%s: q_x agree %.6f, rows %.3f, q_h agree %.6f, out cos %.7f err %.4f" % (
+        wl.name, with_hidden, st["q_x"], st["rows"], st["q_h"], st["cos"], st["err"]))
 
 
 def test_out_may_alias_residual(case):

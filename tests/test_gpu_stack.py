@@ -1,13 +1,21 @@
-"""Free-running stack parity, graph capture/replay and calibration against the
-oracle ("FlashRT docs/architecture.md", 6 Calibration Framework and 7 CUDA
-Graph Capture; itsolotime FlashRT article, 4.1-4.2)."""
+"""Stack parity, graph capture/replay and calibration against the oracle
+("FlashRT docs/architecture.md", 6 Calibration Framework and 7 CUDA Graph
+Capture; itsolotime FlashRT article, 4.1-4.2).
+
+Per-layer parity through the whole stack is teacher-forced: GPU layer l runs
+on the oracle's own layer-l input (oracle values may feed the GPU, never the
+reverse).  Free-running, the two pipelines round different elements across
+E4M3 boundaries and drift apart like two FP8 runs with different summation
+orders; there the stack is held to the cosine claim against the unquantised
+forward and to cosine >= 0.999 against the oracle."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
 import synthetic
-from parity import Case, bits, check_bf16
+from parity import Case, bits, cosine
+from test_gpu_layer import compare_layer
 
 pytestmark = pytest.mark.gpu
 
@@ -24,12 +32,33 @@ def case(request):
     c.close()
 
 
-def test_eager_forward_matches_oracle_stack(case):
+def test_every_layer_teacher_forced(case):
+    wl = case.wl
+    traces = case.oracle_forward(trace=True)
+    cur = bits(case.r)
+    for l in range(wl.L):
+        st = compare_layer(case.plan, l, cur, bits(case.h) if l == 0 else None, case.q[l], case.s_x[l],
+                           case.s_h[l], wl.act_id, case.dev, "%s layer %d" % (wl.name, l))
+        print("%s layer %2d: q_x %.6f rows %.3f q_h %.6f out cos %.7f err %.4f" % (
+            wl.name, l, st["q_x"], st["rows"], st["q_h"], st["cos"], st["err"]))
+        cur = traces[l].out
+
+
+def test_free_running_stack(case):
     dev = case.dev
     out = case.plan.forward(case.r.to(dev), case.h.to(dev))
     torch.cuda.synchronize()
     case.plan.device_status()
-    check_bf16(bits(out), case.oracle_forward(), "stack output")
+    got = oracle.bf16_decode(bits(out)).astype(np.float64)
+    ref_q = oracle.bf16_decode(case.oracle_forward()).astype(np.float64)
+    ws = [{k: bits(v) for k, v in w.items()} for w in case.weights]
+    ref32 = oracle.ref_stack_f32(ws, bits(case.r), bits(case.h), case.wl.act_id).astype(np.float64)
+    c_q, c_gpu, c_orc = cosine(got, ref_q), cosine(got, ref32), cosine(ref_q, ref32)
+    print("%s free-running: cos(gpu, oracle) %.7f, cos(gpu, fp32) %.7f, cos(oracle, fp32) %.7f, "
+          "max|gpu-oracle|/rms %.4f" % (case.wl.name, c_q, c_gpu, c_orc,
+                                        np.abs(got - ref_q).max() / np.sqrt((ref_q ** 2).mean())))
+    assert c_q >= 0.999
+    assert c_gpu >= c_orc - 1e-3
 
 
 def test_graph_replay_equals_eager(case):
@@ -37,6 +66,7 @@ def test_graph_replay_equals_eager(case):
     r = case.r.to(dev)
     h = case.h.to(dev)
     eager = case.plan.forward(r, h)
+    torch.cuda.synchronize()           # the plan's scratch is shared across streams
     out = torch.empty_like(r)
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
@@ -47,19 +77,48 @@ def test_graph_replay_equals_eager(case):
     s.synchronize()
     case.plan.device_status()
     assert torch.equal(out, eager)
+    again = case.plan.forward(r, h)
+    torch.cuda.synchronize()
+    assert torch.equal(again, eager)
 
 
 def test_gpu_calibration_matches_oracle(case):
+    """Full-stack GPU calibration.  Layer 0: the mean square of each row is
+    summed in a different order on each side, which moves it by at most
+    d * 2^-24 relative, so s_x moves by at most half that (plus rounding).
+    Later layers drift with the free-running pipelines (reported, held to 5%)."""
     dev = case.dev
     saved = case.plan.scales()
     case.plan.calibrate([a.to(dev) for a, _ in case.calib], [b.to(dev) for _, b in case.calib])
     sc = case.plan.scales()
     case.plan.set_scales(saved["s_x"], saved["s_h"])
-    sx = np.array(sc["s_x"], np.float64)
-    sh = np.array(sc["s_h"], np.float64)
-    rx = np.array(case.s_x, np.float64)
-    rh = np.array(case.s_h, np.float64)
-    assert np.all(np.abs(sx - rx) <= 1e-3 * rx), (sx, rx)
-    assert np.all(np.abs(sh - rh) <= 1e-3 * rh), (sh, rh)
-    # layer 0's input scale depends only on RMSNorm: within a few fp32 ulp
-    assert abs(sx[0] - rx[0]) <= 4 * np.spacing(np.float32(rx[0]))
+    sx, sh = np.array(sc["s_x"]), np.array(sc["s_h"])
+    rx, rh = np.array(case.s_x), np.array(case.s_h)
+    rel = np.maximum(np.abs(sx - rx) / rx, np.abs(sh - rh) / rh)
+    print("%s calibration rel diff per layer: %s" % (case.wl.name, np.array2string(rel, precision=2)))
+    assert abs(sx[0] - rx[0]) <= (0.5 * case.wl.d + 4) * 2.0 ** -24 * rx[0]
+    assert abs(sh[0] - rh[0]) <= 1e-3 * rh[0]
+    assert np.all(rel <= 5e-2)
+
+
+def test_calibration_teacher_forced_per_layer(case):
+    """Each layer's calibration on the oracle's own calibration state for that
+    layer (a one-layer plan per layer): scales within 1e-3 of the oracle's."""
+    from realtime_transformer_gb300.ffn import FFNPlan
+    wl = case.wl
+    dev = case.dev
+    rb = [bits(a) for a, _ in case.calib]
+    hb = [bits(b) for _, b in case.calib]
+    for l in range(wl.L):
+        ql = case.q[l]
+        plan = FFNPlan(wl.d, wl.ff, wl.act, wl.M, 1)
+        w = case.weights[l]
+        plan.load_weights(0, *(w[k].to(dev) for k in ("w_norm", "w_gate", "w_up", "w_down")))
+        plan.calibrate([synthetic.from_bf16_bits(x, dev) for x in rb],
+                       [synthetic.from_bf16_bits(x, dev) for x in hb] if l == 0 else None)
+        sc = plan.scales()
+        plan.close()
+        sx, sh, rb = oracle.calibrate_layer(rb, hb if l == 0 else None, ql.w_norm, ql.q_gu, ql.q_down, ql.s_gu,
+                                            ql.s_d, wl.act_id)
+        assert abs(sc["s_x"][0] - sx) <= 1e-3 * sx, (l, sc["s_x"][0], sx)
+        assert abs(sc["s_h"][0] - sh) <= 1e-3 * sh, (l, sc["s_h"][0], sh)
