@@ -158,10 +158,11 @@ frt_status setup_gemm(frt_ffn_plan *P, GemmLaunch &g, int site, int l, int M) {
         g.p.p_row0 = 0;
         g.p.q_row0 = l * N;
     }
-    if (gemm_ws_floats(g) > P->ws_floats || (g.p.splits > 1 && gemm_tiles(g) > COUNTERS_PER_GEMM))
+    if (gemm_ws_floats(g) > P->ws_floats || (g.p.splits > 1 && gemm_tiles(g) > COUNTERS_PER_GEMM / 2))
         return fail(FRT_ERR_UNSUPPORTED, "split-K workspace too small for M=%d site %d", M, site);
     g.p.ws = P->ws;
     g.p.counters = P->counters + site * COUNTERS_PER_GEMM;
+    g.p.done_off = COUNTERS_PER_GEMM / 2;
     g.p.err = P->err;
     return FRT_OK;
 }
@@ -688,7 +689,7 @@ FRT_API frt_status frt_fp8_gemm(frt_ffn_plan_t P, const void *A, const void *B, 
     GemmLaunch g;
     memset(&g.p, 0, sizeof g.p);
     plan_gemm(g, swap, M, N, K, P->num_sms, splits);
-    if (gemm_ws_floats(g) > P->ws_floats || (g.p.splits > 1 && gemm_tiles(g) > COUNTERS_PER_GEMM))
+    if (gemm_ws_floats(g) > P->ws_floats || (g.p.splits > 1 && gemm_tiles(g) > COUNTERS_PER_GEMM / 2))
         return fail(FRT_ERR_UNSUPPORTED, "split-K workspace too small");
     cudaError_t e1, e2;
     if (swap) {
@@ -706,6 +707,7 @@ FRT_API frt_status frt_fp8_gemm(frt_ffn_plan_t P, const void *A, const void *B, 
     g.p.ldo = N;
     g.p.ws = P->ws;
     g.p.counters = P->counters;
+    g.p.done_off = COUNTERS_PER_GEMM / 2;
     g.p.err = P->err;
     CK(launch_gemm(g, static_cast<cudaStream_t>(stream), false));
     return FRT_OK;

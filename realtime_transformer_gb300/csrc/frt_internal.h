@@ -28,6 +28,7 @@ struct GemmParams {
     int n_tiles_p, n_tiles_q;
     int k_blocks;           // ceil(K / 128)
     int splits;             // split-K factor (1 = none)
+    int stages;             // shared-memory pipeline stages of this launch
     int kb_per_split;
     int total_units;        // n_tiles_p * n_tiles_q * splits
     int epi;                // Epi
@@ -39,7 +40,8 @@ struct GemmParams {
     int m_tok;              // valid token rows
     int n_feat;             // valid feature columns
     float *ws;              // split-K partials
-    int *counters;          // split-K arrival counters (zero between launches)
+    int *counters;          // split-K counters: arrivals at [tile], done-reading at [done_off + tile]
+    int done_off;
     int *err;               // device error word
     // gated epilogues
     int act;                // Act

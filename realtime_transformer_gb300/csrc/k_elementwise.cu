@@ -145,8 +145,11 @@ __global__ void __launch_bounds__(256) k_norm_quant(const uint16_t *__restrict__
                                                     const uint16_t *__restrict__ w, int M, int d, float eps,
                                                     float inv_s, uint16_t *__restrict__ rprime,
                                                     uint8_t *__restrict__ qx, unsigned *amax_word) {
-    pdl_wait();
+    // Let the dependent GEMM launch (and stream its weights) right away; it
+    // waits for this grid, and this grid waits for its own predecessor
+    // before it can complete, so ordering is preserved.
     pdl_trigger();
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int row = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
     if (row >= M)

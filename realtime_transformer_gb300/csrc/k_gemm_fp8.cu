@@ -30,6 +30,7 @@
 #include <cuda_fp8.h>
 
 #include <algorithm>
+#include <cstdlib>
 
 #include "frt_internal.h"
 #include "frt_ptx.cuh"
@@ -42,25 +43,35 @@ constexpr int BM = 128;        // MMA M = rows of the P tile = TMEM lanes
 constexpr int BK = 128;        // K bytes per stage = one 128-byte swizzle row
 constexpr int UK = 32;         // K of one tcgen05.mma for 8-bit operands
 constexpr int NTHREADS = 192;  // 4 epilogue warps + producer warp + MMA warp
-constexpr int SMEM_STAGE_BUDGET = 196608;
+constexpr uint32_t SMEM_LIMIT = 232448;  // largest dynamic shared memory of one CTA (227 KB)
 
-template <int BN>
+template <int BN, bool SWAP = false>
 struct Cfg {
     static constexpr uint32_t P_BYTES = BM * BK;
     static constexpr uint32_t Q_BYTES = BN * BK;
     static constexpr uint32_t STAGE_BYTES = P_BYTES + Q_BYTES;
-    static constexpr int STAGES = (SMEM_STAGE_BUDGET / (int)STAGE_BYTES) > 10 ? 10
-                                                                             : (SMEM_STAGE_BUDGET / (int)STAGE_BYTES);
+    static constexpr int CH = BN < 32 ? 16 : 32;  // accumulator columns per tcgen05.ld
+    static constexpr uint32_t XBUF_BYTES = SWAP ? 128 * (CH + 1) * 4 : 0;  // gate/up exchange
+    static constexpr int STAGES_FIT =
+        (int)((SMEM_LIMIT - 1024 - 256 - XBUF_BYTES) / STAGE_BYTES);
+    static constexpr int STAGES = STAGES_FIT > 10 ? 10 : STAGES_FIT;  // most stages a launch may ask for
     static constexpr uint32_t TMEM_COLS = (2 * BN <= 32)    ? 32
                                           : (2 * BN <= 64)  ? 64
                                           : (2 * BN <= 128) ? 128
                                           : (2 * BN <= 256) ? 256
                                                             : 512;
-    static constexpr int CH = BN < 32 ? 16 : 32;  // accumulator columns per tcgen05.ld
-    static constexpr uint32_t XBUF_BYTES = 128 * (CH + 1) * 4;  // gate/up exchange (weight-streaming path)
     static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + 256 + XBUF_BYTES;
+    // Shared memory of a launch with `stages` pipeline stages: a small
+    // footprint lets the next kernel's CTAs share the SM and start streaming
+    // their weights while this one runs.
+    // (the gate/up exchange buffer only for the unsplit gated epilogue)
+    static size_t smem_bytes(int stages, bool xbuf) {
+        return 1024 + (size_t)stages * STAGE_BYTES + 256 + (xbuf ? XBUF_BYTES : 0);
+    }
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
     static_assert(Q_BYTES % 1024 == 0, "tiles must stay 1024-byte aligned");
+    static_assert(STAGES >= 2, "pipeline needs two stages");
+    static_assert(SMEM <= SMEM_LIMIT, "shared memory over the per-CTA limit");
 };
 
 struct Unit {
@@ -88,13 +99,14 @@ __device__ __forceinline__ uint32_t bf16_bits(float x) {
 template <int BN, bool SWAP>
 __device__ void producer(const CUtensorMap *tmP, const CUtensorMap *tmQ, const GemmParams &p, uint8_t *sP,
                          uint8_t *sQ, uint64_t *full, uint64_t *empty, volatile int *abort_f) {
-    using C = Cfg<BN>;
+    using C = Cfg<BN, SWAP>;
     const uint64_t pol_w = l2_policy_evict_first();  // weights: read once per launch
     const uint64_t pol_x = l2_policy_evict_last();   // activations: re-read by many CTAs
     int stage = 0;
     uint32_t phase = 0;
     bool waited = false;
     int n_def = 0;
+    const int NS = p.stages;
     int def_stage[C::STAGES], def_kb[C::STAGES], def_row[C::STAGES];
     uint32_t issued = 0, issued_par = 0;
     for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
@@ -125,7 +137,7 @@ __device__ void producer(const CUtensorMap *tmP, const CUtensorMap *tmQ, const G
                     def_kb[n_def] = kb;
                     def_row[n_def] = xrow;
                     ++n_def;
-                    if (n_def == C::STAGES || kb + 1 == w.kb1) {
+                    if (n_def == NS || kb + 1 == w.kb1) {
                         pdl_wait();
                         waited = true;
                         for (int i = 0; i < n_def; ++i) {
@@ -138,7 +150,7 @@ __device__ void producer(const CUtensorMap *tmP, const CUtensorMap *tmQ, const G
                     }
                 }
             }
-            if (++stage == C::STAGES) {
+            if (++stage == NS) {
                 stage = 0;
                 phase ^= 1u;
             }
@@ -149,17 +161,17 @@ __device__ void producer(const CUtensorMap *tmP, const CUtensorMap *tmQ, const G
     return;
 drain:
     // Give copies in flight a bounded time to land before the CTA exits.
-    for (int s = 0; s < C::STAGES; ++s)
+    for (int s = 0; s < NS; ++s)
         if (issued & (1u << s))
             mbar_wait_for(smem_u32(&full[s]), (issued_par >> s) & 1u, 100000000ull);
 }
 
 // ---------------------------------------------------------- MMA issuer --
-template <int BN>
+template <int BN, bool SWAP>
 __device__ void mma_issuer(const GemmParams &p, uint8_t *sP, uint8_t *sQ, uint64_t *full, uint64_t *empty,
                            uint64_t *tfull, uint64_t *tempty, uint64_t *drain_bar, uint32_t tmem_base,
                            volatile int *abort_f) {
-    using C = Cfg<BN>;
+    using C = Cfg<BN, SWAP>;
     constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
     int stage = 0;
     uint32_t phase = 0;
@@ -185,7 +197,7 @@ __device__ void mma_issuer(const GemmParams &p, uint8_t *sP, uint8_t *sQ, uint64
                                (kb > w.kb0 || k > 0) ? 1u : 0u);
                 issued_any = true;
                 mma_commit(smem_u32(&empty[stage]));  // frees the stage when these MMAs finish
-                if (++stage == C::STAGES) {
+                if (++stage == p.stages) {
                     stage = 0;
                     phase ^= 1u;
                 }
@@ -472,7 +484,7 @@ __device__ __forceinline__ float warp_max_f(float v) {
 template <int BN, bool SWAP>
 __device__ __forceinline__ void consume_unit(const GemmParams &p, const Unit &w, bool from_ws, uint32_t tbase,
                                              const float *tile_ws, int ncols, float *xbuf) {
-    using C = Cfg<BN>;
+    using C = Cfg<BN, SWAP>;
     constexpr int CH = C::CH;
     const int r = threadIdx.x;
     const bool gated_epi = p.epi == EPI_GATED || p.epi == EPI_GATED_AMAX;
@@ -510,10 +522,233 @@ __device__ __forceinline__ void consume_unit(const GemmParams &p, const Unit &w,
     }
 }
 
+// Split-K, cooperative.  Every split CTA of a tile parks its fp32 partial in
+// the workspace, counts itself in on the tile's arrival counter (release),
+// waits until all S splits have arrived (acquire, bounded), then reduces one
+// 1/S slice of the tile's elements over all partials in split order
+// (deterministic) and runs the epilogue for that slice.  All splits of a tile
+// must be resident at once: the planner keeps tiles x splits <= SMs, one unit
+// per CTA, and a dependent kernel only launches once every CTA of this one is
+// resident.  The last CTA to finish reading resets the tile's counters.
+// Partial layout: weight-streaming [column][row] (a warp writes 32
+// consecutive rows), tiled [row][column] (a thread writes its own row).
+__device__ __forceinline__ bool spin_until_geq(const int *addr, int target, volatile int *abort_f, int *err) {
+    const uint64_t t0 = globaltimer();
+    for (uint32_t i = 0;; ++i) {
+        if (ld_acquire_gpu(addr) >= target)
+            return true;
+        if ((i & 15u) == 15u) {
+            if (*abort_f)
+                return false;
+            if (globaltimer() - t0 > WAIT_TIMEOUT_NS) {
+                *abort_f = 1;
+                atomicExch(err, DEVERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+// Index range [lo, hi) of one partial that holds everything the slice of
+// split `k` needs, and the element range [e0, e1) of that slice.  Elements
+// are enumerated so that a slice covers whole accumulator columns (weight-
+// streaming) or rows (tiled) when gated, so the range is contiguous.
+struct Slice {
+    int e0, e1, lo, hi;
+};
+
+template <int BN, bool SWAP>
+__device__ __forceinline__ Slice slice_of(int k, int S, int ncols, int nrows, bool gated_epi) {
+    Slice sl;
+    if (SWAP) {
+        const int inner = gated_epi ? BM / 2 : BM;
+        const int E = ncols * inner;
+        // whole columns per split when gated, else 4-element (16 B) granules
+        const int gran = gated_epi ? inner : 4;
+        const int per = ((E + S - 1) / S + gran - 1) / gran * gran;
+        sl.e0 = min(E, k * per);
+        sl.e1 = min(E, sl.e0 + per);
+        if (gated_epi) {
+            sl.lo = (sl.e0 / inner) * BM;
+            sl.hi = ((sl.e1 + inner - 1) / inner) * BM;
+        } else {
+            sl.lo = sl.e0;
+            sl.hi = (sl.e1 + 3) & ~3;
+        }
+    } else {
+        const int inner = gated_epi ? BN / 2 : BN;
+        const int E = nrows * inner;
+        const int gran = gated_epi ? inner : 4;
+        const int per = ((E + S - 1) / S + gran - 1) / gran * gran;
+        sl.e0 = min(E, k * per);
+        sl.e1 = min(E, sl.e0 + per);
+        if (gated_epi) {
+            sl.lo = (sl.e0 / inner) * BN;
+            sl.hi = ((sl.e1 + inner - 1) / inner) * BN;
+        } else {
+            sl.lo = sl.e0;
+            sl.hi = (sl.e1 + 3) & ~3;
+        }
+    }
+    return sl;
+}
+
+template <int BN, bool SWAP>
+__device__ bool coop_split_unit(const GemmParams &p, const Unit &w, uint32_t tbase, uint64_t *tempty_b,
+                                uint64_t *red_bar, float *red, volatile int *abort_f, volatile int *s_flag) {
+    constexpr int CH = Cfg<BN, SWAP>::CH;
+    const int r = threadIdx.x;
+    const int S = p.splits;
+    const int ncols = SWAP ? min(BN, p.m_tok - w.tq * BN) : BN;
+    const int nrows = SWAP ? BM : min(BM, p.m_tok - w.tp * BM);
+    const float *tile_ws = p.ws + (size_t)w.tile * S * (size_t)(BM * BN);
+    float *mine = p.ws + ((size_t)w.tile * S + w.split) * (size_t)(BM * BN);
+    // 1. this split's partial
+#pragma unroll 1
+    for (int c = 0; c < BN; c += CH) {
+        float v[CH];
+        tmem_load_chunk<CH>(tbase + c, v);
+        if constexpr (SWAP) {
+            if (c < ncols) {
+#pragma unroll
+                for (int j = 0; j < CH; ++j)
+                    mine[(size_t)(c + j) * BM + r] = v[j];
+            }
+        } else {
+            if (r < nrows) {
+#pragma unroll
+                for (int j = 0; j < CH; j += 4)
+                    *reinterpret_cast<float4 *>(mine + (size_t)r * BN + c + j) =
+                        make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+            }
+        }
+    }
+    tc_fence_before();
+    mbar_arrive(smem_u32(tempty_b));
+    named_bar_sync(1, 128);
+    // 2. count in, wait for every split of the tile, pull this CTA's slice of
+    //    every partial into shared memory with bulk copies
+    int *arrive = p.counters + w.tile;
+    int *done = p.counters + p.done_off + w.tile;
+    const bool gated_epi = p.epi == EPI_GATED || p.epi == EPI_GATED_AMAX;
+    const Slice sl = slice_of<BN, SWAP>(w.split, S, ncols, nrows, gated_epi);
+    const int span = sl.hi - sl.lo;
+    if (threadIdx.x == 0) {
+        atomic_add_release_gpu(arrive, 1);
+        bool ok = spin_until_geq(arrive, S, abort_f, p.err);
+        if (ok && span > 0) {
+            fence_proxy_async_global();
+            mbar_arrive_expect_tx(smem_u32(red_bar), (uint32_t)(S * span * 4));
+            for (int k = 0; k < S; ++k)
+                bulk_load(smem_u32(red + (size_t)k * span), tile_ws + (size_t)k * (BM * BN) + sl.lo,
+                          (uint32_t)span * 4u, smem_u32(red_bar));
+            ok = mbar_wait(smem_u32(red_bar), 0, abort_f, p.err);
+        }
+        *s_flag = ok ? 1 : 0;
+    }
+    named_bar_sync(1, 128);
+    if (!*s_flag)
+        return false;
+    // 3. reduce the slice from shared memory, in split order, NB elements
+    //    per thread at a time (residual loads issued first, independent
+    //    accumulations interleaved)
+    constexpr int NB = 8;
+    float amax = 0.0f;
+#pragma unroll 1
+    for (int base = sl.e0 + r; base < sl.e1; base += 128 * NB) {
+        int ia[NB], ib[NB], mm[NB], nn[NB];
+        float acc[NB], acc2[NB], res[NB];
+#pragma unroll
+        for (int i = 0; i < NB; ++i) {
+            const int e = min(base + i * 128, sl.e1 - 1);  // clamped; results of i past the end are dropped
+            if constexpr (SWAP) {
+                const int inner = gated_epi ? BM / 2 : BM;
+                const int col = e / inner, row = e - col * inner;
+                mm[i] = w.tq * BN + col;
+                ia[i] = col * BM + row - sl.lo;
+                ib[i] = ia[i] + BM / 2;
+                nn[i] = gated_epi ? w.tp * (BM / 2) + row : w.tp * BM + row;
+            } else {
+                const int inner = gated_epi ? BN / 2 : BN;
+                const int row = e / inner, col = e - row * inner;
+                mm[i] = w.tp * BM + row;
+                if (gated_epi) {
+                    ia[i] = row * BN + (col >> 6) * 128 + (col & 63) - sl.lo;
+                    ib[i] = ia[i] + 64;
+                    nn[i] = w.tq * (BN / 2) + col;
+                } else {
+                    ia[i] = row * BN + col - sl.lo;
+                    ib[i] = ia[i];
+                    nn[i] = w.tq * BN + col;
+                }
+            }
+            res[i] = 0.0f;
+            if (p.epi == EPI_RESID)
+                res[i] = __uint_as_float(
+                    (uint32_t)static_cast<const uint16_t *>(p.resid)[(size_t)mm[i] * p.ldr + nn[i]] << 16);
+            acc[i] = 0.0f;
+            acc2[i] = 0.0f;
+        }
+#pragma unroll 1
+        for (int k = 0; k < S; ++k) {
+            const float *rk = red + (size_t)k * span;
+#pragma unroll
+            for (int i = 0; i < NB; ++i) {
+                acc[i] = __fadd_rn(acc[i], rk[ia[i]]);
+                if (gated_epi)
+                    acc2[i] = __fadd_rn(acc2[i], rk[ib[i]]);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < NB; ++i) {
+            if (base + i * 128 >= sl.e1)
+                break;
+            const int m = mm[i], n = nn[i];
+            if (gated_epi) {
+                const float gb = round_bf16(__fmul_rn(acc[i], p.alpha));
+                const float ub = round_bf16(__fmul_rn(acc2[i], p.alpha));
+                dbg_store_gu(p, m, n, false, gb);
+                dbg_store_gu(p, m, n, true, ub);
+                const float a = gated(p.act, gb, ub);
+                if (p.epi == EPI_GATED_AMAX)
+                    amax = fmaxf(amax, fabsf(a));
+                else
+                    static_cast<uint8_t *>(p.out)[(size_t)m * p.ldo + n] =
+                        (uint8_t)(e4m3x2(__fmul_rn(a, p.inv_s), 0.0f) & 0xFFu);
+            } else {
+                float f = __fmul_rn(acc[i], p.alpha);
+                if (p.epi == EPI_F32) {
+                    static_cast<float *>(p.out)[(size_t)m * p.ldo + n] = f;
+                } else {
+                    if (p.epi == EPI_RESID)
+                        f = __fadd_rn(res[i], f);
+                    static_cast<uint16_t *>(p.out)[(size_t)m * p.ldo + n] = (uint16_t)bf16_bits(f);
+                }
+            }
+        }
+    }
+    if (p.epi == EPI_GATED_AMAX) {
+        amax = warp_max_f(amax);
+        if ((threadIdx.x & 31) == 0)
+            atomicMax(p.amax, __float_as_uint(amax));
+    }
+    // 4. done reading; the last CTA of the tile resets its counters
+    named_bar_sync(1, 128);
+    if (threadIdx.x == 0) {
+        const int prev = atomic_add_acq_rel_gpu(done, 1);
+        if (prev == S - 1) {
+            *arrive = 0;
+            *done = 0;
+        }
+    }
+    return true;
+}
+
 template <int BN, bool SWAP>
 __device__ void epilogue(const GemmParams &p, uint64_t *tfull, uint64_t *tempty, uint32_t tmem_base,
-                         volatile int *abort_f, volatile int *s_ok, volatile int *s_last, float *xbuf) {
-    using C = Cfg<BN>;
+                         volatile int *abort_f, volatile int *s_ok, volatile int *s_last, float *xbuf,
+                         uint64_t *red_bar, float *red) {
+    using C = Cfg<BN, SWAP>;
     constexpr int CH = C::CH;
     const int warp = threadIdx.x >> 5;
     const int r = threadIdx.x;  // P-tile row = TMEM lane (warps 0..3)
@@ -536,39 +771,8 @@ __device__ void epilogue(const GemmParams &p, uint64_t *tfull, uint64_t *tempty,
             tc_fence_before();
             mbar_arrive(smem_u32(&tempty[abuf]));
         } else {
-            // Split-K: park this split's fp32 partial in the workspace
-            // ([column][row], so a warp's accesses are contiguous); the last
-            // split to arrive on the tile sums all partials in split order.
-            // Columns past the last valid token (weight-streaming path) are
-            // padding and are skipped.
-            const int ncols = SWAP ? min(BN, p.m_tok - w.tq * BN) : BN;
-            float *mine = p.ws + ((size_t)w.tile * p.splits + w.split) * (size_t)(BM * BN);
-#pragma unroll 1
-            for (int c = 0; c < BN; c += CH) {
-                float v[CH];
-                tmem_load_chunk<CH>(tbase + c, v);
-                if (c < ncols) {
-#pragma unroll
-                    for (int j = 0; j < CH; ++j)
-                        mine[(size_t)(c + j) * BM + r] = v[j];
-                }
-            }
-            tc_fence_before();
-            mbar_arrive(smem_u32(&tempty[abuf]));
-            named_bar_sync(1, 128);
-            if (threadIdx.x == 0) {
-                // release: this CTA's partial (ordered before by the barrier);
-                // acquire: every other split's partial, for the last arriver
-                const int prev = atomic_add_acq_rel_gpu(&p.counters[w.tile], 1);
-                s_last[abuf] = (prev == p.splits - 1) ? 1 : 0;
-            }
-            named_bar_sync(1, 128);
-            if (s_last[abuf]) {
-                const float *tile_ws = p.ws + (size_t)w.tile * p.splits * (size_t)(BM * BN);
-                consume_unit<BN, SWAP>(p, w, true, tbase, tile_ws, ncols, xbuf);
-                if (threadIdx.x == 0)
-                    p.counters[w.tile] = 0;  // ready for the next launch
-            }
+            if (!coop_split_unit<BN, SWAP>(p, w, tbase, &tempty[abuf], red_bar, red, abort_f, &s_last[abuf]))
+                break;
         }
         if (++abuf == 2) {
             abuf = 0;
@@ -582,18 +786,20 @@ template <int BN, bool SWAP>
 __global__ void __launch_bounds__(NTHREADS, 1)
     k_gemm_fp8(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmQ,
                const GemmParams p) {
-    using C = Cfg<BN>;
+    using C = Cfg<BN, SWAP>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *sP = smem;
-    uint8_t *sQ = smem + (size_t)C::STAGES * C::P_BYTES;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sQ + (size_t)C::STAGES * C::Q_BYTES);
+    const int NS = p.stages;
+    uint8_t *sQ = smem + (size_t)NS * C::P_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sQ + (size_t)NS * C::Q_BYTES);
     uint64_t *full = bars;
-    uint64_t *empty = bars + C::STAGES;
-    uint64_t *tfull = bars + 2 * C::STAGES;
+    uint64_t *empty = bars + NS;
+    uint64_t *tfull = bars + 2 * NS;
     uint64_t *tempty = tfull + 2;
     uint64_t *drain_bar = tempty + 2;
-    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain_bar + 1);
+    uint64_t *red_bar = drain_bar + 1;   // split-K: slice of every partial landed in shared memory
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(red_bar + 1);
     volatile int *abort_f = reinterpret_cast<volatile int *>(tmem_holder + 1);
     volatile int *s_ok = abort_f + 1;    // [2]
     volatile int *s_last = s_ok + 2;     // [2]
@@ -602,7 +808,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < C::STAGES; ++s) {
+        for (int s = 0; s < NS; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), 1);
         }
@@ -611,6 +817,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mbar_init(smem_u32(&tempty[b]), 128);
         }
         mbar_init(smem_u32(drain_bar), 1);
+        mbar_init(smem_u32(red_bar), 1);
         *abort_f = 0;
         fence_mbar_init();
     }
@@ -629,13 +836,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     pdl_trigger();
 
     if (warp < 4) {
-        epilogue<BN, SWAP>(p, tfull, tempty, tmem_base, abort_f, s_ok, s_last, xbuf);
+        // split-K runs one unit per CTA, so the pipeline stages are free to
+        // receive the partial slices once the last MMA has completed
+        epilogue<BN, SWAP>(p, tfull, tempty, tmem_base, abort_f, s_ok, s_last, xbuf, red_bar,
+                           reinterpret_cast<float *>(smem));
     } else if (warp == 4) {
         if (lane == 0)
             producer<BN, SWAP>(&tmP, &tmQ, p, sP, sQ, full, empty, abort_f);
     } else {
         if (lane == 0)
-            mma_issuer<BN>(p, sP, sQ, full, empty, tfull, tempty, drain_bar, tmem_base, abort_f);
+            mma_issuer<BN, SWAP>(p, sP, sQ, full, empty, tfull, tempty, drain_bar, tmem_base, abort_f);
     }
     tc_fence_before();
     __syncthreads();
@@ -647,18 +857,28 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 }
 
 template <int BN, bool SWAP>
-cudaError_t run(const GemmLaunch &g, cudaStream_t s, bool pdl) {
-    using C = Cfg<BN>;
-    static int attr_done = 0;
-    if (!attr_done) {
+cudaError_t set_attrs() {
+    using C = Cfg<BN, SWAP>;
+    static int done = 0;
+    if (!done) {
         cudaError_t e = cudaFuncSetAttribute(k_gemm_fp8<BN, SWAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)C::SMEM);
         if (e != cudaSuccess)
             return e;
-        attr_done = 1;
+        done = 1;
     }
-    return launch_ex(k_gemm_fp8<BN, SWAP>, dim3((unsigned)g.grid), dim3(NTHREADS), C::SMEM, s, pdl, g.tmP, g.tmQ,
-                     g.p);
+    return cudaSuccess;
+}
+
+template <int BN, bool SWAP>
+cudaError_t run(const GemmLaunch &g, cudaStream_t s, bool pdl) {
+    using C = Cfg<BN, SWAP>;
+    cudaError_t e = set_attrs<BN, SWAP>();
+    if (e != cudaSuccess)
+        return e;
+    const bool xbuf = SWAP && g.p.splits == 1 && (g.p.epi == EPI_GATED || g.p.epi == EPI_GATED_AMAX);
+    return launch_ex(k_gemm_fp8<BN, SWAP>, dim3((unsigned)g.grid), dim3(NTHREADS), C::smem_bytes(g.p.stages, xbuf),
+                     s, pdl, g.tmP, g.tmQ, g.p);
 }
 
 }  // namespace
@@ -697,6 +917,31 @@ cudaError_t encode_tmap_u8(CUtensorMap *m, const void *base, uint64_t rows, uint
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+namespace {
+
+struct StageInfo {
+    size_t stage_bytes, fixed_bytes;
+    int max_stages;
+};
+
+template <int BN, bool SWAP>
+StageInfo stage_info() {
+    using C = Cfg<BN, SWAP>;
+    return {C::STAGE_BYTES, C::smem_bytes(0, SWAP), C::STAGES};
+}
+
+StageInfo stage_info_for(int bn, bool swap) {
+    if (swap)
+        return bn == 16 ? stage_info<16, true>() : (bn == 32 ? stage_info<32, true>() : stage_info<64, true>());
+    return bn == 128 ? stage_info<128, false>() : stage_info<256, false>();
+}
+
+// Shared memory a short launch may use so that CTAs of two consecutive
+// GEMMs fit on one SM (228 KB) and the later one can prefetch its weights.
+constexpr size_t COHABIT_SMEM = 112 * 1024;
+
+}  // namespace
+
 void plan_gemm(GemmLaunch &g, bool swap, int m_tok, int n_feat, int K, int num_sms, int force_splits) {
     GemmParams &p = g.p;
     g.swap = swap;
@@ -716,11 +961,34 @@ void plan_gemm(GemmLaunch &g, bool swap, int m_tok, int n_feat, int K, int num_s
         splits = force_splits;
     else if (tiles < num_sms)
         splits = num_sms / tiles;
-    splits = std::max(1, std::min(splits, p.k_blocks));
+    // cooperative split-K: every split of a tile resident at once, and at
+    // most 16 partials per element
+    splits = std::min(splits, std::max(1, num_sms / tiles));
+    splits = std::max(1, std::min(std::min(splits, 16), p.k_blocks));
     p.kb_per_split = (p.k_blocks + splits - 1) / splits;
     p.splits = (p.k_blocks + p.kb_per_split - 1) / p.kb_per_split;
     p.total_units = tiles * p.splits;
     g.grid = std::min(p.total_units, num_sms);
+    // pipeline depth: short launches keep a small footprint (see COHABIT_SMEM),
+    // long ones take every stage they can
+    const StageInfo si = stage_info_for(g.bn, swap);
+    const int units_per_cta = (p.total_units + g.grid - 1) / g.grid;
+    const int kb_cta = p.kb_per_split * units_per_cta;
+    int cohabit = (int)((COHABIT_SMEM - si.fixed_bytes) / si.stage_bytes);
+    cohabit = std::max(2, std::min(cohabit, si.max_stages));
+    p.stages = kb_cta <= 2 * cohabit ? std::min(cohabit, std::max(2, kb_cta)) : si.max_stages;
+    if (const char *e = getenv("FRT_FFN_STAGES")) {
+        const int v = atoi(e);
+        if (v >= 2)
+            p.stages = std::min(v, si.max_stages);
+    }
+    if (p.splits > 1) {
+        // the stage buffers receive this CTA's slice of all S partials: at most
+        // the whole tile plus one column/row and 16 bytes of padding per split
+        const size_t need = (size_t)BM * g.bn * 4 + (size_t)p.splits * ((size_t)std::max(BM, g.bn) * 4 + 16);
+        while ((size_t)p.stages * si.stage_bytes < need && p.stages < si.max_stages)
+            ++p.stages;
+    }
     p.m_tok = m_tok;
     p.n_feat = n_feat;
 }
