@@ -196,6 +196,34 @@ frt_status frt_fp8_gemm(frt_ffn_plan_t plan, const void *A, const void *B, void 
 /* Message of the last failed call on this host thread ("" if none). */
 const char *frt_ffn_last_error(void);
 
+/*
+ * FP8 GEMM that allocates nothing.  The pages have no counterpart: this entry
+ * point is for callers that cannot call cudaMalloc -- code running while a
+ * CUDA graph is captured in global mode, embedded or real-time hosts that
+ * forbid allocation after start-up, hosts that give all device memory to
+ * their own pool.  It computes what frt_fp8_gemm computes with path 0 and
+ * splits 0, C[m][n] = alpha * sum_k A[m][k] B[n][k] as fp32, with A [M, K],
+ * B [N, K] E4M3 and C [M, N] fp32 (device, 16-byte aligned, K-major), on the
+ * same kernels, but needs no plan: its split-K workspace and counters live in
+ * one fixed array of 5 MiB + 16 KiB in this library's device memory, which
+ * every GPU that loads the library holds until the process exits.
+ *   - The first call on a device looks up that array's device address
+ *     (cudaGetSymbolAddress, once per device, with the device current); make
+ *     that first call before any stream capture.
+ *   - Every call clears the counters on `stream` and then launches; no call
+ *     allocates or frees.  Calls share the array, which keeps the last call's
+ *     contents: calls that overlap on the GPU (different streams, different
+ *     host threads) race and must be ordered by the caller.
+ *   - Shapes whose split-K workspace would exceed the array are rejected
+ *     with FRT_ERR_UNSUPPORTED before anything is launched.
+ * Requires 1 <= M <= 65536, N % 128 == 0, K >= 16, K % 16 == 0.
+ * Errors: INVALID_ARG, UNSUPPORTED, CUDA; the message comes from
+ * frt_fp8_gemm_noalloc_last_error().
+ */
+frt_status frt_fp8_gemm_noalloc(const void *A, const void *B, void *C, int M, int N, int K, float alpha,
+                                frt_stream_t stream);
+const char *frt_fp8_gemm_noalloc_last_error(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -42,6 +42,8 @@ SIGNATURES = {
     "frt_ffn_debug_step": (_I, [_P, _I, _I, _I, _P]),
     "frt_fp8_gemm": (_I, [_P, _P, _P, _P, _I, _I, _I, _F, _I, _I, _P]),
     "frt_ffn_last_error": (ctypes.c_char_p, []),
+    "frt_fp8_gemm_noalloc": (_I, [_P, _P, _P, _I, _I, _I, _F, _P]),
+    "frt_fp8_gemm_noalloc_last_error": (ctypes.c_char_p, []),
 }
 
 
@@ -143,6 +145,14 @@ def frt_ffn_device_status(plan, stream) -> None:
 
 def frt_fp8_gemm(plan, A, B, C, M, N, K, alpha, path, splits, stream) -> None:
     _check(lib().frt_fp8_gemm(plan, A, B, C, M, N, K, alpha, path, splits, stream))
+
+
+def frt_fp8_gemm_noalloc(A, B, C, M, N, K, alpha, stream) -> None:
+    """FP8 GEMM with no plan and no allocation (scratch in a fixed device array)."""
+    st = lib().frt_fp8_gemm_noalloc(A, B, C, M, N, K, alpha, stream)
+    if st != FRT_OK:
+        msg = lib().frt_fp8_gemm_noalloc_last_error()
+        raise FrtError(st, msg.decode() if msg else "")
 
 
 def frt_ffn_last_error() -> str:

@@ -16,7 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfrt_ffn.so")
-SOURCES = ["frt_ffn.cu", "k_elementwise.cu", "k_gemm_fp8.cu"]
+SOURCES = ["frt_ffn.cu", "k_elementwise.cu", "k_gemm_fp8.cu", "frt_noalloc.cu"]
 HEADERS = ["frt_internal.h", "frt_ptx.cuh"]
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
