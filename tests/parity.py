@@ -53,6 +53,21 @@ def check_bf16(got_bits, ref_bits, what=""):
     return c, err
 
 
+def check_rows(got_bits, ref_bits, same_rows, what=""):
+    """Layer outputs: the contract on rows whose q_x codes agree; rows with an
+    allowed one-step q_x flip (a different, equally valid quantisation of
+    that row) are held to the pages' cosine claim, row by row."""
+    if same_rows.any():
+        c, e = check_bf16(got_bits[same_rows], ref_bits[same_rows], what)
+    else:
+        c, e = 1.0, 0.0
+    for i in np.nonzero(~same_rows)[0]:
+        g = oracle.bf16_decode(got_bits[i]).astype(np.float64)
+        r = oracle.bf16_decode(ref_bits[i]).astype(np.float64)
+        assert cosine(g, r) > 0.999, "%s: row %d (q_x flip) cosine %.6f" % (what, i, cosine(g, r))
+    return c, e
+
+
 def bits(t: torch.Tensor) -> np.ndarray:
     return synthetic.bf16_bits(t)
 
