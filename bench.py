@@ -381,10 +381,15 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(synthetic.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="profiling aid: run a plan of this many layers of the workload's shape "
+                         "(the line is then not the workload's bench line)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     wl = synthetic.WORKLOADS[args.config]
+    if args.layers > 0:
+        wl = wl.with_(L=args.layers, name=wl.name + "_%dlayers" % args.layers)
     world, rank, local = dist_setup(args.gpus)
     if args.impl == "reference":
         line = run_reference(args, wl, world, rank)

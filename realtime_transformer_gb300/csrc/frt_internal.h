@@ -26,6 +26,7 @@ enum Epi : int {
 struct GemmParams {
     int p_row0, q_row0;     // row offsets of the P and Q tiles in their tensor maps
     int n_tiles_p, n_tiles_q;
+    int group;              // P-tiles per rasterisation group (see decode)
     int k_blocks;           // ceil(K / 128)
     int splits;             // split-K factor (1 = none)
     int stages;             // shared-memory pipeline stages of this launch

@@ -137,10 +137,11 @@ __global__ void k_quant_gu_interleave(const uint16_t *__restrict__ gate, const u
 
 // ------------------------------------------------------------------- A1 --
 
-// One warp per row.  Pass 1: r' = bf16(r + h) (stored if rprime != null),
-// sum of squares.  Pass 2: y = (r' * inv) * w, then either amax (measure) or
-// q = E4M3(y * inv_s).  d % 8 == 0.
-template <bool MEASURE>
+// WPR warps per row (1, or 8 for few wide rows).  Pass 1: r' = bf16(r + h)
+// (stored if rprime != null), sum of squares (per lane, then a warp-shuffle
+// tree, then the warps of the row in order).  Pass 2: y = (r' * inv) * w,
+// then either amax (measure) or q = E4M3(y * inv_s).  d % 8 == 0.
+template <bool MEASURE, int WPR>
 __global__ void __launch_bounds__(256) k_norm_quant(const uint16_t *__restrict__ r, const uint16_t *__restrict__ h,
                                                     const uint16_t *__restrict__ w, int M, int d, float eps,
                                                     float inv_s, uint16_t *__restrict__ rprime,
@@ -150,40 +151,58 @@ __global__ void __launch_bounds__(256) k_norm_quant(const uint16_t *__restrict__
     // before it can complete, so ordering is preserved.
     pdl_trigger();
     pdl_wait();
+    constexpr int ROWS_PER_CTA = 8 / WPR;
+    __shared__ float s_part[8];
     const int lane = threadIdx.x & 31;
-    const int row = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
-    if (row >= M)
-        return;
+    const int warp = threadIdx.x >> 5;
+    const int sub = warp % WPR;                       // warp index within the row
+    const int tid = sub * 32 + lane;                  // thread index within the row
+    const int row = blockIdx.x * ROWS_PER_CTA + warp / WPR;
+    const bool active = row < M;
     const int nv = d >> 3;
-    const uint4 *rv = reinterpret_cast<const uint4 *>(r + (size_t)row * d);
-    const uint4 *hv = h ? reinterpret_cast<const uint4 *>(h + (size_t)row * d) : nullptr;
-    uint4 *rpv = rprime ? reinterpret_cast<uint4 *>(rprime + (size_t)row * d) : nullptr;
+    const size_t roff = (size_t)(active ? row : 0) * d;
+    const uint4 *rv = reinterpret_cast<const uint4 *>(r + roff);
+    const uint4 *hv = h ? reinterpret_cast<const uint4 *>(h + roff) : nullptr;
+    uint4 *rpv = rprime ? reinterpret_cast<uint4 *>(rprime + roff) : nullptr;
     const uint4 *wv = reinterpret_cast<const uint4 *>(w);
 
     float ss = 0.0f;
-    for (int v = lane; v < nv; v += 32) {
-        float x[8];
-        unpack8(rv[v], x);
-        if (hv) {
-            float hh[8];
-            unpack8(hv[v], hh);
+    if (active) {
+        for (int v = tid; v < nv; v += 32 * WPR) {
+            float x[8];
+            unpack8(rv[v], x);
+            if (hv) {
+                float hh[8];
+                unpack8(hv[v], hh);
+#pragma unroll
+                for (int j = 0; j < 8; j++)
+                    x[j] = __bfloat162float(__float2bfloat16_rn(__fadd_rn(x[j], hh[j])));
+                if (rpv)
+                    rpv[v] = pack8_bf16(x);
+            }
 #pragma unroll
             for (int j = 0; j < 8; j++)
-                x[j] = __bfloat162float(__float2bfloat16_rn(__fadd_rn(x[j], hh[j])));
-            if (rpv)
-                rpv[v] = pack8_bf16(x);
+                ss = __fadd_rn(ss, __fmul_rn(x[j], x[j]));
         }
-#pragma unroll
-        for (int j = 0; j < 8; j++)
-            ss = __fadd_rn(ss, __fmul_rn(x[j], x[j]));
     }
     ss = warp_sum(ss);
+    if (WPR > 1) {
+        if (lane == 0)
+            s_part[warp] = ss;
+        __syncthreads();
+        const int w0 = (warp / WPR) * WPR;
+        ss = 0.0f;
+        for (int k = 0; k < WPR; ++k)
+            ss = __fadd_rn(ss, s_part[w0 + k]);
+    }
+    if (!active)
+        return;
     const float ms = __fdiv_rn(ss, (float)d);
     const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
 
     float amax = 0.0f;
-    uint2 *qv = reinterpret_cast<uint2 *>(qx + (size_t)row * d);
-    for (int v = lane; v < nv; v += 32) {
+    uint2 *qv = reinterpret_cast<uint2 *>(qx + roff);
+    for (int v = tid; v < nv; v += 32 * WPR) {
         float x[8], wf[8];
         unpack8(rv[v], x);
         if (hv) {
@@ -269,15 +288,25 @@ cudaError_t launch_quant_gu_interleave(const void *gate, const void *up, int ff,
 cudaError_t launch_norm_quant(const void *r, const void *h, const void *w, int M, int d, float eps, float inv_s,
                               void *rprime, uint8_t *qx, unsigned *amax_word, bool measure, cudaStream_t s,
                               bool pdl) {
-    const dim3 grid((unsigned)((M + 7) / 8)), block(256);
     auto rr = static_cast<const uint16_t *>(r);
     auto hh = static_cast<const uint16_t *>(h);
     auto ww = static_cast<const uint16_t *>(w);
     auto rp = static_cast<uint16_t *>(rprime);
-    if (measure)
-        return launch_ex(k_norm_quant<true>, grid, block, 0, s, pdl, rr, hh, ww, M, d, eps, inv_s, rp, qx,
+    const dim3 block(256);
+    // few wide rows: a whole CTA per row; otherwise a warp per row
+    if (M <= 256 && d >= 2048) {
+        const dim3 grid((unsigned)M);
+        if (measure)
+            return launch_ex(k_norm_quant<true, 8>, grid, block, 0, s, pdl, rr, hh, ww, M, d, eps, inv_s, rp, qx,
+                             amax_word);
+        return launch_ex(k_norm_quant<false, 8>, grid, block, 0, s, pdl, rr, hh, ww, M, d, eps, inv_s, rp, qx,
                          amax_word);
-    return launch_ex(k_norm_quant<false>, grid, block, 0, s, pdl, rr, hh, ww, M, d, eps, inv_s, rp, qx, amax_word);
+    }
+    const dim3 grid((unsigned)((M + 7) / 8));
+    if (measure)
+        return launch_ex(k_norm_quant<true, 1>, grid, block, 0, s, pdl, rr, hh, ww, M, d, eps, inv_s, rp, qx,
+                         amax_word);
+    return launch_ex(k_norm_quant<false, 1>, grid, block, 0, s, pdl, rr, hh, ww, M, d, eps, inv_s, rp, qx, amax_word);
 }
 
 }  // namespace frt

@@ -78,12 +78,19 @@ struct Unit {
     int tp, tq, kb0, kb1, tile, split;
 };
 
+// Tiles run in groups of p.group P-tiles: within a group the P-tile index
+// changes fastest, so a wave of CTAs covers a block of group x (SMs / group)
+// tiles whose operands stay in L2 together.
 __device__ __forceinline__ Unit decode(const GemmParams &p, int u) {
     Unit w;
     w.split = u % p.splits;
     w.tile = u / p.splits;
-    w.tp = w.tile % p.n_tiles_p;
-    w.tq = w.tile / p.n_tiles_p;
+    const int per_group = p.group * p.n_tiles_q;
+    const int grp = w.tile / per_group;
+    const int rem = w.tile - grp * per_group;
+    const int gsize = min(p.group, p.n_tiles_p - grp * p.group);
+    w.tp = grp * p.group + rem % gsize;
+    w.tq = rem / gsize;
     w.kb0 = w.split * p.kb_per_split;
     w.kb1 = min(p.k_blocks, w.kb0 + p.kb_per_split);
     return w;
@@ -969,6 +976,17 @@ void plan_gemm(GemmLaunch &g, bool swap, int m_tok, int n_feat, int K, int num_s
     p.splits = (p.k_blocks + p.kb_per_split - 1) / p.kb_per_split;
     p.total_units = tiles * p.splits;
     g.grid = std::min(p.total_units, num_sms);
+    // rasterisation: all P-tiles at once if the P operand of a wave fits
+    // comfortably in L2 (for weight streaming P is the weights, each read
+    // once anyway); else groups of P-tiles whose rows take about 32 MB
+    {
+        const size_t p_tile_bytes = (size_t)BM * (size_t)p.k_blocks * BK;
+        const size_t budget = (size_t)32 << 20;
+        int grp = (int)std::max<size_t>(1, budget / p_tile_bytes);
+        if (swap || (size_t)p.n_tiles_p * p_tile_bytes <= ((size_t)48 << 20))
+            grp = p.n_tiles_p;
+        p.group = std::max(1, std::min(grp, p.n_tiles_p));
+    }
     // pipeline depth: short launches keep a small footprint (see COHABIT_SMEM),
     // long ones take every stage they can
     const StageInfo si = stage_info_for(g.bn, swap);
