@@ -205,7 +205,7 @@ const char *frt_ffn_last_error(void);
  * splits 0, C[m][n] = alpha * sum_k A[m][k] B[n][k] as fp32, with A [M, K],
  * B [N, K] E4M3 and C [M, N] fp32 (device, 16-byte aligned, K-major), on the
  * same kernels, but needs no plan: its split-K workspace and counters live in
- * one fixed array of 5 MiB + 16 KiB in this library's device memory, which
+ * one fixed array of 5 MiB + 136 KiB in this library's device memory, which
  * every GPU that loads the library holds until the process exits.
  *   - The first call on a device looks up that array's device address
  *     (cudaGetSymbolAddress, once per device, with the device current); make

@@ -38,7 +38,6 @@ namespace {
 
 constexpr float RMS_EPS = 1e-6f;     // reading: the pages never state the epsilon
 constexpr int SWAP_MAX_TOKENS = 64;  // weight-streaming GEMM path up to this many tokens
-constexpr int COUNTERS_PER_GEMM = 4096;
 constexpr int N_GEMM_SITES = 2;      // gate/up and down keep separate split-K counters
 
 thread_local std::string g_last_error;
@@ -158,11 +157,10 @@ frt_status setup_gemm(frt_ffn_plan *P, GemmLaunch &g, int site, int l, int M) {
         g.p.p_row0 = 0;
         g.p.q_row0 = l * N;
     }
-    if (gemm_ws_floats(g) > P->ws_floats || (g.p.splits > 1 && gemm_tiles(g) > COUNTERS_PER_GEMM / 2))
+    if (gemm_ws_floats(g) > P->ws_floats || (g.p.splits > 1 && gemm_tiles(g) > MAX_SPLIT_TILES))
         return fail(FRT_ERR_UNSUPPORTED, "split-K workspace too small for M=%d site %d", M, site);
     g.p.ws = P->ws;
-    g.p.counters = P->counters + site * COUNTERS_PER_GEMM;
-    g.p.done_off = COUNTERS_PER_GEMM / 2;
+    g.p.counters = split_counters(P->counters + (size_t)site * SPLIT_COUNTERS, g.p.splits);
     g.p.err = P->err;
     return FRT_OK;
 }
@@ -337,7 +335,7 @@ FRT_API frt_status frt_ffn_plan_create(int d, int ff, int act, int M_max, int n_
         {(void **)&P->qx, MA * D},
         {(void **)&P->qh, MA * F},
         {(void **)&P->ws, P->ws_floats * 4},
-        {(void **)&P->counters, (size_t)N_GEMM_SITES * COUNTERS_PER_GEMM * 4},
+        {(void **)&P->counters, (size_t)(N_GEMM_SITES + 1) * SPLIT_COUNTERS * 4},
         {(void **)&P->amax, 2 * 4},
         {(void **)&P->err, 4},
     };
@@ -353,7 +351,7 @@ FRT_API frt_status frt_ffn_plan_create(int d, int ff, int act, int M_max, int n_
     cudaError_t e = cudaSuccess;
     if (e == cudaSuccess) e = cudaMemset(P->qx, 0, MA * D);
     if (e == cudaSuccess) e = cudaMemset(P->qh, 0, MA * F);
-    if (e == cudaSuccess) e = cudaMemset(P->counters, 0, (size_t)N_GEMM_SITES * COUNTERS_PER_GEMM * 4);
+    if (e == cudaSuccess) e = cudaMemset(P->counters, 0, (size_t)(N_GEMM_SITES + 1) * SPLIT_COUNTERS * 4);
     if (e == cudaSuccess) e = cudaMemset(P->err, 0, 4);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
@@ -666,6 +664,8 @@ FRT_API frt_status frt_ffn_device_status(frt_ffn_plan_t P, frt_stream_t stream) 
     int h = 0;
     CK(cudaMemcpy(&h, P->err, 4, cudaMemcpyDeviceToHost));
     if (h) {
+        // a launch that gave up may have left split-K counters mid-generation
+        CK(cudaMemset(P->counters, 0, (size_t)(N_GEMM_SITES + 1) * SPLIT_COUNTERS * 4));
         CK(cudaMemset(P->err, 0, 4));
         CK(cudaDeviceSynchronize());
         return fail(FRT_ERR_DEVICE_TIMEOUT, "a kernel gave up a bounded wait (code %d)", h);
@@ -689,7 +689,7 @@ FRT_API frt_status frt_fp8_gemm(frt_ffn_plan_t P, const void *A, const void *B, 
     GemmLaunch g;
     memset(&g.p, 0, sizeof g.p);
     plan_gemm(g, swap, M, N, K, P->num_sms, splits);
-    if (gemm_ws_floats(g) > P->ws_floats || (g.p.splits > 1 && gemm_tiles(g) > COUNTERS_PER_GEMM / 2))
+    if (gemm_ws_floats(g) > P->ws_floats || (g.p.splits > 1 && gemm_tiles(g) > MAX_SPLIT_TILES))
         return fail(FRT_ERR_UNSUPPORTED, "split-K workspace too small");
     cudaError_t e1, e2;
     if (swap) {
@@ -706,8 +706,7 @@ FRT_API frt_status frt_fp8_gemm(frt_ffn_plan_t P, const void *A, const void *B, 
     g.p.out = C;
     g.p.ldo = N;
     g.p.ws = P->ws;
-    g.p.counters = P->counters;
-    g.p.done_off = COUNTERS_PER_GEMM / 2;
+    g.p.counters = split_counters(P->counters + (size_t)N_GEMM_SITES * SPLIT_COUNTERS, g.p.splits);
     g.p.err = P->err;
     CK(launch_gemm(g, static_cast<cudaStream_t>(stream), false));
     return FRT_OK;

@@ -41,8 +41,7 @@ struct GemmParams {
     int m_tok;              // valid token rows
     int n_feat;             // valid feature columns
     float *ws;              // split-K partials
-    int *counters;          // split-K counters: arrivals at [tile], done-reading at [done_off + tile]
-    int done_off;
+    int *counters;          // split-K arrival counters, one per tile, for this launch's split count
     int *err;               // device error word
     // gated epilogues
     int act;                // Act
@@ -61,6 +60,12 @@ struct GemmLaunch {
 };
 
 // Host side --------------------------------------------------------------
+
+// Split-K arrival counters only grow, so every split count gets its own
+// range of counters (a counter is shared only by launches with the same S).
+constexpr int MAX_SPLIT_TILES = 2048;
+constexpr int SPLIT_COUNTERS = 17 * MAX_SPLIT_TILES;  // ranges for S = 0..16
+inline int *split_counters(int *base, int splits) { return base + (size_t)splits * MAX_SPLIT_TILES; }
 
 // Encode a 2-D E4M3 tensor map: rows x cols bytes, row stride `cols` bytes,
 // box of 128 bytes x box_rows rows, 128-byte swizzle.

@@ -23,10 +23,9 @@ namespace {
 
 // Maximum split-K workspace: 160 partial tiles of 128 x 64 fp32 values
 // (5 MiB), enough for the weight-streaming path on every SM of a GB300, then
-// 2048 arrival and 2048 done-reading counters.
+// the split-K arrival counters (2048 per split count, 136 KiB) and an error word.
 constexpr size_t NOALLOC_WS_FLOATS = (size_t)160 * 128 * 64;
-constexpr int NOALLOC_COUNTERS = 2048;
-constexpr size_t NOALLOC_BYTES = NOALLOC_WS_FLOATS * 4 + (size_t)2 * NOALLOC_COUNTERS * 4 + 4;
+constexpr size_t NOALLOC_BYTES = NOALLOC_WS_FLOATS * 4 + (size_t)frt::SPLIT_COUNTERS * 4 + 4;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_BYTES];
 
@@ -84,18 +83,18 @@ FRT_API frt_status frt_fp8_gemm_noalloc(const void *A, const void *B, void *C, i
     plan_gemm(g, swap, M, N, K, ds.num_sms, 0);
     if (gemm_ws_floats(g) > NOALLOC_WS_FLOATS)
         return fail(FRT_ERR_UNSUPPORTED, "this shape needs more split-K workspace than the fixed 5 MiB scratch");
-    if (g.p.splits > 1 && gemm_tiles(g) > NOALLOC_COUNTERS)
+    if (g.p.splits > 1 && gemm_tiles(g) > MAX_SPLIT_TILES)
         return fail(FRT_ERR_UNSUPPORTED, "this shape has more split-K tiles than the fixed scratch counts");
     if (encode_tmap_u8(&g.tmP, swap ? B : A, swap ? N : M, K, 128) != cudaSuccess ||
         encode_tmap_u8(&g.tmQ, swap ? A : B, swap ? M : N, K, g.bn) != cudaSuccess)
         return fail(FRT_ERR_CUDA, "cuTensorMapEncodeTiled failed");
     float *ws = reinterpret_cast<float *>(ds.base);
     int *counters = reinterpret_cast<int *>(ds.base + NOALLOC_WS_FLOATS * 4);
-    int *err = counters + 2 * NOALLOC_COUNTERS;
+    int *err = counters + SPLIT_COUNTERS;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // The counters must start at zero; a call that gave up a wait could have
     // left some set, so clear them on the stream before every launch.
-    e = cudaMemsetAsync(counters, 0, (size_t)2 * NOALLOC_COUNTERS * 4 + 4, s);
+    e = cudaMemsetAsync(counters, 0, (size_t)SPLIT_COUNTERS * 4 + 4, s);
     if (e != cudaSuccess)
         return fail(FRT_ERR_CUDA, cudaGetErrorString(e));
     g.p.epi = EPI_F32;
@@ -103,8 +102,7 @@ FRT_API frt_status frt_fp8_gemm_noalloc(const void *A, const void *B, void *C, i
     g.p.out = C;
     g.p.ldo = N;
     g.p.ws = ws;
-    g.p.counters = counters;
-    g.p.done_off = NOALLOC_COUNTERS;
+    g.p.counters = split_counters(counters, g.p.splits);
     g.p.err = err;
     e = launch_gemm(g, s, false);
     if (e != cudaSuccess)

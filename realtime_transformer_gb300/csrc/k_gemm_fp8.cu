@@ -536,13 +536,14 @@ __device__ __forceinline__ void consume_unit(const GemmParams &p, const Unit &w,
 // (deterministic) and runs the epilogue for that slice.  All splits of a tile
 // must be resident at once: the planner keeps tiles x splits <= SMs, one unit
 // per CTA, and a dependent kernel only launches once every CTA of this one is
-// resident.  The last CTA to finish reading resets the tile's counters.
+// resident.
 // Partial layout: weight-streaming [column][row] (a warp writes 32
 // consecutive rows), tiled [row][column] (a thread writes its own row).
-__device__ __forceinline__ bool spin_until_geq(const int *addr, int target, volatile int *abort_f, int *err) {
+// Wait until the counter has reached `target` (wrap-around safe).
+__device__ __forceinline__ bool spin_until_geq(const int *addr, unsigned target, volatile int *abort_f, int *err) {
     const uint64_t t0 = globaltimer();
     for (uint32_t i = 0;; ++i) {
-        if (ld_acquire_gpu(addr) >= target)
+        if ((int)((unsigned)ld_acquire_gpu(addr) - target) >= 0)
             return true;
         if ((i & 15u) == 15u) {
             if (*abort_f)
@@ -600,6 +601,108 @@ __device__ __forceinline__ Slice slice_of(int k, int S, int ncols, int nrows, bo
     return sl;
 }
 
+// Element e of a slice -> its offsets in the staged partials (a, and b for
+// the up half when gated) and its output coordinates (token m, feature n).
+template <int BN, bool SWAP, bool GATED>
+__device__ __forceinline__ void elem_map(const Unit &w, const Slice &sl, int e, int &ia, int &ib, int &m, int &n) {
+    if constexpr (SWAP) {
+        constexpr int inner = GATED ? BM / 2 : BM;
+        const int col = e / inner, row = e - col * inner;
+        m = w.tq * BN + col;
+        ia = col * BM + row - sl.lo;
+        ib = ia + BM / 2;
+        n = GATED ? w.tp * (BM / 2) + row : w.tp * BM + row;
+    } else {
+        constexpr int inner = GATED ? BN / 2 : BN;
+        const int row = e / inner, col = e - row * inner;
+        m = w.tp * BM + row;
+        if constexpr (GATED) {
+            ia = row * BN + (col >> 6) * 128 + (col & 63) - sl.lo;
+            ib = ia + 64;
+            n = w.tq * (BN / 2) + col;
+        } else {
+            ia = row * BN + col - sl.lo;
+            ib = ia;
+            n = w.tq * BN + col;
+        }
+    }
+}
+
+constexpr int RED_NB = 8;  // slice elements per thread per batch
+
+// Reduce this CTA's slice over the S staged partials (split order) and run
+// the epilogue, RED_NB elements per thread at a time: index math, the
+// accumulations, then every element's math (independent chains), then the
+// predicated stores.  res0: residuals of the first batch, loaded early.
+template <int BN, bool SWAP, bool GATED>
+__device__ __forceinline__ float reduce_slice(const GemmParams &p, const Unit &w, const Slice &sl, const float *red,
+                                              int span, const float (&res0)[RED_NB]) {
+    constexpr int NB = RED_NB;
+    const int r = threadIdx.x;
+    const int S = p.splits;
+    float amax = 0.0f;
+#pragma unroll 1
+    for (int base = sl.e0 + r; base < sl.e1; base += 128 * NB) {
+        int ia[NB], ib[NB], mm[NB], nn[NB];
+        float acc[NB], acc2[NB], res[NB];
+#pragma unroll
+        for (int i = 0; i < NB; ++i) {
+            elem_map<BN, SWAP, GATED>(w, sl, min(base + i * 128, sl.e1 - 1), ia[i], ib[i], mm[i], nn[i]);
+            res[i] = res0[i];
+            if (!GATED && p.epi == EPI_RESID && base != sl.e0 + r)
+                res[i] = __uint_as_float(
+                    (uint32_t)static_cast<const uint16_t *>(p.resid)[(size_t)mm[i] * p.ldr + nn[i]] << 16);
+            acc[i] = 0.0f;
+            acc2[i] = 0.0f;
+        }
+#pragma unroll 1
+        for (int k = 0; k < S; ++k) {
+            const float *rk = red + (size_t)k * span;
+#pragma unroll
+            for (int i = 0; i < NB; ++i) {
+                acc[i] = __fadd_rn(acc[i], rk[ia[i]]);
+                if (GATED)
+                    acc2[i] = __fadd_rn(acc2[i], rk[ib[i]]);
+            }
+        }
+        float outv[NB];
+#pragma unroll
+        for (int i = 0; i < NB; ++i) {
+            if constexpr (GATED) {
+                const float gb = round_bf16(__fmul_rn(acc[i], p.alpha));
+                const float ub = round_bf16(__fmul_rn(acc2[i], p.alpha));
+                acc[i] = gb;
+                acc2[i] = ub;
+                outv[i] = gated(p.act, gb, ub);
+            } else {
+                const float f = __fmul_rn(acc[i], p.alpha);
+                outv[i] = p.epi == EPI_RESID ? __fadd_rn(res[i], f) : f;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < NB; ++i) {
+            if (base + i * 128 < sl.e1) {
+                const int m = mm[i], n = nn[i];
+                if constexpr (GATED) {
+                    dbg_store_gu(p, m, n, false, acc[i]);
+                    dbg_store_gu(p, m, n, true, acc2[i]);
+                    if (p.epi == EPI_GATED_AMAX)
+                        amax = fmaxf(amax, fabsf(outv[i]));
+                    else
+                        static_cast<uint8_t *>(p.out)[(size_t)m * p.ldo + n] =
+                            (uint8_t)(e4m3x2(__fmul_rn(outv[i], p.inv_s), 0.0f) & 0xFFu);
+                } else {
+                    if (p.epi == EPI_F32)
+                        static_cast<float *>(p.out)[(size_t)m * p.ldo + n] = outv[i];
+                    else
+                        static_cast<uint16_t *>(p.out)[(size_t)m * p.ldo + n] = (uint16_t)bf16_bits(outv[i]);
+                }
+            }
+        }
+    }
+    return amax;
+}
+
 template <int BN, bool SWAP>
 __device__ bool coop_split_unit(const GemmParams &p, const Unit &w, uint32_t tbase, uint64_t *tempty_b,
                                 uint64_t *red_bar, float *red, volatile int *abort_f, volatile int *s_flag) {
@@ -634,15 +737,31 @@ __device__ bool coop_split_unit(const GemmParams &p, const Unit &w, uint32_t tba
     mbar_arrive(smem_u32(tempty_b));
     named_bar_sync(1, 128);
     // 2. count in, wait for every split of the tile, pull this CTA's slice of
-    //    every partial into shared memory with bulk copies
+    //    every partial into shared memory with bulk copies.  The counter only
+    //    grows: the S splits of one launch fetch S consecutive values, which
+    //    name their generation, and wait for the generation's last arrival.
     int *arrive = p.counters + w.tile;
-    int *done = p.counters + p.done_off + w.tile;
     const bool gated_epi = p.epi == EPI_GATED || p.epi == EPI_GATED_AMAX;
     const Slice sl = slice_of<BN, SWAP>(w.split, S, ncols, nrows, gated_epi);
     const int span = sl.hi - sl.lo;
+    // the first batch's residuals do not depend on the other splits: load
+    // them now so their latency hides behind the wait
+    float res0[RED_NB];
+#pragma unroll
+    for (int i = 0; i < RED_NB; ++i)
+        res0[i] = 0.0f;
+    if (p.epi == EPI_RESID && sl.e1 > sl.e0) {
+#pragma unroll
+        for (int i = 0; i < RED_NB; ++i) {
+            int ia, ib, m, n;
+            elem_map<BN, SWAP, false>(w, sl, min(sl.e0 + r + i * 128, sl.e1 - 1), ia, ib, m, n);
+            res0[i] = __uint_as_float((uint32_t)static_cast<const uint16_t *>(p.resid)[(size_t)m * p.ldr + n] << 16);
+        }
+    }
     if (threadIdx.x == 0) {
-        atomic_add_release_gpu(arrive, 1);
-        bool ok = spin_until_geq(arrive, S, abort_f, p.err);
+        const unsigned old = (unsigned)atomic_add_release_gpu(arrive, 1);
+        const unsigned target = (old / (unsigned)S + 1u) * (unsigned)S;
+        bool ok = spin_until_geq(arrive, target, abort_f, p.err);
         if (ok && span > 0) {
             fence_proxy_async_global();
             mbar_arrive_expect_tx(smem_u32(red_bar), (uint32_t)(S * span * 4));
@@ -656,97 +775,13 @@ __device__ bool coop_split_unit(const GemmParams &p, const Unit &w, uint32_t tba
     named_bar_sync(1, 128);
     if (!*s_flag)
         return false;
-    // 3. reduce the slice from shared memory, in split order, NB elements
-    //    per thread at a time (residual loads issued first, independent
-    //    accumulations interleaved)
-    constexpr int NB = 8;
-    float amax = 0.0f;
-#pragma unroll 1
-    for (int base = sl.e0 + r; base < sl.e1; base += 128 * NB) {
-        int ia[NB], ib[NB], mm[NB], nn[NB];
-        float acc[NB], acc2[NB], res[NB];
-#pragma unroll
-        for (int i = 0; i < NB; ++i) {
-            const int e = min(base + i * 128, sl.e1 - 1);  // clamped; results of i past the end are dropped
-            if constexpr (SWAP) {
-                const int inner = gated_epi ? BM / 2 : BM;
-                const int col = e / inner, row = e - col * inner;
-                mm[i] = w.tq * BN + col;
-                ia[i] = col * BM + row - sl.lo;
-                ib[i] = ia[i] + BM / 2;
-                nn[i] = gated_epi ? w.tp * (BM / 2) + row : w.tp * BM + row;
-            } else {
-                const int inner = gated_epi ? BN / 2 : BN;
-                const int row = e / inner, col = e - row * inner;
-                mm[i] = w.tp * BM + row;
-                if (gated_epi) {
-                    ia[i] = row * BN + (col >> 6) * 128 + (col & 63) - sl.lo;
-                    ib[i] = ia[i] + 64;
-                    nn[i] = w.tq * (BN / 2) + col;
-                } else {
-                    ia[i] = row * BN + col - sl.lo;
-                    ib[i] = ia[i];
-                    nn[i] = w.tq * BN + col;
-                }
-            }
-            res[i] = 0.0f;
-            if (p.epi == EPI_RESID)
-                res[i] = __uint_as_float(
-                    (uint32_t)static_cast<const uint16_t *>(p.resid)[(size_t)mm[i] * p.ldr + nn[i]] << 16);
-            acc[i] = 0.0f;
-            acc2[i] = 0.0f;
-        }
-#pragma unroll 1
-        for (int k = 0; k < S; ++k) {
-            const float *rk = red + (size_t)k * span;
-#pragma unroll
-            for (int i = 0; i < NB; ++i) {
-                acc[i] = __fadd_rn(acc[i], rk[ia[i]]);
-                if (gated_epi)
-                    acc2[i] = __fadd_rn(acc2[i], rk[ib[i]]);
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < NB; ++i) {
-            if (base + i * 128 >= sl.e1)
-                break;
-            const int m = mm[i], n = nn[i];
-            if (gated_epi) {
-                const float gb = round_bf16(__fmul_rn(acc[i], p.alpha));
-                const float ub = round_bf16(__fmul_rn(acc2[i], p.alpha));
-                dbg_store_gu(p, m, n, false, gb);
-                dbg_store_gu(p, m, n, true, ub);
-                const float a = gated(p.act, gb, ub);
-                if (p.epi == EPI_GATED_AMAX)
-                    amax = fmaxf(amax, fabsf(a));
-                else
-                    static_cast<uint8_t *>(p.out)[(size_t)m * p.ldo + n] =
-                        (uint8_t)(e4m3x2(__fmul_rn(a, p.inv_s), 0.0f) & 0xFFu);
-            } else {
-                float f = __fmul_rn(acc[i], p.alpha);
-                if (p.epi == EPI_F32) {
-                    static_cast<float *>(p.out)[(size_t)m * p.ldo + n] = f;
-                } else {
-                    if (p.epi == EPI_RESID)
-                        f = __fadd_rn(res[i], f);
-                    static_cast<uint16_t *>(p.out)[(size_t)m * p.ldo + n] = (uint16_t)bf16_bits(f);
-                }
-            }
-        }
-    }
+    // 3. reduce the slice and run the epilogue
+    const float amax = gated_epi ? reduce_slice<BN, SWAP, true>(p, w, sl, red, span, res0)
+                                 : reduce_slice<BN, SWAP, false>(p, w, sl, red, span, res0);
     if (p.epi == EPI_GATED_AMAX) {
-        amax = warp_max_f(amax);
+        const float m = warp_max_f(amax);
         if ((threadIdx.x & 31) == 0)
-            atomicMax(p.amax, __float_as_uint(amax));
-    }
-    // 4. done reading; the last CTA of the tile resets its counters
-    named_bar_sync(1, 128);
-    if (threadIdx.x == 0) {
-        const int prev = atomic_add_acq_rel_gpu(done, 1);
-        if (prev == S - 1) {
-            *arrive = 0;
-            *done = 0;
-        }
+            atomicMax(p.amax, __float_as_uint(m));
     }
     return true;
 }
