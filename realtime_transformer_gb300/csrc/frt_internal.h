@@ -42,6 +42,8 @@ struct GemmParams {
     int n_feat;             // valid feature columns
     float *ws;              // split-K partials
     int *counters;          // split-K arrival counters, one per tile, for this launch's split count
+    int cluster;            // 1: the splits of a tile are one thread-block cluster and exchange
+                            //    partials in distributed shared memory (ws, counters unused)
     int *err;               // device error word
     // gated epilogues
     int act;                // Act
@@ -91,20 +93,31 @@ cudaError_t launch_norm_quant(const void *r, const void *h, const void *w, int M
 namespace frt {
 
 // cudaLaunchKernelEx with an optional programmatic-dependent-launch edge to
-// the previous work on the stream.
+// the previous work on the stream and an optional 1-D cluster shape.
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                             bool pdl, Args &&...args) {
+                             bool pdl, unsigned cluster, Args &&...args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    if (pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (cluster > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = cluster;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
+    cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
 }
 

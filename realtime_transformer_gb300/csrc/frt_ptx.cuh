@@ -51,6 +51,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// Same, but a thread whose phase is still open is suspended (until the phase
+// completes, or at most about a millisecond) instead of returning at once, so
+// waiting warps take no issue slots from the warps they share the SM with.
+constexpr uint32_t WAIT_SUSPEND_NS = 1u << 20;
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "n"(WAIT_SUSPEND_NS)
+        : "memory");
+    return ok != 0;
+}
 
 // Wait with a time bound.  Gives up (returns false) when the CTA's abort flag
 // is set by another thread, or after WAIT_TIMEOUT_NS, in which case it sets
@@ -60,7 +75,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
         return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity))
+        if (mbar_try_wait_sleep(bar, parity))
             return true;
         if ((i & 63u) == 0) {
             if (*abort_flag)
@@ -78,7 +93,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 // after an abort).
 __device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, uint64_t ns) {
     const uint64_t t0 = globaltimer();
-    while (!mbar_try_wait(bar, parity)) {
+    while (!mbar_try_wait_sleep(bar, parity)) {
         if (globaltimer() - t0 > ns)
             return false;
     }
@@ -123,6 +138,75 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
 // later async-proxy (bulk copy) accesses.
 __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+// Order this thread's earlier generic writes to its CTA's shared memory
+// before later async-proxy (bulk copy) reads of it.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ----------------------------------------------------------------- clusters --
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Address, in the cluster's shared window, of the same shared variable in
+// CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+// Arrive on an mbarrier of any CTA of the cluster (address from
+// mapa_shared).  Relaxed: it orders none of this thread's earlier memory
+// accesses, so it does not wait for them to complete.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t bar) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "n"(WAIT_SUSPEND_NS)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait, with acquire at cluster scope, for arrivals and copies that
+// other CTAs of the cluster make on this CTA's mbarrier.
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, volatile int *abort_flag, int *err) {
+    if (mbar_try_wait_cluster(bar, parity))
+        return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait_cluster(bar, parity))
+            return true;
+        if ((i & 63u) == 0) {
+            if (*abort_flag)
+                return false;
+            if (globaltimer() - t0 > WAIT_TIMEOUT_NS) {
+                *abort_flag = 1;
+                atomicExch(err, DEVERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+// Bulk copy from this CTA's shared memory to a CTA of the cluster (dst and
+// bar from mapa_shared); the bytes complete on that CTA's mbarrier.  src,
+// dst 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_copy_to_cta(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst),
+                 "r"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+// Every thread of every CTA of the cluster (all must call it).
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ tcgen05 --

@@ -137,11 +137,17 @@ __global__ void k_quant_gu_interleave(const uint16_t *__restrict__ gate, const u
 
 // ------------------------------------------------------------------- A1 --
 
-// WPR warps per row (1, or 8 for few wide rows).  Pass 1: r' = bf16(r + h)
-// (stored if rprime != null), sum of squares (per lane, then a warp-shuffle
-// tree, then the warps of the row in order).  Pass 2: y = (r' * inv) * w,
-// then either amax (measure) or q = E4M3(y * inv_s).  d % 8 == 0.
-template <bool MEASURE, int WPR>
+// WPR warps per row (1, 2, 4 or 8).  Pass 1: r' = bf16(r + h) (stored if
+// rprime != null), sum of squares (per thread, then a warp-shuffle tree, then
+// the warps of the row in order).  Pass 2: y = (r' * inv) * w, then either
+// amax (measure) or q = E4M3(y * inv_s).  d % 8 == 0.
+//
+// VPT > 0: each thread owns at most VPT 16-byte vectors of its row (the
+// launcher guarantees d / 8 <= 32 * WPR * VPT) and issues every load of r, h
+// and w before the first use, so the row costs one memory round trip; the
+// values stay in registers for pass 2.  VPT == 0: any d, a strided loop that
+// re-reads r (and h) in pass 2.
+template <bool MEASURE, int WPR, int VPT>
 __global__ void __launch_bounds__(256) k_norm_quant(const uint16_t *__restrict__ r, const uint16_t *__restrict__ h,
                                                     const uint16_t *__restrict__ w, int M, int d, float eps,
                                                     float inv_s, uint16_t *__restrict__ rprime,
@@ -150,8 +156,8 @@ __global__ void __launch_bounds__(256) k_norm_quant(const uint16_t *__restrict__
     // waits for this grid, and this grid waits for its own predecessor
     // before it can complete, so ordering is preserved.
     pdl_trigger();
-    pdl_wait();
     constexpr int ROWS_PER_CTA = 8 / WPR;
+    constexpr int STRIDE = 32 * WPR;
     __shared__ float s_part[8];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -165,72 +171,145 @@ __global__ void __launch_bounds__(256) k_norm_quant(const uint16_t *__restrict__
     const uint4 *hv = h ? reinterpret_cast<const uint4 *>(h + roff) : nullptr;
     uint4 *rpv = rprime ? reinterpret_cast<uint4 *>(rprime + roff) : nullptr;
     const uint4 *wv = reinterpret_cast<const uint4 *>(w);
+    uint2 *qv = reinterpret_cast<uint2 *>(qx + roff);
 
     float ss = 0.0f;
-    if (active) {
-        for (int v = tid; v < nv; v += 32 * WPR) {
-            float x[8];
-            unpack8(rv[v], x);
+    float x[VPT > 0 ? VPT : 1][8];
+    if constexpr (VPT > 0) {
+        // the norm weights do not depend on the previous kernel
+        uint4 wraw[VPT];
+#pragma unroll
+        for (int k = 0; k < VPT; ++k)
+            wraw[k] = (tid + k * STRIDE < nv) ? __ldg(wv + tid + k * STRIDE) : make_uint4(0, 0, 0, 0);
+        pdl_wait();
+        uint4 rraw[VPT], hraw[VPT];
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const bool in = active && tid + k * STRIDE < nv;
+            rraw[k] = in ? rv[tid + k * STRIDE] : make_uint4(0, 0, 0, 0);
+            hraw[k] = (in && hv) ? hv[tid + k * STRIDE] : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            unpack8(rraw[k], x[k]);
+            if (hv) {
+                float hh[8];
+                unpack8(hraw[k], hh);
+#pragma unroll
+                for (int j = 0; j < 8; j++)
+                    x[k][j] = __bfloat162float(__float2bfloat16_rn(__fadd_rn(x[k][j], hh[j])));
+                if (rpv && active && tid + k * STRIDE < nv)
+                    rpv[tid + k * STRIDE] = pack8_bf16(x[k]);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; j++)
+                ss = __fadd_rn(ss, __fmul_rn(x[k][j], x[k][j]));
+        }
+        ss = warp_sum(ss);
+        if (WPR > 1) {
+            if (lane == 0)
+                s_part[warp] = ss;
+            __syncthreads();
+            const int w0 = (warp / WPR) * WPR;
+            ss = 0.0f;
+            for (int k = 0; k < WPR; ++k)
+                ss = __fadd_rn(ss, s_part[w0 + k]);
+        }
+        if (!active)
+            return;
+        const float ms = __fdiv_rn(ss, (float)d);
+        const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+        float amax = 0.0f;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            if (tid + k * STRIDE >= nv)
+                break;
+            float wf[8];
+            unpack8(wraw[k], wf);
+#pragma unroll
+            for (int j = 0; j < 8; j++)
+                x[k][j] = __fmul_rn(__fmul_rn(x[k][j], inv), wf[j]);
+            if (MEASURE) {
+#pragma unroll
+                for (int j = 0; j < 8; j++)
+                    amax = fmaxf(amax, fabsf(x[k][j]));
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; j++)
+                    x[k][j] = __fmul_rn(x[k][j], inv_s);
+                qv[tid + k * STRIDE] = pack8_e4m3(x[k]);
+            }
+        }
+        if (MEASURE) {
+            amax = warp_max(amax);
+            if (lane == 0)
+                atomic_amax(amax_word, amax);
+        }
+        return;
+    } else {
+        pdl_wait();
+        if (active) {
+            for (int v = tid; v < nv; v += STRIDE) {
+                unpack8(rv[v], x[0]);
+                if (hv) {
+                    float hh[8];
+                    unpack8(hv[v], hh);
+#pragma unroll
+                    for (int j = 0; j < 8; j++)
+                        x[0][j] = __bfloat162float(__float2bfloat16_rn(__fadd_rn(x[0][j], hh[j])));
+                    if (rpv)
+                        rpv[v] = pack8_bf16(x[0]);
+                }
+#pragma unroll
+                for (int j = 0; j < 8; j++)
+                    ss = __fadd_rn(ss, __fmul_rn(x[0][j], x[0][j]));
+            }
+        }
+        ss = warp_sum(ss);
+        if (WPR > 1) {
+            if (lane == 0)
+                s_part[warp] = ss;
+            __syncthreads();
+            const int w0 = (warp / WPR) * WPR;
+            ss = 0.0f;
+            for (int k = 0; k < WPR; ++k)
+                ss = __fadd_rn(ss, s_part[w0 + k]);
+        }
+        if (!active)
+            return;
+        const float ms = __fdiv_rn(ss, (float)d);
+        const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+        float amax = 0.0f;
+        for (int v = tid; v < nv; v += STRIDE) {
+            float wf[8];
+            unpack8(rv[v], x[0]);
             if (hv) {
                 float hh[8];
                 unpack8(hv[v], hh);
 #pragma unroll
                 for (int j = 0; j < 8; j++)
-                    x[j] = __bfloat162float(__float2bfloat16_rn(__fadd_rn(x[j], hh[j])));
-                if (rpv)
-                    rpv[v] = pack8_bf16(x);
+                    x[0][j] = __bfloat162float(__float2bfloat16_rn(__fadd_rn(x[0][j], hh[j])));
             }
+            unpack8(__ldg(wv + v), wf);
 #pragma unroll
             for (int j = 0; j < 8; j++)
-                ss = __fadd_rn(ss, __fmul_rn(x[j], x[j]));
-        }
-    }
-    ss = warp_sum(ss);
-    if (WPR > 1) {
-        if (lane == 0)
-            s_part[warp] = ss;
-        __syncthreads();
-        const int w0 = (warp / WPR) * WPR;
-        ss = 0.0f;
-        for (int k = 0; k < WPR; ++k)
-            ss = __fadd_rn(ss, s_part[w0 + k]);
-    }
-    if (!active)
-        return;
-    const float ms = __fdiv_rn(ss, (float)d);
-    const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
-
-    float amax = 0.0f;
-    uint2 *qv = reinterpret_cast<uint2 *>(qx + roff);
-    for (int v = tid; v < nv; v += 32 * WPR) {
-        float x[8], wf[8];
-        unpack8(rv[v], x);
-        if (hv) {
-            float hh[8];
-            unpack8(hv[v], hh);
+                x[0][j] = __fmul_rn(__fmul_rn(x[0][j], inv), wf[j]);
+            if (MEASURE) {
 #pragma unroll
-            for (int j = 0; j < 8; j++)
-                x[j] = __bfloat162float(__float2bfloat16_rn(__fadd_rn(x[j], hh[j])));
-        }
-        unpack8(__ldg(wv + v), wf);
+                for (int j = 0; j < 8; j++)
+                    amax = fmaxf(amax, fabsf(x[0][j]));
+            } else {
 #pragma unroll
-        for (int j = 0; j < 8; j++)
-            x[j] = __fmul_rn(__fmul_rn(x[j], inv), wf[j]);
+                for (int j = 0; j < 8; j++)
+                    x[0][j] = __fmul_rn(x[0][j], inv_s);
+                qv[v] = pack8_e4m3(x[0]);
+            }
+        }
         if (MEASURE) {
-#pragma unroll
-            for (int j = 0; j < 8; j++)
-                amax = fmaxf(amax, fabsf(x[j]));
-        } else {
-#pragma unroll
-            for (int j = 0; j < 8; j++)
-                x[j] = __fmul_rn(x[j], inv_s);
-            qv[v] = pack8_e4m3(x);
+            amax = warp_max(amax);
+            if (lane == 0)
+                atomic_amax(amax_word, amax);
         }
-    }
-    if (MEASURE) {
-        amax = warp_max(amax);
-        if (lane == 0)
-            atomic_amax(amax_word, amax);
     }
 }
 
@@ -285,6 +364,48 @@ cudaError_t launch_quant_gu_interleave(const void *gate, const void *up, int ff,
     return cudaGetLastError();
 }
 
+namespace {
+
+template <bool MEASURE, int WPR, int VPT>
+cudaError_t norm_launch(int M, bool pdl, cudaStream_t s, const uint16_t *r, const uint16_t *h, const uint16_t *w,
+                        int d, float eps, float inv_s, uint16_t *rp, uint8_t *qx, unsigned *amax_word) {
+    const dim3 grid((unsigned)((M + 8 / WPR - 1) / (8 / WPR)));
+    return launch_ex(k_norm_quant<MEASURE, WPR, VPT>, grid, dim3(256), 0, s, pdl, 1u, r, h, w, M, d, eps, inv_s, rp, qx,
+                     amax_word);
+}
+
+template <bool MEASURE>
+cudaError_t norm_dispatch(int M, bool pdl, cudaStream_t s, const uint16_t *r, const uint16_t *h, const uint16_t *w,
+                          int d, float eps, float inv_s, uint16_t *rp, uint8_t *qx, unsigned *amax_word) {
+    const int nv = d / 8;
+    // Few rows: spread each row over enough warps that a thread holds one
+    // vector (latency first).  Many rows: a warp per row, up to four vectors
+    // a thread, widening the row only as d requires (throughput first).
+    int wpr = 1;
+    if (M <= 256) {
+        while (wpr < 8 && nv > 32 * wpr)
+            wpr *= 2;
+    } else {
+        while (wpr < 8 && nv > 32 * wpr * 4)
+            wpr *= 2;
+    }
+    const int per = 32 * wpr;
+    const int vpt = (nv + per - 1) / per;
+#define FRT_NORM(W, V) return norm_launch<MEASURE, W, V>(M, pdl, s, r, h, w, d, eps, inv_s, rp, qx, amax_word)
+    if (vpt > 4) {
+        FRT_NORM(8, 0);
+    }
+    switch (wpr) {
+    case 1: if (vpt == 1) FRT_NORM(1, 1); FRT_NORM(1, 4);
+    case 2: if (vpt == 1) FRT_NORM(2, 1); FRT_NORM(2, 4);
+    case 4: if (vpt == 1) FRT_NORM(4, 1); FRT_NORM(4, 4);
+    default: if (vpt == 1) FRT_NORM(8, 1); FRT_NORM(8, 4);
+    }
+#undef FRT_NORM
+}
+
+}  // namespace
+
 cudaError_t launch_norm_quant(const void *r, const void *h, const void *w, int M, int d, float eps, float inv_s,
                               void *rprime, uint8_t *qx, unsigned *amax_word, bool measure, cudaStream_t s,
                               bool pdl) {
@@ -292,21 +413,9 @@ cudaError_t launch_norm_quant(const void *r, const void *h, const void *w, int M
     auto hh = static_cast<const uint16_t *>(h);
     auto ww = static_cast<const uint16_t *>(w);
     auto rp = static_cast<uint16_t *>(rprime);
-    const dim3 block(256);
-    // few wide rows: a whole CTA per row; otherwise a warp per row
-    if (M <= 256 && d >= 2048) {
-        const dim3 grid((unsigned)M);
-        if (measure)
-            return launch_ex(k_norm_quant<true, 8>, grid, block, 0, s, pdl, rr, hh, ww, M, d, eps, inv_s, rp, qx,
-                             amax_word);
-        return launch_ex(k_norm_quant<false, 8>, grid, block, 0, s, pdl, rr, hh, ww, M, d, eps, inv_s, rp, qx,
-                         amax_word);
-    }
-    const dim3 grid((unsigned)((M + 7) / 8));
     if (measure)
-        return launch_ex(k_norm_quant<true, 1>, grid, block, 0, s, pdl, rr, hh, ww, M, d, eps, inv_s, rp, qx,
-                         amax_word);
-    return launch_ex(k_norm_quant<false, 1>, grid, block, 0, s, pdl, rr, hh, ww, M, d, eps, inv_s, rp, qx, amax_word);
+        return norm_dispatch<true>(M, pdl, s, rr, hh, ww, d, eps, inv_s, rp, qx, amax_word);
+    return norm_dispatch<false>(M, pdl, s, rr, hh, ww, d, eps, inv_s, rp, qx, amax_word);
 }
 
 }  // namespace frt

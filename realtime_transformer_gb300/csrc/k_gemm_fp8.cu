@@ -72,6 +72,7 @@ struct Cfg {
     static_assert(Q_BYTES % 1024 == 0, "tiles must stay 1024-byte aligned");
     static_assert(STAGES >= 2, "pipeline needs two stages");
     static_assert(SMEM <= SMEM_LIMIT, "shared memory over the per-CTA limit");
+    static_assert((2 * STAGES + 8) * 8 + 24 <= 256, "mbarriers and flags fit their 256-byte block");
 };
 
 struct Unit {
@@ -374,16 +375,23 @@ __device__ __forceinline__ void store_chunk(const GemmParams &p, const Unit &w, 
 
 __device__ __forceinline__ float round_bf16(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
 
-// GELU, tanh form: 0.5 g (1 + tanh(sqrt(2/pi) (g + 0.044715 g^3))).
+// GELU, tanh form: 0.5 g (1 + tanh(y)), y = sqrt(2/pi) (g + 0.044715 g^3).
+// Because 1 + tanh(y) = 2 / (1 + exp(-2y)), this equals g / (1 + exp(-2y)):
+// one exponential and one division, free of branches and of the
+// cancellation in 1 + tanh(y) for negative y.  __expf and __fdividef are the
+// hardware approximations (a few ulp; the error of __expf grows by about one
+// ulp per unit of its argument); the E4M3 code of the result keeps 3 bits.
+// An overflowing exponential gives g / inf = -0 for very negative g, and an
+// underflowing one gives g.
 __device__ __forceinline__ float gelu_tanh(float g) {
     const float k0 = 0.7978845608028654f;
     const float k1 = 0.044715f;
-    float g3 = __fmul_rn(__fmul_rn(g, g), g);
-    float inner = __fmul_rn(k0, __fadd_rn(g, __fmul_rn(k1, g3)));
-    return __fmul_rn(__fmul_rn(0.5f, g), __fadd_rn(1.0f, tanhf(inner)));
+    const float g3 = __fmul_rn(__fmul_rn(g, g), g);
+    const float y = __fmul_rn(k0, __fadd_rn(g, __fmul_rn(k1, g3)));
+    return __fdividef(g, __fadd_rn(1.0f, __expf(__fmul_rn(-2.0f, y))));
 }
-// SiLU: g / (1 + exp(-g)).
-__device__ __forceinline__ float silu(float g) { return __fdiv_rn(g, __fadd_rn(1.0f, expf(-g))); }
+// SiLU: g / (1 + exp(-g)), with the same approximations.
+__device__ __forceinline__ float silu(float g) { return __fdividef(g, __fadd_rn(1.0f, __expf(-g))); }
 
 __device__ __forceinline__ float gated(int act, float g, float u) {
     return __fmul_rn(act == ACT_SWIGLU ? silu(g) : gelu_tanh(g), u);
@@ -632,28 +640,44 @@ constexpr int RED_NB = 8;  // slice elements per thread per batch
 
 // Reduce this CTA's slice over the S staged partials (split order) and run
 // the epilogue, RED_NB elements per thread at a time: index math, the
-// accumulations, then every element's math (independent chains), then the
-// predicated stores.  res0: residuals of the first batch, loaded early.
+// accumulations, every element's math, then the stores.  Each step is a
+// straight run over the RED_NB elements with the launch-uniform choices
+// (activation, epilogue kind, diagnostics) taken once around it, so the
+// elements' instruction chains interleave.  Elements past the slice end
+// repeat its last element -- the same value to the same address -- so no
+// store needs a predicate.  res0: residuals of the first batch, loaded early.
 template <int BN, bool SWAP, bool GATED>
 __device__ __forceinline__ float reduce_slice(const GemmParams &p, const Unit &w, const Slice &sl, const float *red,
                                               int span, const float (&res0)[RED_NB]) {
     constexpr int NB = RED_NB;
     const int r = threadIdx.x;
     const int S = p.splits;
+    const int epi = p.epi;
+    const float alpha = p.alpha;
     float amax = 0.0f;
+    bool first = true;
 #pragma unroll 1
     for (int base = sl.e0 + r; base < sl.e1; base += 128 * NB) {
         int ia[NB], ib[NB], mm[NB], nn[NB];
-        float acc[NB], acc2[NB], res[NB];
+        float acc[NB], acc2[NB];
 #pragma unroll
         for (int i = 0; i < NB; ++i) {
             elem_map<BN, SWAP, GATED>(w, sl, min(base + i * 128, sl.e1 - 1), ia[i], ib[i], mm[i], nn[i]);
-            res[i] = res0[i];
-            if (!GATED && p.epi == EPI_RESID && base != sl.e0 + r)
-                res[i] = __uint_as_float(
-                    (uint32_t)static_cast<const uint16_t *>(p.resid)[(size_t)mm[i] * p.ldr + nn[i]] << 16);
             acc[i] = 0.0f;
             acc2[i] = 0.0f;
+        }
+        float res[NB];
+        if (!GATED && epi == EPI_RESID) {
+            if (first) {
+#pragma unroll
+                for (int i = 0; i < NB; ++i)
+                    res[i] = res0[i];
+            } else {
+#pragma unroll
+                for (int i = 0; i < NB; ++i)
+                    res[i] = __uint_as_float(
+                        (uint32_t)static_cast<const uint16_t *>(p.resid)[(size_t)mm[i] * p.ldr + nn[i]] << 16);
+            }
         }
 #pragma unroll 1
         for (int k = 0; k < S; ++k) {
@@ -665,40 +689,63 @@ __device__ __forceinline__ float reduce_slice(const GemmParams &p, const Unit &w
                     acc2[i] = __fadd_rn(acc2[i], rk[ib[i]]);
             }
         }
-        float outv[NB];
+        if constexpr (GATED) {
+            float outv[NB];
 #pragma unroll
-        for (int i = 0; i < NB; ++i) {
-            if constexpr (GATED) {
-                const float gb = round_bf16(__fmul_rn(acc[i], p.alpha));
-                const float ub = round_bf16(__fmul_rn(acc2[i], p.alpha));
-                acc[i] = gb;
-                acc2[i] = ub;
-                outv[i] = gated(p.act, gb, ub);
-            } else {
-                const float f = __fmul_rn(acc[i], p.alpha);
-                outv[i] = p.epi == EPI_RESID ? __fadd_rn(res[i], f) : f;
+            for (int i = 0; i < NB; ++i) {
+                acc[i] = round_bf16(__fmul_rn(acc[i], alpha));
+                acc2[i] = round_bf16(__fmul_rn(acc2[i], alpha));
             }
-        }
+            if (p.act == ACT_SWIGLU) {
 #pragma unroll
-        for (int i = 0; i < NB; ++i) {
-            if (base + i * 128 < sl.e1) {
-                const int m = mm[i], n = nn[i];
-                if constexpr (GATED) {
-                    dbg_store_gu(p, m, n, false, acc[i]);
-                    dbg_store_gu(p, m, n, true, acc2[i]);
-                    if (p.epi == EPI_GATED_AMAX)
-                        amax = fmaxf(amax, fabsf(outv[i]));
-                    else
-                        static_cast<uint8_t *>(p.out)[(size_t)m * p.ldo + n] =
-                            (uint8_t)(e4m3x2(__fmul_rn(outv[i], p.inv_s), 0.0f) & 0xFFu);
-                } else {
-                    if (p.epi == EPI_F32)
-                        static_cast<float *>(p.out)[(size_t)m * p.ldo + n] = outv[i];
-                    else
-                        static_cast<uint16_t *>(p.out)[(size_t)m * p.ldo + n] = (uint16_t)bf16_bits(outv[i]);
+                for (int i = 0; i < NB; ++i)
+                    outv[i] = __fmul_rn(silu(acc[i]), acc2[i]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < NB; ++i)
+                    outv[i] = __fmul_rn(gelu_tanh(acc[i]), acc2[i]);
+            }
+            if (p.dbg_gu) {
+#pragma unroll
+                for (int i = 0; i < NB; ++i) {
+                    dbg_store_gu(p, mm[i], nn[i], false, acc[i]);
+                    dbg_store_gu(p, mm[i], nn[i], true, acc2[i]);
                 }
             }
+            if (epi == EPI_GATED_AMAX) {
+#pragma unroll
+                for (int i = 0; i < NB; ++i)
+                    amax = fmaxf(amax, fabsf(outv[i]));
+            } else {
+                uint8_t *out = static_cast<uint8_t *>(p.out);
+                const float inv_s = p.inv_s;
+#pragma unroll
+                for (int i = 0; i < NB; ++i)
+                    out[(size_t)mm[i] * p.ldo + nn[i]] = (uint8_t)(e4m3x2(__fmul_rn(outv[i], inv_s), 0.0f) & 0xFFu);
+            }
+        } else {
+            if (epi == EPI_F32) {
+                float *out = static_cast<float *>(p.out);
+#pragma unroll
+                for (int i = 0; i < NB; ++i)
+                    out[(size_t)mm[i] * p.ldo + nn[i]] = __fmul_rn(acc[i], alpha);
+            } else {
+                uint16_t *out = static_cast<uint16_t *>(p.out);
+                if (epi == EPI_RESID) {
+#pragma unroll
+                    for (int i = 0; i < NB; ++i)
+                        acc[i] = __fadd_rn(res[i], __fmul_rn(acc[i], alpha));
+                } else {
+#pragma unroll
+                    for (int i = 0; i < NB; ++i)
+                        acc[i] = __fmul_rn(acc[i], alpha);
+                }
+#pragma unroll
+                for (int i = 0; i < NB; ++i)
+                    out[(size_t)mm[i] * p.ldo + nn[i]] = (uint16_t)bf16_bits(acc[i]);
+            }
         }
+        first = false;
     }
     return amax;
 }
@@ -713,18 +760,28 @@ __device__ bool coop_split_unit(const GemmParams &p, const Unit &w, uint32_t tba
     const int nrows = SWAP ? BM : min(BM, p.m_tok - w.tp * BM);
     const float *tile_ws = p.ws + (size_t)w.tile * S * (size_t)(BM * BN);
     float *mine = p.ws + ((size_t)w.tile * S + w.split) * (size_t)(BM * BN);
-    // 1. this split's partial
-#pragma unroll 1
-    for (int c = 0; c < BN; c += CH) {
-        float v[CH];
-        tmem_load_chunk<CH>(tbase + c, v);
-        if constexpr (SWAP) {
-            if (c < ncols) {
+    // 1. this split's partial (weight-streaming: every TMEM load in flight at
+    //    once, then the stores)
+    if constexpr (SWAP) {
+        uint32_t v[BN];
+        __syncwarp();
 #pragma unroll
-                for (int j = 0; j < CH; ++j)
-                    mine[(size_t)(c + j) * BM + r] = v[j];
-            }
-        } else {
+        for (int c = 0; c < BN; c += CH) {
+            if constexpr (CH == 16)
+                tmem_ld_x16(tbase + c, *reinterpret_cast<uint32_t(*)[16]>(&v[c]));
+            else
+                tmem_ld_x32(tbase + c, *reinterpret_cast<uint32_t(*)[32]>(&v[c]));
+        }
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < BN; ++c)
+            if (c < ncols)
+                mine[(size_t)c * BM + r] = __uint_as_float(v[c]);
+    } else {
+#pragma unroll 1
+        for (int c = 0; c < BN; c += CH) {
+            float v[CH];
+            tmem_load_chunk<CH>(tbase + c, v);
             if (r < nrows) {
 #pragma unroll
                 for (int j = 0; j < CH; j += 4)
@@ -786,10 +843,112 @@ __device__ bool coop_split_unit(const GemmParams &p, const Unit &w, uint32_t tba
     return true;
 }
 
+// Split-K inside one thread-block cluster (weight-streaming tiles): the S
+// splits of a tile are the S CTAs of a cluster, CTA rank = split.  Each CTA
+// stages its whole partial in its own shared memory and bulk-copies slice j
+// of it into CTA j's shared memory over the cluster's distributed shared
+// memory; CTA j then reduces the S copies of its slice in split order, the
+// same arithmetic as the global-memory path, so results are identical.
+// A CTA's pipeline stages receive the copies, so each CTA first tells the
+// others (remote mbarrier arrivals) that its last MMA has completed.
+template <int BN, bool SWAP>
+__device__ bool coop_cluster_unit(const GemmParams &p, const Unit &w, uint32_t tbase, uint64_t *tempty_b,
+                                  uint64_t *free_bar, uint64_t *data_bar, float *red, float *stg,
+                                  volatile int *abort_f, volatile int *s_flag) {
+    static_assert(SWAP, "cluster split-K stages partials in weight-streaming order");
+    constexpr int CH = Cfg<BN, SWAP>::CH;
+    const int r = threadIdx.x;
+    const int S = p.splits;
+    const int k = w.split;  // == cluster rank
+    const int ncols = min(BN, p.m_tok - w.tq * BN);
+    const bool gated_epi = p.epi == EPI_GATED || p.epi == EPI_GATED_AMAX;
+    const Slice sl = slice_of<BN, SWAP>(k, S, ncols, BM, gated_epi);
+    const int span = sl.hi - sl.lo;
+    // 1. expect this slice from every split; free this CTA's stages for them
+    //    (no ordering needed: the MMAs that read the stages have completed,
+    //    which the wait on the accumulator barrier established)
+    if (threadIdx.x == 0) {
+        mbar_arrive_expect_tx(smem_u32(data_bar), (uint32_t)(S * span * 4));
+        for (int j = 0; j < S; ++j)
+            if (j != k)
+                mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(free_bar), (uint32_t)j));
+    }
+    // residuals of the first batch: independent of the other splits
+    float res0[RED_NB];
+#pragma unroll
+    for (int i = 0; i < RED_NB; ++i)
+        res0[i] = 0.0f;
+    if (p.epi == EPI_RESID && sl.e1 > sl.e0) {
+#pragma unroll
+        for (int i = 0; i < RED_NB; ++i) {
+            int ia, ib, m, n;
+            elem_map<BN, SWAP, false>(w, sl, min(sl.e0 + r + i * 128, sl.e1 - 1), ia, ib, m, n);
+            res0[i] = __uint_as_float((uint32_t)static_cast<const uint16_t *>(p.resid)[(size_t)m * p.ldr + n] << 16);
+        }
+    }
+    // 2. stage the partial in partial-index order (column-major, lane = row):
+    //    every TMEM load in flight at once, then the stores
+    {
+        uint32_t v[BN];
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < BN; c += CH) {
+            if constexpr (CH == 16)
+                tmem_ld_x16(tbase + c, *reinterpret_cast<uint32_t(*)[16]>(&v[c]));
+            else
+                tmem_ld_x32(tbase + c, *reinterpret_cast<uint32_t(*)[32]>(&v[c]));
+        }
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < BN; ++c)
+            if (c < ncols)
+                stg[c * BM + r] = __uint_as_float(v[c]);
+    }
+    fence_proxy_async_shared();
+    tc_fence_before();
+    mbar_arrive(smem_u32(tempty_b));
+    named_bar_sync(1, 128);
+    // 3. once every CTA of the cluster has freed its stages, send slice j of
+    //    this partial to CTA j, into row k of its slice buffer; then wait for
+    //    this CTA's slice from all S splits
+    if (threadIdx.x == 0) {
+        bool ok = mbar_wait_cluster(smem_u32(free_bar), 0, abort_f, p.err);
+        if (ok) {
+            for (int j = 0; j < S; ++j) {
+                const Slice sj = slice_of<BN, SWAP>(j, S, ncols, BM, gated_epi);
+                const int spj = sj.hi - sj.lo;
+                if (spj > 0)
+                    bulk_copy_to_cta(mapa_shared(smem_u32(red + (size_t)k * spj), (uint32_t)j), smem_u32(stg + sj.lo),
+                                     (uint32_t)spj * 4u, mapa_shared(smem_u32(data_bar), (uint32_t)j));
+            }
+            ok = mbar_wait_cluster(smem_u32(data_bar), 0, abort_f, p.err);
+        }
+        *s_flag = ok ? 1 : 0;
+    }
+    named_bar_sync(1, 128);
+    if (!*s_flag)
+        return false;
+    // 4. reduce the slice and run the epilogue
+    const float amax = gated_epi ? reduce_slice<BN, SWAP, true>(p, w, sl, red, span, res0)
+                                 : reduce_slice<BN, SWAP, false>(p, w, sl, red, span, res0);
+    if (p.epi == EPI_GATED_AMAX) {
+        const float m = warp_max_f(amax);
+        if ((threadIdx.x & 31) == 0)
+            atomicMax(p.amax, __float_as_uint(m));
+    }
+    return true;
+}
+
+// Floats of the slice buffer at the start of shared memory: the S slices
+// of a split-K tile, with the per-split rounding slack.
+__host__ __device__ constexpr size_t red_floats(int bn, int splits) {
+    return ((size_t)BM * bn + (size_t)splits * ((BM > bn ? BM : bn) + 4) + 31) & ~(size_t)31;
+}
+
 template <int BN, bool SWAP>
 __device__ void epilogue(const GemmParams &p, uint64_t *tfull, uint64_t *tempty, uint32_t tmem_base,
                          volatile int *abort_f, volatile int *s_ok, volatile int *s_last, float *xbuf,
-                         uint64_t *red_bar, float *red) {
+                         uint64_t *red_bar, uint64_t *free_bar, uint64_t *data_bar, float *red) {
     using C = Cfg<BN, SWAP>;
     constexpr int CH = C::CH;
     const int warp = threadIdx.x >> 5;
@@ -812,6 +971,12 @@ __device__ void epilogue(const GemmParams &p, uint64_t *tfull, uint64_t *tempty,
             consume_unit<BN, SWAP>(p, w, false, tbase, nullptr, BN, xbuf);
             tc_fence_before();
             mbar_arrive(smem_u32(&tempty[abuf]));
+        } else if (SWAP && p.cluster) {
+            if constexpr (SWAP) {
+                if (!coop_cluster_unit<BN, SWAP>(p, w, tbase, &tempty[abuf], free_bar, data_bar, red,
+                                                 red + red_floats(BN, p.splits), abort_f, &s_last[abuf]))
+                    break;
+            }
         } else {
             if (!coop_split_unit<BN, SWAP>(p, w, tbase, &tempty[abuf], red_bar, red, abort_f, &s_last[abuf]))
                 break;
@@ -827,7 +992,7 @@ __device__ void epilogue(const GemmParams &p, uint64_t *tfull, uint64_t *tempty,
 template <int BN, bool SWAP>
 __global__ void __launch_bounds__(NTHREADS, 1)
     k_gemm_fp8(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmQ,
-               const GemmParams p) {
+               const __grid_constant__ GemmParams p) {
     using C = Cfg<BN, SWAP>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -841,7 +1006,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     uint64_t *tempty = tfull + 2;
     uint64_t *drain_bar = tempty + 2;
     uint64_t *red_bar = drain_bar + 1;   // split-K: slice of every partial landed in shared memory
-    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(red_bar + 1);
+    uint64_t *free_bar = red_bar + 1;    // cluster split-K: every other CTA's stages are free
+    uint64_t *data_bar = free_bar + 1;   // cluster split-K: this CTA's slice of every partial landed
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(data_bar + 1);
     volatile int *abort_f = reinterpret_cast<volatile int *>(tmem_holder + 1);
     volatile int *s_ok = abort_f + 1;    // [2]
     volatile int *s_last = s_ok + 2;     // [2]
@@ -860,6 +1027,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         mbar_init(smem_u32(drain_bar), 1);
         mbar_init(smem_u32(red_bar), 1);
+        mbar_init(smem_u32(free_bar), p.cluster ? (uint32_t)(p.splits - 1) : 1u);
+        mbar_init(smem_u32(data_bar), 1);
         *abort_f = 0;
         fence_mbar_init();
     }
@@ -874,13 +1043,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // the other CTAs of the cluster touch this CTA's barriers only after
+    // they have been initialised
+    if (p.cluster)
+        cluster_sync();
     const uint32_t tmem_base = *tmem_holder;
     pdl_trigger();
 
     if (warp < 4) {
         // split-K runs one unit per CTA, so the pipeline stages are free to
         // receive the partial slices once the last MMA has completed
-        epilogue<BN, SWAP>(p, tfull, tempty, tmem_base, abort_f, s_ok, s_last, xbuf, red_bar,
+        epilogue<BN, SWAP>(p, tfull, tempty, tmem_base, abort_f, s_ok, s_last, xbuf, red_bar, free_bar, data_bar,
                            reinterpret_cast<float *>(smem));
     } else if (warp == 4) {
         if (lane == 0)
@@ -892,6 +1065,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // no CTA leaves while another may still copy into its shared memory
+    if (p.cluster)
+        cluster_sync();
     if (warp == 5) {
         __syncwarp();
         tmem_dealloc(tmem_base, C::TMEM_COLS);
@@ -920,7 +1096,7 @@ cudaError_t run(const GemmLaunch &g, cudaStream_t s, bool pdl) {
         return e;
     const bool xbuf = SWAP && g.p.splits == 1 && (g.p.epi == EPI_GATED || g.p.epi == EPI_GATED_AMAX);
     return launch_ex(k_gemm_fp8<BN, SWAP>, dim3((unsigned)g.grid), dim3(NTHREADS), C::smem_bytes(g.p.stages, xbuf),
-                     s, pdl, g.tmP, g.tmQ, g.p);
+                     s, pdl, g.p.cluster ? (unsigned)g.p.splits : 1u, g.tmP, g.tmQ, g.p);
 }
 
 }  // namespace
@@ -1035,19 +1211,31 @@ void plan_gemm(GemmLaunch &g, bool swap, int m_tok, int n_feat, int K, int num_s
         if (v >= 2)
             p.stages = std::min(v, si.max_stages);
     }
+    // cluster split-K (weight-streaming tiles, at most 8 splits: a portable
+    // cluster): the splits exchange partials in distributed shared memory
+    p.cluster = 0;
+    if (swap && p.splits >= 2 && p.splits <= 8) {
+        const char *e = getenv("FRT_FFN_CLUSTER");
+        p.cluster = (e && e[0] == '0') ? 0 : 1;
+    }
+    if (p.cluster)
+        g.grid = p.total_units;
     if (p.splits > 1) {
-        // the stage buffers receive this CTA's slice of all S partials: at most
-        // the whole tile plus one column/row and 16 bytes of padding per split
-        const size_t need = (size_t)BM * g.bn * 4 + (size_t)p.splits * ((size_t)std::max(BM, g.bn) * 4 + 16);
+        // the stage buffers receive this CTA's slice of all S partials (at most
+        // the whole tile plus one column/row and 16 bytes of padding per split)
+        // and, for cluster split-K, stage this CTA's whole partial after them
+        const size_t need = red_floats(g.bn, p.splits) * 4 + (p.cluster ? (size_t)BM * g.bn * 4 : 0);
         while ((size_t)p.stages * si.stage_bytes < need && p.stages < si.max_stages)
             ++p.stages;
+        if ((size_t)p.stages * si.stage_bytes < need)
+            p.cluster = 0, g.grid = std::min(p.total_units, num_sms);
     }
     p.m_tok = m_tok;
     p.n_feat = n_feat;
 }
 
 size_t gemm_ws_floats(const GemmLaunch &g) {
-    if (g.p.splits <= 1)
+    if (g.p.splits <= 1 || g.p.cluster)
         return 0;
     return (size_t)g.p.total_units * BM * (size_t)g.bn;
 }
