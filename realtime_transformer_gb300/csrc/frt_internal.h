@@ -59,6 +59,7 @@ struct GemmLaunch {
     int bn;                 // MMA N (Q tile rows)
     bool swap;
     int grid;
+    size_t min_smem;        // dynamic shared memory floor (see plan_gemm)
 };
 
 // Host side --------------------------------------------------------------

@@ -72,7 +72,7 @@ struct Cfg {
     static_assert(Q_BYTES % 1024 == 0, "tiles must stay 1024-byte aligned");
     static_assert(STAGES >= 2, "pipeline needs two stages");
     static_assert(SMEM <= SMEM_LIMIT, "shared memory over the per-CTA limit");
-    static_assert((2 * STAGES + 8) * 8 + 24 <= 256, "mbarriers and flags fit their 256-byte block");
+    static_assert((2 * STAGES + 9) * 8 + 24 <= 256, "mbarriers and flags fit their 256-byte block");
 };
 
 struct Unit {
@@ -393,8 +393,19 @@ __device__ __forceinline__ float gelu_tanh(float g) {
 // SiLU: g / (1 + exp(-g)), with the same approximations.
 __device__ __forceinline__ float silu(float g) { return __fdividef(g, __fadd_rn(1.0f, __expf(-g))); }
 
-__device__ __forceinline__ float gated(int act, float g, float u) {
-    return __fmul_rn(act == ACT_SWIGLU ? silu(g) : gelu_tanh(g), u);
+// a[j] = act(g[j]) * u[j] over a run of N elements, the activation chosen
+// once for the run so the N chains interleave.
+template <int N>
+__device__ __forceinline__ void gated_run(int act, const float *g, const float *u, float *a) {
+    if (act == ACT_SWIGLU) {
+#pragma unroll
+        for (int j = 0; j < N; ++j)
+            a[j] = __fmul_rn(silu(g[j]), u[j]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < N; ++j)
+            a[j] = __fmul_rn(gelu_tanh(g[j]), u[j]);
+    }
 }
 
 __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
@@ -416,12 +427,17 @@ __device__ __forceinline__ void gated_swap_chunk(const GemmParams &p, const Unit
     {
         const int f = w.tp * (BM / 2) + (r & 63);
         const bool up = r >= 64;
+        float gv[CH];
 #pragma unroll
         for (int j = 0; j < CH; ++j) {
-            const float gv = round_bf16(__fmul_rn(v[j], p.alpha));
-            xbuf[r * (CH + 1) + j] = gv;
-            if (m0 + j < p.m_tok)
-                dbg_store_gu(p, m0 + j, f, up, gv);
+            gv[j] = round_bf16(__fmul_rn(v[j], p.alpha));
+            xbuf[r * (CH + 1) + j] = gv[j];
+        }
+        if (p.dbg_gu) {
+#pragma unroll
+            for (int j = 0; j < CH; ++j)
+                if (m0 + j < p.m_tok)
+                    dbg_store_gu(p, m0 + j, f, up, gv[j]);
         }
     }
     named_bar_sync(1, 128);
@@ -432,19 +448,25 @@ __device__ __forceinline__ void gated_swap_chunk(const GemmParams &p, const Unit
         const int f = w.tp * (BM / 2) + fl;
         const int j0 = (r >> 6) * HALF;
         uint8_t *qh = static_cast<uint8_t *>(p.out);
-        float a[HALF];
-#pragma unroll
-        for (int j = 0; j < HALF; ++j)
-            a[j] = gated(p.act, xbuf[fl * (CH + 1) + j0 + j], xbuf[(fl + 64) * (CH + 1) + j0 + j]);
+        float g[HALF], u[HALF], a[HALF];
 #pragma unroll
         for (int j = 0; j < HALF; ++j) {
-            const int m = m0 + j0 + j;
-            if (m < p.m_tok) {
-                if (p.epi == EPI_GATED_AMAX)
+            g[j] = xbuf[fl * (CH + 1) + j0 + j];
+            u[j] = xbuf[(fl + 64) * (CH + 1) + j0 + j];
+        }
+        gated_run<HALF>(p.act, g, u, a);
+        const int nv = p.m_tok - (m0 + j0);  // valid tokens of this half
+        if (p.epi == EPI_GATED_AMAX) {
+#pragma unroll
+            for (int j = 0; j < HALF; ++j)
+                if (j < nv)
                     amax = fmaxf(amax, fabsf(a[j]));
-                else
-                    qh[(size_t)m * p.ldo + f] = (uint8_t)(e4m3x2(__fmul_rn(a[j], p.inv_s), 0.0f) & 0xFFu);
-            }
+        } else {
+            const float inv_s = p.inv_s;
+#pragma unroll
+            for (int j = 0; j < HALF; ++j)
+                if (j < nv)
+                    qh[(size_t)(m0 + j0 + j) * p.ldo + f] = (uint8_t)(e4m3x2(__fmul_rn(a[j], inv_s), 0.0f) & 0xFFu);
         }
     }
     named_bar_sync(1, 128);
@@ -457,15 +479,20 @@ __device__ __forceinline__ void gated_tiled_chunk(const GemmParams &p, int m, in
                                                   const float (&u)[CH], float &amax) {
     if (m >= p.m_tok)
         return;
-    float a[CH];
+    float gb[CH], ub[CH], a[CH];
 #pragma unroll
     for (int j = 0; j < CH; ++j) {
-        const float gb = round_bf16(__fmul_rn(g[j], p.alpha));
-        const float ub = round_bf16(__fmul_rn(u[j], p.alpha));
-        dbg_store_gu(p, m, f0 + j, false, gb);
-        dbg_store_gu(p, m, f0 + j, true, ub);
-        a[j] = gated(p.act, gb, ub);
+        gb[j] = round_bf16(__fmul_rn(g[j], p.alpha));
+        ub[j] = round_bf16(__fmul_rn(u[j], p.alpha));
     }
+    if (p.dbg_gu) {
+#pragma unroll
+        for (int j = 0; j < CH; ++j) {
+            dbg_store_gu(p, m, f0 + j, false, gb[j]);
+            dbg_store_gu(p, m, f0 + j, true, ub[j]);
+        }
+    }
+    gated_run<CH>(p.act, gb, ub, a);
     if (p.epi == EPI_GATED_AMAX) {
 #pragma unroll
         for (int j = 0; j < CH; ++j)
@@ -696,15 +723,7 @@ __device__ __forceinline__ float reduce_slice(const GemmParams &p, const Unit &w
                 acc[i] = round_bf16(__fmul_rn(acc[i], alpha));
                 acc2[i] = round_bf16(__fmul_rn(acc2[i], alpha));
             }
-            if (p.act == ACT_SWIGLU) {
-#pragma unroll
-                for (int i = 0; i < NB; ++i)
-                    outv[i] = __fmul_rn(silu(acc[i]), acc2[i]);
-            } else {
-#pragma unroll
-                for (int i = 0; i < NB; ++i)
-                    outv[i] = __fmul_rn(gelu_tanh(acc[i]), acc2[i]);
-            }
+            gated_run<NB>(p.act, acc, acc2, outv);
             if (p.dbg_gu) {
 #pragma unroll
                 for (int i = 0; i < NB; ++i) {
@@ -850,10 +869,11 @@ __device__ bool coop_split_unit(const GemmParams &p, const Unit &w, uint32_t tba
 // memory; CTA j then reduces the S copies of its slice in split order, the
 // same arithmetic as the global-memory path, so results are identical.
 // A CTA's pipeline stages receive the copies, so each CTA first tells the
-// others (remote mbarrier arrivals) that its last MMA has completed.
+// others (remote mbarrier arrivals) that its last MMA has completed; and a
+// CTA leaves only once every CTA it copied to has reported the copy landed.
 template <int BN, bool SWAP>
 __device__ bool coop_cluster_unit(const GemmParams &p, const Unit &w, uint32_t tbase, uint64_t *tempty_b,
-                                  uint64_t *free_bar, uint64_t *data_bar, float *red, float *stg,
+                                  uint64_t *free_bar, uint64_t *data_bar, uint64_t *sent_bar, float *red, float *stg,
                                   volatile int *abort_f, volatile int *s_flag) {
     static_assert(SWAP, "cluster split-K stages partials in weight-streaming order");
     constexpr int CH = Cfg<BN, SWAP>::CH;
@@ -923,6 +943,13 @@ __device__ bool coop_cluster_unit(const GemmParams &p, const Unit &w, uint32_t t
             }
             ok = mbar_wait_cluster(smem_u32(data_bar), 0, abort_f, p.err);
         }
+        if (ok) {
+            // every copy into this CTA has landed, so every source may let
+            // its staging go
+            for (int j = 0; j < S; ++j)
+                if (j != k)
+                    mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(sent_bar), (uint32_t)j));
+        }
         *s_flag = ok ? 1 : 0;
     }
     named_bar_sync(1, 128);
@@ -936,7 +963,9 @@ __device__ bool coop_cluster_unit(const GemmParams &p, const Unit &w, uint32_t t
         if ((threadIdx.x & 31) == 0)
             atomicMax(p.amax, __float_as_uint(m));
     }
-    return true;
+    // 5. the CTA may leave once every copy out of its staging has landed
+    //    (normally long done by now)
+    return threadIdx.x != 0 || mbar_wait_cluster(smem_u32(sent_bar), 0, abort_f, p.err);
 }
 
 // Floats of the slice buffer at the start of shared memory: the S slices
@@ -948,7 +977,8 @@ __host__ __device__ constexpr size_t red_floats(int bn, int splits) {
 template <int BN, bool SWAP>
 __device__ void epilogue(const GemmParams &p, uint64_t *tfull, uint64_t *tempty, uint32_t tmem_base,
                          volatile int *abort_f, volatile int *s_ok, volatile int *s_last, float *xbuf,
-                         uint64_t *red_bar, uint64_t *free_bar, uint64_t *data_bar, float *red) {
+                         uint64_t *red_bar, uint64_t *free_bar, uint64_t *data_bar, uint64_t *sent_bar,
+                         float *red) {
     using C = Cfg<BN, SWAP>;
     constexpr int CH = C::CH;
     const int warp = threadIdx.x >> 5;
@@ -973,9 +1003,17 @@ __device__ void epilogue(const GemmParams &p, uint64_t *tfull, uint64_t *tempty,
             mbar_arrive(smem_u32(&tempty[abuf]));
         } else if (SWAP && p.cluster) {
             if constexpr (SWAP) {
-                if (!coop_cluster_unit<BN, SWAP>(p, w, tbase, &tempty[abuf], free_bar, data_bar, red,
-                                                 red + red_floats(BN, p.splits), abort_f, &s_last[abuf]))
+                if (!coop_cluster_unit<BN, SWAP>(p, w, tbase, &tempty[abuf], free_bar, data_bar, sent_bar, red,
+                                                 red + red_floats(BN, p.splits), abort_f, &s_last[abuf])) {
+                    // gave up: other CTAs of the cluster may still be copying
+                    // into or out of this one; wait for them, bounded
+                    if (threadIdx.x == 0) {
+                        mbar_wait_for(smem_u32(free_bar), 0, 500000000ull);
+                        mbar_wait_for(smem_u32(data_bar), 0, 500000000ull);
+                        mbar_wait_for(smem_u32(sent_bar), 0, 500000000ull);
+                    }
                     break;
+                }
             }
         } else {
             if (!coop_split_unit<BN, SWAP>(p, w, tbase, &tempty[abuf], red_bar, red, abort_f, &s_last[abuf]))
@@ -1008,7 +1046,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     uint64_t *red_bar = drain_bar + 1;   // split-K: slice of every partial landed in shared memory
     uint64_t *free_bar = red_bar + 1;    // cluster split-K: every other CTA's stages are free
     uint64_t *data_bar = free_bar + 1;   // cluster split-K: this CTA's slice of every partial landed
-    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(data_bar + 1);
+    uint64_t *sent_bar = data_bar + 1;   // cluster split-K: every copy out of this CTA landed
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(sent_bar + 1);
     volatile int *abort_f = reinterpret_cast<volatile int *>(tmem_holder + 1);
     volatile int *s_ok = abort_f + 1;    // [2]
     volatile int *s_last = s_ok + 2;     // [2]
@@ -1029,6 +1068,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mbar_init(smem_u32(red_bar), 1);
         mbar_init(smem_u32(free_bar), p.cluster ? (uint32_t)(p.splits - 1) : 1u);
         mbar_init(smem_u32(data_bar), 1);
+        mbar_init(smem_u32(sent_bar), p.cluster ? (uint32_t)(p.splits - 1) : 1u);
         *abort_f = 0;
         fence_mbar_init();
     }
@@ -1054,7 +1094,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // split-K runs one unit per CTA, so the pipeline stages are free to
         // receive the partial slices once the last MMA has completed
         epilogue<BN, SWAP>(p, tfull, tempty, tmem_base, abort_f, s_ok, s_last, xbuf, red_bar, free_bar, data_bar,
-                           reinterpret_cast<float *>(smem));
+                           sent_bar, reinterpret_cast<float *>(smem));
     } else if (warp == 4) {
         if (lane == 0)
             producer<BN, SWAP>(&tmP, &tmQ, p, sP, sQ, full, empty, abort_f);
@@ -1065,9 +1105,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // no CTA leaves while another may still copy into its shared memory
-    if (p.cluster)
-        cluster_sync();
     if (warp == 5) {
         __syncwarp();
         tmem_dealloc(tmem_base, C::TMEM_COLS);
@@ -1083,6 +1120,10 @@ cudaError_t set_attrs() {
                                              (int)C::SMEM);
         if (e != cudaSuccess)
             return e;
+        // split-K clusters of up to 16 CTAs
+        e = cudaFuncSetAttribute(k_gemm_fp8<BN, SWAP>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess)
+            return e;
         done = 1;
     }
     return cudaSuccess;
@@ -1095,8 +1136,9 @@ cudaError_t run(const GemmLaunch &g, cudaStream_t s, bool pdl) {
     if (e != cudaSuccess)
         return e;
     const bool xbuf = SWAP && g.p.splits == 1 && (g.p.epi == EPI_GATED || g.p.epi == EPI_GATED_AMAX);
-    return launch_ex(k_gemm_fp8<BN, SWAP>, dim3((unsigned)g.grid), dim3(NTHREADS), C::smem_bytes(g.p.stages, xbuf),
-                     s, pdl, g.p.cluster ? (unsigned)g.p.splits : 1u, g.tmP, g.tmQ, g.p);
+    return launch_ex(k_gemm_fp8<BN, SWAP>, dim3((unsigned)g.grid), dim3(NTHREADS),
+                     std::max(C::smem_bytes(g.p.stages, xbuf), g.min_smem), s, pdl,
+                     g.p.cluster ? (unsigned)g.p.splits : 1u, g.tmP, g.tmQ, g.p);
 }
 
 }  // namespace
@@ -1157,6 +1199,9 @@ StageInfo stage_info_for(int bn, bool swap) {
 // Shared memory a short launch may use so that CTAs of two consecutive
 // GEMMs fit on one SM (228 KB) and the later one can prefetch its weights.
 constexpr size_t COHABIT_SMEM = 112 * 1024;
+// Just over half of an SM's 228 KB of shared memory (less the 1 KB each
+// resident CTA reserves).
+constexpr size_t SPREAD_SMEM = 115 * 1024;
 
 }  // namespace
 
@@ -1164,10 +1209,18 @@ void plan_gemm(GemmLaunch &g, bool swap, int m_tok, int n_feat, int K, int num_s
     GemmParams &p = g.p;
     g.swap = swap;
     p.k_blocks = (K + BK - 1) / BK;
+    const char *pol_env = getenv("FRT_FFN_SPLIT_POLICY");
+    const int policy = pol_env ? atoi(pol_env) : 0;
+    const char *cmax_env = getenv("FRT_FFN_CLUSTER_MAX");
+    const int cluster_max = cmax_env ? std::max(2, std::min(16, atoi(cmax_env))) : 8;
     if (swap) {
         g.bn = m_tok <= 16 ? 16 : (m_tok <= 32 ? 32 : 64);
         p.n_tiles_p = (n_feat + BM - 1) / BM;
         p.n_tiles_q = (m_tok + g.bn - 1) / g.bn;
+        if (policy == 2 && force_splits == 0 && g.bn > 16 && p.n_tiles_p * p.n_tiles_q * cluster_max < num_sms) {
+            g.bn /= 2;
+            p.n_tiles_q = (m_tok + g.bn - 1) / g.bn;
+        }
     } else {
         g.bn = (n_feat % 256 == 0) ? 256 : 128;
         p.n_tiles_p = (m_tok + BM - 1) / BM;
@@ -1183,6 +1236,8 @@ void plan_gemm(GemmLaunch &g, bool swap, int m_tok, int n_feat, int K, int num_s
     // most 16 partials per element
     splits = std::min(splits, std::max(1, num_sms / tiles));
     splits = std::max(1, std::min(std::min(splits, 16), p.k_blocks));
+    if (policy >= 1 && swap && force_splits == 0)
+        splits = std::min(splits, cluster_max);
     p.kb_per_split = (p.k_blocks + splits - 1) / splits;
     p.splits = (p.k_blocks + p.kb_per_split - 1) / p.kb_per_split;
     p.total_units = tiles * p.splits;
@@ -1214,12 +1269,22 @@ void plan_gemm(GemmLaunch &g, bool swap, int m_tok, int n_feat, int K, int num_s
     // cluster split-K (weight-streaming tiles, at most 8 splits: a portable
     // cluster): the splits exchange partials in distributed shared memory
     p.cluster = 0;
-    if (swap && p.splits >= 2 && p.splits <= 8) {
+    if (swap && p.splits >= 2 && p.splits <= cluster_max) {
         const char *e = getenv("FRT_FFN_CLUSTER");
         p.cluster = (e && e[0] == '0') ? 0 : 1;
     }
     if (p.cluster)
         g.grid = p.total_units;
+    // A cluster launch of at most one wave is spread one CTA per SM: more
+    // than half an SM's shared memory keeps two of its CTAs off one SM (the
+    // cluster scheduler would otherwise pack them), while a CTA of another
+    // launch still fits beside it.
+    g.min_smem = 0;
+    if (p.cluster && p.total_units <= num_sms) {
+        const char *e = getenv("FRT_FFN_SPREAD");
+        if (!(e && e[0] == '0'))
+            g.min_smem = SPREAD_SMEM;
+    }
     if (p.splits > 1) {
         // the stage buffers receive this CTA's slice of all S partials (at most
         // the whole tile plus one column/row and 16 bytes of padding per split)
