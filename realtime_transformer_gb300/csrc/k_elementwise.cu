@@ -369,6 +369,17 @@ namespace {
 template <bool MEASURE, int WPR, int VPT>
 cudaError_t norm_launch(int M, bool pdl, cudaStream_t s, const uint16_t *r, const uint16_t *h, const uint16_t *w,
                         int d, float eps, float inv_s, uint16_t *rp, uint8_t *qx, unsigned *amax_word) {
+    // the largest shared-memory carve-out, like the GEMMs, so that GEMM CTAs
+    // can start on an SM while this kernel's CTAs run there
+    static bool attr_set = false;
+    if (!attr_set) {
+        const cudaError_t e = cudaFuncSetAttribute(k_norm_quant<MEASURE, WPR, VPT>,
+                                                   cudaFuncAttributePreferredSharedMemoryCarveout,
+                                                   (int)cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess)
+            return e;
+        attr_set = true;
+    }
     const dim3 grid((unsigned)((M + 8 / WPR - 1) / (8 / WPR)));
     return launch_ex(k_norm_quant<MEASURE, WPR, VPT>, grid, dim3(256), 0, s, pdl, 1u, r, h, w, M, d, eps, inv_s, rp, qx,
                      amax_word);

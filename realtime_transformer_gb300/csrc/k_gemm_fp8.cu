@@ -1120,8 +1120,11 @@ cudaError_t set_attrs() {
                                              (int)C::SMEM);
         if (e != cudaSuccess)
             return e;
-        // split-K clusters of up to 16 CTAs
-        e = cudaFuncSetAttribute(k_gemm_fp8<BN, SWAP>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        // every kernel of the layer asks for the largest shared-memory
+        // carve-out, so an SM never needs to drain before a CTA of the next
+        // kernel (with its own footprint) can start beside the running ones
+        e = cudaFuncSetAttribute(k_gemm_fp8<BN, SWAP>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess)
             return e;
         done = 1;
@@ -1209,18 +1212,17 @@ void plan_gemm(GemmLaunch &g, bool swap, int m_tok, int n_feat, int K, int num_s
     GemmParams &p = g.p;
     g.swap = swap;
     p.k_blocks = (K + BK - 1) / BK;
-    const char *pol_env = getenv("FRT_FFN_SPLIT_POLICY");
-    const int policy = pol_env ? atoi(pol_env) : 0;
-    const char *cmax_env = getenv("FRT_FFN_CLUSTER_MAX");
-    const int cluster_max = cmax_env ? std::max(2, std::min(16, atoi(cmax_env))) : 8;
+    // cluster split-K (weight-streaming tiles): the splits of a tile form one
+    // portable cluster of at most 8 CTAs and exchange partials in
+    // distributed shared memory; FRT_FFN_CLUSTER=0 selects the global-memory
+    // exchange (up to 16 splits) instead
+    const char *cl_env = getenv("FRT_FFN_CLUSTER");
+    const bool cluster_on = swap && !(cl_env && cl_env[0] == '0');
+    constexpr int CLUSTER_MAX = 8;
     if (swap) {
         g.bn = m_tok <= 16 ? 16 : (m_tok <= 32 ? 32 : 64);
         p.n_tiles_p = (n_feat + BM - 1) / BM;
         p.n_tiles_q = (m_tok + g.bn - 1) / g.bn;
-        if (policy == 2 && force_splits == 0 && g.bn > 16 && p.n_tiles_p * p.n_tiles_q * cluster_max < num_sms) {
-            g.bn /= 2;
-            p.n_tiles_q = (m_tok + g.bn - 1) / g.bn;
-        }
     } else {
         g.bn = (n_feat % 256 == 0) ? 256 : 128;
         p.n_tiles_p = (m_tok + BM - 1) / BM;
@@ -1236,8 +1238,8 @@ void plan_gemm(GemmLaunch &g, bool swap, int m_tok, int n_feat, int K, int num_s
     // most 16 partials per element
     splits = std::min(splits, std::max(1, num_sms / tiles));
     splits = std::max(1, std::min(std::min(splits, 16), p.k_blocks));
-    if (policy >= 1 && swap && force_splits == 0)
-        splits = std::min(splits, cluster_max);
+    if (cluster_on && force_splits == 0)
+        splits = std::min(splits, CLUSTER_MAX);
     p.kb_per_split = (p.k_blocks + splits - 1) / splits;
     p.splits = (p.k_blocks + p.kb_per_split - 1) / p.kb_per_split;
     p.total_units = tiles * p.splits;
@@ -1266,13 +1268,7 @@ void plan_gemm(GemmLaunch &g, bool swap, int m_tok, int n_feat, int K, int num_s
         if (v >= 2)
             p.stages = std::min(v, si.max_stages);
     }
-    // cluster split-K (weight-streaming tiles, at most 8 splits: a portable
-    // cluster): the splits exchange partials in distributed shared memory
-    p.cluster = 0;
-    if (swap && p.splits >= 2 && p.splits <= cluster_max) {
-        const char *e = getenv("FRT_FFN_CLUSTER");
-        p.cluster = (e && e[0] == '0') ? 0 : 1;
-    }
+    p.cluster = (cluster_on && p.splits >= 2 && p.splits <= CLUSTER_MAX) ? 1 : 0;
     if (p.cluster)
         g.grid = p.total_units;
     // A cluster launch of at most one wave is spread one CTA per SM: more
