@@ -113,9 +113,12 @@ __device__ void producer(const CUtensorMap *tmP, const CUtensorMap *tmQ, const G
     int stage = 0;
     uint32_t phase = 0;
     bool waited = false;
-    int n_def = 0;
     const int NS = p.stages;
-    int def_stage[C::STAGES], def_kb[C::STAGES], def_row[C::STAGES];
+    // activation loads deferred until the previous grid has completed: a run
+    // of consecutive k-blocks of one unit in consecutive stages (registers,
+    // not an indexed array: local memory would cost a trip to L2 after the
+    // dependency wait)
+    int n_def = 0, def_kb = 0, def_stage = 0, def_row = 0;
     uint32_t issued = 0, issued_par = 0;
     for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
         const Unit w = decode(p, u);
@@ -141,18 +144,23 @@ __device__ void producer(const CUtensorMap *tmP, const CUtensorMap *tmQ, const G
                 if (waited) {
                     tma_load_2d(dX, mX, fb, kb * BK, xrow, pol_x);
                 } else {
-                    def_stage[n_def] = stage;
-                    def_kb[n_def] = kb;
-                    def_row[n_def] = xrow;
+                    if (n_def == 0) {
+                        def_kb = kb;
+                        def_stage = stage;
+                        def_row = xrow;
+                    }
                     ++n_def;
                     if (n_def == NS || kb + 1 == w.kb1) {
                         pdl_wait();
                         waited = true;
+                        int st = def_stage;
                         for (int i = 0; i < n_def; ++i) {
-                            const uint32_t fbi = smem_u32(&full[def_stage[i]]);
-                            const uint32_t dst = SWAP ? smem_u32(sQ + (size_t)def_stage[i] * C::Q_BYTES)
-                                                      : smem_u32(sP + (size_t)def_stage[i] * C::P_BYTES);
-                            tma_load_2d(dst, mX, fbi, def_kb[i] * BK, def_row[i], pol_x);
+                            const uint32_t fbi = smem_u32(&full[st]);
+                            const uint32_t dst = SWAP ? smem_u32(sQ + (size_t)st * C::Q_BYTES)
+                                                      : smem_u32(sP + (size_t)st * C::P_BYTES);
+                            tma_load_2d(dst, mX, fbi, (def_kb + i) * BK, def_row, pol_x);
+                            if (++st == NS)
+                                st = 0;
                         }
                         n_def = 0;
                     }
@@ -238,6 +246,27 @@ __device__ __forceinline__ void tmem_load_chunk(uint32_t taddr, float (&v)[CH]) 
 #pragma unroll
     for (int j = 0; j < CH; ++j)
         v[j] = __uint_as_float(r[j]);
+}
+
+// This thread's row of a weight-streaming accumulator, columns [0, BN),
+// handed to put(c, v) 16 columns at a time; every TMEM load is in flight
+// before the wait.
+template <int BN, typename Put>
+__device__ __forceinline__ void unit_row(uint32_t tbase, Put &&put) {
+    __syncwarp();  // tcgen05.ld is .sync.aligned: the whole warp, converged
+    uint32_t a[BN];
+#pragma unroll
+    for (int c = 0; c < BN; c += 16)
+        tmem_ld_x16(tbase + c, *reinterpret_cast<uint32_t(*)[16]>(&a[c]));
+    tmem_ld_wait();
+#pragma unroll
+    for (int c = 0; c < BN; c += 16) {
+        float v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            v[j] = __uint_as_float(a[c + j]);
+        put(c, v);
+    }
 }
 
 // Accumulator columns c .. c+CH-1 of this thread's row: straight from TMEM,
@@ -782,20 +811,12 @@ __device__ bool coop_split_unit(const GemmParams &p, const Unit &w, uint32_t tba
     // 1. this split's partial (weight-streaming: every TMEM load in flight at
     //    once, then the stores)
     if constexpr (SWAP) {
-        uint32_t v[BN];
-        __syncwarp();
+        unit_row<BN>(tbase, [&](int c, const float (&v)[16]) {
 #pragma unroll
-        for (int c = 0; c < BN; c += CH) {
-            if constexpr (CH == 16)
-                tmem_ld_x16(tbase + c, *reinterpret_cast<uint32_t(*)[16]>(&v[c]));
-            else
-                tmem_ld_x32(tbase + c, *reinterpret_cast<uint32_t(*)[32]>(&v[c]));
-        }
-        tmem_ld_wait();
-#pragma unroll
-        for (int c = 0; c < BN; ++c)
-            if (c < ncols)
-                mine[(size_t)c * BM + r] = __uint_as_float(v[c]);
+            for (int j = 0; j < 16; ++j)
+                if (c + j < ncols)
+                    mine[(size_t)(c + j) * BM + r] = v[j];
+        });
     } else {
 #pragma unroll 1
         for (int c = 0; c < BN; c += CH) {
@@ -876,7 +897,6 @@ __device__ bool coop_cluster_unit(const GemmParams &p, const Unit &w, uint32_t t
                                   uint64_t *free_bar, uint64_t *data_bar, uint64_t *sent_bar, float *red, float *stg,
                                   volatile int *abort_f, volatile int *s_flag) {
     static_assert(SWAP, "cluster split-K stages partials in weight-streaming order");
-    constexpr int CH = Cfg<BN, SWAP>::CH;
     const int r = threadIdx.x;
     const int S = p.splits;
     const int k = w.split;  // == cluster rank
@@ -908,22 +928,12 @@ __device__ bool coop_cluster_unit(const GemmParams &p, const Unit &w, uint32_t t
     }
     // 2. stage the partial in partial-index order (column-major, lane = row):
     //    every TMEM load in flight at once, then the stores
-    {
-        uint32_t v[BN];
-        __syncwarp();
+    unit_row<BN>(tbase, [&](int c, const float (&v)[16]) {
 #pragma unroll
-        for (int c = 0; c < BN; c += CH) {
-            if constexpr (CH == 16)
-                tmem_ld_x16(tbase + c, *reinterpret_cast<uint32_t(*)[16]>(&v[c]));
-            else
-                tmem_ld_x32(tbase + c, *reinterpret_cast<uint32_t(*)[32]>(&v[c]));
-        }
-        tmem_ld_wait();
-#pragma unroll
-        for (int c = 0; c < BN; ++c)
-            if (c < ncols)
-                stg[c * BM + r] = __uint_as_float(v[c]);
-    }
+        for (int j = 0; j < 16; ++j)
+            if (c + j < ncols)
+                stg[(c + j) * BM + r] = v[j];
+    });
     fence_proxy_async_shared();
     tc_fence_before();
     mbar_arrive(smem_u32(tempty_b));
@@ -1269,6 +1279,7 @@ void plan_gemm(GemmLaunch &g, bool swap, int m_tok, int n_feat, int K, int num_s
             p.stages = std::min(v, si.max_stages);
     }
     p.cluster = (cluster_on && p.splits >= 2 && p.splits <= CLUSTER_MAX) ? 1 : 0;
+
     if (p.cluster)
         g.grid = p.total_units;
     // A cluster launch of at most one wave is spread one CTA per SM: more
