@@ -692,105 +692,163 @@ __device__ __forceinline__ void elem_map(const Unit &w, const Slice &sl, int e, 
     }
 }
 
-constexpr int RED_NB = 8;  // slice elements per thread per batch
+constexpr int RED_Q = 2;        // plain epilogues: quads (4 elements) per thread per batch
+constexpr int RED_Q_GATED = 4;  // gated epilogue: a whole gate/up slice in one batch
 
 // Reduce this CTA's slice over the S staged partials (split order) and run
-// the epilogue, RED_NB elements per thread at a time: index math, the
-// accumulations, every element's math, then the stores.  Each step is a
-// straight run over the RED_NB elements with the launch-uniform choices
-// (activation, epilogue kind, diagnostics) taken once around it, so the
-// elements' instruction chains interleave.  Elements past the slice end
-// repeat its last element -- the same value to the same address -- so no
-// store needs a predicate.  res0: residuals of the first batch, loaded early.
+// the epilogue.  A thread takes quads: 4 consecutive elements of one token,
+// i.e. 4 consecutive features, which sit next to each other in the staged
+// partials (one 16-byte shared load per partial) and in the output (one
+// 4-, 8- or 16-byte store).  Each step -- index math, accumulations, every
+// element's math, stores -- is a straight run over the thread's quads with
+// the launch-uniform choices (activation, epilogue kind, diagnostics) taken
+// once around it, so the elements' instruction chains interleave.  Quads
+// past the slice end repeat its last quad -- the same values to the same
+// addresses -- so no store needs a predicate.  Output coordinates are
+// recomputed at the store rather than held.  res0: residuals of the first
+// batch, loaded early.
 template <int BN, bool SWAP, bool GATED>
 __device__ __forceinline__ float reduce_slice(const GemmParams &p, const Unit &w, const Slice &sl, const float *red,
-                                              int span, const float (&res0)[RED_NB]) {
-    constexpr int NB = RED_NB;
+                                              int span, const uint2 (&res0)[RED_Q]) {
+    constexpr int NQ = GATED ? RED_Q_GATED : RED_Q;
+    constexpr int UP = SWAP ? BM / 2 : 64;  // offset of an element's up partner (gated)
     const int r = threadIdx.x;
     const int S = p.splits;
     const int epi = p.epi;
     const float alpha = p.alpha;
+    const int q0 = sl.e0 >> 2, q1 = sl.e1 >> 2;
     float amax = 0.0f;
     bool first = true;
+    auto coords = [&](int base, int i, int &m, int &n) {
+        int ia, ib;
+        elem_map<BN, SWAP, GATED>(w, sl, 4 * min(base + i * 128, q1 - 1), ia, ib, m, n);
+    };
 #pragma unroll 1
-    for (int base = sl.e0 + r; base < sl.e1; base += 128 * NB) {
-        int ia[NB], ib[NB], mm[NB], nn[NB];
-        float acc[NB], acc2[NB];
+    for (int base = q0 + r; base < q1; base += 128 * NQ) {
+        int ia[NQ];
+        float acc[NQ][4], acc2[NQ][4];
 #pragma unroll
-        for (int i = 0; i < NB; ++i) {
-            elem_map<BN, SWAP, GATED>(w, sl, min(base + i * 128, sl.e1 - 1), ia[i], ib[i], mm[i], nn[i]);
-            acc[i] = 0.0f;
-            acc2[i] = 0.0f;
+        for (int i = 0; i < NQ; ++i) {
+            int ib, m, n;
+            elem_map<BN, SWAP, GATED>(w, sl, 4 * min(base + i * 128, q1 - 1), ia[i], ib, m, n);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                acc[i][j] = 0.0f;
+                acc2[i][j] = 0.0f;
+            }
         }
-        float res[NB];
-        if (!GATED && epi == EPI_RESID) {
-            if (first) {
+        uint2 res[NQ];
+        if constexpr (!GATED) {
+            if (epi == EPI_RESID) {
+                if (first) {
 #pragma unroll
-                for (int i = 0; i < NB; ++i)
-                    res[i] = res0[i];
-            } else {
+                    for (int i = 0; i < NQ; ++i)
+                        res[i] = res0[i];
+                } else {
 #pragma unroll
-                for (int i = 0; i < NB; ++i)
-                    res[i] = __uint_as_float(
-                        (uint32_t)static_cast<const uint16_t *>(p.resid)[(size_t)mm[i] * p.ldr + nn[i]] << 16);
+                    for (int i = 0; i < NQ; ++i) {
+                        int m, n;
+                        coords(base, i, m, n);
+                        res[i] = *reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(p.resid) +
+                                                                  (size_t)m * p.ldr + n);
+                    }
+                }
             }
         }
 #pragma unroll 1
         for (int k = 0; k < S; ++k) {
             const float *rk = red + (size_t)k * span;
 #pragma unroll
-            for (int i = 0; i < NB; ++i) {
-                acc[i] = __fadd_rn(acc[i], rk[ia[i]]);
-                if (GATED)
-                    acc2[i] = __fadd_rn(acc2[i], rk[ib[i]]);
+            for (int i = 0; i < NQ; ++i) {
+                const float4 v = *reinterpret_cast<const float4 *>(rk + ia[i]);
+                acc[i][0] = __fadd_rn(acc[i][0], v.x);
+                acc[i][1] = __fadd_rn(acc[i][1], v.y);
+                acc[i][2] = __fadd_rn(acc[i][2], v.z);
+                acc[i][3] = __fadd_rn(acc[i][3], v.w);
+                if (GATED) {
+                    const float4 u = *reinterpret_cast<const float4 *>(rk + ia[i] + UP);
+                    acc2[i][0] = __fadd_rn(acc2[i][0], u.x);
+                    acc2[i][1] = __fadd_rn(acc2[i][1], u.y);
+                    acc2[i][2] = __fadd_rn(acc2[i][2], u.z);
+                    acc2[i][3] = __fadd_rn(acc2[i][3], u.w);
+                }
             }
         }
         if constexpr (GATED) {
-            float outv[NB];
+            float g[4 * NQ], u[4 * NQ], a[4 * NQ];
 #pragma unroll
-            for (int i = 0; i < NB; ++i) {
-                acc[i] = round_bf16(__fmul_rn(acc[i], alpha));
-                acc2[i] = round_bf16(__fmul_rn(acc2[i], alpha));
-            }
-            gated_run<NB>(p.act, acc, acc2, outv);
+            for (int i = 0; i < NQ; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    g[4 * i + j] = round_bf16(__fmul_rn(acc[i][j], alpha));
+                    u[4 * i + j] = round_bf16(__fmul_rn(acc2[i][j], alpha));
+                }
+            gated_run<4 * NQ>(p.act, g, u, a);
             if (p.dbg_gu) {
 #pragma unroll
-                for (int i = 0; i < NB; ++i) {
-                    dbg_store_gu(p, mm[i], nn[i], false, acc[i]);
-                    dbg_store_gu(p, mm[i], nn[i], true, acc2[i]);
+                for (int i = 0; i < NQ; ++i) {
+                    int m, n;
+                    coords(base, i, m, n);
+                    uint16_t *row = p.dbg_gu + (size_t)m * 2 * p.ff + n;
+                    *reinterpret_cast<uint2 *>(row) =
+                        make_uint2(bf16_bits(g[4 * i]) | (bf16_bits(g[4 * i + 1]) << 16),
+                                   bf16_bits(g[4 * i + 2]) | (bf16_bits(g[4 * i + 3]) << 16));
+                    *reinterpret_cast<uint2 *>(row + p.ff) =
+                        make_uint2(bf16_bits(u[4 * i]) | (bf16_bits(u[4 * i + 1]) << 16),
+                                   bf16_bits(u[4 * i + 2]) | (bf16_bits(u[4 * i + 3]) << 16));
                 }
             }
             if (epi == EPI_GATED_AMAX) {
 #pragma unroll
-                for (int i = 0; i < NB; ++i)
-                    amax = fmaxf(amax, fabsf(outv[i]));
+                for (int i = 0; i < 4 * NQ; ++i)
+                    amax = fmaxf(amax, fabsf(a[i]));
             } else {
                 uint8_t *out = static_cast<uint8_t *>(p.out);
                 const float inv_s = p.inv_s;
 #pragma unroll
-                for (int i = 0; i < NB; ++i)
-                    out[(size_t)mm[i] * p.ldo + nn[i]] = (uint8_t)(e4m3x2(__fmul_rn(outv[i], inv_s), 0.0f) & 0xFFu);
+                for (int i = 0; i < NQ; ++i) {
+                    int m, n;
+                    coords(base, i, m, n);
+                    *reinterpret_cast<uint32_t *>(out + (size_t)m * p.ldo + n) =
+                        e4m3x2(__fmul_rn(a[4 * i], inv_s), __fmul_rn(a[4 * i + 1], inv_s)) |
+                        (e4m3x2(__fmul_rn(a[4 * i + 2], inv_s), __fmul_rn(a[4 * i + 3], inv_s)) << 16);
+                }
             }
         } else {
             if (epi == EPI_F32) {
                 float *out = static_cast<float *>(p.out);
 #pragma unroll
-                for (int i = 0; i < NB; ++i)
-                    out[(size_t)mm[i] * p.ldo + nn[i]] = __fmul_rn(acc[i], alpha);
+                for (int i = 0; i < NQ; ++i) {
+                    int m, n;
+                    coords(base, i, m, n);
+                    *reinterpret_cast<float4 *>(out + (size_t)m * p.ldo + n) =
+                        make_float4(__fmul_rn(acc[i][0], alpha), __fmul_rn(acc[i][1], alpha),
+                                    __fmul_rn(acc[i][2], alpha), __fmul_rn(acc[i][3], alpha));
+                }
             } else {
                 uint16_t *out = static_cast<uint16_t *>(p.out);
+#pragma unroll
+                for (int i = 0; i < NQ; ++i)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        acc[i][j] = __fmul_rn(acc[i][j], alpha);
                 if (epi == EPI_RESID) {
 #pragma unroll
-                    for (int i = 0; i < NB; ++i)
-                        acc[i] = __fadd_rn(res[i], __fmul_rn(acc[i], alpha));
-                } else {
-#pragma unroll
-                    for (int i = 0; i < NB; ++i)
-                        acc[i] = __fmul_rn(acc[i], alpha);
+                    for (int i = 0; i < NQ; ++i) {
+                        acc[i][0] = __fadd_rn(bf_lo(res[i].x), acc[i][0]);
+                        acc[i][1] = __fadd_rn(bf_hi(res[i].x), acc[i][1]);
+                        acc[i][2] = __fadd_rn(bf_lo(res[i].y), acc[i][2]);
+                        acc[i][3] = __fadd_rn(bf_hi(res[i].y), acc[i][3]);
+                    }
                 }
 #pragma unroll
-                for (int i = 0; i < NB; ++i)
-                    out[(size_t)mm[i] * p.ldo + nn[i]] = (uint16_t)bf16_bits(acc[i]);
+                for (int i = 0; i < NQ; ++i) {
+                    int m, n;
+                    coords(base, i, m, n);
+                    *reinterpret_cast<uint2 *>(out + (size_t)m * p.ldo + n) =
+                        make_uint2(bf16_bits(acc[i][0]) | (bf16_bits(acc[i][1]) << 16),
+                                   bf16_bits(acc[i][2]) | (bf16_bits(acc[i][3]) << 16));
+                }
             }
         }
         first = false;
@@ -843,16 +901,17 @@ __device__ bool coop_split_unit(const GemmParams &p, const Unit &w, uint32_t tba
     const int span = sl.hi - sl.lo;
     // the first batch's residuals do not depend on the other splits: load
     // them now so their latency hides behind the wait
-    float res0[RED_NB];
+    uint2 res0[RED_Q];
 #pragma unroll
-    for (int i = 0; i < RED_NB; ++i)
-        res0[i] = 0.0f;
+    for (int i = 0; i < RED_Q; ++i)
+        res0[i] = make_uint2(0u, 0u);
     if (p.epi == EPI_RESID && sl.e1 > sl.e0) {
+        const int q0 = sl.e0 >> 2, q1 = sl.e1 >> 2;
 #pragma unroll
-        for (int i = 0; i < RED_NB; ++i) {
+        for (int i = 0; i < RED_Q; ++i) {
             int ia, ib, m, n;
-            elem_map<BN, SWAP, false>(w, sl, min(sl.e0 + r + i * 128, sl.e1 - 1), ia, ib, m, n);
-            res0[i] = __uint_as_float((uint32_t)static_cast<const uint16_t *>(p.resid)[(size_t)m * p.ldr + n] << 16);
+            elem_map<BN, SWAP, false>(w, sl, 4 * min(q0 + r + i * 128, q1 - 1), ia, ib, m, n);
+            res0[i] = *reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(p.resid) + (size_t)m * p.ldr + n);
         }
     }
     if (threadIdx.x == 0) {
@@ -914,16 +973,17 @@ __device__ bool coop_cluster_unit(const GemmParams &p, const Unit &w, uint32_t t
                 mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(free_bar), (uint32_t)j));
     }
     // residuals of the first batch: independent of the other splits
-    float res0[RED_NB];
+    uint2 res0[RED_Q];
 #pragma unroll
-    for (int i = 0; i < RED_NB; ++i)
-        res0[i] = 0.0f;
+    for (int i = 0; i < RED_Q; ++i)
+        res0[i] = make_uint2(0u, 0u);
     if (p.epi == EPI_RESID && sl.e1 > sl.e0) {
+        const int q0 = sl.e0 >> 2, q1 = sl.e1 >> 2;
 #pragma unroll
-        for (int i = 0; i < RED_NB; ++i) {
+        for (int i = 0; i < RED_Q; ++i) {
             int ia, ib, m, n;
-            elem_map<BN, SWAP, false>(w, sl, min(sl.e0 + r + i * 128, sl.e1 - 1), ia, ib, m, n);
-            res0[i] = __uint_as_float((uint32_t)static_cast<const uint16_t *>(p.resid)[(size_t)m * p.ldr + n] << 16);
+            elem_map<BN, SWAP, false>(w, sl, 4 * min(q0 + r + i * 128, q1 - 1), ia, ib, m, n);
+            res0[i] = *reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(p.resid) + (size_t)m * p.ldr + n);
         }
     }
     // 2. stage the partial in partial-index order (column-major, lane = row):
@@ -1038,7 +1098,7 @@ __device__ void epilogue(const GemmParams &p, uint64_t *tfull, uint64_t *tempty,
 
 // -------------------------------------------------------------- kernel --
 template <int BN, bool SWAP>
-__global__ void __launch_bounds__(NTHREADS, 1)
+__global__ void __launch_bounds__(NTHREADS, SWAP ? 2 : 1)
     k_gemm_fp8(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmQ,
                const __grid_constant__ GemmParams p) {
     using C = Cfg<BN, SWAP>;

@@ -78,3 +78,17 @@ def test_split_k_is_deterministic(plan):
     c1 = run(plan, A, B, 1, 8)
     c2 = run(plan, A, B, 1, 8)
     assert np.array_equal(c1, c2)
+
+
+@pytest.mark.parametrize("M,N,K,splits", [(40, 512, 2048, 2), (50, 1024, 4096, 8), (1, 640, 1536, 3), (17, 256, 1024, 5)])
+def test_cluster_and_global_split_k_agree_bitwise(plan, monkeypatch, M, N, K, splits):
+    """The two split-K exchanges (distributed shared memory inside a cluster,
+    or a global workspace) reduce the same partials in the same order."""
+    rng = np.random.default_rng(M + N + K)
+    A = rng.integers(0, 0x7E, (M, K)).astype(np.uint8)
+    B = rng.integers(0, 0x7E, (N, K)).astype(np.uint8)
+    monkeypatch.delenv("FRT_FFN_CLUSTER", raising=False)
+    c_cluster = run(plan, A, B, 1, splits)
+    monkeypatch.setenv("FRT_FFN_CLUSTER", "0")
+    c_global = run(plan, A, B, 1, splits)
+    assert np.array_equal(c_cluster, c_global)
