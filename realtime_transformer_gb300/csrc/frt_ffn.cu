@@ -95,7 +95,12 @@ struct frt_ffn_plan {
     int *counters = nullptr;
     unsigned *amax = nullptr;  // [2]
     int *err = nullptr;
-    std::map<std::pair<int, int>, CUtensorMap> tmaps;
+    // Tensor maps of the plan's buffers, built once at creation; a copy of
+    // each also lives in device memory (tmap_dev), where the GEMM kernels
+    // read it: one fixed address per map stays warm in the TMA unit's
+    // descriptor cache from launch to launch, unlike a kernel parameter.
+    std::map<std::pair<int, int>, std::pair<CUtensorMap, int>> tmaps;
+    CUtensorMap *tmap_dev = nullptr;
     std::map<int, GraphEntry> graphs;
     int force_path = 0;        // 0 auto, 1 swap, 2 tiled (FRT_FFN_FORCE_PATH)
     bool pdl = true;           // programmatic dependent launch (FRT_FFN_NO_PDL=1 disables)
@@ -104,26 +109,46 @@ struct frt_ffn_plan {
 
 namespace {
 
-frt_status get_tmap(frt_ffn_plan *P, int buf, int box_rows, CUtensorMap *out) {
-    auto key = std::make_pair(buf, box_rows);
-    auto it = P->tmaps.find(key);
-    if (it != P->tmaps.end()) {
-        *out = it->second;
-        return FRT_OK;
-    }
-    CUtensorMap m;
-    cudaError_t e;
-    switch (buf) {
-    case B_WGU: e = encode_tmap_u8(&m, P->w_gu, (uint64_t)P->L * 2 * P->ff, P->d, box_rows); break;
-    case B_WDOWN: e = encode_tmap_u8(&m, P->w_down, (uint64_t)P->L * P->d, P->ff, box_rows); break;
-    case B_QX: e = encode_tmap_u8(&m, P->qx, P->M_alloc, P->d, box_rows); break;
-    default: e = encode_tmap_u8(&m, P->qh, P->M_alloc, P->ff, box_rows); break;
-    }
-    if (e != cudaSuccess)
-        return fail(FRT_ERR_CUDA, "cuTensorMapEncodeTiled failed for buffer %d box %d", buf, box_rows);
-    P->tmaps[key] = m;
-    *out = m;
+constexpr int TMAP_SLOTS = 16;
+
+// The map of buffer `buf` with boxes of `box_rows` rows: the host copy (for
+// the kernel parameter) and its device copy.
+frt_status get_tmap(frt_ffn_plan *P, int buf, int box_rows, CUtensorMap *out, const CUtensorMap **dev) {
+    auto it = P->tmaps.find(std::make_pair(buf, box_rows));
+    if (it == P->tmaps.end())
+        return fail(FRT_ERR_UNSUPPORTED, "no tensor map for buffer %d box %d", buf, box_rows);
+    *out = it->second.first;
+    *dev = P->tmap_dev + it->second.second;
     return FRT_OK;
+}
+
+// Every map a launch of this plan can ask for (weights with 128/256-row
+// boxes, activations with the weight-streaming widths and 128), uploaded in
+// one copy.
+frt_status build_tmaps(frt_ffn_plan *P) {
+    const int combos[][2] = {{B_WGU, 128}, {B_WGU, 256}, {B_WDOWN, 128}, {B_WDOWN, 256},
+                             {B_QX, 16},   {B_QX, 32},   {B_QX, 64},     {B_QX, 128},
+                             {B_QH, 16},   {B_QH, 32},   {B_QH, 64},     {B_QH, 128}};
+    CUtensorMap host[TMAP_SLOTS];
+    int n = 0;
+    for (const auto &c : combos) {
+        const int buf = c[0], box_rows = c[1];
+        CUtensorMap m;
+        cudaError_t e;
+        switch (buf) {
+        case B_WGU: e = encode_tmap_u8(&m, P->w_gu, (uint64_t)P->L * 2 * P->ff, P->d, box_rows); break;
+        case B_WDOWN: e = encode_tmap_u8(&m, P->w_down, (uint64_t)P->L * P->d, P->ff, box_rows); break;
+        case B_QX: e = encode_tmap_u8(&m, P->qx, P->M_alloc, P->d, box_rows); break;
+        default: e = encode_tmap_u8(&m, P->qh, P->M_alloc, P->ff, box_rows); break;
+        }
+        if (e != cudaSuccess)
+            return fail(FRT_ERR_CUDA, "cuTensorMapEncodeTiled failed for buffer %d box %d", buf, box_rows);
+        host[n] = m;
+        P->tmaps[std::make_pair(buf, box_rows)] = std::make_pair(m, n);
+        ++n;
+    }
+    const cudaError_t e = cudaMemcpy(P->tmap_dev, host, sizeof(CUtensorMap) * n, cudaMemcpyHostToDevice);
+    return e == cudaSuccess ? FRT_OK : cuda_fail(e, "tensor map upload");
 }
 
 bool use_swap(const frt_ffn_plan *P, int M) {
@@ -147,13 +172,13 @@ frt_status setup_gemm(frt_ffn_plan *P, GemmLaunch &g, int site, int l, int M) {
         plan_gemm(g, swap, M, N, K, P->num_sms, P->max_splits);
     frt_status st;
     if (swap) {
-        if ((st = get_tmap(P, wbuf, 128, &g.tmP)) != FRT_OK) return st;
-        if ((st = get_tmap(P, xbuf, g.bn, &g.tmQ)) != FRT_OK) return st;
+        if ((st = get_tmap(P, wbuf, 128, &g.tmP, &g.p.gtm_p)) != FRT_OK) return st;
+        if ((st = get_tmap(P, xbuf, g.bn, &g.tmQ, &g.p.gtm_q)) != FRT_OK) return st;
         g.p.p_row0 = l * N;
         g.p.q_row0 = 0;
     } else {
-        if ((st = get_tmap(P, xbuf, 128, &g.tmP)) != FRT_OK) return st;
-        if ((st = get_tmap(P, wbuf, g.bn, &g.tmQ)) != FRT_OK) return st;
+        if ((st = get_tmap(P, xbuf, 128, &g.tmP, &g.p.gtm_p)) != FRT_OK) return st;
+        if ((st = get_tmap(P, wbuf, g.bn, &g.tmQ, &g.p.gtm_q)) != FRT_OK) return st;
         g.p.p_row0 = 0;
         g.p.q_row0 = l * N;
     }
@@ -269,8 +294,8 @@ void free_plan(frt_ffn_plan *P) {
         if (kv.second.exec) cudaGraphExecDestroy(kv.second.exec);
         if (kv.second.graph) cudaGraphDestroy(kv.second.graph);
     }
-    void *ptrs[] = {P->w_gu, P->w_down, P->w_norm, P->rbuf[0], P->rbuf[1], P->rprime,
-                    P->qx,   P->qh,     P->ws,     P->counters, P->amax,  P->err};
+    void *ptrs[] = {P->w_gu, P->w_down, P->w_norm, P->rbuf[0], P->rbuf[1], P->rprime, P->qx,
+                    P->qh,   P->ws,     P->counters, P->amax, P->err,     P->tmap_dev};
     for (void *p : ptrs)
         if (p) cudaFree(p);
     delete P;
@@ -338,6 +363,7 @@ FRT_API frt_status frt_ffn_plan_create(int d, int ff, int act, int M_max, int n_
         {(void **)&P->counters, (size_t)(N_GEMM_SITES + 1) * SPLIT_COUNTERS * 4},
         {(void **)&P->amax, 2 * 4},
         {(void **)&P->err, 4},
+        {(void **)&P->tmap_dev, TMAP_SLOTS * sizeof(CUtensorMap)},
     };
     for (auto &a : allocs) {
         cudaError_t e = cudaMalloc(a.p, a.bytes);
@@ -356,6 +382,11 @@ FRT_API frt_status frt_ffn_plan_create(int d, int ff, int act, int M_max, int n_
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
         frt_status st = cuda_fail(e, "plan initialisation");
+        free_plan(P);
+        return st;
+    }
+    const frt_status st = build_tmaps(P);
+    if (st != FRT_OK) {
         free_plan(P);
         return st;
     }

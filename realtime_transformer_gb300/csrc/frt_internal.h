@@ -24,6 +24,7 @@ enum Epi : int {
 // (P = X tiles, Q = W tiles) -- the tiled path -- or (P = W tiles, Q = X tiles)
 // -- the weight-streaming path for few tokens ("swap").
 struct GemmParams {
+    const CUtensorMap *gtm_p, *gtm_q;  // tensor maps in device memory (null: the kernel parameters)
     int p_row0, q_row0;     // row offsets of the P and Q tiles in their tensor maps
     int n_tiles_p, n_tiles_q;
     int group;              // P-tiles per rasterisation group (see decode)

@@ -204,10 +204,13 @@ __device__ __forceinline__ void bulk_copy_to_cta(uint32_t dst, uint32_t src, uin
                  "r"(src), "r"(bytes), "r"(bar)
                  : "memory");
 }
-// Every thread of every CTA of the cluster (all must call it).
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+// The cluster barrier in two halves: every thread of every CTA of the
+// cluster arrives once (release: e.g. its mbarrier initialisation) and
+// waits once (acquire), the wait as late as its first need.
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 
 // ------------------------------------------------------------------ tcgen05 --
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {

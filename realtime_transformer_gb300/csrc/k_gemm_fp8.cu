@@ -1053,6 +1053,8 @@ __device__ void epilogue(const GemmParams &p, uint64_t *tfull, uint64_t *tempty,
     constexpr int CH = C::CH;
     const int warp = threadIdx.x >> 5;
     const int r = threadIdx.x;  // P-tile row = TMEM lane (warps 0..3)
+    if (p.cluster)
+        cluster_wait();
     pdl_wait();
     int abuf = 0;
     uint32_t aphase = 0;
@@ -1142,9 +1144,11 @@ __global__ void __launch_bounds__(NTHREADS, SWAP ? 2 : 1)
         *abort_f = 0;
         fence_mbar_init();
     }
+    const CUtensorMap *mapP = p.gtm_p ? p.gtm_p : &tmP;
+    const CUtensorMap *mapQ = p.gtm_q ? p.gtm_q : &tmQ;
     if (warp == 4 && lane == 0) {
-        prefetch_tmap(&tmP);
-        prefetch_tmap(&tmQ);
+        prefetch_tmap(mapP);
+        prefetch_tmap(mapQ);
     }
     if (warp == 5) {
         tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
@@ -1154,9 +1158,10 @@ __global__ void __launch_bounds__(NTHREADS, SWAP ? 2 : 1)
     __syncthreads();
     tc_fence_after();
     // the other CTAs of the cluster touch this CTA's barriers only after
-    // they have been initialised
+    // they have been initialised: every thread arrives now, and waits before
+    // its first access to another CTA (the epilogue) or at its end
     if (p.cluster)
-        cluster_sync();
+        cluster_arrive();
     const uint32_t tmem_base = *tmem_holder;
     pdl_trigger();
 
@@ -1167,10 +1172,16 @@ __global__ void __launch_bounds__(NTHREADS, SWAP ? 2 : 1)
                            sent_bar, reinterpret_cast<float *>(smem));
     } else if (warp == 4) {
         if (lane == 0)
-            producer<BN, SWAP>(&tmP, &tmQ, p, sP, sQ, full, empty, abort_f);
+            producer<BN, SWAP>(mapP, mapQ, p, sP, sQ, full, empty, abort_f);
+        __syncwarp();
+        if (p.cluster)
+            cluster_wait();
     } else {
         if (lane == 0)
             mma_issuer<BN, SWAP>(p, sP, sQ, full, empty, tfull, tempty, drain_bar, tmem_base, abort_f);
+        __syncwarp();
+        if (p.cluster)
+            cluster_wait();
     }
     tc_fence_before();
     __syncthreads();
