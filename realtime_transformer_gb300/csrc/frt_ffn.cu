@@ -109,7 +109,7 @@ struct frt_ffn_plan {
 
 namespace {
 
-constexpr int TMAP_SLOTS = 16;
+constexpr int TMAP_SLOTS = 24;
 
 // The map of buffer `buf` with boxes of `box_rows` rows: the host copy (for
 // the kernel parameter) and its device copy.
@@ -122,13 +122,14 @@ frt_status get_tmap(frt_ffn_plan *P, int buf, int box_rows, CUtensorMap *out, co
     return FRT_OK;
 }
 
-// Every map a launch of this plan can ask for (weights with 128/256-row
-// boxes, activations with the weight-streaming widths and 128), uploaded in
-// one copy.
+// Every map a launch of this plan can ask for (weights with boxes of a
+// 128/256-row tile or a multicast slice of one, activations with the
+// weight-streaming widths and 128), uploaded in one copy.
 frt_status build_tmaps(frt_ffn_plan *P) {
-    const int combos[][2] = {{B_WGU, 128}, {B_WGU, 256}, {B_WDOWN, 128}, {B_WDOWN, 256},
-                             {B_QX, 16},   {B_QX, 32},   {B_QX, 64},     {B_QX, 128},
-                             {B_QH, 16},   {B_QH, 32},   {B_QH, 64},     {B_QH, 128}};
+    const int combos[][2] = {{B_WGU, 32},   {B_WGU, 64},   {B_WGU, 128}, {B_WGU, 256},
+                             {B_WDOWN, 32}, {B_WDOWN, 64}, {B_WDOWN, 128}, {B_WDOWN, 256},
+                             {B_QX, 16},    {B_QX, 32},    {B_QX, 64},    {B_QX, 128},
+                             {B_QH, 16},    {B_QH, 32},    {B_QH, 64},    {B_QH, 128}};
     CUtensorMap host[TMAP_SLOTS];
     int n = 0;
     for (const auto &c : combos) {
@@ -167,7 +168,11 @@ frt_status setup_gemm(frt_ffn_plan *P, GemmLaunch &g, int site, int l, int M) {
     const int wbuf = site == 0 ? B_WGU : B_WDOWN;
     const int xbuf = site == 0 ? B_QX : B_QH;
     memset(&g.p, 0, sizeof g.p);
-    plan_gemm(g, swap, M, N, K, P->num_sms, 0);
+    // tuning: FRT_FFN_GU_SPLITS / FRT_FFN_DOWN_SPLITS force one site's split-K
+    int force = 0;
+    if (const char *e = getenv(site == 0 ? "FRT_FFN_GU_SPLITS" : "FRT_FFN_DOWN_SPLITS"))
+        force = atoi(e);
+    plan_gemm(g, swap, M, N, K, P->num_sms, force);
     if (P->max_splits > 0 && g.p.splits > P->max_splits)
         plan_gemm(g, swap, M, N, K, P->num_sms, P->max_splits);
     frt_status st;
@@ -178,7 +183,8 @@ frt_status setup_gemm(frt_ffn_plan *P, GemmLaunch &g, int site, int l, int M) {
         g.p.q_row0 = 0;
     } else {
         if ((st = get_tmap(P, xbuf, 128, &g.tmP, &g.p.gtm_p)) != FRT_OK) return st;
-        if ((st = get_tmap(P, wbuf, g.bn, &g.tmQ, &g.p.gtm_q)) != FRT_OK) return st;
+        // with weight multicast each CTA loads BN / mcast rows of the tile
+        if ((st = get_tmap(P, wbuf, g.bn / g.p.mcast, &g.tmQ, &g.p.gtm_q)) != FRT_OK) return st;
         g.p.p_row0 = 0;
         g.p.q_row0 = l * N;
     }
@@ -728,7 +734,7 @@ FRT_API frt_status frt_fp8_gemm(frt_ffn_plan_t P, const void *A, const void *B, 
         e2 = encode_tmap_u8(&g.tmQ, A, M, K, g.bn);
     } else {
         e1 = encode_tmap_u8(&g.tmP, A, M, K, 128);
-        e2 = encode_tmap_u8(&g.tmQ, B, N, K, g.bn);
+        e2 = encode_tmap_u8(&g.tmQ, B, N, K, g.bn / g.p.mcast);  // weight slice per multicasting CTA
     }
     if (e1 != cudaSuccess || e2 != cudaSuccess)
         return fail(FRT_ERR_CUDA, "cuTensorMapEncodeTiled failed");

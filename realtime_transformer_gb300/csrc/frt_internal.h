@@ -43,6 +43,7 @@ struct GemmParams {
     int n_feat;             // valid feature columns
     float *ws;              // split-K partials
     int *counters;          // split-K arrival counters, one per tile, for this launch's split count
+    int mcast;              // tiled role: CTAs per cluster sharing each weight tile by TMA multicast (1 = none)
     int cluster;            // 1: the splits of a tile are one thread-block cluster and exchange
                             //    partials in distributed shared memory (ws, counters unused)
     int *err;               // device error word

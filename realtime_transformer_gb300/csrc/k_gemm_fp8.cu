@@ -51,7 +51,7 @@ struct Cfg {
     static constexpr uint32_t Q_BYTES = BN * BK;
     static constexpr uint32_t STAGE_BYTES = P_BYTES + Q_BYTES;
     static constexpr int CH = BN < 32 ? 16 : 32;  // accumulator columns per tcgen05.ld
-    static constexpr uint32_t XBUF_BYTES = SWAP ? 128 * (CH + 1) * 4 : 0;  // gate/up exchange
+    static constexpr uint32_t XBUF_BYTES = SWAP ? 128 * (BN + 1) * 4 : 0;  // gate/up exchange, whole tile
     static constexpr int STAGES_FIT =
         (int)((SMEM_LIMIT - 1024 - 256 - XBUF_BYTES) / STAGE_BYTES);
     static constexpr int STAGES = STAGES_FIT > 10 ? 10 : STAGES_FIT;  // most stages a launch may ask for
@@ -84,14 +84,34 @@ struct Unit {
 // tiles whose operands stay in L2 together.
 __device__ __forceinline__ Unit decode(const GemmParams &p, int u) {
     Unit w;
-    w.split = u % p.splits;
-    w.tile = u / p.splits;
-    const int per_group = p.group * p.n_tiles_q;
-    const int grp = w.tile / per_group;
-    const int rem = w.tile - grp * per_group;
-    const int gsize = min(p.group, p.n_tiles_p - grp * p.group);
-    w.tp = grp * p.group + rem % gsize;
-    w.tq = rem / gsize;
+    if (p.mcast <= 1) {
+        w.split = u % p.splits;
+        w.tile = u / p.splits;
+        const int per_group = p.group * p.n_tiles_q;
+        const int grp = w.tile / per_group;
+        const int rem = w.tile - grp * per_group;
+        const int gsize = min(p.group, p.n_tiles_p - grp * p.group);
+        w.tp = grp * p.group + rem % gsize;
+        w.tq = rem / gsize;
+    } else {
+        // weight multicast: the C CTAs of a cluster (consecutive units) take
+        // C consecutive P-tiles of the same weight tile and split; the raster
+        // runs over blocks of C P-tiles
+        const int C = p.mcast;
+        const int rank = u % C;
+        const int v = u / C;
+        w.split = v % p.splits;
+        const int t = v / p.splits;
+        const int nblk = p.n_tiles_p / C;
+        const int group = max(1, p.group / C);
+        const int per_group = group * p.n_tiles_q;
+        const int grp = t / per_group;
+        const int rem = t - grp * per_group;
+        const int gsize = min(group, nblk - grp * group);
+        w.tp = (grp * group + rem % gsize) * C + rank;
+        w.tq = rem / gsize;
+        w.tile = w.tq * p.n_tiles_p + w.tp;
+    }
     w.kb0 = w.split * p.kb_per_split;
     w.kb1 = min(p.k_blocks, w.kb0 + p.kb_per_split);
     return w;
@@ -140,7 +160,15 @@ __device__ void producer(const CUtensorMap *tmP, const CUtensorMap *tmQ, const G
                 const uint32_t dX = SWAP ? dQ : dP;
                 const CUtensorMap *mW = SWAP ? tmP : tmQ;
                 const CUtensorMap *mX = SWAP ? tmQ : tmP;
-                tma_load_2d(dW, mW, fb, kb * BK, wrow, pol_w);
+                if (!SWAP && p.mcast > 1) {
+                    // this CTA's 1/C of the weight tile, to every CTA of the cluster
+                    const int rows = BN / p.mcast;
+                    const int rank = (int)(blockIdx.x % (unsigned)p.mcast);
+                    tma_load_2d_mcast(dW + (uint32_t)(rank * rows * BK), mW, fb, kb * BK, wrow + rank * rows,
+                                      (uint16_t)((1u << p.mcast) - 1u), pol_w);
+                } else {
+                    tma_load_2d(dW, mW, fb, kb * BK, wrow, pol_w);
+                }
                 if (waited) {
                     tma_load_2d(dX, mX, fb, kb * BK, xrow, pol_x);
                 } else {
@@ -212,7 +240,13 @@ __device__ void mma_issuer(const GemmParams &p, uint8_t *sP, uint8_t *sQ, uint64
                     mma_f8f6f4(dt, smem_desc_k128(aP + k * UK), smem_desc_k128(aQ + k * UK), idesc,
                                (kb > w.kb0 || k > 0) ? 1u : 0u);
                 issued_any = true;
-                mma_commit(smem_u32(&empty[stage]));  // frees the stage when these MMAs finish
+                // frees the stage when these MMAs finish (with weight
+                // multicast: in every CTA of the cluster, whose producers
+                // write into this CTA's stage)
+                if (!SWAP && p.mcast > 1)
+                    mma_commit_mcast(smem_u32(&empty[stage]), (uint16_t)((1u << p.mcast) - 1u));
+                else
+                    mma_commit(smem_u32(&empty[stage]));
                 if (++stage == p.stages) {
                     stage = 0;
                     phase ^= 1u;
@@ -266,40 +300,6 @@ __device__ __forceinline__ void unit_row(uint32_t tbase, Put &&put) {
         for (int j = 0; j < 16; ++j)
             v[j] = __uint_as_float(a[c + j]);
         put(c, v);
-    }
-}
-
-// Accumulator columns c .. c+CH-1 of this thread's row: straight from TMEM,
-// or (split-K, last arriver) the sum of every split's partial in split order.
-template <int BN, int CH>
-__device__ __forceinline__ void fetch_chunk(bool from_ws, uint32_t tbase, const float *tile_ws, int splits, int r,
-                                            int c, float (&v)[CH]) {
-    if (!from_ws) {
-        tmem_load_chunk<CH>(tbase + c, v);
-        return;
-    }
-#pragma unroll
-    for (int j = 0; j < CH; ++j)
-        v[j] = 0.0f;
-    const float *src = tile_ws + (size_t)c * BM + r;
-    int sp = 0;
-#pragma unroll 1
-    for (; sp + 2 <= splits; sp += 2) {
-        float t0[CH], t1[CH];
-#pragma unroll
-        for (int j = 0; j < CH; ++j)
-            t0[j] = __ldcg(src + (size_t)sp * (BM * BN) + (size_t)j * BM);
-#pragma unroll
-        for (int j = 0; j < CH; ++j)
-            t1[j] = __ldcg(src + (size_t)(sp + 1) * (BM * BN) + (size_t)j * BM);
-#pragma unroll
-        for (int j = 0; j < CH; ++j)
-            v[j] = __fadd_rn(__fadd_rn(v[j], t0[j]), t1[j]);
-    }
-    if (sp < splits) {
-#pragma unroll
-        for (int j = 0; j < CH; ++j)
-            v[j] = __fadd_rn(v[j], __ldcg(src + (size_t)sp * (BM * BN) + (size_t)j * BM));
     }
 }
 
@@ -446,57 +446,63 @@ __device__ __forceinline__ void dbg_store_gu(const GemmParams &p, int m, int f, 
         p.dbg_gu[(size_t)m * 2 * p.ff + (up ? p.ff : 0) + f] = (uint16_t)bf16_bits(val);
 }
 
-// Weight-streaming path: TMEM lanes 0..63 are gate rows, 64..127 the up rows
-// of the same 64 features; columns are tokens.  Up values go through shared
-// memory to the gate threads.  Called by all 128 epilogue threads.
-template <int BN, int CH>
-__device__ __forceinline__ void gated_swap_chunk(const GemmParams &p, const Unit &w, int r, int c,
-                                                 const float (&v)[CH], float *xbuf, float &amax) {
-    const int m0 = w.tq * BN + c;  // first token of the chunk
-    {
+// Weight-streaming path, whole tile at once: TMEM lanes 0..63 are gate rows,
+// 64..127 the up rows of the same 64 features; columns are tokens.  Every
+// thread parks its row (rounded to BF16) in xbuf and frees the accumulator;
+// then thread t takes features 4(t % 16) .. +3 and tokens t / 16, t / 16 + 8,
+// ...: for each token the 4 activations leave as one 4-byte store of E4M3
+// codes.  Called by all 128 epilogue threads; returns after a barrier, so
+// xbuf is free again.
+template <int BN>
+__device__ __forceinline__ void gated_swap_tile(const GemmParams &p, const Unit &w, int r, uint32_t tbase,
+                                                uint64_t *tempty_b, float *xbuf, float &amax) {
+    constexpr int LD = BN + 1;
+    const int m0 = w.tq * BN;  // first token of the tile
+    const int ncols = min(BN, p.m_tok - m0);
+    const float alpha = p.alpha;
+    unit_row<BN>(tbase, [&](int c, const float (&v)[16]) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            xbuf[r * LD + c + j] = round_bf16(__fmul_rn(v[j], alpha));
+    });
+    tc_fence_before();
+    mbar_arrive(smem_u32(tempty_b));  // the accumulator is read: the next unit's MMAs may start
+    named_bar_sync(1, 128);
+    if (p.dbg_gu) {
         const int f = w.tp * (BM / 2) + (r & 63);
-        const bool up = r >= 64;
-        float gv[CH];
+        for (int c = 0; c < ncols; ++c)
+            dbg_store_gu(p, m0 + c, f, r >= 64, xbuf[r * LD + c]);
+    }
+    constexpr int TG = BN / 8;  // tokens per thread
+    const int fq = r & 15;      // feature quad
+    const int t0 = r >> 4;      // first token
+    float g[4 * TG], u[4 * TG], a[4 * TG];
 #pragma unroll
-        for (int j = 0; j < CH; ++j) {
-            gv[j] = round_bf16(__fmul_rn(v[j], p.alpha));
-            xbuf[r * (CH + 1) + j] = gv[j];
-        }
-        if (p.dbg_gu) {
+    for (int i = 0; i < TG; ++i) {
+        const int c = min(t0 + 8 * i, BN - 1);
 #pragma unroll
-            for (int j = 0; j < CH; ++j)
-                if (m0 + j < p.m_tok)
-                    dbg_store_gu(p, m0 + j, f, up, gv[j]);
+        for (int j = 0; j < 4; ++j) {
+            g[4 * i + j] = xbuf[(4 * fq + j) * LD + c];
+            u[4 * i + j] = xbuf[(64 + 4 * fq + j) * LD + c];
         }
     }
-    named_bar_sync(1, 128);
-    // thread t: feature t % 64, tokens of half t / 64 of the chunk
-    {
-        constexpr int HALF = CH / 2;
-        const int fl = r & 63;
-        const int f = w.tp * (BM / 2) + fl;
-        const int j0 = (r >> 6) * HALF;
-        uint8_t *qh = static_cast<uint8_t *>(p.out);
-        float g[HALF], u[HALF], a[HALF];
+    gated_run<4 * TG>(p.act, g, u, a);
+    if (p.epi == EPI_GATED_AMAX) {
 #pragma unroll
-        for (int j = 0; j < HALF; ++j) {
-            g[j] = xbuf[fl * (CH + 1) + j0 + j];
-            u[j] = xbuf[(fl + 64) * (CH + 1) + j0 + j];
-        }
-        gated_run<HALF>(p.act, g, u, a);
-        const int nv = p.m_tok - (m0 + j0);  // valid tokens of this half
-        if (p.epi == EPI_GATED_AMAX) {
+        for (int i = 0; i < TG; ++i)
+            if (t0 + 8 * i < ncols)
 #pragma unroll
-            for (int j = 0; j < HALF; ++j)
-                if (j < nv)
-                    amax = fmaxf(amax, fabsf(a[j]));
-        } else {
-            const float inv_s = p.inv_s;
+                for (int j = 0; j < 4; ++j)
+                    amax = fmaxf(amax, fabsf(a[4 * i + j]));
+    } else {
+        uint8_t *qh = static_cast<uint8_t *>(p.out) + (size_t)w.tp * (BM / 2) + 4 * fq;
+        const float inv_s = p.inv_s;
 #pragma unroll
-            for (int j = 0; j < HALF; ++j)
-                if (j < nv)
-                    qh[(size_t)(m0 + j0 + j) * p.ldo + f] = (uint8_t)(e4m3x2(__fmul_rn(a[j], inv_s), 0.0f) & 0xFFu);
-        }
+        for (int i = 0; i < TG; ++i)
+            if (t0 + 8 * i < ncols)
+                *reinterpret_cast<uint32_t *>(qh + (size_t)(m0 + t0 + 8 * i) * p.ldo) =
+                    e4m3x2(__fmul_rn(a[4 * i], inv_s), __fmul_rn(a[4 * i + 1], inv_s)) |
+                    (e4m3x2(__fmul_rn(a[4 * i + 2], inv_s), __fmul_rn(a[4 * i + 3], inv_s)) << 16);
     }
     named_bar_sync(1, 128);
 }
@@ -551,10 +557,10 @@ __device__ __forceinline__ float warp_max_f(float v) {
     return v;
 }
 
-// Consume one unit's accumulator (from TMEM or from the split-K workspace).
+// Consume one unit's accumulator from TMEM: the tiled gated epilogue, or a
+// plain one (the weight-streaming gated epilogue is gated_swap_tile).
 template <int BN, bool SWAP>
-__device__ __forceinline__ void consume_unit(const GemmParams &p, const Unit &w, bool from_ws, uint32_t tbase,
-                                             const float *tile_ws, int ncols, float *xbuf) {
+__device__ __forceinline__ void consume_unit(const GemmParams &p, const Unit &w, uint32_t tbase) {
     using C = Cfg<BN, SWAP>;
     constexpr int CH = C::CH;
     const int r = threadIdx.x;
@@ -566,8 +572,8 @@ __device__ __forceinline__ void consume_unit(const GemmParams &p, const Unit &w,
 #pragma unroll 1
             for (int sub = 0; sub < 64; sub += CH) {
                 float g[CH], u[CH];
-                fetch_chunk<BN, CH>(from_ws, tbase, tile_ws, p.splits, r, c0 + sub, g);
-                fetch_chunk<BN, CH>(from_ws, tbase, tile_ws, p.splits, r, c0 + 64 + sub, u);
+                tmem_load_chunk<CH>(tbase + c0 + sub, g);
+                tmem_load_chunk<CH>(tbase + c0 + 64 + sub, u);
                 gated_tiled_chunk<CH>(p, w.tp * BM + r, w.tq * (BN / 2) + c0 / 2 + sub, g, u, amax);
             }
         }
@@ -575,15 +581,8 @@ __device__ __forceinline__ void consume_unit(const GemmParams &p, const Unit &w,
 #pragma unroll 1
         for (int c = 0; c < BN; c += CH) {
             float v[CH];
-            if (from_ws && c >= ncols)
-                break;  // uniform: padding columns of the split-K partials
-            fetch_chunk<BN, CH>(from_ws, tbase, tile_ws, p.splits, r, c, v);
-            if (gated_epi) {
-                if constexpr (SWAP)
-                    gated_swap_chunk<BN, CH>(p, w, r, c, v, xbuf, amax);
-            } else {
-                store_chunk<BN, SWAP, CH>(p, w, r, c, v);
-            }
+            tmem_load_chunk<CH>(tbase + c, v);
+            store_chunk<BN, SWAP, CH>(p, w, r, c, v);
         }
     }
     if (p.epi == EPI_GATED_AMAX) {
@@ -1070,9 +1069,21 @@ __device__ void epilogue(const GemmParams &p, uint64_t *tfull, uint64_t *tempty,
         tc_fence_after();
         const uint32_t tbase = tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(abuf * BN);
         if (p.splits == 1) {
-            consume_unit<BN, SWAP>(p, w, false, tbase, nullptr, BN, xbuf);
-            tc_fence_before();
-            mbar_arrive(smem_u32(&tempty[abuf]));
+            if (SWAP && (p.epi == EPI_GATED || p.epi == EPI_GATED_AMAX)) {
+                if constexpr (SWAP) {
+                    float amax = 0.0f;
+                    gated_swap_tile<BN>(p, w, r, tbase, &tempty[abuf], xbuf, amax);
+                    if (p.epi == EPI_GATED_AMAX) {
+                        amax = warp_max_f(amax);
+                        if ((threadIdx.x & 31) == 0)
+                            atomicMax(p.amax, __float_as_uint(amax));
+                    }
+                }
+            } else {
+                consume_unit<BN, SWAP>(p, w, tbase);
+                tc_fence_before();
+                mbar_arrive(smem_u32(&tempty[abuf]));
+            }
         } else if (SWAP && p.cluster) {
             if constexpr (SWAP) {
                 if (!coop_cluster_unit<BN, SWAP>(p, w, tbase, &tempty[abuf], free_bar, data_bar, sent_bar, red,
@@ -1130,7 +1141,7 @@ __global__ void __launch_bounds__(NTHREADS, SWAP ? 2 : 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
-            mbar_init(smem_u32(&empty[s]), 1);
+            mbar_init(smem_u32(&empty[s]), p.mcast > 1 ? (uint32_t)p.mcast : 1u);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&tfull[b]), 1);
@@ -1162,6 +1173,12 @@ __global__ void __launch_bounds__(NTHREADS, SWAP ? 2 : 1)
     // its first access to another CTA (the epilogue) or at its end
     if (p.cluster)
         cluster_arrive();
+    if (p.mcast > 1) {
+        // weight multicast writes into, and MMA commits arrive on, the other
+        // CTAs' stages and barriers from the first k-block on
+        cluster_arrive();
+        cluster_wait();
+    }
     const uint32_t tmem_base = *tmem_holder;
     pdl_trigger();
 
@@ -1186,6 +1203,11 @@ __global__ void __launch_bounds__(NTHREADS, SWAP ? 2 : 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (p.mcast > 1) {
+        // no CTA leaves while another may still write into it
+        cluster_arrive();
+        cluster_wait();
+    }
     if (warp == 5) {
         __syncwarp();
         tmem_dealloc(tmem_base, C::TMEM_COLS);
@@ -1222,7 +1244,8 @@ cudaError_t run(const GemmLaunch &g, cudaStream_t s, bool pdl) {
     const bool xbuf = SWAP && g.p.splits == 1 && (g.p.epi == EPI_GATED || g.p.epi == EPI_GATED_AMAX);
     return launch_ex(k_gemm_fp8<BN, SWAP>, dim3((unsigned)g.grid), dim3(NTHREADS),
                      std::max(C::smem_bytes(g.p.stages, xbuf), g.min_smem), s, pdl,
-                     g.p.cluster ? (unsigned)g.p.splits : 1u, g.tmP, g.tmQ, g.p);
+                     g.p.cluster ? (unsigned)g.p.splits : (g.p.mcast > 1 ? (unsigned)g.p.mcast : 1u), g.tmP, g.tmQ,
+                     g.p);
 }
 
 }  // namespace
@@ -1264,14 +1287,14 @@ cudaError_t encode_tmap_u8(CUtensorMap *m, const void *base, uint64_t rows, uint
 namespace {
 
 struct StageInfo {
-    size_t stage_bytes, fixed_bytes;
+    size_t stage_bytes, fixed_bytes, xbuf_bytes;  // fixed_bytes without the gate/up exchange buffer
     int max_stages;
 };
 
 template <int BN, bool SWAP>
 StageInfo stage_info() {
     using C = Cfg<BN, SWAP>;
-    return {C::STAGE_BYTES, C::smem_bytes(0, SWAP), C::STAGES};
+    return {C::STAGE_BYTES, C::smem_bytes(0, false), C::XBUF_BYTES, C::STAGES};
 }
 
 StageInfo stage_info_for(int bn, bool swap) {
@@ -1321,10 +1344,32 @@ void plan_gemm(GemmLaunch &g, bool swap, int m_tok, int n_feat, int K, int num_s
     splits = std::max(1, std::min(std::min(splits, 16), p.k_blocks));
     if (cluster_on && force_splits == 0)
         splits = std::min(splits, CLUSTER_MAX);
+    // weight-streaming tiles whose whole K fits the stage ring: no split-K
+    // (each CTA prefetches its entire weight panel; no partials to exchange),
+    // as long as there are enough tiles to spread the weight stream
+    if (swap && force_splits == 0 && tiles >= 16 && p.k_blocks <= stage_info_for(g.bn, swap).max_stages)
+        splits = 1;
     p.kb_per_split = (p.k_blocks + splits - 1) / splits;
     p.splits = (p.k_blocks + p.kb_per_split - 1) / p.kb_per_split;
     p.total_units = tiles * p.splits;
     g.grid = std::min(p.total_units, num_sms);
+    // tiled role, opt-in (FRT_FFN_MCAST = 2 or 4; needs C | token tiles and
+    // C | grid): clusters of C CTAs on C consecutive token tiles share each
+    // weight tile, every CTA loading 1/C of it and multicasting it.  Off by
+    // default: on GB300 the lockstep it imposes on the C pipelines cost more
+    // than the L2 traffic it saves on the prefill shapes.
+    p.mcast = 1;
+    if (!swap) {
+        const char *e = getenv("FRT_FFN_MCAST");
+        int c = e ? atoi(e) : 1;
+        c = c >= 4 ? 4 : (c >= 2 ? 2 : 1);
+        while (c > 1 && p.n_tiles_p % c)
+            c /= 2;
+        if (c > 1) {
+            p.mcast = c;
+            g.grid = g.grid / c * c;
+        }
+    }
     // rasterisation: all P-tiles at once if the P operand of a wave fits
     // comfortably in L2 (for weight streaming P is the weights, each read
     // once anyway); else groups of P-tiles whose rows take about 32 MB
@@ -1341,7 +1386,9 @@ void plan_gemm(GemmLaunch &g, bool swap, int m_tok, int n_feat, int K, int num_s
     const StageInfo si = stage_info_for(g.bn, swap);
     const int units_per_cta = (p.total_units + g.grid - 1) / g.grid;
     const int kb_cta = p.kb_per_split * units_per_cta;
-    int cohabit = (int)((COHABIT_SMEM - si.fixed_bytes) / si.stage_bytes);
+    // the gate/up exchange buffer is only in unsplit weight-streaming launches
+    const size_t fixed = si.fixed_bytes + (swap && p.splits == 1 ? si.xbuf_bytes : 0);
+    int cohabit = (int)((COHABIT_SMEM - fixed) / si.stage_bytes);
     cohabit = std::max(2, std::min(cohabit, si.max_stages));
     p.stages = kb_cta <= 2 * cohabit ? std::min(cohabit, std::max(2, kb_cta)) : si.max_stages;
     if (const char *e = getenv("FRT_FFN_STAGES")) {
