@@ -51,7 +51,7 @@ struct Cfg {
     static constexpr uint32_t Q_BYTES = BN * BK;
     static constexpr uint32_t STAGE_BYTES = P_BYTES + Q_BYTES;
     static constexpr int CH = BN < 32 ? 16 : 32;  // accumulator columns per tcgen05.ld
-    static constexpr uint32_t XBUF_BYTES = SWAP ? 128 * (BN + 1) * 4 : 0;  // gate/up exchange, whole tile
+    static constexpr uint32_t XBUF_BYTES = SWAP ? BN * (128 + 4) * 4 : 0;  // gate/up exchange, whole tile
     static constexpr int STAGES_FIT =
         (int)((SMEM_LIMIT - 1024 - 256 - XBUF_BYTES) / STAGE_BYTES);
     static constexpr int STAGES = STAGES_FIT > 10 ? 10 : STAGES_FIT;  // most stages a launch may ask for
@@ -404,23 +404,36 @@ __device__ __forceinline__ void store_chunk(const GemmParams &p, const Unit &w, 
 
 __device__ __forceinline__ float round_bf16(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
 
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // GELU, tanh form: 0.5 g (1 + tanh(y)), y = sqrt(2/pi) (g + 0.044715 g^3).
-// Because 1 + tanh(y) = 2 / (1 + exp(-2y)), this equals g / (1 + exp(-2y)):
-// one exponential and one division, free of branches and of the
-// cancellation in 1 + tanh(y) for negative y.  __expf and __fdividef are the
-// hardware approximations (a few ulp; the error of __expf grows by about one
-// ulp per unit of its argument); the E4M3 code of the result keeps 3 bits.
-// An overflowing exponential gives g / inf = -0 for very negative g, and an
+// Because 1 + tanh(y) = 2 / (1 + exp(-2y)), this equals g / (1 + exp(-2y)),
+// and exp(-2y) = 2^(g (c1 + c2 g^2)) with c1 = -2 sqrt(2/pi) log2(e),
+// c2 = 0.044715 c1: one base-2 exponential and one reciprocal (the hardware
+// approximations, a few ulp), free of branches and of the cancellation in
+// 1 + tanh(y) for negative y; the E4M3 code of the result keeps 3 bits.  An
+// overflowing exponential gives g * 0 = -0 for very negative g, an
 // underflowing one gives g.
 __device__ __forceinline__ float gelu_tanh(float g) {
-    const float k0 = 0.7978845608028654f;
-    const float k1 = 0.044715f;
-    const float g3 = __fmul_rn(__fmul_rn(g, g), g);
-    const float y = __fmul_rn(k0, __fadd_rn(g, __fmul_rn(k1, g3)));
-    return __fdividef(g, __fadd_rn(1.0f, __expf(__fmul_rn(-2.0f, y))));
+    const float c1 = -2.3022081981f;  // -2 * 0.7978845608 * 1.4426950409
+    const float c2 = -0.1029432396f;  // 0.044715 * c1
+    const float t = __fmul_rn(g, __fadd_rn(c1, __fmul_rn(c2, __fmul_rn(g, g))));
+    return __fmul_rn(g, rcp_approx(__fadd_rn(1.0f, ex2_approx(t))));
 }
-// SiLU: g / (1 + exp(-g)), with the same approximations.
-__device__ __forceinline__ float silu(float g) { return __fdividef(g, __fadd_rn(1.0f, __expf(-g))); }
+// SiLU: g / (1 + exp(-g)) = g / (1 + 2^(-g log2 e)), same approximations.
+__device__ __forceinline__ float silu(float g) {
+    const float t = __fmul_rn(g, -1.4426950409f);
+    return __fmul_rn(g, rcp_approx(__fadd_rn(1.0f, ex2_approx(t))));
+}
 
 // a[j] = act(g[j]) * u[j] over a run of N elements, the activation chosen
 // once for the run so the N chains interleave.
@@ -448,22 +461,23 @@ __device__ __forceinline__ void dbg_store_gu(const GemmParams &p, int m, int f, 
 
 // Weight-streaming path, whole tile at once: TMEM lanes 0..63 are gate rows,
 // 64..127 the up rows of the same 64 features; columns are tokens.  Every
-// thread parks its row (rounded to BF16) in xbuf and frees the accumulator;
-// then thread t takes features 4(t % 16) .. +3 and tokens t / 16, t / 16 + 8,
-// ...: for each token the 4 activations leave as one 4-byte store of E4M3
-// codes.  Called by all 128 epilogue threads; returns after a barrier, so
-// xbuf is free again.
+// thread parks its row (rounded to BF16) in xbuf, token-major (a token's 128
+// rows are contiguous), and frees the accumulator; then thread t takes
+// features 4(t % 16) .. +3 of tokens 8(t / 16) .. +7, reading each token's
+// four gate and four up values with one 16-byte load each, and stores the
+// four activations of a token as one 4-byte word of E4M3 codes.  Called by
+// all 128 epilogue threads; returns after a barrier, so xbuf is free again.
 template <int BN>
 __device__ __forceinline__ void gated_swap_tile(const GemmParams &p, const Unit &w, int r, uint32_t tbase,
                                                 uint64_t *tempty_b, float *xbuf, float &amax) {
-    constexpr int LD = BN + 1;
-    const int m0 = w.tq * BN;  // first token of the tile
+    constexpr int LD = 128 + 4;  // floats per token
+    const int m0 = w.tq * BN;    // first token of the tile
     const int ncols = min(BN, p.m_tok - m0);
     const float alpha = p.alpha;
     unit_row<BN>(tbase, [&](int c, const float (&v)[16]) {
 #pragma unroll
         for (int j = 0; j < 16; ++j)
-            xbuf[r * LD + c + j] = round_bf16(__fmul_rn(v[j], alpha));
+            xbuf[(c + j) * LD + r] = round_bf16(__fmul_rn(v[j], alpha));
     });
     tc_fence_before();
     mbar_arrive(smem_u32(tempty_b));  // the accumulator is read: the next unit's MMAs may start
@@ -471,26 +485,24 @@ __device__ __forceinline__ void gated_swap_tile(const GemmParams &p, const Unit 
     if (p.dbg_gu) {
         const int f = w.tp * (BM / 2) + (r & 63);
         for (int c = 0; c < ncols; ++c)
-            dbg_store_gu(p, m0 + c, f, r >= 64, xbuf[r * LD + c]);
+            dbg_store_gu(p, m0 + c, f, r >= 64, xbuf[c * LD + r]);
     }
     constexpr int TG = BN / 8;  // tokens per thread
     const int fq = r & 15;      // feature quad
-    const int t0 = r >> 4;      // first token
+    const int c0 = (r >> 4) * TG;
     float g[4 * TG], u[4 * TG], a[4 * TG];
 #pragma unroll
     for (int i = 0; i < TG; ++i) {
-        const int c = min(t0 + 8 * i, BN - 1);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            g[4 * i + j] = xbuf[(4 * fq + j) * LD + c];
-            u[4 * i + j] = xbuf[(64 + 4 * fq + j) * LD + c];
-        }
+        const float4 gv = *reinterpret_cast<const float4 *>(xbuf + (c0 + i) * LD + 4 * fq);
+        const float4 uv = *reinterpret_cast<const float4 *>(xbuf + (c0 + i) * LD + 64 + 4 * fq);
+        g[4 * i] = gv.x; g[4 * i + 1] = gv.y; g[4 * i + 2] = gv.z; g[4 * i + 3] = gv.w;
+        u[4 * i] = uv.x; u[4 * i + 1] = uv.y; u[4 * i + 2] = uv.z; u[4 * i + 3] = uv.w;
     }
     gated_run<4 * TG>(p.act, g, u, a);
     if (p.epi == EPI_GATED_AMAX) {
 #pragma unroll
         for (int i = 0; i < TG; ++i)
-            if (t0 + 8 * i < ncols)
+            if (c0 + i < ncols)
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
                     amax = fmaxf(amax, fabsf(a[4 * i + j]));
@@ -499,8 +511,8 @@ __device__ __forceinline__ void gated_swap_tile(const GemmParams &p, const Unit 
         const float inv_s = p.inv_s;
 #pragma unroll
         for (int i = 0; i < TG; ++i)
-            if (t0 + 8 * i < ncols)
-                *reinterpret_cast<uint32_t *>(qh + (size_t)(m0 + t0 + 8 * i) * p.ldo) =
+            if (c0 + i < ncols)
+                *reinterpret_cast<uint32_t *>(qh + (size_t)(m0 + c0 + i) * p.ldo) =
                     e4m3x2(__fmul_rn(a[4 * i], inv_s), __fmul_rn(a[4 * i + 1], inv_s)) |
                     (e4m3x2(__fmul_rn(a[4 * i + 2], inv_s), __fmul_rn(a[4 * i + 3], inv_s)) << 16);
     }
