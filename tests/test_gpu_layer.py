@@ -29,6 +29,8 @@ SHAPES = [
     WL["tiny"].with_(name="m65_tiled", M=65, d=512, ff=1536, n_calib=1, seed=12),
     WL["vla_prefix"].with_(name="prefix_small", M=300, d=512, ff=2048, L=1),
     WL["long_prefill"].with_(name="prefill_small", M=257, d=640, ff=1280, L=1),
+    # gate/up K beyond the stage ring with few tiles: gated split-K epilogue
+    WL["tiny"].with_(name="gu_split", M=32, d=2048, ff=1024, n_calib=1, seed=13),
 ]
 
 
@@ -86,3 +88,24 @@ def test_out_may_alias_residual(case):
     case.plan.forward(buf, h, out=buf)
     torch.cuda.synchronize()
     assert torch.equal(sep, buf)
+
+
+@pytest.mark.parametrize("M", [32, 50])
+def test_cluster_and_global_split_k_layers_agree(monkeypatch, M):
+    """A layer whose gate/up and down GEMMs both split K gives the same bits
+    with the split-K partials exchanged through distributed shared memory
+    inside a cluster or through a global workspace (same partials, same
+    reduction order)."""
+    wl = WL["tiny"].with_(name="xchg", M=M, d=2048, ff=1024, n_calib=1, seed=17)
+    c = Case(wl)
+    dev = torch.device("cuda")
+    r, h = c.r.to(dev), c.h.to(dev)
+    monkeypatch.delenv("FRT_FFN_CLUSTER", raising=False)
+    a = {k: v.clone() for k, v in c.plan.trace_layer(0, r, h).items()}
+    monkeypatch.setenv("FRT_FFN_CLUSTER", "0")
+    b = c.plan.trace_layer(0, r, h)
+    torch.cuda.synchronize()
+    c.plan.device_status()
+    for k in ("q_x", "gu", "q_h", "out"):
+        assert torch.equal(a[k], b[k]), k
+    c.close()
