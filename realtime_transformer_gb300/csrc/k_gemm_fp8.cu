@@ -705,6 +705,7 @@ __device__ __forceinline__ void elem_map(const Unit &w, const Slice &sl, int e, 
 
 constexpr int RED_Q = 2;        // plain epilogues: quads (4 elements) per thread per batch
 constexpr int RED_Q_GATED = 4;  // gated epilogue: a whole gate/up slice in one batch
+constexpr int RED_Q_TILED = 8;  // plain epilogue of a tiled slice (half a 128 x 256 tile and up)
 
 // Reduce this CTA's slice over the S staged partials (split order) and run
 // the epilogue.  A thread takes quads: 4 consecutive elements of one token,
@@ -721,7 +722,7 @@ constexpr int RED_Q_GATED = 4;  // gated epilogue: a whole gate/up slice in one 
 template <int BN, bool SWAP, bool GATED>
 __device__ __forceinline__ float reduce_slice(const GemmParams &p, const Unit &w, const Slice &sl, const float *red,
                                               int span, const uint2 (&res0)[RED_Q]) {
-    constexpr int NQ = GATED ? RED_Q_GATED : RED_Q;
+    constexpr int NQ = GATED ? RED_Q_GATED : (SWAP ? RED_Q : RED_Q_TILED);
     constexpr int UP = SWAP ? BM / 2 : 64;  // offset of an element's up partner (gated)
     const int r = threadIdx.x;
     const int S = p.splits;
@@ -751,10 +752,10 @@ __device__ __forceinline__ float reduce_slice(const GemmParams &p, const Unit &w
         uint2 res[NQ];
         if constexpr (!GATED) {
             if (epi == EPI_RESID) {
-                if (first) {
+                if (first && NQ == RED_Q) {
 #pragma unroll
                     for (int i = 0; i < NQ; ++i)
-                        res[i] = res0[i];
+                        res[i] = res0[i % RED_Q];
                 } else {
 #pragma unroll
                     for (int i = 0; i < NQ; ++i) {
