@@ -888,20 +888,38 @@ __device__ bool coop_split_unit(const GemmParams &p, const Unit &w, uint32_t tba
                     mine[(size_t)(c + j) * BM + r] = v[j];
         });
     } else {
+        // Tiled: a thread holds a whole row (BN floats); written straight to
+        // global memory a warp's 16-byte stores would land 4*BN bytes apart.
+        // Stage the tile row-major in the (now idle) pipeline stages instead,
+        // 16-byte chunks XOR-swizzled by row so 8 consecutive rows hit all 32
+        // banks, then copy it out with whole-warp contiguous 16-byte stores.
+        float *stg = red;  // the slices arrive here only after the copy-out
+        constexpr int CPR = BN / 4;  // 16-byte chunks per row
 #pragma unroll 1
         for (int c = 0; c < BN; c += CH) {
             float v[CH];
             tmem_load_chunk<CH>(tbase + c, v);
-            if (r < nrows) {
 #pragma unroll
-                for (int j = 0; j < CH; j += 4)
-                    *reinterpret_cast<float4 *>(mine + (size_t)r * BN + c + j) =
-                        make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+            for (int j = 0; j < CH; j += 4) {
+                const int ch = (c + j) >> 2;
+                *reinterpret_cast<float4 *>(stg + (size_t)r * BN + 4 * (ch ^ (r & 7))) =
+                    make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
             }
         }
+        tc_fence_before();
+        mbar_arrive(smem_u32(tempty_b));
+        named_bar_sync(1, 128);
+#pragma unroll 4
+        for (int i = r; i < nrows * CPR; i += 128) {
+            const int row = i / CPR, ch = i - row * CPR;
+            *reinterpret_cast<float4 *>(mine + (size_t)row * BN + 4 * ch) =
+                *reinterpret_cast<const float4 *>(stg + (size_t)row * BN + 4 * (ch ^ (row & 7)));
+        }
     }
-    tc_fence_before();
-    mbar_arrive(smem_u32(tempty_b));
+    if constexpr (SWAP) {
+        tc_fence_before();
+        mbar_arrive(smem_u32(tempty_b));
+    }
     named_bar_sync(1, 128);
     // 2. count in, wait for every split of the tile, pull this CTA's slice of
     //    every partial into shared memory with bulk copies.  The counter only
