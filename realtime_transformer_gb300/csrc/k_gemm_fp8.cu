@@ -996,11 +996,14 @@ __device__ bool coop_cluster_unit(const GemmParams &p, const Unit &w, uint32_t t
     // 1. expect this slice from every split; free this CTA's stages for them
     //    (no ordering needed: the MMAs that read the stages have completed,
     //    which the wait on the accumulator barrier established)
-    if (threadIdx.x == 0) {
-        mbar_arrive_expect_tx(smem_u32(data_bar), (uint32_t)(S * span * 4));
-        for (int j = 0; j < S; ++j)
-            if (j != k)
-                mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(free_bar), (uint32_t)j));
+    //    Lane j of warp 0 handles CTA j; the expected bytes may land before
+    //    lane 0 declares them (the phase needs lane 0's arrival to complete).
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        if (lane == 0)
+            mbar_arrive_expect_tx(smem_u32(data_bar), (uint32_t)(S * span * 4));
+        if (lane < S && lane != k)
+            mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(free_bar), (uint32_t)lane));
     }
     // residuals of the first batch: independent of the other splits
     uint2 res0[RED_Q];
@@ -1031,26 +1034,29 @@ __device__ bool coop_cluster_unit(const GemmParams &p, const Unit &w, uint32_t t
     // 3. once every CTA of the cluster has freed its stages, send slice j of
     //    this partial to CTA j, into row k of its slice buffer; then wait for
     //    this CTA's slice from all S splits
-    if (threadIdx.x == 0) {
-        bool ok = mbar_wait_cluster(smem_u32(free_bar), 0, abort_f, p.err);
-        if (ok) {
-            for (int j = 0; j < S; ++j) {
-                const Slice sj = slice_of<BN, SWAP>(j, S, ncols, BM, gated_epi);
-                const int spj = sj.hi - sj.lo;
-                if (spj > 0)
-                    bulk_copy_to_cta(mapa_shared(smem_u32(red + (size_t)k * spj), (uint32_t)j), smem_u32(stg + sj.lo),
-                                     (uint32_t)spj * 4u, mapa_shared(smem_u32(data_bar), (uint32_t)j));
-            }
-            ok = mbar_wait_cluster(smem_u32(data_bar), 0, abort_f, p.err);
+    //    (lane j of warp 0 copies to, and later reports to, CTA j)
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        int ok = 1;
+        if (lane == 0)
+            ok = mbar_wait_cluster(smem_u32(free_bar), 0, abort_f, p.err) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (ok && lane < S) {
+            const Slice sj = slice_of<BN, SWAP>(lane, S, ncols, BM, gated_epi);
+            const int spj = sj.hi - sj.lo;
+            if (spj > 0)
+                bulk_copy_to_cta(mapa_shared(smem_u32(red + (size_t)k * spj), (uint32_t)lane), smem_u32(stg + sj.lo),
+                                 (uint32_t)spj * 4u, mapa_shared(smem_u32(data_bar), (uint32_t)lane));
         }
-        if (ok) {
-            // every copy into this CTA has landed, so every source may let
-            // its staging go
-            for (int j = 0; j < S; ++j)
-                if (j != k)
-                    mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(sent_bar), (uint32_t)j));
-        }
-        *s_flag = ok ? 1 : 0;
+        if (ok && lane == 0)
+            ok = mbar_wait_cluster(smem_u32(data_bar), 0, abort_f, p.err) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        // every copy into this CTA has landed, so every source may let its
+        // staging go
+        if (ok && lane < S && lane != k)
+            mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(sent_bar), (uint32_t)lane));
+        if (lane == 0)
+            *s_flag = ok;
     }
     named_bar_sync(1, 128);
     if (!*s_flag)
