@@ -18,6 +18,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import math
 import os
@@ -71,11 +72,21 @@ def layer_algorithmic_bytes(wl, M):
     return 3 * wl.d * wl.ff + 2 * 2 * M * wl.d
 
 
+def source_code_only(text):
+    """The code of a CUDA/C++ source without its comments and blank lines
+    (string literals in these sources hold no comment markers)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = [re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines()]
+    return "\n".join(ln for ln in lines if ln.strip())
+
+
 def source_hash(names):
+    """Hash of the kernels' code (comments excluded), recorded with each ncu
+    summary so that `traffic` is reported only for the code it was measured on."""
     h = hashlib.sha256()
     for n in names:
-        with open(os.path.join(ROOT, "realtime_transformer_gb300", "csrc", n), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "realtime_transformer_gb300", "csrc", n)) as f:
+            h.update(source_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -4,26 +4,31 @@
 // docs/architecture.md", 6: alpha = act_scale x weight_scale applied in the
 // GEMM as a host scalar).
 //
-// One persistent kernel template, 192 threads per CTA, one CTA per SM:
+// One persistent kernel template, 192 threads per CTA:
 //   warp 4      TMA producer: streams 128-byte-wide K slices of the two
 //               operands into a ring of shared-memory stages (128B swizzle);
 //   warp 5      MMA issuer: one thread issues tcgen05.mma (kind::f8f6f4,
 //               M = 128, N = BN, K = 32) into a double-buffered TMEM
 //               accumulator and commits to mbarriers;
 //   warps 0..3  epilogue: tcgen05.ld of the accumulator (one TMEM lane per
-//               thread), scale by alpha, optional residual add, BF16 store;
-//               with split-K, fp32 partials go to a workspace and the last
-//               CTA to arrive on a tile sums them in split order
-//               (deterministic) and runs the epilogue.
+//               thread), scale by alpha, gated activation + E4M3 requantise
+//               or residual add + BF16 store.
+// Split-K is cooperative (one unit per CTA): each split stages its fp32
+// partial, the S partials of a tile are exchanged -- over distributed shared
+// memory inside a thread-block cluster, or through a global workspace --
+// and every split reduces a 1/S slice of the tile in split order
+// (deterministic) and runs the epilogue for it.
 // Two operand roles:
 //   tiled  (P = token tiles of 128 rows, Q = weight tiles of BN rows) for
 //          many tokens;
 //   swap   (P = weight tiles of 128 rows, Q = the <= 64 tokens padded to BN)
 //          for few tokens: the layer is then bound by streaming the weights
-//          from HBM, and split-K spreads that stream over all SMs.
+//          from HBM, spread over the SMs by the tile count and split-K.
 // Weight tiles are requested before griddepcontrol.wait, so with
 // programmatic dependent launch they stream in while the previous kernel of
-// the layer finishes; activation tiles are requested after it.
+// the layer finishes (a short launch keeps a small shared-memory footprint so
+// that its CTAs share SMs with the previous kernel's); activation tiles are
+// requested after it.
 // Every wait is bounded (frt_ptx.cuh); on a timeout the CTA drains its
 // in-flight copies and MMAs, frees TMEM and exits with the error word set.
 #include <cuda_bf16.h>
@@ -613,7 +618,8 @@ __device__ __forceinline__ void consume_unit(const GemmParams &p, const Unit &w,
 // per CTA, and a dependent kernel only launches once every CTA of this one is
 // resident.
 // Partial layout: weight-streaming [column][row] (a warp writes 32
-// consecutive rows), tiled [row][column] (a thread writes its own row).
+// consecutive rows), tiled [row][column] (staged in shared memory, then
+// copied out with contiguous whole-warp stores).
 // Wait until the counter has reached `target` (wrap-around safe).
 __device__ __forceinline__ bool spin_until_geq(const int *addr, unsigned target, volatile int *abort_f, int *err) {
     const uint64_t t0 = globaltimer();
