@@ -179,6 +179,18 @@ frt_status frt_ffn_debug_step(frt_ffn_plan_t plan, int layer, int step, int M, f
 frt_status frt_ffn_device_status(frt_ffn_plan_t plan, frt_stream_t stream);
 
 /*
+ * Test hook for the failure path (no counterpart in the pages): launch one
+ * small GEMM of the plan's kernels on the plan's scratch whose MMA thread
+ * first waits for a barrier phase that nothing completes.  The bounded wait
+ * gives up after about 2 s, sets the plan's error word, and every role of the
+ * kernel drains its copies, frees its tensor memory and exits; the call then
+ * returns what frt_ffn_device_status reports -- DEVICE_TIMEOUT -- and the
+ * plan (and the CUDA context) stay usable.  Overwrites the plan's split-K
+ * workspace.  Errors: INVALID_ARG, CUDA.
+ */
+frt_status frt_ffn_debug_stall(frt_ffn_plan_t plan, frt_stream_t stream);
+
+/*
  * Test/diagnostic: the plan's FP8 GEMM kernels on caller buffers,
  * C[m][n] = alpha * sum_k A[m][k] B[n][k] stored as fp32 (the contraction of
  * steps A2/A4, itsolotime article 7.2).  A [M, K] and B [N, K] E4M3 (device,

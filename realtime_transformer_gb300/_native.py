@@ -39,6 +39,7 @@ SIGNATURES = {
     "frt_ffn_graph_replay": (_I, [_P, _I, _P]),
     "frt_ffn_debug_trace": (_I, [_P, _I, _P, _P, _I, _P, _P, _P, _P, _P, _P]),
     "frt_ffn_device_status": (_I, [_P, _P]),
+    "frt_ffn_debug_stall": (_I, [_P, _P]),
     "frt_ffn_debug_step": (_I, [_P, _I, _I, _I, _P]),
     "frt_fp8_gemm": (_I, [_P, _P, _P, _P, _I, _I, _I, _F, _I, _I, _P]),
     "frt_ffn_last_error": (ctypes.c_char_p, []),
@@ -141,6 +142,10 @@ def frt_ffn_debug_step(plan, layer, step, M, stream) -> None:
 
 def frt_ffn_device_status(plan, stream) -> None:
     _check(lib().frt_ffn_device_status(plan, stream))
+
+
+def frt_ffn_debug_stall(plan, stream) -> None:
+    _check(lib().frt_ffn_debug_stall(plan, stream))
 
 
 def frt_fp8_gemm(plan, A, B, C, M, N, K, alpha, path, splits, stream) -> None:

@@ -710,6 +710,32 @@ FRT_API frt_status frt_ffn_device_status(frt_ffn_plan_t P, frt_stream_t stream) 
     return FRT_OK;
 }
 
+FRT_API frt_status frt_ffn_debug_stall(frt_ffn_plan_t P, frt_stream_t stream) {
+    if (!P)
+        return fail(FRT_ERR_INVALID_ARG, "null plan");
+    // a 64 x 256 x d weight-streaming GEMM on the plan's own scratch: q_x
+    // codes against the first 256 gate/up weight rows, fp32 into the
+    // split-K workspace, without split-K
+    const int M = 64, N = 256, K = P->d;
+    GemmLaunch g;
+    memset(&g.p, 0, sizeof g.p);
+    plan_gemm(g, true, M, N, K, P->num_sms, 1);
+    if (encode_tmap_u8(&g.tmP, P->w_gu, N, K, 128) != cudaSuccess ||
+        encode_tmap_u8(&g.tmQ, P->qx, M, K, g.bn) != cudaSuccess)
+        return fail(FRT_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+    g.p.epi = EPI_F32;
+    g.p.alpha = 1.0f;
+    g.p.out = P->ws;
+    g.p.ldo = N;
+    g.p.ws = P->ws;
+    g.p.counters = split_counters(P->counters + (size_t)N_GEMM_SITES * SPLIT_COUNTERS, g.p.splits);
+    g.p.err = P->err;
+    g.p.stall_test = 1;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    CK(launch_gemm(g, s, false));
+    return frt_ffn_device_status(P, stream);
+}
+
 FRT_API frt_status frt_fp8_gemm(frt_ffn_plan_t P, const void *A, const void *B, void *C, int M, int N, int K,
                                 float alpha, int path, int splits, frt_stream_t stream) {
     if (!P)

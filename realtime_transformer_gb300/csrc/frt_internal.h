@@ -47,6 +47,7 @@ struct GemmParams {
     int cluster;            // 1: the splits of a tile are one thread-block cluster and exchange
                             //    partials in distributed shared memory (ws, counters unused)
     int *err;               // device error word
+    int stall_test;         // test hook: the MMA issuer first waits on a phase nothing completes
     // gated epilogues
     int act;                // Act
     int ff;                 // hidden width (feature count of q_h)

@@ -227,6 +227,11 @@ __device__ void mma_issuer(const GemmParams &p, uint8_t *sP, uint8_t *sQ, uint64
     int abuf = 0;
     uint32_t aphase = 0;
     bool issued_any = false;
+    // Test hook for the failure path: wait for a phase of the drain barrier,
+    // which nothing completes before an MMA is issued.  The bounded wait gives
+    // up, sets the abort flag and the error word, and every role drains.
+    if (p.stall_test && !mbar_wait(smem_u32(drain_bar), 0, abort_f, p.err))
+        goto drain;
     for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
         const Unit w = decode(p, u);
         if (!mbar_wait(smem_u32(&tempty[abuf]), aphase ^ 1u, abort_f, p.err))

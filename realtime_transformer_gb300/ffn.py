@@ -130,6 +130,11 @@ class FFNPlan:
     def device_status(self, stream=None):
         N.frt_ffn_device_status(self.handle, _stream(stream))
 
+    def debug_stall(self, stream=None):
+        """Failure-path test hook: raises FrtError(FRT_ERR_DEVICE_TIMEOUT)
+        after a kernel gives up its bounded wait (about 2 s)."""
+        N.frt_ffn_debug_stall(self.handle, _stream(stream))
+
     def trace_layer(self, layer, residual, hidden=None, stream=None):
         """Run one layer alone and return its intermediates (diagnostics)."""
         M, d, ff = residual.shape[0], self.d, self.ff
