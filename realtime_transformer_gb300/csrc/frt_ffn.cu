@@ -183,8 +183,9 @@ frt_status setup_gemm(frt_ffn_plan *P, GemmLaunch &g, int site, int l, int M) {
         g.p.q_row0 = 0;
     } else {
         if ((st = get_tmap(P, xbuf, 128, &g.tmP, &g.p.gtm_p)) != FRT_OK) return st;
-        // with weight multicast each CTA loads BN / mcast rows of the tile
-        if ((st = get_tmap(P, wbuf, g.bn / g.p.mcast, &g.tmQ, &g.p.gtm_q)) != FRT_OK) return st;
+        // with weight multicast each CTA loads BN / mcast rows of the tile, on
+        // a CTA pair half of them
+        if ((st = get_tmap(P, wbuf, g.bn / (g.p.pair ? 2 : g.p.mcast), &g.tmQ, &g.p.gtm_q)) != FRT_OK) return st;
         g.p.p_row0 = 0;
         g.p.q_row0 = l * N;
     }
@@ -760,7 +761,7 @@ FRT_API frt_status frt_fp8_gemm(frt_ffn_plan_t P, const void *A, const void *B, 
         e2 = encode_tmap_u8(&g.tmQ, A, M, K, g.bn);
     } else {
         e1 = encode_tmap_u8(&g.tmP, A, M, K, 128);
-        e2 = encode_tmap_u8(&g.tmQ, B, N, K, g.bn / g.p.mcast);  // weight slice per multicasting CTA
+        e2 = encode_tmap_u8(&g.tmQ, B, N, K, g.bn / (g.p.pair ? 2 : g.p.mcast));  // weight slice per CTA
     }
     if (e1 != cudaSuccess || e2 != cudaSuccess)
         return fail(FRT_ERR_CUDA, "cuTensorMapEncodeTiled failed");

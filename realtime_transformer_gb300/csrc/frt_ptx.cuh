@@ -318,6 +318,56 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int m, int n) {
            | ((uint32_t)(m >> 4) << 24);   // M >> 4
 }
 
+// ------------------------------------------- CTA pairs (cta_group::2) --
+// A kernel uses either these or the single-CTA forms, never both.
+// Collective over the pair: one warp in each of the two CTAs executes it.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// D[256 x N] (+)= A[256 x K] B[N x K]^T over the pair: issued by the even
+// CTA; A's rows 0..127 and B's rows 0..N/2-1 come from its shared memory,
+// the other halves from the odd CTA's at the same offsets; each CTA's TMEM
+// receives its 128 rows of D.
+__device__ __forceinline__ void mma_f8f6f4_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive on the mbarrier at the offset of `bar` in the CTAs of the pair named
+// in `mask` once the pair MMAs issued so far are done.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t mask) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                     bar),
+                 "h"(mask)
+                 : "memory");
+}
+// TMA 2-D load into this CTA's shared memory whose bytes complete on an
+// mbarrier of either CTA of the pair (`bar` from mapa_shared).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *m, uint32_t bar, int x, int y,
+                                                 uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2.L2::cache_hint"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "l"(policy)
+        : "memory");
+}
+// Arrive, with release at cluster scope, on an mbarrier of any CTA of the
+// cluster (address from mapa_shared).
+__device__ __forceinline__ void mbar_arrive_cluster_release(uint32_t bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
 // ---------------------------------------------- programmatic dependent launch --
 // Block until the grids this grid depends on have completed and their memory
 // is visible.  A no-op when the launch had no programmatic dependency.

@@ -50,10 +50,13 @@ constexpr int UK = 32;         // K of one tcgen05.mma for 8-bit operands
 constexpr int NTHREADS = 192;  // 4 epilogue warps + producer warp + MMA warp
 constexpr uint32_t SMEM_LIMIT = 232448;  // largest dynamic shared memory of one CTA (227 KB)
 
-template <int BN, bool SWAP = false>
+// PAIR: the tiled role on a CTA pair (cta_group::2): each CTA stages its own
+// token tile and half of the weight tile.
+template <int BN, bool SWAP = false, bool PAIR = false>
 struct Cfg {
+    static_assert(!(PAIR && SWAP), "CTA pairs serve the tiled role");
     static constexpr uint32_t P_BYTES = BM * BK;
-    static constexpr uint32_t Q_BYTES = BN * BK;
+    static constexpr uint32_t Q_BYTES = (PAIR ? BN / 2 : BN) * BK;
     static constexpr uint32_t STAGE_BYTES = P_BYTES + Q_BYTES;
     static constexpr int CH = BN < 32 ? 16 : 32;  // accumulator columns per tcgen05.ld
     static constexpr uint32_t XBUF_BYTES = SWAP ? BN * (128 + 4) * 4 : 0;  // gate/up exchange, whole tile
@@ -89,7 +92,7 @@ struct Unit {
 // tiles whose operands stay in L2 together.
 __device__ __forceinline__ Unit decode(const GemmParams &p, int u) {
     Unit w;
-    if (p.mcast <= 1) {
+    if (p.mcast <= 1 && !p.pair) {
         w.split = u % p.splits;
         w.tile = u / p.splits;
         const int per_group = p.group * p.n_tiles_q;
@@ -102,7 +105,7 @@ __device__ __forceinline__ Unit decode(const GemmParams &p, int u) {
         // weight multicast: the C CTAs of a cluster (consecutive units) take
         // C consecutive P-tiles of the same weight tile and split; the raster
         // runs over blocks of C P-tiles
-        const int C = p.mcast;
+        const int C = p.pair ? 2 : p.mcast;
         const int rank = u % C;
         const int v = u / C;
         w.split = v % p.splits;
@@ -129,10 +132,13 @@ __device__ __forceinline__ uint32_t bf16_bits(float x) {
 }
 
 // ------------------------------------------------------------ producer --
-template <int BN, bool SWAP>
+template <int BN, bool SWAP, bool PAIR>
 __device__ void producer(const CUtensorMap *tmP, const CUtensorMap *tmQ, const GemmParams &p, uint8_t *sP,
                          uint8_t *sQ, uint64_t *full, uint64_t *empty, volatile int *abort_f) {
-    using C = Cfg<BN, SWAP>;
+    using C = Cfg<BN, SWAP, PAIR>;
+    // CTA pair: both CTAs' copies complete on the even CTA's stage barrier,
+    // which alone is armed (with both CTAs' bytes)
+    const uint32_t rank = PAIR ? (blockIdx.x & 1u) : 0u;
     const uint64_t pol_w = l2_policy_evict_first();  // weights: read once per launch
     const uint64_t pol_x = l2_policy_evict_last();   // activations: re-read by many CTAs
     int stage = 0;
@@ -155,8 +161,11 @@ __device__ void producer(const CUtensorMap *tmP, const CUtensorMap *tmQ, const G
             if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, abort_f, p.err))
                 goto drain;
             {
-                const uint32_t fb = smem_u32(&full[stage]);
-                mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+                const uint32_t fb = PAIR ? mapa_shared(smem_u32(&full[stage]), 0u) : smem_u32(&full[stage]);
+                if (!PAIR)
+                    mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+                else if (rank == 0)
+                    mbar_arrive_expect_tx(smem_u32(&full[stage]), 2u * C::STAGE_BYTES);
                 issued |= 1u << stage;
                 issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
                 const uint32_t dP = smem_u32(sP + (size_t)stage * C::P_BYTES);
@@ -165,17 +174,23 @@ __device__ void producer(const CUtensorMap *tmP, const CUtensorMap *tmQ, const G
                 const uint32_t dX = SWAP ? dQ : dP;
                 const CUtensorMap *mW = SWAP ? tmP : tmQ;
                 const CUtensorMap *mX = SWAP ? tmQ : tmP;
-                if (!SWAP && p.mcast > 1) {
+                if constexpr (PAIR) {
+                    // this CTA's half of the weight tile
+                    tma_load_2d_pair(dW, mW, fb, kb * BK, wrow + (int)rank * (BN / 2), pol_w);
+                } else if (!SWAP && p.mcast > 1) {
                     // this CTA's 1/C of the weight tile, to every CTA of the cluster
                     const int rows = BN / p.mcast;
-                    const int rank = (int)(blockIdx.x % (unsigned)p.mcast);
-                    tma_load_2d_mcast(dW + (uint32_t)(rank * rows * BK), mW, fb, kb * BK, wrow + rank * rows,
+                    const int crank = (int)(blockIdx.x % (unsigned)p.mcast);
+                    tma_load_2d_mcast(dW + (uint32_t)(crank * rows * BK), mW, fb, kb * BK, wrow + crank * rows,
                                       (uint16_t)((1u << p.mcast) - 1u), pol_w);
                 } else {
                     tma_load_2d(dW, mW, fb, kb * BK, wrow, pol_w);
                 }
                 if (waited) {
-                    tma_load_2d(dX, mX, fb, kb * BK, xrow, pol_x);
+                    if constexpr (PAIR)
+                        tma_load_2d_pair(dX, mX, fb, kb * BK, xrow, pol_x);
+                    else
+                        tma_load_2d(dX, mX, fb, kb * BK, xrow, pol_x);
                 } else {
                     if (n_def == 0) {
                         def_kb = kb;
@@ -188,10 +203,14 @@ __device__ void producer(const CUtensorMap *tmP, const CUtensorMap *tmQ, const G
                         waited = true;
                         int st = def_stage;
                         for (int i = 0; i < n_def; ++i) {
-                            const uint32_t fbi = smem_u32(&full[st]);
+                            const uint32_t fbi =
+                                PAIR ? mapa_shared(smem_u32(&full[st]), 0u) : smem_u32(&full[st]);
                             const uint32_t dst = SWAP ? smem_u32(sQ + (size_t)st * C::Q_BYTES)
                                                       : smem_u32(sP + (size_t)st * C::P_BYTES);
-                            tma_load_2d(dst, mX, fbi, (def_kb + i) * BK, def_row, pol_x);
+                            if constexpr (PAIR)
+                                tma_load_2d_pair(dst, mX, fbi, (def_kb + i) * BK, def_row, pol_x);
+                            else
+                                tma_load_2d(dst, mX, fbi, (def_kb + i) * BK, def_row, pol_x);
                             if (++st == NS)
                                 st = 0;
                         }
@@ -209,19 +228,23 @@ __device__ void producer(const CUtensorMap *tmP, const CUtensorMap *tmQ, const G
         pdl_wait();
     return;
 drain:
-    // Give copies in flight a bounded time to land before the CTA exits.
-    for (int s = 0; s < NS; ++s)
-        if (issued & (1u << s))
-            mbar_wait_for(smem_u32(&full[s]), (issued_par >> s) & 1u, 100000000ull);
+    // Give copies in flight a bounded time to land before the CTA exits (a
+    // pair's odd CTA has no armed stage barrier of its own; the pair's
+    // closing cluster barrier holds it until the even one is done).
+    if (!PAIR || rank == 0)
+        for (int s = 0; s < NS; ++s)
+            if (issued & (1u << s))
+                mbar_wait_for(smem_u32(&full[s]), (issued_par >> s) & 1u, 100000000ull);
 }
 
 // ---------------------------------------------------------- MMA issuer --
-template <int BN, bool SWAP>
+template <int BN, bool SWAP, bool PAIR>
 __device__ void mma_issuer(const GemmParams &p, uint8_t *sP, uint8_t *sQ, uint64_t *full, uint64_t *empty,
                            uint64_t *tfull, uint64_t *tempty, uint64_t *drain_bar, uint32_t tmem_base,
                            volatile int *abort_f) {
-    using C = Cfg<BN, SWAP>;
-    constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
+    using C = Cfg<BN, SWAP, PAIR>;
+    // a pair's MMAs (issued by the even CTA only) cover 256 token rows
+    constexpr uint32_t idesc = idesc_e4m3_f32(PAIR ? 2 * BM : BM, BN);
     int stage = 0;
     uint32_t phase = 0;
     int abuf = 0;
@@ -246,14 +269,20 @@ __device__ void mma_issuer(const GemmParams &p, uint8_t *sP, uint8_t *sQ, uint64
                 const uint32_t aP = smem_u32(sP + (size_t)stage * C::P_BYTES);
                 const uint32_t aQ = smem_u32(sQ + (size_t)stage * C::Q_BYTES);
 #pragma unroll
-                for (int k = 0; k < BK / UK; ++k)
-                    mma_f8f6f4(dt, smem_desc_k128(aP + k * UK), smem_desc_k128(aQ + k * UK), idesc,
-                               (kb > w.kb0 || k > 0) ? 1u : 0u);
+                for (int k = 0; k < BK / UK; ++k) {
+                    if constexpr (PAIR)
+                        mma_f8f6f4_pair(dt, smem_desc_k128(aP + k * UK), smem_desc_k128(aQ + k * UK), idesc,
+                                        (kb > w.kb0 || k > 0) ? 1u : 0u);
+                    else
+                        mma_f8f6f4(dt, smem_desc_k128(aP + k * UK), smem_desc_k128(aQ + k * UK), idesc,
+                                   (kb > w.kb0 || k > 0) ? 1u : 0u);
+                }
                 issued_any = true;
                 // frees the stage when these MMAs finish (with weight
-                // multicast: in every CTA of the cluster, whose producers
-                // write into this CTA's stage)
-                if (!SWAP && p.mcast > 1)
+                // multicast or a CTA pair: in every CTA that writes into it)
+                if constexpr (PAIR)
+                    mma_commit_pair(smem_u32(&empty[stage]), 0x3);
+                else if (!SWAP && p.mcast > 1)
                     mma_commit_mcast(smem_u32(&empty[stage]), (uint16_t)((1u << p.mcast) - 1u));
                 else
                     mma_commit(smem_u32(&empty[stage]));
@@ -263,7 +292,11 @@ __device__ void mma_issuer(const GemmParams &p, uint8_t *sP, uint8_t *sQ, uint64
                 }
             }
         }
-        mma_commit(smem_u32(&tfull[abuf]));  // accumulator ready for the epilogue
+        // accumulator ready for the epilogue (of both CTAs of a pair)
+        if constexpr (PAIR)
+            mma_commit_pair(smem_u32(&tfull[abuf]), 0x3);
+        else
+            mma_commit(smem_u32(&tfull[abuf]));
         if (++abuf == 2) {
             abuf = 0;
             aphase ^= 1u;
@@ -272,7 +305,10 @@ __device__ void mma_issuer(const GemmParams &p, uint8_t *sP, uint8_t *sQ, uint64
     return;
 drain:
     if (issued_any) {
-        mma_commit(smem_u32(drain_bar));
+        if constexpr (PAIR)
+            mma_commit_pair(smem_u32(drain_bar), 0x1);
+        else
+            mma_commit(smem_u32(drain_bar));
         mbar_wait_for(smem_u32(drain_bar), 0, 100000000ull);
     }
 }
@@ -1091,7 +1127,7 @@ __host__ __device__ constexpr size_t red_floats(int bn, int splits) {
     return ((size_t)BM * bn + (size_t)splits * ((BM > bn ? BM : bn) + 4) + 31) & ~(size_t)31;
 }
 
-template <int BN, bool SWAP>
+template <int BN, bool SWAP, bool PAIR>
 __device__ void epilogue(const GemmParams &p, uint64_t *tfull, uint64_t *tempty, uint32_t tmem_base,
                          volatile int *abort_f, volatile int *s_ok, volatile int *s_last, float *xbuf,
                          uint64_t *red_bar, uint64_t *free_bar, uint64_t *data_bar, uint64_t *sent_bar,
@@ -1130,7 +1166,15 @@ __device__ void epilogue(const GemmParams &p, uint64_t *tfull, uint64_t *tempty,
             } else {
                 consume_unit<BN, SWAP>(p, w, tbase);
                 tc_fence_before();
-                mbar_arrive(smem_u32(&tempty[abuf]));
+                if constexpr (PAIR) {
+                    // the even CTA's MMA refills both CTAs' accumulators:
+                    // one arrival per CTA on its barrier
+                    named_bar_sync(1, 128);
+                    if (threadIdx.x == 0)
+                        mbar_arrive_cluster_release(mapa_shared(smem_u32(&tempty[abuf]), 0u));
+                } else {
+                    mbar_arrive(smem_u32(&tempty[abuf]));
+                }
             }
         } else if (SWAP && p.cluster) {
             if constexpr (SWAP) {
@@ -1158,11 +1202,11 @@ __device__ void epilogue(const GemmParams &p, uint64_t *tfull, uint64_t *tempty,
 }
 
 // -------------------------------------------------------------- kernel --
-template <int BN, bool SWAP>
+template <int BN, bool SWAP, bool PAIR>
 __global__ void __launch_bounds__(NTHREADS, SWAP ? 2 : 1)
     k_gemm_fp8(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmQ,
                const __grid_constant__ GemmParams p) {
-    using C = Cfg<BN, SWAP>;
+    using C = Cfg<BN, SWAP, PAIR>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *sP = smem;
@@ -1193,7 +1237,7 @@ __global__ void __launch_bounds__(NTHREADS, SWAP ? 2 : 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&tfull[b]), 1);
-            mbar_init(smem_u32(&tempty[b]), 128);
+            mbar_init(smem_u32(&tempty[b]), PAIR ? 2u : 128u);
         }
         mbar_init(smem_u32(drain_bar), 1);
         mbar_init(smem_u32(red_bar), 1);
@@ -1210,8 +1254,13 @@ __global__ void __launch_bounds__(NTHREADS, SWAP ? 2 : 1)
         prefetch_tmap(mapQ);
     }
     if (warp == 5) {
-        tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
-        tmem_relinquish();
+        if constexpr (PAIR) {
+            tmem_alloc_pair(smem_u32(tmem_holder), C::TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -1221,9 +1270,10 @@ __global__ void __launch_bounds__(NTHREADS, SWAP ? 2 : 1)
     // its first access to another CTA (the epilogue) or at its end
     if (p.cluster)
         cluster_arrive();
-    if (p.mcast > 1) {
+    if (PAIR || p.mcast > 1) {
         // weight multicast writes into, and MMA commits arrive on, the other
-        // CTAs' stages and barriers from the first k-block on
+        // CTAs' stages and barriers from the first k-block on (a pair's
+        // copies and MMAs likewise)
         cluster_arrive();
         cluster_wait();
     }
@@ -1233,17 +1283,17 @@ __global__ void __launch_bounds__(NTHREADS, SWAP ? 2 : 1)
     if (warp < 4) {
         // split-K runs one unit per CTA, so the pipeline stages are free to
         // receive the partial slices once the last MMA has completed
-        epilogue<BN, SWAP>(p, tfull, tempty, tmem_base, abort_f, s_ok, s_last, xbuf, red_bar, free_bar, data_bar,
-                           sent_bar, reinterpret_cast<float *>(smem));
+        epilogue<BN, SWAP, PAIR>(p, tfull, tempty, tmem_base, abort_f, s_ok, s_last, xbuf, red_bar, free_bar,
+                                 data_bar, sent_bar, reinterpret_cast<float *>(smem));
     } else if (warp == 4) {
         if (lane == 0)
-            producer<BN, SWAP>(mapP, mapQ, p, sP, sQ, full, empty, abort_f);
+            producer<BN, SWAP, PAIR>(mapP, mapQ, p, sP, sQ, full, empty, abort_f);
         __syncwarp();
         if (p.cluster)
             cluster_wait();
     } else {
-        if (lane == 0)
-            mma_issuer<BN, SWAP>(p, sP, sQ, full, empty, tfull, tempty, drain_bar, tmem_base, abort_f);
+        if (lane == 0 && (!PAIR || (blockIdx.x & 1u) == 0))
+            mma_issuer<BN, SWAP, PAIR>(p, sP, sQ, full, empty, tfull, tempty, drain_bar, tmem_base, abort_f);
         __syncwarp();
         if (p.cluster)
             cluster_wait();
@@ -1251,30 +1301,33 @@ __global__ void __launch_bounds__(NTHREADS, SWAP ? 2 : 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (p.mcast > 1) {
+    if (PAIR || p.mcast > 1) {
         // no CTA leaves while another may still write into it
         cluster_arrive();
         cluster_wait();
     }
     if (warp == 5) {
         __syncwarp();
-        tmem_dealloc(tmem_base, C::TMEM_COLS);
+        if constexpr (PAIR)
+            tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+        else
+            tmem_dealloc(tmem_base, C::TMEM_COLS);
     }
 }
 
-template <int BN, bool SWAP>
+template <int BN, bool SWAP, bool PAIR = false>
 cudaError_t set_attrs() {
-    using C = Cfg<BN, SWAP>;
+    using C = Cfg<BN, SWAP, PAIR>;
     static int done = 0;
     if (!done) {
-        cudaError_t e = cudaFuncSetAttribute(k_gemm_fp8<BN, SWAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(k_gemm_fp8<BN, SWAP, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)C::SMEM);
         if (e != cudaSuccess)
             return e;
         // every kernel of the layer asks for the largest shared-memory
         // carve-out, so an SM never needs to drain before a CTA of the next
         // kernel (with its own footprint) can start beside the running ones
-        e = cudaFuncSetAttribute(k_gemm_fp8<BN, SWAP>, cudaFuncAttributePreferredSharedMemoryCarveout,
+        e = cudaFuncSetAttribute(k_gemm_fp8<BN, SWAP, PAIR>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  (int)cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess)
             return e;
@@ -1283,17 +1336,16 @@ cudaError_t set_attrs() {
     return cudaSuccess;
 }
 
-template <int BN, bool SWAP>
+template <int BN, bool SWAP, bool PAIR = false>
 cudaError_t run(const GemmLaunch &g, cudaStream_t s, bool pdl) {
-    using C = Cfg<BN, SWAP>;
-    cudaError_t e = set_attrs<BN, SWAP>();
+    using C = Cfg<BN, SWAP, PAIR>;
+    cudaError_t e = set_attrs<BN, SWAP, PAIR>();
     if (e != cudaSuccess)
         return e;
     const bool xbuf = SWAP && g.p.splits == 1 && (g.p.epi == EPI_GATED || g.p.epi == EPI_GATED_AMAX);
-    return launch_ex(k_gemm_fp8<BN, SWAP>, dim3((unsigned)g.grid), dim3(NTHREADS),
-                     std::max(C::smem_bytes(g.p.stages, xbuf), g.min_smem), s, pdl,
-                     g.p.cluster ? (unsigned)g.p.splits : (g.p.mcast > 1 ? (unsigned)g.p.mcast : 1u), g.tmP, g.tmQ,
-                     g.p);
+    const unsigned cluster = PAIR ? 2u : g.p.cluster ? (unsigned)g.p.splits : (g.p.mcast > 1 ? (unsigned)g.p.mcast : 1u);
+    return launch_ex(k_gemm_fp8<BN, SWAP, PAIR>, dim3((unsigned)g.grid), dim3(NTHREADS),
+                     std::max(C::smem_bytes(g.p.stages, xbuf), g.min_smem), s, pdl, cluster, g.tmP, g.tmQ, g.p);
 }
 
 }  // namespace
@@ -1339,15 +1391,17 @@ struct StageInfo {
     int max_stages;
 };
 
-template <int BN, bool SWAP>
+template <int BN, bool SWAP, bool PAIR = false>
 StageInfo stage_info() {
-    using C = Cfg<BN, SWAP>;
+    using C = Cfg<BN, SWAP, PAIR>;
     return {C::STAGE_BYTES, C::smem_bytes(0, false), C::XBUF_BYTES, C::STAGES};
 }
 
-StageInfo stage_info_for(int bn, bool swap) {
+StageInfo stage_info_for(int bn, bool swap, bool pair = false) {
     if (swap)
         return bn == 16 ? stage_info<16, true>() : (bn == 32 ? stage_info<32, true>() : stage_info<64, true>());
+    if (pair)
+        return stage_info<256, false, true>();
     return bn == 128 ? stage_info<128, false>() : stage_info<256, false>();
 }
 
@@ -1418,6 +1472,19 @@ void plan_gemm(GemmLaunch &g, bool swap, int m_tok, int n_feat, int K, int num_s
             g.grid = g.grid / c * c;
         }
     }
+    // tiled role on CTA pairs (FRT_FFN_PAIR=0 disables): 256-token tiles
+    // computed by two CTAs with cta_group::2 MMAs, each staging its own 128
+    // tokens and half of the 256-row weight tile -- half the weight traffic
+    // per CTA and 7 pipeline stages instead of 4; unsplit 256-wide tiles on
+    // an even number of token tiles only
+    p.pair = 0;
+    if (!swap && p.mcast == 1 && p.splits == 1 && g.bn == 256 && p.n_tiles_p % 2 == 0) {
+        const char *e = getenv("FRT_FFN_PAIR");
+        if (!(e && e[0] == '0')) {
+            p.pair = 1;
+            g.grid = g.grid / 2 * 2;
+        }
+    }
     // rasterisation: all P-tiles at once if the P operand of a wave fits
     // comfortably in L2 (for weight streaming P is the weights, each read
     // once anyway); else groups of P-tiles whose rows take about 32 MB
@@ -1431,7 +1498,7 @@ void plan_gemm(GemmLaunch &g, bool swap, int m_tok, int n_feat, int K, int num_s
     }
     // pipeline depth: short launches keep a small footprint (see COHABIT_SMEM),
     // long ones take every stage they can
-    const StageInfo si = stage_info_for(g.bn, swap);
+    const StageInfo si = stage_info_for(g.bn, swap, p.pair != 0);
     const int units_per_cta = (p.total_units + g.grid - 1) / g.grid;
     const int kb_cta = p.kb_per_split * units_per_cta;
     // the gate/up exchange buffer is only in unsplit weight-streaming launches
@@ -1491,7 +1558,7 @@ cudaError_t launch_gemm(const GemmLaunch &g, cudaStream_t s, bool pdl) {
     }
     switch (g.bn) {
     case 128: return run<128, false>(g, s, pdl);
-    case 256: return run<256, false>(g, s, pdl);
+    case 256: return g.p.pair ? run<256, false, true>(g, s, pdl) : run<256, false>(g, s, pdl);
     default: return cudaErrorInvalidValue;
     }
 }
