@@ -954,7 +954,10 @@ __device__ bool coop_split_unit(const GemmParams &p, const Unit &w, uint32_t tba
             }
         }
         tc_fence_before();
-        mbar_arrive(smem_u32(tempty_b));
+        // (a CTA pair's accumulator barrier counts one arrival per CTA; with
+        // one unit per CTA nothing waits on it again, so pairs skip it)
+        if (!p.pair)
+            mbar_arrive(smem_u32(tempty_b));
         named_bar_sync(1, 128);
 #pragma unroll 4
         for (int i = r; i < nrows * CPR; i += 128) {
@@ -1475,10 +1478,10 @@ void plan_gemm(GemmLaunch &g, bool swap, int m_tok, int n_feat, int K, int num_s
     // tiled role on CTA pairs (FRT_FFN_PAIR=0 disables): 256-token tiles
     // computed by two CTAs with cta_group::2 MMAs, each staging its own 128
     // tokens and half of the 256-row weight tile -- half the weight traffic
-    // per CTA and 7 pipeline stages instead of 4; unsplit 256-wide tiles on
-    // an even number of token tiles only
+    // per CTA and 7 pipeline stages instead of 4; 256-wide tiles on an even
+    // number of token tiles
     p.pair = 0;
-    if (!swap && p.mcast == 1 && p.splits == 1 && g.bn == 256 && p.n_tiles_p % 2 == 0) {
+    if (!swap && p.mcast == 1 && g.bn == 256 && p.n_tiles_p % 2 == 0) {
         const char *e = getenv("FRT_FFN_PAIR");
         if (!(e && e[0] == '0')) {
             p.pair = 1;

@@ -108,8 +108,9 @@ def test_weight_multicast_matches_plain_loads(plan, monkeypatch, M, N, K, splits
     assert np.array_equal(c_plain, c_mcast)
 
 
-@pytest.mark.parametrize("M,N,K", [(256, 256, 512), (512, 512, 1024), (1000, 768, 2048)])
-def test_cta_pair_matches_single_cta(plan, monkeypatch, M, N, K):
+@pytest.mark.parametrize("M,N,K,splits", [(256, 256, 512, 1), (512, 512, 1024, 1), (1000, 768, 2048, 1),
+                                          (1000, 512, 4096, 2), (256, 768, 2048, 0)])
+def test_cta_pair_matches_single_cta(plan, monkeypatch, M, N, K, splits):
     """Tiled role on CTA pairs (cta_group::2 MMAs over 256 token rows, each
     CTA staging half of the weight tile) gives the same bits as one CTA per
     128-token tile."""
@@ -117,7 +118,7 @@ def test_cta_pair_matches_single_cta(plan, monkeypatch, M, N, K):
     A = rng.integers(0, 0x7E, (M, K)).astype(np.uint8)
     B = rng.integers(0, 0x7E, (N, K)).astype(np.uint8)
     monkeypatch.setenv("FRT_FFN_PAIR", "0")
-    c_single = run(plan, A, B, 2, 1)
+    c_single = run(plan, A, B, 2, splits)
     monkeypatch.delenv("FRT_FFN_PAIR", raising=False)
-    c_pair = run(plan, A, B, 2, 1)
+    c_pair = run(plan, A, B, 2, splits)
     assert np.array_equal(c_single, c_pair)
