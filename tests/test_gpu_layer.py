@@ -31,6 +31,12 @@ SHAPES = [
     WL["long_prefill"].with_(name="prefill_small", M=257, d=640, ff=1280, L=1),
     # gate/up K beyond the stage ring with few tiles: gated split-K epilogue
     WL["tiny"].with_(name="gu_split", M=32, d=2048, ff=1024, n_calib=1, seed=13),
+    # ragged shapes: 3-way gated and 5-way plain cluster split-K, odd K-block counts
+    WL["tiny"].with_(name="m17_odd", M=17, d=384, ff=640, n_calib=1, seed=14),
+    WL["tiny"].with_(name="m3_swiglu", M=3, d=768, ff=1152, act=synthetic.SWIGLU, outliers=False, n_calib=1,
+                     seed=15),
+    # two token tiles: CTA pairs with split-K on both GEMMs
+    WL["tiny"].with_(name="m130_pairs", M=130, d=512, ff=1024, n_calib=1, seed=16),
 ]
 
 
