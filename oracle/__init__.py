@@ -163,6 +163,32 @@ def quantize_layer_weights(w_gate, w_up, w_down):
     return q_gu, s_gu, q_d, s_d
 
 
+BF16_ONE = 0x3F80
+
+
+def fold_norm_weight(w_gate, w_up, w_norm) -> np.ndarray:
+    """The RMSNorm weight folded into the gate/up weights (itsolotime
+    article, 5.2: the Pi0 spec's FusedGateUp(..., norm_fuse=...) ahead of
+    Quant()): W'[j][k] = W[j][k] * w[k] over [W_gate; W_up], fp32.  The
+    product of two BF16 values has at most 16 significant bits, so it is
+    exact in fp32 (reading: the fold happens on the BF16 checkpoint tensors,
+    before quantisation, with no rounding of its own)."""
+    w_gu = bf16_decode(np.concatenate([_u16(w_gate), _u16(w_up)], axis=0))
+    return (w_gu * bf16_decode(w_norm)[None, :]).astype(np.float32)
+
+
+def quantize_layer_weights_folded(w_gate, w_up, w_down, w_norm):
+    """Step A0 with the norm weight folded into [W_gate; W_up]: one scale
+    over the folded fp32 matrix (amax / 448, the same rule as every weight),
+    codes E4M3(W' * (1/s)); W_down as without the fold.  The layer's norm
+    then multiplies by ones (the weight now lives in the GEMM)."""
+    w_f = fold_norm_weight(w_gate, w_up, w_norm)
+    s_gu = scale_from_amax(amax_f32(w_f))
+    q_gu = quantize_f32(w_f, recip(s_gu))
+    q_d, s_d = quantize_weight(w_down)
+    return q_gu, s_gu, q_d, s_d
+
+
 def residual_rmsnorm(r, h, w_norm, eps: float = EPS):
     """Step A1 before quantisation -> (r' BF16 bits, y fp32)."""
     r = _u16(r)
@@ -305,12 +331,19 @@ class QuantLayer:
     s_d: float
 
 
-def quantize_stack(layers) -> list[QuantLayer]:
-    """Step A0 over a list of dicts with w_norm, w_gate, w_up, w_down (BF16 bits)."""
+def quantize_stack(layers, fold_norm: bool = False) -> list[QuantLayer]:
+    """Step A0 over a list of dicts with w_norm, w_gate, w_up, w_down (BF16
+    bits); fold_norm: the norm weight folded into the gate/up weights."""
     out = []
     for lw in layers:
-        q_gu, s_gu, q_d, s_d = quantize_layer_weights(lw["w_gate"], lw["w_up"], lw["w_down"])
-        out.append(QuantLayer(_u16(lw["w_norm"]), q_gu, s_gu, q_d, s_d))
+        if fold_norm:
+            q_gu, s_gu, q_d, s_d = quantize_layer_weights_folded(lw["w_gate"], lw["w_up"], lw["w_down"],
+                                                                 lw["w_norm"])
+            w_norm = np.full(_u16(lw["w_norm"]).shape, BF16_ONE, dtype=np.uint16)
+        else:
+            q_gu, s_gu, q_d, s_d = quantize_layer_weights(lw["w_gate"], lw["w_up"], lw["w_down"])
+            w_norm = _u16(lw["w_norm"])
+        out.append(QuantLayer(w_norm, q_gu, s_gu, q_d, s_d))
     return out
 
 
