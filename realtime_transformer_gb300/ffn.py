@@ -8,12 +8,11 @@ a key made of a hash of the weights and the token count ("{hash}_Se{M}.json").
 from __future__ import annotations
 
 import hashlib
-import json
-import os
 
 import torch
 
 from . import _native as N
+from . import calibration
 
 ACTS = {"geglu_tanh": N.FRT_ACT_GEGLU_TANH, "swiglu": N.FRT_ACT_SWIGLU}
 
@@ -83,30 +82,38 @@ class FFNPlan:
         N.frt_ffn_set_scales(self.handle, list(map(float, s_x)), list(map(float, s_h)))
 
     # -- calibration cache ---------------------------------------------------
+    def _shape(self):
+        return {"d": self.d, "ff": self.ff, "act": self.act, "n_layers": self.n_layers}
+
     def cache_key(self, M: int) -> str:
-        h = hashlib.sha256()
-        h.update(json.dumps([self.d, self.ff, self.act, self.n_layers]).encode())
-        for dg in self._digest:
-            h.update((dg or "").encode())
-        return "%s_Se%d" % (h.hexdigest()[:16], M)
+        """"{hash}_Se{M}": hash of the shape and the loaded weights."""
+        return calibration.cache_key(calibration.checkpoint_hash(self._shape(), self._digest), M)
 
-    def save_scales(self, directory: str, M: int) -> str:
-        os.makedirs(directory, exist_ok=True)
-        path = os.path.join(directory, self.cache_key(M) + ".json")
+    def save_scales(self, directory: str | None, M: int, extra: dict | None = None) -> str:
+        """Save the plan's scales for token count M; returns the file path."""
+        rec = calibration.make_record(self._shape(), M, self.scales(), extra)
+        return calibration.save(directory or calibration.default_dir(), self.cache_key(M), rec)
+
+    def load_scales(self, directory: str | None, M: int) -> dict | None:
+        """Set the scales cached for M, if a record matching this plan's
+        shape and weight scales exists; returns the record (None: miss)."""
         sc = self.scales()
-        with open(path, "w") as f:
-            json.dump({"s_x": sc["s_x"], "s_h": sc["s_h"], "extra": {"s_gu": sc["s_gu"], "s_down": sc["s_down"]}},
-                      f)
-        return path
+        rec = calibration.load(directory or calibration.default_dir(), self.cache_key(M), self._shape(), M,
+                               {"s_gu": sc["s_gu"], "s_down": sc["s_down"]})
+        if rec is not None:
+            self.set_scales(rec["s_x"], rec["s_h"])
+        return rec
 
-    def load_scales(self, directory: str, M: int) -> bool:
-        path = os.path.join(directory, self.cache_key(M) + ".json")
-        if not os.path.exists(path):
-            return False
-        with open(path) as f:
-            js = json.load(f)
-        self.set_scales(js["s_x"], js["s_h"])
-        return True
+    def calibrate_cached(self, residuals, hiddens=None, directory: str | None = None, extra: dict | None = None,
+                         stream=None) -> bool:
+        """Cache hit: load the scales.  Miss: calibrate on the batches and
+        save them.  Returns True on a hit."""
+        M = residuals[0].shape[0]
+        if self.load_scales(directory, M) is not None:
+            return True
+        self.calibrate(residuals, hiddens, stream)
+        self.save_scales(directory, M, extra)
+        return False
 
     # -- forward -------------------------------------------------------------
     def forward(self, residual, hidden=None, out=None, stream=None):
@@ -123,6 +130,14 @@ class FFNPlan:
         N.frt_ffn_graph_capture(self.handle, _bf16(residual, (M, self.d), "residual"),
                                 _bf16(hidden, (M, self.d), "hidden") if hidden is not None else None,
                                 _bf16(out, (M, self.d), "out"), M, _stream(stream))
+
+    def graph_autotune(self, residual, hidden, out, stream, n_tries=3, n_replays=20):
+        """Capture n_tries times, keep the fastest capture (median of
+        n_replays timed replays each); returns its replay time in us."""
+        M = residual.shape[0]
+        return N.frt_ffn_graph_autotune(self.handle, _bf16(residual, (M, self.d), "residual"),
+                                        _bf16(hidden, (M, self.d), "hidden") if hidden is not None else None,
+                                        _bf16(out, (M, self.d), "out"), M, n_tries, n_replays, _stream(stream))
 
     def graph_replay(self, M: int, stream=None):
         N.frt_ffn_graph_replay(self.handle, M, _stream(stream))
