@@ -97,6 +97,23 @@ frt_status frt_ffn_plan_destroy(frt_ffn_plan_t plan);
 frt_status frt_ffn_load_weights(frt_ffn_plan_t plan, int layer, const void *w_norm, const void *w_gate,
                                 const void *w_up, const void *w_down, frt_stream_t stream);
 
+/* Flags of frt_ffn_load_weights_ex. */
+#define FRT_LOAD_FOLD_NORM 1u
+
+/*
+ * frt_ffn_load_weights with options.  flags 0: the same.  FRT_LOAD_FOLD_NORM
+ * (itsolotime article, 5.2: the Pi0 spec folds the RMSNorm weight into the
+ * fused gate/up weights; the Pi0.5 spec does not): the gate/up weights are
+ * quantised as W'[j][k] = W[j][k] * w_norm[k] (the fp32 product of two BF16
+ * values, exact), s_gu = amax(W') / 448, and the layer's norm multiplies by
+ * ones; the layer computes the same function up to quantisation, with the
+ * norm weight inside the GEMM.  Activation scales measured without the fold
+ * do not apply to a folded layer: calibrate (or set scales) after loading.
+ * Errors: as frt_ffn_load_weights; INVALID_ARG for unknown flags.
+ */
+frt_status frt_ffn_load_weights_ex(frt_ffn_plan_t plan, int layer, const void *w_norm, const void *w_gate,
+                                   const void *w_up, const void *w_down, unsigned flags, frt_stream_t stream);
+
 /*
  * Step A6 ("FlashRT docs/architecture.md", 6 Calibration Framework: amax per
  * FP8 GEMM input; "What happens when you call model.predict": run one
@@ -150,6 +167,21 @@ frt_status frt_ffn_graph_capture(frt_ffn_plan_t plan, const void *residual_in, c
  * Errors: CAPTURE (no graph for M), STALE_GRAPH (scales changed since the
  * capture), CUDA. */
 frt_status frt_ffn_graph_replay(frt_ffn_plan_t plan, int M, frt_stream_t stream);
+
+/*
+ * Tactic-stable capture ("FlashRT docs/architecture.md", 7 Graph: re-capture
+ * up to N times and keep the fastest schedule).  Captures the forward for M
+ * n_tries times as frt_ffn_graph_capture does, times n_replays replays of each
+ * capture (CUDA events on `stream`, each replay timed alone, after one untimed
+ * replay; the median counts), and keeps the fastest capture as the plan's
+ * graph for M.  The timed replays run the forward, so `out` holds its result
+ * afterwards.  *best_us (may be NULL) receives the kept graph's median replay
+ * time in microseconds.  Synchronises `stream`.  1 <= n_tries <= 64,
+ * 1 <= n_replays <= 10000.  Errors: as frt_ffn_graph_capture, INVALID_ARG for
+ * the counts, CUDA for a failed replay or timing.
+ */
+frt_status frt_ffn_graph_autotune(frt_ffn_plan_t plan, const void *residual_in, const void *hidden_in, void *out,
+                                  int M, int n_tries, int n_replays, float *best_us, frt_stream_t stream);
 
 /*
  * Test/diagnostic: run layer `layer` alone on residual_in (+ hidden_in if not

@@ -31,12 +31,14 @@ SIGNATURES = {
     "frt_ffn_plan_create": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(_P)]),
     "frt_ffn_plan_destroy": (_I, [_P]),
     "frt_ffn_load_weights": (_I, [_P, _I, _P, _P, _P, _P, _P]),
+    "frt_ffn_load_weights_ex": (_I, [_P, _I, _P, _P, _P, _P, ctypes.c_uint, _P]),
     "frt_ffn_calibrate": (_I, [_P, ctypes.POINTER(_P), ctypes.POINTER(_P), _I, _I, _P]),
     "frt_ffn_get_scales": (_I, [_P, _FP, _FP, _FP, _FP]),
     "frt_ffn_set_scales": (_I, [_P, _FP, _FP]),
     "frt_ffn_forward": (_I, [_P, _P, _P, _P, _I, _P]),
     "frt_ffn_graph_capture": (_I, [_P, _P, _P, _P, _I, _P]),
     "frt_ffn_graph_replay": (_I, [_P, _I, _P]),
+    "frt_ffn_graph_autotune": (_I, [_P, _P, _P, _P, _I, _I, _I, ctypes.POINTER(ctypes.c_float), _P]),
     "frt_ffn_debug_trace": (_I, [_P, _I, _P, _P, _I, _P, _P, _P, _P, _P, _P]),
     "frt_ffn_device_status": (_I, [_P, _P]),
     "frt_ffn_debug_stall": (_I, [_P, _P]),
@@ -99,6 +101,13 @@ def frt_ffn_load_weights(plan, layer, w_norm, w_gate, w_up, w_down, stream) -> N
     _check(lib().frt_ffn_load_weights(plan, layer, w_norm, w_gate, w_up, w_down, stream))
 
 
+FRT_LOAD_FOLD_NORM = 1
+
+
+def frt_ffn_load_weights_ex(plan, layer, w_norm, w_gate, w_up, w_down, flags, stream) -> None:
+    _check(lib().frt_ffn_load_weights_ex(plan, layer, w_norm, w_gate, w_up, w_down, flags, stream))
+
+
 def frt_ffn_calibrate(plan, residual_ptrs, hidden_ptrs, M, stream) -> None:
     n = len(residual_ptrs)
     r = _ptrs(residual_ptrs)
@@ -130,6 +139,13 @@ def frt_ffn_graph_capture(plan, residual_in, hidden_in, out, M, stream) -> None:
 
 def frt_ffn_graph_replay(plan, M, stream) -> None:
     _check(lib().frt_ffn_graph_replay(plan, M, stream))
+
+
+def frt_ffn_graph_autotune(plan, residual_in, hidden_in, out, M, n_tries, n_replays, stream) -> float:
+    best = ctypes.c_float(0.0)
+    _check(lib().frt_ffn_graph_autotune(plan, residual_in, hidden_in, out, M, n_tries, n_replays,
+                                        ctypes.byref(best), stream))
+    return best.value
 
 
 def frt_ffn_debug_trace(plan, layer, residual_in, hidden_in, M, r_prime, q_x, gu, q_h, out, stream) -> None:

@@ -17,6 +17,7 @@
 // stored interleaved in 64-row blocks so one tile holds matching rows).
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -411,8 +412,17 @@ FRT_API frt_status frt_ffn_plan_destroy(frt_ffn_plan_t P) {
 
 FRT_API frt_status frt_ffn_load_weights(frt_ffn_plan_t P, int layer, const void *w_norm, const void *w_gate,
                                         const void *w_up, const void *w_down, frt_stream_t stream) {
+    return frt_ffn_load_weights_ex(P, layer, w_norm, w_gate, w_up, w_down, 0u, stream);
+}
+
+FRT_API frt_status frt_ffn_load_weights_ex(frt_ffn_plan_t P, int layer, const void *w_norm, const void *w_gate,
+                                           const void *w_up, const void *w_down, unsigned flags,
+                                           frt_stream_t stream) {
     if (!P)
         return fail(FRT_ERR_INVALID_ARG, "null plan");
+    if (flags & ~(unsigned)FRT_LOAD_FOLD_NORM)
+        return fail(FRT_ERR_INVALID_ARG, "unknown load flags 0x%x", flags);
+    const bool fold = (flags & FRT_LOAD_FOLD_NORM) != 0;
     if (layer < 0 || layer >= P->L)
         return fail(FRT_ERR_INVALID_ARG, "layer %d out of range [0, %d)", layer, P->L);
     if (!w_norm || !w_gate || !w_up || !w_down)
@@ -423,11 +433,20 @@ FRT_API frt_status frt_ffn_load_weights(frt_ffn_plan_t P, int layer, const void 
     const size_t D = P->d, F = P->ff;
     uint8_t *gu_dst = P->w_gu + (size_t)layer * 2 * F * D;
     uint8_t *d_dst = P->w_down + (size_t)layer * D * F;
-    CK(cudaMemcpyAsync(P->w_norm + (size_t)layer * D, w_norm, D * 2, cudaMemcpyDeviceToDevice, s));
+    // folded: the norm weight moves into the gate/up weights and the norm
+    // multiplies by ones (BF16 1.0 = 0x3F80)
+    const std::vector<uint16_t> ones(fold ? D : 0, (uint16_t)0x3F80);
+    CK(cudaMemcpyAsync(P->w_norm + (size_t)layer * D, fold ? (const void *)ones.data() : w_norm, D * 2,
+                       fold ? cudaMemcpyHostToDevice : cudaMemcpyDeviceToDevice, s));
     // one scale for [W_gate; W_up], one for W_down
     CK(cudaMemsetAsync(P->amax, 0, 8, s));
-    CK(launch_amax_bf16(w_gate, F * D, P->amax, s));
-    CK(launch_amax_bf16(w_up, F * D, P->amax, s));
+    if (fold) {
+        CK(launch_amax_fold(w_gate, F, (int)D, w_norm, P->amax, s));
+        CK(launch_amax_fold(w_up, F, (int)D, w_norm, P->amax, s));
+    } else {
+        CK(launch_amax_bf16(w_gate, F * D, P->amax, s));
+        CK(launch_amax_bf16(w_up, F * D, P->amax, s));
+    }
     CK(launch_amax_bf16(w_down, D * F, P->amax + 1, s));
     unsigned h_amax[2];
     CK(cudaMemcpyAsync(h_amax, P->amax, 8, cudaMemcpyDeviceToHost, s));
@@ -436,7 +455,7 @@ FRT_API frt_status frt_ffn_load_weights(frt_ffn_plan_t P, int layer, const void 
     memcpy(&a_gu, &h_amax[0], 4);
     memcpy(&a_d, &h_amax[1], 4);
     const float s_gu = scale_from_amax(a_gu), s_d = scale_from_amax(a_d);
-    CK(launch_quant_gu_interleave(w_gate, w_up, (int)F, (int)D, 1.0f / s_gu, gu_dst, s));
+    CK(launch_quant_gu_interleave(w_gate, w_up, (int)F, (int)D, fold ? w_norm : nullptr, 1.0f / s_gu, gu_dst, s));
     CK(launch_quant_bf16(w_down, D * F, 1.0f / s_d, d_dst, s));
     CK(cudaStreamSynchronize(s));
     P->s_gu[layer] = s_gu;
@@ -580,8 +599,11 @@ FRT_API frt_status frt_ffn_forward(frt_ffn_plan_t P, const void *residual_in, co
     return run_stack(P, residual_in, hidden_in, out, M, static_cast<cudaStream_t>(stream));
 }
 
-FRT_API frt_status frt_ffn_graph_capture(frt_ffn_plan_t P, const void *residual_in, const void *hidden_in,
-                                         void *out, int M, frt_stream_t stream) {
+namespace {
+
+// Checks shared by the capturing entry points.
+frt_status capture_checks(frt_ffn_plan *P, const void *residual_in, const void *hidden_in, void *out, int M,
+                          cudaStream_t s) {
     frt_status st = check_io(P, residual_in, hidden_in, out, M);
     if (st != FRT_OK)
         return st;
@@ -589,7 +611,6 @@ FRT_API frt_status frt_ffn_graph_capture(frt_ffn_plan_t P, const void *residual_
         return st;
     if (M == 0)
         return fail(FRT_ERR_INVALID_ARG, "cannot capture M == 0");
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (s == nullptr)
         return fail(FRT_ERR_CAPTURE, "capture needs a non-default stream");
     cudaStreamCaptureStatus cs;
@@ -602,8 +623,14 @@ FRT_API frt_status frt_ffn_graph_capture(frt_ffn_plan_t P, const void *residual_
         if ((st = setup_gemm(P, g, site, 0, M)) != FRT_OK)
             return st;
     }
+    return FRT_OK;
+}
+
+// Capture the stack for M on s and instantiate it into ge.
+frt_status capture_one(frt_ffn_plan *P, const void *residual_in, const void *hidden_in, void *out, int M,
+                       cudaStream_t s, GraphEntry &ge) {
     CK(cudaStreamBeginCapture(s, cudaStreamCaptureModeRelaxed));
-    st = run_stack(P, residual_in, hidden_in, out, M, s);
+    frt_status st = run_stack(P, residual_in, hidden_in, out, M, s);
     cudaGraph_t graph = nullptr;
     cudaError_t e = cudaStreamEndCapture(s, &graph);
     if (st != FRT_OK) {
@@ -618,16 +645,103 @@ FRT_API frt_status frt_ffn_graph_capture(frt_ffn_plan_t P, const void *residual_
         cudaGraphDestroy(graph);
         return fail(FRT_ERR_CAPTURE, "cudaGraphInstantiate: %s", cudaGetErrorString(e));
     }
-    auto it = P->graphs.find(M);
-    if (it != P->graphs.end()) {
-        cudaGraphExecDestroy(it->second.exec);
-        cudaGraphDestroy(it->second.graph);
-    }
-    GraphEntry ge;
     ge.graph = graph;
     ge.exec = exec;
     ge.version = P->version;
+    return FRT_OK;
+}
+
+void destroy_graph(GraphEntry &ge) {
+    if (ge.exec) cudaGraphExecDestroy(ge.exec);
+    if (ge.graph) cudaGraphDestroy(ge.graph);
+    ge.exec = nullptr;
+    ge.graph = nullptr;
+}
+
+// Keep ge as the plan's graph for M, releasing the one it replaces.
+void install_graph(frt_ffn_plan *P, int M, const GraphEntry &ge) {
+    auto it = P->graphs.find(M);
+    if (it != P->graphs.end())
+        destroy_graph(it->second);
     P->graphs[M] = ge;
+}
+
+// Median duration in microseconds of n replays of exec on s, each timed
+// alone with events on s after one untimed replay.
+frt_status time_replays(cudaGraphExec_t exec, int n, cudaStream_t s, float *median_us) {
+    cudaEvent_t ev[2];
+    CK(cudaEventCreate(&ev[0]));
+    cudaError_t e = cudaEventCreate(&ev[1]);
+    if (e != cudaSuccess) {
+        cudaEventDestroy(ev[0]);
+        return cuda_fail(e, "cudaEventCreate");
+    }
+    std::vector<float> t;
+    e = cudaGraphLaunch(exec, s);
+    for (int i = 0; i < n && e == cudaSuccess; ++i) {
+        float ms = 0.0f;
+        if ((e = cudaEventRecord(ev[0], s)) != cudaSuccess) break;
+        if ((e = cudaGraphLaunch(exec, s)) != cudaSuccess) break;
+        if ((e = cudaEventRecord(ev[1], s)) != cudaSuccess) break;
+        if ((e = cudaEventSynchronize(ev[1])) != cudaSuccess) break;
+        if ((e = cudaEventElapsedTime(&ms, ev[0], ev[1])) != cudaSuccess) break;
+        t.push_back(ms * 1000.0f);
+    }
+    cudaEventDestroy(ev[0]);
+    cudaEventDestroy(ev[1]);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "timing graph replays");
+    std::sort(t.begin(), t.end());
+    *median_us = t[t.size() / 2];
+    return FRT_OK;
+}
+
+}  // namespace
+
+FRT_API frt_status frt_ffn_graph_capture(frt_ffn_plan_t P, const void *residual_in, const void *hidden_in,
+                                         void *out, int M, frt_stream_t stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    frt_status st = capture_checks(P, residual_in, hidden_in, out, M, s);
+    if (st != FRT_OK)
+        return st;
+    GraphEntry ge;
+    if ((st = capture_one(P, residual_in, hidden_in, out, M, s, ge)) != FRT_OK)
+        return st;
+    install_graph(P, M, ge);
+    return FRT_OK;
+}
+
+FRT_API frt_status frt_ffn_graph_autotune(frt_ffn_plan_t P, const void *residual_in, const void *hidden_in,
+                                          void *out, int M, int n_tries, int n_replays, float *best_us,
+                                          frt_stream_t stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (n_tries < 1 || n_tries > 64 || n_replays < 1 || n_replays > 10000)
+        return fail(FRT_ERR_INVALID_ARG, "need 1 <= n_tries <= 64 and 1 <= n_replays <= 10000");
+    frt_status st = capture_checks(P, residual_in, hidden_in, out, M, s);
+    if (st != FRT_OK)
+        return st;
+    GraphEntry best;
+    float best_t = 0.0f;
+    for (int i = 0; i < n_tries; ++i) {
+        GraphEntry ge;
+        float t = 0.0f;
+        if ((st = capture_one(P, residual_in, hidden_in, out, M, s, ge)) != FRT_OK ||
+            (st = time_replays(ge.exec, n_replays, s, &t)) != FRT_OK) {
+            destroy_graph(ge);
+            destroy_graph(best);
+            return st;
+        }
+        if (!best.exec || t < best_t) {
+            destroy_graph(best);
+            best = ge;
+            best_t = t;
+        } else {
+            destroy_graph(ge);
+        }
+    }
+    install_graph(P, M, best);
+    if (best_us)
+        *best_us = best_t;
     return FRT_OK;
 }
 

@@ -87,8 +87,9 @@ cudaError_t launch_gemm(const GemmLaunch &g, cudaStream_t s, bool pdl);
 
 cudaError_t launch_amax_bf16(const void *x, size_t n, unsigned *amax_word, cudaStream_t s);
 cudaError_t launch_quant_bf16(const void *x, size_t n, float inv_s, uint8_t *q, cudaStream_t s);
-cudaError_t launch_quant_gu_interleave(const void *gate, const void *up, int ff, int d, float inv_s, uint8_t *dst,
-                                      cudaStream_t s);
+cudaError_t launch_quant_gu_interleave(const void *gate, const void *up, int ff, int d, const void *fold,
+                                      float inv_s, uint8_t *dst, cudaStream_t s);
+cudaError_t launch_amax_fold(const void *x, size_t rows, int d, const void *w, unsigned *amax_word, cudaStream_t s);
 cudaError_t launch_norm_quant(const void *r, const void *h, const void *w, int M, int d, float eps, float inv_s,
                               void *rprime, uint8_t *qx, unsigned *amax_word, bool measure, cudaStream_t s,
                               bool pdl);

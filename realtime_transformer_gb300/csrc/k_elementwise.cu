@@ -112,12 +112,35 @@ __global__ void k_quant_bf16(const uint4 *__restrict__ x, size_t nvec, const uin
     }
 }
 
+// amax of W[j][k] * w[k] over a [rows, d] BF16 matrix: the RMSNorm weight
+// w folded into the gate/up weights (itsolotime article, 5.2, the Pi0 spec's
+// norm_fuse).  A BF16 x BF16 product is exact in fp32.  d % 8 == 0.
+__global__ void k_amax_fold(const uint4 *__restrict__ x, size_t rows, int d, const uint4 *__restrict__ w,
+                            unsigned *amax_word) {
+    const size_t vpr = (size_t)d / 8;
+    const size_t nvec = rows * vpr;
+    float m = 0.0f;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < nvec; i += (size_t)gridDim.x * blockDim.x) {
+        float f[8], c[8];
+        unpack8(__ldg(x + i), f);
+        unpack8(__ldg(w + i % vpr), c);
+#pragma unroll
+        for (int j = 0; j < 8; j++)
+            m = fmaxf(m, fabsf(__fmul_rn(f[j], c[j])));
+    }
+    m = warp_max(m);
+    if ((threadIdx.x & 31) == 0)
+        atomic_amax(amax_word, m);
+}
+
 // [W_gate; W_up] quantised into the interleaved arena layout: blocks of 128
 // rows, each 64 gate rows followed by the 64 up rows of the same features,
-// so that one GEMM tile holds matching gate and up rows.  d % 8 == 0,
-// ff % 64 == 0.
+// so that one GEMM tile holds matching gate and up rows.  With fold != null
+// every column k is first multiplied by fold[k] (the norm weight, exact in
+// fp32).  d % 8 == 0, ff % 64 == 0.
 __global__ void k_quant_gu_interleave(const uint16_t *__restrict__ gate, const uint16_t *__restrict__ up, int ff,
-                                      int d, float inv_s, uint8_t *__restrict__ dst) {
+                                      int d, const uint16_t *__restrict__ fold, float inv_s,
+                                      uint8_t *__restrict__ dst) {
     const size_t vpr = (size_t)d / 8;
     const size_t total = (size_t)2 * ff * vpr;
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
@@ -128,6 +151,13 @@ __global__ void k_quant_gu_interleave(const uint16_t *__restrict__ gate, const u
         const uint16_t *src = (within < 64 ? gate : up) + srow * d + v * 8;
         float f[8];
         unpack8(__ldg(reinterpret_cast<const uint4 *>(src)), f);
+        if (fold) {
+            float c[8];
+            unpack8(__ldg(reinterpret_cast<const uint4 *>(fold + v * 8)), c);
+#pragma unroll
+            for (int j = 0; j < 8; j++)
+                f[j] = __fmul_rn(f[j], c[j]);
+        }
 #pragma unroll
         for (int j = 0; j < 8; j++)
             f[j] = __fmul_rn(f[j], inv_s);
@@ -352,15 +382,27 @@ cudaError_t launch_quant_bf16(const void *x, size_t n, float inv_s, uint8_t *q, 
     return cudaGetLastError();
 }
 
-cudaError_t launch_quant_gu_interleave(const void *gate, const void *up, int ff, int d, float inv_s, uint8_t *dst,
-                                      cudaStream_t s) {
+cudaError_t launch_quant_gu_interleave(const void *gate, const void *up, int ff, int d, const void *fold,
+                                      float inv_s, uint8_t *dst, cudaStream_t s) {
     const size_t total = (size_t)2 * ff * (d / 8);
     size_t blocks = (total + 255) / 256;
     const size_t cap = (size_t)sm_count() * 8;
     if (blocks > cap) blocks = cap;
     if (blocks == 0) blocks = 1;
     k_quant_gu_interleave<<<(unsigned)blocks, 256, 0, s>>>(static_cast<const uint16_t *>(gate),
-                                                            static_cast<const uint16_t *>(up), ff, d, inv_s, dst);
+                                                            static_cast<const uint16_t *>(up), ff, d,
+                                                            static_cast<const uint16_t *>(fold), inv_s, dst);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_amax_fold(const void *x, size_t rows, int d, const void *w, unsigned *amax_word, cudaStream_t s) {
+    const size_t nvec = rows * (size_t)(d / 8);
+    size_t blocks = (nvec + 255) / 256;
+    const size_t cap = (size_t)sm_count() * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks == 0) blocks = 1;
+    k_amax_fold<<<(unsigned)blocks, 256, 0, s>>>(static_cast<const uint4 *>(x), rows, d,
+                                                  static_cast<const uint4 *>(w), amax_word);
     return cudaGetLastError();
 }
 

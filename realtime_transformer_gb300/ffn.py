@@ -58,12 +58,15 @@ class FFNPlan:
             pass
 
     # -- weights / scales --------------------------------------------------
-    def load_weights(self, layer, w_norm, w_gate, w_up, w_down, stream=None):
+    def load_weights(self, layer, w_norm, w_gate, w_up, w_down, stream=None, fold_norm=False):
+        """Quantise one layer's BF16 weights into the plan; fold_norm: fold
+        the RMSNorm weight into the gate/up weights (the Pi0 layout)."""
         d, ff = self.d, self.ff
-        N.frt_ffn_load_weights(self.handle, layer, _bf16(w_norm, (d,), "w_norm"),
-                               _bf16(w_gate, (ff, d), "w_gate"), _bf16(w_up, (ff, d), "w_up"),
-                               _bf16(w_down, (d, ff), "w_down"), _stream(stream))
-        h = hashlib.sha256()
+        N.frt_ffn_load_weights_ex(self.handle, layer, _bf16(w_norm, (d,), "w_norm"),
+                                  _bf16(w_gate, (ff, d), "w_gate"), _bf16(w_up, (ff, d), "w_up"),
+                                  _bf16(w_down, (d, ff), "w_down"), N.FRT_LOAD_FOLD_NORM if fold_norm else 0,
+                                  _stream(stream))
+        h = hashlib.sha256(b"fold" if fold_norm else b"plain")
         for t in (w_norm, w_gate, w_up, w_down):
             h.update(t.reshape(-1)[:: max(1, t.numel() // 4096)].contiguous().view(torch.int16).cpu().numpy().tobytes())
         self._digest[layer] = h.hexdigest()

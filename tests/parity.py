@@ -80,20 +80,23 @@ class Case:
     """One workload: seeded weights/inputs, oracle-quantised weights and
     oracle-calibrated scales, and a loaded GPU plan."""
 
-    def __init__(self, wl, device="cuda", gen_device="cpu", M_max=None, calib_rows=None):
+    def __init__(self, wl, device="cuda", gen_device="cpu", M_max=None, calib_rows=None, fold_norm=False):
         from realtime_transformer_gb300.ffn import FFNPlan
         self.wl = wl
+        self.fold = fold_norm
         self.dev = torch.device(device)
         self.weights = [synthetic.layer_weights(wl, l, device=gen_device) for l in range(wl.L)]
         self.r, self.h = synthetic.inputs(wl, device=gen_device)
         self.calib = synthetic.calibration_batches(wl, device=gen_device)
-        self.q = oracle.quantize_stack([{k: bits(v) for k, v in w.items()} for w in self.weights])
+        self.q = oracle.quantize_stack([{k: bits(v) for k, v in w.items()} for w in self.weights],
+                                       fold_norm=fold_norm)
         rows = slice(None) if calib_rows is None else slice(0, calib_rows)
         self.s_x, self.s_h = oracle.calibrate_stack(self.q, [bits(a[rows]) for a, _ in self.calib],
                                                     [bits(b[rows]) for _, b in self.calib], wl.act_id)
         self.plan = FFNPlan(wl.d, wl.ff, wl.act, M_max or wl.M, wl.L)
         for l, w in enumerate(self.weights):
-            self.plan.load_weights(l, *(w[k].to(self.dev) for k in ("w_norm", "w_gate", "w_up", "w_down")))
+            self.plan.load_weights(l, *(w[k].to(self.dev) for k in ("w_norm", "w_gate", "w_up", "w_down")),
+                                   fold_norm=fold_norm)
         self.plan.set_scales(self.s_x, self.s_h)
 
     def oracle_forward(self, rows=None, trace=False):

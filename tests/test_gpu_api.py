@@ -1,6 +1,8 @@
 """Boundary behaviour of the C ABI on the GPU: status codes, stale graphs,
 empty and oversized inputs, misaligned pointers ("FlashRT
 docs/architecture.md", 7: pointer-only forward, graphs with baked alpha)."""
+import os
+
 import pytest
 import torch
 
@@ -90,3 +92,58 @@ def test_smaller_M_than_M_max_and_repeat_calls(loaded):
     torch.cuda.synchronize()
     assert torch.equal(full[:3], part)
     assert torch.equal(full, again)
+
+
+def test_graph_autotune_keeps_a_working_graph(loaded):
+    """Tactic-stable capture: several captures, the fastest kept; its replay
+    computes the forward, and it goes stale like a plain capture."""
+    plan, r, h = loaded
+    plan.set_scales([0.02], [0.003])
+    out = torch.empty_like(r)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        best = plan.graph_autotune(r, h, out, s, n_tries=3, n_replays=5)
+        out.zero_()
+        plan.graph_replay(r.shape[0], s)
+    s.synchronize()
+    assert 0.0 < best < 1e5
+    ref = plan.forward(r, h)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+    assert status_of(plan.graph_autotune, r, h, out, s, 0, 5) == "FRT_ERR_INVALID_ARG"
+    plan.set_scales([0.02], [0.003])
+    assert status_of(plan.graph_replay, r.shape[0], s) == "FRT_ERR_STALE_GRAPH"
+
+
+def test_calibration_cache_hit_and_miss(tmp_path):
+    """First plan: cache miss, calibrates and saves; a second plan with the
+    same weights: hit, the same scales and the same output; other weights:
+    another key, a miss."""
+    wl = synthetic.WORKLOADS["tiny"]
+    dev = torch.device("cuda")
+    r, h = synthetic.inputs(wl, device=dev)
+    cb = synthetic.calibration_batches(wl, device=dev)
+    res, hid = [x for x, _ in cb], [y for _, y in cb]
+
+    def make(seed_layer):
+        p = FFNPlan(wl.d, wl.ff, wl.act, wl.M, 1)
+        w = synthetic.layer_weights(wl, seed_layer, device=dev)
+        p.load_weights(0, w["w_norm"], w["w_gate"], w["w_up"], w["w_down"])
+        return p
+
+    a = make(0)
+    assert a.calibrate_cached(res, hid, directory=str(tmp_path), extra={"source": "test"}) is False
+    assert os.listdir(tmp_path) == [a.cache_key(wl.M) + ".json"]
+    b = make(0)
+    assert b.cache_key(wl.M) == a.cache_key(wl.M)
+    assert b.calibrate_cached(res, hid, directory=str(tmp_path)) is True
+    assert a.scales() == b.scales()
+    ya, yb = a.forward(r, h), b.forward(r, h)
+    torch.cuda.synchronize()
+    assert torch.equal(ya, yb)
+    c = make(1)
+    assert c.cache_key(wl.M) != a.cache_key(wl.M)
+    assert c.calibrate_cached(res, hid, directory=str(tmp_path)) is False
+    assert len(os.listdir(tmp_path)) == 2
+    for p in (a, b, c):
+        p.close()

@@ -2,6 +2,10 @@
 ("FlashRT docs/architecture.md", 6 Calibration Framework and 7 CUDA Graph
 Capture; itsolotime FlashRT article, 4.1-4.2).
 
+Stacks with the RMSNorm weight folded into the gate/up weights (the Pi0
+layout, itsolotime article 5.2) run the same tests against the oracle's
+folded quantisation.
+
 Per-layer parity through the whole stack is teacher-forced: GPU layer l runs
 on the oracle's own layer-l input (oracle values may feed the GPU, never the
 reverse).  Free-running, the two pipelines round different elements across
@@ -22,14 +26,24 @@ pytestmark = pytest.mark.gpu
 WL = synthetic.WORKLOADS
 
 
-@pytest.fixture(scope="module", params=[WL["tiny"], WL["vla_action_expert"],
-                                        WL["tiny"].with_(name="deep_small", L=6, M=20, d=384, ff=1152,
-                                                         act=synthetic.SWIGLU, outliers=True, n_calib=2)],
-                ids=lambda w: w.name)
+# (workload, norm weight folded into the gate/up weights -- the Pi0 layout)
+@pytest.fixture(scope="module", params=[(WL["tiny"], False), (WL["vla_action_expert"], False),
+                                        (WL["tiny"].with_(name="deep_small", L=6, M=20, d=384, ff=1152,
+                                                          act=synthetic.SWIGLU, outliers=True, n_calib=2), False),
+                                        (WL["vla_action_expert"].with_(name="vla_ae", L=4), True),
+                                        (WL["vla_prefix"].with_(name="tiled", M=200, d=512, ff=1024, L=2), True)],
+                ids=lambda p: p[0].name + ("_folded" if p[1] else ""))
 def case(request):
-    c = Case(request.param)
+    c = Case(request.param[0], fold_norm=request.param[1])
     yield c
     c.close()
+
+
+def test_weight_scales_match_oracle_exactly(case):
+    sc = case.plan.scales()
+    for l, ql in enumerate(case.q):
+        assert sc["s_gu"][l] == np.float32(ql.s_gu)
+        assert sc["s_down"][l] == np.float32(ql.s_d)
 
 
 def test_every_layer_teacher_forced(case):
@@ -113,7 +127,7 @@ def test_calibration_teacher_forced_per_layer(case):
         ql = case.q[l]
         plan = FFNPlan(wl.d, wl.ff, wl.act, wl.M, 1)
         w = case.weights[l]
-        plan.load_weights(0, *(w[k].to(dev) for k in ("w_norm", "w_gate", "w_up", "w_down")))
+        plan.load_weights(0, *(w[k].to(dev) for k in ("w_norm", "w_gate", "w_up", "w_down")), fold_norm=case.fold)
         plan.calibrate([synthetic.from_bf16_bits(x, dev) for x in rb],
                        [synthetic.from_bf16_bits(x, dev) for x in hb] if l == 0 else None)
         sc = plan.scales()
