@@ -773,6 +773,8 @@ __device__ __forceinline__ float reduce_slice(const GemmParams &p, const Unit &w
                                               int span, const uint2 (&res0)[RED_Q]) {
     constexpr int NQ = GATED ? RED_Q_GATED : (SWAP ? RED_Q : RED_Q_TILED);
     constexpr int UP = SWAP ? BM / 2 : 64;  // offset of an element's up partner (gated)
+    // partials per batch (registers allowing)
+    constexpr int KU = (GATED ? 2 : 1) * NQ <= 4 ? 2 : 1;
     const int r = threadIdx.x;
     const int S = p.splits;
     const int epi = p.epi;
@@ -816,22 +818,39 @@ __device__ __forceinline__ float reduce_slice(const GemmParams &p, const Unit &w
                 }
             }
         }
+        // KU partials at a time: all their loads first, then the additions
+        // in split order (the same order for every KU)
 #pragma unroll 1
-        for (int k = 0; k < S; ++k) {
-            const float *rk = red + (size_t)k * span;
+        for (int k0 = 0; k0 < S; k0 += KU) {
+            float4 v[KU][NQ], uv[KU][NQ];
 #pragma unroll
-            for (int i = 0; i < NQ; ++i) {
-                const float4 v = *reinterpret_cast<const float4 *>(rk + ia[i]);
-                acc[i][0] = __fadd_rn(acc[i][0], v.x);
-                acc[i][1] = __fadd_rn(acc[i][1], v.y);
-                acc[i][2] = __fadd_rn(acc[i][2], v.z);
-                acc[i][3] = __fadd_rn(acc[i][3], v.w);
-                if (GATED) {
-                    const float4 u = *reinterpret_cast<const float4 *>(rk + ia[i] + UP);
-                    acc2[i][0] = __fadd_rn(acc2[i][0], u.x);
-                    acc2[i][1] = __fadd_rn(acc2[i][1], u.y);
-                    acc2[i][2] = __fadd_rn(acc2[i][2], u.z);
-                    acc2[i][3] = __fadd_rn(acc2[i][3], u.w);
+            for (int kk = 0; kk < KU; ++kk) {
+                if (k0 + kk < S) {
+                    const float *rk = red + (size_t)(k0 + kk) * span;
+#pragma unroll
+                    for (int i = 0; i < NQ; ++i) {
+                        v[kk][i] = *reinterpret_cast<const float4 *>(rk + ia[i]);
+                        if (GATED)
+                            uv[kk][i] = *reinterpret_cast<const float4 *>(rk + ia[i] + UP);
+                    }
+                }
+            }
+#pragma unroll
+            for (int kk = 0; kk < KU; ++kk) {
+                if (k0 + kk < S) {
+#pragma unroll
+                    for (int i = 0; i < NQ; ++i) {
+                        acc[i][0] = __fadd_rn(acc[i][0], v[kk][i].x);
+                        acc[i][1] = __fadd_rn(acc[i][1], v[kk][i].y);
+                        acc[i][2] = __fadd_rn(acc[i][2], v[kk][i].z);
+                        acc[i][3] = __fadd_rn(acc[i][3], v[kk][i].w);
+                        if (GATED) {
+                            acc2[i][0] = __fadd_rn(acc2[i][0], uv[kk][i].x);
+                            acc2[i][1] = __fadd_rn(acc2[i][1], uv[kk][i].y);
+                            acc2[i][2] = __fadd_rn(acc2[i][2], uv[kk][i].z);
+                            acc2[i][3] = __fadd_rn(acc2[i][3], uv[kk][i].w);
+                        }
+                    }
                 }
             }
         }
@@ -1086,7 +1105,7 @@ __device__ bool coop_cluster_unit(const GemmParams &p, const Unit &w, uint32_t t
     // 3. once every CTA of the cluster has freed its stages, send slice j of
     //    this partial to CTA j, into row k of its slice buffer; then wait for
     //    this CTA's slice from all S splits
-    //    (lane j of warp 0 copies to, and later reports to, CTA j)
+    //    (lane j of warp 0 copies to CTA j)
     if (threadIdx.x < 32) {
         const int lane = threadIdx.x;
         int ok = 1;
@@ -1102,11 +1121,6 @@ __device__ bool coop_cluster_unit(const GemmParams &p, const Unit &w, uint32_t t
         }
         if (ok && lane == 0)
             ok = mbar_wait_cluster(smem_u32(data_bar), 0, abort_f, p.err) ? 1 : 0;
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        // every copy into this CTA has landed, so every source may let its
-        // staging go
-        if (ok && lane < S && lane != k)
-            mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(sent_bar), (uint32_t)lane));
         if (lane == 0)
             *s_flag = ok;
     }
@@ -1121,8 +1135,9 @@ __device__ bool coop_cluster_unit(const GemmParams &p, const Unit &w, uint32_t t
         if ((threadIdx.x & 31) == 0)
             atomicMax(p.amax, __float_as_uint(m));
     }
-    // 5. the CTA may leave once every copy out of its staging has landed
-    //    (normally long done by now)
+    // 5. the CTA may leave once every copy out of its staging has landed (the
+    //    receivers' producer warps report it as soon as their data barrier
+    //    completes; normally long done by now)
     return threadIdx.x != 0 || mbar_wait_cluster(smem_u32(sent_bar), 0, abort_f, p.err);
 }
 
@@ -1294,8 +1309,22 @@ __global__ void __launch_bounds__(NTHREADS, SWAP ? 2 : 1)
         if (lane == 0)
             producer<BN, SWAP, PAIR>(mapP, mapQ, p, sP, sQ, full, empty, abort_f);
         __syncwarp();
-        if (p.cluster)
+        if (p.cluster) {
             cluster_wait();
+            if constexpr (SWAP) {
+                // Cluster split-K: once this CTA's slice of every split's
+                // partial has landed, tell each source CTA that its staging
+                // may go (it leaves only then).  The producer warp does this,
+                // off the epilogue's path to the reduction.
+                int ok = 0;
+                if (lane == 0)
+                    ok = mbar_wait_cluster(smem_u32(data_bar), 0, abort_f, p.err) ? 1 : 0;
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                const int k = decode(p, (int)blockIdx.x).split;  // == cluster rank
+                if (ok && lane < p.splits && lane != k)
+                    mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(sent_bar), (uint32_t)lane));
+            }
+        }
     } else {
         if (lane == 0 && (!PAIR || (blockIdx.x & 1u) == 0))
             mma_issuer<BN, SWAP, PAIR>(p, sP, sQ, full, empty, tfull, tempty, drain_bar, tmem_base, abort_f);
