@@ -87,6 +87,12 @@ struct Unit {
     int tp, tq, kb0, kb1, tile, split;
 };
 
+// Epilogue roles a kernel is compiled for: every epilogue (ROLE_ANY), or
+// only the one a launch of the layer uses -- the weight-streaming gated
+// epilogue without split-K (the gate/up GEMM) or the plain cluster split-K
+// epilogue (the down GEMM) -- so that the code a launch runs is compact.
+enum Role : int { ROLE_ANY = 0, ROLE_GATED_TILE = 1, ROLE_CLUSTER_PLAIN = 2 };
+
 // Tiles run in groups of p.group P-tiles: within a group the P-tile index
 // changes fastest, so a wave of CTAs covers a block of group x (SMs / group)
 // tiles whose operands stay in L2 together.
@@ -1052,7 +1058,7 @@ __device__ bool coop_split_unit(const GemmParams &p, const Unit &w, uint32_t tba
 // A CTA's pipeline stages receive the copies, so each CTA first tells the
 // others (remote mbarrier arrivals) that its last MMA has completed; and a
 // CTA leaves only once every CTA it copied to has reported the copy landed.
-template <int BN, bool SWAP>
+template <int BN, bool SWAP, bool PLAIN_ONLY>
 __device__ bool coop_cluster_unit(const GemmParams &p, const Unit &w, uint32_t tbase, uint64_t *tempty_b,
                                   uint64_t *free_bar, uint64_t *data_bar, uint64_t *sent_bar, float *red, float *stg,
                                   volatile int *abort_f, volatile int *s_flag) {
@@ -1061,7 +1067,7 @@ __device__ bool coop_cluster_unit(const GemmParams &p, const Unit &w, uint32_t t
     const int S = p.splits;
     const int k = w.split;  // == cluster rank
     const int ncols = min(BN, p.m_tok - w.tq * BN);
-    const bool gated_epi = p.epi == EPI_GATED || p.epi == EPI_GATED_AMAX;
+    const bool gated_epi = !PLAIN_ONLY && (p.epi == EPI_GATED || p.epi == EPI_GATED_AMAX);
     const Slice sl = slice_of<BN, SWAP>(k, S, ncols, BM, gated_epi);
     const int span = sl.hi - sl.lo;
     // 1. expect this slice from every split; free this CTA's stages for them
@@ -1128,8 +1134,12 @@ __device__ bool coop_cluster_unit(const GemmParams &p, const Unit &w, uint32_t t
     if (!*s_flag)
         return false;
     // 4. reduce the slice and run the epilogue
-    const float amax = gated_epi ? reduce_slice<BN, SWAP, true>(p, w, sl, red, span, res0)
-                                 : reduce_slice<BN, SWAP, false>(p, w, sl, red, span, res0);
+    float amax = 0.0f;
+    if constexpr (PLAIN_ONLY)
+        amax = reduce_slice<BN, SWAP, false>(p, w, sl, red, span, res0);
+    else
+        amax = gated_epi ? reduce_slice<BN, SWAP, true>(p, w, sl, red, span, res0)
+                         : reduce_slice<BN, SWAP, false>(p, w, sl, red, span, res0);
     if (p.epi == EPI_GATED_AMAX) {
         const float m = warp_max_f(amax);
         if ((threadIdx.x & 31) == 0)
@@ -1147,7 +1157,7 @@ __host__ __device__ constexpr size_t red_floats(int bn, int splits) {
     return ((size_t)BM * bn + (size_t)splits * ((BM > bn ? BM : bn) + 4) + 31) & ~(size_t)31;
 }
 
-template <int BN, bool SWAP, bool PAIR>
+template <int BN, bool SWAP, bool PAIR, int ROLE>
 __device__ void epilogue(const GemmParams &p, uint64_t *tfull, uint64_t *tempty, uint32_t tmem_base,
                          volatile int *abort_f, volatile int *s_ok, volatile int *s_last, float *xbuf,
                          uint64_t *red_bar, uint64_t *free_bar, uint64_t *data_bar, uint64_t *sent_bar,
@@ -1172,7 +1182,26 @@ __device__ void epilogue(const GemmParams &p, uint64_t *tfull, uint64_t *tempty,
             break;
         tc_fence_after();
         const uint32_t tbase = tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(abuf * BN);
-        if (p.splits == 1) {
+        if constexpr (ROLE == ROLE_GATED_TILE) {
+            float amax = 0.0f;
+            gated_swap_tile<BN>(p, w, r, tbase, &tempty[abuf], xbuf, amax);
+            if (p.epi == EPI_GATED_AMAX) {
+                amax = warp_max_f(amax);
+                if ((threadIdx.x & 31) == 0)
+                    atomicMax(p.amax, __float_as_uint(amax));
+            }
+        } else if constexpr (ROLE == ROLE_CLUSTER_PLAIN) {
+            if (!coop_cluster_unit<BN, SWAP, true>(p, w, tbase, &tempty[abuf], free_bar, data_bar, sent_bar, red,
+                                                   red + red_floats(BN, p.splits), abort_f, &s_last[abuf])) {
+                // gave up: as below
+                if (threadIdx.x == 0) {
+                    mbar_wait_for(smem_u32(free_bar), 0, 500000000ull);
+                    mbar_wait_for(smem_u32(data_bar), 0, 500000000ull);
+                    mbar_wait_for(smem_u32(sent_bar), 0, 500000000ull);
+                }
+                break;
+            }
+        } else if (p.splits == 1) {
             if (SWAP && (p.epi == EPI_GATED || p.epi == EPI_GATED_AMAX)) {
                 if constexpr (SWAP) {
                     float amax = 0.0f;
@@ -1198,8 +1227,9 @@ __device__ void epilogue(const GemmParams &p, uint64_t *tfull, uint64_t *tempty,
             }
         } else if (SWAP && p.cluster) {
             if constexpr (SWAP) {
-                if (!coop_cluster_unit<BN, SWAP>(p, w, tbase, &tempty[abuf], free_bar, data_bar, sent_bar, red,
-                                                 red + red_floats(BN, p.splits), abort_f, &s_last[abuf])) {
+                if (!coop_cluster_unit<BN, SWAP, false>(p, w, tbase, &tempty[abuf], free_bar, data_bar, sent_bar,
+                                                        red, red + red_floats(BN, p.splits), abort_f,
+                                                        &s_last[abuf])) {
                     // gave up: other CTAs of the cluster may still be copying
                     // into or out of this one; wait for them, bounded
                     if (threadIdx.x == 0) {
@@ -1222,7 +1252,7 @@ __device__ void epilogue(const GemmParams &p, uint64_t *tfull, uint64_t *tempty,
 }
 
 // -------------------------------------------------------------- kernel --
-template <int BN, bool SWAP, bool PAIR>
+template <int BN, bool SWAP, bool PAIR, int ROLE>
 __global__ void __launch_bounds__(NTHREADS, SWAP ? 2 : 1)
     k_gemm_fp8(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmQ,
                const __grid_constant__ GemmParams p) {
@@ -1303,7 +1333,7 @@ __global__ void __launch_bounds__(NTHREADS, SWAP ? 2 : 1)
     if (warp < 4) {
         // split-K runs one unit per CTA, so the pipeline stages are free to
         // receive the partial slices once the last MMA has completed
-        epilogue<BN, SWAP, PAIR>(p, tfull, tempty, tmem_base, abort_f, s_ok, s_last, xbuf, red_bar, free_bar,
+        epilogue<BN, SWAP, PAIR, ROLE>(p, tfull, tempty, tmem_base, abort_f, s_ok, s_last, xbuf, red_bar, free_bar,
                                  data_bar, sent_bar, reinterpret_cast<float *>(smem));
     } else if (warp == 4) {
         if (lane == 0)
@@ -1349,19 +1379,19 @@ __global__ void __launch_bounds__(NTHREADS, SWAP ? 2 : 1)
     }
 }
 
-template <int BN, bool SWAP, bool PAIR = false>
+template <int BN, bool SWAP, bool PAIR = false, int ROLE = ROLE_ANY>
 cudaError_t set_attrs() {
     using C = Cfg<BN, SWAP, PAIR>;
     static int done = 0;
     if (!done) {
-        cudaError_t e = cudaFuncSetAttribute(k_gemm_fp8<BN, SWAP, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(k_gemm_fp8<BN, SWAP, PAIR, ROLE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)C::SMEM);
         if (e != cudaSuccess)
             return e;
         // every kernel of the layer asks for the largest shared-memory
         // carve-out, so an SM never needs to drain before a CTA of the next
         // kernel (with its own footprint) can start beside the running ones
-        e = cudaFuncSetAttribute(k_gemm_fp8<BN, SWAP, PAIR>, cudaFuncAttributePreferredSharedMemoryCarveout,
+        e = cudaFuncSetAttribute(k_gemm_fp8<BN, SWAP, PAIR, ROLE>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  (int)cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess)
             return e;
@@ -1370,15 +1400,15 @@ cudaError_t set_attrs() {
     return cudaSuccess;
 }
 
-template <int BN, bool SWAP, bool PAIR = false>
+template <int BN, bool SWAP, bool PAIR = false, int ROLE = ROLE_ANY>
 cudaError_t run(const GemmLaunch &g, cudaStream_t s, bool pdl) {
     using C = Cfg<BN, SWAP, PAIR>;
-    cudaError_t e = set_attrs<BN, SWAP, PAIR>();
+    cudaError_t e = set_attrs<BN, SWAP, PAIR, ROLE>();
     if (e != cudaSuccess)
         return e;
     const bool xbuf = SWAP && g.p.splits == 1 && (g.p.epi == EPI_GATED || g.p.epi == EPI_GATED_AMAX);
     const unsigned cluster = PAIR ? 2u : g.p.cluster ? (unsigned)g.p.splits : (g.p.mcast > 1 ? (unsigned)g.p.mcast : 1u);
-    return launch_ex(k_gemm_fp8<BN, SWAP, PAIR>, dim3((unsigned)g.grid), dim3(NTHREADS),
+    return launch_ex(k_gemm_fp8<BN, SWAP, PAIR, ROLE>, dim3((unsigned)g.grid), dim3(NTHREADS),
                      std::max(C::smem_bytes(g.p.stages, xbuf), g.min_smem), s, pdl, cluster, g.tmP, g.tmQ, g.p);
 }
 
@@ -1583,10 +1613,22 @@ int gemm_tiles(const GemmLaunch &g) { return g.p.n_tiles_p * g.p.n_tiles_q; }
 
 cudaError_t launch_gemm(const GemmLaunch &g, cudaStream_t s, bool pdl) {
     if (g.swap) {
-        switch (g.bn) {
-        case 16: return run<16, true>(g, s, pdl);
-        case 32: return run<32, true>(g, s, pdl);
-        case 64: return run<64, true>(g, s, pdl);
+        // the layer's two weight-streaming launches run kernels compiled for
+        // their epilogue alone
+        const bool gated = g.p.epi == EPI_GATED || g.p.epi == EPI_GATED_AMAX;
+        const int role = (g.p.splits == 1 && gated) ? ROLE_GATED_TILE
+                         : (g.p.cluster && !gated)  ? ROLE_CLUSTER_PLAIN
+                                                    : ROLE_ANY;
+        switch (g.bn * 4 + role) {
+        case 16 * 4 + ROLE_ANY: return run<16, true, false, ROLE_ANY>(g, s, pdl);
+        case 16 * 4 + ROLE_GATED_TILE: return run<16, true, false, ROLE_GATED_TILE>(g, s, pdl);
+        case 16 * 4 + ROLE_CLUSTER_PLAIN: return run<16, true, false, ROLE_CLUSTER_PLAIN>(g, s, pdl);
+        case 32 * 4 + ROLE_ANY: return run<32, true, false, ROLE_ANY>(g, s, pdl);
+        case 32 * 4 + ROLE_GATED_TILE: return run<32, true, false, ROLE_GATED_TILE>(g, s, pdl);
+        case 32 * 4 + ROLE_CLUSTER_PLAIN: return run<32, true, false, ROLE_CLUSTER_PLAIN>(g, s, pdl);
+        case 64 * 4 + ROLE_ANY: return run<64, true, false, ROLE_ANY>(g, s, pdl);
+        case 64 * 4 + ROLE_GATED_TILE: return run<64, true, false, ROLE_GATED_TILE>(g, s, pdl);
+        case 64 * 4 + ROLE_CLUSTER_PLAIN: return run<64, true, false, ROLE_CLUSTER_PLAIN>(g, s, pdl);
         default: return cudaErrorInvalidValue;
         }
     }
