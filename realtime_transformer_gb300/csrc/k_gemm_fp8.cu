@@ -48,6 +48,7 @@ constexpr int BM = 128;        // MMA M = rows of the P tile = TMEM lanes
 constexpr int BK = 128;        // K bytes per stage = one 128-byte swizzle row
 constexpr int UK = 32;         // K of one tcgen05.mma for 8-bit operands
 constexpr int NTHREADS = 192;  // 4 epilogue warps + producer warp + MMA warp
+constexpr int GATED_TOKENS = 2;  // tokens per step of the weight-streaming gated epilogue
 constexpr uint32_t SMEM_LIMIT = 232448;  // largest dynamic shared memory of one CTA (227 KB)
 
 // PAIR: the tiled role on a CTA pair (cta_group::2): each CTA stages its own
@@ -542,33 +543,38 @@ __device__ __forceinline__ void gated_swap_tile(const GemmParams &p, const Unit 
             dbg_store_gu(p, m0 + c, f, r >= 64, xbuf[c * LD + r]);
     }
     constexpr int TG = BN / 8;  // tokens per thread
+    constexpr int TS = TG < GATED_TOKENS ? TG : GATED_TOKENS;  // tokens per step
     const int fq = r & 15;      // feature quad
     const int c0 = (r >> 4) * TG;
-    float g[4 * TG], u[4 * TG], a[4 * TG];
+    const bool meas = p.epi == EPI_GATED_AMAX;
+    uint8_t *qh = static_cast<uint8_t *>(p.out) + (size_t)w.tp * (BM / 2) + 4 * fq;
+    const float inv_s = p.inv_s;
+    // TS tokens per step: short code, 4 TS independent activations in flight
+#pragma unroll 1
+    for (int i0 = 0; i0 < TG; i0 += TS) {
+        float g[4 * TS], u[4 * TS], a[4 * TS];
 #pragma unroll
-    for (int i = 0; i < TG; ++i) {
-        const float4 gv = *reinterpret_cast<const float4 *>(xbuf + (c0 + i) * LD + 4 * fq);
-        const float4 uv = *reinterpret_cast<const float4 *>(xbuf + (c0 + i) * LD + 64 + 4 * fq);
-        g[4 * i] = gv.x; g[4 * i + 1] = gv.y; g[4 * i + 2] = gv.z; g[4 * i + 3] = gv.w;
-        u[4 * i] = uv.x; u[4 * i + 1] = uv.y; u[4 * i + 2] = uv.z; u[4 * i + 3] = uv.w;
-    }
-    gated_run<4 * TG>(p.act, g, u, a);
-    if (p.epi == EPI_GATED_AMAX) {
+        for (int i = 0; i < TS; ++i) {
+            const float4 gv = *reinterpret_cast<const float4 *>(xbuf + (c0 + i0 + i) * LD + 4 * fq);
+            const float4 uv = *reinterpret_cast<const float4 *>(xbuf + (c0 + i0 + i) * LD + 64 + 4 * fq);
+            g[4 * i] = gv.x; g[4 * i + 1] = gv.y; g[4 * i + 2] = gv.z; g[4 * i + 3] = gv.w;
+            u[4 * i] = uv.x; u[4 * i + 1] = uv.y; u[4 * i + 2] = uv.z; u[4 * i + 3] = uv.w;
+        }
+        gated_run<4 * TS>(p.act, g, u, a);
 #pragma unroll
-        for (int i = 0; i < TG; ++i)
-            if (c0 + i < ncols)
+        for (int i = 0; i < TS; ++i) {
+            if (c0 + i0 + i >= ncols)
+                continue;
+            if (meas) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
                     amax = fmaxf(amax, fabsf(a[4 * i + j]));
-    } else {
-        uint8_t *qh = static_cast<uint8_t *>(p.out) + (size_t)w.tp * (BM / 2) + 4 * fq;
-        const float inv_s = p.inv_s;
-#pragma unroll
-        for (int i = 0; i < TG; ++i)
-            if (c0 + i < ncols)
-                *reinterpret_cast<uint32_t *>(qh + (size_t)(m0 + c0 + i) * p.ldo) =
+            } else {
+                *reinterpret_cast<uint32_t *>(qh + (size_t)(m0 + c0 + i0 + i) * p.ldo) =
                     e4m3x2(__fmul_rn(a[4 * i], inv_s), __fmul_rn(a[4 * i + 1], inv_s)) |
                     (e4m3x2(__fmul_rn(a[4 * i + 2], inv_s), __fmul_rn(a[4 * i + 3], inv_s)) << 16);
+            }
+        }
     }
     named_bar_sync(1, 128);
 }
@@ -1162,8 +1168,6 @@ __device__ void epilogue(const GemmParams &p, uint64_t *tfull, uint64_t *tempty,
                          volatile int *abort_f, volatile int *s_ok, volatile int *s_last, float *xbuf,
                          uint64_t *red_bar, uint64_t *free_bar, uint64_t *data_bar, uint64_t *sent_bar,
                          float *red) {
-    using C = Cfg<BN, SWAP>;
-    constexpr int CH = C::CH;
     const int warp = threadIdx.x >> 5;
     const int r = threadIdx.x;  // P-tile row = TMEM lane (warps 0..3)
     if (p.cluster)
