@@ -48,7 +48,7 @@ constexpr int BM = 128;        // MMA M = rows of the P tile = TMEM lanes
 constexpr int BK = 128;        // K bytes per stage = one 128-byte swizzle row
 constexpr int UK = 32;         // K of one tcgen05.mma for 8-bit operands
 constexpr int NTHREADS = 192;  // 4 epilogue warps + producer warp + MMA warp
-constexpr int GATED_TOKENS = 2;  // tokens per step of the weight-streaming gated epilogue
+constexpr int GATED_TOKENS = 4;  // tokens per step of the weight-streaming gated epilogue
 constexpr uint32_t SMEM_LIMIT = 232448;  // largest dynamic shared memory of one CTA (227 KB)
 
 // PAIR: the tiled role on a CTA pair (cta_group::2): each CTA stages its own
