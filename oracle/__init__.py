@@ -385,3 +385,88 @@ def ref_stack_f32(layers, r, h, act: int, eps: float = EPS) -> np.ndarray:
         cur = ref_layer_f32(cur, hf if l == 0 else None, lw["w_norm"], lw["w_gate"], lw["w_up"],
                             lw["w_down"], act, eps)
     return cur
+
+
+# --------------------------------------------------------------------------
+# Attention-side input projections: residual + RMSNorm + E4M3 quantise ->
+# FP8 fused-QKV GEMM -> QKV split + RoPE (agentlenshq FlashRT summary,
+# "What it is": residual-norm-quantise and RoPE kernels; itsolotime article,
+# 5.2: FusedQKV(q, k, v) quantised as one tensor; "FlashRT
+# docs/architecture.md", 8 Kernel Library: "qkv split + RoPE").
+# --------------------------------------------------------------------------
+
+def rope_inv_freq(head_dim: int, base: float) -> np.ndarray:
+    """theta_i = base^(-2i / head_dim), i < head_dim / 2, evaluated in fp64
+    and rounded to fp32 (reading: the usual inverse-frequency vector)."""
+    i = np.arange(head_dim // 2, dtype=np.float64)
+    return (float(base) ** (-2.0 * i / head_dim)).astype(np.float32)
+
+
+def rope(x, pos, inv_freq) -> np.ndarray:
+    """Rotary position embedding, rotate-half layout (reading): element i of
+    the first half pairs with element i + hd/2.  angle = fp32(pos * theta_i)
+    (fp32 product), cos and sin of that fp32 angle rounded to fp32, then in
+    fp32: o_i = x_i cos - x_{i+hd/2} sin, o_{i+hd/2} = x_{i+hd/2} cos + x_i sin.
+    x [..., M, H, hd] fp32 values, pos [M] integers; returns fp32."""
+    x = np.asarray(x, dtype=np.float32)
+    hd = x.shape[-1]
+    half = hd // 2
+    ang = (np.asarray(pos).astype(np.float32)[:, None] * np.asarray(inv_freq, np.float32)[None, :])
+    c = np.cos(ang.astype(np.float64)).astype(np.float32)[:, None, :]
+    s = np.sin(ang.astype(np.float64)).astype(np.float32)[:, None, :]
+    x1 = x[..., :half]
+    x2 = x[..., half:]
+    o1 = (x1 * c).astype(np.float32) - (x2 * s).astype(np.float32)
+    o2 = (x2 * c).astype(np.float32) + (x1 * s).astype(np.float32)
+    return np.concatenate([o1.astype(np.float32), o2.astype(np.float32)], axis=-1)
+
+
+def quantize_qkv_weights(w_q, w_k, w_v):
+    """Step A0 for the fused QKV weight: [W_q; W_k; W_v] as one tensor with
+    one per-tensor scale -> (codes, scale)."""
+    return quantize_weight(np.concatenate([_u16(w_q), _u16(w_k), _u16(w_v)], axis=0))
+
+
+@dataclass
+class QKVTrace:
+    r_prime: np.ndarray   # [M,d] BF16 bits
+    q_x: np.ndarray       # [M,d] E4M3 codes
+    qkv: np.ndarray       # [M,(Hq+2Hkv)hd] BF16 bits (GEMM output)
+    q: np.ndarray         # [Hq,M,hd] BF16 bits (rotated)
+    k: np.ndarray         # [Hkv,M,hd] BF16 bits (rotated)
+    v: np.ndarray         # [Hkv,M,hd] BF16 bits
+
+
+def qkv_layer(r, h, w_norm, q_qkv, s_x, s_qkv, n_q: int, n_kv: int, head_dim: int, pos, inv_freq,
+              eps: float = EPS) -> QKVTrace:
+    """One attention-input sublayer with fixed scales: r' = bf16(r + h),
+    y = RMSNorm(r') w, q_x = E4M3(y / s_x) (step A1); qkv = bf16(acc * alpha),
+    acc = q_x . W_qkv^T in fp32, alpha = s_x s_qkv (as step A2, plain BF16
+    output); split into heads (the first Hq*hd columns are Q, then K, then V)
+    and RoPE on Q and K, each rounded to BF16; outputs head-major [H, M, hd]
+    (reading: the layout an attention kernel reads per head)."""
+    r = _u16(r)
+    M, d = r.shape
+    rp, y = residual_rmsnorm(r, h, w_norm, eps)
+    q_x = quantize_f32(y, recip(s_x))
+    acc = gemm_e4m3(q_x, q_qkv)
+    alpha = np.float32(np.float32(s_x) * np.float32(s_qkv))
+    qkv = bf16_encode((acc * alpha).astype(np.float32))
+    vals = bf16_decode(qkv)
+    nq, nk = n_q * head_dim, n_kv * head_dim
+    qh = vals[:, :nq].reshape(M, n_q, head_dim)
+    kh = vals[:, nq:nq + nk].reshape(M, n_kv, head_dim)
+    vh = qkv[:, nq + nk:nq + 2 * nk].reshape(M, n_kv, head_dim)
+    q = bf16_encode(rope(qh, pos, inv_freq)).transpose(1, 0, 2)
+    k = bf16_encode(rope(kh, pos, inv_freq)).transpose(1, 0, 2)
+    v = vh.transpose(1, 0, 2)
+    return QKVTrace(rp, q_x, qkv, np.ascontiguousarray(q), np.ascontiguousarray(k), np.ascontiguousarray(v))
+
+
+def calibrate_qkv_layer(r_batches, h_batches, w_norm, eps: float = EPS) -> float:
+    """Step A6 for the QKV sublayer: s_x = amax(y) / 448 over the batches."""
+    amax = 0.0
+    for i, r in enumerate(r_batches):
+        _, y = residual_rmsnorm(r, h_batches[i] if h_batches is not None else None, w_norm, eps)
+        amax = max(amax, amax_f32(y))
+    return scale_from_amax(np.float32(amax))
