@@ -12,4 +12,7 @@ def __getattr__(name):
     if name == "FFNPlan":
         from .ffn import FFNPlan
         return FFNPlan
+    if name == "QKVPlan":
+        from .qkv import QKVPlan
+        return QKVPlan
     raise AttributeError(name)

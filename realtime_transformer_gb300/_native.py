@@ -1,4 +1,4 @@
-"""ctypes binding of libfrt_ffn.so (include/frt_ffn.h).
+"""ctypes binding of libfrt_ffn.so (include/frt_ffn.h, include/frt_qkv.h).
 
 Argument marshalling only: every step of the FFN path runs in the CUDA
 library.  The functions keep the C names; a non-OK status raises FrtError
@@ -47,6 +47,16 @@ SIGNATURES = {
     "frt_ffn_last_error": (ctypes.c_char_p, []),
     "frt_fp8_gemm_noalloc": (_I, [_P, _P, _P, _I, _I, _I, _F, _P]),
     "frt_fp8_gemm_noalloc_last_error": (ctypes.c_char_p, []),
+    # include/frt_qkv.h
+    "frt_qkv_plan_create": (_I, [_I, _I, _I, _I, _F, _I, _I, ctypes.POINTER(_P)]),
+    "frt_qkv_plan_destroy": (_I, [_P]),
+    "frt_qkv_load_weights": (_I, [_P, _I, _P, _P, _P, _P, _P]),
+    "frt_qkv_calibrate": (_I, [_P, _I, ctypes.POINTER(_P), ctypes.POINTER(_P), _I, _I, _P]),
+    "frt_qkv_get_scales": (_I, [_P, _FP, _FP]),
+    "frt_qkv_set_scales": (_I, [_P, _FP]),
+    "frt_qkv_forward": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _P]),
+    "frt_qkv_debug_trace": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P]),
+    "frt_qkv_device_status": (_I, [_P, _P]),
 }
 
 
@@ -179,3 +189,54 @@ def frt_fp8_gemm_noalloc(A, B, C, M, N, K, alpha, stream) -> None:
 def frt_ffn_last_error() -> str:
     msg = lib().frt_ffn_last_error()
     return msg.decode() if msg else ""
+
+
+
+# -- attention-input sublayer (include/frt_qkv.h) ----------------------------
+
+def frt_qkv_plan_create(d, n_q_heads, n_kv_heads, head_dim, rope_base, M_max, n_layers) -> int:
+    out = _P()
+    _check(lib().frt_qkv_plan_create(d, n_q_heads, n_kv_heads, head_dim, rope_base, M_max, n_layers,
+                                     ctypes.byref(out)))
+    return out.value
+
+
+def frt_qkv_plan_destroy(plan) -> None:
+    _check(lib().frt_qkv_plan_destroy(plan))
+
+
+def frt_qkv_load_weights(plan, layer, w_norm, w_q, w_k, w_v, stream) -> None:
+    _check(lib().frt_qkv_load_weights(plan, layer, w_norm, w_q, w_k, w_v, stream))
+
+
+def frt_qkv_calibrate(plan, layer, residual_ptrs, hidden_ptrs, M, stream) -> None:
+    n = len(residual_ptrs)
+    r = _ptrs(residual_ptrs)
+    h = _ptrs(hidden_ptrs) if hidden_ptrs is not None else None
+    _check(lib().frt_qkv_calibrate(plan, layer, ctypes.cast(r, ctypes.POINTER(_P)),
+                                   ctypes.cast(h, ctypes.POINTER(_P)) if h is not None else None, n, M, stream))
+
+
+def frt_qkv_get_scales(plan, n_layers: int):
+    arrs = [(ctypes.c_float * n_layers)() for _ in range(2)]
+    _check(lib().frt_qkv_get_scales(plan, *[ctypes.cast(a, _FP) for a in arrs]))
+    return [list(a) for a in arrs]
+
+
+def frt_qkv_set_scales(plan, s_x) -> None:
+    arr = (ctypes.c_float * len(s_x))(*s_x)
+    _check(lib().frt_qkv_set_scales(plan, ctypes.cast(arr, _FP)))
+
+
+def frt_qkv_forward(plan, layer, residual_in, hidden_in, positions, r_prime, q, k, v, M, stream) -> None:
+    _check(lib().frt_qkv_forward(plan, layer, residual_in, hidden_in, positions, r_prime, q, k, v, M, stream))
+
+
+def frt_qkv_debug_trace(plan, layer, residual_in, hidden_in, positions, r_prime, q, k, v, q_x, qkv, M,
+                        stream) -> None:
+    _check(lib().frt_qkv_debug_trace(plan, layer, residual_in, hidden_in, positions, r_prime, q, k, v, q_x, qkv,
+                                     M, stream))
+
+
+def frt_qkv_device_status(plan, stream) -> None:
+    _check(lib().frt_qkv_device_status(plan, stream))

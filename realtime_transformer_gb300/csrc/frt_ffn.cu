@@ -58,6 +58,13 @@ frt_status cuda_fail(cudaError_t e, const char *what) {
                 cudaGetErrorString(e), cudaGetErrorName(e));
 }
 
+}  // namespace
+
+// The per-thread message of the last failed call, shared by every plan type.
+void frt::set_last_error(const char *msg) { g_last_error = msg; }
+
+namespace {
+
 #define CK(call)                                   \
     do {                                           \
         cudaError_t e_ = (call);                   \

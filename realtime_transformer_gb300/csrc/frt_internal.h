@@ -68,6 +68,9 @@ struct GemmLaunch {
 
 // Host side --------------------------------------------------------------
 
+// Message returned by frt_ffn_last_error() on this host thread.
+void set_last_error(const char *msg);
+
 // Split-K arrival counters only grow, so every split count gets its own
 // range of counters (a counter is shared only by launches with the same S).
 constexpr int MAX_SPLIT_TILES = 2048;
@@ -90,6 +93,8 @@ cudaError_t launch_quant_bf16(const void *x, size_t n, float inv_s, uint8_t *q, 
 cudaError_t launch_quant_gu_interleave(const void *gate, const void *up, int ff, int d, const void *fold,
                                       float inv_s, uint8_t *dst, cudaStream_t s);
 cudaError_t launch_amax_fold(const void *x, size_t rows, int d, const void *w, unsigned *amax_word, cudaStream_t s);
+cudaError_t launch_rope_split(const void *qkv, int M, int nq, int nkv, int hd, const int *pos, const float *inv_freq,
+                              void *q, void *k, void *v, cudaStream_t s, bool pdl);
 cudaError_t launch_norm_quant(const void *r, const void *h, const void *w, int M, int d, float eps, float inv_s,
                               void *rprime, uint8_t *qx, unsigned *amax_word, bool measure, cudaStream_t s,
                               bool pdl);

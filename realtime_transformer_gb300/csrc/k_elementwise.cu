@@ -343,6 +343,63 @@ __global__ void __launch_bounds__(256) k_norm_quant(const uint16_t *__restrict__
     }
 }
 
+// ------------------------------------------------------- QKV split + RoPE --
+
+// qkv [M, (Hq + 2 Hkv) hd] BF16 (Q heads, then K heads, then V heads) ->
+// q [Hq, M, hd], k [Hkv, M, hd] rotated by RoPE at pos[m], v [Hkv, M, hd]
+// copied.  Rotate-half layout: element i of a head's first half pairs with
+// element i + hd/2, angle = pos * theta_i in fp32, then in fp32
+// o_i = x_i cos - x_{i+hd/2} sin, o_{i+hd/2} = x_{i+hd/2} cos + x_i sin,
+// rounded to BF16.  A thread takes 4 consecutive pairs of a Q/K head (two
+// 8-byte loads and stores) or 8 consecutive elements of a V head.
+__global__ void __launch_bounds__(256) k_rope_split(const uint16_t *__restrict__ qkv, int M, int nq, int nkv, int hd,
+                                                   const int *__restrict__ pos, const float *__restrict__ inv_freq,
+                                                   uint16_t *__restrict__ q, uint16_t *__restrict__ k,
+                                                   uint16_t *__restrict__ v) {
+    pdl_trigger();
+    pdl_wait();
+    const int G = hd / 8;  // work items per head: 4 pairs, or 8 V elements
+    const int H = nq + 2 * nkv;
+    const size_t N = (size_t)H * hd;
+    const size_t total = (size_t)M * H * G;
+    for (size_t t = blockIdx.x * (size_t)blockDim.x + threadIdx.x; t < total; t += (size_t)gridDim.x * blockDim.x) {
+        const int g = (int)(t % G);
+        const size_t mh = t / G;
+        const int h = (int)(mh % H);
+        const int m = (int)(mh / H);
+        const uint16_t *src = qkv + (size_t)m * N + (size_t)h * hd;
+        if (h >= nq + nkv) {
+            const int hv = h - nq - nkv;
+            *reinterpret_cast<uint4 *>(v + ((size_t)hv * M + m) * hd + 8 * g) =
+                __ldg(reinterpret_cast<const uint4 *>(src + 8 * g));
+            continue;
+        }
+        const int half = hd / 2;
+        const uint2 a = __ldg(reinterpret_cast<const uint2 *>(src + 4 * g));
+        const uint2 b = __ldg(reinterpret_cast<const uint2 *>(src + half + 4 * g));
+        const float x1[4] = {bf_lo(a.x), bf_hi(a.x), bf_lo(a.y), bf_hi(a.y)};
+        const float x2[4] = {bf_lo(b.x), bf_hi(b.x), bf_lo(b.y), bf_hi(b.y)};
+        const float p = (float)__ldg(pos + m);
+        uint32_t o1[2], o2[2];
+#pragma unroll
+        for (int j = 0; j < 4; j += 2) {
+            float r1[2], r2[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                float sn, cs;
+                sincosf(__fmul_rn(p, __ldg(inv_freq + 4 * g + j + e)), &sn, &cs);
+                r1[e] = __fsub_rn(__fmul_rn(x1[j + e], cs), __fmul_rn(x2[j + e], sn));
+                r2[e] = __fadd_rn(__fmul_rn(x2[j + e], cs), __fmul_rn(x1[j + e], sn));
+            }
+            o1[j / 2] = bf16_bits(r1[0]) | (bf16_bits(r1[1]) << 16);
+            o2[j / 2] = bf16_bits(r2[0]) | (bf16_bits(r2[1]) << 16);
+        }
+        uint16_t *dst = h < nq ? q + ((size_t)h * M + m) * hd : k + ((size_t)(h - nq) * M + m) * hd;
+        *reinterpret_cast<uint2 *>(dst + 4 * g) = make_uint2(o1[0], o1[1]);
+        *reinterpret_cast<uint2 *>(dst + half + 4 * g) = make_uint2(o2[0], o2[1]);
+    }
+}
+
 int sm_count() {
     static int n = 0;
     if (n == 0) {
@@ -469,6 +526,18 @@ cudaError_t launch_norm_quant(const void *r, const void *h, const void *w, int M
     if (measure)
         return norm_dispatch<true>(M, pdl, s, rr, hh, ww, d, eps, inv_s, rp, qx, amax_word);
     return norm_dispatch<false>(M, pdl, s, rr, hh, ww, d, eps, inv_s, rp, qx, amax_word);
+}
+
+cudaError_t launch_rope_split(const void *qkv, int M, int nq, int nkv, int hd, const int *pos, const float *inv_freq,
+                              void *q, void *k, void *v, cudaStream_t s, bool pdl) {
+    const size_t total = (size_t)M * (nq + 2 * nkv) * (hd / 8);
+    size_t blocks = (total + 255) / 256;
+    const size_t cap = (size_t)sm_count() * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks == 0) blocks = 1;
+    return launch_ex(k_rope_split, dim3((unsigned)blocks), dim3(256), 0, s, pdl, 1u,
+                     static_cast<const uint16_t *>(qkv), M, nq, nkv, hd, pos, inv_freq, static_cast<uint16_t *>(q),
+                     static_cast<uint16_t *>(k), static_cast<uint16_t *>(v));
 }
 
 }  // namespace frt

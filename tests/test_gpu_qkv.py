@@ -1,0 +1,157 @@
+"""Attention-input sublayer on the GPU against the oracle: residual + RMSNorm
++ E4M3 quantise, FP8 fused-QKV GEMM, QKV split + RoPE (agentlenshq FlashRT
+summary, "What it is"; itsolotime FlashRT article, 5.2 FusedQKV; "FlashRT
+docs/architecture.md", 8 Kernel Library).  Same inputs and scales on both
+sides; q_x codes, the GEMM output and Q/K/V held to the parity contract."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic
+from parity import bits, check_bf16, check_codes, u8
+
+pytestmark = pytest.mark.gpu
+
+# (name, M, d, n_q, n_kv, head_dim, rope_base, first position, hidden)
+SHAPES = [
+    ("tiny", 8, 256, 4, 1, 64, 1.0e4, 0, True),
+    ("action_expert", 50, 1024, 8, 1, 256, 1.0e4, 0, True),
+    ("decode", 1, 5120, 40, 8, 128, 1.0e6, 4096, False),
+    ("ragged", 17, 384, 6, 3, 32, 1.0e4, 100, True),
+    ("tiled", 300, 512, 4, 2, 64, 1.0e4, 0, False),
+    ("far_positions", 3, 256, 4, 2, 32, 1.0e6, 100000, False),
+]
+
+
+def weights(d, nq, nkv, hd, seed):
+    g = torch.Generator().manual_seed(seed)
+    w = {"w_q": torch.randn(nq * hd, d, generator=g) * 0.02, "w_k": torch.randn(nkv * hd, d, generator=g) * 0.02,
+         "w_v": torch.randn(nkv * hd, d, generator=g) * 0.02, "w_norm": 1 + 0.1 * torch.randn(d, generator=g)}
+    return {k: v.to(torch.bfloat16) for k, v in w.items()}
+
+
+@pytest.fixture(scope="module", params=SHAPES, ids=lambda s: s[0])
+def case(request):
+    from realtime_transformer_gb300.qkv import QKVPlan
+    name, M, d, nq, nkv, hd, base, p0, with_h = request.param
+    wl = synthetic.WORKLOADS["tiny"].with_(name=name, M=M, d=d, seed=31)
+    r, h = synthetic.inputs(wl)
+    h = h if with_h else None
+    w = weights(d, nq, nkv, hd, 7 + M)
+    pos = (p0 + 3 * np.arange(M)).astype(np.int32)
+    codes, s_qkv = oracle.quantize_qkv_weights(bits(w["w_q"]), bits(w["w_k"]), bits(w["w_v"]))
+    s_x = oracle.calibrate_qkv_layer([bits(r)], [bits(h)] if with_h else None, bits(w["w_norm"]))
+    dev = torch.device("cuda")
+    plan = QKVPlan(d, nq, nkv, hd, base, M, 1)
+    plan.load_weights(0, *(w[k].to(dev) for k in ("w_norm", "w_q", "w_k", "w_v")))
+    plan.set_scales([s_x])
+    c = dict(name=name, M=M, d=d, nq=nq, nkv=nkv, hd=hd, base=base, r=r, h=h, w=w, pos=pos, codes=codes,
+             s_qkv=s_qkv, s_x=s_x, plan=plan, dev=dev)
+    yield c
+    plan.close()
+
+
+def test_weight_scale_matches_oracle_exactly(case):
+    assert case["plan"].scales()["s_qkv"][0] == np.float32(case["s_qkv"])
+
+
+def test_sublayer_matches_oracle(case):
+    c = case
+    dev = c["dev"]
+    tr = c["plan"].trace(0, c["r"].to(dev), c["h"].to(dev) if c["h"] is not None else None,
+                         torch.from_numpy(c["pos"]).to(dev))
+    torch.cuda.synchronize()
+    c["plan"].device_status()
+    ref = oracle.qkv_layer(bits(c["r"]), bits(c["h"]) if c["h"] is not None else None, bits(c["w"]["w_norm"]),
+                           c["codes"], c["s_x"], c["s_qkv"], c["nq"], c["nkv"], c["hd"], c["pos"],
+                           oracle.rope_inv_freq(c["hd"], c["base"]))
+    assert np.array_equal(bits(tr["r_prime"]), ref.r_prime), "r' = bf16(r + h) must be bit-exact"
+    qx = u8(tr["q_x"])
+    check_codes(qx, ref.q_x, c["name"] + " q_x")
+    rows = np.all(qx == ref.q_x, axis=1)
+    assert rows.mean() >= 0.5
+    check_bf16(bits(tr["qkv"])[rows], ref.qkv[rows], c["name"] + " qkv (rows with identical q_x)")
+    for k in ("q", "k", "v"):
+        got = bits(tr[k])
+        assert got.shape == getattr(ref, k).shape, k
+        check_bf16(got[:, rows], getattr(ref, k)[:, rows], "%s %s" % (c["name"], k))
+    # the forward entry point computes the same as the trace
+    o = c["plan"].forward(0, c["r"].to(dev), c["h"].to(dev) if c["h"] is not None else None,
+                          torch.from_numpy(c["pos"]).to(dev))
+    torch.cuda.synchronize()
+    for k in ("q", "k", "v", "r_prime"):
+        assert torch.equal(o[k], tr[k]), k
+
+
+def test_gpu_calibration_matches_oracle(case):
+    c = case
+    dev = c["dev"]
+    saved = c["plan"].scales()["s_x"]
+    c["plan"].calibrate(0, [c["r"].to(dev)], [c["h"].to(dev)] if c["h"] is not None else None)
+    got = c["plan"].scales()["s_x"][0]
+    c["plan"].set_scales(saved)
+    assert abs(got - c["s_x"]) <= (0.5 * c["d"] + 4) * 2.0 ** -24 * c["s_x"]
+
+
+def test_forward_can_be_captured_in_a_cuda_graph(case):
+    c = case
+    dev = c["dev"]
+    r = c["r"].to(dev)
+    h = c["h"].to(dev) if c["h"] is not None else None
+    pos = torch.from_numpy(c["pos"]).to(dev)
+    eager = c["plan"].forward(0, r, h, pos)
+    torch.cuda.synchronize()
+    out = {k: torch.empty_like(v) for k, v in eager.items()}
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        c["plan"].forward(0, r, h, pos, out=out, stream=s)  # warm up (tensor maps, attributes) outside capture
+        s.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            c["plan"].forward(0, r, h, pos, out=out, stream=s)
+    for v in out.values():
+        v.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    for k in ("q", "k", "v"):
+        assert torch.equal(out[k], eager[k]), k
+
+
+def test_boundary_errors():
+    from realtime_transformer_gb300 import _native as N
+    from realtime_transformer_gb300.qkv import QKVPlan
+    with pytest.raises(N.FrtError) as e:
+        QKVPlan(256, 3, 2, 64, 1e4, 8, 1)  # 2 does not divide 3
+    assert e.value.name == "FRT_ERR_INVALID_ARG"
+    with pytest.raises(N.FrtError):
+        QKVPlan(256, 4, 1, 60, 1e4, 8, 1)  # head_dim % 8
+    dev = torch.device("cuda")
+    p = QKVPlan(256, 4, 1, 64, 1e4, 8, 2)
+    r = torch.zeros(8, 256, dtype=torch.bfloat16, device=dev)
+    pos = torch.zeros(8, dtype=torch.int32, device=dev)
+    with pytest.raises(N.FrtError) as e:
+        p.forward(0, r, None, pos)
+    assert e.value.name == "FRT_ERR_NOT_READY"
+    w = weights(256, 4, 1, 64, 3)
+    p.load_weights(1, *(w[k].to(dev) for k in ("w_norm", "w_q", "w_k", "w_v")))
+    with pytest.raises(N.FrtError) as e:
+        p.forward(1, r, None, pos)  # no activation scale yet
+    assert e.value.name == "FRT_ERR_NOT_READY"
+    with pytest.raises(N.FrtError) as e:
+        p.set_scales([0.01, float("nan")])
+    assert e.value.name == "FRT_ERR_INVALID_ARG"
+    p.set_scales([0.01, 0.01])
+    big = torch.zeros(9, 256, dtype=torch.bfloat16, device=dev)
+    with pytest.raises(N.FrtError) as e:
+        p.forward(1, big, None, torch.zeros(9, dtype=torch.int32, device=dev))
+    assert e.value.name == "FRT_ERR_SHAPE"
+    o = p._outs(8, dev)
+    with pytest.raises(N.FrtError) as e:
+        N.frt_qkv_forward(p.handle, 1, r.data_ptr(), None, None, None, o["q"].data_ptr(), o["k"].data_ptr(),
+                          o["v"].data_ptr(), 8, None)
+    assert e.value.name == "FRT_ERR_INVALID_ARG"
+    N.frt_qkv_forward(p.handle, 1, r.data_ptr(), None, pos.data_ptr(), None, o["q"].data_ptr(), o["k"].data_ptr(),
+                      o["v"].data_ptr(), 0, None)  # M == 0: nothing
+    p.device_status()
+    p.close()
