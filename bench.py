@@ -384,6 +384,143 @@ def run_ours(args, wl, world, rank, local):
     return line
 
 
+def qkv_config_of(wl):
+    nq, nkv, hd, base = synthetic.ATTENTION[wl.name]
+    return {"workload": wl.name + " attention input (QKV)", "M": wl.M, "d": wl.d, "n_q_heads": nq,
+            "n_kv_heads": nkv, "head_dim": hd, "rope_base": base, "layers": wl.L, "weights": "E4M3 per-tensor",
+            "graph": "the stack's L sublayer forwards in one CUDA graph (same input per layer)",
+            "l2": "flushed between timed steps (%d MiB write)" % (L2_FLUSH_BYTES >> 20), "parallelism": "replicas"}
+
+
+def run_qkv(args, wl, world, rank, local):
+    """The attention-input sublayer (norm + FP8 fused-QKV GEMM + split/RoPE):
+    one step = the L layers' sublayers, each on the workload's residual (the
+    attention between them is not this library's), captured in one graph."""
+    from realtime_transformer_gb300.qkv import QKVPlan
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    P = peaks()
+    nq, nkv, hd, base = synthetic.ATTENTION[wl.name]
+    N = (nq + 2 * nkv) * hd
+    r, h = synthetic.inputs(wl, device=dev)
+    calib = synthetic.calibration_batches(wl, device=dev)
+    pos = torch.from_numpy(synthetic.positions(wl)).to(dev)
+    plan = QKVPlan(wl.d, nq, nkv, hd, base, wl.M, wl.L)
+    ws = [synthetic.qkv_weights(wl, l, device=dev) for l in range(wl.L)]
+    for l, w in enumerate(ws):
+        plan.load_weights(l, w["w_norm"], w["w_q"], w["w_k"], w["w_v"])
+        plan.calibrate(l, [a for a, _ in calib], [b for _, b in calib] if l == 0 else None)
+    outs = [plan._outs(wl.M, dev) for _ in range(wl.L)]
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def stack():
+        for l in range(wl.L):
+            plan.forward(l, r, h if l == 0 else None, pos, out=outs[l], stream=stream)
+
+    with torch.cuda.stream(stream):
+        stack()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            stack()
+    torch.cuda.synchronize()
+
+    def timed(fn, n, warm):
+        for _ in range(warm):
+            with torch.cuda.stream(stream):
+                flush.zero_()
+                fn()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        with torch.cuda.stream(stream):
+            for e0, e1 in evs:
+                flush.zero_()
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+        torch.cuda.synchronize()
+        return [e0.elapsed_time(e1) for e0, e1 in evs]
+
+    timed(graph.replay, 0, args.warmup)
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    t_wall0 = time.perf_counter()
+    step_ms = timed(graph.replay, args.steps, 0)
+    t_wall = time.perf_counter() - t_wall0
+    clocks = sampler.stop()
+    barrier(world)
+    plan.device_status(stream)
+    total_s = reduce_max(sum(step_ms) / 1000.0, world, dev)
+    value = world * wl.M * args.steps / total_s
+    ms_step = 1000.0 * total_s / args.steps
+
+    # end to end: pinned host residual/hidden in, the graph, Q/K/V of every layer out
+    h_r = r.cpu().pin_memory()
+    h_h = h.cpu().pin_memory()
+    h_out = [{k: torch.empty_like(o[k], device="cpu").pin_memory() for k in ("q", "k", "v")} for o in outs]
+
+    def e2e_step():
+        r.copy_(h_r, non_blocking=True)
+        h.copy_(h_h, non_blocking=True)
+        graph.replay()
+        for ho, o in zip(h_out, outs):
+            for k in ho:
+                ho[k].copy_(o[k], non_blocking=True)
+
+    e2e_ms = timed(e2e_step, args.steps, args.warmup)
+    e2e_s = reduce_max(sum(e2e_ms) / 1000.0, world, dev)
+    d2h = sum(t.numel() * 2 for ho in h_out for t in ho.values())
+
+    # roofline of one sublayer (its three kernels together): weights + residual
+    # in + Q/K/V out, against HBM or the FP8 tensor peak by intensity
+    layer_s = ms_step / 1000.0 / wl.L
+    nbytes = N * wl.d + 2 * wl.M * wl.d + 2 * wl.M * N
+    flops = 2.0 * wl.M * wl.d * N
+    fp8_peak = 2.0 * P["bf16_tflops"]
+    if flops / nbytes > fp8_peak * 1e12 / (P["hbm_gbs"] * 1e9):
+        ach = flops / layer_s / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": fp8_peak, "unit": "TFLOP/s", "frac": ach / fp8_peak,
+                "peak_note": "FP8 dense = 2 x measured bf16 burst (%s)" % P["src"]}
+    else:
+        ach = nbytes / layer_s / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": P["hbm_gbs"], "unit": "GB/s", "frac": ach / P["hbm_gbs"],
+                "peak_note": "%s HBM copy bandwidth" % P["src"]}
+    roof.update({"kernel": "qkv sublayer (norm_quant + FP8 QKV GEMM + rope_split, graph-replayed)",
+                 "us_per_launch": 1e6 * layer_s, "algorithmic_bytes": nbytes, "traffic": None})
+    line = {
+        "metric": "FP8 QKV sublayer tokens/s (graph-replayed, %s)" % wl.name, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "us_per_layer": 1e6 * layer_s, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8_e4m3 (fp32 accumulate, bf16 outputs)", "data": "synthetic", "config": qkv_config_of(wl),
+        "roofline": roof,
+        "e2e": {"value": world * wl.M * args.steps / e2e_s, "unit": "tokens/s",
+                "h2d_bytes_per_step": h_r.numel() * 2 + h_h.numel() * 2, "d2h_bytes_per_step": d2h,
+                "ms_per_step": 1000.0 * e2e_s / args.steps},
+        "gpu_launches": args.steps * wl.L * 3, "clocks": clocks, "wall_s_timed_region": t_wall,
+    }
+    plan.close()
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        bits = synthetic.bf16_bits
+        w0 = {k: bits(v) for k, v in ws[0].items()}
+        codes, s_qkv = oracle.quantize_qkv_weights(w0["w_q"], w0["w_k"], w0["w_v"])
+        rows = min(wl.M, 16)
+        s_x = oracle.calibrate_qkv_layer([bits(calib[0][0][:rows])], [bits(calib[0][1][:rows])], w0["w_norm"])
+        f = oracle.rope_inv_freq(hd, base)
+        p = synthetic.positions(wl)
+        t0 = time.perf_counter()
+        oracle.qkv_layer(bits(r[:rows]), bits(h[:rows]), w0["w_norm"], codes, s_x, s_qkv, nq, nkv, hd, p[:rows], f)
+        dt = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": rows / (dt * wl.L), "unit": "tokens/s", "cores": cpu_cores(),
+                                "kind": "oracle", "sample": "%d of %d tokens through one of the %d layers, "
+                                "scaled to the stack" % (rows, wl.M, wl.L)}
+    return line
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -392,6 +529,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(synthetic.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sublayer", choices=["ffn", "qkv"], default="ffn",
+                    help="ffn: the FFN stack (the default bench line); qkv: the attention-input projections")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling aid: run a plan of this many layers of the workload's shape "
                          "(the line is then not the workload's bench line)")
@@ -404,6 +543,8 @@ def main():
     world, rank, local = dist_setup(args.gpus)
     if args.impl == "reference":
         line = run_reference(args, wl, world, rank)
+    elif args.sublayer == "qkv":
+        line = run_qkv(args, wl, world, rank, local)
     else:
         line = run_ours(args, wl, world, rank, local)
     if rank == 0 and line is not None:

@@ -75,8 +75,23 @@ WORKLOADS = {
                              outliers=True, n_calib=1),
 }
 
+# Attention-input projections of each workload's model family (readings: the
+# pages name the models, not their heads): (query heads, key/value heads,
+# head dim, RoPE base) -- Gemma-style 8 query heads sharing one 256-wide
+# key/value head for the VLA shapes (base 10^4), a Qwen-style 40 / 8 heads of
+# 128 at width 5120 (base 10^6) for the LLM shapes.
+ATTENTION = {
+    "tiny": (4, 1, 64, 1.0e4),
+    "vla_action_expert": (8, 1, 256, 1.0e4),
+    "vla_prefix": (8, 1, 256, 1.0e4),
+    "llm_decode": (40, 8, 128, 1.0e6),
+    "long_prefill": (40, 8, 128, 1.0e6),
+}
+DECODE_CONTEXT = 4096  # the decoded token's position in the LLM decode workload
+
 # sub-stream identifiers
 _S_WNORM, _S_WGATE, _S_WUP, _S_WDOWN, _S_RES, _S_HID, _S_OUTL = range(7)
+_S_WQ, _S_WK, _S_WV, _S_WNORM_ATTN = range(7, 11)
 _S_CALIB_BASE = 1000
 
 
@@ -108,6 +123,26 @@ def layer_weights(wl: Workload, layer: int, device="cpu") -> dict[str, torch.Ten
     w_down = 0.02 * _normal((wl.d, wl.ff), _seed(s, _S_WDOWN, layer), device)
     return {k: v.to(torch.bfloat16) for k, v in
             dict(w_norm=w_norm, w_gate=w_gate, w_up=w_up, w_down=w_down).items()}
+
+
+def qkv_weights(wl: Workload, layer: int, device="cpu") -> dict[str, torch.Tensor]:
+    """BF16 attention-input weights of one layer: w_norm [d], w_q [Hq hd, d],
+    w_k [Hkv hd, d], w_v [Hkv hd, d]; same distributions as the FFN's."""
+    nq, nkv, hd, _ = ATTENTION.get(wl.name, ATTENTION["tiny"])
+    s = wl.seed
+    w = dict(w_norm=1.0 + 0.1 * _normal((wl.d,), _seed(s, _S_WNORM_ATTN, layer), device),
+             w_q=0.02 * _normal((nq * hd, wl.d), _seed(s, _S_WQ, layer), device),
+             w_k=0.02 * _normal((nkv * hd, wl.d), _seed(s, _S_WK, layer), device),
+             w_v=0.02 * _normal((nkv * hd, wl.d), _seed(s, _S_WV, layer), device))
+    return {k: v.to(torch.bfloat16) for k, v in w.items()}
+
+
+def positions(wl: Workload, M: int | None = None) -> np.ndarray:
+    """Token positions (int32): the decode workload's token sits after a
+    DECODE_CONTEXT-token context; the other workloads start at 0."""
+    M = wl.M if M is None else M
+    p0 = DECODE_CONTEXT if wl.name == "llm_decode" else 0
+    return (p0 + np.arange(M)).astype(np.int32)
 
 
 def _activation(wl: Workload, M: int, seed: int, device) -> torch.Tensor:
