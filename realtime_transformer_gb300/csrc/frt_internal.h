@@ -17,6 +17,7 @@ enum Epi : int {
     EPI_F32 = 2,    // out[m][n] = acc * alpha (fp32; diagnostics)
     EPI_GATED = 3,  // out = q_h[m][f] = E4M3(act(g) * u * inv_s), g/u = bf16(acc * alpha) (interleaved rows)
     EPI_GATED_AMAX = 4,  // atomicMax(amax, |act(g) * u|) (calibration)
+    EPI_ROPE = 5,   // tiled role: x = bf16(acc * alpha), split into Q/K/V heads, RoPE on Q and K (rope_* fields)
 };
 
 // One GEMM launch: C[token][feature] = epilogue(sum_k X[token][k] W[feature][k]).
@@ -55,6 +56,13 @@ struct GemmParams {
     float inv_s;            // 1 / s_h
     unsigned *amax;         // EPI_GATED_AMAX target
     uint16_t *dbg_gu;       // optional: BF16 [g | u] [M, 2ff] (diagnostics)
+    // QKV split + RoPE epilogue (EPI_ROPE): heads of rope_hd columns, the
+    // first rope_nq query heads, then rope_nkv key and rope_nkv value heads;
+    // outputs head-major [H, m_tok, hd] BF16
+    const int *rope_pos;
+    const float *rope_freq;
+    int rope_hd, rope_nq, rope_nkv;
+    uint16_t *rope_q, *rope_k, *rope_v;
 };
 
 struct GemmLaunch {

@@ -4,8 +4,10 @@
 // (agentlenshq FlashRT summary, "What it is"; itsolotime FlashRT article, 5.2
 // FusedQKV; "FlashRT docs/architecture.md", 8 Kernel Library).
 //
-// Per call three kernels on the caller's stream, each with a programmatic-
-// dependent-launch edge to its predecessor.  Tensor maps are encoded per
+// Per call two or three kernels on the caller's stream, each with a
+// programmatic-dependent-launch edge to its predecessor: the split + RoPE
+// runs in the GEMM's epilogue where the GEMM's tiles hold whole heads and
+// need no split-K (many tokens), else as a kernel of its own.  Tensor maps are encoded per
 // launch on the host (kernel parameters), so a forward holds no state that a
 // later call could invalidate, and it can be captured by the caller.
 #include <cuda_runtime.h>
@@ -13,6 +15,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <vector>
 
@@ -90,9 +93,12 @@ frt_status check_layer_ready(frt_qkv_plan *P, int layer) {
     return FRT_OK;
 }
 
-// The fused-QKV GEMM launch of layer l for M tokens (BF16 epilogue into the
-// plan's qkv scratch); tensor maps encoded here.
-frt_status setup_qkv_gemm(frt_qkv_plan *P, GemmLaunch &g, int l, int M) {
+// The fused-QKV GEMM launch of layer l for M tokens; tensor maps encoded
+// here.  Epilogue: the split + RoPE itself (tiled tiles without split-K that
+// hold whole heads; outputs q, k, v) when `fuse` allows, else BF16 into the
+// plan's qkv scratch for the split + RoPE kernel.  *fused tells which.
+frt_status setup_qkv_gemm(frt_qkv_plan *P, GemmLaunch &g, int l, int M, bool fuse, const int *pos, void *q,
+                          void *k, void *v, bool *fused) {
     const bool swap = M <= QKV_SWAP_MAX_TOKENS;
     memset(&g.p, 0, sizeof g.p);
     plan_gemm(g, swap, M, P->N, P->d, P->num_sms, 0);
@@ -109,10 +115,19 @@ frt_status setup_qkv_gemm(frt_qkv_plan *P, GemmLaunch &g, int l, int M) {
     }
     if (e1 != cudaSuccess || e2 != cudaSuccess)
         return qfail(FRT_ERR_CUDA, "cuTensorMapEncodeTiled failed");
-    g.p.epi = EPI_BF16;
+    *fused = fuse && !swap && g.p.splits == 1 && g.bn % P->hd == 0 && P->hd % 64 == 0;
+    g.p.epi = *fused ? EPI_ROPE : EPI_BF16;
     g.p.alpha = P->s_x[l] * P->s_qkv[l];
     g.p.out = P->qkv;
     g.p.ldo = P->N;
+    g.p.rope_pos = pos;
+    g.p.rope_freq = P->inv_freq;
+    g.p.rope_hd = P->hd;
+    g.p.rope_nq = P->nq;
+    g.p.rope_nkv = P->nkv;
+    g.p.rope_q = static_cast<uint16_t *>(q);
+    g.p.rope_k = static_cast<uint16_t *>(k);
+    g.p.rope_v = static_cast<uint16_t *>(v);
     g.p.ws = P->ws;
     g.p.counters = split_counters(P->counters, g.p.splits);
     g.p.err = P->err;
@@ -121,8 +136,14 @@ frt_status setup_qkv_gemm(frt_qkv_plan *P, GemmLaunch &g, int l, int M) {
 
 frt_status run_qkv(frt_qkv_plan *P, int l, const void *r, const void *h, const int *pos, void *rp, void *q, void *k,
                    void *v, int M, cudaStream_t s, void *trace_qx, void *trace_qkv) {
+    // the split + RoPE in the GEMM's epilogue where it can run there
+    // (FRT_QKV_FUSE=0 keeps it a kernel of its own); a trace of the
+    // intermediates needs the GEMM's BF16 output, so it runs the kernel
+    const char *fe = getenv("FRT_QKV_FUSE");
+    const bool fuse = !trace_qkv && !(fe && fe[0] == '0');
     GemmLaunch g;
-    frt_status st = setup_qkv_gemm(P, g, l, M);
+    bool fused = false;
+    frt_status st = setup_qkv_gemm(P, g, l, M, fuse, pos, q, k, v, &fused);
     if (st != FRT_OK)
         return st;
     const float inv_sx = 1.0f / P->s_x[l];
@@ -130,7 +151,8 @@ frt_status run_qkv(frt_qkv_plan *P, int l, const void *r, const void *h, const i
     QCK(launch_norm_quant(r, h, P->w_norm + (size_t)l * P->d, M, P->d, QKV_RMS_EPS, inv_sx, h ? rp : nullptr, P->qx,
                           nullptr, false, s, true));
     QCK(launch_gemm(g, s, true));
-    QCK(launch_rope_split(P->qkv, M, P->nq, P->nkv, P->hd, pos, P->inv_freq, q, k, v, s, true));
+    if (!fused)
+        QCK(launch_rope_split(P->qkv, M, P->nq, P->nkv, P->hd, pos, P->inv_freq, q, k, v, s, true));
     if (rp && !h)
         QCK(cudaMemcpyAsync(rp, r, (size_t)M * P->d * 2, cudaMemcpyDeviceToDevice, s));
     if (trace_qx)

@@ -638,7 +638,60 @@ __device__ __forceinline__ void consume_unit(const GemmParams &p, const Unit &w,
     const int r = threadIdx.x;
     const bool gated_epi = p.epi == EPI_GATED || p.epi == EPI_GATED_AMAX;
     float amax = 0.0f;
-    if (gated_epi && !SWAP) {
+    if (!SWAP && p.epi == EPI_ROPE) {
+        // QKV split + RoPE of a token row (the tile's heads whole: BN % hd == 0,
+        // hd % 64 == 0): element i of a head's first half pairs with i + hd/2;
+        // x = bf16(acc * alpha), angle = pos * theta_i (fp32), then in fp32
+        // x_i cos - x_{i+hd/2} sin and x_{i+hd/2} cos + x_i sin, rounded to BF16
+        const int m = w.tp * BM + r;
+        const bool live = m < p.m_tok;
+        const int hd = p.rope_hd, half = hd / 2;
+        const float pos = live ? (float)p.rope_pos[m] : 0.0f;
+#pragma unroll 1
+        for (int hc = 0; hc < BN; hc += hd) {
+            const int head = (w.tq * BN + hc) / hd;
+            const bool rot = head < p.rope_nq + p.rope_nkv;
+            uint16_t *dst = head < p.rope_nq ? p.rope_q + ((size_t)head * p.m_tok + m) * hd
+                            : rot ? p.rope_k + ((size_t)(head - p.rope_nq) * p.m_tok + m) * hd
+                                  : p.rope_v + ((size_t)(head - p.rope_nq - p.rope_nkv) * p.m_tok + m) * hd;
+#pragma unroll 1
+            for (int j = 0; j < half; j += CH) {
+                float a[CH], b[CH];
+                tmem_load_chunk<CH>(tbase + hc + j, a);
+                tmem_load_chunk<CH>(tbase + hc + half + j, b);
+                if (!live)
+                    continue;
+#pragma unroll
+                for (int e = 0; e < CH; ++e) {
+                    const float x1 = round_bf16(__fmul_rn(a[e], p.alpha));
+                    const float x2 = round_bf16(__fmul_rn(b[e], p.alpha));
+                    if (rot) {
+                        float sn, cs;
+                        sincosf(__fmul_rn(pos, __ldg(p.rope_freq + j + e)), &sn, &cs);
+                        a[e] = __fsub_rn(__fmul_rn(x1, cs), __fmul_rn(x2, sn));
+                        b[e] = __fadd_rn(__fmul_rn(x2, cs), __fmul_rn(x1, sn));
+                    } else {
+                        a[e] = x1;
+                        b[e] = x2;
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < CH; e += 8) {
+                    uint4 o1, o2;
+                    o1.x = bf16_bits(a[e]) | (bf16_bits(a[e + 1]) << 16);
+                    o1.y = bf16_bits(a[e + 2]) | (bf16_bits(a[e + 3]) << 16);
+                    o1.z = bf16_bits(a[e + 4]) | (bf16_bits(a[e + 5]) << 16);
+                    o1.w = bf16_bits(a[e + 6]) | (bf16_bits(a[e + 7]) << 16);
+                    o2.x = bf16_bits(b[e]) | (bf16_bits(b[e + 1]) << 16);
+                    o2.y = bf16_bits(b[e + 2]) | (bf16_bits(b[e + 3]) << 16);
+                    o2.z = bf16_bits(b[e + 4]) | (bf16_bits(b[e + 5]) << 16);
+                    o2.w = bf16_bits(b[e + 6]) | (bf16_bits(b[e + 7]) << 16);
+                    *reinterpret_cast<uint4 *>(dst + j + e) = o1;
+                    *reinterpret_cast<uint4 *>(dst + half + j + e) = o2;
+                }
+            }
+        }
+    } else if (gated_epi && !SWAP) {
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 128) {
 #pragma unroll 1

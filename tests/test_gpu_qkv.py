@@ -21,6 +21,9 @@ SHAPES = [
     ("ragged", 17, 384, 6, 3, 32, 1.0e4, 100, True),
     ("tiled", 300, 512, 4, 2, 64, 1.0e4, 0, False),
     ("far_positions", 3, 256, 4, 2, 32, 1.0e6, 100000, False),
+    # tiled tiles without split-K that hold whole heads: split + RoPE in the GEMM epilogue
+    ("fused_hd256", 1000, 512, 8, 1, 256, 1.0e4, 0, True),
+    ("fused_hd128", 1280, 256, 12, 2, 128, 1.0e6, 7, False),
 ]
 
 
@@ -76,7 +79,8 @@ def test_sublayer_matches_oracle(case):
         got = bits(tr[k])
         assert got.shape == getattr(ref, k).shape, k
         check_bf16(got[:, rows], getattr(ref, k)[:, rows], "%s %s" % (c["name"], k))
-    # the forward entry point computes the same as the trace
+    # the forward entry point computes the same as the trace (which runs the
+    # split + RoPE kernel; the forward may run it in the GEMM's epilogue)
     o = c["plan"].forward(0, c["r"].to(dev), c["h"].to(dev) if c["h"] is not None else None,
                           torch.from_numpy(c["pos"]).to(dev))
     torch.cuda.synchronize()
