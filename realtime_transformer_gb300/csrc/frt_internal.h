@@ -59,8 +59,7 @@ struct GemmParams {
     // QKV split + RoPE epilogue (EPI_ROPE): heads of rope_hd columns, the
     // first rope_nq query heads, then rope_nkv key and rope_nkv value heads;
     // outputs head-major [H, m_tok, hd] BF16
-    const int *rope_pos;
-    const float *rope_freq;
+    const float2 *rope_cs;  // (cos, sin) [m_tok, hd / 2] of each token's angles
     int rope_hd, rope_nq, rope_nkv;
     uint16_t *rope_q, *rope_k, *rope_v;
 };
@@ -101,6 +100,8 @@ cudaError_t launch_quant_bf16(const void *x, size_t n, float inv_s, uint8_t *q, 
 cudaError_t launch_quant_gu_interleave(const void *gate, const void *up, int ff, int d, const void *fold,
                                       float inv_s, uint8_t *dst, cudaStream_t s);
 cudaError_t launch_amax_fold(const void *x, size_t rows, int d, const void *w, unsigned *amax_word, cudaStream_t s);
+cudaError_t launch_rope_table(const int *pos, const float *inv_freq, int M, int half, float2 *cs, cudaStream_t s,
+                              bool pdl);
 cudaError_t launch_rope_split(const void *qkv, int M, int nq, int nkv, int hd, const int *pos, const float *inv_freq,
                               void *q, void *k, void *v, cudaStream_t s, bool pdl);
 cudaError_t launch_norm_quant(const void *r, const void *h, const void *w, int M, int d, float eps, float inv_s,

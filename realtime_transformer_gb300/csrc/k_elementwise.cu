@@ -400,6 +400,23 @@ __global__ void __launch_bounds__(256) k_rope_split(const uint16_t *__restrict__
     }
 }
 
+// (cos, sin) of angle pos[m] * theta_i for every token and pair: the table the
+// GEMM epilogue's fused split + RoPE reads (the same sincosf of the same fp32
+// angle as k_rope_split, so both give the same bits).
+__global__ void __launch_bounds__(256) k_rope_table(const int *__restrict__ pos, const float *__restrict__ inv_freq,
+                                                   int M, int half, float2 *__restrict__ cs) {
+    pdl_trigger();
+    pdl_wait();
+    const size_t total = (size_t)M * half;
+    for (size_t t = blockIdx.x * (size_t)blockDim.x + threadIdx.x; t < total; t += (size_t)gridDim.x * blockDim.x) {
+        const int i = (int)(t % half);
+        const int m = (int)(t / half);
+        float sn, c;
+        sincosf(__fmul_rn((float)__ldg(pos + m), __ldg(inv_freq + i)), &sn, &c);
+        cs[t] = make_float2(c, sn);
+    }
+}
+
 int sm_count() {
     static int n = 0;
     if (n == 0) {
@@ -538,6 +555,16 @@ cudaError_t launch_rope_split(const void *qkv, int M, int nq, int nkv, int hd, c
     return launch_ex(k_rope_split, dim3((unsigned)blocks), dim3(256), 0, s, pdl, 1u,
                      static_cast<const uint16_t *>(qkv), M, nq, nkv, hd, pos, inv_freq, static_cast<uint16_t *>(q),
                      static_cast<uint16_t *>(k), static_cast<uint16_t *>(v));
+}
+
+cudaError_t launch_rope_table(const int *pos, const float *inv_freq, int M, int half, float2 *cs, cudaStream_t s,
+                              bool pdl) {
+    const size_t total = (size_t)M * half;
+    size_t blocks = (total + 255) / 256;
+    const size_t cap = (size_t)sm_count() * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks == 0) blocks = 1;
+    return launch_ex(k_rope_table, dim3((unsigned)blocks), dim3(256), 0, s, pdl, 1u, pos, inv_freq, M, half, cs);
 }
 
 }  // namespace frt

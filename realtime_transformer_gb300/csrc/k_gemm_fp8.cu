@@ -641,12 +641,13 @@ __device__ __forceinline__ void consume_unit(const GemmParams &p, const Unit &w,
     if (!SWAP && p.epi == EPI_ROPE) {
         // QKV split + RoPE of a token row (the tile's heads whole: BN % hd == 0,
         // hd % 64 == 0): element i of a head's first half pairs with i + hd/2;
-        // x = bf16(acc * alpha), angle = pos * theta_i (fp32), then in fp32
-        // x_i cos - x_{i+hd/2} sin and x_{i+hd/2} cos + x_i sin, rounded to BF16
+        // x = bf16(acc * alpha), (cos, sin) of the token's angle pos * theta_i
+        // from rope_cs [m_tok, hd/2], then in fp32 x_i cos - x_{i+hd/2} sin and
+        // x_{i+hd/2} cos + x_i sin, rounded to BF16
         const int m = w.tp * BM + r;
         const bool live = m < p.m_tok;
         const int hd = p.rope_hd, half = hd / 2;
-        const float pos = live ? (float)p.rope_pos[m] : 0.0f;
+        const float2 *cs_row = p.rope_cs + (size_t)(live ? m : 0) * half;
 #pragma unroll 1
         for (int hc = 0; hc < BN; hc += hd) {
             const int head = (w.tq * BN + hc) / hd;
@@ -666,10 +667,9 @@ __device__ __forceinline__ void consume_unit(const GemmParams &p, const Unit &w,
                     const float x1 = round_bf16(__fmul_rn(a[e], p.alpha));
                     const float x2 = round_bf16(__fmul_rn(b[e], p.alpha));
                     if (rot) {
-                        float sn, cs;
-                        sincosf(__fmul_rn(pos, __ldg(p.rope_freq + j + e)), &sn, &cs);
-                        a[e] = __fsub_rn(__fmul_rn(x1, cs), __fmul_rn(x2, sn));
-                        b[e] = __fadd_rn(__fmul_rn(x2, cs), __fmul_rn(x1, sn));
+                        const float2 t = cs_row[j + e];
+                        a[e] = __fsub_rn(__fmul_rn(x1, t.x), __fmul_rn(x2, t.y));
+                        b[e] = __fadd_rn(__fmul_rn(x2, t.x), __fmul_rn(x1, t.y));
                     } else {
                         a[e] = x1;
                         b[e] = x2;

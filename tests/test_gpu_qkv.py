@@ -59,8 +59,9 @@ def test_weight_scale_matches_oracle_exactly(case):
     assert case["plan"].scales()["s_qkv"][0] == np.float32(case["s_qkv"])
 
 
-def test_sublayer_matches_oracle(case):
+def test_sublayer_matches_oracle(case, monkeypatch):
     c = case
+    monkeypatch.setenv("FRT_QKV_FUSE", "1")  # the fused split + RoPE wherever the tiles allow it
     dev = c["dev"]
     tr = c["plan"].trace(0, c["r"].to(dev), c["h"].to(dev) if c["h"] is not None else None,
                          torch.from_numpy(c["pos"]).to(dev))
@@ -86,6 +87,12 @@ def test_sublayer_matches_oracle(case):
     torch.cuda.synchronize()
     for k in ("q", "k", "v", "r_prime"):
         assert torch.equal(o[k], tr[k]), k
+    monkeypatch.setenv("FRT_QKV_FUSE", "0")
+    o2 = c["plan"].forward(0, c["r"].to(dev), c["h"].to(dev) if c["h"] is not None else None,
+                           torch.from_numpy(c["pos"]).to(dev))
+    torch.cuda.synchronize()
+    for k in ("q", "k", "v"):
+        assert torch.equal(o2[k], tr[k]), k
 
 
 def test_gpu_calibration_matches_oracle(case):
