@@ -91,8 +91,9 @@ struct Unit {
 // Epilogue roles a kernel is compiled for: every epilogue (ROLE_ANY), or
 // only the one a launch of the layer uses -- the weight-streaming gated
 // epilogue without split-K (the gate/up GEMM) or the plain cluster split-K
-// epilogue (the down GEMM) -- so that the code a launch runs is compact.
-enum Role : int { ROLE_ANY = 0, ROLE_GATED_TILE = 1, ROLE_CLUSTER_PLAIN = 2 };
+// epilogue (the down GEMM) -- so that the code a launch runs is compact; the
+// tiled QKV split + RoPE epilogue (ROLE_ROPE) is compiled only for itself.
+enum Role : int { ROLE_ANY = 0, ROLE_GATED_TILE = 1, ROLE_CLUSTER_PLAIN = 2, ROLE_ROPE = 3 };
 
 // Tiles run in groups of p.group P-tiles: within a group the P-tile index
 // changes fastest, so a wave of CTAs covers a block of group x (SMs / group)
@@ -631,14 +632,14 @@ __device__ __forceinline__ float warp_max_f(float v) {
 
 // Consume one unit's accumulator from TMEM: the tiled gated epilogue, or a
 // plain one (the weight-streaming gated epilogue is gated_swap_tile).
-template <int BN, bool SWAP>
+template <int BN, bool SWAP, bool ROPE = false>
 __device__ __forceinline__ void consume_unit(const GemmParams &p, const Unit &w, uint32_t tbase) {
     using C = Cfg<BN, SWAP>;
     constexpr int CH = C::CH;
     const int r = threadIdx.x;
     const bool gated_epi = p.epi == EPI_GATED || p.epi == EPI_GATED_AMAX;
     float amax = 0.0f;
-    if (!SWAP && p.epi == EPI_ROPE) {
+    if constexpr (!SWAP && ROPE) {
         // QKV split + RoPE of a token row (the tile's heads whole: BN % hd == 0,
         // hd % 64 == 0): element i of a head's first half pairs with i + hd/2;
         // x = bf16(acc * alpha), (cos, sin) of the token's angle pos * theta_i
@@ -1270,7 +1271,7 @@ __device__ void epilogue(const GemmParams &p, uint64_t *tfull, uint64_t *tempty,
                     }
                 }
             } else {
-                consume_unit<BN, SWAP>(p, w, tbase);
+                consume_unit<BN, SWAP, ROLE == ROLE_ROPE>(p, w, tbase);
                 tc_fence_before();
                 if constexpr (PAIR) {
                     // the even CTA's MMA refills both CTAs' accumulators:
@@ -1686,6 +1687,13 @@ cudaError_t launch_gemm(const GemmLaunch &g, cudaStream_t s, bool pdl) {
         case 64 * 4 + ROLE_ANY: return run<64, true, false, ROLE_ANY>(g, s, pdl);
         case 64 * 4 + ROLE_GATED_TILE: return run<64, true, false, ROLE_GATED_TILE>(g, s, pdl);
         case 64 * 4 + ROLE_CLUSTER_PLAIN: return run<64, true, false, ROLE_CLUSTER_PLAIN>(g, s, pdl);
+        default: return cudaErrorInvalidValue;
+        }
+    }
+    if (g.p.epi == EPI_ROPE) {
+        switch (g.bn) {
+        case 128: return run<128, false, false, ROLE_ROPE>(g, s, pdl);
+        case 256: return g.p.pair ? run<256, false, true, ROLE_ROPE>(g, s, pdl) : run<256, false, false, ROLE_ROPE>(g, s, pdl);
         default: return cudaErrorInvalidValue;
         }
     }
