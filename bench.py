@@ -263,6 +263,9 @@ def run_ours(args, wl, world, rank, local):
     torch.cuda.set_device(dev)
     P = peaks()
     weights, r, h, calib = gen_workload(wl, dev)
+    # residual and hidden side by side in one buffer: one host-to-device copy per step
+    io = torch.stack([r, h]).contiguous()
+    r, h = io[0], io[1]
     plan = FFNPlan(wl.d, wl.ff, wl.act, wl.M, wl.L)
     for l, w in enumerate(weights):
         plan.load_weights(l, w["w_norm"], w["w_gate"], w["w_up"], w["w_down"])
@@ -312,19 +315,17 @@ def run_ours(args, wl, world, rank, local):
     ms_step = 1000.0 * total_s / args.steps
 
     # end to end through the public API: pinned host in, graph, host out
-    h_r = r.cpu().pin_memory()
-    h_h = h.cpu().pin_memory()
+    h_io = io.cpu().pin_memory()
     h_o = torch.empty_like(out, device="cpu").pin_memory()
 
     def e2e_step():
-        r.copy_(h_r, non_blocking=True)
-        h.copy_(h_h, non_blocking=True)
+        io.copy_(h_io, non_blocking=True)
         plan.graph_replay(wl.M, stream)
         h_o.copy_(out, non_blocking=True)
 
     e2e_ms = timed(e2e_step, args.steps, args.warmup)
     e2e_s = reduce_max(sum(e2e_ms) / 1000.0, world, dev)
-    h2d = h_r.numel() * 2 + h_h.numel() * 2
+    h2d = h_io.numel() * 2
     d2h = h_o.numel() * 2
 
     # per-kernel timing (one layer's four kernels launched alone)
