@@ -328,7 +328,7 @@ def run_ours(args, wl, world, rank, local):
     h2d = h_io.numel() * 2
     d2h = h_o.numel() * 2
 
-    # per-kernel timing (one layer's four kernels launched alone)
+    # per-kernel timing (one layer's three kernels launched alone)
     kern = {}
     n_k = max(20, min(200, args.steps))
     for step in range(len(STEP_NAMES)):
