@@ -55,7 +55,9 @@ def test_exact_sum_inputs_are_bit_exact(plan, M, N, K, path, splits):
 
 
 @pytest.mark.parametrize("M,N,K,path,splits", [(50, 1024, 1024, 1, 0), (7, 256, 4096, 1, 8), (300, 512, 2048, 2, 0),
-                                               (256, 256, 5120, 2, 3)])
+                                               (256, 256, 5120, 2, 3),
+                                               # weight-streaming with idle SMs / a ragged second wave of tiles
+                                               (8, 2176, 13824, 1, 0), (4, 20480, 1536, 1, 0), (1, 7168, 5120, 1, 0)])
 def test_random_codes_within_summation_bound(plan, M, N, K, path, splits):
     rng = np.random.default_rng(K + M)
     A = rng.integers(0, 256, (M, K)).astype(np.uint8)

@@ -37,6 +37,8 @@ SHAPES = [
                      seed=15),
     # two token tiles: CTA pairs with split-K on both GEMMs
     WL["tiny"].with_(name="m130_pairs", M=130, d=512, ff=1024, n_calib=1, seed=16),
+    # wide decode-like layer: 128 gate/up tiles, 4-way cluster split-K down GEMM
+    WL["llm_decode"].with_(name="m2_wide", M=2, d=4096, ff=8192, L=1, seed=19),
 ]
 
 
