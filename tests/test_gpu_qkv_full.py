@@ -1,0 +1,47 @@
+"""Attention-input sublayer at the workloads' full sizes, in the launch
+configuration the benchmark times (full M; on the long-prefill shape the split
++ RoPE runs in the GEMM epilogue).  Rows are independent once the scale is
+fixed, so the oracle checks a handful of rows spread over the token tiles,
+the last row included (agentlenshq FlashRT summary, "What it is";
+itsolotime FlashRT article, 5.2 FusedQKV)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic
+from parity import bits, check_bf16, check_codes
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("name", ["vla_action_expert", "vla_prefix", "llm_decode", "long_prefill"])
+def test_full_size_qkv(name):
+    from realtime_transformer_gb300.qkv import QKVPlan
+    wl = synthetic.WORKLOADS[name]
+    nq, nkv, hd, base = synthetic.ATTENTION[name]
+    dev = torch.device("cuda")
+    w = synthetic.qkv_weights(wl, 0, device=dev)
+    r, h = synthetic.inputs(wl, device=dev)
+    pos = synthetic.positions(wl)
+    hw = {k: bits(v) for k, v in w.items()}
+    codes, s_qkv = oracle.quantize_qkv_weights(hw["w_q"], hw["w_k"], hw["w_v"])
+    crow = min(wl.M, 64)
+    s_x = oracle.calibrate_qkv_layer([bits(r[:crow])], [bits(h[:crow])], hw["w_norm"])
+    plan = QKVPlan(wl.d, nq, nkv, hd, base, wl.M, 1)
+    plan.load_weights(0, w["w_norm"], w["w_q"], w["w_k"], w["w_v"])
+    assert plan.scales()["s_qkv"][0] == np.float32(s_qkv)
+    plan.set_scales([s_x])
+    out = plan.forward(0, r, h, torch.from_numpy(pos).to(dev))
+    torch.cuda.synchronize()
+    plan.device_status()
+    rows = np.array(sorted(set([0, wl.M - 1] + [int(x) for x in np.linspace(0, wl.M - 1, 8)])), dtype=np.int64)
+    hr = bits(r)[rows]
+    hh = bits(h)[rows]
+    ref = oracle.qkv_layer(hr, hh, hw["w_norm"], codes, s_x, s_qkv, nq, nkv, hd, pos[rows],
+                           oracle.rope_inv_freq(hd, base))
+    assert np.array_equal(bits(out["r_prime"])[rows], ref.r_prime)
+    for k in ("q", "k", "v"):
+        got = bits(out[k])[:, rows]
+        check_bf16(got, getattr(ref, k), "%s %s" % (name, k))
+    plan.close()
