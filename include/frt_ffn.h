@@ -171,17 +171,23 @@ frt_status frt_ffn_graph_replay(frt_ffn_plan_t plan, int M, frt_stream_t stream)
 /*
  * Tactic-stable capture ("FlashRT docs/architecture.md", 7 Graph: re-capture
  * up to N times and keep the fastest schedule).  Captures the forward for M
- * n_tries times as frt_ffn_graph_capture does, times n_replays replays of each
- * capture (CUDA events on `stream`, each replay timed alone, after one untimed
- * replay; the median counts), and keeps the fastest capture as the plan's
- * graph for M.  The timed replays run the forward, so `out` holds its result
- * afterwards.  *best_us (may be NULL) receives the kept graph's median replay
- * time in microseconds.  Synchronises `stream`.  1 <= n_tries <= 64,
- * 1 <= n_replays <= 10000.  Errors: as frt_ffn_graph_capture, INVALID_ARG for
- * the counts, CUDA for a failed replay or timing.
+ * n_tries times as frt_ffn_graph_capture does, cycling through the schedules
+ * below (each gives the same results bit for bit), times n_replays replays of
+ * each capture (CUDA events on `stream`, each replay timed alone, after one
+ * untimed replay; the median counts), and keeps the fastest capture as the
+ * plan's graph for M.  Schedules: 0 the defaults, 1 split-K partials
+ * exchanged through global memory instead of inside a cluster, 2 single-CTA
+ * tiles instead of CTA pairs (many tokens), 3 no programmatic dependent
+ * launch.  The timed replays run the forward, so `out` holds its result
+ * afterwards.  *best_us and *best_tactic (either may be NULL) receive the kept
+ * graph's median replay time in microseconds and its schedule.  Synchronises
+ * `stream`.  1 <= n_tries <= 64, 1 <= n_replays <= 10000.  Errors: as
+ * frt_ffn_graph_capture, INVALID_ARG for the counts, CUDA for a failed replay
+ * or timing.
  */
 frt_status frt_ffn_graph_autotune(frt_ffn_plan_t plan, const void *residual_in, const void *hidden_in, void *out,
-                                  int M, int n_tries, int n_replays, float *best_us, frt_stream_t stream);
+                                  int M, int n_tries, int n_replays, float *best_us, int *best_tactic,
+                                  frt_stream_t stream);
 
 /*
  * Test/diagnostic: run layer `layer` alone on residual_in (+ hidden_in if not

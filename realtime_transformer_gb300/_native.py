@@ -38,7 +38,8 @@ SIGNATURES = {
     "frt_ffn_forward": (_I, [_P, _P, _P, _P, _I, _P]),
     "frt_ffn_graph_capture": (_I, [_P, _P, _P, _P, _I, _P]),
     "frt_ffn_graph_replay": (_I, [_P, _I, _P]),
-    "frt_ffn_graph_autotune": (_I, [_P, _P, _P, _P, _I, _I, _I, ctypes.POINTER(ctypes.c_float), _P]),
+    "frt_ffn_graph_autotune": (_I, [_P, _P, _P, _P, _I, _I, _I, ctypes.POINTER(ctypes.c_float),
+                                   ctypes.POINTER(ctypes.c_int), _P]),
     "frt_ffn_debug_trace": (_I, [_P, _I, _P, _P, _I, _P, _P, _P, _P, _P, _P]),
     "frt_ffn_device_status": (_I, [_P, _P]),
     "frt_ffn_debug_stall": (_I, [_P, _P]),
@@ -151,11 +152,16 @@ def frt_ffn_graph_replay(plan, M, stream) -> None:
     _check(lib().frt_ffn_graph_replay(plan, M, stream))
 
 
-def frt_ffn_graph_autotune(plan, residual_in, hidden_in, out, M, n_tries, n_replays, stream) -> float:
+GRAPH_TACTICS = ("defaults", "global split-K exchange", "single-CTA tiles", "no programmatic dependent launch")
+
+
+def frt_ffn_graph_autotune(plan, residual_in, hidden_in, out, M, n_tries, n_replays, stream):
+    """-> (median replay time of the kept graph in us, index into GRAPH_TACTICS)."""
     best = ctypes.c_float(0.0)
+    tactic = ctypes.c_int(0)
     _check(lib().frt_ffn_graph_autotune(plan, residual_in, hidden_in, out, M, n_tries, n_replays,
-                                        ctypes.byref(best), stream))
-    return best.value
+                                        ctypes.byref(best), ctypes.byref(tactic), stream))
+    return best.value, tactic.value
 
 
 def frt_ffn_debug_trace(plan, layer, residual_in, hidden_in, M, r_prime, q_x, gu, q_h, out, stream) -> None:

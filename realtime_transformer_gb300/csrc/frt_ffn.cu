@@ -113,6 +113,7 @@ struct frt_ffn_plan {
     int force_path = 0;        // 0 auto, 1 swap, 2 tiled (FRT_FFN_FORCE_PATH)
     bool pdl = true;           // programmatic dependent launch (FRT_FFN_NO_PDL=1 disables)
     int max_splits = 0;        // cap on split-K (FRT_FFN_MAX_SPLITS; 0 = none)
+    const Tactic *tactic = nullptr;  // schedule variant of the capture being autotuned (null: defaults)
 };
 
 namespace {
@@ -180,9 +181,9 @@ frt_status setup_gemm(frt_ffn_plan *P, GemmLaunch &g, int site, int l, int M) {
     int force = 0;
     if (const char *e = getenv(site == 0 ? "FRT_FFN_GU_SPLITS" : "FRT_FFN_DOWN_SPLITS"))
         force = atoi(e);
-    plan_gemm(g, swap, M, N, K, P->num_sms, force);
+    plan_gemm(g, swap, M, N, K, P->num_sms, force, P->tactic);
     if (P->max_splits > 0 && g.p.splits > P->max_splits)
-        plan_gemm(g, swap, M, N, K, P->num_sms, P->max_splits);
+        plan_gemm(g, swap, M, N, K, P->num_sms, P->max_splits, P->tactic);
     frt_status st;
     if (swap) {
         if ((st = get_tmap(P, wbuf, 128, &g.tmP, &g.p.gtm_p)) != FRT_OK) return st;
@@ -718,30 +719,52 @@ FRT_API frt_status frt_ffn_graph_capture(frt_ffn_plan_t P, const void *residual_
     return FRT_OK;
 }
 
+// Schedules tried by the autotuned capture, each giving the same results
+// bit for bit: the defaults; split-K partials exchanged through global memory;
+// single-CTA tiles instead of CTA pairs; launches without programmatic
+// dependent launch.
+constexpr int N_TACTICS = 4;
+
 FRT_API frt_status frt_ffn_graph_autotune(frt_ffn_plan_t P, const void *residual_in, const void *hidden_in,
                                           void *out, int M, int n_tries, int n_replays, float *best_us,
-                                          frt_stream_t stream) {
+                                          int *best_tactic, frt_stream_t stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (n_tries < 1 || n_tries > 64 || n_replays < 1 || n_replays > 10000)
         return fail(FRT_ERR_INVALID_ARG, "need 1 <= n_tries <= 64 and 1 <= n_replays <= 10000");
     frt_status st = capture_checks(P, residual_in, hidden_in, out, M, s);
     if (st != FRT_OK)
         return st;
+    const bool pdl0 = P->pdl;
+    // FRT_FFN_AUTOTUNE_ONLY=k: every capture uses schedule k (tests, tuning)
+    const char *only = getenv("FRT_FFN_AUTOTUNE_ONLY");
+    const int only_k = only ? atoi(only) : -1;
     GraphEntry best;
     float best_t = 0.0f;
+    int best_k = 0;
     for (int i = 0; i < n_tries; ++i) {
+        const int k = (only_k >= 0 && only_k < N_TACTICS) ? only_k : i % N_TACTICS;
+        Tactic t;
+        t.global_exchange = k == 1;
+        t.no_pairs = k == 2;
+        P->tactic = &t;
+        P->pdl = pdl0 && k != 3;
         GraphEntry ge;
-        float t = 0.0f;
-        if ((st = capture_one(P, residual_in, hidden_in, out, M, s, ge)) != FRT_OK ||
-            (st = time_replays(ge.exec, n_replays, s, &t)) != FRT_OK) {
+        float tm = 0.0f;
+        st = capture_one(P, residual_in, hidden_in, out, M, s, ge);
+        P->tactic = nullptr;
+        P->pdl = pdl0;
+        if (st == FRT_OK)
+            st = time_replays(ge.exec, n_replays, s, &tm);
+        if (st != FRT_OK) {
             destroy_graph(ge);
             destroy_graph(best);
             return st;
         }
-        if (!best.exec || t < best_t) {
+        if (!best.exec || tm < best_t) {
             destroy_graph(best);
             best = ge;
-            best_t = t;
+            best_t = tm;
+            best_k = k;
         } else {
             destroy_graph(ge);
         }
@@ -749,6 +772,8 @@ FRT_API frt_status frt_ffn_graph_autotune(frt_ffn_plan_t P, const void *residual
     install_graph(P, M, best);
     if (best_us)
         *best_us = best_t;
+    if (best_tactic)
+        *best_tactic = best_k;
     return FRT_OK;
 }
 

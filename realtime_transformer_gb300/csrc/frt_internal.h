@@ -88,9 +88,20 @@ inline int *split_counters(int *base, int splits) { return base + (size_t)splits
 // box of 128 bytes x box_rows rows, 128-byte swizzle.
 cudaError_t encode_tmap_u8(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows);
 
+// Schedule variants of a GEMM launch that leave its results unchanged bit
+// for bit (a "tactic"): the split-K partials exchanged through global memory
+// instead of inside a cluster (same splits, same reduction order), and the
+// tiled role on single CTAs instead of CTA pairs.
+struct Tactic {
+    bool global_exchange = false;
+    bool no_pairs = false;
+};
+
 // Choose tiling / split-K for a GEMM of m_tok tokens x n_feat features x K
-// and fill the launch (tensor maps excluded).  swap: weight-streaming path.
-void plan_gemm(GemmLaunch &g, bool swap, int m_tok, int n_feat, int K, int num_sms, int force_splits);
+// and fill the launch (tensor maps excluded).  swap: weight-streaming path;
+// tactic: null for the defaults.
+void plan_gemm(GemmLaunch &g, bool swap, int m_tok, int n_feat, int K, int num_sms, int force_splits,
+               const Tactic *tactic = nullptr);
 size_t gemm_ws_floats(const GemmLaunch &g);
 int gemm_tiles(const GemmLaunch &g);
 cudaError_t launch_gemm(const GemmLaunch &g, cudaStream_t s, bool pdl);

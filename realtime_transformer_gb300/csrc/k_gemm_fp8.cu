@@ -1536,7 +1536,8 @@ constexpr size_t SPREAD_SMEM = 115 * 1024;
 
 }  // namespace
 
-void plan_gemm(GemmLaunch &g, bool swap, int m_tok, int n_feat, int K, int num_sms, int force_splits) {
+void plan_gemm(GemmLaunch &g, bool swap, int m_tok, int n_feat, int K, int num_sms, int force_splits,
+               const Tactic *tactic) {
     GemmParams &p = g.p;
     g.swap = swap;
     p.k_blocks = (K + BK - 1) / BK;
@@ -1600,7 +1601,7 @@ void plan_gemm(GemmLaunch &g, bool swap, int m_tok, int n_feat, int K, int num_s
     // per CTA and 7 pipeline stages instead of 4; 256-wide tiles on an even
     // number of token tiles
     p.pair = 0;
-    if (!swap && p.mcast == 1 && g.bn == 256 && p.n_tiles_p % 2 == 0) {
+    if (!swap && p.mcast == 1 && g.bn == 256 && p.n_tiles_p % 2 == 0 && !(tactic && tactic->no_pairs)) {
         const char *e = getenv("FRT_FFN_PAIR");
         if (!(e && e[0] == '0')) {
             p.pair = 1;
@@ -1633,7 +1634,8 @@ void plan_gemm(GemmLaunch &g, bool swap, int m_tok, int n_feat, int K, int num_s
         if (v >= 2)
             p.stages = std::min(v, si.max_stages);
     }
-    p.cluster = (cluster_on && p.splits >= 2 && p.splits <= CLUSTER_MAX) ? 1 : 0;
+    p.cluster = (cluster_on && p.splits >= 2 && p.splits <= CLUSTER_MAX && !(tactic && tactic->global_exchange))
+                    ? 1 : 0;
 
     if (p.cluster)
         g.grid = p.total_units;

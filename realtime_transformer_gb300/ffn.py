@@ -134,9 +134,10 @@ class FFNPlan:
                                 _bf16(hidden, (M, self.d), "hidden") if hidden is not None else None,
                                 _bf16(out, (M, self.d), "out"), M, _stream(stream))
 
-    def graph_autotune(self, residual, hidden, out, stream, n_tries=3, n_replays=20):
-        """Capture n_tries times, keep the fastest capture (median of
-        n_replays timed replays each); returns its replay time in us."""
+    def graph_autotune(self, residual, hidden, out, stream, n_tries=4, n_replays=20):
+        """Capture n_tries times cycling through the result-neutral schedules
+        (_native.GRAPH_TACTICS), keep the fastest capture (median of n_replays
+        timed replays each); returns (its replay time in us, its schedule)."""
         M = residual.shape[0]
         return N.frt_ffn_graph_autotune(self.handle, _bf16(residual, (M, self.d), "residual"),
                                         _bf16(hidden, (M, self.d), "hidden") if hidden is not None else None,

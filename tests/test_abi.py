@@ -46,7 +46,7 @@ def test_null_plan_is_rejected_without_touching_the_gpu(native):
     L = native.lib()
     assert L.frt_ffn_forward(None, None, None, None, 1, None) == 1
     assert L.frt_ffn_graph_replay(None, 1, None) == 1
-    assert L.frt_ffn_graph_autotune(None, None, None, None, 1, 3, 10, None, None) == 1
+    assert L.frt_ffn_graph_autotune(None, None, None, None, 1, 3, 10, None, None, None) == 1
     assert L.frt_ffn_set_scales(None, None, None) == 1
     assert L.frt_ffn_plan_destroy(None) == 0
     assert "null plan" in native.frt_ffn_last_error()

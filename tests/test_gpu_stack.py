@@ -136,3 +136,27 @@ def test_calibration_teacher_forced_per_layer(case):
                                             ql.s_d, wl.act_id)
         assert abs(sc["s_x"][0] - sx) <= 1e-3 * sx, (l, sc["s_x"][0], sx)
         assert abs(sc["s_h"][0] - sh) <= 1e-3 * sh, (l, sc["s_h"][0], sh)
+
+
+@pytest.mark.parametrize("tactic", range(4))
+def test_every_autotune_schedule_gives_the_eager_bits(case, monkeypatch, tactic):
+    """Each schedule the autotuned capture may keep (defaults, global split-K
+    exchange, single-CTA tiles, no programmatic dependent launch) replays to
+    exactly the eager forward's output."""
+    from realtime_transformer_gb300 import _native as N
+    dev = case.dev
+    r = case.r.to(dev)
+    h = case.h.to(dev)
+    eager = case.plan.forward(r, h)
+    torch.cuda.synchronize()
+    out = torch.empty_like(r)
+    s = torch.cuda.Stream()
+    monkeypatch.setenv("FRT_FFN_AUTOTUNE_ONLY", str(tactic))
+    with torch.cuda.stream(s):
+        t_us, k = case.plan.graph_autotune(r, h, out, s, n_tries=1, n_replays=2)
+        out.zero_()
+        case.plan.graph_replay(case.wl.M, s)
+    s.synchronize()
+    case.plan.device_status()
+    assert k == tactic and N.GRAPH_TACTICS[k]
+    assert torch.equal(out, eager)
