@@ -1,6 +1,8 @@
 """The seeded input recipe: shapes, determinism, outlier channels."""
 import math
 
+import numpy as np
+
 import torch
 
 import synthetic
@@ -49,3 +51,25 @@ def test_distribution():
     assert abs(w["w_gate"].float().std().item() - 0.02) < 1e-3
     assert abs(w["w_norm"].float().mean().item() - 1.0) < 0.02
     assert abs(w["w_norm"].float().std().item() - 0.1) < 0.01
+
+
+def test_attention_shapes_cover_every_workload():
+    for name, wl in synthetic.WORKLOADS.items():
+        nq, nkv, hd, base = synthetic.ATTENTION[name]
+        assert nq % nkv == 0 and hd % 64 == 0 and base > 1
+        assert ((nq + 2 * nkv) * hd) % 128 == 0
+    wl = synthetic.WORKLOADS["tiny"]
+    w = synthetic.qkv_weights(wl, 0)
+    nq, nkv, hd, _ = synthetic.ATTENTION["tiny"]
+    assert tuple(w["w_q"].shape) == (nq * hd, wl.d) and tuple(w["w_k"].shape) == (nkv * hd, wl.d)
+    assert tuple(w["w_v"].shape) == (nkv * hd, wl.d) and tuple(w["w_norm"].shape) == (wl.d,)
+    assert all(v.dtype == torch.bfloat16 for v in w.values())
+    # seeded: the same layer twice is the same tensor, another layer is not
+    assert torch.equal(synthetic.qkv_weights(wl, 0)["w_q"], w["w_q"])
+    assert not torch.equal(synthetic.qkv_weights(wl, 1)["w_q"], w["w_q"])
+
+
+def test_positions():
+    assert list(synthetic.positions(synthetic.WORKLOADS["tiny"])) == list(range(8))
+    p = synthetic.positions(synthetic.WORKLOADS["llm_decode"])
+    assert p.dtype == np.int32 and list(p) == [synthetic.DECODE_CONTEXT]
