@@ -470,3 +470,90 @@ def calibrate_qkv_layer(r_batches, h_batches, w_norm, eps: float = EPS) -> float
         _, y = residual_rmsnorm(r, h_batches[i] if h_batches is not None else None, w_norm, eps)
         amax = max(amax, amax_f32(y))
     return scale_from_amax(np.float32(amax))
+
+
+# --------------------------------------------------------------------------
+# AdaRMSNorm variant (itsolotime FlashRT article, 5.2: Pi0.5's decoder
+# modulates "via AdaRMSNorm Dense layers" instead of a norm weight).  The
+# pages give no formula; reading (the adaptive-norm form of diffusion
+# transformers): a Dense layer of the conditioning gives per-token
+# modulation vectors scale, shift and gate [M, d] (one row shared by all
+# tokens when the conditioning is per sample); the norm output is
+# y = (r' * inv) * (1 + scale) + shift (no norm weight), and the sublayer
+# output is r' + gate * FFN(y).  Each operation in fp32, in that order.
+# --------------------------------------------------------------------------
+
+def split_modulation(mod, M: int, d: int):
+    """mod [R, 3d] BF16 bits (scale | shift | gate), R = 1 (shared) or M ->
+    (scale, shift, gate) fp32 [M, d]."""
+    m = bf16_decode(mod).reshape(-1, 3 * d)
+    assert m.shape[0] in (1, M)
+    m = np.broadcast_to(m, (M, 3 * d))
+    return (np.ascontiguousarray(m[:, :d]), np.ascontiguousarray(m[:, d:2 * d]),
+            np.ascontiguousarray(m[:, 2 * d:]))
+
+
+def ada_rmsnorm(r, h, mod, eps: float = EPS):
+    """Step A1 with AdaRMSNorm before quantisation -> (r' BF16 bits, y fp32)."""
+    r = _u16(r)
+    M, d = r.shape
+    rp, y0 = residual_rmsnorm(r, h, np.full(d, BF16_ONE, dtype=np.uint16), eps)  # y0 = r' * inv exactly
+    scale, shift, _ = split_modulation(mod, M, d)
+    one_plus = (np.float32(1.0) + scale).astype(np.float32)
+    y = ((y0 * one_plus).astype(np.float32) + shift).astype(np.float32)
+    return rp, y
+
+
+def ffn_layer_ada(r, h, mod, q_gu, q_down, s_x, s_h, s_gu, s_d, act: int, eps: float = EPS,
+                  trace: bool = False):
+    """Steps A1..A4 of one AdaRMSNorm layer with fixed scales: A1 as
+    ada_rmsnorm then q_x = E4M3(y / s_x); A2, A3 as ffn_layer (BF16 g/u,
+    a = act(g) u, q_h = E4M3(a / s_h)); A4 out = bf16(r' + (acc * alpha_d) *
+    gate)."""
+    r = _u16(r)
+    M, d = r.shape
+    ff = _u8(q_down).shape[1]
+    rp, y = ada_rmsnorm(r, h, mod, eps)
+    q_x = quantize_f32(y, recip(s_x))
+    gu = bf16_encode((gemm_e4m3(q_x, q_gu) * np.float32(np.float32(s_x) * np.float32(s_gu))).astype(np.float32))
+    a = gated_act(gu, act)
+    q_h = quantize_f32(a, recip(s_h))
+    t = (gemm_e4m3(q_h, q_down) * np.float32(np.float32(s_h) * np.float32(s_d))).astype(np.float32)
+    _, _, gate = split_modulation(mod, M, d)
+    t = (t * gate).astype(np.float32)
+    out = bf16_encode((bf16_decode(rp) + t).astype(np.float32))
+    if trace:
+        return LayerTrace(out, rp, q_x, gu, q_h)
+    return out
+
+
+def calibrate_stack_ada(qlayers, mods, r_batches, h_batches, act: int, eps: float = EPS):
+    """Step A6 over an AdaRMSNorm stack (progressive, as calibrate_stack);
+    mods[l] is layer l's modulation -> (s_x[L], s_h[L])."""
+    s_x, s_h = [], []
+    rb = [_u16(r) for r in r_batches]
+    hb = [_u16(h) for h in h_batches] if h_batches is not None else None
+    for l, ql in enumerate(qlayers):
+        hl = hb if l == 0 else None
+        ys = [ada_rmsnorm(r, hl[i] if hl is not None else None, mods[l], eps) for i, r in enumerate(rb)]
+        sx = scale_from_amax(np.float32(max(amax_f32(y) for _, y in ys)))
+        acts = []
+        for _, y in ys:
+            q_x = quantize_f32(y, recip(sx))
+            gu = bf16_encode((gemm_e4m3(q_x, ql.q_gu) * np.float32(np.float32(sx) * np.float32(ql.s_gu)))
+                             .astype(np.float32))
+            acts.append(gated_act(gu, act))
+        sh = scale_from_amax(np.float32(max(amax_f32(a) for a in acts)))
+        rb = [ffn_layer_ada(r, hl[i] if hl is not None else None, mods[l], ql.q_gu, ql.q_down, sx, sh, ql.s_gu,
+                            ql.s_d, act, eps) for i, r in enumerate(rb)]
+        s_x.append(sx)
+        s_h.append(sh)
+    return s_x, s_h
+
+
+def stack_forward_ada(qlayers, mods, r, h, s_x, s_h, act: int, eps: float = EPS):
+    cur = _u16(r)
+    for l, ql in enumerate(qlayers):
+        cur = ffn_layer_ada(cur, h if l == 0 else None, mods[l], ql.q_gu, ql.q_down, s_x[l], s_h[l], ql.s_gu,
+                            ql.s_d, act, eps)
+    return cur
