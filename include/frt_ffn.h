@@ -153,6 +153,23 @@ frt_status frt_ffn_forward(frt_ffn_plan_t plan, const void *residual_in, const v
                            frt_stream_t stream);
 
 /*
+ * AdaRMSNorm (itsolotime article, 5.2: the Pi0.5 spec modulates through
+ * AdaRMSNorm Dense layers instead of a norm weight).  mod: host array of
+ * n_layers device pointers, each to mod_rows rows of [scale | shift | gate]
+ * (3d BF16 values a row, row-major; the Dense layers' outputs, computed by the
+ * caller); mod_rows = 1 (one row for every token: per-sample conditioning)
+ * or M_max (row m for token m).  While set, every layer's norm computes
+ * y = (r' / sqrt(mean(r'^2) + eps)) * (1 + scale) + shift (the norm weight is
+ * not used) and its down GEMM's epilogue out = bf16(r' + gate * (acc *
+ * alpha_d)), each operation in fp32 in that order.  The plan keeps the
+ * pointers: the buffers must stay valid, and may be rewritten between calls
+ * (captured graphs read them at replay).  Calibrate after setting it (the
+ * activation scales depend on it).  mod == NULL returns to the plain norm.
+ * Marks captured graphs stale.  Errors: INVALID_ARG.
+ */
+frt_status frt_ffn_set_modulation(frt_ffn_plan_t plan, const void *const *mod, int mod_rows);
+
+/*
  * Capture the forward for token count M into a CUDA graph owned by the plan
  * (itsolotime article, 4.1: cudaStreamBeginCapture in Relaxed mode on this
  * stream only; 4.2: stable pointers, no allocation).  The pointers are baked

@@ -34,6 +34,7 @@ SIGNATURES = {
     "frt_ffn_load_weights_ex": (_I, [_P, _I, _P, _P, _P, _P, ctypes.c_uint, _P]),
     "frt_ffn_calibrate": (_I, [_P, ctypes.POINTER(_P), ctypes.POINTER(_P), _I, _I, _P]),
     "frt_ffn_get_scales": (_I, [_P, _FP, _FP, _FP, _FP]),
+    "frt_ffn_set_modulation": (_I, [_P, ctypes.POINTER(_P), _I]),
     "frt_ffn_set_scales": (_I, [_P, _FP, _FP]),
     "frt_ffn_forward": (_I, [_P, _P, _P, _P, _I, _P]),
     "frt_ffn_graph_capture": (_I, [_P, _P, _P, _P, _I, _P]),
@@ -125,6 +126,14 @@ def frt_ffn_calibrate(plan, residual_ptrs, hidden_ptrs, M, stream) -> None:
     h = _ptrs(hidden_ptrs) if hidden_ptrs is not None else None
     _check(lib().frt_ffn_calibrate(plan, ctypes.cast(r, ctypes.POINTER(_P)),
                                    ctypes.cast(h, ctypes.POINTER(_P)) if h is not None else None, n, M, stream))
+
+
+def frt_ffn_set_modulation(plan, mod_ptrs, mod_rows) -> None:
+    if mod_ptrs is None:
+        _check(lib().frt_ffn_set_modulation(plan, None, 0))
+        return
+    arr = _ptrs(mod_ptrs)
+    _check(lib().frt_ffn_set_modulation(plan, ctypes.cast(arr, ctypes.POINTER(_P)), mod_rows))
 
 
 def frt_ffn_get_scales(plan, n_layers: int):

@@ -114,6 +114,10 @@ struct frt_ffn_plan {
     bool pdl = true;           // programmatic dependent launch (FRT_FFN_NO_PDL=1 disables)
     int max_splits = 0;        // cap on split-K (FRT_FFN_MAX_SPLITS; 0 = none)
     const Tactic *tactic = nullptr;  // schedule variant of the capture being autotuned (null: defaults)
+    // AdaRMSNorm modulation (frt_ffn_set_modulation): per layer a caller
+    // buffer of mod_rows rows of [scale | shift | gate], each d wide, BF16
+    std::vector<const uint16_t *> mod;
+    int mod_rows = 0;
 };
 
 namespace {
@@ -206,6 +210,16 @@ frt_status setup_gemm(frt_ffn_plan *P, GemmLaunch &g, int site, int l, int M) {
     return FRT_OK;
 }
 
+// Layer l's AdaRMSNorm modulation of the norm (none when unset).
+NormMod norm_mod(const frt_ffn_plan *P, int l) {
+    NormMod m;
+    if (!P->mod.empty()) {
+        m.p = P->mod[l];
+        m.stride = P->mod_rows == 1 ? 0 : 3 * P->d;
+    }
+    return m;
+}
+
 // Gate/up GEMM of layer l with the gated epilogue (q_h, or its amax).
 frt_status setup_gate_up(frt_ffn_plan *P, GemmLaunch &g, int l, int M, int epi) {
     frt_status st = setup_gemm(P, g, 0, l, M);
@@ -229,6 +243,11 @@ frt_status setup_down(frt_ffn_plan *P, GemmLaunch &g, int l, int M, const void *
         return st;
     g.p.epi = EPI_RESID;
     g.p.alpha = P->s_h[l] * P->s_d[l];
+    if (!P->mod.empty()) {
+        // AdaRMSNorm: the update enters the residual stream scaled by the gate
+        g.p.gate = P->mod[l] + 2 * (size_t)P->d;
+        g.p.ldgate = P->mod_rows == 1 ? 0 : 3 * P->d;
+    }
     g.p.out = out;
     g.p.ldo = P->d;
     g.p.resid = resid;
@@ -246,7 +265,7 @@ frt_status run_layer(frt_ffn_plan *P, int l, const void *in, const void *hid, vo
     void *rp = hid ? (void *)P->rprime : nullptr;
     const bool pdl = P->pdl;
     CK(launch_norm_quant(in, hid, P->w_norm + (size_t)l * d, M, d, RMS_EPS, inv_sx, rp, P->qx, nullptr, false, s,
-                         pdl));
+                         pdl, norm_mod(P, l)));
     GemmLaunch g;
     frt_status st = setup_gate_up(P, g, l, M, EPI_GATED);
     if (st != FRT_OK)
@@ -473,6 +492,29 @@ FRT_API frt_status frt_ffn_load_weights_ex(frt_ffn_plan_t P, int layer, const vo
     return FRT_OK;
 }
 
+FRT_API frt_status frt_ffn_set_modulation(frt_ffn_plan_t P, const void *const *mod, int mod_rows) {
+    if (!P)
+        return fail(FRT_ERR_INVALID_ARG, "null plan");
+    if (!mod) {
+        P->mod.clear();
+        P->mod_rows = 0;
+        P->version++;
+        return FRT_OK;
+    }
+    if (mod_rows != 1 && mod_rows != P->M_max)
+        return fail(FRT_ERR_INVALID_ARG, "mod_rows must be 1 or M_max=%d (got %d)", P->M_max, mod_rows);
+    std::vector<const uint16_t *> ptrs(P->L);
+    for (int l = 0; l < P->L; ++l) {
+        if (!mod[l] || !aligned16(mod[l]))
+            return fail(FRT_ERR_INVALID_ARG, "modulation of layer %d: null or misaligned pointer", l);
+        ptrs[l] = static_cast<const uint16_t *>(mod[l]);
+    }
+    P->mod = ptrs;
+    P->mod_rows = mod_rows;
+    P->version++;  // captured graphs bake the previous choice
+    return FRT_OK;
+}
+
 FRT_API frt_status frt_ffn_get_scales(frt_ffn_plan_t P, float *s_x, float *s_h, float *s_gu, float *s_down) {
     if (!P)
         return fail(FRT_ERR_INVALID_ARG, "null plan");
@@ -533,7 +575,8 @@ FRT_API frt_status frt_ffn_calibrate(frt_ffn_plan_t P, const void *const *residu
             for (int b = 0; b < n_batches; ++b) {
                 const void *in = l == 0 ? residual[b] : (const void *)st_of(b);
                 const void *hid = (l == 0 && hidden) ? hidden[b] : nullptr;
-                CK(launch_norm_quant(in, hid, wn, M, d, RMS_EPS, 1.0f, nullptr, P->qx, P->amax, true, s, false));
+                CK(launch_norm_quant(in, hid, wn, M, d, RMS_EPS, 1.0f, nullptr, P->qx, P->amax, true, s, false,
+                                     norm_mod(P, l)));
             }
             CK(cudaMemcpyAsync(&h_amax, P->amax, 4, cudaMemcpyDeviceToHost, s));
             CK(cudaStreamSynchronize(s));
@@ -548,7 +591,7 @@ FRT_API frt_status frt_ffn_calibrate(frt_ffn_plan_t P, const void *const *residu
                 if (l == 0 && !hid)
                     CK(cudaMemcpyAsync(st_of(b), residual[b], row_bytes, cudaMemcpyDeviceToDevice, s));
                 CK(launch_norm_quant(in, hid, wn, M, d, RMS_EPS, 1.0f / sx[l], hid ? (void *)st_of(b) : nullptr,
-                                     P->qx, nullptr, false, s, false));
+                                     P->qx, nullptr, false, s, false, norm_mod(P, l)));
                 GemmLaunch g;
                 P->s_x[l] = sx[l];
                 P->s_h[l] = 1.0f;
@@ -824,7 +867,7 @@ FRT_API frt_status frt_ffn_debug_step(frt_ffn_plan_t P, int layer, int step, int
     switch (step) {
     case 0:
         CK(launch_norm_quant(P->rbuf[0], nullptr, P->w_norm + (size_t)layer * d, M, d, RMS_EPS, 1.0f / P->s_x[layer],
-                             nullptr, P->qx, nullptr, false, s, false));
+                             nullptr, P->qx, nullptr, false, s, false, norm_mod(P, layer)));
         break;
     case 1:
         if ((st = setup_gate_up(P, g, layer, M, EPI_GATED)) != FRT_OK)

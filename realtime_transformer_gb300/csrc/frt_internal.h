@@ -48,6 +48,8 @@ struct GemmParams {
     int pair;               // tiled role on CTA pairs (cta_group::2): 256-token MMAs, half a weight tile per CTA
     int cluster;            // 1: the splits of a tile are one thread-block cluster and exchange
                             //    partials in distributed shared memory (ws, counters unused)
+    const uint16_t *gate;   // EPI_RESID with AdaRMSNorm: out = bf16(resid + gate * acc * alpha), BF16 gate
+    int ldgate;             //   at gate[m * ldgate + n] (0: one row for all tokens); null: no gate
     int *err;               // device error word
     int stall_test;         // test hook: the MMA issuer first waits on a phase nothing completes
     // gated epilogues
@@ -115,9 +117,15 @@ cudaError_t launch_rope_table(const int *pos, const float *inv_freq, int M, int 
                               bool pdl);
 cudaError_t launch_rope_split(const void *qkv, int M, int nq, int nkv, int hd, const int *pos, const float *inv_freq,
                               void *q, void *k, void *v, cudaStream_t s, bool pdl);
+// AdaRMSNorm modulation of the norm: row m's scale vector at p + m * stride
+// (its shift vector d elements after it); stride 0 = one row for all tokens.
+struct NormMod {
+    const uint16_t *p = nullptr;
+    int stride = 0;
+};
 cudaError_t launch_norm_quant(const void *r, const void *h, const void *w, int M, int d, float eps, float inv_s,
                               void *rprime, uint8_t *qx, unsigned *amax_word, bool measure, cudaStream_t s,
-                              bool pdl);
+                              bool pdl, NormMod mod = NormMod());
 
 }  // namespace frt
 

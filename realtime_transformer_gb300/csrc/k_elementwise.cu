@@ -169,19 +169,21 @@ __global__ void k_quant_gu_interleave(const uint16_t *__restrict__ gate, const u
 
 // WPR warps per row (1, 2, 4 or 8).  Pass 1: r' = bf16(r + h) (stored if
 // rprime != null), sum of squares (per thread, then a warp-shuffle tree, then
-// the warps of the row in order).  Pass 2: y = (r' * inv) * w, then either
-// amax (measure) or q = E4M3(y * inv_s).  d % 8 == 0.
+// the warps of the row in order).  Pass 2: y = (r' * inv) * w -- or, with a
+// modulation (AdaRMSNorm), y = (r' * inv) * (1 + scale) + shift from the
+// row's modulation vectors -- then either amax (measure) or
+// q = E4M3(y * inv_s).  d % 8 == 0.
 //
 // VPT > 0: each thread owns at most VPT 16-byte vectors of its row (the
 // launcher guarantees d / 8 <= 32 * WPR * VPT) and issues every load of r, h
 // and w before the first use, so the row costs one memory round trip; the
 // values stay in registers for pass 2.  VPT == 0: any d, a strided loop that
 // re-reads r (and h) in pass 2.
-template <bool MEASURE, int WPR, int VPT>
+template <bool MEASURE, int WPR, int VPT, bool ADA>
 __global__ void __launch_bounds__(256) k_norm_quant(const uint16_t *__restrict__ r, const uint16_t *__restrict__ h,
                                                     const uint16_t *__restrict__ w, int M, int d, float eps,
                                                     float inv_s, uint16_t *__restrict__ rprime,
-                                                    uint8_t *__restrict__ qx, unsigned *amax_word) {
+                                                    uint8_t *__restrict__ qx, unsigned *amax_word, NormMod mod) {
     // Let the dependent GEMM launch (and stream its weights) right away; it
     // waits for this grid, and this grid waits for its own predecessor
     // before it can complete, so ordering is preserved.
@@ -202,15 +204,23 @@ __global__ void __launch_bounds__(256) k_norm_quant(const uint16_t *__restrict__
     uint4 *rpv = rprime ? reinterpret_cast<uint4 *>(rprime + roff) : nullptr;
     const uint4 *wv = reinterpret_cast<const uint4 *>(w);
     uint2 *qv = reinterpret_cast<uint2 *>(qx + roff);
+    // AdaRMSNorm: the row's scale vector (in place of the norm weight) and shift vector
+    const uint4 *scv =
+        ADA ? reinterpret_cast<const uint4 *>(mod.p + (size_t)(active ? row : 0) * mod.stride) : nullptr;
+    const uint4 *shv = ADA ? scv + nv : nullptr;
 
     float ss = 0.0f;
     float x[VPT > 0 ? VPT : 1][8];
     if constexpr (VPT > 0) {
-        // the norm weights do not depend on the previous kernel
-        uint4 wraw[VPT];
+        // the norm weights (or the modulation) do not depend on the previous kernel
+        uint4 wraw[VPT], shraw[ADA ? VPT : 1];
 #pragma unroll
-        for (int k = 0; k < VPT; ++k)
-            wraw[k] = (tid + k * STRIDE < nv) ? __ldg(wv + tid + k * STRIDE) : make_uint4(0, 0, 0, 0);
+        for (int k = 0; k < VPT; ++k) {
+            const bool in = tid + k * STRIDE < nv;
+            wraw[k] = in ? __ldg((ADA ? scv : wv) + tid + k * STRIDE) : make_uint4(0, 0, 0, 0);
+            if constexpr (ADA)
+                shraw[k] = in ? __ldg(shv + tid + k * STRIDE) : make_uint4(0, 0, 0, 0);
+        }
         pdl_wait();
         uint4 rraw[VPT], hraw[VPT];
 #pragma unroll
@@ -256,9 +266,17 @@ __global__ void __launch_bounds__(256) k_norm_quant(const uint16_t *__restrict__
                 break;
             float wf[8];
             unpack8(wraw[k], wf);
+            if constexpr (ADA) {
+                float sh[8];
+                unpack8(shraw[k], sh);
 #pragma unroll
-            for (int j = 0; j < 8; j++)
-                x[k][j] = __fmul_rn(__fmul_rn(x[k][j], inv), wf[j]);
+                for (int j = 0; j < 8; j++)
+                    x[k][j] = __fadd_rn(__fmul_rn(__fmul_rn(x[k][j], inv), __fadd_rn(1.0f, wf[j])), sh[j]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; j++)
+                    x[k][j] = __fmul_rn(__fmul_rn(x[k][j], inv), wf[j]);
+            }
             if (MEASURE) {
 #pragma unroll
                 for (int j = 0; j < 8; j++)
@@ -320,10 +338,18 @@ __global__ void __launch_bounds__(256) k_norm_quant(const uint16_t *__restrict__
                 for (int j = 0; j < 8; j++)
                     x[0][j] = __bfloat162float(__float2bfloat16_rn(__fadd_rn(x[0][j], hh[j])));
             }
-            unpack8(__ldg(wv + v), wf);
+            unpack8(__ldg((ADA ? scv : wv) + v), wf);
+            if constexpr (ADA) {
+                float sh[8];
+                unpack8(__ldg(shv + v), sh);
 #pragma unroll
-            for (int j = 0; j < 8; j++)
-                x[0][j] = __fmul_rn(__fmul_rn(x[0][j], inv), wf[j]);
+                for (int j = 0; j < 8; j++)
+                    x[0][j] = __fadd_rn(__fmul_rn(__fmul_rn(x[0][j], inv), __fadd_rn(1.0f, wf[j])), sh[j]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; j++)
+                    x[0][j] = __fmul_rn(__fmul_rn(x[0][j], inv), wf[j]);
+            }
             if (MEASURE) {
 #pragma unroll
                 for (int j = 0; j < 8; j++)
@@ -482,14 +508,15 @@ cudaError_t launch_amax_fold(const void *x, size_t rows, int d, const void *w, u
 
 namespace {
 
-template <bool MEASURE, int WPR, int VPT>
-cudaError_t norm_launch(int M, bool pdl, cudaStream_t s, const uint16_t *r, const uint16_t *h, const uint16_t *w,
+template <bool MEASURE, int WPR, int VPT, bool ADA>
+cudaError_t norm_launch(NormMod mod, int M, bool pdl, cudaStream_t s, const uint16_t *r, const uint16_t *h,
+                        const uint16_t *w,
                         int d, float eps, float inv_s, uint16_t *rp, uint8_t *qx, unsigned *amax_word) {
     // the largest shared-memory carve-out, like the GEMMs, so that GEMM CTAs
     // can start on an SM while this kernel's CTAs run there
     static bool attr_set = false;
     if (!attr_set) {
-        const cudaError_t e = cudaFuncSetAttribute(k_norm_quant<MEASURE, WPR, VPT>,
+        const cudaError_t e = cudaFuncSetAttribute(k_norm_quant<MEASURE, WPR, VPT, ADA>,
                                                    cudaFuncAttributePreferredSharedMemoryCarveout,
                                                    (int)cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess)
@@ -497,13 +524,14 @@ cudaError_t norm_launch(int M, bool pdl, cudaStream_t s, const uint16_t *r, cons
         attr_set = true;
     }
     const dim3 grid((unsigned)((M + 8 / WPR - 1) / (8 / WPR)));
-    return launch_ex(k_norm_quant<MEASURE, WPR, VPT>, grid, dim3(256), 0, s, pdl, 1u, r, h, w, M, d, eps, inv_s, rp, qx,
-                     amax_word);
+    return launch_ex(k_norm_quant<MEASURE, WPR, VPT, ADA>, grid, dim3(256), 0, s, pdl, 1u, r, h, w, M, d, eps, inv_s,
+                     rp, qx, amax_word, mod);
 }
 
 template <bool MEASURE>
-cudaError_t norm_dispatch(int M, bool pdl, cudaStream_t s, const uint16_t *r, const uint16_t *h, const uint16_t *w,
-                          int d, float eps, float inv_s, uint16_t *rp, uint8_t *qx, unsigned *amax_word) {
+cudaError_t norm_dispatch(NormMod mod, int M, bool pdl, cudaStream_t s, const uint16_t *r, const uint16_t *h,
+                          const uint16_t *w, int d, float eps, float inv_s, uint16_t *rp, uint8_t *qx,
+                          unsigned *amax_word) {
     const int nv = d / 8;
     // Few rows: spread each row over enough warps that a thread holds one
     // vector (latency first).  Many rows: a warp per row, up to four vectors
@@ -518,7 +546,9 @@ cudaError_t norm_dispatch(int M, bool pdl, cudaStream_t s, const uint16_t *r, co
     }
     const int per = 32 * wpr;
     const int vpt = (nv + per - 1) / per;
-#define FRT_NORM(W, V) return norm_launch<MEASURE, W, V>(M, pdl, s, r, h, w, d, eps, inv_s, rp, qx, amax_word)
+#define FRT_NORM(W, V)                                                                                \
+    return mod.p ? norm_launch<MEASURE, W, V, true>(mod, M, pdl, s, r, h, w, d, eps, inv_s, rp, qx, amax_word) \
+                 : norm_launch<MEASURE, W, V, false>(mod, M, pdl, s, r, h, w, d, eps, inv_s, rp, qx, amax_word)
     if (vpt > 4) {
         FRT_NORM(8, 0);
     }
@@ -535,14 +565,14 @@ cudaError_t norm_dispatch(int M, bool pdl, cudaStream_t s, const uint16_t *r, co
 
 cudaError_t launch_norm_quant(const void *r, const void *h, const void *w, int M, int d, float eps, float inv_s,
                               void *rprime, uint8_t *qx, unsigned *amax_word, bool measure, cudaStream_t s,
-                              bool pdl) {
+                              bool pdl, NormMod mod) {
     auto rr = static_cast<const uint16_t *>(r);
     auto hh = static_cast<const uint16_t *>(h);
     auto ww = static_cast<const uint16_t *>(w);
     auto rp = static_cast<uint16_t *>(rprime);
     if (measure)
-        return norm_dispatch<true>(M, pdl, s, rr, hh, ww, d, eps, inv_s, rp, qx, amax_word);
-    return norm_dispatch<false>(M, pdl, s, rr, hh, ww, d, eps, inv_s, rp, qx, amax_word);
+        return norm_dispatch<true>(mod, M, pdl, s, rr, hh, ww, d, eps, inv_s, rp, qx, amax_word);
+    return norm_dispatch<false>(mod, M, pdl, s, rr, hh, ww, d, eps, inv_s, rp, qx, amax_word);
 }
 
 cudaError_t launch_rope_split(const void *qkv, int M, int nq, int nkv, int hd, const int *pos, const float *inv_freq,

@@ -92,8 +92,10 @@ struct Unit {
 // only the one a launch of the layer uses -- the weight-streaming gated
 // epilogue without split-K (the gate/up GEMM) or the plain cluster split-K
 // epilogue (the down GEMM) -- so that the code a launch runs is compact; the
-// tiled QKV split + RoPE epilogue (ROLE_ROPE) is compiled only for itself.
-enum Role : int { ROLE_ANY = 0, ROLE_GATED_TILE = 1, ROLE_CLUSTER_PLAIN = 2, ROLE_ROPE = 3 };
+// tiled QKV split + RoPE epilogue (ROLE_ROPE) is compiled only for itself,
+// and the AdaRMSNorm gate of the residual only where a launch has one
+// (ROLE_CLUSTER_GATE, and the general ROLE_ANY).
+enum Role : int { ROLE_ANY = 0, ROLE_GATED_TILE = 1, ROLE_CLUSTER_PLAIN = 2, ROLE_ROPE = 3, ROLE_CLUSTER_GATE = 4 };
 
 // Tiles run in groups of p.group P-tiles: within a group the P-tile index
 // changes fastest, so a wave of CTAs covers a block of group x (SMs / group)
@@ -389,6 +391,7 @@ __device__ __forceinline__ void store_chunk(const GemmParams &p, const Unit &w, 
                 rvs[j / 8] = *reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.resid) +
                                                              (size_t)m * p.ldr + n0 + j);
         }
+        const uint16_t *gt = p.gate ? p.gate + (size_t)m * p.ldgate + n0 : nullptr;
 #pragma unroll
         for (int j = 0; j < CH; j += 8) {
             if (n0 + j >= p.n_feat)
@@ -397,6 +400,17 @@ __device__ __forceinline__ void store_chunk(const GemmParams &p, const Unit &w, 
 #pragma unroll
             for (int t = 0; t < 8; ++t)
                 f[t] = __fmul_rn(v[j + t], p.alpha);
+            if (gt) {
+                const uint4 gv = *reinterpret_cast<const uint4 *>(gt + j);
+                f[0] = __fmul_rn(f[0], bf_lo(gv.x));
+                f[1] = __fmul_rn(f[1], bf_hi(gv.x));
+                f[2] = __fmul_rn(f[2], bf_lo(gv.y));
+                f[3] = __fmul_rn(f[3], bf_hi(gv.y));
+                f[4] = __fmul_rn(f[4], bf_lo(gv.z));
+                f[5] = __fmul_rn(f[5], bf_hi(gv.z));
+                f[6] = __fmul_rn(f[6], bf_lo(gv.w));
+                f[7] = __fmul_rn(f[7], bf_hi(gv.w));
+            }
             if (p.epi == EPI_RESID) {
                 const uint4 rv = rvs[j / 8];
                 f[0] = __fadd_rn(bf_lo(rv.x), f[0]);
@@ -444,6 +458,8 @@ __device__ __forceinline__ void store_chunk(const GemmParams &p, const Unit &w, 
         for (int j = 0; j < CH; ++j) {
             if (j < nv) {
                 float f = __fmul_rn(v[j], p.alpha);
+                if (p.gate)
+                    f = __fmul_rn(f, __uint_as_float((uint32_t)p.gate[(size_t)(m0 + j) * p.ldgate + n] << 16));
                 if (p.epi == EPI_RESID)
                     f = __fadd_rn(res[j], f);
                 static_cast<uint16_t *>(p.out)[(size_t)(m0 + j) * p.ldo + n] = (uint16_t)bf16_bits(f);
@@ -834,7 +850,7 @@ constexpr int RED_Q_TILED = 8;  // plain epilogue of a tiled slice (half a 128 x
 // addresses -- so no store needs a predicate.  Output coordinates are
 // recomputed at the store rather than held.  res0: residuals of the first
 // batch, loaded early.
-template <int BN, bool SWAP, bool GATED>
+template <int BN, bool SWAP, bool GATED, bool RESID_GATE = true>
 __device__ __forceinline__ float reduce_slice(const GemmParams &p, const Unit &w, const Slice &sl, const float *red,
                                               int span, const uint2 (&res0)[RED_Q]) {
     constexpr int NQ = GATED ? RED_Q_GATED : (SWAP ? RED_Q : RED_Q_TILED);
@@ -978,6 +994,18 @@ __device__ __forceinline__ float reduce_slice(const GemmParams &p, const Unit &w
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
                         acc[i][j] = __fmul_rn(acc[i][j], alpha);
+                if (RESID_GATE && p.gate) {
+#pragma unroll
+                    for (int i = 0; i < NQ; ++i) {
+                        int m, n;
+                        coords(base, i, m, n);
+                        const uint2 gv = *reinterpret_cast<const uint2 *>(p.gate + (size_t)m * p.ldgate + n);
+                        acc[i][0] = __fmul_rn(acc[i][0], bf_lo(gv.x));
+                        acc[i][1] = __fmul_rn(acc[i][1], bf_hi(gv.x));
+                        acc[i][2] = __fmul_rn(acc[i][2], bf_lo(gv.y));
+                        acc[i][3] = __fmul_rn(acc[i][3], bf_hi(gv.y));
+                    }
+                }
                 if (epi == EPI_RESID) {
 #pragma unroll
                     for (int i = 0; i < NQ; ++i) {
@@ -1118,7 +1146,7 @@ __device__ bool coop_split_unit(const GemmParams &p, const Unit &w, uint32_t tba
 // A CTA's pipeline stages receive the copies, so each CTA first tells the
 // others (remote mbarrier arrivals) that its last MMA has completed; and a
 // CTA leaves only once every CTA it copied to has reported the copy landed.
-template <int BN, bool SWAP, bool PLAIN_ONLY>
+template <int BN, bool SWAP, bool PLAIN_ONLY, bool RESID_GATE = true>
 __device__ bool coop_cluster_unit(const GemmParams &p, const Unit &w, uint32_t tbase, uint64_t *tempty_b,
                                   uint64_t *free_bar, uint64_t *data_bar, uint64_t *sent_bar, float *red, float *stg,
                                   volatile int *abort_f, volatile int *s_flag) {
@@ -1196,7 +1224,7 @@ __device__ bool coop_cluster_unit(const GemmParams &p, const Unit &w, uint32_t t
     // 4. reduce the slice and run the epilogue
     float amax = 0.0f;
     if constexpr (PLAIN_ONLY)
-        amax = reduce_slice<BN, SWAP, false>(p, w, sl, red, span, res0);
+        amax = reduce_slice<BN, SWAP, false, RESID_GATE>(p, w, sl, red, span, res0);
     else
         amax = gated_epi ? reduce_slice<BN, SWAP, true>(p, w, sl, red, span, res0)
                          : reduce_slice<BN, SWAP, false>(p, w, sl, red, span, res0);
@@ -1248,9 +1276,10 @@ __device__ void epilogue(const GemmParams &p, uint64_t *tfull, uint64_t *tempty,
                 if ((threadIdx.x & 31) == 0)
                     atomicMax(p.amax, __float_as_uint(amax));
             }
-        } else if constexpr (ROLE == ROLE_CLUSTER_PLAIN) {
-            if (!coop_cluster_unit<BN, SWAP, true>(p, w, tbase, &tempty[abuf], free_bar, data_bar, sent_bar, red,
-                                                   red + red_floats(BN, p.splits), abort_f, &s_last[abuf])) {
+        } else if constexpr (ROLE == ROLE_CLUSTER_PLAIN || ROLE == ROLE_CLUSTER_GATE) {
+            if (!coop_cluster_unit<BN, SWAP, true, ROLE == ROLE_CLUSTER_GATE>(
+                    p, w, tbase, &tempty[abuf], free_bar, data_bar, sent_bar, red, red + red_floats(BN, p.splits),
+                    abort_f, &s_last[abuf])) {
                 // gave up: as below
                 if (threadIdx.x == 0) {
                     mbar_wait_for(smem_u32(free_bar), 0, 500000000ull);
@@ -1677,18 +1706,21 @@ cudaError_t launch_gemm(const GemmLaunch &g, cudaStream_t s, bool pdl) {
         // their epilogue alone
         const bool gated = g.p.epi == EPI_GATED || g.p.epi == EPI_GATED_AMAX;
         const int role = (g.p.splits == 1 && gated) ? ROLE_GATED_TILE
-                         : (g.p.cluster && !gated)  ? ROLE_CLUSTER_PLAIN
+                         : (g.p.cluster && !gated)  ? (g.p.gate ? ROLE_CLUSTER_GATE : ROLE_CLUSTER_PLAIN)
                                                     : ROLE_ANY;
-        switch (g.bn * 4 + role) {
-        case 16 * 4 + ROLE_ANY: return run<16, true, false, ROLE_ANY>(g, s, pdl);
-        case 16 * 4 + ROLE_GATED_TILE: return run<16, true, false, ROLE_GATED_TILE>(g, s, pdl);
-        case 16 * 4 + ROLE_CLUSTER_PLAIN: return run<16, true, false, ROLE_CLUSTER_PLAIN>(g, s, pdl);
-        case 32 * 4 + ROLE_ANY: return run<32, true, false, ROLE_ANY>(g, s, pdl);
-        case 32 * 4 + ROLE_GATED_TILE: return run<32, true, false, ROLE_GATED_TILE>(g, s, pdl);
-        case 32 * 4 + ROLE_CLUSTER_PLAIN: return run<32, true, false, ROLE_CLUSTER_PLAIN>(g, s, pdl);
-        case 64 * 4 + ROLE_ANY: return run<64, true, false, ROLE_ANY>(g, s, pdl);
-        case 64 * 4 + ROLE_GATED_TILE: return run<64, true, false, ROLE_GATED_TILE>(g, s, pdl);
-        case 64 * 4 + ROLE_CLUSTER_PLAIN: return run<64, true, false, ROLE_CLUSTER_PLAIN>(g, s, pdl);
+        switch (g.bn * 8 + role) {
+        case 16 * 8 + ROLE_ANY: return run<16, true, false, ROLE_ANY>(g, s, pdl);
+        case 16 * 8 + ROLE_GATED_TILE: return run<16, true, false, ROLE_GATED_TILE>(g, s, pdl);
+        case 16 * 8 + ROLE_CLUSTER_PLAIN: return run<16, true, false, ROLE_CLUSTER_PLAIN>(g, s, pdl);
+        case 16 * 8 + ROLE_CLUSTER_GATE: return run<16, true, false, ROLE_CLUSTER_GATE>(g, s, pdl);
+        case 32 * 8 + ROLE_ANY: return run<32, true, false, ROLE_ANY>(g, s, pdl);
+        case 32 * 8 + ROLE_GATED_TILE: return run<32, true, false, ROLE_GATED_TILE>(g, s, pdl);
+        case 32 * 8 + ROLE_CLUSTER_PLAIN: return run<32, true, false, ROLE_CLUSTER_PLAIN>(g, s, pdl);
+        case 32 * 8 + ROLE_CLUSTER_GATE: return run<32, true, false, ROLE_CLUSTER_GATE>(g, s, pdl);
+        case 64 * 8 + ROLE_ANY: return run<64, true, false, ROLE_ANY>(g, s, pdl);
+        case 64 * 8 + ROLE_GATED_TILE: return run<64, true, false, ROLE_GATED_TILE>(g, s, pdl);
+        case 64 * 8 + ROLE_CLUSTER_PLAIN: return run<64, true, false, ROLE_CLUSTER_PLAIN>(g, s, pdl);
+        case 64 * 8 + ROLE_CLUSTER_GATE: return run<64, true, false, ROLE_CLUSTER_GATE>(g, s, pdl);
         default: return cudaErrorInvalidValue;
         }
     }

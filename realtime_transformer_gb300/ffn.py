@@ -77,6 +77,19 @@ class FFNPlan:
         hp = [_bf16(h, (M, self.d), "hidden") if h is not None else None for h in hiddens] if hiddens else None
         N.frt_ffn_calibrate(self.handle, rp, hp, M, _stream(stream))
 
+    def set_modulation(self, mods):
+        """AdaRMSNorm: mods = one BF16 tensor [R, 3d] (scale | shift | gate)
+        per layer, R = 1 (shared by all tokens) or M_max; None: plain norm.
+        The plan reads the tensors at every forward and replay: keep them."""
+        if mods is None:
+            N.frt_ffn_set_modulation(self.handle, None, 0)
+            self._mods = None
+            return
+        rows = mods[0].shape[0]
+        ptrs = [_bf16(m, (rows, 3 * self.d), "modulation") for m in mods]
+        N.frt_ffn_set_modulation(self.handle, ptrs, rows)
+        self._mods = list(mods)
+
     def scales(self):
         s_x, s_h, s_gu, s_d = N.frt_ffn_get_scales(self.handle, self.n_layers)
         return {"s_x": s_x, "s_h": s_h, "s_gu": s_gu, "s_down": s_d}
