@@ -427,6 +427,18 @@ def quantize_qkv_weights(w_q, w_k, w_v):
     return quantize_weight(np.concatenate([_u16(w_q), _u16(w_k), _u16(w_v)], axis=0))
 
 
+def quantize_qkv_weights_folded(w_q, w_k, w_v, w_norm):
+    """The fused QKV weight with the RMSNorm weight folded in (itsolotime
+    article, 5.2: the Pi0 spec's FusedQKV(..., norm_fuse=...)): W'[j][k] =
+    W[j][k] * w[k] over [W_q; W_k; W_v] in fp32 (exact), one scale
+    amax(W') / 448 -> (codes, scale); the sublayer's norm then multiplies by
+    ones."""
+    w = bf16_decode(np.concatenate([_u16(w_q), _u16(w_k), _u16(w_v)], axis=0))
+    f = (w * bf16_decode(w_norm)[None, :]).astype(np.float32)
+    s = scale_from_amax(amax_f32(f))
+    return quantize_f32(f, recip(s)), s
+
+
 @dataclass
 class QKVTrace:
     r_prime: np.ndarray   # [M,d] BF16 bits

@@ -126,3 +126,31 @@ def test_qkv_calibration_constant_rows(orc):
     r = orc.bf16_encode(np.where(np.arange(4 * d).reshape(4, d) % 3, 2.0, -2.0).astype(np.float32))
     s = orc.calibrate_qkv_layer([r], None, wn, eps=0.0)
     assert np.float32(s) == np.float32(np.float32(orc.bf16_decode(wn).max()) / np.float32(448.0))
+
+
+def test_qkv_fold_unit_and_power_of_two_norm_weights(orc):
+    """Fold with w = 1 is the plain quantisation; with w = c (a power of two)
+    the codes stay and the scale is multiplied by c exactly; the folded
+    sublayer with s_x / c then equals the unfolded one with w = c bit for bit."""
+    rng = np.random.default_rng(9)
+    d, nq, nkv, hd = 256, 4, 1, 64
+    wq, wk, wv = [orc.bf16_encode(rng.normal(0, 0.02, (n * hd, d)).astype(np.float32)) for n in (nq, nkv, nkv)]
+    ones = np.full(d, orc.BF16_ONE, dtype=np.uint16)
+    a = orc.quantize_qkv_weights_folded(wq, wk, wv, ones)
+    b = orc.quantize_qkv_weights(wq, wk, wv)
+    assert np.array_equal(a[0], b[0]) and a[1] == b[1]
+    c = 0.5
+    wc = orc.bf16_encode(np.full(d, c, np.float32))
+    f = orc.quantize_qkv_weights_folded(wq, wk, wv, wc)
+    assert np.array_equal(f[0], b[0]) and np.float32(f[1]) == np.float32(b[1]) * np.float32(c)
+    r = orc.bf16_encode(rng.standard_normal((6, d)).astype(np.float32))
+    pos = np.arange(6) * 5
+    inv = orc.rope_inv_freq(hd, 1.0e4)
+    s_x = 0.0113
+    u = orc.qkv_layer(r, None, wc, b[0], s_x, b[1], nq, nkv, hd, pos, inv)
+    g = orc.qkv_layer(r, None, ones, f[0], float(np.float32(s_x) / np.float32(c)), f[1], nq, nkv, hd, pos, inv)
+    for k in ("q_x", "qkv", "q", "k", "v"):
+        assert np.array_equal(getattr(u, k), getattr(g, k)), k
+    # and a real norm weight changes the folded codes (columns scaled by w[k])
+    wr = orc.bf16_encode((1 + 0.1 * rng.standard_normal(d)).astype(np.float32))
+    assert not np.array_equal(orc.quantize_qkv_weights_folded(wq, wk, wv, wr)[0], b[0])
