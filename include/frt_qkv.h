@@ -70,6 +70,17 @@ frt_status frt_qkv_load_weights(frt_qkv_plan_t plan, int layer, const void *w_no
                                 const void *w_v, frt_stream_t stream);
 
 /*
+ * frt_qkv_load_weights with options.  flags FRT_LOAD_FOLD_NORM (itsolotime
+ * article, 5.2: the Pi0 spec folds the RMSNorm weight into the FusedQKV
+ * weight): [W_q; W_k; W_v] quantised as W'[j][k] = W[j][k] * w_norm[k] (exact
+ * in fp32), one scale amax(W') / 448, and the sublayer's norm multiplies by
+ * ones.  Calibrate (or set the scale) after loading.  Errors: as
+ * frt_qkv_load_weights; INVALID_ARG for unknown flags.
+ */
+frt_status frt_qkv_load_weights_ex(frt_qkv_plan_t plan, int layer, const void *w_norm, const void *w_q,
+                                   const void *w_k, const void *w_v, unsigned flags, frt_stream_t stream);
+
+/*
  * Calibrate layer `layer`'s activation scale: s_x = amax(y) / 448 over
  * n_batches batches of M rows (residual[b] [M, d] BF16, hidden[b] the same
  * or hidden == NULL / hidden[b] == NULL for none).  Synchronises `stream`.

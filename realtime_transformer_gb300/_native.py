@@ -53,6 +53,7 @@ SIGNATURES = {
     "frt_qkv_plan_create": (_I, [_I, _I, _I, _I, _F, _I, _I, ctypes.POINTER(_P)]),
     "frt_qkv_plan_destroy": (_I, [_P]),
     "frt_qkv_load_weights": (_I, [_P, _I, _P, _P, _P, _P, _P]),
+    "frt_qkv_load_weights_ex": (_I, [_P, _I, _P, _P, _P, _P, ctypes.c_uint, _P]),
     "frt_qkv_calibrate": (_I, [_P, _I, ctypes.POINTER(_P), ctypes.POINTER(_P), _I, _I, _P]),
     "frt_qkv_get_scales": (_I, [_P, _FP, _FP]),
     "frt_qkv_set_scales": (_I, [_P, _FP]),
@@ -222,6 +223,10 @@ def frt_qkv_plan_destroy(plan) -> None:
 
 def frt_qkv_load_weights(plan, layer, w_norm, w_q, w_k, w_v, stream) -> None:
     _check(lib().frt_qkv_load_weights(plan, layer, w_norm, w_q, w_k, w_v, stream))
+
+
+def frt_qkv_load_weights_ex(plan, layer, w_norm, w_q, w_k, w_v, flags, stream) -> None:
+    _check(lib().frt_qkv_load_weights_ex(plan, layer, w_norm, w_q, w_k, w_v, flags, stream))
 
 
 def frt_qkv_calibrate(plan, layer, residual_ptrs, hidden_ptrs, M, stream) -> None:

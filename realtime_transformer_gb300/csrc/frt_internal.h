@@ -113,6 +113,8 @@ cudaError_t launch_quant_bf16(const void *x, size_t n, float inv_s, uint8_t *q, 
 cudaError_t launch_quant_gu_interleave(const void *gate, const void *up, int ff, int d, const void *fold,
                                       float inv_s, uint8_t *dst, cudaStream_t s);
 cudaError_t launch_amax_fold(const void *x, size_t rows, int d, const void *w, unsigned *amax_word, cudaStream_t s);
+cudaError_t launch_quant_fold(const void *x, size_t rows, int d, const void *w, float inv_s, uint8_t *q,
+                              cudaStream_t s);
 cudaError_t launch_rope_table(const int *pos, const float *inv_freq, int M, int half, float2 *cs, cudaStream_t s,
                               bool pdl);
 cudaError_t launch_rope_split(const void *qkv, int M, int nq, int nkv, int hd, const int *pos, const float *inv_freq,

@@ -246,8 +246,16 @@ FRT_API frt_status frt_qkv_plan_destroy(frt_qkv_plan_t P) {
 
 FRT_API frt_status frt_qkv_load_weights(frt_qkv_plan_t P, int layer, const void *w_norm, const void *w_q,
                                         const void *w_k, const void *w_v, frt_stream_t stream) {
+    return frt_qkv_load_weights_ex(P, layer, w_norm, w_q, w_k, w_v, 0u, stream);
+}
+
+FRT_API frt_status frt_qkv_load_weights_ex(frt_qkv_plan_t P, int layer, const void *w_norm, const void *w_q,
+                                           const void *w_k, const void *w_v, unsigned flags, frt_stream_t stream) {
     if (!P)
         return qfail(FRT_ERR_INVALID_ARG, "null plan");
+    if (flags & ~(unsigned)FRT_LOAD_FOLD_NORM)
+        return qfail(FRT_ERR_INVALID_ARG, "unknown load flags 0x%x", flags);
+    const bool fold = (flags & FRT_LOAD_FOLD_NORM) != 0;
     if (layer < 0 || layer >= P->L)
         return qfail(FRT_ERR_INVALID_ARG, "layer %d out of range [0, %d)", layer, P->L);
     if (!w_norm || !w_q || !w_k || !w_v || !al16(w_norm) || !al16(w_q) || !al16(w_k) || !al16(w_v))
@@ -255,12 +263,21 @@ FRT_API frt_status frt_qkv_load_weights(frt_qkv_plan_t P, int layer, const void 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const size_t d = P->d, nq = (size_t)P->nq * P->hd, nk = (size_t)P->nkv * P->hd;
     uint8_t *dst = P->w + (size_t)layer * P->N * d;
-    QCK(cudaMemcpyAsync(P->w_norm + (size_t)layer * d, w_norm, d * 2, cudaMemcpyDeviceToDevice, s));
+    // folded: the norm weight moves into [W_q; W_k; W_v] and the norm multiplies by ones
+    const std::vector<uint16_t> ones(fold ? d : 0, (uint16_t)0x3F80);
+    QCK(cudaMemcpyAsync(P->w_norm + (size_t)layer * d, fold ? (const void *)ones.data() : w_norm, d * 2,
+                        fold ? cudaMemcpyHostToDevice : cudaMemcpyDeviceToDevice, s));
     // one scale over [W_q; W_k; W_v]
     QCK(cudaMemsetAsync(P->amax, 0, 4, s));
-    QCK(launch_amax_bf16(w_q, nq * d, P->amax, s));
-    QCK(launch_amax_bf16(w_k, nk * d, P->amax, s));
-    QCK(launch_amax_bf16(w_v, nk * d, P->amax, s));
+    if (fold) {
+        QCK(launch_amax_fold(w_q, nq, (int)d, w_norm, P->amax, s));
+        QCK(launch_amax_fold(w_k, nk, (int)d, w_norm, P->amax, s));
+        QCK(launch_amax_fold(w_v, nk, (int)d, w_norm, P->amax, s));
+    } else {
+        QCK(launch_amax_bf16(w_q, nq * d, P->amax, s));
+        QCK(launch_amax_bf16(w_k, nk * d, P->amax, s));
+        QCK(launch_amax_bf16(w_v, nk * d, P->amax, s));
+    }
     unsigned h_amax = 0;
     QCK(cudaMemcpyAsync(&h_amax, P->amax, 4, cudaMemcpyDeviceToHost, s));
     QCK(cudaStreamSynchronize(s));
@@ -268,9 +285,15 @@ FRT_API frt_status frt_qkv_load_weights(frt_qkv_plan_t P, int layer, const void 
     memcpy(&a, &h_amax, 4);
     const float sc = a == 0.0f ? 1.0f : a / 448.0f;
     const float inv = 1.0f / sc;
-    QCK(launch_quant_bf16(w_q, nq * d, inv, dst, s));
-    QCK(launch_quant_bf16(w_k, nk * d, inv, dst + nq * d, s));
-    QCK(launch_quant_bf16(w_v, nk * d, inv, dst + (nq + nk) * d, s));
+    if (fold) {
+        QCK(launch_quant_fold(w_q, nq, (int)d, w_norm, inv, dst, s));
+        QCK(launch_quant_fold(w_k, nk, (int)d, w_norm, inv, dst + nq * d, s));
+        QCK(launch_quant_fold(w_v, nk, (int)d, w_norm, inv, dst + (nq + nk) * d, s));
+    } else {
+        QCK(launch_quant_bf16(w_q, nq * d, inv, dst, s));
+        QCK(launch_quant_bf16(w_k, nk * d, inv, dst + nq * d, s));
+        QCK(launch_quant_bf16(w_v, nk * d, inv, dst + (nq + nk) * d, s));
+    }
     QCK(cudaStreamSynchronize(s));
     P->s_qkv[layer] = sc;
     P->loaded[layer] = 1;

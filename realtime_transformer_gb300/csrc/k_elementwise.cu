@@ -133,6 +133,23 @@ __global__ void k_amax_fold(const uint4 *__restrict__ x, size_t rows, int d, con
         atomic_amax(amax_word, m);
 }
 
+// E4M3(W[j][k] * w[k] * inv_s) of a [rows, d] BF16 matrix into dst (row-major):
+// a weight with the RMSNorm weight folded in.  d % 8 == 0.
+__global__ void k_quant_fold(const uint4 *__restrict__ x, size_t rows, int d, const uint4 *__restrict__ w,
+                             float inv_s, uint2 *__restrict__ q) {
+    const size_t vpr = (size_t)d / 8;
+    const size_t nvec = rows * vpr;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < nvec; i += (size_t)gridDim.x * blockDim.x) {
+        float f[8], c[8];
+        unpack8(__ldg(x + i), f);
+        unpack8(__ldg(w + i % vpr), c);
+#pragma unroll
+        for (int j = 0; j < 8; j++)
+            f[j] = __fmul_rn(__fmul_rn(f[j], c[j]), inv_s);
+        q[i] = pack8_e4m3(f);
+    }
+}
+
 // [W_gate; W_up] quantised into the interleaved arena layout: blocks of 128
 // rows, each 64 gate rows followed by the 64 up rows of the same features,
 // so that one GEMM tile holds matching gate and up rows.  With fold != null
@@ -595,6 +612,18 @@ cudaError_t launch_rope_table(const int *pos, const float *inv_freq, int M, int 
     if (blocks > cap) blocks = cap;
     if (blocks == 0) blocks = 1;
     return launch_ex(k_rope_table, dim3((unsigned)blocks), dim3(256), 0, s, pdl, 1u, pos, inv_freq, M, half, cs);
+}
+
+cudaError_t launch_quant_fold(const void *x, size_t rows, int d, const void *w, float inv_s, uint8_t *q,
+                              cudaStream_t s) {
+    const size_t nvec = rows * (size_t)(d / 8);
+    size_t blocks = (nvec + 255) / 256;
+    const size_t cap = (size_t)sm_count() * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks == 0) blocks = 1;
+    k_quant_fold<<<(unsigned)blocks, 256, 0, s>>>(static_cast<const uint4 *>(x), rows, d,
+                                                   static_cast<const uint4 *>(w), inv_s, reinterpret_cast<uint2 *>(q));
+    return cudaGetLastError();
 }
 
 }  // namespace frt

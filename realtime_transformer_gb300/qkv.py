@@ -30,11 +30,13 @@ class QKVPlan:
         except Exception:
             pass
 
-    def load_weights(self, layer, w_norm, w_q, w_k, w_v, stream=None):
+    def load_weights(self, layer, w_norm, w_q, w_k, w_v, stream=None, fold_norm=False):
+        """fold_norm: fold the RMSNorm weight into the fused QKV weight (the Pi0 layout)."""
         d, hd = self.d, self.hd
-        N.frt_qkv_load_weights(self.handle, layer, _bf16(w_norm, (d,), "w_norm"),
-                               _bf16(w_q, (self.nq * hd, d), "w_q"), _bf16(w_k, (self.nkv * hd, d), "w_k"),
-                               _bf16(w_v, (self.nkv * hd, d), "w_v"), _stream(stream))
+        N.frt_qkv_load_weights_ex(self.handle, layer, _bf16(w_norm, (d,), "w_norm"),
+                                  _bf16(w_q, (self.nq * hd, d), "w_q"), _bf16(w_k, (self.nkv * hd, d), "w_k"),
+                                  _bf16(w_v, (self.nkv * hd, d), "w_v"), N.FRT_LOAD_FOLD_NORM if fold_norm else 0,
+                                  _stream(stream))
 
     def calibrate(self, layer, residuals, hiddens=None, stream=None):
         M = residuals[0].shape[0]

@@ -24,6 +24,9 @@ SHAPES = [
     # tiled tiles without split-K that hold whole heads: split + RoPE in the GEMM epilogue
     ("fused_hd256", 1000, 512, 8, 1, 256, 1.0e4, 0, True),
     ("fused_hd128", 1280, 256, 12, 2, 128, 1.0e6, 7, False),
+    # the norm weight folded into [W_q; W_k; W_v] (the Pi0 layout)
+    ("folded", 50, 1024, 8, 1, 256, 1.0e4, 0, True, True),
+    ("folded_tiled", 300, 512, 4, 2, 64, 1.0e4, 0, False, True),
 ]
 
 
@@ -37,20 +40,27 @@ def weights(d, nq, nkv, hd, seed):
 @pytest.fixture(scope="module", params=SHAPES, ids=lambda s: s[0])
 def case(request):
     from realtime_transformer_gb300.qkv import QKVPlan
-    name, M, d, nq, nkv, hd, base, p0, with_h = request.param
+    name, M, d, nq, nkv, hd, base, p0, with_h = request.param[:9]
+    fold = len(request.param) > 9 and request.param[9]
     wl = synthetic.WORKLOADS["tiny"].with_(name=name, M=M, d=d, seed=31)
     r, h = synthetic.inputs(wl)
     h = h if with_h else None
     w = weights(d, nq, nkv, hd, 7 + M)
     pos = (p0 + 3 * np.arange(M)).astype(np.int32)
-    codes, s_qkv = oracle.quantize_qkv_weights(bits(w["w_q"]), bits(w["w_k"]), bits(w["w_v"]))
-    s_x = oracle.calibrate_qkv_layer([bits(r)], [bits(h)] if with_h else None, bits(w["w_norm"]))
+    if fold:
+        codes, s_qkv = oracle.quantize_qkv_weights_folded(bits(w["w_q"]), bits(w["w_k"]), bits(w["w_v"]),
+                                                          bits(w["w_norm"]))
+        w_norm_ref = np.full(d, oracle.BF16_ONE, dtype=np.uint16)
+    else:
+        codes, s_qkv = oracle.quantize_qkv_weights(bits(w["w_q"]), bits(w["w_k"]), bits(w["w_v"]))
+        w_norm_ref = bits(w["w_norm"])
+    s_x = oracle.calibrate_qkv_layer([bits(r)], [bits(h)] if with_h else None, w_norm_ref)
     dev = torch.device("cuda")
     plan = QKVPlan(d, nq, nkv, hd, base, M, 1)
-    plan.load_weights(0, *(w[k].to(dev) for k in ("w_norm", "w_q", "w_k", "w_v")))
+    plan.load_weights(0, *(w[k].to(dev) for k in ("w_norm", "w_q", "w_k", "w_v")), fold_norm=fold)
     plan.set_scales([s_x])
     c = dict(name=name, M=M, d=d, nq=nq, nkv=nkv, hd=hd, base=base, r=r, h=h, w=w, pos=pos, codes=codes,
-             s_qkv=s_qkv, s_x=s_x, plan=plan, dev=dev)
+             s_qkv=s_qkv, s_x=s_x, plan=plan, dev=dev, w_norm_ref=w_norm_ref)
     yield c
     plan.close()
 
@@ -67,7 +77,7 @@ def test_sublayer_matches_oracle(case, monkeypatch):
                          torch.from_numpy(c["pos"]).to(dev))
     torch.cuda.synchronize()
     c["plan"].device_status()
-    ref = oracle.qkv_layer(bits(c["r"]), bits(c["h"]) if c["h"] is not None else None, bits(c["w"]["w_norm"]),
+    ref = oracle.qkv_layer(bits(c["r"]), bits(c["h"]) if c["h"] is not None else None, c["w_norm_ref"],
                            c["codes"], c["s_x"], c["s_qkv"], c["nq"], c["nkv"], c["hd"], c["pos"],
                            oracle.rope_inv_freq(c["hd"], c["base"]))
     assert np.array_equal(bits(tr["r_prime"]), ref.r_prime), "r' = bf16(r + h) must be bit-exact"
@@ -146,6 +156,11 @@ def test_boundary_errors():
     assert e.value.name == "FRT_ERR_NOT_READY"
     w = weights(256, 4, 1, 64, 3)
     p.load_weights(1, *(w[k].to(dev) for k in ("w_norm", "w_q", "w_k", "w_v")))
+    wd = {k: w[k].to(dev) for k in w}
+    with pytest.raises(N.FrtError) as e:
+        N.frt_qkv_load_weights_ex(p.handle, 1, wd["w_norm"].data_ptr(), wd["w_q"].data_ptr(), wd["w_k"].data_ptr(),
+                                  wd["w_v"].data_ptr(), 2, None)  # unknown flag
+    assert e.value.name == "FRT_ERR_INVALID_ARG"
     with pytest.raises(N.FrtError) as e:
         p.forward(1, r, None, pos)  # no activation scale yet
     assert e.value.name == "FRT_ERR_NOT_READY"
