@@ -74,6 +74,7 @@ def lib() -> ctypes.CDLL:
             "orc_gelu_tanh": (f32, [f32]),
             "orc_silu": (f32, [f32]),
             "orc_gated_act": (None, [i32, i32, i32, P, P]),
+            "orc_gated_act_f32": (None, [i64, i32, P, P, P]),
             "orc_ffn_layer": (i32, [i32, i32, i32, i32, f32, P, P, P, P, P, f32, f32, f32, f32, P, P, P, P, P]),
             "orc_calibrate_layer": (i32, [i32, i32, i32, i32, f32, i32, P, P, P, P, P, f32, f32,
                                           ctypes.POINTER(f32), ctypes.POINTER(f32), P]),
@@ -569,3 +570,232 @@ def stack_forward_ada(qlayers, mods, r, h, s_x, s_h, act: int, eps: float = EPS)
         cur = ffn_layer_ada(cur, h if l == 0 else None, mods[l], ql.q_gu, ql.q_down, s_x[l], s_h[l], ql.s_gu,
                             ql.s_d, act, eps)
     return cur
+
+
+# --------------------------------------------------------------------------
+# NVFP4 variant of the sublayer (itsolotime article, 7.2: gate and up as two
+# NVFP4 GEMMs that emit packed FP4 plus scales, a fused GeGLU kernel that
+# requantises FP4 to FP4, an NVFP4 down GEMM, the residual kept in 16 bits,
+# AWQ pre-scaling of the normalised activation).  The pages do not define the
+# format; reading: NVFP4 as published by NVIDIA -- E2M1 elements, one E4M3
+# scale per 16 consecutive elements along K, one fp32 scale per tensor.
+# --------------------------------------------------------------------------
+
+FP4_BLOCK = 16
+E2M1_MAX = 6.0
+NVFP4_RANGE = 448.0 * 6.0  # amax -> per-tensor scale: the block scales then span E4M3
+_E2M1_MAG = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], dtype=np.float32)
+
+
+def e2m1_decode(codes) -> np.ndarray:
+    """4-bit E2M1 codes (bit 3 sign, bits 2..1 exponent, bit 0 mantissa) -> fp32."""
+    c = _u8(codes)
+    mag = _E2M1_MAG[c & 7]
+    return np.where(c & 8, -mag, mag).astype(np.float32)
+
+
+def e2m1_encode(x) -> np.ndarray:
+    """fp32 -> E2M1 codes: nearest of the eight magnitudes, a tie to the even
+    mantissa bit, saturating at 6; the sign kept (a negative that rounds to 0
+    gives code 8, -0)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    a = np.abs(x)
+    lo = np.clip(np.searchsorted(_E2M1_MAG, a, side="right") - 1, 0, 7)
+    hi = np.minimum(lo + 1, 7)
+    d_lo = a - _E2M1_MAG[lo]
+    d_hi = _E2M1_MAG[hi] - a
+    up = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    idx = np.where(a >= np.float32(E2M1_MAX), 7, np.where(up, hi, lo))
+    return (idx | np.where(np.signbit(x), 8, 0)).astype(np.uint8)
+
+
+def nvfp4_scale_from_amax(amax: float) -> float:
+    """Per-tensor scale amax / (448 * 6) in fp32 (1 for an all-zero tensor)."""
+    a = np.float32(amax)
+    return float(a / np.float32(NVFP4_RANGE)) if a > 0 else 1.0
+
+
+def nvfp4_quantize(x, s: float):
+    """fp32 [rows, K] with per-tensor scale s -> (E2M1 codes [rows, K], E4M3
+    block-scale codes [rows, K / 16]).  Per block of 16 along K (fp32 ops):
+    b = E4M3(amax_block * (1 / (6 s))); then every element
+    q = E2M1(x * (1 / (dec(b) * s))), or code 0 where dec(b) is 0."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    rows, K = x.shape
+    assert K % FP4_BLOCK == 0
+    blk = x.reshape(rows, K // FP4_BLOCK, FP4_BLOCK)
+    amax_b = np.abs(blk).max(axis=2)
+    inv6 = np.float32(recip(np.float32(6.0) * np.float32(s)))
+    sb = e4m3_encode((amax_b * inv6).astype(np.float32))
+    den = (e4m3_decode(sb) * np.float32(s)).astype(np.float32)
+    safe = np.where(den > 0, den, np.float32(1.0))
+    inv = np.where(den > 0, np.float32(1.0) / safe, np.float32(0.0)).astype(np.float32)
+    q = e2m1_encode((blk * inv[:, :, None]).astype(np.float32))
+    return q.reshape(rows, K), sb
+
+
+def nvfp4_decode(q, sb, s: float) -> np.ndarray:
+    """Codes + block scales + tensor scale -> fp32 values: (e2m1 * dec(b)) is
+    exact in fp32; the product with s is rounded once."""
+    q = _u8(q)
+    rows, K = q.shape
+    v = e2m1_decode(q).reshape(rows, K // FP4_BLOCK, FP4_BLOCK) * e4m3_decode(sb)[:, :, None]
+    return (v.astype(np.float32) * np.float32(s)).astype(np.float32).reshape(rows, K)
+
+
+def nvfp4_gemm(qa, sa, qb, sb) -> np.ndarray:
+    """Block-scaled product without the tensor scales: acc[m][n] =
+    sum_k e2m1(A[m][k]) dec(sa[m][k/16]) e2m1(B[n][k]) dec(sb[n][k/16]),
+    A [M, K], B [N, K]; evaluated in fp64 (every product exact), rounded to fp32."""
+    a = (e2m1_decode(qa).astype(np.float64).reshape(_u8(qa).shape[0], -1, FP4_BLOCK)
+         * e4m3_decode(sa).astype(np.float64)[:, :, None]).reshape(_u8(qa).shape)
+    b = (e2m1_decode(qb).astype(np.float64).reshape(_u8(qb).shape[0], -1, FP4_BLOCK)
+         * e4m3_decode(sb).astype(np.float64)[:, :, None]).reshape(_u8(qb).shape)
+    return (a @ b.T).astype(np.float32)
+
+
+@dataclass
+class NVFP4Weight:
+    q: np.ndarray    # [rows, K] E2M1 codes
+    sb: np.ndarray   # [rows, K / 16] E4M3 block-scale codes
+    s: float         # fp32 tensor scale
+
+
+def quantize_weight_nvfp4(w_bf16, col_scale=None) -> NVFP4Weight:
+    """NVFP4 weight preparation: W'[j][k] = fp32(W[j][k] * c[k]) (c the AWQ
+    scale of input channel k, or none), one tensor scale amax(W') / 2688."""
+    w = bf16_decode(w_bf16)
+    if col_scale is not None:
+        w = (w * np.asarray(col_scale, np.float32)[None, :]).astype(np.float32)
+    s = nvfp4_scale_from_amax(amax_f32(w))
+    q, sb = nvfp4_quantize(w, s)
+    return NVFP4Weight(q, sb, s)
+
+
+def awq_scales(y_batches, alpha: float = 0.5) -> np.ndarray:
+    """AWQ per-input-channel scales from calibration activations (the
+    normalised y the gate/up GEMMs read): c_k = max(mean_t |y[t][k]|, 1e-5)^alpha
+    in fp64, rounded to fp32 (reading: the pages name AWQ and an alpha, not
+    the search; this is the activation-magnitude rule of the AWQ method)."""
+    y = np.concatenate([np.asarray(b, np.float64) for b in y_batches], axis=0)
+    return np.power(np.maximum(np.abs(y).mean(axis=0), 1e-5), alpha).astype(np.float32)
+
+
+@dataclass
+class NVFP4Layer:
+    w_norm: np.ndarray       # [d] BF16 bits
+    awq: np.ndarray | None   # [d] fp32 AWQ scales (None: no pre-scaling)
+    gate: NVFP4Weight        # [ff, d]
+    up: NVFP4Weight          # [ff, d]
+    down: NVFP4Weight        # [d, ff]
+
+
+def quantize_layer_nvfp4(w_norm, w_gate, w_up, w_down, awq=None) -> NVFP4Layer:
+    """Weights of one NVFP4 layer: gate and up quantised separately (the split
+    gate/up of the pages), each with the AWQ column scales; down without."""
+    return NVFP4Layer(_u16(w_norm), None if awq is None else np.asarray(awq, np.float32),
+                      quantize_weight_nvfp4(w_gate, awq), quantize_weight_nvfp4(w_up, awq),
+                      quantize_weight_nvfp4(w_down))
+
+
+@dataclass
+class NVFP4Scales:
+    s_x: float   # normalised (and AWQ-divided) activation
+    s_g: float   # gate GEMM output
+    s_u: float   # up GEMM output
+    s_h: float   # gated activation
+
+
+@dataclass
+class NVFP4Trace:
+    out: np.ndarray      # [M, d] BF16 bits
+    r_prime: np.ndarray  # [M, d] BF16 bits
+    x: tuple             # (codes [M, d], block scales [M, d/16])
+    g: tuple             # (codes [M, ff], block scales [M, ff/16])
+    u: tuple
+    h: tuple
+    y: np.ndarray        # [M, d] fp32, before quantisation
+    g_f32: np.ndarray    # [M, ff] fp32 gate GEMM output before quantisation
+    u_f32: np.ndarray
+    a: np.ndarray        # [M, ff] fp32 gated activation before quantisation
+
+
+def _nvfp4_awq_divide(y, awq):
+    if awq is None:
+        return y
+    inv = (np.float32(1.0) / np.asarray(awq, np.float32)).astype(np.float32)
+    return (y * inv[None, :]).astype(np.float32)
+
+
+def _nvfp4_gated(g4, u4, s_g, s_u, act):
+    gd = nvfp4_decode(g4[0], g4[1], s_g)
+    ud = nvfp4_decode(u4[0], u4[1], s_u)
+    a = np.empty(gd.shape, dtype=np.float32)
+    lib().orc_gated_act_f32(gd.size, act, _p(np.ascontiguousarray(gd)), _p(np.ascontiguousarray(ud)), _p(a))
+    return a
+
+
+def ffn_layer_nvfp4(r, h, L: NVFP4Layer, sc: NVFP4Scales, act: int, eps: float = EPS, trace: bool = False):
+    """One NVFP4 layer with fixed scales, in the pages' order: r' = bf16(r + h);
+    y = RMSNorm(r') (fp32); y / c (AWQ); X = NVFP4(y, s_x);
+    G = NVFP4(acc(X, W_g) * (s_x s_g'), s_g), U likewise (s_g', s_u' the weight
+    scales); A = NVFP4(act(dec G) * dec U, s_h);
+    out = bf16(r' + acc(A, W_d) * (s_h s_d'))."""
+    rp, y = residual_rmsnorm(r, h, L.w_norm, eps)
+    ys = _nvfp4_awq_divide(y, L.awq)
+    x4 = nvfp4_quantize(ys, sc.s_x)
+    alpha_g = np.float32(np.float32(sc.s_x) * np.float32(L.gate.s))
+    alpha_u = np.float32(np.float32(sc.s_x) * np.float32(L.up.s))
+    g = (nvfp4_gemm(x4[0], x4[1], L.gate.q, L.gate.sb) * alpha_g).astype(np.float32)
+    u = (nvfp4_gemm(x4[0], x4[1], L.up.q, L.up.sb) * alpha_u).astype(np.float32)
+    g4 = nvfp4_quantize(g, sc.s_g)
+    u4 = nvfp4_quantize(u, sc.s_u)
+    a = _nvfp4_gated(g4, u4, sc.s_g, sc.s_u, act)
+    h4 = nvfp4_quantize(a, sc.s_h)
+    alpha_d = np.float32(np.float32(sc.s_h) * np.float32(L.down.s))
+    o = (nvfp4_gemm(h4[0], h4[1], L.down.q, L.down.sb) * alpha_d).astype(np.float32)
+    out = bf16_encode((bf16_decode(rp) + o).astype(np.float32))
+    if trace:
+        return NVFP4Trace(out, rp, x4, g4, u4, h4, ys, g, u, a)
+    return out
+
+
+def calibrate_layer_nvfp4(r_batches, h_batches, L: NVFP4Layer, act: int, eps: float = EPS):
+    """Progressive per-tensor calibration of one NVFP4 layer: each scale is
+    amax / 2688 over the batches of the tensor it quantises, measured with
+    the scales before it already applied.  Returns (NVFP4Scales, outs)."""
+    nb = len(r_batches)
+    hb = h_batches if h_batches is not None else [None] * nb
+    pre = [residual_rmsnorm(r_batches[b], hb[b], L.w_norm, eps) for b in range(nb)]
+    ys = [_nvfp4_awq_divide(y, L.awq) for _, y in pre]
+    s_x = nvfp4_scale_from_amax(max(amax_f32(y) for y in ys))
+    x4 = [nvfp4_quantize(y, s_x) for y in ys]
+    alpha_g = np.float32(np.float32(s_x) * np.float32(L.gate.s))
+    alpha_u = np.float32(np.float32(s_x) * np.float32(L.up.s))
+    g = [(nvfp4_gemm(q, sb, L.gate.q, L.gate.sb) * alpha_g).astype(np.float32) for q, sb in x4]
+    u = [(nvfp4_gemm(q, sb, L.up.q, L.up.sb) * alpha_u).astype(np.float32) for q, sb in x4]
+    s_g = nvfp4_scale_from_amax(max(amax_f32(t) for t in g))
+    s_u = nvfp4_scale_from_amax(max(amax_f32(t) for t in u))
+    a = [_nvfp4_gated(nvfp4_quantize(g[b], s_g), nvfp4_quantize(u[b], s_u), s_g, s_u, act) for b in range(nb)]
+    s_h = nvfp4_scale_from_amax(max(amax_f32(t) for t in a))
+    sc = NVFP4Scales(s_x, s_g, s_u, s_h)
+    outs = [ffn_layer_nvfp4(r_batches[b], hb[b], L, sc, act, eps) for b in range(nb)]
+    return sc, outs
+
+
+def calibrate_stack_nvfp4(layers, r_batches, h_batches, act: int, eps: float = EPS):
+    """Calibration over the stack (hidden added at layer 0 only) -> [NVFP4Scales]."""
+    out = []
+    rb = list(r_batches)
+    for l, L in enumerate(layers):
+        sc, rb = calibrate_layer_nvfp4(rb, h_batches if l == 0 else None, L, act, eps)
+        out.append(sc)
+    return out
+
+
+def stack_forward_nvfp4(layers, scales, r, h, act: int, eps: float = EPS):
+    cur = _u16(r)
+    for l, L in enumerate(layers):
+        cur = ffn_layer_nvfp4(cur, h if l == 0 else None, L, scales[l], act, eps)
+    return cur
+

@@ -284,6 +284,17 @@ ORC_API void orc_gated_act(int M, int ff, int act, const uint16_t *gu, float *a)
     }
 }
 
+/* a[i] = act(g[i]) * u[i] on fp32 operands (the NVFP4 path decodes its FP4
+ * gate and up values to fp32 instead of BF16). */
+ORC_API void orc_gated_act_f32(int64_t n, int act, const float *g, const float *u, float *a)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; i++) {
+        float ag = (act == ORC_ACT_SWIGLU) ? orc_silu(g[i]) : orc_gelu_tanh(g[i]);
+        a[i] = ag * u[i];
+    }
+}
+
 static float amax_f32(const float *x, int64_t n)
 {
     float m = 0.0f;
