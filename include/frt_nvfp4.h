@@ -1,0 +1,133 @@
+/*
+ * frt_nvfp4.h -- C ABI of the NVFP4 variant of the FFN sublayer in
+ * libfrt_ffn.so (itsolotime FlashRT article, 7.2: the NVFP4 encoder FFN --
+ * gate and up as two NVFP4 GEMMs that emit packed FP4 plus scales, a fused
+ * GeGLU kernel that requantises FP4 to FP4, an NVFP4 down GEMM, the residual
+ * kept in 16 bits, AWQ pre-scaling; 7.2's closing remark: the residual
+ * stream stays in high precision).
+ *
+ * Per layer l, on M tokens (fp32 operations, each rounded):
+ *   N1  r' = bf16(r + h);  y = ((r' * inv_rms) * w_norm) / c   (c: AWQ scales or 1)
+ *       X = NVFP4(y, s_x)
+ *   N2  G = NVFP4(acc(X, W_g') * (s_x s_wg), s_g);  U = NVFP4(acc(X, W_u') * (s_x s_wu), s_u)
+ *       W_g' = NVFP4(W_g[j][k] * c[k], s_wg) and likewise W_u'
+ *   N3  A = NVFP4(act(dec G) * dec U, s_h)
+ *   N4  out = bf16(r' + acc(A, W_d') * (s_h s_wd));  W_d' = NVFP4(W_d, s_wd)
+ * NVFP4(x, s): E2M1 codes with one E4M3 scale per 16 consecutive elements
+ * along K, b = E4M3(amax_block / (6 s)), q = E2M1(x / (dec(b) s)); the
+ * tensor scales s = amax / (448 * 6) -- of the weights when they are loaded,
+ * of the activations by calibration (progressive, layer by layer).
+ * Readings (the pages give the loop, not the format or the AWQ rule): NVFP4
+ * as NVIDIA publishes it; AWQ scales supplied by the caller (the oracle's
+ * awq_scales gives the activation-magnitude rule c_k = mean|y_k|^alpha).
+ *
+ * Layouts: codes are packed two per byte, element 2i in the low nibble,
+ * row-major [rows, K/2]; the block scales of GEMM operands (X, A and the
+ * weights) are stored in the tensor cores' TMEM-ready order: per 128-row tile
+ * and 64-element K chunk a 512-byte block, byte (r % 32) * 16 + (r / 32) * 4 + j
+ * for row r of the tile and 16-element group j of the chunk (tiles major,
+ * chunks minor); the block scales of G and U are row-major [M, ff/16].
+ *
+ * Conventions: as frt_ffn.h (BF16 bit patterns, 16-byte aligned device
+ * pointers, frt_ffn_last_error() for messages, one host thread and one stream
+ * at a time per plan).  Nothing is allocated after plan creation except by
+ * frt_fp4_calibrate; frt_fp4_forward may be captured into a CUDA graph.
+ */
+#ifndef FRT_NVFP4_H
+#define FRT_NVFP4_H
+
+#include "frt_ffn.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct frt_fp4_plan *frt_fp4_plan_t;
+
+/*
+ * Create a plan for n_layers NVFP4 sublayers of width d and hidden width ff,
+ * activation act (frt_act), at most M_max tokens per call.  Allocates the
+ * weight arenas (codes and scales), norm weights, AWQ reciprocals and
+ * scratch.  Requires: d % 256 == 0; ff % 256 == 0; 1 <= M_max <= 65536;
+ * 1 <= n_layers <= 4096; a compute-capability 10.3 GPU.
+ * Errors: INVALID_ARG, UNSUPPORTED, OOM, CUDA.  *out is NULL on failure.
+ */
+frt_status frt_fp4_plan_create(int d, int ff, int act, int M_max, int n_layers, frt_fp4_plan_t *out);
+
+/* Free the plan and its device memory (synchronises the device).  NULL is accepted. */
+frt_status frt_fp4_plan_destroy(frt_fp4_plan_t plan);
+
+/*
+ * Quantise one layer's BF16 weights into the plan: w_norm [d], w_gate [ff, d],
+ * w_up [ff, d], w_down [d, ff] (device, nn.Linear layout); awq: device fp32
+ * [d] AWQ scales c (each > 0) applied to the gate and up weights' columns and
+ * divided out of the activation, or NULL for none.  Synchronises `stream`.
+ * Errors: INVALID_ARG (null/misaligned pointer, layer out of range), CUDA.
+ */
+frt_status frt_fp4_load_weights(frt_fp4_plan_t plan, int layer, const void *w_norm, const void *w_gate,
+                                const void *w_up, const void *w_down, const float *awq, frt_stream_t stream);
+
+/*
+ * Progressive calibration over the whole stack: for layer 0..L-1 in turn,
+ * s_x, then s_g and s_u, then s_h from the amax over the n_batches batches
+ * (each [M, d] BF16; hidden[b] added at layer 0, hidden == NULL for none),
+ * every later tensor measured with the earlier scales applied; the layer's
+ * outputs are the next layer's inputs.  Allocates (and frees) 2 n_batches M d
+ * BF16 of scratch.  Synchronises `stream`.
+ * Errors: INVALID_ARG, NOT_READY (weights missing), SHAPE (M > M_max), OOM, CUDA.
+ */
+frt_status frt_fp4_calibrate(frt_fp4_plan_t plan, const void *const *residual, const void *const *hidden,
+                             int n_batches, int M, frt_stream_t stream);
+
+/* Host arrays: act [n_layers * 4] = (s_x, s_g, s_u, s_h) per layer, weight
+ * [n_layers * 3] = (s_wg, s_wu, s_wd) per layer (either may be NULL). */
+frt_status frt_fp4_get_scales(frt_fp4_plan_t plan, float *act, float *weight);
+/* Set every layer's activation scales (host [n_layers * 4], each finite and > 0). */
+frt_status frt_fp4_set_scales(frt_fp4_plan_t plan, const float *act);
+
+/*
+ * The stack on M tokens: residual_in [M, d] BF16, hidden_in [M, d] BF16 (added
+ * at layer 0) or NULL, out [M, d] BF16 (may not alias the inputs).  M == 0
+ * does nothing.  Five kernels per layer; no allocation.
+ * Errors: INVALID_ARG, NOT_READY (weights or scales missing), SHAPE, CUDA.
+ */
+frt_status frt_fp4_forward(frt_fp4_plan_t plan, const void *residual_in, const void *hidden_in, void *out, int M,
+                           frt_stream_t stream);
+
+/*
+ * Test/diagnostic: layer `layer` alone on its input, with the same kernels,
+ * copying the intermediates to caller buffers (any may be NULL): r_prime
+ * [M, d] BF16 (only when hidden_in is given), x_codes [M, d/2] and x_sf
+ * (TMEM-ready, ceil(M/128) * 128 * d/16 bytes), g/u codes [M, ff/2] and
+ * row-major scales [M, ff/16], h_codes [M, ff/2] and h_sf (TMEM-ready,
+ * ceil(M/128) * 128 * ff/16 bytes).  Synchronises `stream`.
+ */
+frt_status frt_fp4_debug_trace(frt_fp4_plan_t plan, int layer, const void *residual_in, const void *hidden_in,
+                               void *out, void *r_prime, void *x_codes, void *x_sf, void *g_codes, void *g_sf,
+                               void *u_codes, void *u_sf, void *h_codes, void *h_sf, int M, frt_stream_t stream);
+
+/*
+ * Test/diagnostic: copy a layer's quantised weight (which: 0 gate, 1 up,
+ * 2 down) -- codes [rows, K/2] and TMEM-ready scales rows * K/16 bytes.
+ */
+frt_status frt_fp4_debug_weights(frt_fp4_plan_t plan, int layer, int which, void *codes, void *sf,
+                                 frt_stream_t stream);
+
+/*
+ * Test/diagnostic: out[m][n] = alpha * sum_k A[m][k] B[n][k] over NVFP4
+ * operands (codes [M, K/2] and [N, K/2]; TMEM-ready scales sized for
+ * ceil(M/128) and N/128 tiles), fp32 [M, N] out.  N % 128 == 0, K % 256 == 0,
+ * 1 <= M <= 65536.  err: a device int the kernel sets on a timed-out wait.
+ */
+frt_status frt_nvfp4_gemm(const void *a_codes, const void *a_sf, const void *b_codes, const void *b_sf, int M, int N,
+                          int K, float alpha, float *out, int *err, frt_stream_t stream);
+
+/* Synchronise `stream` and report a kernel that gave up a bounded wait
+ * (DEVICE_TIMEOUT; the plan's error word is then cleared). */
+frt_status frt_fp4_device_status(frt_fp4_plan_t plan, frt_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FRT_NVFP4_H */

@@ -15,4 +15,7 @@ def __getattr__(name):
     if name == "QKVPlan":
         from .qkv import QKVPlan
         return QKVPlan
+    if name == "FP4Plan":
+        from .nvfp4 import FP4Plan
+        return FP4Plan
     raise AttributeError(name)

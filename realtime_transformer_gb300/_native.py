@@ -1,4 +1,4 @@
-"""ctypes binding of libfrt_ffn.so (include/frt_ffn.h, include/frt_qkv.h).
+"""ctypes binding of libfrt_ffn.so (include/frt_ffn.h, include/frt_qkv.h, include/frt_nvfp4.h).
 
 Argument marshalling only: every step of the FFN path runs in the CUDA
 library.  The functions keep the C names; a non-OK status raises FrtError
@@ -60,6 +60,18 @@ SIGNATURES = {
     "frt_qkv_forward": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _P]),
     "frt_qkv_debug_trace": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P]),
     "frt_qkv_device_status": (_I, [_P, _P]),
+    # include/frt_nvfp4.h
+    "frt_fp4_plan_create": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(_P)]),
+    "frt_fp4_plan_destroy": (_I, [_P]),
+    "frt_fp4_load_weights": (_I, [_P, _I, _P, _P, _P, _P, _P, _P]),
+    "frt_fp4_calibrate": (_I, [_P, ctypes.POINTER(_P), ctypes.POINTER(_P), _I, _I, _P]),
+    "frt_fp4_get_scales": (_I, [_P, _FP, _FP]),
+    "frt_fp4_set_scales": (_I, [_P, _FP]),
+    "frt_fp4_forward": (_I, [_P, _P, _P, _P, _I, _P]),
+    "frt_fp4_debug_trace": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P]),
+    "frt_fp4_debug_weights": (_I, [_P, _I, _I, _P, _P, _P]),
+    "frt_nvfp4_gemm": (_I, [_P, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P]),
+    "frt_fp4_device_status": (_I, [_P, _P]),
 }
 
 
@@ -260,3 +272,61 @@ def frt_qkv_debug_trace(plan, layer, residual_in, hidden_in, positions, r_prime,
 
 def frt_qkv_device_status(plan, stream) -> None:
     _check(lib().frt_qkv_device_status(plan, stream))
+
+
+# -- NVFP4 sublayer (include/frt_nvfp4.h) -----------------------------------
+
+def frt_fp4_plan_create(d, ff, act, M_max, n_layers) -> int:
+    out = _P()
+    _check(lib().frt_fp4_plan_create(d, ff, act, M_max, n_layers, ctypes.byref(out)))
+    return out.value
+
+
+def frt_fp4_plan_destroy(plan) -> None:
+    _check(lib().frt_fp4_plan_destroy(plan))
+
+
+def frt_fp4_load_weights(plan, layer, w_norm, w_gate, w_up, w_down, awq, stream) -> None:
+    _check(lib().frt_fp4_load_weights(plan, layer, w_norm, w_gate, w_up, w_down, awq, stream))
+
+
+def frt_fp4_calibrate(plan, residual_ptrs, hidden_ptrs, M, stream) -> None:
+    n = len(residual_ptrs)
+    r = _ptrs(residual_ptrs)
+    h = _ptrs(hidden_ptrs) if hidden_ptrs is not None else None
+    _check(lib().frt_fp4_calibrate(plan, ctypes.cast(r, ctypes.POINTER(_P)),
+                                   ctypes.cast(h, ctypes.POINTER(_P)) if h is not None else None, n, M, stream))
+
+
+def frt_fp4_get_scales(plan, n_layers: int):
+    act = (ctypes.c_float * (4 * n_layers))()
+    w = (ctypes.c_float * (3 * n_layers))()
+    _check(lib().frt_fp4_get_scales(plan, ctypes.cast(act, _FP), ctypes.cast(w, _FP)))
+    return list(act), list(w)
+
+
+def frt_fp4_set_scales(plan, act) -> None:
+    arr = (ctypes.c_float * len(act))(*act)
+    _check(lib().frt_fp4_set_scales(plan, ctypes.cast(arr, _FP)))
+
+
+def frt_fp4_forward(plan, residual_in, hidden_in, out, M, stream) -> None:
+    _check(lib().frt_fp4_forward(plan, residual_in, hidden_in, out, M, stream))
+
+
+def frt_fp4_debug_trace(plan, layer, residual_in, hidden_in, out, r_prime, x_codes, x_sf, g_codes, g_sf, u_codes,
+                        u_sf, h_codes, h_sf, M, stream) -> None:
+    _check(lib().frt_fp4_debug_trace(plan, layer, residual_in, hidden_in, out, r_prime, x_codes, x_sf, g_codes,
+                                     g_sf, u_codes, u_sf, h_codes, h_sf, M, stream))
+
+
+def frt_fp4_debug_weights(plan, layer, which, codes, sf, stream) -> None:
+    _check(lib().frt_fp4_debug_weights(plan, layer, which, codes, sf, stream))
+
+
+def frt_nvfp4_gemm(a_codes, a_sf, b_codes, b_sf, M, N, K, alpha, out, err, stream) -> None:
+    _check(lib().frt_nvfp4_gemm(a_codes, a_sf, b_codes, b_sf, M, N, K, alpha, out, err, stream))
+
+
+def frt_fp4_device_status(plan, stream) -> None:
+    _check(lib().frt_fp4_device_status(plan, stream))

@@ -16,7 +16,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfrt_ffn.so")
-SOURCES = ["frt_ffn.cu", "k_elementwise.cu", "k_gemm_fp8.cu", "frt_noalloc.cu", "frt_qkv.cu"]
+SOURCES = ["frt_ffn.cu", "k_elementwise.cu", "k_gemm_fp8.cu", "frt_noalloc.cu", "frt_qkv.cu", "k_nvfp4.cu",
+           "frt_nvfp4.cu"]
 HEADERS = ["frt_internal.h", "frt_ptx.cuh"]
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
@@ -35,7 +36,8 @@ def _stale(target: str, deps: list[str]) -> bool:
 def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(BUILD, exist_ok=True)
     hdrs = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(INCLUDE, "frt_ffn.h"),
-                                                       os.path.join(INCLUDE, "frt_qkv.h")]
+                                                       os.path.join(INCLUDE, "frt_qkv.h"),
+                                                       os.path.join(INCLUDE, "frt_nvfp4.h")]
 
     def compile_one(src: str) -> str:
         obj = os.path.join(BUILD, src.replace(".cu", ".o"))

@@ -129,6 +129,50 @@ cudaError_t launch_norm_quant(const void *r, const void *h, const void *w, int M
                               void *rprime, uint8_t *qx, unsigned *amax_word, bool measure, cudaStream_t s,
                               bool pdl, NormMod mod = NormMod());
 
+// ---------------------------------------------------------------- NVFP4 --
+// Epilogues of the block-scaled FP4 GEMM (k_nvfp4.cu).
+enum F4Epi : int {
+    F4_EPI_F32 = 0,    // out[m][n] = acc * alpha (fp32; diagnostics)
+    F4_EPI_AMAX = 1,   // atomicMax(amax, |acc * alpha|) (calibration)
+    F4_EPI_FP4 = 2,    // NVFP4 of acc * alpha: codes out[m][n/2], row-major block scales out_sf[m][n/16]
+    F4_EPI_RESID = 3,  // out[m][n] = bf16(resid[m][n] + acc * alpha)
+};
+
+// C[m][n] = epi(sum_k A[m][k] B[n][k]) over E2M1 operands with E4M3 block
+// scales; A rows a_row0.., B rows b_row0.. of their tensor maps (packed
+// bytes, box 128 bytes x 128 rows); sfa / sfb the TMEM-ready scales of the
+// A tiles and of the B tiles starting at b_row0.
+struct F4GemmParams {
+    const uint8_t *sfa, *sfb;
+    int a_row0, b_row0;
+    int M, K;               // valid rows of A; K % 256 == 0
+    int epi;                // F4Epi
+    float alpha;
+    float s_out, inv6_out;  // F4_EPI_FP4: tensor scale of the output and 1 / (6 s_out)
+    void *out;
+    int ldo;                // F32 / RESID: elements; FP4: bytes
+    uint8_t *out_sf;
+    int ldsf;
+    const uint16_t *resid;
+    int ldr;
+    unsigned *amax;
+    int *err;
+};
+
+size_t f4_gemm_smem();
+cudaError_t launch_f4_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const F4GemmParams &p, int n_cols,
+                           cudaStream_t s);
+cudaError_t launch_f4_amax_w(const void *w, size_t rows, int K, const float *col, unsigned *amax_word,
+                             cudaStream_t s);
+cudaError_t launch_f4_quant_w(const void *w, int rows, int K, const float *col, float sc, float inv6, uint8_t *q,
+                              uint8_t *sf, cudaStream_t s);
+cudaError_t launch_f4_norm_quant(const void *r, const void *h, const void *w, const float *awq_inv, int M, int d,
+                                 float eps, float sc, float inv6, void *rprime, uint8_t *q, uint8_t *sf,
+                                 unsigned *amax_word, bool measure, cudaStream_t s);
+cudaError_t launch_f4_geglu(const uint8_t *gq, const uint8_t *gs, float s_g, const uint8_t *uq, const uint8_t *us,
+                            float s_u, int act, int M, int ff, float s_h, float inv6, uint8_t *hq, uint8_t *hsf,
+                            unsigned *amax_word, bool measure, cudaStream_t s);
+
 }  // namespace frt
 
 namespace frt {

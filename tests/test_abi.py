@@ -82,3 +82,18 @@ def test_product_package_does_not_import_the_oracle():
             else:
                 continue
             assert not any(m.split(".")[0] in ("oracle", "synthetic") for m in mods), path
+
+
+def test_nvfp4_entry_points_check_arguments_before_any_cuda_call(native):
+    L = native.lib()
+    out = ctypes.c_void_p()
+    assert L.frt_fp4_plan_create(1000, 4096, 0, 8, 1, ctypes.byref(out)) == 1
+    assert "multiples of 256" in native.frt_ffn_last_error()
+    assert L.frt_fp4_plan_create(1024, 4096, 5, 8, 1, ctypes.byref(out)) == 1
+    assert L.frt_fp4_plan_create(1024, 4096, 0, 0, 1, ctypes.byref(out)) == 1
+    assert L.frt_fp4_forward(None, None, None, None, 1, None) == 1
+    assert L.frt_fp4_set_scales(None, None) == 1
+    assert L.frt_fp4_device_status(None, None) == 1
+    assert L.frt_fp4_plan_destroy(None) == 0
+    # the diagnostic GEMM rejects shapes its tiles do not cover
+    assert L.frt_nvfp4_gemm(None, None, None, None, 8, 128, 256, ctypes.c_float(1.0), None, None, None) == 1
