@@ -3,9 +3,12 @@ article, 7.2: norm + AWQ + FP4 quantise, gate and up NVFP4 GEMMs emitting
 FP4, GeGLU FP4 -> FP4, NVFP4 down GEMM + residual).  Same inputs and scales on
 both sides.  Contract: the block-scaled GEMM equals the exact sum within fp32
 accumulation; weight preparation bit-exact; activation codes and block scales
-identical on >= 99.9% of elements (never more than one step apart), E2M1
-codes compared with +0 and -0 equal; layer outputs under the FP8 path's
-contract on rows whose quantised activations agree."""
+identical wherever the oracle's value before rounding is not at a rounding
+tie, E2M1 codes compared with +0 and -0 equal (FP4 values lie on a coarse
+grid, so exact ties are common, and a last-ulp difference -- accumulation
+order, tanhf -- may take the other side; both roundings are valid there and
+must be one step apart); layer outputs under the FP8 path's contract on rows
+whose quantised activations agree."""
 import numpy as np
 import pytest
 import torch
@@ -16,7 +19,6 @@ from parity import bits, check_bf16, cosine
 
 pytestmark = pytest.mark.gpu
 
-AGREE = 0.999
 
 
 # ---------------------------------------------------------------- layouts --
@@ -66,22 +68,47 @@ def ordinal(codes):
     return np.where(c & 8, -(c & 7), c & 7)
 
 
-def check_fp4(got, ref, what):
-    g, r = ordinal(got), ordinal(ref)
-    assert g.shape == r.shape, what
-    same = float(np.mean(g == r))
-    assert same >= AGREE, "%s: only %.5f of E2M1 codes agree" % (what, same)
-    assert int(np.abs(g - r).max()) <= 1, "%s: E2M1 codes more than one step apart" % what
-    return same
+E2M1_MIDS = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
+_E4M3_POS = oracle.e4m3_decode(np.arange(0, 0x7F, dtype=np.uint8)).astype(np.float64)
+E4M3_MIDS = (_E4M3_POS[:-1] + _E4M3_POS[1:]) / 2
+TIE_REL = 2e-3  # two fp32 evaluations of the same value (accumulation order, tanhf ulps) differ far less
 
 
-def check_scales(got, ref, what):
-    g = np.asarray(got, np.int32)
-    r = np.asarray(ref, np.int32)
-    same = float(np.mean(g == r))
-    assert same >= AGREE, "%s: only %.5f of block scales agree" % (what, same)
-    assert int(np.abs(g - r).max()) <= 1, "%s: block scales more than one step apart" % what
-    return same
+def near_tie(t, mids):
+    """|t| within TIE_REL of a rounding midpoint (where either rounding is valid)."""
+    t = np.abs(np.asarray(t, np.float64)).ravel()
+    if t.size == 0:
+        return np.zeros(0, bool)
+    d = np.abs(t[:, None] - mids[None, :]).min(axis=1)
+    return d <= TIE_REL * np.maximum(t, 1e-30)
+
+
+def check_nvfp4(got_q, got_sb, ref_q, ref_sb, x, s, what):
+    """GPU NVFP4 codes and block scales against the oracle's: identical except
+    where the oracle's own pre-rounding value sits at a rounding tie (block
+    scale: amax / (6 s) at an E4M3 midpoint; element: x / (dec(b) s) at an
+    E2M1 midpoint), and then one step apart.  x: the oracle's fp32 values
+    before quantisation [rows, K]."""
+    x = np.asarray(x, np.float32)
+    rows, K = x.shape
+    blk = x.reshape(rows, K // 16, 16)
+    inv6 = np.float32(oracle.recip(np.float32(6.0) * np.float32(s)))
+    t_sb = (np.abs(blk).max(axis=2) * inv6).astype(np.float32)
+    gsb, rsb = np.asarray(got_sb, np.int32), np.asarray(ref_sb, np.int32)
+    dsb = gsb != rsb
+    assert np.abs(gsb - rsb).max(initial=0) <= 1, "%s: block scales more than one step apart" % what
+    assert near_tie(t_sb[dsb], E4M3_MIDS).all(), "%s: a block scale differs off a rounding tie" % what
+    assert dsb.mean() <= 0.01, "%s: %.4f of block scales differ" % (what, dsb.mean())
+    den = (oracle.e4m3_decode(np.asarray(ref_sb, np.uint8)) * np.float32(s)).astype(np.float32)
+    inv = np.where(den > 0, np.float32(1) / np.where(den > 0, den, 1), 0).astype(np.float32)
+    t_q = (blk * inv[:, :, None]).astype(np.float32).reshape(rows, K)
+    g, r = ordinal(got_q), ordinal(ref_q)
+    same_blk = np.repeat(~dsb, 16, axis=1)
+    dq = (g != r) & same_blk
+    assert np.abs(g - r)[same_blk].max(initial=0) <= 1, "%s: E2M1 codes more than one step apart" % what
+    assert near_tie(t_q[dq], E2M1_MIDS).all(), "%s: an E2M1 code differs off a rounding tie" % what
+    assert dq.mean() <= 0.01, "%s: %.4f of E2M1 codes differ" % (what, dq.mean())
+    return ~(dsb.any(axis=1) | (g != r).any(axis=1))
 
 
 def dev(a):
@@ -199,26 +226,22 @@ def test_layer_matches_oracle(layer_case):
     # N1: the normalised activation
     xq = unpack(tr["x_codes"].cpu().numpy())
     xs = sf_from_tmem(tr["x_sf"].cpu().numpy(), M, d)
-    check_scales(xs, ref.x[1], "x block scales")
-    check_fp4(xq, ref.x[0], "x codes")
-    rows = np.all(canon(xq) == canon(ref.x[0]), axis=1) & np.all(xs == ref.x[1], axis=1)
+    rows = check_nvfp4(xq, xs, ref.x[0], ref.x[1], ref.y, c["sc"].s_x, "x")
     assert rows.mean() >= 0.5
     # N2: gate and up, on rows whose X agrees
     gq, uq = unpack(tr["g_codes"].cpu().numpy()), unpack(tr["u_codes"].cpu().numpy())
     gs, us = tr["g_sf"].cpu().numpy(), tr["u_sf"].cpu().numpy()
-    check_scales(gs[rows], ref.g[1][rows], "gate block scales")
-    check_fp4(gq[rows], ref.g[0][rows], "gate codes")
-    check_scales(us[rows], ref.u[1][rows], "up block scales")
-    check_fp4(uq[rows], ref.u[0][rows], "up codes")
-    rows &= np.all(canon(gq) == canon(ref.g[0]), axis=1) & np.all(canon(uq) == canon(ref.u[0]), axis=1)
-    rows &= np.all(gs == ref.g[1], axis=1) & np.all(us == ref.u[1], axis=1)
+    rows_g = check_nvfp4(gq[rows], gs[rows], ref.g[0][rows], ref.g[1][rows], ref.g_f32[rows], c["sc"].s_g, "gate")
+    rows_u = check_nvfp4(uq[rows], us[rows], ref.u[0][rows], ref.u[1][rows], ref.u_f32[rows], c["sc"].s_u, "up")
+    sel = np.nonzero(rows)[0]
+    rows[sel[~(rows_g & rows_u)]] = False
     assert rows.mean() >= 0.25
     # N3: the gated activation, on rows whose G and U agree
     hq = unpack(tr["h_codes"].cpu().numpy())
     hs = sf_from_tmem(tr["h_sf"].cpu().numpy(), M, ff)
-    check_scales(hs[rows], ref.h[1][rows], "h block scales")
-    check_fp4(hq[rows], ref.h[0][rows], "h codes")
-    rows &= np.all(canon(hq) == canon(ref.h[0]), axis=1) & np.all(hs == ref.h[1], axis=1)
+    rows_h = check_nvfp4(hq[rows], hs[rows], ref.h[0][rows], ref.h[1][rows], ref.a[rows], c["sc"].s_h, "h")
+    sel = np.nonzero(rows)[0]
+    rows[sel[~rows_h]] = False
     # N4: the output, on rows whose every quantised activation agrees
     if rows.any():
         check_bf16(bits(tr["out"])[rows], ref.out[rows], "out")
