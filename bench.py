@@ -522,6 +522,128 @@ def run_qkv(args, wl, world, rank, local):
     return line
 
 
+def run_fp4(args, wl, world, rank, local):
+    """The NVFP4 variant of the FFN stack (norm + AWQ-free FP4 quantise, gate
+    and up NVFP4 GEMMs emitting FP4, GeGLU FP4 -> FP4, NVFP4 down GEMM +
+    residual): one step = the L layers on one batch, one CUDA graph."""
+    from realtime_transformer_gb300.nvfp4 import FP4Plan
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    P = peaks()
+    r, h = synthetic.inputs(wl, device=dev)
+    calib = synthetic.calibration_batches(wl, device=dev)
+    plan = FP4Plan(wl.d, wl.ff, wl.act, wl.M, wl.L)
+    for l in range(wl.L):
+        w = synthetic.layer_weights(wl, l, device=dev)
+        plan.load_weights(l, w["w_norm"], w["w_gate"], w["w_up"], w["w_down"])
+    plan.calibrate([a for a, _ in calib], [b for _, b in calib])
+    out = torch.empty_like(r)
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    with torch.cuda.stream(stream):
+        plan.forward(r, h, out=out, stream=stream)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            plan.forward(r, h, out=out, stream=stream)
+    torch.cuda.synchronize()
+
+    def timed(fn, n, warm):
+        for _ in range(warm):
+            with torch.cuda.stream(stream):
+                flush.zero_()
+                fn()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        with torch.cuda.stream(stream):
+            for e0, e1 in evs:
+                flush.zero_()
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+        torch.cuda.synchronize()
+        return [e0.elapsed_time(e1) for e0, e1 in evs]
+
+    timed(graph.replay, 0, args.warmup)
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    t_wall0 = time.perf_counter()
+    step_ms = timed(graph.replay, args.steps, 0)
+    t_wall = time.perf_counter() - t_wall0
+    clocks = sampler.stop()
+    barrier(world)
+    plan.device_status(stream)
+    total_s = reduce_max(sum(step_ms) / 1000.0, world, dev)
+    value = world * wl.M * args.steps / total_s
+    ms_step = 1000.0 * total_s / args.steps
+
+    # end to end: pinned host residual + hidden in, the graph, the output back
+    h_io = torch.cat([r, h]).cpu().pin_memory()
+    h_out = torch.empty_like(out, device="cpu").pin_memory()
+    io = torch.empty_like(h_io, device=dev)
+
+    def e2e_step():
+        io.copy_(h_io, non_blocking=True)
+        r.copy_(io[:wl.M])
+        h.copy_(io[wl.M:])
+        graph.replay()
+        h_out.copy_(out, non_blocking=True)
+
+    e2e_ms = timed(e2e_step, args.steps, args.warmup)
+    e2e_s = reduce_max(sum(e2e_ms) / 1000.0, world, dev)
+
+    # roofline of one layer (its five kernels together): FP4 weights and their
+    # scales + the residual stream in and out, against HBM or the FP4 tensor
+    # peak by intensity
+    layer_s = ms_step / 1000.0 / wl.L
+    nbytes = 3 * wl.d * wl.ff // 2 + 3 * wl.d * wl.ff // 16 + 4 * wl.M * wl.d
+    flops = 6.0 * wl.M * wl.d * wl.ff
+    fp4_peak = 6.0 * P["bf16_tflops"]
+    if flops / nbytes > fp4_peak * 1e12 / (P["hbm_gbs"] * 1e9):
+        ach = flops / layer_s / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": fp4_peak, "unit": "TFLOP/s", "frac": ach / fp4_peak,
+                "peak_note": "FP4 dense = 6 x measured bf16 burst (%s; nominal 13.5 / 2.25)" % P["src"]}
+    else:
+        ach = nbytes / layer_s / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": P["hbm_gbs"], "unit": "GB/s", "frac": ach / P["hbm_gbs"],
+                "peak_note": "%s HBM copy bandwidth" % P["src"]}
+    roof.update({"kernel": "nvfp4 layer (norm_quant + gate + up GEMMs + geglu + down GEMM, graph-replayed)",
+                 "us_per_launch": 1e6 * layer_s, "algorithmic_bytes": nbytes, "traffic": None})
+    line = {
+        "metric": "NVFP4 FFN stack tokens/s (graph-replayed, %s)" % wl.name, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "us_per_layer": 1e6 * layer_s, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "nvfp4 (e2m1 + e4m3 block scales, fp32 accumulate, bf16 residual)", "data": "synthetic",
+        "config": dict(config_of(wl), weights="NVFP4 (E2M1, E4M3 scale per 16, fp32 per tensor)",
+                       activations="NVFP4, calibrated per-tensor scales", graph="one CUDA graph per stack"),
+        "roofline": roof,
+        "e2e": {"value": world * wl.M * args.steps / e2e_s, "unit": "tokens/s",
+                "h2d_bytes_per_step": h_io.numel() * 2, "d2h_bytes_per_step": h_out.numel() * 2,
+                "ms_per_step": 1000.0 * e2e_s / args.steps},
+        "gpu_launches": args.steps * wl.L * 5, "clocks": clocks, "wall_s_timed_region": t_wall,
+    }
+    plan.close()
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        bits = synthetic.bf16_bits
+        w0 = {k: bits(v) for k, v in synthetic.layer_weights(wl, 0).items()}
+        L0 = oracle.quantize_layer_nvfp4(w0["w_norm"], w0["w_gate"], w0["w_up"], w0["w_down"])
+        rows = min(wl.M, 16)
+        rc, hc = calib[0][0][:rows].cpu(), calib[0][1][:rows].cpu()
+        sc, _ = oracle.calibrate_layer_nvfp4([bits(rc)], [bits(hc)], L0, wl.act_id)
+        rr, hh = bits(r[:rows].cpu()), bits(h[:rows].cpu())
+        t0 = time.perf_counter()
+        oracle.ffn_layer_nvfp4(rr, hh, L0, sc, wl.act_id)
+        dt = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": rows / (dt * wl.L), "unit": "tokens/s", "cores": cpu_cores(),
+                                "kind": "oracle", "sample": "%d of %d tokens through one of the %d layers, "
+                                "scaled to the stack" % (rows, wl.M, wl.L)}
+    return line
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -530,8 +652,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(synthetic.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--sublayer", choices=["ffn", "qkv"], default="ffn",
-                    help="ffn: the FFN stack (the default bench line); qkv: the attention-input projections")
+    ap.add_argument("--sublayer", choices=["ffn", "qkv", "ffn_nvfp4"], default="ffn",
+                    help="ffn: the FFN stack (the default bench line); qkv: the attention-input projections; "
+                         "ffn_nvfp4: the NVFP4 variant of the FFN stack")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling aid: run a plan of this many layers of the workload's shape "
                          "(the line is then not the workload's bench line)")
@@ -546,6 +669,8 @@ def main():
         line = run_reference(args, wl, world, rank)
     elif args.sublayer == "qkv":
         line = run_qkv(args, wl, world, rank, local)
+    elif args.sublayer == "ffn_nvfp4":
+        line = run_fp4(args, wl, world, rank, local)
     else:
         line = run_ours(args, wl, world, rank, local)
     if rank == 0 and line is not None:
