@@ -117,10 +117,15 @@ frt_status frt_fp4_debug_weights(frt_fp4_plan_t plan, int layer, int which, void
  * Test/diagnostic: out[m][n] = alpha * sum_k A[m][k] B[n][k] over NVFP4
  * operands (codes [M, K/2] and [N, K/2]; TMEM-ready scales sized for
  * ceil(M/128) and N/128 tiles), fp32 [M, N] out.  N % 128 == 0, K % 256 == 0,
- * 1 <= M <= 65536.  err: a device int the kernel sets on a timed-out wait.
+ * 1 <= M <= 65536.  splits: split-K factor (1 <= splits <= K / 256); above 1,
+ * ws (fp32, tiles * splits * 128 * 128, tiles = N/128 * ceil(M/128) <= 4096)
+ * and counters (tiles zeroed ints, left zeroed) are device scratch; the
+ * partials are summed in split order.  err: a device int the kernel sets on a
+ * timed-out wait.
  */
 frt_status frt_nvfp4_gemm(const void *a_codes, const void *a_sf, const void *b_codes, const void *b_sf, int M, int N,
-                          int K, float alpha, float *out, int *err, frt_stream_t stream);
+                          int K, float alpha, float *out, int splits, float *ws, int *counters, int *err,
+                          frt_stream_t stream);
 
 /* Synchronise `stream` and report a kernel that gave up a bounded wait
  * (DEVICE_TIMEOUT; the plan's error word is then cleared). */

@@ -70,7 +70,7 @@ SIGNATURES = {
     "frt_fp4_forward": (_I, [_P, _P, _P, _P, _I, _P]),
     "frt_fp4_debug_trace": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P]),
     "frt_fp4_debug_weights": (_I, [_P, _I, _I, _P, _P, _P]),
-    "frt_nvfp4_gemm": (_I, [_P, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P]),
+    "frt_nvfp4_gemm": (_I, [_P, _P, _P, _P, _I, _I, _I, _F, _P, _I, _P, _P, _P, _P]),
     "frt_fp4_device_status": (_I, [_P, _P]),
 }
 
@@ -324,8 +324,9 @@ def frt_fp4_debug_weights(plan, layer, which, codes, sf, stream) -> None:
     _check(lib().frt_fp4_debug_weights(plan, layer, which, codes, sf, stream))
 
 
-def frt_nvfp4_gemm(a_codes, a_sf, b_codes, b_sf, M, N, K, alpha, out, err, stream) -> None:
-    _check(lib().frt_nvfp4_gemm(a_codes, a_sf, b_codes, b_sf, M, N, K, alpha, out, err, stream))
+def frt_nvfp4_gemm(a_codes, a_sf, b_codes, b_sf, M, N, K, alpha, out, splits, ws, counters, err, stream) -> None:
+    _check(lib().frt_nvfp4_gemm(a_codes, a_sf, b_codes, b_sf, M, N, K, alpha, out, splits, ws, counters, err,
+                                stream))
 
 
 def frt_fp4_device_status(plan, stream) -> None:

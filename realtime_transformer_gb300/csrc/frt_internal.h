@@ -157,6 +157,9 @@ struct F4GemmParams {
     int ldr;
     unsigned *amax;
     int *err;
+    int splits;             // split-K factor (grid z); > 1 needs ws and counters
+    float *ws;              // fp32 partial tiles: [tiles][splits][128 x 128]
+    int *counters;          // one zeroed arrival counter per output tile (re-armed by the kernel)
 };
 
 size_t f4_gemm_smem();

@@ -79,8 +79,11 @@ struct frt_fp4_plan {
     uint16_t *res[2] = {nullptr, nullptr};  // layer outputs between layers
     unsigned *amax = nullptr;               // [4]
     int *err = nullptr;
-    CUtensorMap tm_wg, tm_wu, tm_wd, tm_xq, tm_hq;
+    int num_sms = 0;
+    float *ws = nullptr;                    // split-K partial tiles: num_sms x 128 x 128 fp32
+    int *counters = nullptr;                // split-K arrival counters, one per tile
     std::vector<float> s_wg, s_wu, s_wd, s_x, s_g, s_u, s_h;
+    CUtensorMap tm_wg, tm_wu, tm_wd, tm_xq, tm_hq;
     std::vector<char> loaded, has_awq;
     bool scaled = false;
 };
@@ -90,7 +93,7 @@ namespace {
 void free_fp4(frt_fp4_plan *P) {
     void *ptrs[] = {P->wg, P->wu,  P->wd,  P->sg,  P->su,     P->sd,     P->w_norm, P->awq_inv, P->xq,
                     P->xsf, P->gq, P->gs,  P->uq,  P->us,     P->hq,     P->hsf,    P->rp,      P->res[0],
-                    P->res[1], P->amax, P->err};
+                    P->res[1], P->amax, P->err, P->ws, P->counters};
     for (void *p : ptrs)
         if (p) cudaFree(p);
     delete P;
@@ -106,6 +109,20 @@ frt_status check_ready(frt_fp4_plan *P) {
 }
 
 size_t wsf_bytes(size_t rows, size_t K) { return rows * K / 16; }
+
+constexpr int F4_MAX_TILES = 4096;
+
+// Split-K factor of a GEMM with `tiles` output tiles and K / 256 stages:
+// enough splits to put a CTA on most SMs, each split at least two stages
+// long (one CTA per SM: the kernel's shared memory allows no more).
+int f4_splits(int tiles, int KB, int num_sms) {
+    if (tiles > F4_MAX_TILES)
+        return 1;
+    int s = num_sms / tiles;
+    if (s > KB / 2)
+        s = KB / 2;
+    return s < 1 ? 1 : s;
+}
 
 }  // namespace
 
@@ -159,6 +176,10 @@ FRT_API frt_status frt_fp4_plan_create(int d, int ff, int act, int M_max, int n_
     if (e == cudaSuccess) e = cudaMalloc(&P->res[1], MA * D * 2);
     if (e == cudaSuccess) e = cudaMalloc(&P->amax, 16);
     if (e == cudaSuccess) e = cudaMalloc(&P->err, 4);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&P->num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaMalloc(&P->ws, (size_t)P->num_sms * 128 * 128 * 4);
+    if (e == cudaSuccess) e = cudaMalloc(&P->counters, F4_MAX_TILES * 4);
+    if (e == cudaSuccess) e = cudaMemset(P->counters, 0, F4_MAX_TILES * 4);
     // the GEMMs read operand rows (and their scales) up to M_alloc: padding stays zero
     if (e == cudaSuccess) e = cudaMemset(P->xq, 0, MA * D / 2);
     if (e == cudaSuccess) e = cudaMemset(P->xsf, 0, MA * D / 16);
@@ -271,6 +292,9 @@ cudaError_t f4_gate_up(frt_fp4_plan *P, int l, bool up, int M, int epi, cudaStre
     p.ldsf = P->ff / 16;
     p.amax = P->amax + (up ? 1 : 0);
     p.err = P->err;
+    p.splits = f4_splits((P->ff / 128) * ((M + 127) / 128), P->d / 256, P->num_sms);
+    p.ws = P->ws;
+    p.counters = P->counters;
     return launch_f4_gemm(P->tm_xq, up ? P->tm_wu : P->tm_wg, p, P->ff, s);
 }
 
@@ -297,6 +321,9 @@ cudaError_t f4_down(frt_fp4_plan *P, int l, const void *resid, void *out, int M,
     p.resid = static_cast<const uint16_t *>(resid);
     p.ldr = P->d;
     p.err = P->err;
+    p.splits = f4_splits((P->d / 128) * ((M + 127) / 128), P->ff / 256, P->num_sms);
+    p.ws = P->ws;
+    p.counters = P->counters;
     return launch_f4_gemm(P->tm_hq, P->tm_wd, p, P->d, s);
 }
 
@@ -522,13 +549,18 @@ FRT_API frt_status frt_fp4_debug_weights(frt_fp4_plan_t P, int layer, int which,
 }
 
 FRT_API frt_status frt_nvfp4_gemm(const void *a_codes, const void *a_sf, const void *b_codes, const void *b_sf,
-                                  int M, int N, int K, float alpha, float *out, int *err, frt_stream_t stream) {
+                                  int M, int N, int K, float alpha, float *out, int splits, float *ws, int *counters,
+                                  int *err, frt_stream_t stream) {
     if (!a_codes || !a_sf || !b_codes || !b_sf || !out || !err || !al16(a_codes) || !al16(a_sf) ||
         !al16(b_codes) || !al16(b_sf) || !al16(out))
         return ffail(FRT_ERR_INVALID_ARG, "pointers must be non-null and 16-byte aligned");
     if (M < 1 || M > 65536 || N < 128 || N % 128 || K < 256 || K % 256)
         return ffail(FRT_ERR_INVALID_ARG, "M=%d N=%d K=%d: need 1 <= M <= 65536, N %% 128 == 0, K %% 256 == 0", M,
                      N, K);
+    const int tiles = (N / 128) * ((M + 127) / 128);
+    if (splits < 1 || splits > K / 256 || (splits > 1 && (!ws || !counters || !al16(ws) || tiles > F4_MAX_TILES)))
+        return ffail(FRT_ERR_INVALID_ARG, "splits=%d: need 1 <= splits <= K / 256 and, above 1, ws and counters",
+                     splits);
     CUtensorMap ta, tb;
     if (encode_tmap_u8(&ta, a_codes, (uint64_t)M, (uint64_t)K / 2, 128) != cudaSuccess ||
         encode_tmap_u8(&tb, b_codes, (uint64_t)N, (uint64_t)K / 2, 128) != cudaSuccess)
@@ -544,6 +576,9 @@ FRT_API frt_status frt_nvfp4_gemm(const void *a_codes, const void *a_sf, const v
     p.out = out;
     p.ldo = N;
     p.err = err;
+    p.splits = splits;
+    p.ws = ws;
+    p.counters = counters;
     FCK(launch_f4_gemm(ta, tb, p, N, static_cast<cudaStream_t>(stream)));
     return FRT_OK;
 }

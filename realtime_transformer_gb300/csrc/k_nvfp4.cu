@@ -178,26 +178,29 @@ __global__ void k_f4_quant_w(const uint4 *__restrict__ w, int rows, int K, const
 
 // ------------------------------------------- residual + norm + quantise --
 
-// One warp per row, eight rows per CTA.  Pass 1: r' = bf16(r + h) (stored
-// if rprime), the sum of squares; pass 2: y = ((r' * inv) * w) [* awq_inv],
-// then the amax (MEASURE) or the NVFP4 codes and TMEM-ready scales of y.
-template <bool MEASURE>
+// WPR warps per row (1, 2, 4 or 8), 8 / WPR rows per CTA; a thread takes
+// blocks of 16 elements strided by 32 WPR.  Pass 1: r' = bf16(r + h) (stored
+// if rprime), the sum of squares (per thread, a warp-shuffle tree, then the
+// row's warps in order); pass 2: y = ((r' * inv) * w) [* awq_inv], then the
+// amax (MEASURE) or the NVFP4 codes and TMEM-ready scales of y.
+template <bool MEASURE, int WPR>
 __global__ void __launch_bounds__(256) k_f4_norm_quant(const uint16_t *__restrict__ r, const uint16_t *__restrict__ h,
                                                        const uint16_t *__restrict__ w,
                                                        const float *__restrict__ awq_inv, int M, int d, float eps,
                                                        float s, float inv6, uint16_t *__restrict__ rprime,
                                                        uint8_t *__restrict__ q, uint8_t *__restrict__ sf,
                                                        unsigned *amax_word) {
-    const int lane = threadIdx.x & 31;
-    const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (row >= M)
-        return;
-    const int ng = d / 16;
-    const uint4 *rv = reinterpret_cast<const uint4 *>(r + (size_t)row * d);
-    const uint4 *hv = h ? reinterpret_cast<const uint4 *>(h + (size_t)row * d) : nullptr;
+    __shared__ float s_part[8];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int tid = (warp % WPR) * 32 + lane;
+    const int row = blockIdx.x * (8 / WPR) + warp / WPR;
+    const bool active = row < M;
+    const int ng = active ? d / 16 : 0;
+    const uint4 *rv = reinterpret_cast<const uint4 *>(r + (size_t)(active ? row : 0) * d);
+    const uint4 *hv = h ? reinterpret_cast<const uint4 *>(h + (size_t)(active ? row : 0) * d) : nullptr;
     const uint4 *wv = reinterpret_cast<const uint4 *>(w);
     float ss = 0.0f;
-    for (int g = lane; g < ng; g += 32) {
+    for (int g = tid; g < ng; g += 32 * WPR) {
         float x[16];
         unpack8(rv[2 * g], x);
         unpack8(rv[2 * g + 1], x + 8);
@@ -223,9 +226,20 @@ __global__ void __launch_bounds__(256) k_f4_norm_quant(const uint16_t *__restric
             ss = __fadd_rn(ss, __fmul_rn(x[j], x[j]));
     }
     ss = warp_sum(ss);
+    if (WPR > 1) {
+        if (lane == 0)
+            s_part[warp] = ss;
+        __syncthreads();
+        const int w0 = (warp / WPR) * WPR;
+        ss = 0.0f;
+        for (int k = 0; k < WPR; ++k)
+            ss = __fadd_rn(ss, s_part[w0 + k]);
+    }
+    if (!active)
+        return;
     const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)d), eps)));
     float amax = 0.0f;
-    for (int g = lane; g < ng; g += 32) {
+    for (int g = tid; g < ng; g += 32 * WPR) {
         float x[16], wf[16];
         unpack8(rv[2 * g], x);
         unpack8(rv[2 * g + 1], x + 8);
@@ -265,46 +279,68 @@ __global__ void __launch_bounds__(256) k_f4_norm_quant(const uint16_t *__restric
 
 // ------------------------------------------------ GeGLU FP4 -> FP4 --
 
+// E2M1 code of one fp32 value (low nibble of a pair conversion with 0).
+__device__ __forceinline__ uint32_t e2m1_one(float x) {
+    uint32_t v;
+    asm("{\n\t.reg .b8 b;\n\tcvt.rn.satfinite.e2m1x2.f32 b, %2, %1;\n\tcvt.u32.u8 %0, b;\n\t}"
+        : "=r"(v)
+        : "f"(x), "f"(0.0f));
+    return v & 15u;
+}
+
 // a = act(dec G) * dec U per element, then the amax (MEASURE) or the NVFP4
 // codes and TMEM-ready scales of a.  G and U: codes [M, ff/2], row-major
-// block scales [M, ff/16], tensor scales s_g, s_u.  One thread per block of 16.
+// block scales [M, ff/16], tensor scales s_g, s_u.  One thread per element,
+// a block of 16 on 16 lanes: its amax by shuffles, the codes of lane pairs
+// combined into bytes.  The element count M ff is a multiple of 16, so a
+// half-warp is a whole block or wholly past the end.
 template <bool MEASURE>
 __global__ void k_f4_geglu(const uint8_t *__restrict__ gq, const uint8_t *__restrict__ gs, float s_g,
                            const uint8_t *__restrict__ uq, const uint8_t *__restrict__ us, float s_u, int act, int M,
                            int ff, float s_h, float inv6, uint8_t *__restrict__ hq, uint8_t *__restrict__ hsf,
                            unsigned *amax_word) {
+    const int lane = threadIdx.x & 31;
     const int gpr = ff / 16;
-    const size_t n = (size_t)M * gpr;
-    float amax = 0.0f;
-    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
-        const int m = (int)(i / gpr), g = (int)(i % gpr);
-        const uint2 gc = reinterpret_cast<const uint2 *>(gq)[i];
-        const uint2 uc = reinterpret_cast<const uint2 *>(uq)[i];
-        const float gb = e4m3_dec(gs[i]), ub = e4m3_dec(us[i]);
-        float a[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const uint32_t gw = j < 8 ? gc.x : gc.y, uw = j < 8 ? uc.x : uc.y;
-            const int sh = 4 * (j & 7);
-            const float gv = __fmul_rn(__fmul_rn(e2m1_dec((gw >> sh) & 15u), gb), s_g);
-            const float uv = __fmul_rn(__fmul_rn(e2m1_dec((uw >> sh) & 15u), ub), s_u);
-            a[j] = __fmul_rn(act_f32(act, gv), uv);
+    const size_t total = (size_t)M * ff;
+    const size_t step = (size_t)gridDim.x * blockDim.x;
+    float amax_all = 0.0f;
+    for (size_t base = (size_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31u); base < total; base += step) {
+        const size_t e = base + lane;
+        const bool valid = e < total;
+        const size_t i = valid ? e / 16 : 0;  // block index
+        const int j = lane & 15;
+        float a = 0.0f;
+        if (valid) {
+            const uint32_t gb = gq[e / 2], ub = uq[e / 2];
+            const uint32_t gc = (j & 1) ? gb >> 4 : gb & 15u, uc = (j & 1) ? ub >> 4 : ub & 15u;
+            const float gv = __fmul_rn(__fmul_rn(e2m1_dec(gc), e4m3_dec(gs[i])), s_g);
+            const float uv = __fmul_rn(__fmul_rn(e2m1_dec(uc), e4m3_dec(us[i])), s_u);
+            a = __fmul_rn(act_f32(act, gv), uv);
         }
         if (MEASURE) {
+            amax_all = fmaxf(amax_all, fabsf(a));
+            continue;
+        }
+        float m = fabsf(a);
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-                amax = fmaxf(amax, fabsf(a[j]));
-        } else {
-            uint2 c;
-            const uint32_t b = quant_block16(a, s_h, inv6, c);
-            reinterpret_cast<uint2 *>(hq)[i] = c;
-            hsf[sf_offset(m, g, ff)] = (uint8_t)b;
+        for (int o = 8; o > 0; o >>= 1)
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        const uint32_t b = (uint32_t)__nv_cvt_float_to_fp8(__fmul_rn(m, inv6), __NV_SATFINITE, __NV_E4M3);
+        const float den = __fmul_rn(e4m3_dec(b), s_h);
+        const float inv = den > 0.0f ? __frcp_rn(den) : 0.0f;
+        const uint32_t c = e2m1_one(__fmul_rn(a, inv));
+        const uint32_t hi = __shfl_xor_sync(0xffffffffu, c, 1);
+        if (valid && !(j & 1))
+            hq[e / 2] = (uint8_t)(c | (hi << 4));
+        if (valid && j == 0) {
+            const int row = (int)(i / gpr), g = (int)(i % gpr);
+            hsf[sf_offset(row, g, ff)] = (uint8_t)b;
         }
     }
     if (MEASURE) {
-        amax = warp_max(amax);
-        if ((threadIdx.x & 31) == 0)
-            atomicMax(amax_word, __float_as_uint(amax));
+        amax_all = warp_max(amax_all);
+        if (lane == 0)
+            atomicMax(amax_word, __float_as_uint(amax_all));
     }
 }
 
@@ -346,11 +382,44 @@ __host__ __device__ constexpr uint32_t idesc_nvf4(int m, int n) {
     return (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
+// The epilogue of 16 consecutive output columns n.. of one row, v = acc * alpha.
+template <int EPI>
+__device__ __forceinline__ void epi_chunk(const F4GemmParams &p, int row, int n, const float *v, float &amax) {
+    if constexpr (EPI == F4_EPI_F32) {
+        float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + (size_t)row * p.ldo + n);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            o[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    } else if constexpr (EPI == F4_EPI_AMAX) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            amax = fmaxf(amax, fabsf(v[j]));
+    } else if constexpr (EPI == F4_EPI_FP4) {
+        uint2 c2;
+        const uint32_t b = quant_block16(v, p.s_out, p.inv6_out, c2);
+        *reinterpret_cast<uint2 *>(static_cast<uint8_t *>(p.out) + (size_t)row * p.ldo + n / 2) = c2;
+        p.out_sf[(size_t)row * p.ldsf + n / 16] = (uint8_t)b;
+    } else {  // F4_EPI_RESID: out = bf16(r' + acc * alpha)
+        const uint4 *rr = reinterpret_cast<const uint4 *>(p.resid + (size_t)row * p.ldr + n);
+        float x[16];
+        unpack8(rr[0], x);
+        unpack8(rr[1], x + 8);
+        uint32_t w[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            w[j] = bf16_bits(__fadd_rn(x[2 * j], v[2 * j])) | (bf16_bits(__fadd_rn(x[2 * j + 1], v[2 * j + 1])) << 16);
+        uint4 *o = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) + (size_t)row * p.ldo + n);
+        o[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        o[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+}
+
 template <int EPI>
 __global__ void __launch_bounds__(192, 1)
     k_gemm_nvfp4(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ F4GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
+    __shared__ int s_last;  // split-K: this CTA reduces the tile
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *sA = smem;
     uint8_t *sB = sA + F4_STAGES * F4_TILE;
@@ -365,7 +434,10 @@ __global__ void __launch_bounds__(192, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * F4_BN, m0 = blockIdx.y * F4_BM;
+    // this CTA's split of the K stages
     const int KB = p.K / 256;
+    const int z = blockIdx.z;
+    const int kb0 = (int)((long)z * KB / p.splits), kb1 = (int)((long)(z + 1) * KB / p.splits);
     if (threadIdx.x == 0) {
         for (int s = 0; s < F4_STAGES; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
@@ -399,7 +471,7 @@ __global__ void __launch_bounds__(192, 1)
             int stage = 0;
             uint32_t phase = 0, issued = 0, issued_par = 0;
             bool ok = true;
-            for (int kb = 0; kb < KB && ok; ++kb) {
+            for (int kb = kb0; kb < kb1 && ok; ++kb) {
                 if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, abort_f, p.err)) {
                     ok = false;
                     break;
@@ -431,7 +503,7 @@ __global__ void __launch_bounds__(192, 1)
             int stage = 0;
             uint32_t phase = 0;
             bool issued_any = false, ok = true;
-            for (int kb = 0; kb < KB; ++kb) {
+            for (int kb = kb0; kb < kb1; ++kb) {
                 if (!mbar_wait(smem_u32(&full[stage]), phase, abort_f, p.err)) {
                     ok = false;
                     break;
@@ -448,7 +520,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
                     mma_nvf4(tmem_base, smem_desc_k128(aA + j * F4_UKB), smem_desc_k128(aB + j * F4_UKB), idesc,
-                             t_sf + 4 * j, t_sf + 16 + 4 * j, (kb > 0 || j > 0) ? 1u : 0u);
+                             t_sf + 4 * j, t_sf + 16 + 4 * j, (kb > kb0 || j > 0) ? 1u : 0u);
                 issued_any = true;
                 mma_commit(smem_u32(&empty[stage]));
                 if (++stage == F4_STAGES) {
@@ -470,57 +542,92 @@ __global__ void __launch_bounds__(192, 1)
         if (lane == 0)
             ok = mbar_wait(smem_u32(tfull), 0, abort_f, p.err) ? 1 : 0;
         ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (ok) {
-            tc_fence_after();
-            const int row = m0 + warp * 32 + lane;
-            const bool valid = row < p.M;
-            float amax = 0.0f;
+        const int r = warp * 32 + lane;
+        const int row = m0 + r;
+        const bool valid = row < p.M;
+        float amax = 0.0f;
+        if (p.splits == 1) {
+            if (ok) {
+                tc_fence_after();
 #pragma unroll 1
-            for (int c = 0; c < F4_BN / 16; ++c) {
-                uint32_t raw[16];
-                __syncwarp();
-                tmem_ld_x16(tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(c * 16), raw);
-                tmem_ld_wait();
-                float v[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    v[j] = __fmul_rn(__uint_as_float(raw[j]), p.alpha);
-                const int n = n0 + c * 16;
-                if (!valid) {
-                } else if constexpr (EPI == F4_EPI_F32) {
-                    float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + (size_t)row * p.ldo + n);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        o[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-                } else if constexpr (EPI == F4_EPI_AMAX) {
+                for (int c = 0; c < F4_BN / 16; ++c) {
+                    uint32_t raw[16];
+                    __syncwarp();
+                    tmem_ld_x16(tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(c * 16), raw);
+                    tmem_ld_wait();
+                    float v[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
-                        amax = fmaxf(amax, fabsf(v[j]));
-                } else if constexpr (EPI == F4_EPI_FP4) {
-                    uint2 c2;
-                    const uint32_t b = quant_block16(v, p.s_out, p.inv6_out, c2);
-                    *reinterpret_cast<uint2 *>(static_cast<uint8_t *>(p.out) + (size_t)row * p.ldo + n / 2) = c2;
-                    p.out_sf[(size_t)row * p.ldsf + n / 16] = (uint8_t)b;
-                } else {  // F4_EPI_RESID: out = bf16(r' + acc * alpha)
-                    const uint4 *rr = reinterpret_cast<const uint4 *>(p.resid + (size_t)row * p.ldr + n);
-                    float x[16];
-                    unpack8(rr[0], x);
-                    unpack8(rr[1], x + 8);
-                    uint32_t w[8];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        w[j] = bf16_bits(__fadd_rn(x[2 * j], v[2 * j])) |
-                               (bf16_bits(__fadd_rn(x[2 * j + 1], v[2 * j + 1])) << 16);
-                    uint4 *o = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) + (size_t)row * p.ldo + n);
-                    o[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                    o[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                        v[j] = __fmul_rn(__uint_as_float(raw[j]), p.alpha);
+                    if (valid)
+                        epi_chunk<EPI>(p, row, n0 + c * 16, v, amax);
                 }
             }
-            if constexpr (EPI == F4_EPI_AMAX) {
-                amax = warp_max(amax);
-                if (lane == 0)
-                    atomicMax(p.amax, __float_as_uint(amax));
+        } else {
+            // Split-K: every split stores its fp32 partial tile (valid rows);
+            // the last split to arrive sums the partials in split order and
+            // runs the epilogue, then re-arms the tile's counter.
+            const int tile = blockIdx.y * gridDim.x + blockIdx.x;
+            float *ws_t = p.ws + (size_t)tile * p.splits * (F4_BM * F4_BN);
+            if (ok) {
+                tc_fence_after();
+#pragma unroll 1
+                for (int c = 0; c < F4_BN / 16; ++c) {
+                    uint32_t raw[16];
+                    __syncwarp();
+                    tmem_ld_x16(tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(c * 16), raw);
+                    tmem_ld_wait();
+                    if (valid) {
+                        float4 *o = reinterpret_cast<float4 *>(ws_t + (size_t)z * (F4_BM * F4_BN) + r * F4_BN + c * 16);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            o[j] = make_float4(__uint_as_float(raw[4 * j]), __uint_as_float(raw[4 * j + 1]),
+                                               __uint_as_float(raw[4 * j + 2]), __uint_as_float(raw[4 * j + 3]));
+                    }
+                }
             }
+            __threadfence();
+            named_bar_sync(1, 128);
+            if (threadIdx.x == 0)
+                s_last = atomicAdd(p.counters + tile, 1) == p.splits - 1 ? 1 : 0;
+            named_bar_sync(1, 128);
+            if (s_last) {
+                __threadfence();
+                if (valid) {
+#pragma unroll 1
+                    for (int c = 0; c < F4_BN / 16; ++c) {
+                        float v[16];
+                        const float4 *src = reinterpret_cast<const float4 *>(ws_t + r * F4_BN + c * 16);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const float4 t = __ldcg(src + j);
+                            v[4 * j] = t.x; v[4 * j + 1] = t.y; v[4 * j + 2] = t.z; v[4 * j + 3] = t.w;
+                        }
+                        for (int k = 1; k < p.splits; ++k) {
+                            const float4 *sk = src + (size_t)k * (F4_BM * F4_BN / 4);
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const float4 t = __ldcg(sk + j);
+                                v[4 * j] = __fadd_rn(v[4 * j], t.x);
+                                v[4 * j + 1] = __fadd_rn(v[4 * j + 1], t.y);
+                                v[4 * j + 2] = __fadd_rn(v[4 * j + 2], t.z);
+                                v[4 * j + 3] = __fadd_rn(v[4 * j + 3], t.w);
+                            }
+                        }
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            v[j] = __fmul_rn(v[j], p.alpha);
+                        epi_chunk<EPI>(p, row, n0 + c * 16, v, amax);
+                    }
+                }
+                if (threadIdx.x == 0)
+                    p.counters[tile] = 0;
+            }
+        }
+        if constexpr (EPI == F4_EPI_AMAX) {
+            amax = warp_max(amax);
+            if (lane == 0)
+                atomicMax(p.amax, __float_as_uint(amax));
         }
     }
     tc_fence_before();
@@ -573,22 +680,33 @@ cudaError_t launch_f4_quant_w(const void *w, int rows, int K, const float *col, 
 cudaError_t launch_f4_norm_quant(const void *r, const void *h, const void *w, const float *awq_inv, int M, int d,
                                  float eps, float sc, float inv6, void *rprime, uint8_t *q, uint8_t *sf,
                                  unsigned *amax_word, bool measure, cudaStream_t s) {
-    const dim3 grid((M + 7) / 8);
-    if (measure)
-        k_f4_norm_quant<true><<<grid, 256, 0, s>>>(static_cast<const uint16_t *>(r), static_cast<const uint16_t *>(h),
-                                                   static_cast<const uint16_t *>(w), awq_inv, M, d, eps, sc, inv6,
-                                                   static_cast<uint16_t *>(rprime), q, sf, amax_word);
-    else
-        k_f4_norm_quant<false><<<grid, 256, 0, s>>>(static_cast<const uint16_t *>(r), static_cast<const uint16_t *>(h),
-                                                    static_cast<const uint16_t *>(w), awq_inv, M, d, eps, sc, inv6,
-                                                    static_cast<uint16_t *>(rprime), q, sf, amax_word);
+    // warps per row: enough threads for the row's blocks of 16 (at most 8 warps)
+    const int ng = d / 16;
+    const int wpr = ng >= 256 ? 8 : ng >= 128 ? 4 : ng >= 64 ? 2 : 1;
+    const dim3 grid((M + 8 / wpr - 1) / (8 / wpr));
+    const uint16_t *rr = static_cast<const uint16_t *>(r), *hh = static_cast<const uint16_t *>(h);
+    const uint16_t *ww = static_cast<const uint16_t *>(w);
+    uint16_t *rp = static_cast<uint16_t *>(rprime);
+#define FRT_F4_NORM(MEAS, W) \
+    k_f4_norm_quant<MEAS, W><<<grid, 256, 0, s>>>(rr, hh, ww, awq_inv, M, d, eps, sc, inv6, rp, q, sf, amax_word)
+    switch (wpr * 2 + (measure ? 1 : 0)) {
+    case 2: FRT_F4_NORM(false, 1); break;
+    case 3: FRT_F4_NORM(true, 1); break;
+    case 4: FRT_F4_NORM(false, 2); break;
+    case 5: FRT_F4_NORM(true, 2); break;
+    case 8: FRT_F4_NORM(false, 4); break;
+    case 9: FRT_F4_NORM(true, 4); break;
+    case 16: FRT_F4_NORM(false, 8); break;
+    default: FRT_F4_NORM(true, 8); break;
+    }
+#undef FRT_F4_NORM
     return cudaGetLastError();
 }
 
 cudaError_t launch_f4_geglu(const uint8_t *gq, const uint8_t *gs, float s_g, const uint8_t *uq, const uint8_t *us,
                             float s_u, int act, int M, int ff, float s_h, float inv6, uint8_t *hq, uint8_t *hsf,
                             unsigned *amax_word, bool measure, cudaStream_t s) {
-    const unsigned grid = blocks_for((size_t)M * (ff / 16), 256);
+    const unsigned grid = blocks_for((size_t)M * ff, 256);
     if (measure)
         k_f4_geglu<true><<<grid, 256, 0, s>>>(gq, gs, s_g, uq, us, s_u, act, M, ff, s_h, inv6, hq, hsf, amax_word);
     else
@@ -598,7 +716,7 @@ cudaError_t launch_f4_geglu(const uint8_t *gq, const uint8_t *gs, float s_g, con
 
 cudaError_t launch_f4_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const F4GemmParams &p, int n_cols,
                            cudaStream_t s) {
-    const dim3 grid(n_cols / F4_BN, (p.M + F4_BM - 1) / F4_BM);
+    const dim3 grid(n_cols / F4_BN, (p.M + F4_BM - 1) / F4_BM, p.splits);
     cudaError_t e = cudaSuccess;
     switch (p.epi) {
 #define FRT_F4_CASE(E)                                                                                    \

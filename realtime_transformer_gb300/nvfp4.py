@@ -97,10 +97,15 @@ class FP4Plan:
         N.frt_fp4_device_status(self.handle, _stream(stream))
 
 
-def nvfp4_gemm(a_codes, a_sf, b_codes, b_sf, M, N_, K, alpha=1.0, stream=None):
-    """Diagnostic block-scaled GEMM: fp32 [M, N] = alpha * A . B^T over NVFP4 operands."""
-    out = torch.empty((M, N_), dtype=torch.float32, device=a_codes.device)
-    err = torch.zeros(1, dtype=torch.int32, device=a_codes.device)
+def nvfp4_gemm(a_codes, a_sf, b_codes, b_sf, M, N_, K, alpha=1.0, splits=1, stream=None):
+    """Diagnostic block-scaled GEMM: fp32 [M, N] = alpha * A . B^T over NVFP4
+    operands, split-K into `splits` partials summed in split order."""
+    dev = a_codes.device
+    out = torch.empty((M, N_), dtype=torch.float32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    tiles = (N_ // 128) * ((M + 127) // 128)
+    ws = torch.empty(tiles * splits * 128 * 128 if splits > 1 else 4, dtype=torch.float32, device=dev)
+    counters = torch.zeros(max(tiles, 1), dtype=torch.int32, device=dev)
     N.frt_nvfp4_gemm(_ptr(a_codes), _ptr(a_sf), _ptr(b_codes), _ptr(b_sf), M, N_, K, float(alpha), out.data_ptr(),
-                     err.data_ptr(), _stream(stream))
-    return out, err
+                     int(splits), ws.data_ptr(), counters.data_ptr(), err.data_ptr(), _stream(stream))
+    return out, err, counters

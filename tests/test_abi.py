@@ -96,4 +96,5 @@ def test_nvfp4_entry_points_check_arguments_before_any_cuda_call(native):
     assert L.frt_fp4_device_status(None, None) == 1
     assert L.frt_fp4_plan_destroy(None) == 0
     # the diagnostic GEMM rejects shapes its tiles do not cover
-    assert L.frt_nvfp4_gemm(None, None, None, None, 8, 128, 256, ctypes.c_float(1.0), None, None, None) == 1
+    assert L.frt_nvfp4_gemm(None, None, None, None, 8, 128, 256, ctypes.c_float(1.0), None, 1, None, None, None,
+                            None) == 1

@@ -117,8 +117,9 @@ def dev(a):
 
 # ------------------------------------------------------------------- GEMM --
 
-@pytest.mark.parametrize("M,N,K", [(1, 128, 256), (50, 256, 512), (128, 128, 2048), (300, 384, 1024)])
-def test_block_scaled_gemm_matches_the_exact_sum(M, N, K):
+@pytest.mark.parametrize("M,N,K,S", [(1, 128, 256, 1), (50, 256, 512, 1), (128, 128, 2048, 1), (300, 384, 1024, 1),
+                                     (1, 256, 2048, 3), (50, 128, 4096, 8), (300, 256, 1024, 2)])
+def test_block_scaled_gemm_matches_the_exact_sum(M, N, K, S):
     from realtime_transformer_gb300.nvfp4 import nvfp4_gemm
     rng = np.random.default_rng(M * 7 + N + K)
     qa = rng.integers(0, 16, (M, K)).astype(np.uint8)
@@ -126,9 +127,11 @@ def test_block_scaled_gemm_matches_the_exact_sum(M, N, K):
     sa = rng.integers(0x28, 0x48, (M, K // 16)).astype(np.uint8)
     sb = rng.integers(0x28, 0x48, (N, K // 16)).astype(np.uint8)
     alpha = 0.375
-    out, err = nvfp4_gemm(dev(pack(qa)), dev(sf_to_tmem(sa)), dev(pack(qb)), dev(sf_to_tmem(sb)), M, N, K, alpha)
+    out, err, counters = nvfp4_gemm(dev(pack(qa)), dev(sf_to_tmem(sa)), dev(pack(qb)), dev(sf_to_tmem(sb)), M, N, K,
+                                    alpha, splits=S)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
+    assert int(counters.abs().sum().item()) == 0, "split-K counters must be re-armed"
     ref = (oracle.nvfp4_gemm(qa, sa, qb, sb).astype(np.float64) * alpha)
     got = out.cpu().numpy().astype(np.float64)
     rms = np.sqrt((ref ** 2).mean())
@@ -148,7 +151,8 @@ def test_gemm_scale_placement_one_block_at_a_time():
     for (m, g) in [(0, 0), (37, 5), (99, 31), (129, 17)]:
         sa = np.zeros((M, K // 16), np.uint8)
         sa[m, g] = 0x38
-        out, err = nvfp4_gemm(dev(pack(qa)), dev(sf_to_tmem(sa)), dev(pack(qb)), dev(sf_to_tmem(sb)), M, N, K)
+        out, err, _ = nvfp4_gemm(dev(pack(qa)), dev(sf_to_tmem(sa)), dev(pack(qb)), dev(sf_to_tmem(sb)), M, N, K,
+                                 splits=2)
         torch.cuda.synchronize()
         got = out.cpu().numpy()
         ref = oracle.nvfp4_gemm(qa, sa, qb, sb)
@@ -158,7 +162,8 @@ def test_gemm_scale_placement_one_block_at_a_time():
     for (n, g) in [(0, 3), (64, 12), (127, 30)]:
         sb = np.zeros((N, K // 16), np.uint8)
         sb[n, g] = 0x38
-        out, err = nvfp4_gemm(dev(pack(qa)), dev(sf_to_tmem(sa)), dev(pack(qb)), dev(sf_to_tmem(sb)), M, N, K)
+        out, err, _ = nvfp4_gemm(dev(pack(qa)), dev(sf_to_tmem(sa)), dev(pack(qb)), dev(sf_to_tmem(sb)), M, N, K,
+                                 splits=2)
         torch.cuda.synchronize()
         got = out.cpu().numpy()
         assert np.array_equal(got, oracle.nvfp4_gemm(qa, sa, qb, sb)), (n, g)
