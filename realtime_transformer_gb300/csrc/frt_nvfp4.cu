@@ -113,14 +113,14 @@ size_t wsf_bytes(size_t rows, size_t K) { return rows * K / 16; }
 constexpr int F4_MAX_TILES = 4096;
 
 // Split-K factor of a GEMM with `tiles` output tiles and K / 256 stages:
-// enough splits to put a CTA on most SMs, each split at least two stages
+// enough splits to put a CTA on most SMs, each split at least four stages
 // long (one CTA per SM: the kernel's shared memory allows no more).
 int f4_splits(int tiles, int KB, int num_sms) {
     if (tiles > F4_MAX_TILES)
         return 1;
     int s = num_sms / tiles;
-    if (s > KB / 2)
-        s = KB / 2;
+    if (s > KB / 4)
+        s = KB / 4;
     return s < 1 ? 1 : s;
 }
 

@@ -294,6 +294,48 @@ __device__ __forceinline__ uint32_t e2m1_one(float x) {
 // a block of 16 on 16 lanes: its amax by shuffles, the codes of lane pairs
 // combined into bytes.  The element count M ff is a multiple of 16, so a
 // half-warp is a whole block or wholly past the end.
+// One thread per block of 16 (many blocks: enough threads to fill the GPU).
+template <bool MEASURE>
+__global__ void k_f4_geglu_blk(const uint8_t *__restrict__ gq, const uint8_t *__restrict__ gs, float s_g,
+                               const uint8_t *__restrict__ uq, const uint8_t *__restrict__ us, float s_u, int act,
+                               int M, int ff, float s_h, float inv6, uint8_t *__restrict__ hq,
+                               uint8_t *__restrict__ hsf, unsigned *amax_word) {
+    const int gpr = ff / 16;
+    const size_t n = (size_t)M * gpr;
+    float amax = 0.0f;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        const int m = (int)(i / gpr), g = (int)(i % gpr);
+        const uint2 gc = reinterpret_cast<const uint2 *>(gq)[i];
+        const uint2 uc = reinterpret_cast<const uint2 *>(uq)[i];
+        const float gb = e4m3_dec(gs[i]), ub = e4m3_dec(us[i]);
+        float a[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const uint32_t gw = j < 8 ? gc.x : gc.y, uw = j < 8 ? uc.x : uc.y;
+            const int sh = 4 * (j & 7);
+            const float gv = __fmul_rn(__fmul_rn(e2m1_dec((gw >> sh) & 15u), gb), s_g);
+            const float uv = __fmul_rn(__fmul_rn(e2m1_dec((uw >> sh) & 15u), ub), s_u);
+            a[j] = __fmul_rn(act_f32(act, gv), uv);
+        }
+        if (MEASURE) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                amax = fmaxf(amax, fabsf(a[j]));
+        } else {
+            uint2 c;
+            const uint32_t b = quant_block16(a, s_h, inv6, c);
+            reinterpret_cast<uint2 *>(hq)[i] = c;
+            hsf[sf_offset(m, g, ff)] = (uint8_t)b;
+        }
+    }
+    if (MEASURE) {
+        amax = warp_max(amax);
+        if ((threadIdx.x & 31) == 0)
+            atomicMax(amax_word, __float_as_uint(amax));
+    }
+}
+
+// One thread per element (few blocks: sixteen times the parallelism).
 template <bool MEASURE>
 __global__ void k_f4_geglu(const uint8_t *__restrict__ gq, const uint8_t *__restrict__ gs, float s_g,
                            const uint8_t *__restrict__ uq, const uint8_t *__restrict__ us, float s_u, int act, int M,
@@ -593,32 +635,46 @@ __global__ void __launch_bounds__(192, 1)
             named_bar_sync(1, 128);
             if (s_last) {
                 __threadfence();
-                if (valid) {
+                // (row, 16-column chunk) items over the 128 threads, the
+                // partials of four splits in flight at a time, summed in order
+                const int rows = min(F4_BM, p.M - m0);
 #pragma unroll 1
-                    for (int c = 0; c < F4_BN / 16; ++c) {
-                        float v[16];
-                        const float4 *src = reinterpret_cast<const float4 *>(ws_t + r * F4_BN + c * 16);
+                for (int it = threadIdx.x; it < rows * (F4_BN / 16); it += 128) {
+                    const int rr = it / (F4_BN / 16), c = it % (F4_BN / 16);
+                    const float4 *src = reinterpret_cast<const float4 *>(ws_t + rr * F4_BN + c * 16);
+                    float v[16];
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const float4 t = __ldcg(src + j);
-                            v[4 * j] = t.x; v[4 * j + 1] = t.y; v[4 * j + 2] = t.z; v[4 * j + 3] = t.w;
-                        }
-                        for (int k = 1; k < p.splits; ++k) {
-                            const float4 *sk = src + (size_t)k * (F4_BM * F4_BN / 4);
+                    for (int j = 0; j < 4; ++j) {
+                        const float4 t = __ldcg(src + j);
+                        v[4 * j] = t.x; v[4 * j + 1] = t.y; v[4 * j + 2] = t.z; v[4 * j + 3] = t.w;
+                    }
+#pragma unroll 1
+                    for (int k0 = 1; k0 < p.splits; k0 += 4) {
+                        float4 t[4][4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                t[k][j] = k0 + k < p.splits
+                                              ? __ldcg(src + (size_t)(k0 + k) * (F4_BM * F4_BN / 4) + j)
+                                              : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            if (k0 + k >= p.splits)
+                                break;
 #pragma unroll
                             for (int j = 0; j < 4; ++j) {
-                                const float4 t = __ldcg(sk + j);
-                                v[4 * j] = __fadd_rn(v[4 * j], t.x);
-                                v[4 * j + 1] = __fadd_rn(v[4 * j + 1], t.y);
-                                v[4 * j + 2] = __fadd_rn(v[4 * j + 2], t.z);
-                                v[4 * j + 3] = __fadd_rn(v[4 * j + 3], t.w);
+                                v[4 * j] = __fadd_rn(v[4 * j], t[k][j].x);
+                                v[4 * j + 1] = __fadd_rn(v[4 * j + 1], t[k][j].y);
+                                v[4 * j + 2] = __fadd_rn(v[4 * j + 2], t[k][j].z);
+                                v[4 * j + 3] = __fadd_rn(v[4 * j + 3], t[k][j].w);
                             }
                         }
-#pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            v[j] = __fmul_rn(v[j], p.alpha);
-                        epi_chunk<EPI>(p, row, n0 + c * 16, v, amax);
                     }
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        v[j] = __fmul_rn(v[j], p.alpha);
+                    epi_chunk<EPI>(p, m0 + rr, n0 + c * 16, v, amax);
                 }
                 if (threadIdx.x == 0)
                     p.counters[tile] = 0;
@@ -706,11 +762,23 @@ cudaError_t launch_f4_norm_quant(const void *r, const void *h, const void *w, co
 cudaError_t launch_f4_geglu(const uint8_t *gq, const uint8_t *gs, float s_g, const uint8_t *uq, const uint8_t *us,
                             float s_u, int act, int M, int ff, float s_h, float inv6, uint8_t *hq, uint8_t *hsf,
                             unsigned *amax_word, bool measure, cudaStream_t s) {
-    const unsigned grid = blocks_for((size_t)M * ff, 256);
-    if (measure)
-        k_f4_geglu<true><<<grid, 256, 0, s>>>(gq, gs, s_g, uq, us, s_u, act, M, ff, s_h, inv6, hq, hsf, amax_word);
-    else
-        k_f4_geglu<false><<<grid, 256, 0, s>>>(gq, gs, s_g, uq, us, s_u, act, M, ff, s_h, inv6, hq, hsf, amax_word);
+    const size_t nblk = (size_t)M * (ff / 16);
+    if (nblk >= 65536) {
+        const unsigned grid = blocks_for(nblk, 256);
+        if (measure)
+            k_f4_geglu_blk<true><<<grid, 256, 0, s>>>(gq, gs, s_g, uq, us, s_u, act, M, ff, s_h, inv6, hq, hsf,
+                                                      amax_word);
+        else
+            k_f4_geglu_blk<false><<<grid, 256, 0, s>>>(gq, gs, s_g, uq, us, s_u, act, M, ff, s_h, inv6, hq, hsf,
+                                                       amax_word);
+    } else {
+        const unsigned grid = blocks_for((size_t)M * ff, 256);
+        if (measure)
+            k_f4_geglu<true><<<grid, 256, 0, s>>>(gq, gs, s_g, uq, us, s_u, act, M, ff, s_h, inv6, hq, hsf, amax_word);
+        else
+            k_f4_geglu<false><<<grid, 256, 0, s>>>(gq, gs, s_g, uq, us, s_u, act, M, ff, s_h, inv6, hq, hsf,
+                                                   amax_word);
+    }
     return cudaGetLastError();
 }
 
