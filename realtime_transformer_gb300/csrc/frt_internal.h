@@ -162,9 +162,11 @@ struct F4GemmParams {
     int *counters;          // one zeroed arrival counter per output tile (re-armed by the kernel)
 };
 
-size_t f4_gemm_smem();
+// swap_n 0: tiled role (A = token tiles of 128 rows, B = weight tiles);
+// 16 / 32 / 64: weight-streaming role for M <= swap_n tokens (A = the weight
+// tiles, B = the tokens padded to swap_n rows; sfa the weights' scales).
 cudaError_t launch_f4_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const F4GemmParams &p, int n_cols,
-                           cudaStream_t s);
+                           int swap_n, cudaStream_t s);
 cudaError_t launch_f4_amax_w(const void *w, size_t rows, int K, const float *col, unsigned *amax_word,
                              cudaStream_t s);
 cudaError_t launch_f4_quant_w(const void *w, int rows, int K, const float *col, float sc, float inv6, uint8_t *q,

@@ -84,6 +84,7 @@ struct frt_fp4_plan {
     int *counters = nullptr;                // split-K arrival counters, one per tile
     std::vector<float> s_wg, s_wu, s_wd, s_x, s_g, s_u, s_h;
     CUtensorMap tm_wg, tm_wu, tm_wd, tm_xq, tm_hq;
+    CUtensorMap tm_xq_n[3], tm_hq_n[3];     // token operands of the weight-streaming role: boxes of 16 / 32 / 64 rows
     std::vector<char> loaded, has_awq;
     bool scaled = false;
 };
@@ -115,6 +116,11 @@ constexpr int F4_MAX_TILES = 4096;
 // Split-K factor of a GEMM with `tiles` output tiles and K / 256 stages:
 // enough splits to put a CTA on most SMs, each split at least four stages
 // long (one CTA per SM: the kernel's shared memory allows no more).
+// Token tile of the weight-streaming role for M tokens (0: the tiled role).
+constexpr int F4_SWAP_MAX_TOKENS = 64;
+int f4_swap_n(int M) { return M > F4_SWAP_MAX_TOKENS ? 0 : M <= 16 ? 16 : M <= 32 ? 32 : 64; }
+int f4_swap_idx(int n) { return n == 16 ? 0 : n == 32 ? 1 : 2; }
+
 int f4_splits(int tiles, int KB, int num_sms) {
     if (tiles > F4_MAX_TILES)
         return 1;
@@ -191,6 +197,10 @@ FRT_API frt_status frt_fp4_plan_create(int d, int ff, int act, int M_max, int n_
     if (e == cudaSuccess) e = encode_tmap_u8(&P->tm_wd, P->wd, L * D, F / 2, 128);
     if (e == cudaSuccess) e = encode_tmap_u8(&P->tm_xq, P->xq, MA, D / 2, 128);
     if (e == cudaSuccess) e = encode_tmap_u8(&P->tm_hq, P->hq, MA, F / 2, 128);
+    for (int i = 0; i < 3; ++i) {
+        if (e == cudaSuccess) e = encode_tmap_u8(&P->tm_xq_n[i], P->xq, MA, D / 2, 16u << i);
+        if (e == cudaSuccess) e = encode_tmap_u8(&P->tm_hq_n[i], P->hq, MA, F / 2, 16u << i);
+    }
     if (e != cudaSuccess) {
         free_fp4(P);
         return fcuda_fail(e, "frt_fp4_plan_create");
@@ -274,12 +284,14 @@ cudaError_t f4_norm(frt_fp4_plan *P, int l, const void *r, const void *h, int M,
 // F4_EPI_AMAX (into amax[0] / amax[1]).
 cudaError_t f4_gate_up(frt_fp4_plan *P, int l, bool up, int M, int epi, cudaStream_t s) {
     const size_t d = P->d, ff = P->ff;
+    const int sw = f4_swap_n(M);
     F4GemmParams p;
     memset(&p, 0, sizeof p);
-    p.sfa = P->xsf;
-    p.sfb = (up ? P->su : P->sg) + (size_t)l * wsf_bytes(ff, d);
-    p.a_row0 = 0;
-    p.b_row0 = l * P->ff;
+    const uint8_t *wsf = (up ? P->su : P->sg) + (size_t)l * wsf_bytes(ff, d);
+    p.sfa = sw ? wsf : P->xsf;
+    p.sfb = sw ? P->xsf : wsf;
+    p.a_row0 = sw ? l * P->ff : 0;
+    p.b_row0 = sw ? 0 : l * P->ff;
     p.M = M;
     p.K = P->d;
     p.epi = epi;
@@ -292,10 +304,13 @@ cudaError_t f4_gate_up(frt_fp4_plan *P, int l, bool up, int M, int epi, cudaStre
     p.ldsf = P->ff / 16;
     p.amax = P->amax + (up ? 1 : 0);
     p.err = P->err;
-    p.splits = f4_splits((P->ff / 128) * ((M + 127) / 128), P->d / 256, P->num_sms);
+    p.splits = f4_splits((P->ff / 128) * (sw ? 1 : (M + 127) / 128), P->d / 256, P->num_sms);
     p.ws = P->ws;
     p.counters = P->counters;
-    return launch_f4_gemm(P->tm_xq, up ? P->tm_wu : P->tm_wg, p, P->ff, s);
+    const CUtensorMap &w = up ? P->tm_wu : P->tm_wg;
+    if (sw)
+        return launch_f4_gemm(w, P->tm_xq_n[f4_swap_idx(sw)], p, P->ff, sw, s);
+    return launch_f4_gemm(P->tm_xq, w, p, P->ff, 0, s);
 }
 
 // N3: A = NVFP4(act(G) * U) into the A buffers (measure: amax into amax[2]).
@@ -306,12 +321,14 @@ cudaError_t f4_geglu(frt_fp4_plan *P, int l, int M, bool measure, cudaStream_t s
 
 // N4: out = bf16(resid + acc(A, W_d') * alpha).
 cudaError_t f4_down(frt_fp4_plan *P, int l, const void *resid, void *out, int M, cudaStream_t s) {
+    const int sw = f4_swap_n(M);
     F4GemmParams p;
     memset(&p, 0, sizeof p);
-    p.sfa = P->hsf;
-    p.sfb = P->sd + (size_t)l * wsf_bytes(P->d, P->ff);
-    p.a_row0 = 0;
-    p.b_row0 = l * P->d;
+    const uint8_t *wsf = P->sd + (size_t)l * wsf_bytes(P->d, P->ff);
+    p.sfa = sw ? wsf : P->hsf;
+    p.sfb = sw ? P->hsf : wsf;
+    p.a_row0 = sw ? l * P->d : 0;
+    p.b_row0 = sw ? 0 : l * P->d;
     p.M = M;
     p.K = P->ff;
     p.epi = F4_EPI_RESID;
@@ -321,10 +338,12 @@ cudaError_t f4_down(frt_fp4_plan *P, int l, const void *resid, void *out, int M,
     p.resid = static_cast<const uint16_t *>(resid);
     p.ldr = P->d;
     p.err = P->err;
-    p.splits = f4_splits((P->d / 128) * ((M + 127) / 128), P->ff / 256, P->num_sms);
+    p.splits = f4_splits((P->d / 128) * (sw ? 1 : (M + 127) / 128), P->ff / 256, P->num_sms);
     p.ws = P->ws;
     p.counters = P->counters;
-    return launch_f4_gemm(P->tm_hq, P->tm_wd, p, P->d, s);
+    if (sw)
+        return launch_f4_gemm(P->tm_wd, P->tm_hq_n[f4_swap_idx(sw)], p, P->d, sw, s);
+    return launch_f4_gemm(P->tm_hq, P->tm_wd, p, P->d, 0, s);
 }
 
 frt_status f4_layer(frt_fp4_plan *P, int l, const void *r, const void *h, void *out, int M, cudaStream_t s) {
@@ -557,18 +576,20 @@ FRT_API frt_status frt_nvfp4_gemm(const void *a_codes, const void *a_sf, const v
     if (M < 1 || M > 65536 || N < 128 || N % 128 || K < 256 || K % 256)
         return ffail(FRT_ERR_INVALID_ARG, "M=%d N=%d K=%d: need 1 <= M <= 65536, N %% 128 == 0, K %% 256 == 0", M,
                      N, K);
-    const int tiles = (N / 128) * ((M + 127) / 128);
+    const int tiles = (N / 128) * (f4_swap_n(M) ? 1 : (M + 127) / 128);
     if (splits < 1 || splits > K / 256 || (splits > 1 && (!ws || !counters || !al16(ws) || tiles > F4_MAX_TILES)))
         return ffail(FRT_ERR_INVALID_ARG, "splits=%d: need 1 <= splits <= K / 256 and, above 1, ws and counters",
                      splits);
+    // the plan's choice of role: weight-streaming for at most 64 tokens
+    const int sw = f4_swap_n(M);
     CUtensorMap ta, tb;
-    if (encode_tmap_u8(&ta, a_codes, (uint64_t)M, (uint64_t)K / 2, 128) != cudaSuccess ||
+    if (encode_tmap_u8(&ta, a_codes, (uint64_t)M, (uint64_t)K / 2, sw ? (uint32_t)sw : 128u) != cudaSuccess ||
         encode_tmap_u8(&tb, b_codes, (uint64_t)N, (uint64_t)K / 2, 128) != cudaSuccess)
         return ffail(FRT_ERR_CUDA, "cuTensorMapEncodeTiled failed");
     F4GemmParams p;
     memset(&p, 0, sizeof p);
-    p.sfa = static_cast<const uint8_t *>(a_sf);
-    p.sfb = static_cast<const uint8_t *>(b_sf);
+    p.sfa = static_cast<const uint8_t *>(sw ? b_sf : a_sf);
+    p.sfb = static_cast<const uint8_t *>(sw ? a_sf : b_sf);
     p.M = M;
     p.K = K;
     p.epi = F4_EPI_F32;
@@ -579,7 +600,8 @@ FRT_API frt_status frt_nvfp4_gemm(const void *a_codes, const void *a_sf, const v
     p.splits = splits;
     p.ws = ws;
     p.counters = counters;
-    FCK(launch_f4_gemm(ta, tb, p, N, static_cast<cudaStream_t>(stream)));
+    FCK(sw ? launch_f4_gemm(tb, ta, p, N, sw, static_cast<cudaStream_t>(stream))
+           : launch_f4_gemm(ta, tb, p, N, 0, static_cast<cudaStream_t>(stream)));
     return FRT_OK;
 }
 

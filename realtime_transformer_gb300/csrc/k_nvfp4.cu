@@ -40,11 +40,8 @@ constexpr int F4_BM = 128;             // MMA M: output rows of a CTA = TMEM lan
 constexpr int F4_BN = 128;             // MMA N: output columns of a CTA
 constexpr int F4_BKB = 128;            // K bytes per stage (256 elements): one swizzle row
 constexpr int F4_UKB = 32;             // K bytes of one MMA (64 elements)
-constexpr int F4_STAGES = 4;
 constexpr int F4_TILE = F4_BM * F4_BKB;            // bytes of one operand tile per stage
 constexpr int F4_SF_STAGE = 4 * 512;               // scale bytes of one operand per stage
-constexpr int F4_TMEM_COLS = 256;                  // 128 accumulator + 4 stages x (16 + 16) scale columns
-constexpr uint32_t F4_SMEM = 1024 + F4_STAGES * (2 * F4_TILE + 2 * F4_SF_STAGE) + 256;
 
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -456,32 +453,121 @@ __device__ __forceinline__ void epi_chunk(const F4GemmParams &p, int row, int n,
     }
 }
 
+// The epilogue of one feature f over 16 consecutive tokens t.. (weight-
+// streaming role: a thread holds a feature, the lanes of a half-warp the 16
+// features of one block), v = acc * alpha.  Every lane of the warp calls it.
 template <int EPI>
+__device__ __forceinline__ void epi_swap(const F4GemmParams &p, int f, int t, const float *v, float &amax) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const int tok = t + j;
+        const bool tv = tok < p.M;
+        if constexpr (EPI == F4_EPI_F32) {
+            if (tv)
+                static_cast<float *>(p.out)[(size_t)tok * p.ldo + f] = v[j];
+        } else if constexpr (EPI == F4_EPI_AMAX) {
+            if (tv)
+                amax = fmaxf(amax, fabsf(v[j]));
+        } else if constexpr (EPI == F4_EPI_FP4) {
+            float m = tv ? fabsf(v[j]) : 0.0f;
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1)
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            const uint32_t b = (uint32_t)__nv_cvt_float_to_fp8(__fmul_rn(m, p.inv6_out), __NV_SATFINITE, __NV_E4M3);
+            const float den = __fmul_rn(e4m3_dec(b), p.s_out);
+            const float inv = den > 0.0f ? __frcp_rn(den) : 0.0f;
+            const uint32_t c = e2m1_one(__fmul_rn(v[j], inv));
+            const uint32_t hi = __shfl_xor_sync(0xffffffffu, c, 1);
+            if (tv && !(f & 1))
+                static_cast<uint8_t *>(p.out)[(size_t)tok * p.ldo + f / 2] = (uint8_t)(c | (hi << 4));
+            if (tv && !(f & 15))
+                p.out_sf[(size_t)tok * p.ldsf + f / 16] = (uint8_t)b;
+        } else {  // F4_EPI_RESID
+            if (tv) {
+                const float x = __uint_as_float((uint32_t)p.resid[(size_t)tok * p.ldr + f] << 16);
+                static_cast<uint16_t *>(p.out)[(size_t)tok * p.ldo + f] = (uint16_t)bf16_bits(__fadd_rn(x, v[j]));
+            }
+        }
+    }
+}
+
+// One GEMM variant.  Tiled role (SWAP false): 128 token rows x 128 weight
+// rows per CTA.  Weight-streaming role (SWAP true, at most 64 tokens): the
+// 128 weight rows are the MMA's M operand and the tokens its N = BNT
+// columns, so a stage carries 16 KB of weights and BNT x 128 bytes of
+// activations, and more stages fit.
+template <bool SWAP, int BNT>
+struct F4Cfg {
+    static constexpr int NS = SWAP ? (BNT == 16 ? 9 : BNT == 32 ? 8 : 7) : 4;
+    static constexpr int B_TILE = BNT * F4_BKB;
+    static constexpr int TMEM_COLS = SWAP ? 512 : 256;
+    static constexpr uint32_t SMEM = 1024 + NS * (F4_TILE + B_TILE + 2 * F4_SF_STAGE) + 256;
+};
+constexpr int F4_SF_COL = 128;  // first TMEM column of the scale blocks (after the accumulator)
+
+// Sum of the split-K partials of 16 consecutive columns in split order
+// (partials `stride` floats apart), four splits' loads in flight at a time.
+__device__ __forceinline__ void sum_partials(const float *src0, size_t stride, int splits, float *v) {
+    const float4 *src = reinterpret_cast<const float4 *>(src0);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float4 t = __ldcg(src + j);
+        v[4 * j] = t.x; v[4 * j + 1] = t.y; v[4 * j + 2] = t.z; v[4 * j + 3] = t.w;
+    }
+#pragma unroll 1
+    for (int k0 = 1; k0 < splits; k0 += 4) {
+        float4 t[4][4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                t[k][j] = k0 + k < splits ? __ldcg(src + (size_t)(k0 + k) * (stride / 4) + j)
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            if (k0 + k >= splits)
+                break;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                v[4 * j] = __fadd_rn(v[4 * j], t[k][j].x);
+                v[4 * j + 1] = __fadd_rn(v[4 * j + 1], t[k][j].y);
+                v[4 * j + 2] = __fadd_rn(v[4 * j + 2], t[k][j].z);
+                v[4 * j + 3] = __fadd_rn(v[4 * j + 3], t[k][j].w);
+            }
+        }
+    }
+}
+
+template <int EPI, bool SWAP, int BNT>
 __global__ void __launch_bounds__(192, 1)
     k_gemm_nvfp4(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ F4GemmParams p) {
+    using C = F4Cfg<SWAP, BNT>;
+    constexpr int NS = C::NS;
     extern __shared__ uint8_t smem_raw[];
     __shared__ int s_last;  // split-K: this CTA reduces the tile
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *sA = smem;
-    uint8_t *sB = sA + F4_STAGES * F4_TILE;
-    uint8_t *sSF = sB + F4_STAGES * F4_TILE;  // per stage: A scales (2 KB), then B scales (2 KB)
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sSF + F4_STAGES * 2 * F4_SF_STAGE);
+    uint8_t *sB = sA + NS * F4_TILE;
+    uint8_t *sSF = sB + NS * C::B_TILE;  // per stage: A scales (2 KB), then B scales (2 KB)
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sSF + NS * 2 * F4_SF_STAGE);
     uint64_t *full = bars;
-    uint64_t *empty = bars + F4_STAGES;
-    uint64_t *tfull = bars + 2 * F4_STAGES;
+    uint64_t *empty = bars + NS;
+    uint64_t *tfull = bars + 2 * NS;
     uint64_t *drain_bar = tfull + 1;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain_bar + 1);
     volatile int *abort_f = reinterpret_cast<volatile int *>(tmem_holder + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * F4_BN, m0 = blockIdx.y * F4_BM;
+    // the tile: 128 weight rows from f0; tokens from t0 (tiled: 128 of them)
+    const int f0 = blockIdx.x * 128;
+    const int t0 = SWAP ? 0 : blockIdx.y * F4_BM;
     // this CTA's split of the K stages
     const int KB = p.K / 256;
     const int z = blockIdx.z;
     const int kb0 = (int)((long)z * KB / p.splits), kb1 = (int)((long)(z + 1) * KB / p.splits);
     if (threadIdx.x == 0) {
-        for (int s = 0; s < F4_STAGES; ++s) {
+        for (int s = 0; s < NS; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), 1);
         }
@@ -495,7 +581,7 @@ __global__ void __launch_bounds__(192, 1)
         prefetch_tmap(&tmB);
     }
     if (warp == 5) {
-        tmem_alloc(smem_u32(tmem_holder), F4_TMEM_COLS);
+        tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -505,35 +591,36 @@ __global__ void __launch_bounds__(192, 1)
 
     if (warp == 4) {
         if (lane == 0) {
-            // ---- producer
+            // ---- producer: weights first out of L2, activations last
             const uint64_t pol_w = l2_policy_evict_first();
             const uint64_t pol_x = l2_policy_evict_last();
-            const uint8_t *sfa = p.sfa + (size_t)(m0 / F4_BM) * (size_t)(p.K / 64) * 512u;
-            const uint8_t *sfb = p.sfb + (size_t)(n0 / F4_BN) * (size_t)(p.K / 64) * 512u;
+            const int a_row = p.a_row0 + (SWAP ? f0 : t0), b_row = p.b_row0 + (SWAP ? 0 : f0);
+            const uint8_t *sfa = p.sfa + (size_t)((SWAP ? f0 : t0) / 128) * (size_t)(p.K / 64) * 512u;
+            const uint8_t *sfb = p.sfb + (size_t)((SWAP ? 0 : f0) / 128) * (size_t)(p.K / 64) * 512u;
             int stage = 0;
             uint32_t phase = 0, issued = 0, issued_par = 0;
             bool ok = true;
-            for (int kb = kb0; kb < kb1 && ok; ++kb) {
+            for (int kb = kb0; kb < kb1; ++kb) {
                 if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, abort_f, p.err)) {
                     ok = false;
                     break;
                 }
                 const uint32_t fb = smem_u32(&full[stage]);
-                mbar_arrive_expect_tx(fb, 2u * F4_TILE + 2u * F4_SF_STAGE);
+                mbar_arrive_expect_tx(fb, (uint32_t)(F4_TILE + C::B_TILE + 2 * F4_SF_STAGE));
                 issued |= 1u << stage;
                 issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
-                tma_load_2d(smem_u32(sA + stage * F4_TILE), &tmA, fb, kb * F4_BKB, p.a_row0 + m0, pol_x);
-                tma_load_2d(smem_u32(sB + stage * F4_TILE), &tmB, fb, kb * F4_BKB, p.b_row0 + n0, pol_w);
+                tma_load_2d(smem_u32(sA + stage * F4_TILE), &tmA, fb, kb * F4_BKB, a_row, SWAP ? pol_w : pol_x);
+                tma_load_2d(smem_u32(sB + stage * C::B_TILE), &tmB, fb, kb * F4_BKB, b_row, SWAP ? pol_x : pol_w);
                 bulk_load(smem_u32(sSF + stage * 2 * F4_SF_STAGE), sfa + (size_t)kb * F4_SF_STAGE, F4_SF_STAGE, fb);
                 bulk_load(smem_u32(sSF + stage * 2 * F4_SF_STAGE + F4_SF_STAGE), sfb + (size_t)kb * F4_SF_STAGE,
                           F4_SF_STAGE, fb);
-                if (++stage == F4_STAGES) {
+                if (++stage == NS) {
                     stage = 0;
                     phase ^= 1u;
                 }
             }
             if (!ok)
-                for (int s = 0; s < F4_STAGES; ++s)
+                for (int s = 0; s < NS; ++s)
                     if (issued & (1u << s))
                         mbar_wait_for(smem_u32(&full[s]), (issued_par >> s) & 1u, 100000000ull);
         }
@@ -541,7 +628,7 @@ __global__ void __launch_bounds__(192, 1)
     } else if (warp == 5) {
         if (lane == 0) {
             // ---- MMA issuer
-            constexpr uint32_t idesc = idesc_nvf4(F4_BM, F4_BN);
+            constexpr uint32_t idesc = idesc_nvf4(128, BNT);
             int stage = 0;
             uint32_t phase = 0;
             bool issued_any = false, ok = true;
@@ -551,21 +638,21 @@ __global__ void __launch_bounds__(192, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t t_sf = tmem_base + (uint32_t)(F4_BN + stage * 32);
+                const uint32_t t_sf = tmem_base + (uint32_t)(F4_SF_COL + stage * 32);
                 const uint32_t s_sf = smem_u32(sSF + stage * 2 * F4_SF_STAGE);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     tmem_cp_sf(t_sf + 4 * j, smem_desc_sf(s_sf + 512 * j));
                     tmem_cp_sf(t_sf + 16 + 4 * j, smem_desc_sf(s_sf + F4_SF_STAGE + 512 * j));
                 }
-                const uint32_t aA = smem_u32(sA + stage * F4_TILE), aB = smem_u32(sB + stage * F4_TILE);
+                const uint32_t aA = smem_u32(sA + stage * F4_TILE), aB = smem_u32(sB + stage * C::B_TILE);
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
                     mma_nvf4(tmem_base, smem_desc_k128(aA + j * F4_UKB), smem_desc_k128(aB + j * F4_UKB), idesc,
                              t_sf + 4 * j, t_sf + 16 + 4 * j, (kb > kb0 || j > 0) ? 1u : 0u);
                 issued_any = true;
                 mma_commit(smem_u32(&empty[stage]));
-                if (++stage == F4_STAGES) {
+                if (++stage == NS) {
                     stage = 0;
                     phase ^= 1u;
                 }
@@ -579,20 +666,21 @@ __global__ void __launch_bounds__(192, 1)
         }
         __syncwarp();
     } else {
-        // ---- epilogue: thread = TMEM lane = output row m0 + 32 warp + lane
+        // ---- epilogue: thread = TMEM lane r.  Tiled: token row t0 + r over
+        // 128 feature columns; weight-streaming: feature f0 + r over BNT tokens.
         int ok = 0;
         if (lane == 0)
             ok = mbar_wait(smem_u32(tfull), 0, abort_f, p.err) ? 1 : 0;
         ok = __shfl_sync(0xffffffffu, ok, 0);
         const int r = warp * 32 + lane;
-        const int row = m0 + r;
-        const bool valid = row < p.M;
+        constexpr int NCH = SWAP ? BNT / 16 : F4_BN / 16;  // 16-column chunks of the accumulator
+        constexpr int ROWLEN = SWAP ? BNT : F4_BN;
         float amax = 0.0f;
         if (p.splits == 1) {
             if (ok) {
                 tc_fence_after();
 #pragma unroll 1
-                for (int c = 0; c < F4_BN / 16; ++c) {
+                for (int c = 0; c < NCH; ++c) {
                     uint32_t raw[16];
                     __syncwarp();
                     tmem_ld_x16(tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(c * 16), raw);
@@ -601,26 +689,30 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
                         v[j] = __fmul_rn(__uint_as_float(raw[j]), p.alpha);
-                    if (valid)
-                        epi_chunk<EPI>(p, row, n0 + c * 16, v, amax);
+                    if constexpr (SWAP)
+                        epi_swap<EPI>(p, f0 + r, c * 16, v, amax);
+                    else if (t0 + r < p.M)
+                        epi_chunk<EPI>(p, t0 + r, f0 + c * 16, v, amax);
                 }
             }
         } else {
-            // Split-K: every split stores its fp32 partial tile (valid rows);
-            // the last split to arrive sums the partials in split order and
-            // runs the epilogue, then re-arms the tile's counter.
+            // Split-K: every split stores its fp32 partial tile; the last
+            // split to arrive sums the partials in split order and runs the
+            // epilogue, then re-arms the tile's counter.
             const int tile = blockIdx.y * gridDim.x + blockIdx.x;
             float *ws_t = p.ws + (size_t)tile * p.splits * (F4_BM * F4_BN);
+            const bool keep = SWAP || t0 + r < p.M;
             if (ok) {
                 tc_fence_after();
 #pragma unroll 1
-                for (int c = 0; c < F4_BN / 16; ++c) {
+                for (int c = 0; c < NCH; ++c) {
                     uint32_t raw[16];
                     __syncwarp();
                     tmem_ld_x16(tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(c * 16), raw);
                     tmem_ld_wait();
-                    if (valid) {
-                        float4 *o = reinterpret_cast<float4 *>(ws_t + (size_t)z * (F4_BM * F4_BN) + r * F4_BN + c * 16);
+                    if (keep) {
+                        float4 *o =
+                            reinterpret_cast<float4 *>(ws_t + (size_t)z * (F4_BM * F4_BN) + r * ROWLEN + c * 16);
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
                             o[j] = make_float4(__uint_as_float(raw[4 * j]), __uint_as_float(raw[4 * j + 1]),
@@ -635,46 +727,30 @@ __global__ void __launch_bounds__(192, 1)
             named_bar_sync(1, 128);
             if (s_last) {
                 __threadfence();
-                // (row, 16-column chunk) items over the 128 threads, the
-                // partials of four splits in flight at a time, summed in order
-                const int rows = min(F4_BM, p.M - m0);
+                if constexpr (SWAP) {
+                    // thread = feature (the FP4 epilogue's blocks span lanes)
 #pragma unroll 1
-                for (int it = threadIdx.x; it < rows * (F4_BN / 16); it += 128) {
-                    const int rr = it / (F4_BN / 16), c = it % (F4_BN / 16);
-                    const float4 *src = reinterpret_cast<const float4 *>(ws_t + rr * F4_BN + c * 16);
-                    float v[16];
+                    for (int c = 0; c < NCH; ++c) {
+                        float v[16];
+                        sum_partials(ws_t + r * ROWLEN + c * 16, (size_t)F4_BM * F4_BN, p.splits, v);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const float4 t = __ldcg(src + j);
-                        v[4 * j] = t.x; v[4 * j + 1] = t.y; v[4 * j + 2] = t.z; v[4 * j + 3] = t.w;
+                        for (int j = 0; j < 16; ++j)
+                            v[j] = __fmul_rn(v[j], p.alpha);
+                        epi_swap<EPI>(p, f0 + r, c * 16, v, amax);
                     }
+                } else {
+                    // (row, 16-column chunk) items over the 128 threads
+                    const int rows = min(F4_BM, p.M - t0);
 #pragma unroll 1
-                    for (int k0 = 1; k0 < p.splits; k0 += 4) {
-                        float4 t[4][4];
+                    for (int it = threadIdx.x; it < rows * NCH; it += 128) {
+                        const int rr = it / NCH, c = it % NCH;
+                        float v[16];
+                        sum_partials(ws_t + rr * ROWLEN + c * 16, (size_t)F4_BM * F4_BN, p.splits, v);
 #pragma unroll
-                        for (int k = 0; k < 4; ++k)
-#pragma unroll
-                            for (int j = 0; j < 4; ++j)
-                                t[k][j] = k0 + k < p.splits
-                                              ? __ldcg(src + (size_t)(k0 + k) * (F4_BM * F4_BN / 4) + j)
-                                              : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            if (k0 + k >= p.splits)
-                                break;
-#pragma unroll
-                            for (int j = 0; j < 4; ++j) {
-                                v[4 * j] = __fadd_rn(v[4 * j], t[k][j].x);
-                                v[4 * j + 1] = __fadd_rn(v[4 * j + 1], t[k][j].y);
-                                v[4 * j + 2] = __fadd_rn(v[4 * j + 2], t[k][j].z);
-                                v[4 * j + 3] = __fadd_rn(v[4 * j + 3], t[k][j].w);
-                            }
-                        }
+                        for (int j = 0; j < 16; ++j)
+                            v[j] = __fmul_rn(v[j], p.alpha);
+                        epi_chunk<EPI>(p, t0 + rr, f0 + c * 16, v, amax);
                     }
-#pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        v[j] = __fmul_rn(v[j], p.alpha);
-                    epi_chunk<EPI>(p, m0 + rr, n0 + c * 16, v, amax);
                 }
                 if (threadIdx.x == 0)
                     p.counters[tile] = 0;
@@ -691,7 +767,7 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_after();
     if (warp == 5) {
         __syncwarp();
-        tmem_dealloc(tmem_base, F4_TMEM_COLS);
+        tmem_dealloc(tmem_base, C::TMEM_COLS);
     }
 }
 
@@ -716,8 +792,6 @@ unsigned blocks_for(size_t n, int threads) {
 }
 
 }  // namespace
-
-size_t f4_gemm_smem() { return F4_SMEM; }
 
 cudaError_t launch_f4_amax_w(const void *w, size_t rows, int K, const float *col, unsigned *amax_word,
                              cudaStream_t s) {
@@ -782,32 +856,49 @@ cudaError_t launch_f4_geglu(const uint8_t *gq, const uint8_t *gs, float s_g, con
     return cudaGetLastError();
 }
 
-cudaError_t launch_f4_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const F4GemmParams &p, int n_cols,
-                           cudaStream_t s) {
-    const dim3 grid(n_cols / F4_BN, (p.M + F4_BM - 1) / F4_BM, p.splits);
-    cudaError_t e = cudaSuccess;
-    switch (p.epi) {
-#define FRT_F4_CASE(E)                                                                                    \
-    case E: {                                                                                             \
-        static bool attr = false;                                                                         \
-        if (!attr) {                                                                                      \
-            e = cudaFuncSetAttribute(k_gemm_nvfp4<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, F4_SMEM); \
-            if (e != cudaSuccess)                                                                         \
-                return e;                                                                                 \
-            attr = true;                                                                                  \
-        }                                                                                                 \
-        k_gemm_nvfp4<E><<<grid, 192, F4_SMEM, s>>>(tmA, tmB, p);                                          \
-        break;                                                                                            \
+namespace {
+
+template <int EPI, bool SWAP, int BNT>
+cudaError_t launch_one(const CUtensorMap &a, const CUtensorMap &b, const F4GemmParams &p, dim3 grid, cudaStream_t s) {
+    using C = F4Cfg<SWAP, BNT>;
+    static bool attr = false;
+    if (!attr) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(k_gemm_nvfp4<EPI, SWAP, BNT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess)
+            return e;
+        attr = true;
     }
-        FRT_F4_CASE(F4_EPI_F32)
-        FRT_F4_CASE(F4_EPI_AMAX)
-        FRT_F4_CASE(F4_EPI_FP4)
-        FRT_F4_CASE(F4_EPI_RESID)
-#undef FRT_F4_CASE
-    default:
-        return cudaErrorInvalidValue;
-    }
+    k_gemm_nvfp4<EPI, SWAP, BNT><<<grid, 192, C::SMEM, s>>>(a, b, p);
     return cudaGetLastError();
+}
+
+template <bool SWAP, int BNT>
+cudaError_t launch_epi(const CUtensorMap &a, const CUtensorMap &b, const F4GemmParams &p, dim3 grid, cudaStream_t s) {
+    switch (p.epi) {
+    case F4_EPI_F32: return launch_one<F4_EPI_F32, SWAP, BNT>(a, b, p, grid, s);
+    case F4_EPI_AMAX: return launch_one<F4_EPI_AMAX, SWAP, BNT>(a, b, p, grid, s);
+    case F4_EPI_FP4: return launch_one<F4_EPI_FP4, SWAP, BNT>(a, b, p, grid, s);
+    case F4_EPI_RESID: return launch_one<F4_EPI_RESID, SWAP, BNT>(a, b, p, grid, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_f4_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const F4GemmParams &p, int n_cols,
+                           int swap_n, cudaStream_t s) {
+    if (swap_n == 0)
+        return launch_epi<false, 128>(tmA, tmB, p, dim3(n_cols / 128, (p.M + F4_BM - 1) / F4_BM, p.splits), s);
+    if (p.M > swap_n)
+        return cudaErrorInvalidValue;
+    const dim3 grid(n_cols / 128, 1, p.splits);
+    switch (swap_n) {
+    case 16: return launch_epi<true, 16>(tmA, tmB, p, grid, s);
+    case 32: return launch_epi<true, 32>(tmA, tmB, p, grid, s);
+    case 64: return launch_epi<true, 64>(tmA, tmB, p, grid, s);
+    default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace frt

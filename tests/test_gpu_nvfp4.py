@@ -139,16 +139,19 @@ def test_block_scaled_gemm_matches_the_exact_sum(M, N, K, S):
     assert cosine(got, ref) > 0.9999999
 
 
-def test_gemm_scale_placement_one_block_at_a_time():
+@pytest.mark.parametrize("M", [130, 40])  # tiled role; weight-streaming role (at most 64 tokens)
+def test_gemm_scale_placement_one_block_at_a_time(M):
     """Only one (row, K-group) scale of A nonzero: the product picks exactly
     that row's 16 elements of K -- pins the TMEM-ready layout end to end."""
     from realtime_transformer_gb300.nvfp4 import nvfp4_gemm
-    M, N, K = 130, 128, 512
+    N, K = 128, 512
     rng = np.random.default_rng(9)
     qa = rng.integers(0, 16, (M, K)).astype(np.uint8)
     qb = rng.integers(0, 16, (N, K)).astype(np.uint8)
     sb = np.full((N, K // 16), 0x38, np.uint8)  # 1.0
     for (m, g) in [(0, 0), (37, 5), (99, 31), (129, 17)]:
+        if m >= M:
+            continue
         sa = np.zeros((M, K // 16), np.uint8)
         sa[m, g] = 0x38
         out, err, _ = nvfp4_gemm(dev(pack(qa)), dev(sf_to_tmem(sa)), dev(pack(qb)), dev(sf_to_tmem(sb)), M, N, K,
