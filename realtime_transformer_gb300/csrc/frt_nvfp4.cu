@@ -9,6 +9,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <vector>
 
@@ -118,7 +119,16 @@ constexpr int F4_MAX_TILES = 4096;
 // long (one CTA per SM: the kernel's shared memory allows no more).
 // Token tile of the weight-streaming role for M tokens (0: the tiled role).
 constexpr int F4_SWAP_MAX_TOKENS = 64;
-int f4_swap_n(int M) { return M > F4_SWAP_MAX_TOKENS ? 0 : M <= 16 ? 16 : M <= 32 ? 32 : 64; }
+int f4_swap_n(int M) {
+    // FRT_F4_SWAP=0 / 1: force the tiled / weight-streaming role (tuning)
+    static const int force = [] {
+        const char *e = getenv("FRT_F4_SWAP");
+        return e ? atoi(e) : -1;
+    }();
+    if (M > F4_SWAP_MAX_TOKENS || force == 0)
+        return 0;
+    return M <= 16 ? 16 : M <= 32 ? 32 : 64;
+}
 int f4_swap_idx(int n) { return n == 16 ? 0 : n == 32 ? 1 : 2; }
 
 int f4_splits(int tiles, int KB, int num_sms) {

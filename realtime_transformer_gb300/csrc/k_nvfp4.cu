@@ -496,14 +496,38 @@ __device__ __forceinline__ void epi_swap(const F4GemmParams &p, int f, int t, co
 // 128 weight rows are the MMA's M operand and the tokens its N = BNT
 // columns, so a stage carries 16 KB of weights and BNT x 128 bytes of
 // activations, and more stages fit.
+// The four MMAs of a stage rotate over NACC accumulators (summed in the
+// epilogue, in order), so that consecutive MMAs do not wait on each other.
 template <bool SWAP, int BNT>
 struct F4Cfg {
     static constexpr int NS = SWAP ? (BNT == 16 ? 9 : BNT == 32 ? 8 : 7) : 4;
+    static constexpr int NACC = SWAP ? 4 : 2;
     static constexpr int B_TILE = BNT * F4_BKB;
-    static constexpr int TMEM_COLS = SWAP ? 512 : 256;
+    static constexpr int SF_COL = NACC * BNT;  // first TMEM column of the scale blocks
+    static constexpr int TMEM_COLS = 512;
     static constexpr uint32_t SMEM = 1024 + NS * (F4_TILE + B_TILE + 2 * F4_SF_STAGE) + 256;
+    static_assert(SF_COL + NS * 32 <= TMEM_COLS, "TMEM budget");
 };
-constexpr int F4_SF_COL = 128;  // first TMEM column of the scale blocks (after the accumulator)
+
+// 16 accumulator columns c*16.. of this warp's lanes: the sum over the NACC
+// accumulators, ((a0 + a1) + a2) + a3.
+template <int NACC, int BNT>
+__device__ __forceinline__ void load_acc(uint32_t tbase, int c, float *v) {
+    uint32_t raw[16];
+    tmem_ld_x16(tbase + (uint32_t)(c * 16), raw);
+    tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+        v[j] = __uint_as_float(raw[j]);
+#pragma unroll
+    for (int a = 1; a < NACC; ++a) {
+        tmem_ld_x16(tbase + (uint32_t)(a * BNT + c * 16), raw);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            v[j] = __fadd_rn(v[j], __uint_as_float(raw[j]));
+    }
+}
 
 // Sum of the split-K partials of 16 consecutive columns in split order
 // (partials `stride` floats apart), four splits' loads in flight at a time.
@@ -638,7 +662,7 @@ __global__ void __launch_bounds__(192, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t t_sf = tmem_base + (uint32_t)(F4_SF_COL + stage * 32);
+                const uint32_t t_sf = tmem_base + (uint32_t)(C::SF_COL + stage * 32);
                 const uint32_t s_sf = smem_u32(sSF + stage * 2 * F4_SF_STAGE);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
@@ -648,8 +672,9 @@ __global__ void __launch_bounds__(192, 1)
                 const uint32_t aA = smem_u32(sA + stage * F4_TILE), aB = smem_u32(sB + stage * C::B_TILE);
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
-                    mma_nvf4(tmem_base, smem_desc_k128(aA + j * F4_UKB), smem_desc_k128(aB + j * F4_UKB), idesc,
-                             t_sf + 4 * j, t_sf + 16 + 4 * j, (kb > kb0 || j > 0) ? 1u : 0u);
+                    mma_nvf4(tmem_base + (uint32_t)((j % C::NACC) * BNT), smem_desc_k128(aA + j * F4_UKB),
+                             smem_desc_k128(aB + j * F4_UKB), idesc, t_sf + 4 * j, t_sf + 16 + 4 * j,
+                             (kb > kb0 || j >= C::NACC) ? 1u : 0u);
                 issued_any = true;
                 mma_commit(smem_u32(&empty[stage]));
                 if (++stage == NS) {
@@ -681,14 +706,12 @@ __global__ void __launch_bounds__(192, 1)
                 tc_fence_after();
 #pragma unroll 1
                 for (int c = 0; c < NCH; ++c) {
-                    uint32_t raw[16];
-                    __syncwarp();
-                    tmem_ld_x16(tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(c * 16), raw);
-                    tmem_ld_wait();
                     float v[16];
+                    __syncwarp();
+                    load_acc<C::NACC, BNT>(tmem_base + ((uint32_t)(warp * 32) << 16), c, v);
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
-                        v[j] = __fmul_rn(__uint_as_float(raw[j]), p.alpha);
+                        v[j] = __fmul_rn(v[j], p.alpha);
                     if constexpr (SWAP)
                         epi_swap<EPI>(p, f0 + r, c * 16, v, amax);
                     else if (t0 + r < p.M)
@@ -706,17 +729,15 @@ __global__ void __launch_bounds__(192, 1)
                 tc_fence_after();
 #pragma unroll 1
                 for (int c = 0; c < NCH; ++c) {
-                    uint32_t raw[16];
+                    float v[16];
                     __syncwarp();
-                    tmem_ld_x16(tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(c * 16), raw);
-                    tmem_ld_wait();
+                    load_acc<C::NACC, BNT>(tmem_base + ((uint32_t)(warp * 32) << 16), c, v);
                     if (keep) {
                         float4 *o =
                             reinterpret_cast<float4 *>(ws_t + (size_t)z * (F4_BM * F4_BN) + r * ROWLEN + c * 16);
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
-                            o[j] = make_float4(__uint_as_float(raw[4 * j]), __uint_as_float(raw[4 * j + 1]),
-                                               __uint_as_float(raw[4 * j + 2]), __uint_as_float(raw[4 * j + 3]));
+                            o[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
                     }
                 }
             }
