@@ -117,7 +117,8 @@ frt_status frt_fp4_debug_weights(frt_fp4_plan_t plan, int layer, int which, void
  * Test/diagnostic: out[m][n] = alpha * sum_k A[m][k] B[n][k] over NVFP4
  * operands (codes [M, K/2] and [N, K/2]; TMEM-ready scales sized for
  * ceil(M/128) and N/128 tiles), fp32 [M, N] out.  N % 128 == 0, K % 256 == 0,
- * 1 <= M <= 65536.  splits: split-K factor (1 <= splits <= K / 256); above 1,
+ * 1 <= M <= 65536.  Runs the role the plan's GEMMs run (the tiled role; the
+ * weight-streaming role for M <= 64 when FRT_F4_SWAP=1).  splits: split-K factor (1 <= splits <= K / 256); above 1,
  * ws (fp32, tiles * splits * 128 * 128, tiles = N/128 * ceil(M/128) <= 4096)
  * and counters (tiles zeroed ints, left zeroed) are device scratch; the
  * partials are summed in split order.  err: a device int the kernel sets on a

@@ -119,13 +119,12 @@ constexpr int F4_MAX_TILES = 4096;
 // long (one CTA per SM: the kernel's shared memory allows no more).
 // Token tile of the weight-streaming role for M tokens (0: the tiled role).
 constexpr int F4_SWAP_MAX_TOKENS = 64;
+// The tiled role measured faster on every shape (the per-stage cost of the
+// block-scaled pipeline does not shrink with the narrower N), so the
+// weight-streaming role runs only when FRT_F4_SWAP=1 (read per launch).
 int f4_swap_n(int M) {
-    // FRT_F4_SWAP=0 / 1: force the tiled / weight-streaming role (tuning)
-    static const int force = [] {
-        const char *e = getenv("FRT_F4_SWAP");
-        return e ? atoi(e) : -1;
-    }();
-    if (M > F4_SWAP_MAX_TOKENS || force == 0)
+    const char *e = getenv("FRT_F4_SWAP");
+    if (M > F4_SWAP_MAX_TOKENS || !e || atoi(e) != 1)
         return 0;
     return M <= 16 ? 16 : M <= 32 ? 32 : 64;
 }

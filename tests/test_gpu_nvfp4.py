@@ -117,10 +117,15 @@ def dev(a):
 
 # ------------------------------------------------------------------- GEMM --
 
+@pytest.mark.parametrize("swap", [False, True], ids=["tiled", "weight_streaming"])
 @pytest.mark.parametrize("M,N,K,S", [(1, 128, 256, 1), (50, 256, 512, 1), (128, 128, 2048, 1), (300, 384, 1024, 1),
                                      (1, 256, 2048, 3), (50, 128, 4096, 8), (300, 256, 1024, 2)])
-def test_block_scaled_gemm_matches_the_exact_sum(M, N, K, S):
+def test_block_scaled_gemm_matches_the_exact_sum(M, N, K, S, swap, monkeypatch):
     from realtime_transformer_gb300.nvfp4 import nvfp4_gemm
+    if swap:
+        if M > 64:
+            pytest.skip("the weight-streaming role takes at most 64 tokens")
+        monkeypatch.setenv("FRT_F4_SWAP", "1")
     rng = np.random.default_rng(M * 7 + N + K)
     qa = rng.integers(0, 16, (M, K)).astype(np.uint8)
     qb = rng.integers(0, 16, (N, K)).astype(np.uint8)
@@ -139,11 +144,12 @@ def test_block_scaled_gemm_matches_the_exact_sum(M, N, K, S):
     assert cosine(got, ref) > 0.9999999
 
 
-@pytest.mark.parametrize("M", [130, 40])  # tiled role; weight-streaming role (at most 64 tokens)
-def test_gemm_scale_placement_one_block_at_a_time(M):
+@pytest.mark.parametrize("M,swap", [(130, "0"), (40, "0"), (40, "1")])  # "1": the weight-streaming role
+def test_gemm_scale_placement_one_block_at_a_time(M, swap, monkeypatch):
     """Only one (row, K-group) scale of A nonzero: the product picks exactly
     that row's 16 elements of K -- pins the TMEM-ready layout end to end."""
     from realtime_transformer_gb300.nvfp4 import nvfp4_gemm
+    monkeypatch.setenv("FRT_F4_SWAP", swap)
     N, K = 128, 512
     rng = np.random.default_rng(9)
     qa = rng.integers(0, 16, (M, K)).astype(np.uint8)
@@ -259,6 +265,24 @@ def test_layer_matches_oracle(layer_case):
     o = plan.forward(r, h)
     torch.cuda.synchronize()
     assert torch.equal(o, tr["out"])
+
+
+def test_weight_streaming_role_matches_the_tiled_role(layer_case, monkeypatch):
+    """At most 64 tokens: the weight-streaming role computes the same layer
+    (same quantised activations except at rounding ties of the sums)."""
+    c = layer_case
+    if c["wl"].M > 64:
+        pytest.skip("the weight-streaming role takes at most 64 tokens")
+    r, h = c["r"].cuda(), c["h"].cuda()
+    a = c["plan"].trace(0, r, h)
+    monkeypatch.setenv("FRT_F4_SWAP", "1")
+    b = c["plan"].trace(0, r, h)
+    torch.cuda.synchronize()
+    assert torch.equal(a["x_codes"], b["x_codes"]) and torch.equal(a["x_sf"], b["x_sf"])
+    for k in ("g_codes", "u_codes", "h_codes"):
+        same = float((a[k] == b[k]).float().mean())
+        assert same > 0.99, (k, same)
+    assert cosine(oracle.bf16_decode(bits(a["out"])), oracle.bf16_decode(bits(b["out"]))) > 0.9999
 
 
 def test_forward_can_be_captured_in_a_cuda_graph(layer_case):
