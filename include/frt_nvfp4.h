@@ -22,7 +22,8 @@
  * awq_scales gives the activation-magnitude rule c_k = mean|y_k|^alpha).
  *
  * Layouts: codes are packed two per byte, element 2i in the low nibble,
- * row-major [rows, K/2]; the block scales of GEMM operands (X, A and the
+ * row-major [rows, K/2] (activations; the plan stores weights in the tiled
+ * order of frt_fp4_debug_weights, one contiguous copy per pipeline stage); the block scales of GEMM operands (X, A and the
  * weights) are stored in the tensor cores' TMEM-ready order: per 128-row tile
  * and 64-element K chunk a 512-byte block, byte (r % 32) * 16 + (r / 32) * 4 + j
  * for row r of the tile and 16-element group j of the chunk (tiles major,
@@ -108,7 +109,12 @@ frt_status frt_fp4_debug_trace(frt_fp4_plan_t plan, int layer, const void *resid
 
 /*
  * Test/diagnostic: copy a layer's quantised weight (which: 0 gate, 1 up,
- * 2 down) -- codes [rows, K/2] and TMEM-ready scales rows * K/16 bytes.
+ * 2 down) -- codes (rows * K/2 bytes) in the plan's tiled layout and
+ * TMEM-ready scales (rows * K/16 bytes).  Tiled layout: per 128-row tile and
+ * 256-element K stage one 16 KB block (tiles major, stages minor) holding the
+ * shared-memory image of a 128-byte-swizzled copy of that box: row r of the
+ * tile at byte r * 128, its 16-byte chunk c at chunk c ^ (r % 8), element 2i
+ * in the low nibble.
  */
 frt_status frt_fp4_debug_weights(frt_fp4_plan_t plan, int layer, int which, void *codes, void *sf,
                                  frt_stream_t stream);

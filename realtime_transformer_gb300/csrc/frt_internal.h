@@ -158,6 +158,7 @@ struct F4GemmParams {
     unsigned *amax;
     int *err;
     int splits;             // split-K factor (grid z); > 1 needs ws and counters
+    const uint8_t *w_tiles; // weights in the tiled layout (one bulk copy per stage) or null (tensor map)
     float *ws;              // fp32 partial tiles: [tiles][splits][128 x 128]
     int *counters;          // one zeroed arrival counter per output tile (re-armed by the kernel)
 };
@@ -170,7 +171,7 @@ cudaError_t launch_f4_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const
 cudaError_t launch_f4_amax_w(const void *w, size_t rows, int K, const float *col, unsigned *amax_word,
                              cudaStream_t s);
 cudaError_t launch_f4_quant_w(const void *w, int rows, int K, const float *col, float sc, float inv6, uint8_t *q,
-                              uint8_t *sf, cudaStream_t s);
+                              uint8_t *sf, bool tiled, cudaStream_t s);
 cudaError_t launch_f4_norm_quant(const void *r, const void *h, const void *w, const float *awq_inv, int M, int d,
                                  float eps, float sc, float inv6, void *rprime, uint8_t *q, uint8_t *sf,
                                  unsigned *amax_word, bool measure, cudaStream_t s);

@@ -263,11 +263,11 @@ FRT_API frt_status frt_fp4_load_weights(frt_fp4_plan_t P, int layer, const void 
     const float su = scale_of(word_to_float(words[1]));
     const float sd = scale_of(word_to_float(words[2]));
     FCK(launch_f4_quant_w(w_gate, (int)ff, (int)d, awq, sg, inv6_of(sg), P->wg + (size_t)layer * ff * d / 2,
-                          P->sg + (size_t)layer * wsf_bytes(ff, d), s));
+                          P->sg + (size_t)layer * wsf_bytes(ff, d), true, s));
     FCK(launch_f4_quant_w(w_up, (int)ff, (int)d, awq, su, inv6_of(su), P->wu + (size_t)layer * ff * d / 2,
-                          P->su + (size_t)layer * wsf_bytes(ff, d), s));
+                          P->su + (size_t)layer * wsf_bytes(ff, d), true, s));
     FCK(launch_f4_quant_w(w_down, (int)d, (int)ff, nullptr, sd, inv6_of(sd), P->wd + (size_t)layer * d * ff / 2,
-                          P->sd + (size_t)layer * wsf_bytes(d, ff), s));
+                          P->sd + (size_t)layer * wsf_bytes(d, ff), true, s));
     FCK(cudaStreamSynchronize(s));
     P->s_wg[layer] = sg;
     P->s_wu[layer] = su;
@@ -316,6 +316,7 @@ cudaError_t f4_gate_up(frt_fp4_plan *P, int l, bool up, int M, int epi, cudaStre
     p.splits = f4_splits((P->ff / 128) * (sw ? 1 : (M + 127) / 128), P->d / 256, P->num_sms);
     p.ws = P->ws;
     p.counters = P->counters;
+    p.w_tiles = (up ? P->wu : P->wg) + (size_t)l * ff * d / 2;
     const CUtensorMap &w = up ? P->tm_wu : P->tm_wg;
     if (sw)
         return launch_f4_gemm(w, P->tm_xq_n[f4_swap_idx(sw)], p, P->ff, sw, s);
@@ -350,6 +351,7 @@ cudaError_t f4_down(frt_fp4_plan *P, int l, const void *resid, void *out, int M,
     p.splits = f4_splits((P->d / 128) * (sw ? 1 : (M + 127) / 128), P->ff / 256, P->num_sms);
     p.ws = P->ws;
     p.counters = P->counters;
+    p.w_tiles = P->wd + (size_t)l * P->d * P->ff / 2;
     if (sw)
         return launch_f4_gemm(P->tm_wd, P->tm_hq_n[f4_swap_idx(sw)], p, P->d, sw, s);
     return launch_f4_gemm(P->tm_hq, P->tm_wd, p, P->d, 0, s);

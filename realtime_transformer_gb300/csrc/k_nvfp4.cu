@@ -151,9 +151,21 @@ __global__ void k_f4_amax_w(const uint4 *__restrict__ w, size_t rows, int K, con
         atomicMax(amax_word, __float_as_uint(m));
 }
 
-// NVFP4 codes [rows, K/2] and TMEM-ready scales of W (times c) with tensor scale s.
+// Byte offset of the 8 codes of (row, 16-element group g) in the tiled weight
+// layout: per 128-row tile and 256-element stage one 16 KB block holding the
+// shared-memory image a 128-byte-swizzled TMA load of that box would write
+// (row r at r * 128, its 16-byte chunk c at chunk c ^ (r % 8)); tiles major,
+// stages minor.
+__device__ __forceinline__ size_t w_tile_offset(int row, int g, int K) {
+    const int r = row & 127, kbyte = g * 8, c = (kbyte & 127) >> 4;
+    return ((size_t)(row >> 7) * (size_t)(K / 256) + (size_t)(kbyte >> 7)) * F4_TILE + (size_t)(r * 128) +
+           (size_t)(((c ^ (r & 7)) << 4) | (kbyte & 15));
+}
+
+// NVFP4 codes and TMEM-ready scales of W (times c) with tensor scale s; codes
+// row-major [rows, K/2] or, with tiled, in the tiled weight layout.
 __global__ void k_f4_quant_w(const uint4 *__restrict__ w, int rows, int K, const float *__restrict__ col, float s,
-                             float inv6, uint2 *__restrict__ q, uint8_t *__restrict__ sf) {
+                             float inv6, uint2 *__restrict__ q, uint8_t *__restrict__ sf, int tiled) {
     const int gpr = K / 16;
     const size_t n = (size_t)rows * gpr;
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
@@ -168,7 +180,10 @@ __global__ void k_f4_quant_w(const uint4 *__restrict__ w, int rows, int K, const
         }
         uint2 c;
         const uint32_t b = quant_block16(f, s, inv6, c);
-        q[i] = c;
+        if (tiled)
+            *reinterpret_cast<uint2 *>(reinterpret_cast<uint8_t *>(q) + w_tile_offset(row, g, K)) = c;
+        else
+            q[i] = c;
         sf[sf_offset(row, g, K)] = (uint8_t)b;
     }
 }
@@ -633,8 +648,20 @@ __global__ void __launch_bounds__(192, 1)
                 mbar_arrive_expect_tx(fb, (uint32_t)(F4_TILE + C::B_TILE + 2 * F4_SF_STAGE));
                 issued |= 1u << stage;
                 issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
-                tma_load_2d(smem_u32(sA + stage * F4_TILE), &tmA, fb, kb * F4_BKB, a_row, SWAP ? pol_w : pol_x);
-                tma_load_2d(smem_u32(sB + stage * C::B_TILE), &tmB, fb, kb * F4_BKB, b_row, SWAP ? pol_x : pol_w);
+                if (p.w_tiles) {
+                    // weights stored in the stage's shared-memory image: one contiguous copy
+                    const uint8_t *wt = p.w_tiles + ((size_t)(f0 / 128) * (size_t)KB + (size_t)kb) * F4_TILE;
+                    if constexpr (SWAP) {
+                        bulk_load(smem_u32(sA + stage * F4_TILE), wt, F4_TILE, fb);
+                        tma_load_2d(smem_u32(sB + stage * C::B_TILE), &tmB, fb, kb * F4_BKB, b_row, pol_x);
+                    } else {
+                        tma_load_2d(smem_u32(sA + stage * F4_TILE), &tmA, fb, kb * F4_BKB, a_row, pol_x);
+                        bulk_load(smem_u32(sB + stage * C::B_TILE), wt, F4_TILE, fb);
+                    }
+                } else {
+                    tma_load_2d(smem_u32(sA + stage * F4_TILE), &tmA, fb, kb * F4_BKB, a_row, SWAP ? pol_w : pol_x);
+                    tma_load_2d(smem_u32(sB + stage * C::B_TILE), &tmB, fb, kb * F4_BKB, b_row, SWAP ? pol_x : pol_w);
+                }
                 bulk_load(smem_u32(sSF + stage * 2 * F4_SF_STAGE), sfa + (size_t)kb * F4_SF_STAGE, F4_SF_STAGE, fb);
                 bulk_load(smem_u32(sSF + stage * 2 * F4_SF_STAGE + F4_SF_STAGE), sfb + (size_t)kb * F4_SF_STAGE,
                           F4_SF_STAGE, fb);
@@ -822,9 +849,9 @@ cudaError_t launch_f4_amax_w(const void *w, size_t rows, int K, const float *col
 }
 
 cudaError_t launch_f4_quant_w(const void *w, int rows, int K, const float *col, float sc, float inv6, uint8_t *q,
-                              uint8_t *sf, cudaStream_t s) {
+                              uint8_t *sf, bool tiled, cudaStream_t s) {
     k_f4_quant_w<<<blocks_for((size_t)rows * (K / 16), 256), 256, 0, s>>>(
-        static_cast<const uint4 *>(w), rows, K, col, sc, inv6, reinterpret_cast<uint2 *>(q), sf);
+        static_cast<const uint4 *>(w), rows, K, col, sc, inv6, reinterpret_cast<uint2 *>(q), sf, tiled ? 1 : 0);
     return cudaGetLastError();
 }
 

@@ -57,6 +57,15 @@ def sf_from_tmem(buf, rows, K):
     return np.asarray(buf, np.uint8)[_sf_index(rows, K)]
 
 
+def untile_weights(buf, rows, K):
+    """The plan's tiled weight layout -> row-major packed codes [rows, K/2]."""
+    t = np.asarray(buf, np.uint8).reshape(rows // 128, K // 256, 128, 8, 16)  # tile, stage, row, chunk, byte
+    r = np.arange(128)[:, None]
+    c = np.arange(8)[None, :]
+    t = t[:, :, r, c ^ (r % 8), :]                                             # undo the chunk swizzle
+    return t.transpose(0, 2, 1, 3, 4).reshape(rows, K // 2)
+
+
 def canon(codes):
     """E2M1 codes with -0 (8) read as +0."""
     c = np.asarray(codes, np.uint8)
@@ -223,7 +232,7 @@ def test_weight_preparation_is_bit_exact(layer_case):
                                    ("down", L.down, wl.d, wl.ff, s_w[2])]:
         codes, sf = plan.weights(0, which)
         assert np.float32(s) == np.float32(ref.s), which
-        assert np.array_equal(canon(unpack(codes.cpu().numpy())), canon(ref.q)), which
+        assert np.array_equal(canon(unpack(untile_weights(codes.cpu().numpy(), rows, K))), canon(ref.q)), which
         assert np.array_equal(sf_from_tmem(sf.cpu().numpy(), rows, K), ref.sb), which
 
 
