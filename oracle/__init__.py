@@ -79,6 +79,7 @@ def lib() -> ctypes.CDLL:
             "orc_calibrate_layer": (i32, [i32, i32, i32, i32, f32, i32, P, P, P, P, P, f32, f32,
                                           ctypes.POINTER(f32), ctypes.POINTER(f32), P]),
             "orc_ref_layer_f32": (i32, [i32, i32, i32, i32, f32, P, P, P, P, P, P, P]),
+            "orc_ref_layer_f32_ex": (i32, [i32, i32, i32, i32, f32, P, P, P, P, P, P, P, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -358,6 +359,39 @@ def calibrate_stack(qlayers, r_batches, h_batches, act: int, eps: float = EPS):
                                      ql.s_gu, ql.s_d, act, eps)
         s_x.append(sx)
         s_h.append(sh)
+    return s_x, s_h
+
+
+def calibrate_stack_unquantized(layers, r_batches, h_batches, act: int, eps: float = EPS):
+    """Step A6, the other reading of "run one forward, record the amax": the
+    scales from the unquantised fp32 forward (BF16 master weights, fp32
+    activations, no E4M3 rounding anywhere), so no layer sees an earlier
+    layer's quantisation.  A flag of the oracle, not the contract (the
+    progressive calibrate_stack is).  Returns (s_x[L], s_h[L])."""
+    cur = [bf16_decode(b) for b in r_batches]
+    hb = [bf16_decode(b) for b in h_batches] if h_batches is not None else None
+    s_x, s_h = [], []
+    for l, lw in enumerate(layers):
+        my, ma = 0.0, 0.0
+        nxt = []
+        for b, x in enumerate(cur):
+            x = np.ascontiguousarray(x, dtype=np.float32)
+            M, d = x.shape
+            ff = _u16(lw["w_gate"]).shape[0]
+            hh = np.ascontiguousarray(hb[b], dtype=np.float32) if (hb is not None and l == 0) else None
+            out = np.empty((M, d), dtype=np.float32)
+            ry = np.empty(M, dtype=np.float32)
+            ra = np.empty(M, dtype=np.float32)
+            rc = lib().orc_ref_layer_f32_ex(M, d, ff, act, eps, _p(x), _p(hh), _p(_u16(lw["w_norm"])),
+                                            _p(_u16(lw["w_gate"])), _p(_u16(lw["w_up"])), _p(_u16(lw["w_down"])),
+                                            _p(out), _p(ry), _p(ra))
+            if rc != 0:
+                raise MemoryError("oracle reference allocation failed")
+            my, ma = max(my, float(ry.max())), max(ma, float(ra.max()))
+            nxt.append(out)
+        s_x.append(scale_from_amax(my))
+        s_h.append(scale_from_amax(ma))
+        cur = nxt
     return s_x, s_h
 
 

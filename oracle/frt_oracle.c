@@ -464,9 +464,23 @@ ORC_API int orc_calibrate_layer(int M, int d, int ff, int act, float eps, int nb
  * g = y W_gate^T, u = y W_up^T, a = act(g) u, out = r' + a W_down^T, all fp32,
  * with the BF16 master weights decoded exactly.  r, h, out are fp32 [M,d].
  */
+ORC_API int orc_ref_layer_f32_ex(int M, int d, int ff, int act, float eps, const float *r, const float *h,
+                                 const uint16_t *w_norm, const uint16_t *w_gate, const uint16_t *w_up,
+                                 const uint16_t *w_down, float *out, float *row_amax_y, float *row_amax_a);
+
 ORC_API int orc_ref_layer_f32(int M, int d, int ff, int act, float eps, const float *r, const float *h,
                               const uint16_t *w_norm, const uint16_t *w_gate, const uint16_t *w_up,
                               const uint16_t *w_down, float *out)
+{
+    return orc_ref_layer_f32_ex(M, d, ff, act, eps, r, h, w_norm, w_gate, w_up, w_down, out, NULL, NULL);
+}
+
+/* The same, also reporting per row the amax of y (the normalised input of the
+ * gate/up GEMM) and of a (the gated activation), when the pointers are not
+ * NULL: the unquantised-forward reading of calibration. */
+ORC_API int orc_ref_layer_f32_ex(int M, int d, int ff, int act, float eps, const float *r, const float *h,
+                                 const uint16_t *w_norm, const uint16_t *w_gate, const uint16_t *w_up,
+                                 const uint16_t *w_down, float *out, float *row_amax_y, float *row_amax_a)
 {
     int64_t Md = (int64_t)M * d;
     float *rp = (float *)malloc(sizeof(float) * Md);
@@ -485,8 +499,11 @@ ORC_API int orc_ref_layer_f32(int M, int d, int ff, int act, float eps, const fl
         }
         float inv = 1.0f / sqrtf(sum / (float)d + eps);
         float *yrow = (float *)malloc(sizeof(float) * d);
-        for (int i = 0; i < d; i++)
+        float my = 0.0f, ma = 0.0f;
+        for (int i = 0; i < d; i++) {
             yrow[i] = (row[i] * inv) * orc_bf16_decode(w_norm[i]);
+            my = fmaxf(my, fabsf(yrow[i]));
+        }
         for (int j = 0; j < ff; j++) {
             const uint16_t *wg = w_gate + (int64_t)j * d;
             const uint16_t *wu = w_up + (int64_t)j * d;
@@ -497,7 +514,12 @@ ORC_API int orc_ref_layer_f32(int M, int d, int ff, int act, float eps, const fl
             }
             float ag = (act == ORC_ACT_SWIGLU) ? orc_silu(g) : orc_gelu_tanh(g);
             a[(int64_t)m * ff + j] = ag * u;
+            ma = fmaxf(ma, fabsf(ag * u));
         }
+        if (row_amax_y)
+            row_amax_y[m] = my;
+        if (row_amax_a)
+            row_amax_a[m] = ma;
         free(yrow);
     }
 #pragma omp parallel for collapse(2) schedule(static)
