@@ -72,6 +72,12 @@ def layer_algorithmic_bytes(wl, M):
     return 3 * wl.d * wl.ff + 2 * 2 * M * wl.d
 
 
+def fp4_layer_bytes_flops(wl, M):
+    """NVFP4 layer: E2M1 weight codes (half a byte each) + their E4M3 block
+    scales (one byte per 16) + BF16 residual in/out; 3 GEMMs of 2 M d ff FLOPs."""
+    return 3 * wl.d * wl.ff // 2 + 3 * wl.d * wl.ff // 16 + 4 * M * wl.d, 6.0 * M * wl.d * wl.ff
+
+
 def source_code_only(text):
     """The code of a CUDA/C++ source without its comments and blank lines
     (string literals in these sources hold no comment markers)."""
@@ -599,8 +605,7 @@ def run_fp4(args, wl, world, rank, local):
     # scales + the residual stream in and out, against HBM or the FP4 tensor
     # peak by intensity
     layer_s = ms_step / 1000.0 / wl.L
-    nbytes = 3 * wl.d * wl.ff // 2 + 3 * wl.d * wl.ff // 16 + 4 * wl.M * wl.d
-    flops = 6.0 * wl.M * wl.d * wl.ff
+    nbytes, flops = fp4_layer_bytes_flops(wl, wl.M)
     fp4_peak = 6.0 * P["bf16_tflops"]
     if flops / nbytes > fp4_peak * 1e12 / (P["hbm_gbs"] * 1e9):
         ach = flops / layer_s / 1e12

@@ -51,3 +51,12 @@ def test_algorithmic_bytes():
     b, f = bench.kernel_bytes_flops(wl, wl.M, 1)
     assert b == 2 * 4096 * 1024 + 50 * 1024 + 50 * 4096 and f == 2 * 50 * 8192 * 1024
     assert bench.layer_algorithmic_bytes(wl, wl.M) == 3 * 1024 * 4096 + 4 * 50 * 1024
+
+
+def test_nvfp4_layer_bytes():
+    wl = synthetic.WORKLOADS["llm_decode"]
+    b, f = bench.fp4_layer_bytes_flops(wl, wl.M)
+    # 5120 x 17408 weights x 3: 0.5 B of code + 1/16 B of scale each; residual in and out in BF16
+    assert b == 3 * 5120 * 17408 * 9 // 16 + 4 * 1 * 5120
+    assert f == 6.0 * 5120 * 17408
+
