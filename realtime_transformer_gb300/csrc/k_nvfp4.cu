@@ -20,11 +20,13 @@
 // block into four TMEM columns of every lane quarter, which is where a
 // kind::mxf4nvf4 MMA with scale_vec::4X reads the scales of its 128 rows.
 //
-// GEMM: one 128 x 128 output tile per CTA, 192 threads -- warp 4 the TMA
-// producer (operand tiles of 128 rows x 256 elements, 128B swizzle, plus the
-// two 2 KB scale blocks of the stage by bulk copy), warp 5 the MMA issuer
-// (per stage eight tcgen05.cp and four MMAs of K = 64), warps 0..3 the
-// epilogue (one TMEM lane = one output row per thread).  Every wait is
+// GEMM: one output tile per CTA (128 x 128 tiled; 128 weight rows x <= 64
+// tokens in the weight-streaming role), 192 threads -- warp 4 the producer
+// (operand tiles of 256 elements along K: activations by 128B-swizzled TMA,
+// weights by one bulk copy of their pre-swizzled tile, plus the two 2 KB
+// scale blocks of the stage), warp 5 the MMA issuer (per stage eight
+// tcgen05.cp and four MMAs of K = 64), warps 0..3 the epilogue (one TMEM lane
+// per thread), with deterministic split-K for few tiles.  Every wait is
 // bounded; on a timeout the CTA drains and exits with the error word set.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
