@@ -36,6 +36,7 @@ import synthetic  # noqa: E402
 
 DEFAULT_CONFIG = "vla_action_expert"
 L2_FLUSH_BYTES = 2 * 129 * 1024 * 1024
+WARM_L2 = False  # --warm-l2: no flush between timed steps (a diagnostic, not the bench line)
 CLOCK_FIELDS = ["timestamp", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
                 "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
                 "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
@@ -70,6 +71,12 @@ def kernel_bytes_flops(wl, M, step):
 def layer_algorithmic_bytes(wl, M):
     """FP8 weights + BF16 residual in/out of one layer (intermediates excluded)."""
     return 3 * wl.d * wl.ff + 2 * 2 * M * wl.d
+
+
+def l2_note():
+    if WARM_L2:
+        return "warm: not flushed between timed steps (diagnostic)"
+    return "flushed between timed steps (%d MiB write)" % (L2_FLUSH_BYTES >> 20)
 
 
 def fp4_layer_bytes_flops(wl, M):
@@ -259,7 +266,7 @@ def run_reference(args, wl, world, rank):
 def config_of(wl):
     return {"workload": wl.name, "M": wl.M, "d": wl.d, "ff": wl.ff, "act": wl.act, "layers": wl.L,
             "weights": "E4M3 per-tensor", "residual": "BF16", "graph": "one CUDA graph per stack",
-            "l2": "flushed between timed steps (%d MiB write)" % (L2_FLUSH_BYTES >> 20), "parallelism": "replicas"}
+            "l2": l2_note(), "parallelism": "replicas"}
 
 
 def run_ours(args, wl, world, rank, local):
@@ -287,13 +294,15 @@ def run_ours(args, wl, world, rank, local):
     def timed(fn, n, warm):
         for _ in range(warm):
             with torch.cuda.stream(stream):
-                flush.zero_()
+                if not WARM_L2:
+                    flush.zero_()
                 fn()
         torch.cuda.synchronize()
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
         with torch.cuda.stream(stream):
             for e0, e1 in evs:
-                flush.zero_()
+                if not WARM_L2:
+                    flush.zero_()
                 e0.record(stream)
                 fn()
                 e1.record(stream)
@@ -396,7 +405,7 @@ def qkv_config_of(wl):
     return {"workload": wl.name + " attention input (QKV)", "M": wl.M, "d": wl.d, "n_q_heads": nq,
             "n_kv_heads": nkv, "head_dim": hd, "rope_base": base, "layers": wl.L, "weights": "E4M3 per-tensor",
             "graph": "the stack's L sublayer forwards in one CUDA graph (same input per layer)",
-            "l2": "flushed between timed steps (%d MiB write)" % (L2_FLUSH_BYTES >> 20), "parallelism": "replicas"}
+            "l2": l2_note(), "parallelism": "replicas"}
 
 
 def run_qkv(args, wl, world, rank, local):
@@ -437,13 +446,15 @@ def run_qkv(args, wl, world, rank, local):
     def timed(fn, n, warm):
         for _ in range(warm):
             with torch.cuda.stream(stream):
-                flush.zero_()
+                if not WARM_L2:
+                    flush.zero_()
                 fn()
         torch.cuda.synchronize()
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
         with torch.cuda.stream(stream):
             for e0, e1 in evs:
-                flush.zero_()
+                if not WARM_L2:
+                    flush.zero_()
                 e0.record(stream)
                 fn()
                 e1.record(stream)
@@ -558,13 +569,15 @@ def run_fp4(args, wl, world, rank, local):
     def timed(fn, n, warm):
         for _ in range(warm):
             with torch.cuda.stream(stream):
-                flush.zero_()
+                if not WARM_L2:
+                    flush.zero_()
                 fn()
         torch.cuda.synchronize()
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
         with torch.cuda.stream(stream):
             for e0, e1 in evs:
-                flush.zero_()
+                if not WARM_L2:
+                    flush.zero_()
                 e0.record(stream)
                 fn()
                 e1.record(stream)
@@ -663,7 +676,11 @@ def main():
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling aid: run a plan of this many layers of the workload's shape "
                          "(the line is then not the workload's bench line)")
+    ap.add_argument("--warm-l2", action="store_true",
+                    help="diagnostic: do not flush L2 between timed steps (the line says so in config.l2)")
     args = ap.parse_args()
+    global WARM_L2
+    WARM_L2 = args.warm_l2
     if args.warmup < 3:
         args.warmup = 3
     wl = synthetic.WORKLOADS[args.config]

@@ -60,3 +60,10 @@ def test_nvfp4_layer_bytes():
     assert b == 3 * 5120 * 17408 * 9 // 16 + 4 * 1 * 5120
     assert f == 6.0 * 5120 * 17408
 
+
+
+def test_l2_note_states_the_flush(monkeypatch):
+    assert bench.l2_note().startswith("flushed")
+    monkeypatch.setattr(bench, "WARM_L2", True)
+    assert bench.l2_note().startswith("warm")
+    assert bench.config_of(synthetic.WORKLOADS["tiny"])["l2"].startswith("warm")
