@@ -206,3 +206,19 @@ def test_nvfp4_stack_tracks_the_fp32_stack():
     out = oracle.stack_forward_nvfp4(Ls, scs, synthetic.bf16_bits(r), synthetic.bf16_bits(h), oracle.ACT_GEGLU_TANH)
     ref = oracle.ref_stack_f32(layers, synthetic.bf16_bits(r), synthetic.bf16_bits(h), oracle.ACT_GEGLU_TANH)
     assert cosine(oracle.bf16_decode(out), ref) > 0.999
+
+
+def test_values_beyond_the_calibrated_range_saturate():
+    """A block whose amax exceeds the tensor scale's range (an activation
+    larger than any seen in calibration) gets the largest E4M3 scale, 448, and
+    its largest elements the largest E2M1 code, 6."""
+    s = 1.0 / 2688.0  # calibrated for amax 1
+    x = np.zeros((1, 32), np.float32)
+    x[0, :16] = np.linspace(-50.0, 50.0, 16)  # 50x the calibrated amax
+    x[0, 16:] = np.linspace(-0.5, 0.5, 16)
+    q, sb = oracle.nvfp4_quantize(x, s)
+    assert oracle.e4m3_decode(sb)[0, 0] == 448.0
+    assert oracle.e2m1_decode(q[0, [0, 15]]).tolist() == [-6.0, 6.0]
+    # the in-range block is unaffected by its neighbour
+    assert oracle.e4m3_decode(sb)[0, 1] < 448.0
+    assert oracle.e2m1_decode(q[0, [16, 31]]).tolist() == [-6.0, 6.0]
