@@ -37,6 +37,8 @@ import synthetic  # noqa: E402
 DEFAULT_CONFIG = "vla_action_expert"
 L2_FLUSH_BYTES = 2 * 129 * 1024 * 1024
 WARM_L2 = False  # --warm-l2: no flush between timed steps (a diagnostic, not the bench line)
+VARIANTS = {"plain": "RMSNorm weight", "fold": "norm weight folded into W_gate/W_up (Pi0)",
+            "ada": "AdaRMSNorm, one modulation row per token (Pi0.5)"}
 CLOCK_FIELDS = ["timestamp", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
                 "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
                 "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
@@ -281,7 +283,11 @@ def run_ours(args, wl, world, rank, local):
     r, h = io[0], io[1]
     plan = FFNPlan(wl.d, wl.ff, wl.act, wl.M, wl.L)
     for l, w in enumerate(weights):
-        plan.load_weights(l, w["w_norm"], w["w_gate"], w["w_up"], w["w_down"])
+        plan.load_weights(l, w["w_norm"], w["w_gate"], w["w_up"], w["w_down"], fold_norm=args.variant == "fold")
+    if args.variant == "ada":
+        # one modulation row per token (the heavier AdaRMSNorm case); kept alive for the graph
+        mods = [synthetic.modulation(wl, l, wl.M, dev) for l in range(wl.L)]
+        plan.set_modulation(mods)
     plan.calibrate([a for a, _ in calib], [b for _, b in calib])
     out = torch.empty_like(r)
     stream = torch.cuda.Stream(device=dev)
@@ -378,17 +384,20 @@ def run_ours(args, wl, world, rank, local):
     step_roof["tflops"] = 6.0 * wl.M * wl.d * wl.ff / layer_s / 1e12
 
     line = {
-        "metric": "FP8 FFN stack tokens/s (graph-replayed, %s)" % wl.name, "value": value, "unit": "tokens/s",
+        "metric": "FP8 FFN stack tokens/s (graph-replayed, %s)" % (
+            wl.name if args.variant == "plain" else "%s, %s" % (wl.name, VARIANTS[args.variant])),
+        "value": value, "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "us_per_layer": 1000.0 * ms_step / wl.L, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "fp8_e4m3 (fp32 accumulate, bf16 residual)", "data": "synthetic", "config": config_of(wl),
+        "dtype": "fp8_e4m3 (fp32 accumulate, bf16 residual)", "data": "synthetic",
+        "config": config_of(wl) if args.variant == "plain" else dict(config_of(wl), variant=VARIANTS[args.variant]),
         "roofline": roof, "step_roofline": step_roof, "kernels_us": kern,
         "e2e": {"value": world * wl.M * args.steps / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": 1000.0 * e2e_s / args.steps},
         "gpu_launches": args.steps * wl.L * len(STEP_NAMES), "clocks": clocks, "wall_s_timed_region": t_wall,
     }
     plan.close()
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.variant == "plain":
         rows = min(wl.M, 64)
         q, s_x, s_h = oracle_setup(wl, weights, calib, rows)
         budget = float(os.environ.get("FRT_CPU_BASELINE_SECONDS", "15"))
@@ -676,6 +685,9 @@ def main():
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling aid: run a plan of this many layers of the workload's shape "
                          "(the line is then not the workload's bench line)")
+    ap.add_argument("--variant", choices=sorted(VARIANTS), default="plain",
+                    help="FFN stack only: plain (the bench line), fold (norm weight folded into the gate/up "
+                         "weights) or ada (AdaRMSNorm modulation)")
     ap.add_argument("--warm-l2", action="store_true",
                     help="diagnostic: do not flush L2 between timed steps (the line says so in config.l2)")
     args = ap.parse_args()
@@ -686,6 +698,8 @@ def main():
     wl = synthetic.WORKLOADS[args.config]
     if args.layers > 0:
         wl = wl.with_(L=args.layers, name=wl.name + "_%dlayers" % args.layers)
+    if args.variant != "plain" and (args.sublayer != "ffn" or args.impl != "ours"):
+        ap.error("--variant applies to the FFN stack of this implementation only")
     world, rank, local = dist_setup(args.gpus)
     if args.impl == "reference":
         line = run_reference(args, wl, world, rank)

@@ -92,6 +92,7 @@ DECODE_CONTEXT = 4096  # the decoded token's position in the LLM decode workload
 # sub-stream identifiers
 _S_WNORM, _S_WGATE, _S_WUP, _S_WDOWN, _S_RES, _S_HID, _S_OUTL = range(7)
 _S_WQ, _S_WK, _S_WV, _S_WNORM_ATTN = range(7, 11)
+_S_MOD = 11
 _S_CALIB_BASE = 1000
 
 
@@ -123,6 +124,16 @@ def layer_weights(wl: Workload, layer: int, device="cpu") -> dict[str, torch.Ten
     w_down = 0.02 * _normal((wl.d, wl.ff), _seed(s, _S_WDOWN, layer), device)
     return {k: v.to(torch.bfloat16) for k, v in
             dict(w_norm=w_norm, w_gate=w_gate, w_up=w_up, w_down=w_down).items()}
+
+
+def modulation(wl: Workload, layer: int, rows: int, device="cpu") -> torch.Tensor:
+    """AdaRMSNorm modulation of one layer, BF16 [rows, 3d] = [scale | shift | gate]
+    (the outputs of the conditioning Dense layers): scale, shift ~ N(0, 0.1),
+    gate ~ 1 + N(0, 0.1); rows = 1 (one conditioning for all tokens) or M."""
+    z = _normal((rows, 3 * wl.d), _seed(wl.seed, _S_MOD, layer), device)
+    z = 0.1 * z
+    z[:, 2 * wl.d:] += 1.0
+    return z.to(torch.bfloat16)
 
 
 def qkv_weights(wl: Workload, layer: int, device="cpu") -> dict[str, torch.Tensor]:

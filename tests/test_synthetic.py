@@ -73,3 +73,15 @@ def test_positions():
     assert list(synthetic.positions(synthetic.WORKLOADS["tiny"])) == list(range(8))
     p = synthetic.positions(synthetic.WORKLOADS["llm_decode"])
     assert p.dtype == np.int32 and list(p) == [synthetic.DECODE_CONTEXT]
+
+
+def test_modulation_is_seeded_and_shaped():
+    wl = synthetic.WORKLOADS["tiny"]
+    a = synthetic.modulation(wl, 0, 8)
+    b = synthetic.modulation(wl, 0, 8)
+    c = synthetic.modulation(wl, 1, 8)
+    assert a.shape == (8, 3 * wl.d) and a.dtype == torch.bfloat16
+    assert torch.equal(a, b) and not torch.equal(a, c)
+    gate = a[:, 2 * wl.d:].float()
+    assert abs(gate.mean().item() - 1.0) < 0.05 and abs(a[:, :wl.d].float().mean().item()) < 0.05
+
