@@ -136,11 +136,10 @@ frt_status get_tmap(frt_ffn_plan *P, int buf, int box_rows, CUtensorMap *out, co
 }
 
 // Every map a launch of this plan can ask for (weights with boxes of a
-// 128/256-row tile or a multicast slice of one, activations with the
+// 128/256-row tile or a CTA pair's half of one, activations with the
 // weight-streaming widths and 128), uploaded in one copy.
 frt_status build_tmaps(frt_ffn_plan *P) {
-    const int combos[][2] = {{B_WGU, 32},   {B_WGU, 64},   {B_WGU, 128}, {B_WGU, 256},
-                             {B_WDOWN, 32}, {B_WDOWN, 64}, {B_WDOWN, 128}, {B_WDOWN, 256},
+    const int combos[][2] = {{B_WGU, 128},  {B_WGU, 256},  {B_WDOWN, 128}, {B_WDOWN, 256},
                              {B_QX, 16},    {B_QX, 32},    {B_QX, 64},    {B_QX, 128},
                              {B_QH, 16},    {B_QH, 32},    {B_QH, 64},    {B_QH, 128}};
     CUtensorMap host[TMAP_SLOTS];
@@ -196,9 +195,8 @@ frt_status setup_gemm(frt_ffn_plan *P, GemmLaunch &g, int site, int l, int M) {
         g.p.q_row0 = 0;
     } else {
         if ((st = get_tmap(P, xbuf, 128, &g.tmP, &g.p.gtm_p)) != FRT_OK) return st;
-        // with weight multicast each CTA loads BN / mcast rows of the tile, on
-        // a CTA pair half of them
-        if ((st = get_tmap(P, wbuf, g.bn / (g.p.pair ? 2 : g.p.mcast), &g.tmQ, &g.p.gtm_q)) != FRT_OK) return st;
+        // on a CTA pair each CTA loads half of the weight tile's rows
+        if ((st = get_tmap(P, wbuf, g.bn / (g.p.pair ? 2 : 1), &g.tmQ, &g.p.gtm_q)) != FRT_OK) return st;
         g.p.p_row0 = 0;
         g.p.q_row0 = l * N;
     }
@@ -950,7 +948,7 @@ FRT_API frt_status frt_fp8_gemm(frt_ffn_plan_t P, const void *A, const void *B, 
         e2 = encode_tmap_u8(&g.tmQ, A, M, K, g.bn);
     } else {
         e1 = encode_tmap_u8(&g.tmP, A, M, K, 128);
-        e2 = encode_tmap_u8(&g.tmQ, B, N, K, g.bn / (g.p.pair ? 2 : g.p.mcast));  // weight slice per CTA
+        e2 = encode_tmap_u8(&g.tmQ, B, N, K, g.bn / (g.p.pair ? 2 : 1));  // weight slice per CTA
     }
     if (e1 != cudaSuccess || e2 != cudaSuccess)
         return fail(FRT_ERR_CUDA, "cuTensorMapEncodeTiled failed");

@@ -44,7 +44,6 @@ struct GemmParams {
     int n_feat;             // valid feature columns
     float *ws;              // split-K partials
     int *counters;          // split-K arrival counters, one per tile, for this launch's split count
-    int mcast;              // tiled role: CTAs per cluster sharing each weight tile by TMA multicast (1 = none)
     int pair;               // tiled role on CTA pairs (cta_group::2): 256-token MMAs, half a weight tile per CTA
     int cluster;            // 1: the splits of a tile are one thread-block cluster and exchange
                             //    partials in distributed shared memory (ws, counters unused)

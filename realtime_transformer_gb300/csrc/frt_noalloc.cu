@@ -86,7 +86,7 @@ FRT_API frt_status frt_fp8_gemm_noalloc(const void *A, const void *B, void *C, i
     if (g.p.splits > 1 && gemm_tiles(g) > MAX_SPLIT_TILES)
         return fail(FRT_ERR_UNSUPPORTED, "this shape has more split-K tiles than the fixed scratch counts");
     if (encode_tmap_u8(&g.tmP, swap ? B : A, swap ? N : M, K, 128) != cudaSuccess ||
-        encode_tmap_u8(&g.tmQ, swap ? A : B, swap ? M : N, K, swap ? g.bn : g.bn / (g.p.pair ? 2 : g.p.mcast)) != cudaSuccess)
+        encode_tmap_u8(&g.tmQ, swap ? A : B, swap ? M : N, K, swap ? g.bn : g.bn / (g.p.pair ? 2 : 1)) != cudaSuccess)
         return fail(FRT_ERR_CUDA, "cuTensorMapEncodeTiled failed");
     float *ws = reinterpret_cast<float *>(ds.base);
     int *counters = reinterpret_cast<int *>(ds.base + NOALLOC_WS_FLOATS * 4);

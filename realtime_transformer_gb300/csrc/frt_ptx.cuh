@@ -195,17 +195,6 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
         }
     }
 }
-// TMA 2-D load multicast to the CTAs of the cluster named in `mask`: the box
-// lands at the same shared-memory offset in each of them and completes its
-// bytes on each one's mbarrier at the offset of `bar`.
-__device__ __forceinline__ void tma_load_2d_mcast(uint32_t dst, const CUtensorMap *m, uint32_t bar, int x, int y,
-                                                  uint16_t mask, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5, %6;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "h"(mask), "l"(policy)
-        : "memory");
-}
 // Bulk copy from this CTA's shared memory to a CTA of the cluster (dst and
 // bar from mapa_shared); the bytes complete on that CTA's mbarrier.  src,
 // dst 16-byte aligned, bytes a multiple of 16.
@@ -252,14 +241,6 @@ __device__ __forceinline__ void mma_f8f6f4(uint32_t d_tmem, uint64_t adesc, uint
         : "memory");
 }
 
-// Same, on the mbarrier at the offset of `bar` in every CTA of the cluster
-// named in `mask`.
-__device__ __forceinline__ void mma_commit_mcast(uint32_t bar, uint16_t mask) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-                     bar),
-                 "h"(mask)
-                 : "memory");
-}
 // Arrive once on `bar` when all tcgen05.mma issued so far by this thread are done.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)

@@ -112,7 +112,7 @@ frt_status setup_qkv_gemm(frt_qkv_plan *P, GemmLaunch &g, int l, int M, bool fus
         e2 = encode_tmap_u8(&g.tmQ, P->qx, P->M_alloc, P->d, g.bn);
     } else {
         e1 = encode_tmap_u8(&g.tmP, P->qx, P->M_alloc, P->d, 128);
-        e2 = encode_tmap_u8(&g.tmQ, wl, P->N, P->d, g.bn / (g.p.pair ? 2 : g.p.mcast));
+        e2 = encode_tmap_u8(&g.tmQ, wl, P->N, P->d, g.bn / (g.p.pair ? 2 : 1));
     }
     if (e1 != cudaSuccess || e2 != cudaSuccess)
         return qfail(FRT_ERR_CUDA, "cuTensorMapEncodeTiled failed");

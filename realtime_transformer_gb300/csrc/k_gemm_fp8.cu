@@ -102,7 +102,7 @@ enum Role : int { ROLE_ANY = 0, ROLE_GATED_TILE = 1, ROLE_CLUSTER_PLAIN = 2, ROL
 // tiles whose operands stay in L2 together.
 __device__ __forceinline__ Unit decode(const GemmParams &p, int u) {
     Unit w;
-    if (p.mcast <= 1 && !p.pair) {
+    if (!p.pair) {
         w.split = u % p.splits;
         w.tile = u / p.splits;
         const int per_group = p.group * p.n_tiles_q;
@@ -112,10 +112,10 @@ __device__ __forceinline__ Unit decode(const GemmParams &p, int u) {
         w.tp = grp * p.group + rem % gsize;
         w.tq = rem / gsize;
     } else {
-        // weight multicast: the C CTAs of a cluster (consecutive units) take
-        // C consecutive P-tiles of the same weight tile and split; the raster
-        // runs over blocks of C P-tiles
-        const int C = p.pair ? 2 : p.mcast;
+        // CTA pair: the two CTAs of a cluster (consecutive units) take two
+        // consecutive P-tiles of the same weight tile and split; the raster
+        // runs over blocks of two P-tiles
+        constexpr int C = 2;
         const int rank = u % C;
         const int v = u / C;
         w.split = v % p.splits;
@@ -189,12 +189,6 @@ __device__ void producer(const CUtensorMap *tmP, const CUtensorMap *tmQ, const G
                 if constexpr (PAIR) {
                     // this CTA's half of the weight tile
                     tma_load_2d_pair(dW, mW, fb, kb * BK, wrow + (int)rank * (BN / 2), pol_w);
-                } else if (!SWAP && p.mcast > 1) {
-                    // this CTA's 1/C of the weight tile, to every CTA of the cluster
-                    const int rows = BN / p.mcast;
-                    const int crank = (int)(blockIdx.x % (unsigned)p.mcast);
-                    tma_load_2d_mcast(dW + (uint32_t)(crank * rows * BK), mW, fb, kb * BK, wrow + crank * rows,
-                                      (uint16_t)((1u << p.mcast) - 1u), pol_w);
                 } else {
                     tma_load_2d(dW, mW, fb, kb * BK, wrow, pol_w);
                 }
@@ -290,12 +284,10 @@ __device__ void mma_issuer(const GemmParams &p, uint8_t *sP, uint8_t *sQ, uint64
                                    (kb > w.kb0 || k > 0) ? 1u : 0u);
                 }
                 issued_any = true;
-                // frees the stage when these MMAs finish (with weight
-                // multicast or a CTA pair: in every CTA that writes into it)
+                // frees the stage when these MMAs finish (on a CTA pair: in
+                // both CTAs, each of which writes into it)
                 if constexpr (PAIR)
                     mma_commit_pair(smem_u32(&empty[stage]), 0x3);
-                else if (!SWAP && p.mcast > 1)
-                    mma_commit_mcast(smem_u32(&empty[stage]), (uint16_t)((1u << p.mcast) - 1u));
                 else
                     mma_commit(smem_u32(&empty[stage]));
                 if (++stage == p.stages) {
@@ -1370,7 +1362,7 @@ __global__ void __launch_bounds__(NTHREADS, SWAP ? 2 : 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
-            mbar_init(smem_u32(&empty[s]), p.mcast > 1 ? (uint32_t)p.mcast : 1u);
+            mbar_init(smem_u32(&empty[s]), 1u);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&tfull[b]), 1);
@@ -1407,10 +1399,9 @@ __global__ void __launch_bounds__(NTHREADS, SWAP ? 2 : 1)
     // its first access to another CTA (the epilogue) or at its end
     if (p.cluster)
         cluster_arrive();
-    if (PAIR || p.mcast > 1) {
-        // weight multicast writes into, and MMA commits arrive on, the other
-        // CTAs' stages and barriers from the first k-block on (a pair's
-        // copies and MMAs likewise)
+    if (PAIR) {
+        // a pair's copies write into, and its MMA commits arrive on, the
+        // other CTA's stages and barriers from the first k-block on
         cluster_arrive();
         cluster_wait();
     }
@@ -1452,7 +1443,7 @@ __global__ void __launch_bounds__(NTHREADS, SWAP ? 2 : 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (PAIR || p.mcast > 1) {
+    if (PAIR) {
         // no CTA leaves while another may still write into it
         cluster_arrive();
         cluster_wait();
@@ -1494,7 +1485,7 @@ cudaError_t run(const GemmLaunch &g, cudaStream_t s, bool pdl) {
     if (e != cudaSuccess)
         return e;
     const bool xbuf = SWAP && g.p.splits == 1 && (g.p.epi == EPI_GATED || g.p.epi == EPI_GATED_AMAX);
-    const unsigned cluster = PAIR ? 2u : g.p.cluster ? (unsigned)g.p.splits : (g.p.mcast > 1 ? (unsigned)g.p.mcast : 1u);
+    const unsigned cluster = PAIR ? 2u : g.p.cluster ? (unsigned)g.p.splits : 1u;
     return launch_ex(k_gemm_fp8<BN, SWAP, PAIR, ROLE>, dim3((unsigned)g.grid), dim3(NTHREADS),
                      std::max(C::smem_bytes(g.p.stages, xbuf), g.min_smem), s, pdl, cluster, g.tmP, g.tmQ, g.p);
 }
@@ -1607,30 +1598,13 @@ void plan_gemm(GemmLaunch &g, bool swap, int m_tok, int n_feat, int K, int num_s
     p.splits = (p.k_blocks + p.kb_per_split - 1) / p.kb_per_split;
     p.total_units = tiles * p.splits;
     g.grid = std::min(p.total_units, num_sms);
-    // tiled role, opt-in (FRT_FFN_MCAST = 2 or 4; needs C | token tiles and
-    // C | grid): clusters of C CTAs on C consecutive token tiles share each
-    // weight tile, every CTA loading 1/C of it and multicasting it.  Off by
-    // default: on GB300 the lockstep it imposes on the C pipelines cost more
-    // than the L2 traffic it saves on the prefill shapes.
-    p.mcast = 1;
-    if (!swap) {
-        const char *e = getenv("FRT_FFN_MCAST");
-        int c = e ? atoi(e) : 1;
-        c = c >= 4 ? 4 : (c >= 2 ? 2 : 1);
-        while (c > 1 && p.n_tiles_p % c)
-            c /= 2;
-        if (c > 1) {
-            p.mcast = c;
-            g.grid = g.grid / c * c;
-        }
-    }
     // tiled role on CTA pairs (FRT_FFN_PAIR=0 disables): 256-token tiles
     // computed by two CTAs with cta_group::2 MMAs, each staging its own 128
     // tokens and half of the 256-row weight tile -- half the weight traffic
     // per CTA and 7 pipeline stages instead of 4; 256-wide tiles on an even
     // number of token tiles
     p.pair = 0;
-    if (!swap && p.mcast == 1 && g.bn == 256 && p.n_tiles_p % 2 == 0 && !(tactic && tactic->no_pairs)) {
+    if (!swap && g.bn == 256 && p.n_tiles_p % 2 == 0 && !(tactic && tactic->no_pairs)) {
         const char *e = getenv("FRT_FFN_PAIR");
         if (!(e && e[0] == '0')) {
             p.pair = 1;

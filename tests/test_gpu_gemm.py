@@ -96,20 +96,6 @@ def test_cluster_and_global_split_k_agree_bitwise(plan, monkeypatch, M, N, K, sp
     assert np.array_equal(c_cluster, c_global)
 
 
-@pytest.mark.parametrize("M,N,K,splits,mcast", [(512, 512, 1024, 1, 2), (1000, 256, 2048, 2, 4), (256, 768, 512, 0, 2)])
-def test_weight_multicast_matches_plain_loads(plan, monkeypatch, M, N, K, splits, mcast):
-    """Tiled role with each weight tile shared across a cluster by TMA
-    multicast gives the same bits as every CTA loading it alone."""
-    rng = np.random.default_rng(M + 3 * N + K)
-    A = rng.integers(0, 0x7E, (M, K)).astype(np.uint8)
-    B = rng.integers(0, 0x7E, (N, K)).astype(np.uint8)
-    monkeypatch.delenv("FRT_FFN_MCAST", raising=False)
-    c_plain = run(plan, A, B, 2, splits)
-    monkeypatch.setenv("FRT_FFN_MCAST", str(mcast))
-    c_mcast = run(plan, A, B, 2, splits)
-    assert np.array_equal(c_plain, c_mcast)
-
-
 @pytest.mark.parametrize("M,N,K,splits", [(256, 256, 512, 1), (512, 512, 1024, 1), (1000, 768, 2048, 1),
                                           (1000, 512, 4096, 2), (256, 768, 2048, 0)])
 def test_cta_pair_matches_single_cta(plan, monkeypatch, M, N, K, splits):
