@@ -277,18 +277,44 @@ const char *frt_ffn_last_error(void);
  *   - The first call on a device looks up that array's device address
  *     (cudaGetSymbolAddress, once per device, with the device current); make
  *     that first call before any stream capture.
- *   - Every call clears the counters on `stream` and then launches; no call
- *     allocates or frees.  Calls share the array, which keeps the last call's
- *     contents: calls that overlap on the GPU (different streams, different
- *     host threads) race and must be ordered by the caller.
+ *   - Every call clears the split-K counters on `stream` and then launches;
+ *     no call allocates or frees.  Calls share the array, which keeps the
+ *     last call's contents: calls that overlap on the GPU (different streams,
+ *     different host threads) race and must be ordered by the caller.
+ *   - A kernel that gives up a bounded wait (about 2 s) leaves C incomplete
+ *     and sets an error word in the array; the call that launched it has
+ *     already returned FRT_OK.  frt_fp8_gemm_noalloc_status reports it.
  *   - Shapes whose split-K workspace would exceed the array are rejected
  *     with FRT_ERR_UNSUPPORTED before anything is launched.
+ *   - The first call's set-up is safe to race from several host threads.
  * Requires 1 <= M <= 65536, N % 128 == 0, K >= 16, K % 16 == 0.
  * Errors: INVALID_ARG, UNSUPPORTED, CUDA; the message comes from
  * frt_fp8_gemm_noalloc_last_error().
  */
 frt_status frt_fp8_gemm_noalloc(const void *A, const void *B, void *C, int M, int N, int K, float alpha,
                                 frt_stream_t stream);
+
+/*
+ * Synchronise `stream` and report whether an allocation-free GEMM on the
+ * current device gave up a bounded wait since the last report:
+ * FRT_ERR_DEVICE_TIMEOUT (its C is incomplete; the error word and the
+ * split-K counters are then cleared, synchronously), else FRT_OK.  Not for
+ * use while `stream` is being captured.  Allocates nothing.
+ * Errors: CUDA, DEVICE_TIMEOUT.
+ */
+frt_status frt_fp8_gemm_noalloc_status(frt_stream_t stream);
+
+/*
+ * Test hook for that failure path (no counterpart in the pages): launch one
+ * small GEMM on the fixed array whose MMA thread first waits for a barrier
+ * phase that nothing completes; the wait gives up after about 2 s and every
+ * role of the kernel drains and exits.  Returns what
+ * frt_fp8_gemm_noalloc_status then reports: DEVICE_TIMEOUT.  Overwrites the
+ * array's workspace.  Errors: CUDA, DEVICE_TIMEOUT.
+ */
+frt_status frt_fp8_gemm_noalloc_debug_stall(frt_stream_t stream);
+
+/* Message of the last failed frt_fp8_gemm_noalloc* call on this host thread. */
 const char *frt_fp8_gemm_noalloc_last_error(void);
 
 #ifdef __cplusplus

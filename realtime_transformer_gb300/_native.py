@@ -49,6 +49,8 @@ SIGNATURES = {
     "frt_ffn_last_error": (ctypes.c_char_p, []),
     "frt_fp8_gemm_noalloc": (_I, [_P, _P, _P, _I, _I, _I, _F, _P]),
     "frt_fp8_gemm_noalloc_last_error": (ctypes.c_char_p, []),
+    "frt_fp8_gemm_noalloc_status": (_I, [_P]),
+    "frt_fp8_gemm_noalloc_debug_stall": (_I, [_P]),
     # include/frt_qkv.h
     "frt_qkv_plan_create": (_I, [_I, _I, _I, _I, _F, _I, _I, ctypes.POINTER(_P)]),
     "frt_qkv_plan_destroy": (_I, [_P]),
@@ -208,10 +210,22 @@ def frt_fp8_gemm(plan, A, B, C, M, N, K, alpha, path, splits, stream) -> None:
 
 def frt_fp8_gemm_noalloc(A, B, C, M, N, K, alpha, stream) -> None:
     """FP8 GEMM with no plan and no allocation (scratch in a fixed device array)."""
-    st = lib().frt_fp8_gemm_noalloc(A, B, C, M, N, K, alpha, stream)
+    _check_noalloc(lib().frt_fp8_gemm_noalloc(A, B, C, M, N, K, alpha, stream))
+
+
+def _check_noalloc(st: int) -> None:
     if st != FRT_OK:
         msg = lib().frt_fp8_gemm_noalloc_last_error()
         raise FrtError(st, msg.decode() if msg else "")
+
+
+def frt_fp8_gemm_noalloc_status(stream) -> None:
+    """Synchronise `stream`; raise FRT_ERR_DEVICE_TIMEOUT if an allocation-free GEMM gave up a wait."""
+    _check_noalloc(lib().frt_fp8_gemm_noalloc_status(stream))
+
+
+def frt_fp8_gemm_noalloc_debug_stall(stream) -> None:
+    _check_noalloc(lib().frt_fp8_gemm_noalloc_debug_stall(stream))
 
 
 def frt_ffn_last_error() -> str:

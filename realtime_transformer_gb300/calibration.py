@@ -8,7 +8,7 @@ weight scales s_gu, s_down they were measured against) and a free-form
 `extra` map.  A record whose shape or weight scales differ from the plan's is
 stale and is not used.  Scales are fp32; JSON keeps them exactly (the decimal
 repr of a float32 widened to a Python float parses back to the same float32).
-Pure host code: no CUDA.
+Host code: no CUDA kernels (weights_digest reads tensors back to the host).
 """
 from __future__ import annotations
 
@@ -18,6 +18,8 @@ import math
 import os
 import struct
 
+import torch
+
 FORMAT = "frt_ffn_calibration/1"
 
 
@@ -25,6 +27,22 @@ def default_dir() -> str:
     """FRT_FFN_CALIB_DIR, else ~/.cache/frt_ffn/calibration."""
     return os.environ.get("FRT_FFN_CALIB_DIR") or os.path.join(os.path.expanduser("~"), ".cache", "frt_ffn",
                                                                 "calibration")
+
+
+def weights_digest(tag: bytes, tensors, chunk_elems: int = 1 << 26) -> str:
+    """SHA-256 over every element of each tensor in order (its raw bytes,
+    read in chunks so that host memory stays bounded), after a tag naming
+    how the tensors are used (e.g. whether the norm weight is folded).  Two
+    weight sets that differ in any element get different digests."""
+    h = hashlib.sha256(tag)
+    for t in tensors:
+        flat = t.detach().reshape(-1)
+        h.update(("%s:%d;" % (str(flat.dtype), flat.numel())).encode())
+        raw = flat.view(torch.uint8) if flat.element_size() == 1 else flat.view(torch.int16) \
+            if flat.element_size() == 2 else flat.view(torch.int32)
+        for part in raw.split(chunk_elems):
+            h.update(part.contiguous().cpu().numpy())
+    return h.hexdigest()
 
 
 def checkpoint_hash(shape: dict, layer_digests) -> str:

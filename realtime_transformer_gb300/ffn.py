@@ -7,7 +7,6 @@ a key made of a hash of the weights and the token count ("{hash}_Se{M}.json").
 """
 from __future__ import annotations
 
-import hashlib
 
 import torch
 
@@ -58,18 +57,19 @@ class FFNPlan:
             pass
 
     # -- weights / scales --------------------------------------------------
-    def load_weights(self, layer, w_norm, w_gate, w_up, w_down, stream=None, fold_norm=False):
+    def load_weights(self, layer, w_norm, w_gate, w_up, w_down, stream=None, fold_norm=False, digest=True):
         """Quantise one layer's BF16 weights into the plan; fold_norm: fold
-        the RMSNorm weight into the gate/up weights (the Pi0 layout)."""
+        the RMSNorm weight into the gate/up weights (the Pi0 layout).
+        digest: hash every weight element for the calibration cache key
+        (reads the weights back to the host); a plan loaded with
+        digest=False has no cache key."""
         d, ff = self.d, self.ff
         N.frt_ffn_load_weights_ex(self.handle, layer, _bf16(w_norm, (d,), "w_norm"),
                                   _bf16(w_gate, (ff, d), "w_gate"), _bf16(w_up, (ff, d), "w_up"),
                                   _bf16(w_down, (d, ff), "w_down"), N.FRT_LOAD_FOLD_NORM if fold_norm else 0,
                                   _stream(stream))
-        h = hashlib.sha256(b"fold" if fold_norm else b"plain")
-        for t in (w_norm, w_gate, w_up, w_down):
-            h.update(t.reshape(-1)[:: max(1, t.numel() // 4096)].contiguous().view(torch.int16).cpu().numpy().tobytes())
-        self._digest[layer] = h.hexdigest()
+        self._digest[layer] = (calibration.weights_digest(b"fold" if fold_norm else b"plain",
+                                                          (w_norm, w_gate, w_up, w_down)) if digest else None)
 
     def calibrate(self, residuals, hiddens=None, stream=None):
         M = residuals[0].shape[0]
@@ -103,6 +103,10 @@ class FFNPlan:
 
     def cache_key(self, M: int) -> str:
         """"{hash}_Se{M}": hash of the shape and the loaded weights."""
+        missing = [l for l, dg in enumerate(self._digest) if dg is None]
+        if missing:
+            raise ValueError("no weight digest for layers %s (not loaded, or loaded with digest=False)"
+                             % missing[:8])
         return calibration.cache_key(calibration.checkpoint_hash(self._shape(), self._digest), M)
 
     def save_scales(self, directory: str | None, M: int, extra: dict | None = None) -> str:

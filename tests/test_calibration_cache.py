@@ -98,3 +98,27 @@ def test_default_dir_follows_the_environment(monkeypatch, tmp_path):
     assert C.default_dir() == str(tmp_path)
     monkeypatch.delenv("FRT_FFN_CALIB_DIR")
     assert C.default_dir().endswith(os.path.join(".cache", "frt_ffn", "calibration"))
+
+
+def test_weight_digest_covers_every_element():
+    """The cache key's weight digest reads every element: two weight sets
+    that differ in one element anywhere (here one that a strided sample of
+    4096 elements would skip) get different digests, as do other tags and
+    other tensor boundaries."""
+    import torch
+    g = torch.Generator().manual_seed(3)
+    w = [(torch.randn(n, generator=g) * 0.02).to(torch.bfloat16) for n in (1024, 4096 * 1024, 1024 * 4096)]
+    base = C.weights_digest(b"plain", w)
+    assert base == C.weights_digest(b"plain", [t.clone() for t in w])
+    stride = w[1].numel() // 4096
+    for t_i, idx in ((1, 1), (1, stride + 1), (2, w[2].numel() - 1), (0, 17)):
+        v = [t.clone() for t in w]
+        flat = v[t_i].view(-1)
+        flat[idx] = flat[idx] + torch.tensor(1.0, dtype=torch.bfloat16)
+        assert C.weights_digest(b"plain", v) != base, (t_i, idx)
+    assert C.weights_digest(b"fold", w) != base
+    # moving an element across a tensor boundary changes the digest
+    a = torch.cat([w[0], w[1][:1]])
+    assert C.weights_digest(b"plain", [a, w[1][1:], w[2]]) != base
+    # chunked reading gives the same digest as one read
+    assert C.weights_digest(b"plain", w, chunk_elems=1000) == base
