@@ -283,7 +283,8 @@ def run_ours(args, wl, world, rank, local):
     r, h = io[0], io[1]
     plan = FFNPlan(wl.d, wl.ff, wl.act, wl.M, wl.L)
     for l, w in enumerate(weights):
-        plan.load_weights(l, w["w_norm"], w["w_gate"], w["w_up"], w["w_down"], fold_norm=args.variant == "fold")
+        plan.load_weights(l, w["w_norm"], w["w_gate"], w["w_up"], w["w_down"], fold_norm=args.variant == "fold",
+                          digest=False)
     if args.variant == "ada":
         # one modulation row per token (the heavier AdaRMSNorm case); kept alive for the graph
         mods = [synthetic.modulation(wl, l, wl.M, dev) for l in range(wl.L)]

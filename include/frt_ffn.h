@@ -217,6 +217,38 @@ frt_status frt_ffn_debug_trace(frt_ffn_plan_t plan, int layer, const void *resid
                                int M, void *r_prime, void *q_x, void *gu, void *q_h, void *out, frt_stream_t stream);
 
 /*
+ * Test/diagnostic: steps A2..A4 of layer `layer` from caller-supplied step-A1
+ * results, so that another implementation's q_x codes (e.g. a reference
+ * model's) can feed this library's GEMMs: r_prime [M, d] BF16 (the residual
+ * the down GEMM adds) and q_x [M, d] E4M3 (device).  Outputs, each optional
+ * (NULL) except out: gu [M, 2ff] BF16 (g then u), q_h [M, ff] E4M3, out
+ * [M, d] BF16.  Runs the forward's gate/up and down kernels for this M.
+ * Errors: as frt_ffn_debug_trace.
+ */
+frt_status frt_ffn_debug_trace_qx(frt_ffn_plan_t plan, int layer, const void *r_prime, const void *q_x, int M,
+                                  void *gu, void *q_h, void *out, frt_stream_t stream);
+
+/*
+ * Test/diagnostic: copy layer `layer`'s E4M3 weights as the plan stores them
+ * (step A0's output) to caller device buffers (either may be NULL):
+ * w_gu [2ff, d], the gate and up rows interleaved in blocks of 64 -- stored
+ * row 128 b + i holds W_gate row 64 b + i and row 128 b + 64 + i holds W_up
+ * row 64 b + i (0 <= i < 64) -- and w_down [d, ff].  Enqueued on `stream`.
+ * Errors: INVALID_ARG, NOT_READY (layer not loaded), CUDA.
+ */
+frt_status frt_ffn_debug_weights(frt_ffn_plan_t plan, int layer, void *w_gu, void *w_down, frt_stream_t stream);
+
+/*
+ * Test/diagnostic: codes[i] = E4M3 encoding of the fp32 value whose bit
+ * pattern is start + i, for 0 <= i < n, by the conversion every quantising
+ * kernel of this library uses (round to nearest even, saturating to +-448;
+ * steps A1, A3 and A0).  Lets a test sweep all 2^32 fp32 patterns against a
+ * reference encoder.  codes: device, 16-byte aligned, n bytes; n % 8 == 0,
+ * start + n <= 2^32.  Enqueued on `stream`.  Errors: INVALID_ARG, CUDA.
+ */
+frt_status frt_debug_e4m3_encode_range(unsigned start, unsigned long long n, void *codes, frt_stream_t stream);
+
+/*
  * Diagnostics (timing single kernels): launch step `step` of layer `layer`
  * alone, for M tokens, on the plan's own scratch buffers (whatever they hold):
  * 0 = A1 residual+RMSNorm+quantise, 1 = A2 gate/up GEMM with A3 (gated

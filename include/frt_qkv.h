@@ -116,6 +116,24 @@ frt_status frt_qkv_debug_trace(frt_qkv_plan_t plan, int layer, const void *resid
                                const int *positions, void *r_prime_out, void *q_out, void *k_out, void *v_out,
                                void *q_x_out, void *qkv_out, int M, frt_stream_t stream);
 
+/*
+ * Test/diagnostic: the GEMM and split + RoPE steps of layer `layer` from
+ * caller-supplied E4M3 codes q_x_in [M, d] (device) in place of the norm's
+ * output, so that another implementation's codes can feed this library's
+ * GEMM; writes q_out, k_out, v_out as frt_qkv_forward does and, if qkv_out is
+ * not NULL, the GEMM's BF16 output [M, (Hq + 2 Hkv) hd].  Same kernels.
+ * Errors: as frt_qkv_debug_trace.
+ */
+frt_status frt_qkv_debug_trace_qx(frt_qkv_plan_t plan, int layer, const void *q_x_in, const int *positions,
+                                  void *q_out, void *k_out, void *v_out, void *qkv_out, int M, frt_stream_t stream);
+
+/*
+ * Test/diagnostic: copy layer `layer`'s fused E4M3 weight [W_q; W_k; W_v]
+ * ([(Hq + 2 Hkv) hd, d], as the plan stores it) to a caller device buffer,
+ * enqueued on `stream`.  Errors: INVALID_ARG, NOT_READY, CUDA.
+ */
+frt_status frt_qkv_debug_weights(frt_qkv_plan_t plan, int layer, void *w_qkv, frt_stream_t stream);
+
 /* Synchronise `stream` and report a kernel that gave up a bounded wait
  * (DEVICE_TIMEOUT; the plan's error word is then cleared). */
 frt_status frt_qkv_device_status(frt_qkv_plan_t plan, frt_stream_t stream);

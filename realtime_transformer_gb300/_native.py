@@ -42,6 +42,9 @@ SIGNATURES = {
     "frt_ffn_graph_autotune": (_I, [_P, _P, _P, _P, _I, _I, _I, ctypes.POINTER(ctypes.c_float),
                                    ctypes.POINTER(ctypes.c_int), _P]),
     "frt_ffn_debug_trace": (_I, [_P, _I, _P, _P, _I, _P, _P, _P, _P, _P, _P]),
+    "frt_ffn_debug_trace_qx": (_I, [_P, _I, _P, _P, _I, _P, _P, _P, _P]),
+    "frt_ffn_debug_weights": (_I, [_P, _I, _P, _P, _P]),
+    "frt_debug_e4m3_encode_range": (_I, [ctypes.c_uint, ctypes.c_ulonglong, _P, _P]),
     "frt_ffn_device_status": (_I, [_P, _P]),
     "frt_ffn_debug_stall": (_I, [_P, _P]),
     "frt_ffn_debug_step": (_I, [_P, _I, _I, _I, _P]),
@@ -62,6 +65,8 @@ SIGNATURES = {
     "frt_qkv_forward": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _P]),
     "frt_qkv_debug_trace": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P]),
     "frt_qkv_device_status": (_I, [_P, _P]),
+    "frt_qkv_debug_weights": (_I, [_P, _I, _P, _P]),
+    "frt_qkv_debug_trace_qx": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _I, _P]),
     # include/frt_nvfp4.h
     "frt_fp4_plan_create": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(_P)]),
     "frt_fp4_plan_destroy": (_I, [_P]),
@@ -192,6 +197,18 @@ def frt_ffn_debug_trace(plan, layer, residual_in, hidden_in, M, r_prime, q_x, gu
     _check(lib().frt_ffn_debug_trace(plan, layer, residual_in, hidden_in, M, r_prime, q_x, gu, q_h, out, stream))
 
 
+def frt_ffn_debug_trace_qx(plan, layer, r_prime, q_x, M, gu, q_h, out, stream) -> None:
+    _check(lib().frt_ffn_debug_trace_qx(plan, layer, r_prime, q_x, M, gu, q_h, out, stream))
+
+
+def frt_ffn_debug_weights(plan, layer, w_gu, w_down, stream) -> None:
+    _check(lib().frt_ffn_debug_weights(plan, layer, w_gu, w_down, stream))
+
+
+def frt_debug_e4m3_encode_range(start, n, codes, stream) -> None:
+    _check(lib().frt_debug_e4m3_encode_range(start, n, codes, stream))
+
+
 def frt_ffn_debug_step(plan, layer, step, M, stream) -> None:
     _check(lib().frt_ffn_debug_step(plan, layer, step, M, stream))
 
@@ -282,6 +299,14 @@ def frt_qkv_debug_trace(plan, layer, residual_in, hidden_in, positions, r_prime,
                         stream) -> None:
     _check(lib().frt_qkv_debug_trace(plan, layer, residual_in, hidden_in, positions, r_prime, q, k, v, q_x, qkv,
                                      M, stream))
+
+
+def frt_qkv_debug_trace_qx(plan, layer, q_x, positions, q, k, v, qkv, M, stream) -> None:
+    _check(lib().frt_qkv_debug_trace_qx(plan, layer, q_x, positions, q, k, v, qkv, M, stream))
+
+
+def frt_qkv_debug_weights(plan, layer, w_qkv, stream) -> None:
+    _check(lib().frt_qkv_debug_weights(plan, layer, w_qkv, stream))
 
 
 def frt_qkv_device_status(plan, stream) -> None:

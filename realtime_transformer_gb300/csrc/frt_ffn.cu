@@ -849,6 +849,68 @@ FRT_API frt_status frt_ffn_debug_trace(frt_ffn_plan_t P, int layer, const void *
     return run_layer(P, layer, residual_in, hidden_in, dst, M, s, r_prime, q_x, gu, q_h);
 }
 
+FRT_API frt_status frt_ffn_debug_trace_qx(frt_ffn_plan_t P, int layer, const void *r_prime, const void *q_x, int M,
+                                          void *gu, void *q_h, void *out, frt_stream_t stream) {
+    frt_status st = check_io(P, r_prime, nullptr, out, M);
+    if (st != FRT_OK)
+        return st;
+    if (layer < 0 || layer >= P->L)
+        return fail(FRT_ERR_INVALID_ARG, "layer %d out of range", layer);
+    if (!P->loaded[layer] || !P->scales_ok)
+        return fail(FRT_ERR_NOT_READY, "layer %d not loaded or scales not set", layer);
+    if (M > 0 && !q_x)
+        return fail(FRT_ERR_INVALID_ARG, "q_x must be non-null");
+    if (!aligned16(q_x) || !aligned16(gu) || !aligned16(q_h))
+        return fail(FRT_ERR_INVALID_ARG, "trace buffers must be 16-byte aligned");
+    if (M == 0)
+        return FRT_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the caller's codes take the place of step A1's output; the rest of the
+    // layer runs the forward's kernels for this M
+    CK(cudaMemcpyAsync(P->qx, q_x, (size_t)M * P->d, cudaMemcpyDeviceToDevice, s));
+    GemmLaunch g;
+    if ((st = setup_gate_up(P, g, layer, M, EPI_GATED)) != FRT_OK)
+        return st;
+    g.p.dbg_gu = static_cast<uint16_t *>(gu);
+    CK(launch_gemm(g, s, false));
+    if (q_h)
+        CK(cudaMemcpyAsync(q_h, P->qh, (size_t)M * P->ff, cudaMemcpyDeviceToDevice, s));
+    GemmLaunch g2;
+    if ((st = setup_down(P, g2, layer, M, r_prime, out)) != FRT_OK)
+        return st;
+    CK(launch_gemm(g2, s, false));
+    return FRT_OK;
+}
+
+FRT_API frt_status frt_ffn_debug_weights(frt_ffn_plan_t P, int layer, void *w_gu, void *w_down,
+                                         frt_stream_t stream) {
+    if (!P)
+        return fail(FRT_ERR_INVALID_ARG, "null plan");
+    if (layer < 0 || layer >= P->L)
+        return fail(FRT_ERR_INVALID_ARG, "layer %d out of range", layer);
+    if (!P->loaded[layer])
+        return fail(FRT_ERR_NOT_READY, "weights of layer %d not loaded", layer);
+    const size_t D = P->d, F = P->ff;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (w_gu)
+        CK(cudaMemcpyAsync(w_gu, P->w_gu + (size_t)layer * 2 * F * D, 2 * F * D, cudaMemcpyDeviceToDevice, s));
+    if (w_down)
+        CK(cudaMemcpyAsync(w_down, P->w_down + (size_t)layer * D * F, D * F, cudaMemcpyDeviceToDevice, s));
+    return FRT_OK;
+}
+
+FRT_API frt_status frt_debug_e4m3_encode_range(unsigned start, unsigned long long n, void *codes,
+                                               frt_stream_t stream) {
+    if (n == 0)
+        return FRT_OK;
+    if (!codes || !aligned16(codes))
+        return fail(FRT_ERR_INVALID_ARG, "codes must be a non-null, 16-byte aligned device pointer");
+    if (n % 8 || n > 0x100000000ull - start)
+        return fail(FRT_ERR_INVALID_ARG, "need n %% 8 == 0 and start + n <= 2^32");
+    CK(launch_e4m3_sweep(start, (size_t)n, static_cast<uint8_t *>(codes), static_cast<cudaStream_t>(stream)));
+    return FRT_OK;
+}
+
 FRT_API frt_status frt_ffn_debug_step(frt_ffn_plan_t P, int layer, int step, int M, frt_stream_t stream) {
     if (!P)
         return fail(FRT_ERR_INVALID_ARG, "null plan");

@@ -118,6 +118,8 @@ cudaError_t launch_rope_table(const int *pos, const float *inv_freq, int M, int 
                               bool pdl);
 cudaError_t launch_rope_split(const void *qkv, int M, int nq, int nkv, int hd, const int *pos, const float *inv_freq,
                               void *q, void *k, void *v, cudaStream_t s, bool pdl);
+// Diagnostics: q[i] = E4M3 of the fp32 whose bits are start + i (n % 8 == 0).
+cudaError_t launch_e4m3_sweep(uint32_t start, size_t n, uint8_t *q, cudaStream_t s);
 // AdaRMSNorm modulation of the norm: row m's scale vector at p + m * stride
 // (its shift vector d elements after it); stride 0 = one row for all tokens.
 struct NormMod {

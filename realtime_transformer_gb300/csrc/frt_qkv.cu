@@ -134,8 +134,10 @@ frt_status setup_qkv_gemm(frt_qkv_plan *P, GemmLaunch &g, int l, int M, bool fus
     return FRT_OK;
 }
 
+// qx_in != null (diagnostics): the caller's E4M3 codes take the place of the
+// norm's output (r, h, rp unused), launched without dependency edges.
 frt_status run_qkv(frt_qkv_plan *P, int l, const void *r, const void *h, const int *pos, void *rp, void *q, void *k,
-                   void *v, int M, cudaStream_t s, void *trace_qx, void *trace_qkv) {
+                   void *v, int M, cudaStream_t s, void *trace_qx, void *trace_qkv, const void *qx_in = nullptr) {
     // The split + RoPE in the GEMM's epilogue where it can run there and the
     // GEMM's K is long enough to hide it behind the MMAs of the next tile
     // (measured on GB300: 5.6% faster at d = 5120, 8192 tokens; 32% slower at
@@ -151,15 +153,19 @@ frt_status run_qkv(frt_qkv_plan *P, int l, const void *r, const void *h, const i
     const float inv_sx = 1.0f / P->s_x[l];
     // the fused epilogue's (cos, sin) table, ahead of the norm kernel (whose
     // dependency wait orders it before the GEMM)
+    const bool pdl = qx_in == nullptr;
+    if (qx_in)
+        QCK(cudaMemcpyAsync(P->qx, qx_in, (size_t)M * P->d, cudaMemcpyDeviceToDevice, s));
     if (fused)
-        QCK(launch_rope_table(pos, P->inv_freq, M, P->hd / 2, P->rope_cs, s, true));
+        QCK(launch_rope_table(pos, P->inv_freq, M, P->hd / 2, P->rope_cs, s, pdl));
     // r' is stored only with a hidden input (otherwise r' = r) and only if asked for
-    QCK(launch_norm_quant(r, h, P->w_norm + (size_t)l * P->d, M, P->d, QKV_RMS_EPS, inv_sx, h ? rp : nullptr, P->qx,
-                          nullptr, false, s, true));
-    QCK(launch_gemm(g, s, true));
+    if (!qx_in)
+        QCK(launch_norm_quant(r, h, P->w_norm + (size_t)l * P->d, M, P->d, QKV_RMS_EPS, inv_sx, h ? rp : nullptr,
+                              P->qx, nullptr, false, s, true));
+    QCK(launch_gemm(g, s, pdl));
     if (!fused)
-        QCK(launch_rope_split(P->qkv, M, P->nq, P->nkv, P->hd, pos, P->inv_freq, q, k, v, s, true));
-    if (rp && !h)
+        QCK(launch_rope_split(P->qkv, M, P->nq, P->nkv, P->hd, pos, P->inv_freq, q, k, v, s, pdl));
+    if (rp && !h && !qx_in)
         QCK(cudaMemcpyAsync(rp, r, (size_t)M * P->d * 2, cudaMemcpyDeviceToDevice, s));
     if (trace_qx)
         QCK(cudaMemcpyAsync(trace_qx, P->qx, (size_t)M * P->d, cudaMemcpyDeviceToDevice, s));
@@ -379,6 +385,45 @@ FRT_API frt_status frt_qkv_forward(frt_qkv_plan_t P, int layer, const void *resi
                                    int M, frt_stream_t stream) {
     return frt_qkv_debug_trace(P, layer, residual_in, hidden_in, positions, r_prime_out, q_out, k_out, v_out,
                                nullptr, nullptr, M, stream);
+}
+
+FRT_API frt_status frt_qkv_debug_trace_qx(frt_qkv_plan_t P, int layer, const void *q_x_in, const int *positions,
+                                          void *q_out, void *k_out, void *v_out, void *qkv_out, int M,
+                                          frt_stream_t stream) {
+    frt_status st = check_layer_ready(P, layer);
+    if (st != FRT_OK)
+        return st;
+    if (!(P->s_x[layer] > 0.0f))
+        return qfail(FRT_ERR_NOT_READY, "activation scale of layer %d not set", layer);
+    if (M < 0)
+        return qfail(FRT_ERR_INVALID_ARG, "M must be >= 0 (got %d)", M);
+    if (M > P->M_max)
+        return qfail(FRT_ERR_SHAPE, "M=%d exceeds M_max=%d", M, P->M_max);
+    if (M == 0)
+        return FRT_OK;
+    if (!q_x_in || !positions || !q_out || !k_out || !v_out)
+        return qfail(FRT_ERR_INVALID_ARG, "q_x_in, positions, q_out, k_out and v_out must be non-null");
+    const void *ptrs[] = {q_x_in, positions, q_out, k_out, v_out, qkv_out};
+    for (const void *p : ptrs)
+        if (!al16(p))
+            return qfail(FRT_ERR_INVALID_ARG, "device pointers must be 16-byte aligned");
+    return run_qkv(P, layer, nullptr, nullptr, positions, nullptr, q_out, k_out, v_out, M,
+                   static_cast<cudaStream_t>(stream), nullptr, qkv_out, q_x_in);
+}
+
+FRT_API frt_status frt_qkv_debug_weights(frt_qkv_plan_t P, int layer, void *w_qkv, frt_stream_t stream) {
+    if (!P)
+        return qfail(FRT_ERR_INVALID_ARG, "null plan");
+    if (layer < 0 || layer >= P->L)
+        return qfail(FRT_ERR_INVALID_ARG, "layer %d out of range [0, %d)", layer, P->L);
+    if (!P->loaded[layer])
+        return qfail(FRT_ERR_NOT_READY, "weights of layer %d not loaded", layer);
+    if (!w_qkv)
+        return qfail(FRT_ERR_INVALID_ARG, "w_qkv must be non-null");
+    const size_t n = (size_t)P->N * P->d;
+    QCK(cudaMemcpyAsync(w_qkv, P->w + (size_t)layer * n, n, cudaMemcpyDeviceToDevice,
+                        static_cast<cudaStream_t>(stream)));
+    return FRT_OK;
 }
 
 FRT_API frt_status frt_qkv_device_status(frt_qkv_plan_t P, frt_stream_t stream) {

@@ -626,4 +626,28 @@ cudaError_t launch_quant_fold(const void *x, size_t rows, int d, const void *w, 
     return cudaGetLastError();
 }
 
+// Diagnostics: the E4M3 encoding of a range of fp32 bit patterns,
+// q[i] = E4M3(float with bits start + i), eight patterns a thread, by the
+// same conversion (e4m3x2) every quantising kernel here uses.  n % 8 == 0.
+__global__ void k_e4m3_sweep(uint32_t start, size_t n, uint2 *__restrict__ q) {
+    const size_t nv = n / 8;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < nv; i += (size_t)gridDim.x * blockDim.x) {
+        const uint32_t b = start + (uint32_t)(i * 8);
+        float f[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            f[j] = __uint_as_float(b + (uint32_t)j);
+        q[i] = pack8_e4m3(f);
+    }
+}
+
+cudaError_t launch_e4m3_sweep(uint32_t start, size_t n, uint8_t *q, cudaStream_t s) {
+    size_t blocks = (n / 8 + 255) / 256;
+    const size_t cap = (size_t)sm_count() * 16;
+    if (blocks > cap) blocks = cap;
+    if (blocks == 0) blocks = 1;
+    k_e4m3_sweep<<<(unsigned)blocks, 256, 0, s>>>(start, n, reinterpret_cast<uint2 *>(q));
+    return cudaGetLastError();
+}
+
 }  // namespace frt

@@ -188,6 +188,33 @@ class FFNPlan:
                               _ptr(out["out"]), _stream(stream))
         return out
 
+    def trace_layer_from_qx(self, layer, r_prime, q_x, stream=None):
+        """Steps A2..A4 of one layer from caller-supplied r' (BF16 [M, d]) and
+        q_x (E4M3 codes, uint8 [M, d]); returns g/u, q_h and the output
+        (diagnostics: lets another implementation's codes feed the GEMMs)."""
+        M, d, ff = r_prime.shape[0], self.d, self.ff
+        dev = r_prime.device
+        if q_x.dtype != torch.uint8 or tuple(q_x.shape) != (M, d) or not q_x.is_contiguous() or q_x.device != dev:
+            raise ValueError("q_x must be a contiguous uint8 [M, d] tensor on the device of r_prime")
+        out = {
+            "gu": torch.empty((M, 2 * ff), dtype=torch.bfloat16, device=dev),
+            "q_h": torch.empty((M, ff), dtype=torch.uint8, device=dev),
+            "out": torch.empty((M, d), dtype=torch.bfloat16, device=dev),
+        }
+        N.frt_ffn_debug_trace_qx(self.handle, layer, _bf16(r_prime, (M, d), "r_prime"), _ptr(q_x), M,
+                                 _ptr(out["gu"]), _ptr(out["q_h"]), _ptr(out["out"]), _stream(stream))
+        return out
+
+    def weights(self, layer, device="cuda", stream=None):
+        """The plan's E4M3 weights of one layer as stored (diagnostics):
+        w_gu [2ff, d] with gate and up rows interleaved in blocks of 64, and
+        w_down [d, ff], as uint8 tensors."""
+        d, ff = self.d, self.ff
+        w_gu = torch.empty((2 * ff, d), dtype=torch.uint8, device=device)
+        w_down = torch.empty((d, ff), dtype=torch.uint8, device=device)
+        N.frt_ffn_debug_weights(self.handle, layer, _ptr(w_gu), _ptr(w_down), _stream(stream))
+        return w_gu, w_down
+
     def gemm(self, A, B, alpha=1.0, path=0, splits=0, stream=None):
         """Diagnostics: C = alpha * A B^T on the plan's FP8 GEMM kernels (A [M,K], B [N,K] uint8 E4M3)."""
         M, K = A.shape

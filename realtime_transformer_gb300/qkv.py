@@ -82,5 +82,26 @@ class QKVPlan:
                               _ptr(o["q_x"]), _ptr(o["qkv"]), M, _stream(stream))
         return o
 
+    def trace_from_qx(self, layer, q_x, positions, stream=None):
+        """The GEMM and split + RoPE from caller-supplied E4M3 codes q_x
+        (uint8 [M, d]) in place of the norm's output; returns q, k, v and the
+        GEMM's BF16 output (diagnostics)."""
+        M = q_x.shape[0]
+        dev = q_x.device
+        if q_x.dtype != torch.uint8 or tuple(q_x.shape) != (M, self.d) or not q_x.is_contiguous():
+            raise ValueError("q_x must be a contiguous uint8 [M, d] tensor")
+        o = self._outs(M, dev)
+        o["qkv"] = torch.empty((M, (self.nq + 2 * self.nkv) * self.hd), dtype=torch.bfloat16, device=dev)
+        N.frt_qkv_debug_trace_qx(self.handle, layer, _ptr(q_x), _ptr(positions), _ptr(o["q"]), _ptr(o["k"]),
+                                 _ptr(o["v"]), _ptr(o["qkv"]), M, _stream(stream))
+        return o
+
+    def weights(self, layer, device="cuda", stream=None):
+        """The plan's fused E4M3 weight [W_q; W_k; W_v] of one layer as
+        stored, a uint8 [(Hq + 2 Hkv) hd, d] tensor (diagnostics)."""
+        w = torch.empty(((self.nq + 2 * self.nkv) * self.hd, self.d), dtype=torch.uint8, device=device)
+        N.frt_qkv_debug_weights(self.handle, layer, _ptr(w), _stream(stream))
+        return w
+
     def device_status(self, stream=None):
         N.frt_qkv_device_status(self.handle, _stream(stream))

@@ -53,19 +53,47 @@ def check_bf16(got_bits, ref_bits, what=""):
     return c, err
 
 
-def check_rows(got_bits, ref_bits, same_rows, what=""):
-    """Layer outputs: the contract on rows whose q_x codes agree; rows with an
-    allowed one-step q_x flip (a different, equally valid quantisation of
-    that row) are held to the pages' cosine claim, row by row."""
-    if same_rows.any():
-        c, e = check_bf16(got_bits[same_rows], ref_bits[same_rows], what)
+def check_layer(plan, layer, r, h, ref, what="", rows=None):
+    """Parity of one layer against the oracle's trace `ref` of the same input,
+    on every row (or every sampled row), in two passes over the forward's
+    kernels:
+      1. the layer from its input (r, h: device tensors of all M rows): r'
+         bit-exact, q_x codes under the code contract;
+      2. the layer from the oracle's own r' and q_x codes (steps A2..A4 on
+         the GPU; on rows outside `rows` the GPU's own codes), so that an
+         allowed one-step q_x flip does not propagate: g/u (BF16), q_h codes
+         and the layer output on all compared rows under the full contract
+         (codes; cosine and max|err| / RMS).
+    The own-path layer output of pass 1 is also reported and held to the
+    pages' cosine claim.  rows: indices of the rows `ref` covers (None: all).
+    """
+    dev = r.device
+    tr = plan.trace_layer(layer, r, h)
+    torch.cuda.synchronize()
+    plan.device_status()
+    if rows is None:
+        sel = lambda t: t
     else:
-        c, e = 1.0, 0.0
-    for i in np.nonzero(~same_rows)[0]:
-        g = oracle.bf16_decode(got_bits[i]).astype(np.float64)
-        r = oracle.bf16_decode(ref_bits[i]).astype(np.float64)
-        assert cosine(g, r) > 0.999, "%s: row %d (q_x flip) cosine %.6f" % (what, i, cosine(g, r))
-    return c, e
+        rows_t = torch.as_tensor(np.asarray(rows, np.int64), device=dev)
+        sel = lambda t: t.index_select(0, rows_t)
+    assert np.array_equal(bits(sel(tr["r_prime"])), ref.r_prime), what + ": r' = bf16(r + h) must be bit-exact"
+    agree_x = check_codes(u8(sel(tr["q_x"])), ref.q_x, what + " q_x")
+    qx_feed = tr["q_x"].clone()
+    ref_qx = torch.from_numpy(np.ascontiguousarray(ref.q_x)).to(dev)
+    if rows is None:
+        qx_feed.copy_(ref_qx)
+    else:
+        qx_feed.index_copy_(0, rows_t, ref_qx)
+    tq = plan.trace_layer_from_qx(layer, tr["r_prime"], qx_feed)
+    torch.cuda.synchronize()
+    plan.device_status()
+    check_bf16(bits(sel(tq["gu"])), ref.gu, what + " gate/up")
+    agree_h = check_codes(u8(sel(tq["q_h"])), ref.q_h, what + " q_h")
+    c, e = check_bf16(bits(sel(tq["out"])), ref.out, what + " layer output")
+    own = bits(sel(tr["out"]))
+    c_own = cosine(oracle.bf16_decode(own), oracle.bf16_decode(ref.out))
+    assert c_own > 0.999, "%s: own-path output cosine %.7f" % (what, c_own)
+    return dict(q_x=agree_x, q_h=agree_h, cos=c, err=e, cos_own=c_own, out=own, ref_out=ref.out)
 
 
 def bits(t: torch.Tensor) -> np.ndarray:

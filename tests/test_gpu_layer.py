@@ -1,21 +1,22 @@
 """Teacher-forced parity of one layer (steps A0..A4) against the oracle: both
 sides get the same layer input and the same scales, and every intermediate
-is compared (itsolotime FlashRT article, 7.2; agentlenshq summary, "Main
-ideas": fused residual-norm-quantise).
+is compared on every row (itsolotime FlashRT article, 7.2; agentlenshq
+summary, "Main ideas": fused residual-norm-quantise).
 
 GPU and oracle sum the RMSNorm mean square in different orders, so about one
 q_x element per call lands on the other side of an E4M3 rounding boundary
-(allowed: one code step).  Everything after q_x in that row is then a
-different, equally valid computation, so the gate/up output, q_h and the
-layer output are held to the contract on rows whose q_x codes agree, and a
-row with a flip to the pages' cosine claim (> 0.999)."""
+(allowed by the code contract: one step, at most 0.1% of codes).  To keep
+that flip from spreading through the rest of the row, the GEMMs and the
+activation are then checked from the oracle's own q_x codes (steps A2..A4 of
+the GPU's forward kernels on them), on all rows under the full contract.  The
+plan's stored E4M3 weights (step A0) are compared byte for byte."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
 import synthetic
-from parity import Case, bits, check_bf16, check_codes, check_rows, cosine, u8
+from parity import Case, bits, check_bf16, check_codes, check_layer, cosine, u8
 
 pytestmark = pytest.mark.gpu
 
@@ -57,25 +58,39 @@ def test_weight_scales_match_oracle_exactly(case):
 
 
 def compare_layer(plan, layer, r_bits, h_bits, ql, s_x, s_h, act, dev, what=""):
-    """Run GPU layer `layer` and the oracle on the same input; check the contract."""
+    """Run GPU layer `layer` and the oracle on the same input; check the contract on every row."""
     r = synthetic.from_bf16_bits(r_bits, dev)
     h = synthetic.from_bf16_bits(h_bits, dev) if h_bits is not None else None
-    tr = plan.trace_layer(layer, r, h)
-    torch.cuda.synchronize()
-    plan.device_status()
     ref = oracle.ffn_layer(r_bits, h_bits, ql.w_norm, ql.q_gu, ql.q_down, s_x, s_h, ql.s_gu, ql.s_d, act, trace=True)
-    assert np.array_equal(bits(tr["r_prime"]), ref.r_prime), "r' = bf16(r + h) must be bit-exact"
-    qx = u8(tr["q_x"])
-    agree_x = check_codes(qx, ref.q_x, what + " q_x")
-    rows = np.all(qx == ref.q_x, axis=1)
-    assert rows.mean() >= 0.5, what
-    gu = bits(tr["gu"])
-    check_bf16(gu[rows], ref.gu[rows], what + " gate/up (rows with identical q_x)")
-    assert cosine(oracle.bf16_decode(gu), oracle.bf16_decode(ref.gu)) >= 0.9999
-    agree_h = check_codes(u8(tr["q_h"])[rows], ref.q_h[rows], what + " q_h (rows with identical q_x)")
-    c, e = check_rows(bits(tr["out"]), ref.out, rows, what + " layer output")
-    return dict(q_x=agree_x, rows=float(rows.mean()), q_h=agree_h, cos=c, err=e, out=bits(tr["out"]),
-                ref_out=ref.out)
+    return check_layer(plan, layer, r, h, ref, what)
+
+
+def interleave_gu(q_gu, ff):
+    """The plan's stored gate/up order: blocks of 64 gate rows, then the 64
+    up rows of the same features."""
+    g, u = q_gu[:ff], q_gu[ff:]
+    d = q_gu.shape[1]
+    return np.stack([g.reshape(ff // 64, 64, d), u.reshape(ff // 64, 64, d)], axis=1).reshape(2 * ff, d)
+
+
+def check_weight_codes(plan, q, what=""):
+    """Step A0 is byte work: every stored E4M3 weight code equals the
+    oracle's quantisation of the same BF16 weights."""
+    for l, ql in enumerate(q):
+        w_gu, w_down = plan.weights(l)
+        torch.cuda.synchronize()
+        ff = plan.ff
+        assert ql.q_gu.shape == (2 * ff, plan.d)
+        got_gu, got_d = u8(w_gu), u8(w_down)
+        want_gu = interleave_gu(ql.q_gu, ff)
+        bad = np.argwhere(got_gu != want_gu)
+        assert bad.size == 0, (what, l, "gate/up", bad[:5])
+        bad = np.argwhere(got_d != ql.q_down)
+        assert bad.size == 0, (what, l, "down", bad[:5])
+
+
+def test_weight_codes_match_oracle_byte_for_byte(case):
+    check_weight_codes(case.plan, case.q, case.wl.name)
 
 
 @pytest.mark.parametrize("with_hidden", [True, False])
@@ -83,8 +98,8 @@ def test_layer_intermediates_match_oracle(case, with_hidden):
     wl = case.wl
     st = compare_layer(case.plan, 0, bits(case.r), bits(case.h) if with_hidden else None, case.q[0],
                        case.s_x[0], case.s_h[0], wl.act_id, case.dev, wl.name)
-    print("%s hidden=%s: q_x agree %.6f, rows %.3f, q_h agree %.6f, out cos %.7f err %.4f" % (
-        wl.name, with_hidden, st["q_x"], st["rows"], st["q_h"], st["cos"], st["err"]))
+    print("%s hidden=%s: q_x agree %.6f, q_h agree %.6f, out cos %.7f err %.4f (own path cos %.7f)" % (
+        wl.name, with_hidden, st["q_x"], st["q_h"], st["cos"], st["err"], st["cos_own"]))
 
 
 def test_out_may_alias_residual(case):

@@ -10,7 +10,7 @@ import torch
 
 import oracle
 import synthetic
-from parity import bits, check_bf16, check_codes
+from parity import bits, check_bf16, check_codes, u8
 
 pytestmark = pytest.mark.gpu
 
@@ -41,7 +41,25 @@ def test_full_size_qkv(name):
     ref = oracle.qkv_layer(hr, hh, hw["w_norm"], codes, s_x, s_qkv, nq, nkv, hd, pos[rows],
                            oracle.rope_inv_freq(hd, base))
     assert np.array_equal(bits(out["r_prime"])[rows], ref.r_prime)
+    rows_t = torch.from_numpy(rows).to(dev)
+    w_st = plan.weights(0)
+    torch.cuda.synchronize()
+    assert np.array_equal(u8(w_st), codes), name + " stored weight codes"
+    del w_st
+    # q_x under the code contract on the sampled rows, then the GEMM and split
+    # + RoPE at full M from the oracle's codes on those rows (the GPU's own
+    # elsewhere): every sampled row under the full contract
+    tr = plan.trace(0, r, h, torch.from_numpy(pos).to(dev))
+    torch.cuda.synchronize()
+    qx = tr["q_x"].index_select(0, rows_t)
+    check_codes(u8(qx), ref.q_x, name + " q_x")
+    feed = tr["q_x"].clone()
+    feed.index_copy_(0, rows_t, torch.from_numpy(ref.q_x).to(dev))
+    tq = plan.trace_from_qx(0, feed, torch.from_numpy(pos).to(dev))
+    torch.cuda.synchronize()
+    plan.device_status()
+    check_bf16(bits(tq["qkv"].index_select(0, rows_t)), ref.qkv, name + " qkv")
     for k in ("q", "k", "v"):
-        got = bits(out[k])[:, rows]
+        got = bits(tq[k].index_select(1, rows_t))
         check_bf16(got, getattr(ref, k), "%s %s" % (name, k))
     plan.close()

@@ -19,7 +19,7 @@ import torch
 import oracle
 import synthetic
 from parity import Case, bits, cosine
-from test_gpu_layer import compare_layer
+from test_gpu_layer import check_weight_codes, compare_layer
 
 pytestmark = pytest.mark.gpu
 
@@ -46,6 +46,12 @@ def test_weight_scales_match_oracle_exactly(case):
         assert sc["s_down"][l] == np.float32(ql.s_d)
 
 
+def test_weight_codes_match_oracle_byte_for_byte(case):
+    """Plain and folded quantisers alike (the folded stacks compare against
+    the oracle's folded quantisation)."""
+    check_weight_codes(case.plan, case.q, case.wl.name + (" folded" if case.fold else ""))
+
+
 def test_every_layer_teacher_forced(case):
     wl = case.wl
     traces = case.oracle_forward(trace=True)
@@ -53,8 +59,8 @@ def test_every_layer_teacher_forced(case):
     for l in range(wl.L):
         st = compare_layer(case.plan, l, cur, bits(case.h) if l == 0 else None, case.q[l], case.s_x[l],
                            case.s_h[l], wl.act_id, case.dev, "%s layer %d" % (wl.name, l))
-        print("%s layer %2d: q_x %.6f rows %.3f q_h %.6f out cos %.7f err %.4f" % (
-            wl.name, l, st["q_x"], st["rows"], st["q_h"], st["cos"], st["err"]))
+        print("%s layer %2d: q_x %.6f q_h %.6f out cos %.7f err %.4f (own path cos %.7f)" % (
+            wl.name, l, st["q_x"], st["q_h"], st["cos"], st["err"], st["cos_own"]))
         cur = traces[l].out
 
 
