@@ -201,24 +201,41 @@ def barrier(world):
 
 # -------------------------------------------------------------- CPU oracle --
 
-def oracle_setup(wl, weights, calib, rows):
-    """Quantise and calibrate with the oracle (untimed)."""
+def oracle_layers(wl, layers):
+    """Oracle-quantised weights of the given layers (seeded like the GPU's)."""
     import oracle
     bits = synthetic.bf16_bits
-    q = oracle.quantize_stack([{k: bits(v) for k, v in w.items()} for w in weights])
-    s_x, s_h = oracle.calibrate_stack(q, [bits(a[:rows]) for a, _ in calib], [bits(b[:rows]) for _, b in calib],
-                                      wl.act_id)
-    return q, s_x, s_h
+    gen = "cuda" if torch.cuda.is_available() else "cpu"
+    q = []
+    for l in layers:
+        w = synthetic.layer_weights(wl, l, device=gen)
+        q.append(oracle.quantize_stack([{k: bits(v) for k, v in w.items()}])[0])
+        del w
+    return q
 
 
-def oracle_time(wl, q, s_x, s_h, r, h, rows, reps):
+def oracle_sample(wl, q, s_x, s_h, r, h, budget_s):
+    """Time the oracle, as it stands, on a bounded sample of the workload:
+    `rows` tokens through the len(q) layers held in q (the stack's first
+    ones), sized to about budget_s seconds.  Returns (tokens/s of the whole
+    stack, scaled by L / len(q); the sample's seconds; rows)."""
     import oracle
     bits = synthetic.bf16_bits
-    rb, hb = bits(r[:rows]), bits(h[:rows])
+    rb, hb = bits(r.cpu()), bits(h.cpu())
     t0 = time.perf_counter()
-    for _ in range(reps):
-        oracle.stack_forward(q, rb, hb, s_x, s_h, wl.act_id)
-    return time.perf_counter() - t0
+    oracle.stack_forward(q[:1], rb[:1], hb[:1], s_x, s_h, wl.act_id)
+    t1 = max(time.perf_counter() - t0, 1e-6)
+    rows = max(1, min(wl.M, int(budget_s / (t1 * len(q)))))
+    t0 = time.perf_counter()
+    oracle.stack_forward(q, rb[:rows], hb[:rows], s_x, s_h, wl.act_id)
+    dt = time.perf_counter() - t0
+    return rows / (dt * wl.L / len(q)), dt, rows
+
+
+def sample_layers(wl):
+    """How many of the stack's first layers the oracle sample runs."""
+    per_layer = 3 * wl.d * wl.ff
+    return max(1, min(wl.L, int(2.0e8 // per_layer)))
 
 
 def cpu_cores():
@@ -238,22 +255,32 @@ def gen_workload(wl, device):
 
 
 def run_reference(args, wl, world, rank):
-    """The CPU oracle, as it stands, on this host's cores."""
+    """The CPU oracle, as it stands, on this host's cores: each step a bounded
+    sample of the workload (tokens through the stack's first layers, scaled
+    to the whole stack); scales from the oracle's own calibration of those
+    layers on a few rows."""
     if rank != 0:
         return None
-    gen_dev = "cuda" if torch.cuda.is_available() else "cpu"
-    weights, r, h, calib = gen_workload(wl, gen_dev)
-    rows_cal = min(wl.M, 64)
-    q, s_x, s_h = oracle_setup(wl, weights, calib, rows_cal)
-    t1 = oracle_time(wl, q, s_x, s_h, r, h, 1, 1)            # one token through the stack
-    budget = float(os.environ.get("FRT_REFERENCE_SECONDS", "120"))
-    rows = max(1, min(wl.M, int(budget / max(1e-9, t1 * max(1, args.steps + args.warmup)))))
-    oracle_time(wl, q, s_x, s_h, r, h, rows, args.warmup)
-    dt = oracle_time(wl, q, s_x, s_h, r, h, rows, args.steps)
+    import oracle
+    bits = synthetic.bf16_bits
+    n_s = sample_layers(wl)
+    q = oracle_layers(wl, range(n_s))
+    r, h = synthetic.inputs(wl)
+    calib = synthetic.calibration_batches(wl, M=min(wl.M, 8))
+    s_x, s_h = oracle.calibrate_stack(q, [bits(a) for a, _ in calib], [bits(b) for _, b in calib], wl.act_id)
+    budget = float(os.environ.get("FRT_REFERENCE_SECONDS", "60")) / max(1, args.steps + args.warmup)
+    _, _, rows = oracle_sample(wl, q, s_x, s_h, r, h, budget)
+    rb, hb = bits(r[:rows]), bits(h[:rows])
+    for _ in range(args.warmup):
+        oracle.stack_forward(q, rb, hb, s_x, s_h, wl.act_id)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.stack_forward(q, rb, hb, s_x, s_h, wl.act_id)
+    dt = (time.perf_counter() - t0) * wl.L / n_s      # the whole stack, scaled from the sampled layers
     value = rows * args.steps / dt
-    sample = "%d of %d tokens through all %d layers per step" % (rows, wl.M, wl.L)
+    sample = "%d of %d tokens through %d of the %d layers per step, scaled to the stack" % (rows, wl.M, n_s, wl.L)
     line = {
-        "impl": "reference", "metric": "FP8 FFN stack tokens/s (graph-replayed, %s)" % wl.name, "value": value,
+        "impl": "reference", "metric": HEADLINE_METRIC if args.config is None else metric_of(wl), "value": value,
         "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000.0 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "fp32 (E4M3/BF16 emulated)", "data": "synthetic",
@@ -265,26 +292,58 @@ def run_reference(args, wl, world, rank):
     return line
 
 
+def metric_of(wl, variant="plain"):
+    name = wl.name if variant == "plain" else "%s, %s" % (wl.name, VARIANTS[variant])
+    return "FP8 FFN stack tokens/s (graph-replayed, %s)" % name
+
+
 def config_of(wl):
     return {"workload": wl.name, "M": wl.M, "d": wl.d, "ff": wl.ff, "act": wl.act, "layers": wl.L,
             "weights": "E4M3 per-tensor", "residual": "BF16", "graph": "one CUDA graph per stack",
             "l2": l2_note(), "parallelism": "replicas"}
 
 
+def timed_steps(stream, flush, fn, n, warm):
+    """n steps of fn timed with CUDA events on `stream` (after `warm` untimed
+    ones), L2 flushed before each unless --warm-l2; per-step milliseconds."""
+    for _ in range(warm):
+        with torch.cuda.stream(stream):
+            if not WARM_L2:
+                flush.zero_()
+            fn()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    with torch.cuda.stream(stream):
+        for e0, e1 in evs:
+            if not WARM_L2:
+                flush.zero_()
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+    torch.cuda.synchronize()
+    return [e0.elapsed_time(e1) for e0, e1 in evs]
+
+
 def run_ours(args, wl, world, rank, local):
+    """One workload: the stack graph-replayed K times (CUDA events, L2 flushed
+    between steps), end to end through the C ABI with pinned host buffers,
+    the in-stack share of each kernel (graph_profile) for the dominant
+    kernel's roofline, and the oracle on a bounded sample."""
     from realtime_transformer_gb300.ffn import FFNPlan
-    from realtime_transformer_gb300 import _native as N
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     P = peaks()
-    weights, r, h, calib = gen_workload(wl, dev)
+    r, h = synthetic.inputs(wl, device=dev)
+    calib = synthetic.calibration_batches(wl, device=dev)
     # residual and hidden side by side in one buffer: one host-to-device copy per step
     io = torch.stack([r, h]).contiguous()
     r, h = io[0], io[1]
     plan = FFNPlan(wl.d, wl.ff, wl.act, wl.M, wl.L)
-    for l, w in enumerate(weights):
+    for l in range(wl.L):   # generated and loaded one layer at a time
+        w = synthetic.layer_weights(wl, l, device=dev)
         plan.load_weights(l, w["w_norm"], w["w_gate"], w["w_up"], w["w_down"], fold_norm=args.variant == "fold",
                           digest=False)
+        del w
     if args.variant == "ada":
         # one modulation row per token (the heavier AdaRMSNorm case); kept alive for the graph
         mods = [synthetic.modulation(wl, l, wl.M, dev) for l in range(wl.L)]
@@ -297,35 +356,16 @@ def run_ours(args, wl, world, rank, local):
     with torch.cuda.stream(stream):
         plan.graph_capture(r, h, out, stream)
     torch.cuda.synchronize()
-
-    def timed(fn, n, warm):
-        for _ in range(warm):
-            with torch.cuda.stream(stream):
-                if not WARM_L2:
-                    flush.zero_()
-                fn()
-        torch.cuda.synchronize()
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
-        with torch.cuda.stream(stream):
-            for e0, e1 in evs:
-                if not WARM_L2:
-                    flush.zero_()
-                e0.record(stream)
-                fn()
-                e1.record(stream)
-        torch.cuda.synchronize()
-        return [e0.elapsed_time(e1) for e0, e1 in evs]
-
     replay = lambda: plan.graph_replay(wl.M, stream)
 
     # warm-up, then exactly K timed steps between barriers
-    timed(replay, 0, args.warmup)
+    timed_steps(stream, flush, replay, 0, args.warmup)
     barrier(world)
     torch.cuda.synchronize()
     sampler = ClockSampler(local)
     sampler.start()
     t_wall0 = time.perf_counter()
-    step_ms = timed(replay, args.steps, 0)
+    step_ms = timed_steps(stream, flush, replay, args.steps, 0)
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall0
     clocks = sampler.stop()
@@ -345,68 +385,109 @@ def run_ours(args, wl, world, rank, local):
         plan.graph_replay(wl.M, stream)
         h_o.copy_(out, non_blocking=True)
 
-    e2e_ms = timed(e2e_step, args.steps, args.warmup)
+    e2e_ms = timed_steps(stream, flush, e2e_step, args.steps, args.warmup)
     e2e_s = reduce_max(sum(e2e_ms) / 1000.0, world, dev)
     h2d = h_io.numel() * 2
     d2h = h_o.numel() * 2
 
-    # per-kernel timing (one layer's three kernels launched alone)
-    kern = {}
-    n_k = max(20, min(200, args.steps))
-    for step in range(len(STEP_NAMES)):
-        ms = timed(lambda s=step: N.frt_ffn_debug_step(plan.handle, 0, s, wl.M, stream.cuda_stream), n_k, 3)
-        kern[STEP_NAMES[step]] = statistics.mean(ms) * 1000.0
-    plan.device_status(stream)
-    dom = max(kern, key=kern.get)
+    # in-stack share of every launch (stamped profiling replays of the same
+    # graph, L2 flushed before each like the timed steps); the dominant kernel
+    # is the step whose launches take the most of the stack
+    n_prof = max(10, min(50, args.steps))
+    shares = []
+    for _ in range(n_prof):
+        if not WARM_L2:
+            with torch.cuda.stream(stream):
+                flush.zero_()
+        shares.append(plan.graph_profile(wl.M, n_replays=1, stream=stream))
+    n_k = len(shares[0])
+    med = [statistics.median(sh[k] for sh in shares) for k in range(n_k)]
+    per_step = {STEP_NAMES[s]: [med[3 * l + s] for l in range(wl.L)] for s in range(3)}
+    kern_total = {k: sum(v) for k, v in per_step.items()}
+    dom = max(kern_total, key=kern_total.get)
     dom_step = STEP_NAMES.index(dom)
     nbytes, flops = kernel_bytes_flops(wl, wl.M, dom_step)
-    t_dom = kern[dom] * 1e-6
-    fp8_peak = 2.0 * P["bf16_tflops"]
+    t_dom = kern_total[dom] / wl.L * 1e-6          # average in-stack duration of one launch
+    long_step = ms_step >= 1.0
+    fp8_peak = 2.0 * (P["bf16_tflops_sustained"] if long_step else P["bf16_tflops"])
     ridge = fp8_peak * 1e12 / (P["hbm_gbs"] * 1e9)
     tensor_bound = flops > 0 and flops / nbytes > ridge
     if tensor_bound:
         achieved = flops / t_dom / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
                 "frac": achieved / fp8_peak,
-                "peak_note": "FP8 dense = 2 x measured bf16 burst (%s; nominal fp8/bf16 ratio 2)" % P["src"]}
+                "peak_note": "FP8 dense = 2 x %s bf16 (%s; nominal fp8/bf16 ratio 2)" % (
+                    "sustained" if long_step else "burst", P["src"])}
     else:
         achieved = nbytes / t_dom / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": P["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / P["hbm_gbs"], "peak_note": "%s HBM copy bandwidth" % P["src"]}
     roof["kernel"] = dom
-    roof["us_per_launch"] = kern[dom]
+    roof["us_per_launch"] = kern_total[dom] / wl.L
+    roof["timing"] = ("in-stack share of each launch (%%globaltimer stamps, median of %d profiled replays): "
+                      "L x us_per_launch = %.1f us of a %.1f us step" % (n_prof, kern_total[dom],
+                                                                         1000.0 * ms_step))
     roof["algorithmic_bytes"] = nbytes
+    roof["flops"] = flops
     roof["traffic"] = profiled_traffic(dom, wl.name)
 
     layer_s = ms_step / 1000.0 / wl.L
-    step_roof = {"bound": "hbm", "achieved": layer_algorithmic_bytes(wl, wl.M) / layer_s / 1e9,
-                 "peak": P["hbm_gbs"], "unit": "GB/s"}
-    step_roof["frac"] = step_roof["achieved"] / P["hbm_gbs"]
-    step_roof["tflops"] = 6.0 * wl.M * wl.d * wl.ff / layer_s / 1e12
+    lb = layer_algorithmic_bytes(wl, wl.M)
+    lf = 6.0 * wl.M * wl.d * wl.ff
+    step_roof = {"bound": "hbm", "achieved": lb / layer_s / 1e9, "peak": P["hbm_gbs"], "unit": "GB/s",
+                 "frac": lb / layer_s / 1e9 / P["hbm_gbs"], "tflops": lf / layer_s / 1e12}
+    if lf / lb > ridge:
+        step_roof = {"bound": "tensor", "achieved": lf / layer_s / 1e12, "peak": fp8_peak, "unit": "TFLOP/s",
+                     "frac": lf / layer_s / 1e12 / fp8_peak, "hbm_gbs": lb / layer_s / 1e9}
 
     line = {
-        "metric": "FP8 FFN stack tokens/s (graph-replayed, %s)" % (
-            wl.name if args.variant == "plain" else "%s, %s" % (wl.name, VARIANTS[args.variant])),
+        "metric": metric_of(wl, args.variant),
         "value": value, "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "us_per_layer": 1000.0 * ms_step / wl.L, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "fp8_e4m3 (fp32 accumulate, bf16 residual)", "data": "synthetic",
         "config": config_of(wl) if args.variant == "plain" else dict(config_of(wl), variant=VARIANTS[args.variant]),
-        "roofline": roof, "step_roofline": step_roof, "kernels_us": kern,
+        "roofline": roof, "step_roofline": step_roof,
+        "kernels_us_in_stack": {k: v / wl.L for k, v in kern_total.items()},
         "e2e": {"value": world * wl.M * args.steps / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": 1000.0 * e2e_s / args.steps},
-        "gpu_launches": args.steps * wl.L * len(STEP_NAMES), "clocks": clocks, "wall_s_timed_region": t_wall,
+        "gpu_launches": args.steps * n_k, "clocks": clocks, "wall_s_timed_region": t_wall,
     }
+    sc = plan.scales()
     plan.close()
+    del plan, flush
+    torch.cuda.empty_cache()
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.variant == "plain":
-        rows = min(wl.M, 64)
-        q, s_x, s_h = oracle_setup(wl, weights, calib, rows)
-        budget = float(os.environ.get("FRT_CPU_BASELINE_SECONDS", "15"))
-        t1 = oracle_time(wl, q, s_x, s_h, r.cpu(), h.cpu(), 1, 1)
-        rows = max(1, min(wl.M, int(budget / max(t1, 1e-9))))
-        dt = oracle_time(wl, q, s_x, s_h, r.cpu(), h.cpu(), rows, 1)
-        line["cpu_baseline"] = {"value": rows / dt, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
-                                "sample": "%d of %d tokens through all %d layers, once" % (rows, wl.M, wl.L)}
+        n_s = sample_layers(wl)
+        q = oracle_layers(wl, range(n_s))
+        budget = float(os.environ.get("FRT_CPU_BASELINE_SECONDS", "6"))
+        v, dt, rows = oracle_sample(wl, q, sc["s_x"][:n_s], sc["s_h"][:n_s], r, h, budget)
+        line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+                                "sample": "%d of %d tokens through %d of the %d layers (%.1f s), scaled to the "
+                                          "stack" % (rows, wl.M, n_s, wl.L, dt)}
+    return line
+
+
+ALL_WORKLOADS = ["tiny", "vla_action_expert", "vla_prefix", "llm_decode", "long_prefill"]
+HEADLINE = "long_prefill"   # the largest single-GPU workload: the line's top-level figures
+HEADLINE_METRIC = "FP8 FFN stack tokens/s vs M (graph-replayed; headline: %s)" % HEADLINE
+
+
+def run_all(args, world, rank, local):
+    """The metric is quoted against M: every workload in one run, the
+    headline's figures at the top level and each workload's under per_config."""
+    per = {}
+    for name in ALL_WORKLOADS:
+        per[name] = run_ours(args, synthetic.WORKLOADS[name], world, rank, local)
+    line = dict(per[HEADLINE])
+    line["metric"] = HEADLINE_METRIC
+    line["per_config"] = {
+        name: {k: v for k, v in ln.items() if k in ("value", "ms_per_step", "us_per_layer", "roofline",
+                                                   "step_roofline", "kernels_us_in_stack", "e2e", "cpu_baseline",
+                                                   "clocks", "gpu_launches", "config")}
+        for name, ln in per.items()}
+    line["gpu_launches"] = sum(ln["gpu_launches"] for ln in per.values())
+    line["gpu_launches_note"] = "all workloads' timed steps; the headline's own: %d" % per[HEADLINE]["gpu_launches"]
     return line
 
 
@@ -675,10 +756,12 @@ def run_fp4(args, wl, world, rank, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(synthetic.WORKLOADS))
+    ap.add_argument("--config", default=None, choices=sorted(synthetic.WORKLOADS),
+                    help="one workload (default: the FFN stack times all five, the headline on %s; the other "
+                         "sublayers default to %s)" % (HEADLINE, DEFAULT_CONFIG))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sublayer", choices=["ffn", "qkv", "ffn_nvfp4"], default="ffn",
                     help="ffn: the FFN stack (the default bench line); qkv: the attention-input projections; "
@@ -696,7 +779,8 @@ def main():
     WARM_L2 = args.warm_l2
     if args.warmup < 3:
         args.warmup = 3
-    wl = synthetic.WORKLOADS[args.config]
+    all_ffn = args.config is None and args.sublayer == "ffn" and args.layers == 0 and args.variant == "plain"
+    wl = synthetic.WORKLOADS[args.config or (HEADLINE if args.sublayer == "ffn" else DEFAULT_CONFIG)]
     if args.layers > 0:
         wl = wl.with_(L=args.layers, name=wl.name + "_%dlayers" % args.layers)
     if args.variant != "plain" and (args.sublayer != "ffn" or args.impl != "ours"):
@@ -708,6 +792,8 @@ def main():
         line = run_qkv(args, wl, world, rank, local)
     elif args.sublayer == "ffn_nvfp4":
         line = run_fp4(args, wl, world, rank, local)
+    elif all_ffn:
+        line = run_all(args, world, rank, local)
     else:
         line = run_ours(args, wl, world, rank, local)
     if rank == 0 and line is not None:

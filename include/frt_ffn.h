@@ -207,6 +207,27 @@ frt_status frt_ffn_graph_autotune(frt_ffn_plan_t plan, const void *residual_in, 
                                   frt_stream_t stream);
 
 /*
+ * Measurement: where the time of a graph replay goes, kernel by kernel,
+ * inside the stack ("FlashRT docs/architecture.md", 7: the replayed graph is
+ * the unit that runs).  Captures the forward for M again, on the buffers of
+ * the graph held for M, with every launch recording %globaltimer at its
+ * CTAs' starts and ends; replays it n_replays times (synchronising after
+ * each); and writes to kernel_us[k] the median over replays of launch k's
+ * share of the replay: from its first CTA's start, or its predecessor's end
+ * if later, to its last CTA's end -- so the shares of consecutive launches
+ * that overlap (programmatic dependent launch) do not overlap, and they sum
+ * to at most the replay's span.  Launch k = 3 l + s for layer l and step s
+ * (0 norm + quantise, 1 gate/up GEMM with the gated activation, 2 down GEMM
+ * with the residual); *n_kernels (may be NULL) receives how many were written
+ * (kernel_us must hold 3 n_layers floats).  The profiling graph is freed
+ * before returning; the graph held for M is unchanged.  Synchronises.
+ * Errors: INVALID_ARG, CAPTURE (no graph for M), STALE_GRAPH, CUDA,
+ * DEVICE_TIMEOUT.
+ */
+frt_status frt_ffn_graph_profile(frt_ffn_plan_t plan, int M, int n_replays, float *kernel_us, int *n_kernels,
+                                 frt_stream_t stream);
+
+/*
  * Test/diagnostic: run layer `layer` alone on residual_in (+ hidden_in if not
  * NULL) and copy its intermediates to caller device buffers (each may be
  * NULL): r_prime [M, d] BF16, q_x [M, d] E4M3, gu [M, 2ff] BF16 (g then u),

@@ -39,6 +39,7 @@ SIGNATURES = {
     "frt_ffn_forward": (_I, [_P, _P, _P, _P, _I, _P]),
     "frt_ffn_graph_capture": (_I, [_P, _P, _P, _P, _I, _P]),
     "frt_ffn_graph_replay": (_I, [_P, _I, _P]),
+    "frt_ffn_graph_profile": (_I, [_P, _I, _I, _FP, ctypes.POINTER(ctypes.c_int), _P]),
     "frt_ffn_graph_autotune": (_I, [_P, _P, _P, _P, _I, _I, _I, ctypes.POINTER(ctypes.c_float),
                                    ctypes.POINTER(ctypes.c_int), _P]),
     "frt_ffn_debug_trace": (_I, [_P, _I, _P, _P, _I, _P, _P, _P, _P, _P, _P]),
@@ -191,6 +192,14 @@ def frt_ffn_graph_autotune(plan, residual_in, hidden_in, out, M, n_tries, n_repl
     _check(lib().frt_ffn_graph_autotune(plan, residual_in, hidden_in, out, M, n_tries, n_replays,
                                         ctypes.byref(best), ctypes.byref(tactic), stream))
     return best.value, tactic.value
+
+
+def frt_ffn_graph_profile(plan, M, n_replays, n_slots, stream) -> list[float]:
+    """Per-launch shares (us) of a replay of the graph held for M (median of n_replays)."""
+    buf = (ctypes.c_float * n_slots)()
+    n = ctypes.c_int(0)
+    _check(lib().frt_ffn_graph_profile(plan, M, n_replays, buf, ctypes.byref(n), stream))
+    return [float(buf[i]) for i in range(n.value)]
 
 
 def frt_ffn_debug_trace(plan, layer, residual_in, hidden_in, M, r_prime, q_x, gu, q_h, out, stream) -> None:

@@ -82,6 +82,8 @@ struct GraphEntry {
     cudaGraph_t graph = nullptr;
     cudaGraphExec_t exec = nullptr;
     uint64_t version = 0;
+    const void *r = nullptr, *h = nullptr;  // the buffers baked into the graph
+    void *out = nullptr;
 };
 
 }  // namespace
@@ -118,6 +120,10 @@ struct frt_ffn_plan {
     // buffer of mod_rows rows of [scale | shift | gate], each d wide, BF16
     std::vector<const uint16_t *> mod;
     int mod_rows = 0;
+    // profiling (frt_ffn_graph_profile): while set, launches carry a pointer
+    // to their pair of %globaltimer stamps, [layer][step][2]
+    bool profiling = false;
+    unsigned long long *stamps = nullptr;
 };
 
 namespace {
@@ -218,6 +224,11 @@ NormMod norm_mod(const frt_ffn_plan *P, int l) {
     return m;
 }
 
+// Layer l's step s stamp pair while profiling, else null.
+unsigned long long *stamp_of(const frt_ffn_plan *P, int l, int s) {
+    return P->profiling ? P->stamps + 2 * ((size_t)3 * l + s) : nullptr;
+}
+
 // Gate/up GEMM of layer l with the gated epilogue (q_h, or its amax).
 frt_status setup_gate_up(frt_ffn_plan *P, GemmLaunch &g, int l, int M, int epi) {
     frt_status st = setup_gemm(P, g, 0, l, M);
@@ -262,13 +273,16 @@ frt_status run_layer(frt_ffn_plan *P, int l, const void *in, const void *hid, vo
     const float inv_sx = 1.0f / s_x, inv_sh = 1.0f / s_h;
     void *rp = hid ? (void *)P->rprime : nullptr;
     const bool pdl = P->pdl;
+    NormMod nm = norm_mod(P, l);
+    nm.stamp = stamp_of(P, l, 0);
     CK(launch_norm_quant(in, hid, P->w_norm + (size_t)l * d, M, d, RMS_EPS, inv_sx, rp, P->qx, nullptr, false, s,
-                         pdl, norm_mod(P, l)));
+                         pdl, nm));
     GemmLaunch g;
     frt_status st = setup_gate_up(P, g, l, M, EPI_GATED);
     if (st != FRT_OK)
         return st;
     g.p.dbg_gu = static_cast<uint16_t *>(trace_gu);
+    g.p.stamp = stamp_of(P, l, 1);
     CK(launch_gemm(g, s, pdl));
     if (trace_qx)
         CK(cudaMemcpyAsync(trace_qx, P->qx, (size_t)M * d, cudaMemcpyDeviceToDevice, s));
@@ -281,6 +295,7 @@ frt_status run_layer(frt_ffn_plan *P, int l, const void *in, const void *hid, vo
     st = setup_down(P, g2, l, M, hid ? (const void *)P->rprime : in, out);
     if (st != FRT_OK)
         return st;
+    g2.p.stamp = stamp_of(P, l, 2);
     CK(launch_gemm(g2, s, pdl));
     (void)inv_sh;
     return FRT_OK;
@@ -328,7 +343,7 @@ void free_plan(frt_ffn_plan *P) {
         if (kv.second.graph) cudaGraphDestroy(kv.second.graph);
     }
     void *ptrs[] = {P->w_gu, P->w_down, P->w_norm, P->rbuf[0], P->rbuf[1], P->rprime, P->qx,
-                    P->qh,   P->ws,     P->counters, P->amax, P->err,     P->tmap_dev};
+                    P->qh,   P->ws,     P->counters, P->amax, P->err,     P->tmap_dev, P->stamps};
     for (void *p : ptrs)
         if (p) cudaFree(p);
     delete P;
@@ -397,6 +412,7 @@ FRT_API frt_status frt_ffn_plan_create(int d, int ff, int act, int M_max, int n_
         {(void **)&P->amax, 2 * 4},
         {(void **)&P->err, 4},
         {(void **)&P->tmap_dev, TMAP_SLOTS * sizeof(CUtensorMap)},
+        {(void **)&P->stamps, L * 3 * 2 * sizeof(unsigned long long)},
     };
     for (auto &a : allocs) {
         cudaError_t e = cudaMalloc(a.p, a.bytes);
@@ -697,6 +713,9 @@ frt_status capture_one(frt_ffn_plan *P, const void *residual_in, const void *hid
     ge.graph = graph;
     ge.exec = exec;
     ge.version = P->version;
+    ge.r = residual_in;
+    ge.h = hidden_in;
+    ge.out = out;
     return FRT_OK;
 }
 
@@ -828,6 +847,62 @@ FRT_API frt_status frt_ffn_graph_replay(frt_ffn_plan_t P, int M, frt_stream_t st
         return fail(FRT_ERR_STALE_GRAPH, "scales or weights changed since the graph for M=%d was captured", M);
     CK(cudaGraphLaunch(it->second.exec, static_cast<cudaStream_t>(stream)));
     return FRT_OK;
+}
+
+FRT_API frt_status frt_ffn_graph_profile(frt_ffn_plan_t P, int M, int n_replays, float *kernel_us, int *n_kernels,
+                                         frt_stream_t stream) {
+    if (!P)
+        return fail(FRT_ERR_INVALID_ARG, "null plan");
+    if (!kernel_us || n_replays < 1 || n_replays > 10000)
+        return fail(FRT_ERR_INVALID_ARG, "need kernel_us and 1 <= n_replays <= 10000");
+    auto it = P->graphs.find(M);
+    if (it == P->graphs.end())
+        return fail(FRT_ERR_CAPTURE, "no graph captured for M=%d", M);
+    if (it->second.version != P->version)
+        return fail(FRT_ERR_STALE_GRAPH, "scales or weights changed since the graph for M=%d was captured", M);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const GraphEntry base = it->second;
+    frt_status st = capture_checks(P, base.r, base.h, base.out, M, s);
+    if (st != FRT_OK)
+        return st;
+    // the same forward, captured again with every launch stamping its pair
+    GraphEntry ge;
+    P->profiling = true;
+    st = capture_one(P, base.r, base.h, base.out, M, s, ge);
+    P->profiling = false;
+    if (st != FRT_OK)
+        return st;
+    const int nk = 3 * P->L;
+    std::vector<unsigned long long> h(2 * (size_t)nk);
+    std::vector<std::vector<float>> dur(nk);
+    cudaError_t e = cudaSuccess;
+    for (int i = 0; i < n_replays && e == cudaSuccess; ++i) {
+        if ((e = cudaMemsetAsync(P->stamps, 0, h.size() * sizeof(unsigned long long), s)) != cudaSuccess) break;
+        if ((e = cudaGraphLaunch(ge.exec, s)) != cudaSuccess) break;
+        if ((e = cudaMemcpyAsync(h.data(), P->stamps, h.size() * sizeof(unsigned long long), cudaMemcpyDeviceToHost,
+                                 s)) != cudaSuccess) break;
+        if ((e = cudaStreamSynchronize(s)) != cudaSuccess) break;
+        // launch k owns the time from when it started, or its predecessor
+        // ended if later, to its own end: the stack's span split with no
+        // overlap between consecutive (programmatically overlapped) kernels
+        unsigned long long prev_end = 0;
+        for (int k = 0; k < nk; ++k) {
+            const unsigned long long t0 = ~h[2 * k], t1 = h[2 * k + 1];
+            const unsigned long long from = std::max(t0, prev_end);
+            dur[k].push_back(t1 > from ? (float)(t1 - from) * 1e-3f : 0.0f);
+            prev_end = std::max(prev_end, t1);
+        }
+    }
+    destroy_graph(ge);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "profiling replays");
+    for (int k = 0; k < nk; ++k) {
+        std::sort(dur[k].begin(), dur[k].end());
+        kernel_us[k] = dur[k][dur[k].size() / 2];
+    }
+    if (n_kernels)
+        *n_kernels = nk;
+    return frt_ffn_device_status(P, stream);
 }
 
 FRT_API frt_status frt_ffn_debug_trace(frt_ffn_plan_t P, int layer, const void *residual_in, const void *hidden_in,

@@ -51,6 +51,8 @@ struct GemmParams {
     int ldgate;             //   at gate[m * ldgate + n] (0: one row for all tokens); null: no gate
     int *err;               // device error word
     int stall_test;         // test hook: the MMA issuer first waits on a phase nothing completes
+    unsigned long long *stamp;  // profiling (null: off): [0] = max of ~t over the CTAs' starts (so ~[0] is
+                                //   the first start), [1] = max of t over their ends, t = %globaltimer ns
     // gated epilogues
     int act;                // Act
     int ff;                 // hidden width (feature count of q_h)
@@ -125,6 +127,7 @@ cudaError_t launch_e4m3_sweep(uint32_t start, size_t n, uint8_t *q, cudaStream_t
 struct NormMod {
     const uint16_t *p = nullptr;
     int stride = 0;
+    unsigned long long *stamp = nullptr;  // profiling: see GemmParams::stamp
 };
 cudaError_t launch_norm_quant(const void *r, const void *h, const void *w, int M, int d, float eps, float inv_s,
                               void *rprime, uint8_t *qx, unsigned *amax_word, bool measure, cudaStream_t s,

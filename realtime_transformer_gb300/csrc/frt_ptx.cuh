@@ -26,6 +26,16 @@ __device__ __forceinline__ uint64_t globaltimer() {
     return t;
 }
 
+// Profiling stamps of one launch (see GemmParams::stamp): both slots are
+// combined with atomicMax, the start slot on the complement of the time, so
+// that one memset to zero re-arms them.
+__device__ __forceinline__ void stamp_start(unsigned long long *st) {
+    atomicMax(st, ~(unsigned long long)globaltimer());
+}
+__device__ __forceinline__ void stamp_end(unsigned long long *st) {
+    atomicMax(st + 1, (unsigned long long)globaltimer());
+}
+
 // ---------------------------------------------------------------- mbarrier --
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

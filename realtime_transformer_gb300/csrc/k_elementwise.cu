@@ -197,10 +197,10 @@ __global__ void k_quant_gu_interleave(const uint16_t *__restrict__ gate, const u
 // values stay in registers for pass 2.  VPT == 0: any d, a strided loop that
 // re-reads r (and h) in pass 2.
 template <bool MEASURE, int WPR, int VPT, bool ADA>
-__global__ void __launch_bounds__(256) k_norm_quant(const uint16_t *__restrict__ r, const uint16_t *__restrict__ h,
-                                                    const uint16_t *__restrict__ w, int M, int d, float eps,
-                                                    float inv_s, uint16_t *__restrict__ rprime,
-                                                    uint8_t *__restrict__ qx, unsigned *amax_word, NormMod mod) {
+__device__ __forceinline__ void norm_body(const uint16_t *__restrict__ r, const uint16_t *__restrict__ h,
+                                          const uint16_t *__restrict__ w, int M, int d, float eps, float inv_s,
+                                          uint16_t *__restrict__ rprime, uint8_t *__restrict__ qx,
+                                          unsigned *amax_word, const NormMod &mod) {
     // Let the dependent GEMM launch (and stream its weights) right away; it
     // waits for this grid, and this grid waits for its own predecessor
     // before it can complete, so ordering is preserved.
@@ -383,6 +383,23 @@ __global__ void __launch_bounds__(256) k_norm_quant(const uint16_t *__restrict__
             if (lane == 0)
                 atomic_amax(amax_word, amax);
         }
+    }
+}
+
+// Every thread of a CTA passes the same barriers inside the body (rows past
+// M leave only after them), then the stamp's barrier here.
+template <bool MEASURE, int WPR, int VPT, bool ADA>
+__global__ void __launch_bounds__(256) k_norm_quant(const uint16_t *__restrict__ r, const uint16_t *__restrict__ h,
+                                                    const uint16_t *__restrict__ w, int M, int d, float eps,
+                                                    float inv_s, uint16_t *__restrict__ rprime,
+                                                    uint8_t *__restrict__ qx, unsigned *amax_word, NormMod mod) {
+    if (mod.stamp && threadIdx.x == 0)
+        stamp_start(mod.stamp);
+    norm_body<MEASURE, WPR, VPT, ADA>(r, h, w, M, d, eps, inv_s, rprime, qx, amax_word, mod);
+    if (mod.stamp) {
+        __syncthreads();
+        if (threadIdx.x == 0)
+            stamp_end(mod.stamp);
     }
 }
 

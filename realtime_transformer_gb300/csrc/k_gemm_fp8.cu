@@ -1336,6 +1336,8 @@ __global__ void __launch_bounds__(NTHREADS, SWAP ? 2 : 1)
     k_gemm_fp8(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmQ,
                const __grid_constant__ GemmParams p) {
     using C = Cfg<BN, SWAP, PAIR>;
+    if (p.stamp && threadIdx.x == 0)
+        stamp_start(p.stamp);
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *sP = smem;
@@ -1455,6 +1457,8 @@ __global__ void __launch_bounds__(NTHREADS, SWAP ? 2 : 1)
         else
             tmem_dealloc(tmem_base, C::TMEM_COLS);
     }
+    if (p.stamp && threadIdx.x == 0)
+        stamp_end(p.stamp);
 }
 
 template <int BN, bool SWAP, bool PAIR = false, int ROLE = ROLE_ANY>

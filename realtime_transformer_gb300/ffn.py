@@ -163,6 +163,11 @@ class FFNPlan:
     def graph_replay(self, M: int, stream=None):
         N.frt_ffn_graph_replay(self.handle, M, _stream(stream))
 
+    def graph_profile(self, M: int, n_replays: int = 20, stream=None):
+        """Per-launch shares in microseconds of a replay of the graph held for
+        M: launch 3 l + s is layer l's step s (norm, gate/up, down)."""
+        return N.frt_ffn_graph_profile(self.handle, M, n_replays, 3 * self.n_layers, _stream(stream))
+
     def device_status(self, stream=None):
         N.frt_ffn_device_status(self.handle, _stream(stream))
 

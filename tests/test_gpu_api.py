@@ -147,3 +147,46 @@ def test_calibration_cache_hit_and_miss(tmp_path):
     assert len(os.listdir(tmp_path)) == 2
     for p in (a, b, c):
         p.close()
+
+
+def test_graph_profile_splits_the_replay_without_changing_the_graph():
+    """The profiling replays stamp every launch: the per-launch shares are
+    positive and sum to at most the replay's span, and the graph held for M
+    still computes the same output afterwards."""
+    wl = synthetic.WORKLOADS["vla_action_expert"].with_(L=3)
+    dev = torch.device("cuda")
+    plan = FFNPlan(wl.d, wl.ff, wl.act, wl.M, wl.L)
+    for l in range(wl.L):
+        w = synthetic.layer_weights(wl, l, device=dev)
+        plan.load_weights(l, w["w_norm"], w["w_gate"], w["w_up"], w["w_down"], digest=False)
+    plan.set_scales([0.02] * wl.L, [0.01] * wl.L)
+    r, h = synthetic.inputs(wl, device=dev)
+    out = torch.empty_like(r)
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        plan.graph_capture(r, h, out, s)
+        plan.graph_replay(wl.M, s)
+    s.synchronize()
+    first = out.clone()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        e0.record(s)
+        for _ in range(10):
+            plan.graph_replay(wl.M, s)
+        e1.record(s)
+    s.synchronize()
+    replay_us = e0.elapsed_time(e1) * 1000.0 / 10
+    shares = plan.graph_profile(wl.M, n_replays=10, stream=s)
+    assert len(shares) == 3 * wl.L
+    assert all(x > 0 for x in shares), shares
+    assert sum(shares) <= 1.5 * replay_us, (sum(shares), replay_us)
+    out.zero_()
+    with torch.cuda.stream(s):
+        plan.graph_replay(wl.M, s)
+    s.synchronize()
+    assert torch.equal(out, first)
+    with pytest.raises(N.FrtError) as ei:
+        plan.graph_profile(7, stream=s)
+    assert ei.value.name == "FRT_ERR_CAPTURE"
+    plan.close()
