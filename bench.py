@@ -43,8 +43,10 @@ CLOCK_FIELDS = ["timestamp", "clocks.sm", "clocks.max.sm", "power.draw", "clocks
                 "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
                 "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
 STEP_NAMES = ["norm_quant", "gemm_gate_up_act", "gemm_down"]
-KERNEL_SOURCES = {"norm_quant": ["k_elementwise.cu"], "gemm_gate_up_act": ["k_gemm_fp8.cu", "frt_ptx.cuh"],
-                  "gemm_down": ["k_gemm_fp8.cu", "frt_ptx.cuh"]}
+KERNEL_SOURCES = {"norm_quant": ["k_elementwise.cu", "frt_ptx.cuh"],
+                  "gemm_gate_up_act": ["k_gemm_fp8.cu", "frt_ptx.cuh", "frt_epi.cuh"],
+                  "gemm_down": ["k_gemm_fp8.cu", "frt_ptx.cuh", "frt_epi.cuh"],
+                  "ffn_stack": ["k_stack_fp8.cu", "frt_ptx.cuh", "frt_epi.cuh"]}
 
 
 # ----------------------------------------------------------------- helpers --

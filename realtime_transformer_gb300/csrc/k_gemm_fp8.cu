@@ -37,6 +37,7 @@
 #include <algorithm>
 #include <cstdlib>
 
+#include "frt_epi.cuh"
 #include "frt_internal.h"
 #include "frt_ptx.cuh"
 
@@ -133,12 +134,6 @@ __device__ __forceinline__ Unit decode(const GemmParams &p, int u) {
     w.kb0 = w.split * p.kb_per_split;
     w.kb1 = min(p.k_blocks, w.kb0 + p.kb_per_split);
     return w;
-}
-
-__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-__device__ __forceinline__ uint32_t bf16_bits(float x) {
-    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x));
 }
 
 // ------------------------------------------------------------ producer --
@@ -465,58 +460,6 @@ __device__ __forceinline__ void store_chunk(const GemmParams &p, const Unit &w, 
 // (64 gate rows, then the 64 up rows of the same features), so every tile
 // holds matching gate and up rows.  g and u are rounded to BF16 (where the
 // unfused method stores them), then a = act(g) * u and q_h = E4M3(a / s_h).
-
-__device__ __forceinline__ float round_bf16(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
-
-__device__ __forceinline__ float ex2_approx(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-__device__ __forceinline__ float rcp_approx(float x) {
-    float y;
-    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-// GELU, tanh form: 0.5 g (1 + tanh(y)), y = sqrt(2/pi) (g + 0.044715 g^3).
-// Because 1 + tanh(y) = 2 / (1 + exp(-2y)), this equals g / (1 + exp(-2y)),
-// and exp(-2y) = 2^(g (c1 + c2 g^2)) with c1 = -2 sqrt(2/pi) log2(e),
-// c2 = 0.044715 c1: one base-2 exponential and one reciprocal (the hardware
-// approximations, a few ulp), free of branches and of the cancellation in
-// 1 + tanh(y) for negative y; the E4M3 code of the result keeps 3 bits.  An
-// overflowing exponential gives g * 0 = -0 for very negative g, an
-// underflowing one gives g.
-__device__ __forceinline__ float gelu_tanh(float g) {
-    const float c1 = -2.3022081981f;  // -2 * 0.7978845608 * 1.4426950409
-    const float c2 = -0.1029432396f;  // 0.044715 * c1
-    const float t = __fmul_rn(g, __fadd_rn(c1, __fmul_rn(c2, __fmul_rn(g, g))));
-    return __fmul_rn(g, rcp_approx(__fadd_rn(1.0f, ex2_approx(t))));
-}
-// SiLU: g / (1 + exp(-g)) = g / (1 + 2^(-g log2 e)), same approximations.
-__device__ __forceinline__ float silu(float g) {
-    const float t = __fmul_rn(g, -1.4426950409f);
-    return __fmul_rn(g, rcp_approx(__fadd_rn(1.0f, ex2_approx(t))));
-}
-
-// a[j] = act(g[j]) * u[j] over a run of N elements, the activation chosen
-// once for the run so the N chains interleave.
-template <int N>
-__device__ __forceinline__ void gated_run(int act, const float *g, const float *u, float *a) {
-    if (act == ACT_SWIGLU) {
-#pragma unroll
-        for (int j = 0; j < N; ++j)
-            a[j] = __fmul_rn(silu(g[j]), u[j]);
-    } else {
-#pragma unroll
-        for (int j = 0; j < N; ++j)
-            a[j] = __fmul_rn(gelu_tanh(g[j]), u[j]);
-    }
-}
-
-__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
-    return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
-}
 
 __device__ __forceinline__ void dbg_store_gu(const GemmParams &p, int m, int f, bool up, float val) {
     if (p.dbg_gu)
