@@ -218,14 +218,46 @@ frt_status frt_ffn_graph_autotune(frt_ffn_plan_t plan, const void *residual_in, 
  * that overlap (programmatic dependent launch) do not overlap, and they sum
  * to at most the replay's span.  Launch k = 3 l + s for layer l and step s
  * (0 norm + quantise, 1 gate/up GEMM with the gated activation, 2 down GEMM
- * with the residual); *n_kernels (may be NULL) receives how many were written
- * (kernel_us must hold 3 n_layers floats).  The profiling graph is freed
+ * with the residual) -- or, where the forward for M is the one persistent
+ * stack launch (frt_ffn_uses_stack_kernel), that launch alone (k = 0);
+ * *n_kernels (may be NULL) receives how many were written (kernel_us must
+ * hold 3 n_layers floats).  The profiling graph is freed
  * before returning; the graph held for M is unchanged.  Synchronises.
  * Errors: INVALID_ARG, CAPTURE (no graph for M), STALE_GRAPH, CUDA,
  * DEVICE_TIMEOUT.
  */
 frt_status frt_ffn_graph_profile(frt_ffn_plan_t plan, int M, int n_replays, float *kernel_us, int *n_kernels,
                                  frt_stream_t stream);
+
+/*
+ * 1 if the forward for M tokens runs as one persistent kernel over the whole
+ * stack, else 0 (then three launches per layer).  That kernel takes at most
+ * 64 tokens when d is a multiple of 256 up to 2048, ff a multiple of 128, the
+ * norm unmodulated (no frt_ffn_set_modulation), and its (ff/128) x (d/256)
+ * CTAs -- clusters of d/256, one CTA per SM -- fit on the GPU at once;
+ * FRT_FFN_STACK=0 in the environment at plan creation turns it off.  It
+ * computes the same steps with a different fp32 summation order (the
+ * gate/up sum in four K-slices, the down sum in ff/128 K-slices), so its
+ * results equal the per-layer kernels' within rounding, not bit for bit.
+ */
+int frt_ffn_uses_stack_kernel(frt_ffn_plan_t plan, int M);
+
+/*
+ * Test/diagnostic: the forward through the persistent stack kernel
+ * (frt_ffn_uses_stack_kernel(plan, M) must be 1) with optional per-layer
+ * inputs and dumps, all device buffers, each may be NULL: q_x_in [L][M][d]
+ * E4M3 -- layer l's GEMMs read these codes instead of their own step A1
+ * result (which is still computed and dumped), so that another
+ * implementation's codes can feed the kernel at every layer; dumps q_x
+ * [L][M][d] E4M3, gu [L][M][2ff] BF16 (g then u, the sums rounded to BF16
+ * before the activation), q_h [L][M][ff] E4M3 and res [L][M][d] BF16 (each
+ * layer's input r', after the hidden add at layer 0).  out as
+ * frt_ffn_forward.  Errors: as frt_ffn_forward; UNSUPPORTED when the stack
+ * kernel does not take M.
+ */
+frt_status frt_ffn_debug_stack(frt_ffn_plan_t plan, const void *residual_in, const void *hidden_in, void *out,
+                               int M, const void *q_x_in, void *q_x, void *gu, void *q_h, void *res,
+                               frt_stream_t stream);
 
 /*
  * Test/diagnostic: run layer `layer` alone on residual_in (+ hidden_in if not

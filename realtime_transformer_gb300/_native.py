@@ -45,6 +45,8 @@ SIGNATURES = {
     "frt_ffn_debug_trace": (_I, [_P, _I, _P, _P, _I, _P, _P, _P, _P, _P, _P]),
     "frt_ffn_debug_trace_qx": (_I, [_P, _I, _P, _P, _I, _P, _P, _P, _P]),
     "frt_ffn_debug_weights": (_I, [_P, _I, _P, _P, _P]),
+    "frt_ffn_uses_stack_kernel": (_I, [_P, _I]),
+    "frt_ffn_debug_stack": (_I, [_P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _P]),
     "frt_debug_e4m3_encode_range": (_I, [ctypes.c_uint, ctypes.c_ulonglong, _P, _P]),
     "frt_ffn_device_status": (_I, [_P, _P]),
     "frt_ffn_debug_stall": (_I, [_P, _P]),
@@ -208,6 +210,14 @@ def frt_ffn_debug_trace(plan, layer, residual_in, hidden_in, M, r_prime, q_x, gu
 
 def frt_ffn_debug_trace_qx(plan, layer, r_prime, q_x, M, gu, q_h, out, stream) -> None:
     _check(lib().frt_ffn_debug_trace_qx(plan, layer, r_prime, q_x, M, gu, q_h, out, stream))
+
+
+def frt_ffn_uses_stack_kernel(plan, M) -> bool:
+    return bool(lib().frt_ffn_uses_stack_kernel(plan, M))
+
+
+def frt_ffn_debug_stack(plan, r, h, out, M, q_x_in, q_x, gu, q_h, res, stream) -> None:
+    _check(lib().frt_ffn_debug_stack(plan, r, h, out, M, q_x_in, q_x, gu, q_h, res, stream))
 
 
 def frt_ffn_debug_weights(plan, layer, w_gu, w_down, stream) -> None:

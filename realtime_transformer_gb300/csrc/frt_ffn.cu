@@ -124,6 +124,14 @@ struct frt_ffn_plan {
     // to their pair of %globaltimer stamps, [layer][step][2]
     bool profiling = false;
     unsigned long long *stamps = nullptr;
+    // persistent stack kernel (k_stack_fp8.cu) for at most 64 tokens: its
+    // exchange buffers (allocated when the shape allows it), per-layer
+    // scalars, and whether it is used (FRT_FFN_STACK=0 disables it)
+    bool stack_on = false;
+    uint16_t *st_R = nullptr;
+    float *st_SS = nullptr, *st_P = nullptr;
+    int *st_cnt = nullptr;
+    float4 *st_scal = nullptr;
 };
 
 namespace {
@@ -224,6 +232,43 @@ NormMod norm_mod(const frt_ffn_plan *P, int l) {
     return m;
 }
 
+// The persistent stack kernel's launch for M tokens, if it takes this
+// forward (plain norm, shape and residency allowed).
+bool stack_launch_for(frt_ffn_plan *P, int M, StackParams &sp, size_t *smem) {
+    if (!P->stack_on || !P->mod.empty() || M > 64)
+        return false;
+    memset(&sp, 0, sizeof sp);
+    int grid = 0;
+    if (!plan_stack(sp, M, P->d, P->ff, P->num_sms, smem, &grid))
+        return false;
+    CUtensorMap dummy;
+    if (get_tmap(P, B_WGU, 256, &dummy, &sp.tm_gu) != FRT_OK || get_tmap(P, B_WDOWN, 256, &dummy, &sp.tm_d) != FRT_OK)
+        return false;
+    sp.w_norm = P->w_norm;
+    sp.scal = P->st_scal;
+    sp.R = P->st_R;
+    sp.SS = P->st_SS;
+    sp.P = P->st_P;
+    sp.cnt = P->st_cnt;
+    sp.err = P->err;
+    sp.L = P->L;
+    sp.act = P->act;
+    sp.eps = RMS_EPS;
+    return true;
+}
+
+// Per-layer scalars of the stack kernel, (1/s_x, s_x s_gu, 1/s_h, s_h s_down)
+// in fp32 as the per-layer launches compute them; uploaded whenever scales change.
+frt_status upload_stack_scalars(frt_ffn_plan *P) {
+    if (!P->st_scal || !P->scales_ok)
+        return FRT_OK;
+    std::vector<float4> h(P->L);
+    for (int l = 0; l < P->L; ++l)
+        h[l] = make_float4(1.0f / P->s_x[l], P->s_x[l] * P->s_gu[l], 1.0f / P->s_h[l], P->s_h[l] * P->s_d[l]);
+    CK(cudaMemcpy(P->st_scal, h.data(), sizeof(float4) * P->L, cudaMemcpyHostToDevice));
+    return FRT_OK;
+}
+
 // Layer l's step s stamp pair while profiling, else null.
 unsigned long long *stamp_of(const frt_ffn_plan *P, int l, int s) {
     return P->profiling ? P->stamps + 2 * ((size_t)3 * l + s) : nullptr;
@@ -302,6 +347,16 @@ frt_status run_layer(frt_ffn_plan *P, int l, const void *in, const void *hid, vo
 }
 
 frt_status run_stack(frt_ffn_plan *P, const void *r_in, const void *h_in, void *out, int M, cudaStream_t s) {
+    StackParams sp;
+    size_t smem = 0;
+    if (stack_launch_for(P, M, sp, &smem)) {
+        sp.r_in = static_cast<const uint16_t *>(r_in);
+        sp.h_in = static_cast<const uint16_t *>(h_in);
+        sp.out = static_cast<uint16_t *>(out);
+        sp.stamp = P->profiling ? P->stamps : nullptr;
+        CK(launch_stack(sp, smem, s, false));
+        return FRT_OK;
+    }
     const void *cur = r_in;
     for (int l = 0; l < P->L; ++l) {
         void *dst = (l == P->L - 1) ? out : (void *)P->rbuf[l & 1];
@@ -343,10 +398,45 @@ void free_plan(frt_ffn_plan *P) {
         if (kv.second.graph) cudaGraphDestroy(kv.second.graph);
     }
     void *ptrs[] = {P->w_gu, P->w_down, P->w_norm, P->rbuf[0], P->rbuf[1], P->rprime, P->qx,
-                    P->qh,   P->ws,     P->counters, P->amax, P->err,     P->tmap_dev, P->stamps};
+                    P->qh,   P->ws,     P->counters, P->amax, P->err,     P->tmap_dev, P->stamps,
+                    P->st_R, P->st_SS,  P->st_P,     P->st_cnt, P->st_scal};
     for (void *p : ptrs)
         if (p) cudaFree(p);
     delete P;
+}
+
+}  // namespace
+
+namespace {
+
+// The persistent stack kernel's buffers, when the plan's shape allows the
+// kernel at M_max tokens or fewer and all its clusters fit on the GPU at once.
+frt_status setup_stack(frt_ffn_plan *P) {
+    const char *e = getenv("FRT_FFN_STACK");
+    if (e && e[0] == '0')
+        return FRT_OK;
+    StackParams sp;
+    memset(&sp, 0, sizeof sp);
+    size_t smem = 0;
+    int grid = 0;
+    if (!plan_stack(sp, std::min(P->M_max, 64), P->d, P->ff, P->num_sms, &smem, &grid))
+        return FRT_OK;
+    if (stack_max_active_clusters(sp, smem) < sp.nC)
+        return FRT_OK;
+    const size_t S = sp.S, nC = sp.nC, D = P->d;
+    struct A { void **p; size_t bytes; } allocs[] = {
+        {(void **)&P->st_R, 2 * S * 64 * 256 * 2},
+        {(void **)&P->st_SS, 2 * (size_t)sp.n_own * 64 * 4},
+        {(void **)&P->st_P, 2 * nC * (D / 8) * 64 * 8 * 4},
+        {(void **)&P->st_cnt, (size_t)STACK_COUNTER_INTS * 4},
+        {(void **)&P->st_scal, (size_t)P->L * sizeof(float4)},
+    };
+    for (auto &a : allocs)
+        CK(cudaMalloc(a.p, a.bytes));
+    CK(cudaMemset(P->st_cnt, 0, (size_t)STACK_COUNTER_INTS * 4));
+    CK(cudaDeviceSynchronize());
+    P->stack_on = true;
+    return FRT_OK;
 }
 
 }  // namespace
@@ -434,8 +524,12 @@ FRT_API frt_status frt_ffn_plan_create(int d, int ff, int act, int M_max, int n_
         free_plan(P);
         return st;
     }
-    const frt_status st = build_tmaps(P);
+    frt_status st = build_tmaps(P);
     if (st != FRT_OK) {
+        free_plan(P);
+        return st;
+    }
+    if ((st = setup_stack(P)) != FRT_OK) {
         free_plan(P);
         return st;
     }
@@ -503,7 +597,7 @@ FRT_API frt_status frt_ffn_load_weights_ex(frt_ffn_plan_t P, int layer, const vo
     P->s_d[layer] = s_d;
     P->loaded[layer] = 1;
     P->version++;
-    return FRT_OK;
+    return upload_stack_scalars(P);
 }
 
 FRT_API frt_status frt_ffn_set_modulation(frt_ffn_plan_t P, const void *const *mod, int mod_rows) {
@@ -552,7 +646,7 @@ FRT_API frt_status frt_ffn_set_scales(frt_ffn_plan_t P, const float *s_x, const 
     P->s_h.assign(s_h, s_h + P->L);
     P->scales_ok = true;
     P->version++;
-    return FRT_OK;
+    return upload_stack_scalars(P);
 }
 
 FRT_API frt_status frt_ffn_calibrate(frt_ffn_plan_t P, const void *const *residual, const void *const *hidden,
@@ -649,7 +743,7 @@ FRT_API frt_status frt_ffn_calibrate(frt_ffn_plan_t P, const void *const *residu
     P->s_h = sh;
     P->scales_ok = true;
     P->version++;
-    return FRT_OK;
+    return upload_stack_scalars(P);
 }
 
 FRT_API frt_status frt_ffn_forward(frt_ffn_plan_t P, const void *residual_in, const void *hidden_in, void *out,
@@ -872,7 +966,9 @@ FRT_API frt_status frt_ffn_graph_profile(frt_ffn_plan_t P, int M, int n_replays,
     P->profiling = false;
     if (st != FRT_OK)
         return st;
-    const int nk = 3 * P->L;
+    StackParams sp_probe;
+    size_t smem_probe = 0;
+    const int nk = stack_launch_for(P, M, sp_probe, &smem_probe) ? 1 : 3 * P->L;
     std::vector<unsigned long long> h(2 * (size_t)nk);
     std::vector<std::vector<float>> dur(nk);
     cudaError_t e = cudaSuccess;
@@ -986,6 +1082,44 @@ FRT_API frt_status frt_debug_e4m3_encode_range(unsigned start, unsigned long lon
     return FRT_OK;
 }
 
+FRT_API frt_status frt_ffn_debug_stack(frt_ffn_plan_t P, const void *residual_in, const void *hidden_in, void *out,
+                                       int M, const void *q_x_in, void *q_x, void *gu, void *q_h, void *res,
+                                       frt_stream_t stream) {
+    frt_status st = check_io(P, residual_in, hidden_in, out, M);
+    if (st != FRT_OK)
+        return st;
+    if ((st = check_ready(P)) != FRT_OK)
+        return st;
+    if (M == 0)
+        return FRT_OK;
+    const void *ptrs[] = {q_x_in, q_x, gu, q_h, res};
+    for (const void *ptr : ptrs)
+        if (!aligned16(ptr))
+            return fail(FRT_ERR_INVALID_ARG, "debug buffers must be 16-byte aligned");
+    StackParams sp;
+    size_t smem = 0;
+    if (!stack_launch_for(P, M, sp, &smem))
+        return fail(FRT_ERR_UNSUPPORTED, "the persistent stack kernel does not take M=%d on this plan", M);
+    sp.r_in = static_cast<const uint16_t *>(residual_in);
+    sp.h_in = static_cast<const uint16_t *>(hidden_in);
+    sp.out = static_cast<uint16_t *>(out);
+    sp.dbg_qx_in = static_cast<const uint8_t *>(q_x_in);
+    sp.dbg_qx = static_cast<uint8_t *>(q_x);
+    sp.dbg_gu = static_cast<uint16_t *>(gu);
+    sp.dbg_qh = static_cast<uint8_t *>(q_h);
+    sp.dbg_res = static_cast<uint16_t *>(res);
+    CK(launch_stack(sp, smem, static_cast<cudaStream_t>(stream), true));
+    return FRT_OK;
+}
+
+FRT_API int frt_ffn_uses_stack_kernel(frt_ffn_plan_t P, int M) {
+    if (!P)
+        return 0;
+    StackParams sp;
+    size_t smem = 0;
+    return stack_launch_for(P, M, sp, &smem) ? 1 : 0;
+}
+
 FRT_API frt_status frt_ffn_debug_step(frt_ffn_plan_t P, int layer, int step, int M, frt_stream_t stream) {
     if (!P)
         return fail(FRT_ERR_INVALID_ARG, "null plan");
@@ -1028,6 +1162,8 @@ FRT_API frt_status frt_ffn_device_status(frt_ffn_plan_t P, frt_stream_t stream) 
     if (h) {
         // a launch that gave up may have left split-K counters mid-generation
         CK(cudaMemset(P->counters, 0, (size_t)(N_GEMM_SITES + 1) * SPLIT_COUNTERS * 4));
+        if (P->st_cnt)
+            CK(cudaMemset(P->st_cnt, 0, (size_t)STACK_COUNTER_INTS * 4));
         CK(cudaMemset(P->err, 0, 4));
         CK(cudaDeviceSynchronize());
         return fail(FRT_ERR_DEVICE_TIMEOUT, "a kernel gave up a bounded wait (code %d)", h);

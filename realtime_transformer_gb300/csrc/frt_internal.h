@@ -133,6 +133,43 @@ cudaError_t launch_norm_quant(const void *r, const void *h, const void *w, int M
                               void *rprime, uint8_t *qx, unsigned *amax_word, bool measure, cudaStream_t s,
                               bool pdl, NormMod mod = NormMod());
 
+// ------------------------------------------------- persistent stack kernel --
+// The whole FP8 FFN stack for at most 64 tokens in one launch (k_stack_fp8.cu):
+// ff / 128 clusters of d / 256 CTAs, one CTA per SM, all resident together.
+struct StackParams {
+    const CUtensorMap *tm_gu, *tm_d;  // weight maps (device copies), boxes of 128 bytes x 256 rows
+    const uint16_t *w_norm;           // [L][d] BF16
+    const float4 *scal;               // [L]: (1/s_x, s_x s_gu, 1/s_h, s_h s_down)
+    const uint16_t *r_in, *h_in;      // [M][d] BF16; h_in may be null (added before layer 0)
+    uint16_t *out;                    // [M][d] BF16 (may alias r_in)
+    uint16_t *R;                      // [2][d/256][64][256] BF16: the layer input, K-quarter major
+    float *SS;                        // [2][n_own * 64]: per owner and token, sum of squares of its columns
+    float *P;                         // [2][ff/128][d/8][64][8]: down partials per K-slice and column group
+    int *cnt;                         // monotonic counters (see k_stack_fp8.cu), zero between launches
+    int *err;                         // device error word
+    unsigned long long *stamp;        // profiling stamps (null: off)
+    // diagnostics (DEBUG instantiation): q_x injected per layer [L][M][d] (null: computed), and dumps
+    // of q_x [L][M][d], g/u [L][M][2ff] BF16, q_h [L][M][ff], each layer's input r' [L][M][d] BF16
+    const uint8_t *dbg_qx_in;
+    uint8_t *dbg_qx;
+    uint16_t *dbg_gu;
+    uint8_t *dbg_qh;
+    uint16_t *dbg_res;
+    int M, d, ff, L, act;
+    int S, nC, n_own;                 // cluster size d/256, clusters ff/128, column-group owners
+    uint32_t x_bytes;                 // size of the kernel's staging region
+    int res_groups;                   // most 8-column groups an owner holds
+    float eps;
+};
+constexpr int STACK_COUNTER_INTS = 32 * 10;  // residual, 8 N-tile and exit counters, 128 bytes apart
+// Fill the shape fields of p for M tokens; false if the stack kernel does not
+// take this shape.  *smem_bytes, *grid: the launch's dynamic shared memory and CTAs.
+bool plan_stack(StackParams &p, int M, int d, int ff, int num_sms, size_t *smem_bytes, int *grid);
+size_t smem_max_stack();
+// Clusters of the stack kernel that fit on the GPU at once (0 on error).
+int stack_max_active_clusters(const StackParams &p, size_t smem);
+cudaError_t launch_stack(const StackParams &p, size_t smem, cudaStream_t s, bool debug);
+
 // ---------------------------------------------------------------- NVFP4 --
 // Epilogues of the block-scaled FP4 GEMM (k_nvfp4.cu).
 enum F4Epi : int {

@@ -210,6 +210,32 @@ class FFNPlan:
                                  _ptr(out["gu"]), _ptr(out["q_h"]), _ptr(out["out"]), _stream(stream))
         return out
 
+    def uses_stack_kernel(self, M: int) -> bool:
+        """Whether the forward for M tokens is the one persistent stack kernel."""
+        return N.frt_ffn_uses_stack_kernel(self.handle, M)
+
+    def debug_stack(self, residual, hidden=None, q_x_in=None, stream=None):
+        """The forward through the persistent stack kernel with every layer's
+        intermediates dumped (diagnostics); q_x_in (uint8 [L, M, d]) replaces
+        each layer's own E4M3 codes of step A1 as the GEMMs' input."""
+        M, d, ff, L = residual.shape[0], self.d, self.ff, self.n_layers
+        dev = residual.device
+        o = {
+            "out": torch.empty((M, d), dtype=torch.bfloat16, device=dev),
+            "q_x": torch.empty((L, M, d), dtype=torch.uint8, device=dev),
+            "gu": torch.empty((L, M, 2 * ff), dtype=torch.bfloat16, device=dev),
+            "q_h": torch.empty((L, M, ff), dtype=torch.uint8, device=dev),
+            "res": torch.empty((L, M, d), dtype=torch.bfloat16, device=dev),
+        }
+        if q_x_in is not None and (q_x_in.dtype != torch.uint8 or tuple(q_x_in.shape) != (L, M, d)
+                                   or not q_x_in.is_contiguous()):
+            raise ValueError("q_x_in must be a contiguous uint8 [L, M, d] tensor")
+        N.frt_ffn_debug_stack(self.handle, _bf16(residual, (M, d), "residual"),
+                              _bf16(hidden, (M, d), "hidden") if hidden is not None else None, _ptr(o["out"]), M,
+                              _ptr(q_x_in) if q_x_in is not None else None, _ptr(o["q_x"]), _ptr(o["gu"]),
+                              _ptr(o["q_h"]), _ptr(o["res"]), _stream(stream))
+        return o
+
     def weights(self, layer, device="cuda", stream=None):
         """The plan's E4M3 weights of one layer as stored (diagnostics):
         w_gu [2ff, d] with gate and up rows interleaved in blocks of 64, and
