@@ -232,10 +232,11 @@ frt_status frt_ffn_graph_profile(frt_ffn_plan_t plan, int M, int n_replays, floa
 /*
  * 1 if the forward for M tokens runs as one persistent kernel over the whole
  * stack, else 0 (then three launches per layer).  That kernel takes at most
- * 64 tokens when d is a multiple of 256 up to 2048, ff a multiple of 128, the
+ * 64 tokens when it was asked for (FRT_FFN_STACK=1 in the environment at
+ * plan creation; off by default: on GB300 it measured slower than the
+ * per-layer kernels), d is 256, 512, 1024 or 2048, ff a multiple of 128, the
  * norm unmodulated (no frt_ffn_set_modulation), and its (ff/128) x (d/256)
- * CTAs -- clusters of d/256, one CTA per SM -- fit on the GPU at once;
- * FRT_FFN_STACK=0 in the environment at plan creation turns it off.  It
+ * CTAs -- clusters of d/256, one CTA per SM -- fit on the GPU at once.  It
  * computes the same steps with a different fp32 summation order (the
  * gate/up sum in four K-slices, the down sum in ff/128 K-slices), so its
  * results equal the per-layer kernels' within rounding, not bit for bit.
@@ -245,19 +246,24 @@ int frt_ffn_uses_stack_kernel(frt_ffn_plan_t plan, int M);
 /*
  * Test/diagnostic: the forward through the persistent stack kernel
  * (frt_ffn_uses_stack_kernel(plan, M) must be 1) with optional per-layer
- * inputs and dumps, all device buffers, each may be NULL: q_x_in [L][M][d]
- * E4M3 -- layer l's GEMMs read these codes instead of their own step A1
- * result (which is still computed and dumped), so that another
- * implementation's codes can feed the kernel at every layer; dumps q_x
+ * inputs and dumps, all device buffers, each may be NULL.  Inputs, so that
+ * another implementation's values can feed the kernel at every layer:
+ * q_x_in [L][M][d] E4M3 -- layer l's GEMMs read these codes instead of its
+ * own step A1 result (which is still computed and dumped); res_in [L][M][d]
+ * BF16 -- layer l >= 1 starts from res_in[l] (its norm's input and its
+ * residual) instead of layer l-1's output (row 0 unused).  Dumps: q_x
  * [L][M][d] E4M3, gu [L][M][2ff] BF16 (g then u, the sums rounded to BF16
- * before the activation), q_h [L][M][ff] E4M3 and res [L][M][d] BF16 (each
- * layer's input r', after the hidden add at layer 0).  out as
- * frt_ffn_forward.  Errors: as frt_ffn_forward; UNSUPPORTED when the stack
- * kernel does not take M.
+ * before the activation), q_h [L][M][ff] E4M3, layer_out [L][M][d] BF16 (each
+ * layer's computed output), times [CTAs][L][32] uint64 (%globaltimer
+ * nanoseconds at fixed points of each layer in each CTA: 0-12 and 16-25 the
+ * compute warps' phases, 13-15 the MMA issuer's waits; CTAs = (ff/128)
+ * (d/256)).
+ * out as frt_ffn_forward.  Errors: as frt_ffn_forward; UNSUPPORTED when the
+ * stack kernel does not take M.
  */
 frt_status frt_ffn_debug_stack(frt_ffn_plan_t plan, const void *residual_in, const void *hidden_in, void *out,
-                               int M, const void *q_x_in, void *q_x, void *gu, void *q_h, void *res,
-                               frt_stream_t stream);
+                               int M, const void *q_x_in, const void *res_in, void *q_x, void *gu, void *q_h,
+                               void *layer_out, void *times, frt_stream_t stream);
 
 /*
  * Test/diagnostic: run layer `layer` alone on residual_in (+ hidden_in if not

@@ -46,7 +46,7 @@ SIGNATURES = {
     "frt_ffn_debug_trace_qx": (_I, [_P, _I, _P, _P, _I, _P, _P, _P, _P]),
     "frt_ffn_debug_weights": (_I, [_P, _I, _P, _P, _P]),
     "frt_ffn_uses_stack_kernel": (_I, [_P, _I]),
-    "frt_ffn_debug_stack": (_I, [_P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _P]),
+    "frt_ffn_debug_stack": (_I, [_P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P]),
     "frt_debug_e4m3_encode_range": (_I, [ctypes.c_uint, ctypes.c_ulonglong, _P, _P]),
     "frt_ffn_device_status": (_I, [_P, _P]),
     "frt_ffn_debug_stall": (_I, [_P, _P]),
@@ -216,8 +216,8 @@ def frt_ffn_uses_stack_kernel(plan, M) -> bool:
     return bool(lib().frt_ffn_uses_stack_kernel(plan, M))
 
 
-def frt_ffn_debug_stack(plan, r, h, out, M, q_x_in, q_x, gu, q_h, res, stream) -> None:
-    _check(lib().frt_ffn_debug_stack(plan, r, h, out, M, q_x_in, q_x, gu, q_h, res, stream))
+def frt_ffn_debug_stack(plan, r, h, out, M, q_x_in, res_in, q_x, gu, q_h, layer_out, times, stream) -> None:
+    _check(lib().frt_ffn_debug_stack(plan, r, h, out, M, q_x_in, res_in, q_x, gu, q_h, layer_out, times, stream))
 
 
 def frt_ffn_debug_weights(plan, layer, w_gu, w_down, stream) -> None:

@@ -124,9 +124,9 @@ struct frt_ffn_plan {
     // to their pair of %globaltimer stamps, [layer][step][2]
     bool profiling = false;
     unsigned long long *stamps = nullptr;
-    // persistent stack kernel (k_stack_fp8.cu) for at most 64 tokens: its
-    // exchange buffers (allocated when the shape allows it), per-layer
-    // scalars, and whether it is used (FRT_FFN_STACK=0 disables it)
+    // persistent stack kernel (k_stack_fp8.cu) for at most 64 tokens, opt-in
+    // (FRT_FFN_STACK=1): its exchange buffers (allocated when the shape allows
+    // it), per-layer scalars, and whether it is used
     bool stack_on = false;
     uint16_t *st_R = nullptr;
     float *st_SS = nullptr, *st_P = nullptr;
@@ -409,11 +409,13 @@ void free_plan(frt_ffn_plan *P) {
 
 namespace {
 
-// The persistent stack kernel's buffers, when the plan's shape allows the
-// kernel at M_max tokens or fewer and all its clusters fit on the GPU at once.
+// The persistent stack kernel's buffers, when it is asked for (FRT_FFN_STACK=1
+// at plan creation: measured slower than the per-layer kernels on GB300, so
+// not the default), the plan's shape allows the kernel at M_max tokens or
+// fewer, and all its clusters fit on the GPU at once.
 frt_status setup_stack(frt_ffn_plan *P) {
     const char *e = getenv("FRT_FFN_STACK");
-    if (e && e[0] == '0')
+    if (!(e && e[0] == '1'))
         return FRT_OK;
     StackParams sp;
     memset(&sp, 0, sizeof sp);
@@ -1083,8 +1085,8 @@ FRT_API frt_status frt_debug_e4m3_encode_range(unsigned start, unsigned long lon
 }
 
 FRT_API frt_status frt_ffn_debug_stack(frt_ffn_plan_t P, const void *residual_in, const void *hidden_in, void *out,
-                                       int M, const void *q_x_in, void *q_x, void *gu, void *q_h, void *res,
-                                       frt_stream_t stream) {
+                                       int M, const void *q_x_in, const void *res_in, void *q_x, void *gu, void *q_h,
+                                       void *layer_out, void *times, frt_stream_t stream) {
     frt_status st = check_io(P, residual_in, hidden_in, out, M);
     if (st != FRT_OK)
         return st;
@@ -1092,7 +1094,7 @@ FRT_API frt_status frt_ffn_debug_stack(frt_ffn_plan_t P, const void *residual_in
         return st;
     if (M == 0)
         return FRT_OK;
-    const void *ptrs[] = {q_x_in, q_x, gu, q_h, res};
+    const void *ptrs[] = {q_x_in, res_in, q_x, gu, q_h, layer_out, times};
     for (const void *ptr : ptrs)
         if (!aligned16(ptr))
             return fail(FRT_ERR_INVALID_ARG, "debug buffers must be 16-byte aligned");
@@ -1104,11 +1106,15 @@ FRT_API frt_status frt_ffn_debug_stack(frt_ffn_plan_t P, const void *residual_in
     sp.h_in = static_cast<const uint16_t *>(hidden_in);
     sp.out = static_cast<uint16_t *>(out);
     sp.dbg_qx_in = static_cast<const uint8_t *>(q_x_in);
+    sp.dbg_res_in = static_cast<const uint16_t *>(res_in);
     sp.dbg_qx = static_cast<uint8_t *>(q_x);
     sp.dbg_gu = static_cast<uint16_t *>(gu);
     sp.dbg_qh = static_cast<uint8_t *>(q_h);
-    sp.dbg_res = static_cast<uint16_t *>(res);
-    CK(launch_stack(sp, smem, static_cast<cudaStream_t>(stream), true));
+    sp.dbg_out = static_cast<uint16_t *>(layer_out);
+    sp.dbg_t = static_cast<unsigned long long *>(times);
+    // the product instantiation when only the timeline is asked for
+    const bool dumps = q_x_in || res_in || q_x || gu || q_h || layer_out;
+    CK(launch_stack(sp, smem, static_cast<cudaStream_t>(stream), dumps));
     return FRT_OK;
 }
 

@@ -144,17 +144,20 @@ struct StackParams {
     uint16_t *out;                    // [M][d] BF16 (may alias r_in)
     uint16_t *R;                      // [2][d/256][64][256] BF16: the layer input, K-quarter major
     float *SS;                        // [2][n_own * 64]: per owner and token, sum of squares of its columns
-    float *P;                         // [2][ff/128][d/8][64][8]: down partials per K-slice and column group
+    float *P;                         // [2][d/8][ff/128][M][8]: down partials per column group and K-slice
     int *cnt;                         // monotonic counters (see k_stack_fp8.cu), zero between launches
     int *err;                         // device error word
     unsigned long long *stamp;        // profiling stamps (null: off)
-    // diagnostics (DEBUG instantiation): q_x injected per layer [L][M][d] (null: computed), and dumps
-    // of q_x [L][M][d], g/u [L][M][2ff] BF16, q_h [L][M][ff], each layer's input r' [L][M][d] BF16
+    // diagnostics (DEBUG instantiation): injected per layer (null: computed) q_x [L][M][d] and the
+    // input residual of layers >= 1 [L][M][d] BF16; dumps of q_x [L][M][d], g/u [L][M][2ff] BF16,
+    // q_h [L][M][ff] and each layer's output [L][M][d] BF16
     const uint8_t *dbg_qx_in;
+    const uint16_t *dbg_res_in;
     uint8_t *dbg_qx;
     uint16_t *dbg_gu;
     uint8_t *dbg_qh;
-    uint16_t *dbg_res;
+    uint16_t *dbg_out;
+    unsigned long long *dbg_t;        // per-CTA timeline [CTAs][L][16] (%globaltimer)
     int M, d, ff, L, act;
     int S, nC, n_own;                 // cluster size d/256, clusters ff/128, column-group owners
     uint32_t x_bytes;                 // size of the kernel's staging region

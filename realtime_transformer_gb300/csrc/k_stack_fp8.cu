@@ -47,7 +47,9 @@ namespace frt {
 
 namespace {
 
-constexpr int ST_THREADS = 192;  // warps 0-3 compute (TMEM lane quarters), 4 TMA producer, 5 MMA issuer
+constexpr int ST_THREADS = 320;  // warps 0-7 compute (two per TMEM lane quarter), 8 TMA producer, 9 MMA issuer
+constexpr int ST_CT = 256;       // compute threads
+constexpr int W_PROD = 8, W_MMA = 9;
 constexpr int ST_ROWS = 64;      // token rows of the A operands (MMA M)
 constexpr int ST_KQ = 256;       // gate/up K per CTA
 constexpr int ST_FEAT = 128;     // features per cluster
@@ -73,6 +75,9 @@ __device__ __forceinline__ void fence_proxy_async_cluster() {
     asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
 }
 __device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
+// Each thread's own global writes ordered before the release that a thread
+// of its CTA makes after a CTA barrier.
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 __device__ __forceinline__ void red_release_gpu(int *p, int v) {
     asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
@@ -101,16 +106,16 @@ __device__ __forceinline__ bool wait_count(const int *c, int target, volatile in
     }
 }
 
-// The four compute warps: a named barrier over their 128 threads, and the
+// The eight compute warps: a named barrier over their 256 threads, and the
 // same barrier returning whether any of them passed `v` -- so that a failed
 // wait takes all of them out of the layer loop together.
-__device__ __forceinline__ void compute_sync() { named_bar_sync(1, 128); }
+__device__ __forceinline__ void compute_sync() { named_bar_sync(1, ST_CT); }
 __device__ __forceinline__ bool compute_sync_or(bool v) {
     uint32_t r;
     asm volatile(
         "{\n\t.reg .pred p, q;\n\t"
         "setp.ne.u32 p, %1, 0;\n\t"
-        "barrier.red.or.pred q, 1, 128, p;\n\t"
+        "barrier.red.or.pred q, 1, 256, p;\n\t"
         "selp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(r)
         : "r"((uint32_t)v)
@@ -135,6 +140,14 @@ __device__ __forceinline__ uint4 pack8_bf16(const float (&f)[8]) {
 // tile holds two 64-row interleave blocks, [gate 64 | up 64] each.
 __device__ __forceinline__ int gate_col(int f) { return (f >> 6) * 128 + (f & 63); }
 
+// Diagnostics: %globaltimer at point `k` of layer l in this CTA's timeline
+// ([CTAs][L][32], when dbg_t is set; either instantiation).
+#define ST_MARK(k)                                                                            \
+    do {                                                                                      \
+        if (p.dbg_t)                                                                          \
+            p.dbg_t[((size_t)blockIdx.x * L + l) * 32 + (k)] = globaltimer();                 \
+    } while (0)
+
 template <bool DEBUG>
 __global__ void __launch_bounds__(ST_THREADS, 1)
     k_stack_fp8(const __grid_constant__ StackParams p) {
@@ -153,17 +166,20 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
     const int G = k_own < p.n_own ? (ngrp - k_own + p.n_own - 1) / p.n_own : 0;  // groups this CTA owns
 
     // shared memory beyond the fixed tiles
-    const uint32_t rx_bytes = (uint32_t)((S - 1) * M * 2 * FPC * 4);
+    const int RS = 2 * FPC + 4;             // row stride (floats) of the exchange buffers: +16 B per row, so
+                                            // the 16 token rows of a warp fall in different banks
+    const uint32_t rx_bytes = (uint32_t)((S - 1) * M * RS * 4);
     uint8_t *X = smem + OFF_X;
-    float *RX = reinterpret_cast<float *>(X);                       // (c)-(d): (S-1) x [M][2 FPC]
-    float *XS = reinterpret_cast<float *>(X + rx_bytes);            // (c): (S-1) x [M][2 FPC]
+    float *RX = reinterpret_cast<float *>(X);                       // (c)-(d): (S-1) x [M][RS]
+    float *XS = reinterpret_cast<float *>(X + rx_bytes);            // (c): (S-1) x [M][RS]
     uint16_t *RST = reinterpret_cast<uint16_t *>(X + rx_bytes);     // (a): [M][256] BF16
     float *SST = reinterpret_cast<float *>(X + rx_bytes + (uint32_t)M * 512);  // (a): [n_own][Mp]
     float *OWN = reinterpret_cast<float *>(X);                      // (g): [G][nC][M][8]
     const uint32_t res_bytes = (uint32_t)p.res_groups * 64 * 16;
     uint4 *RES = reinterpret_cast<uint4 *>(smem + OFF_X + p.x_bytes);           // [res_groups][64]: kept r' of owned groups
     float *INV = reinterpret_cast<float *>(smem + OFF_X + p.x_bytes + res_bytes);  // [64]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_X + p.x_bytes + res_bytes + 256);
+    uint16_t *WN = reinterpret_cast<uint16_t *>(smem + OFF_X + p.x_bytes + res_bytes + 256);  // [2][256] norm weights
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_X + p.x_bytes + res_bytes + 256 + 1024);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + N_BARS);
     volatile int *abort_f = reinterpret_cast<volatile int *>(tmem_holder + 1);
     auto bar = [&](int b) { return smem_u32(&bars[b]); };
@@ -185,11 +201,11 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
         *abort_f = 0;
         fence_mbar_init();
     }
-    if (warp == 4 && lane == 0) {
+    if (warp == W_PROD && lane == 0) {
         prefetch_tmap(p.tm_gu);
         prefetch_tmap(p.tm_d);
     }
-    if (warp == 5) {
+    if (warp == W_MMA) {
         tmem_alloc(smem_u32(tmem_holder), 512);
         tmem_relinquish();
     }
@@ -213,7 +229,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
     uint32_t w_issued = 0;
     bool mma_issued = false;
 
-    if (warp == 4) {
+    if (warp == W_PROD) {
         // ------------------------------------------------ TMA producer --
         if (lane == 0) {
             const uint64_t pol = l2_policy_evict_first();
@@ -221,10 +237,13 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
                 const uint32_t par = (uint32_t)(l & 1);
                 if (l > 0 && !mbar_wait(bar(B_WEMPTY_GU), par ^ 1u, abort_f, err))
                     break;
-                mbar_arrive_expect_tx(bar(B_WFULL_GU), 2 * ST_NT * 128);
+                // the gate/up tile and this K-quarter of the layer's norm weights
+                mbar_arrive_expect_tx(bar(B_WFULL_GU), 2 * ST_NT * 128 + ST_KQ * 2);
                 const int row_gu = l * 2 * ff + ST_NT * c;
                 tma_load_2d(sbase + OFF_WGU, p.tm_gu, bar(B_WFULL_GU), ST_KQ * j, row_gu, pol);
                 tma_load_2d(sbase + OFF_WGU + ST_NT * 128, p.tm_gu, bar(B_WFULL_GU), ST_KQ * j + 128, row_gu, pol);
+                bulk_load(smem_u32(WN) + (par << 9), p.w_norm + (size_t)l * d + ST_KQ * j, ST_KQ * 2,
+                          bar(B_WFULL_GU));
                 w_issued |= 1u;
                 if (l > 0 && !mbar_wait(bar(B_WEMPTY_D), par ^ 1u, abort_f, err))
                     break;
@@ -233,14 +252,18 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
                 w_issued |= 2u;
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == W_MMA) {
         // -------------------------------------------------- MMA issuer --
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_e4m3_f32(ST_ROWS, ST_NT);
             for (int l = 0; l < L; ++l) {
                 const uint32_t par = (uint32_t)(l & 1);
-                if (!mbar_wait(bar(B_WFULL_GU), par, abort_f, err) || !mbar_wait(bar(B_AGU_READY), par, abort_f, err))
+                if (!mbar_wait(bar(B_WFULL_GU), par, abort_f, err))
                     break;
+                ST_MARK(13);
+                if (!mbar_wait(bar(B_AGU_READY), par, abort_f, err))
+                    break;
+                ST_MARK(14);
                 tc_fence_after();
                 fence_proxy_async_shared();
 #pragma unroll
@@ -256,6 +279,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
                 if (!mbar_wait(bar(B_WFULL_D), par, abort_f, err) ||
                     !mbar_wait_cluster(bar(B_AD_READY), par, abort_f, err))
                     break;
+                ST_MARK(15);
                 tc_fence_after();
                 fence_proxy_async_shared();
 #pragma unroll
@@ -268,10 +292,12 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
         }
     } else {
         // ---------------------------------------------- compute warps --
+        const int q4 = warp & 3;                         // TMEM lane quarter of this warp
+        const int hw = warp >> 2;                        // which half of the columns this warp takes
         const int i16 = lane & 15;
-        const int m_t = 16 * warp + i16;                 // this thread's token in the M = 64 TMEM layout
+        const int m_t = 16 * q4 + i16;                   // this thread's token in the M = 64 TMEM layout
         const bool row_ok = lane < 16 && m_t < M;
-        const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+        const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
         const float eps = p.eps;
 
         // Prologue: owners form layer 0's input r' = bf16(r + h) and publish it.
@@ -293,26 +319,28 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
                     const uint4 v = pack8_bf16(x);
                     RES[gi * 64 + m] = v;
                     *reinterpret_cast<uint4 *>(p.R + ((size_t)(g >> 5) * ST_ROWS + m) * ST_KQ + (g & 31) * 8) = v;
-                    if (DEBUG && p.dbg_res)
-                        *reinterpret_cast<uint4 *>(p.dbg_res + (size_t)m * d + 8 * g) = v;
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
                         ss = __fadd_rn(ss, __fmul_rn(x[e], x[e]));
                 }
                 p.SS[(size_t)k_own * Mp + m] = ss;   // parity 0
             }
-            __threadfence();
+            fence_acq_rel_gpu();
             compute_sync();
             if (tid == 0)
                 red_release_gpu(cnt_R, 1);
         }
 
+        float4 sc_next = p.scal[0];
         for (int l = 0; l < L; ++l) {
             const uint32_t par = (uint32_t)(l & 1);
-            const float4 sc = p.scal[l];  // (1/s_x, s_x s_gu, 1/s_h, s_h s_d)
+            const float4 sc = sc_next;    // (1/s_x, s_x s_gu, 1/s_h, s_h s_d); the next layer's load in flight
+            sc_next = p.scal[l + 1 < L ? l + 1 : l];
             // ---- (a) the layer input, normalised and quantised ----------
             if (tid == 0) {
+                ST_MARK(0);
                 bool w_ok = wait_count(cnt_R, p.n_own * (l + 1), abort_f, err);
+                ST_MARK(1);
                 if (w_ok) {
                     fence_proxy_async_global();
                     mbar_arrive_expect_tx(bar(B_ASTAGE), (uint32_t)(M * 512 + p.n_own * Mp * 4));
@@ -322,19 +350,45 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
                               bar(B_ASTAGE));
                 }
             }
-            if (compute_sync_or(!mbar_wait(bar(B_ASTAGE), par, abort_f, err)))
+            if (compute_sync_or(!mbar_wait(bar(B_ASTAGE), par, abort_f, err) ||
+                                !mbar_wait(bar(B_WFULL_GU), par, abort_f, err)))
                 break;
-            if (tid < M) {
+            if (tid == 0)
+                ST_MARK(2);
+            {
+                // four threads per token: owner partials k = part (mod 4), each
+                // in order, then (part 0 + part 1) + (part 2 + part 3) -- one
+                // fixed order, the same in every CTA
+                const int m = tid >> 2, part = tid & 3;
                 float s = 0.0f;
-                for (int k = 0; k < p.n_own; ++k)
-                    s = __fadd_rn(s, SST[k * Mp + tid]);
-                const float ms = __fdiv_rn(s, (float)d);
-                INV[tid] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+                if (m < M) {
+                    int k = part;
+                    for (; k + 28 < p.n_own; k += 32) {      // eight loads in flight, added in order
+                        float v[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            v[e] = SST[(k + 4 * e) * Mp + m];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            s = __fadd_rn(s, v[e]);
+                    }
+                    for (; k < p.n_own; k += 4)
+                        s = __fadd_rn(s, SST[k * Mp + m]);
+                }
+                const float o1 = __shfl_xor_sync(0xffffffffu, s, 1);
+                const float pair = (part & 1) ? __fadd_rn(o1, s) : __fadd_rn(s, o1);
+                const float o2 = __shfl_xor_sync(0xffffffffu, pair, 2);
+                if (part == 0 && m < M) {
+                    const float ms = __fdiv_rn(__fadd_rn(pair, o2), (float)d);
+                    INV[m] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+                }
             }
             compute_sync();
+            if (tid == 0)
+                ST_MARK(23);
             {
-                const uint16_t *wn = p.w_norm + (size_t)l * d + ST_KQ * j;
-                for (int t = tid; t < M * 16; t += 128) {
+                const uint16_t *wn = WN + (par << 8);
+                for (int t = tid; t < M * 16; t += ST_CT) {
                     const int m = t >> 4, ch = t & 15;
                     const float inv = INV[m];
                     float x[16], w[16];
@@ -342,8 +396,8 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
                     const uint4 *wv = reinterpret_cast<const uint4 *>(wn + 16 * ch);
                     unpack8_bf16(rv[0], *reinterpret_cast<float(*)[8]>(&x[0]));
                     unpack8_bf16(rv[1], *reinterpret_cast<float(*)[8]>(&x[8]));
-                    unpack8_bf16(__ldg(wv), *reinterpret_cast<float(*)[8]>(&w[0]));
-                    unpack8_bf16(__ldg(wv + 1), *reinterpret_cast<float(*)[8]>(&w[8]));
+                    unpack8_bf16(wv[0], *reinterpret_cast<float(*)[8]>(&w[0]));
+                    unpack8_bf16(wv[1], *reinterpret_cast<float(*)[8]>(&w[8]));
                     uint32_t q[4];
 #pragma unroll
                     for (int e = 0; e < 16; e += 4) {
@@ -365,6 +419,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
             fence_proxy_async_shared();
             compute_sync();
             if (tid == 0) {
+                ST_MARK(3);
                 mbar_arrive(bar(B_AGU_READY));
                 // this layer's partials from the other CTAs of the cluster
                 if (S > 1)
@@ -373,30 +428,42 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
             // ---- (c) exchange of the gate/up partials in the cluster ----
             if (compute_sync_or(!mbar_wait(bar(B_ACC_GU), par, abort_f, err)))
                 break;
+            if (tid == 0)
+                ST_MARK(4);
             tc_fence_after();
             for (int pr = 0; pr < S; ++pr) {
                 if (pr == j)
                     continue;
-                float *dst = XS + (size_t)(pr < j ? pr : pr - 1) * M * 2 * FPC;
-                for (int half = 0; half < 2; ++half) {          // gate columns, then up columns
-                    for (int f0 = 0; f0 < FPC; f0 += 16) {
-                        uint32_t v[16];
-                        tmem_ld_x16(t_gu + lane_off + (uint32_t)(gate_col(FPC * pr + f0) + 64 * half), v);
-                        tmem_ld_wait();
-                        if (row_ok) {
-                            float4 *o = reinterpret_cast<float4 *>(dst + (size_t)m_t * 2 * FPC + half * FPC + f0);
+                float *dst = XS + (size_t)(pr < j ? pr : pr - 1) * M * RS + hw * FPC;
+                // this warp's half (gate or up) of the peer's columns, in runs of
+                // 16, all in flight before one wait (FPC <= 64 when S > 1)
+                uint32_t v[4][16];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (16 * q < FPC)
+                        tmem_ld_x16(t_gu + lane_off + (uint32_t)(gate_col(FPC * pr + 16 * q) + 64 * hw), v[q]);
+                tmem_ld_wait();
+                if (row_ok) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        if (16 * q < FPC) {
+                            float4 *o = reinterpret_cast<float4 *>(dst + (size_t)m_t * RS + 16 * q);
 #pragma unroll
                             for (int e = 0; e < 4; ++e)
-                                o[e] = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
-                                                   __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
+                                o[e] = make_float4(__uint_as_float(v[q][4 * e]), __uint_as_float(v[q][4 * e + 1]),
+                                                   __uint_as_float(v[q][4 * e + 2]), __uint_as_float(v[q][4 * e + 3]));
                         }
                     }
                 }
             }
+            if (tid == 0)
+                ST_MARK(16);
             fence_proxy_async_shared();
+            if (tid == 0)
+                ST_MARK(17);
             compute_sync();
             if (tid == 0 && S > 1) {
-                const uint32_t bytes = (uint32_t)(M * 2 * FPC * 4);
+                const uint32_t bytes = (uint32_t)(M * RS * 4);
                 for (int pr = 0; pr < S; ++pr) {
                     if (pr == j)
                         continue;
@@ -407,9 +474,13 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
                 }
             }
             // ---- (d) reduce, gated activation, q_h to the cluster ------
+            if (tid == 0)
+                ST_MARK(5);
             if (compute_sync_or(S > 1 && !mbar_wait_cluster(bar(B_RX), par, abort_f, err)))
                 break;
-            for (int f0 = 0; f0 < FPC; f0 += 16) {
+            if (tid == 0)
+                ST_MARK(6);
+            for (int f0 = 16 * hw; f0 < FPC; f0 += 32) {        // this warp's runs of 16 features
                 const int fl = FPC * j + f0;                    // first feature of the run, in the cluster
                 uint32_t vg[16], vu[16];
                 tmem_ld_x16(t_gu + lane_off + (uint32_t)gate_col(fl), vg);
@@ -430,7 +501,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
                                 u[e] = __fadd_rn(u[e], __uint_as_float(vu[e]));
                             }
                         } else {
-                            const float *src = RX + ((size_t)(s < j ? s : s - 1) * M + m_t) * 2 * FPC + f0;
+                            const float *src = RX + ((size_t)(s < j ? s : s - 1) * M + m_t) * RS + f0;
 #pragma unroll
                             for (int e = 0; e < 16; e += 4) {
                                 const float4 gg = *reinterpret_cast<const float4 *>(src + e);
@@ -480,11 +551,18 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
                     }
                 }
             }
+            if (tid == 0)
+                ST_MARK(18);
             tc_fence_before();
             fence_proxy_async_cluster();
+            if (tid == 0)
+                ST_MARK(19);
             fence_acq_rel_cluster();
+            if (tid == 0)
+                ST_MARK(20);
             compute_sync();
             if (tid == 0) {
+                ST_MARK(7);
                 if (S == 1)
                     mbar_arrive(bar(B_AD_READY));
                 else
@@ -494,30 +572,41 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
             // ---- (f) the down partial of this K-slice to L2 -----------
             if (compute_sync_or(!mbar_wait(bar(B_ACC_D), par, abort_f, err)))
                 break;
+            if (tid == 0)
+                ST_MARK(8);
             tc_fence_after();
             {
-                float *pp = p.P + ((size_t)(par * nC + c) * ngrp + 32 * j) * ST_ROWS * 8;
-                for (int c0 = 0; c0 < ST_NT; c0 += 32) {
-                    uint32_t v[32];
-                    tmem_ld_x32(t_d + lane_off + (uint32_t)c0, v);
+                // P[parity][group][cluster][M][8]: an owner's groups are contiguous
+                float *pp = p.P + (((size_t)par * ngrp + 32 * j) * nC + c) * M * 8;
+                for (int c0 = 128 * hw; c0 < 128 * hw + 128; c0 += 64) {
+                    uint32_t v[2][32];
+                    tmem_ld_x32(t_d + lane_off + (uint32_t)c0, v[0]);
+                    tmem_ld_x32(t_d + lane_off + (uint32_t)(c0 + 32), v[1]);
                     tmem_ld_wait();
                     if (row_ok) {
 #pragma unroll
-                        for (int gq = 0; gq < 4; ++gq) {
-                            float4 *o = reinterpret_cast<float4 *>(pp + ((size_t)(c0 / 8 + gq) * ST_ROWS + m_t) * 8);
-                            o[0] = make_float4(__uint_as_float(v[8 * gq]), __uint_as_float(v[8 * gq + 1]),
-                                               __uint_as_float(v[8 * gq + 2]), __uint_as_float(v[8 * gq + 3]));
-                            o[1] = make_float4(__uint_as_float(v[8 * gq + 4]), __uint_as_float(v[8 * gq + 5]),
-                                               __uint_as_float(v[8 * gq + 6]), __uint_as_float(v[8 * gq + 7]));
+                        for (int gq = 0; gq < 8; ++gq) {
+                            const uint32_t *w8 = &v[gq >> 2][8 * (gq & 3)];
+                            float4 *o = reinterpret_cast<float4 *>(pp + ((size_t)(c0 / 8 + gq) * nC * M + m_t) * 8);
+                            o[0] = make_float4(__uint_as_float(w8[0]), __uint_as_float(w8[1]), __uint_as_float(w8[2]),
+                                               __uint_as_float(w8[3]));
+                            o[1] = make_float4(__uint_as_float(w8[4]), __uint_as_float(w8[5]), __uint_as_float(w8[6]),
+                                               __uint_as_float(w8[7]));
                         }
                     }
                 }
             }
-            tc_fence_before();
-            __threadfence();
-            compute_sync();
             if (tid == 0)
+                ST_MARK(21);
+            tc_fence_before();
+            fence_acq_rel_gpu();
+            if (tid == 0)
+                ST_MARK(22);
+            compute_sync();
+            if (tid == 0) {
+                ST_MARK(9);
                 red_release_gpu(cnt_P + 32 * j, 1);
+            }
             // ---- (g) owners: reduce, residual, publish ----------------
             if (G > 0) {
                 if (tid == 0) {
@@ -529,68 +618,82 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
                             w_ok = wait_count(cnt_P + 32 * jt, nC * (l + 1), abort_f, err);
                         last_tile = jt;
                     }
+                    ST_MARK(10);
                     if (w_ok) {
                         fence_proxy_async_global();
                         mbar_arrive_expect_tx(bar(B_OWN), (uint32_t)(G * nC * M * 32));
-                        for (int gi = 0; gi < G; ++gi) {
+                        for (int gi = 0; gi < G; ++gi) {   // one copy per owned group: all clusters' partials
                             const int g = k_own + gi * p.n_own;
-                            for (int cc = 0; cc < nC; ++cc)
-                                bulk_load(smem_u32(OWN + (size_t)(gi * nC + cc) * M * 8),
-                                          p.P + ((size_t)(par * nC + cc) * ngrp + g) * ST_ROWS * 8, (uint32_t)(M * 32),
-                                          bar(B_OWN));
+                            bulk_load(smem_u32(OWN + (size_t)gi * nC * M * 8),
+                                      p.P + ((size_t)par * ngrp + g) * nC * M * 8, (uint32_t)(nC * M * 32), bar(B_OWN));
                         }
                     }
                 }
                 if (compute_sync_or(!mbar_wait(bar(B_OWN), par, abort_f, err)))
                     break;
+                if (tid == 0)
+                    ST_MARK(11);
                 const bool last = l == L - 1;
-                if (tid < M) {
-                    const int m = tid;
+                {
+                    // four threads per token, columns 2 part and 2 part + 1 of
+                    // every owned group; the token's sum of squares as
+                    // (part 0 + part 1) + (part 2 + part 3)
+                    const int m = tid >> 2, part = tid & 3;
                     float ss = 0.0f;
-                    for (int gi = 0; gi < G; ++gi) {
-                        const int g = k_own + gi * p.n_own;
-                        float acc[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            acc[e] = 0.0f;
-                        for (int cc = 0; cc < nC; ++cc) {     // K-slices in order
-                            const float4 *src = reinterpret_cast<const float4 *>(OWN + ((size_t)(gi * nC + cc) * M + m) * 8);
-                            const float4 a0 = src[0], a1 = src[1];
-                            acc[0] = __fadd_rn(acc[0], a0.x);
-                            acc[1] = __fadd_rn(acc[1], a0.y);
-                            acc[2] = __fadd_rn(acc[2], a0.z);
-                            acc[3] = __fadd_rn(acc[3], a0.w);
-                            acc[4] = __fadd_rn(acc[4], a1.x);
-                            acc[5] = __fadd_rn(acc[5], a1.y);
-                            acc[6] = __fadd_rn(acc[6], a1.z);
-                            acc[7] = __fadd_rn(acc[7], a1.w);
-                        }
-                        float x[8];
-                        unpack8_bf16(RES[gi * 64 + m], x);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            x[e] = round_bf16(__fadd_rn(x[e], __fmul_rn(acc[e], sc.w)));
-                        const uint4 v = pack8_bf16(x);
-                        if (last) {
-                            *reinterpret_cast<uint4 *>(p.out + (size_t)m * d + 8 * g) = v;
-                        } else {
-                            RES[gi * 64 + m] = v;
-                            *reinterpret_cast<uint4 *>(p.R + ((size_t)((par ^ 1u) * S + (g >> 5)) * ST_ROWS + m) * ST_KQ +
-                                                       (g & 31) * 8) = v;
-                            if (DEBUG && p.dbg_res)
-                                *reinterpret_cast<uint4 *>(p.dbg_res + ((size_t)(l + 1) * M + m) * d + 8 * g) = v;
-#pragma unroll
-                            for (int e = 0; e < 8; ++e)
-                                ss = __fadd_rn(ss, __fmul_rn(x[e], x[e]));
+                    if (m < M) {
+                        for (int gi = 0; gi < G; ++gi) {
+                            const int g = k_own + gi * p.n_own;
+                            float a0 = 0.0f, a1 = 0.0f;
+#pragma unroll 8
+                            for (int cc = 0; cc < nC; ++cc) {     // K-slices in order
+                                const float2 v2 =
+                                    *reinterpret_cast<const float2 *>(OWN + ((size_t)(gi * nC + cc) * M + m) * 8 + 2 * part);
+                                a0 = __fadd_rn(a0, v2.x);
+                                a1 = __fadd_rn(a1, v2.y);
+                            }
+                            uint32_t *rw = reinterpret_cast<uint32_t *>(&RES[gi * 64 + m]) + part;
+                            const uint32_t rv = *rw;
+                            const float x0 = round_bf16(__fadd_rn(bf_lo(rv), __fmul_rn(a0, sc.w)));
+                            const float x1 = round_bf16(__fadd_rn(bf_hi(rv), __fmul_rn(a1, sc.w)));
+                            uint32_t v = bf16_bits(x0) | (bf16_bits(x1) << 16);
+                            const size_t col = 8 * (size_t)g + 2 * part;
+                            if (DEBUG && p.dbg_out)
+                                *reinterpret_cast<uint32_t *>(p.dbg_out + ((size_t)l * M + m) * d + col) = v;
+                            if (last) {
+                                *reinterpret_cast<uint32_t *>(p.out + (size_t)m * d + col) = v;
+                            } else {
+                                float y0 = x0, y1 = x1;
+                                if (DEBUG && p.dbg_res_in) {
+                                    // the next layer starts from the caller's residual instead
+                                    v = *reinterpret_cast<const uint32_t *>(p.dbg_res_in + ((size_t)(l + 1) * M + m) * d + col);
+                                    y0 = bf_lo(v);
+                                    y1 = bf_hi(v);
+                                }
+                                *rw = v;
+                                *reinterpret_cast<uint32_t *>(p.R + ((size_t)((par ^ 1u) * S + (g >> 5)) * ST_ROWS + m) * ST_KQ +
+                                                              (g & 31) * 8 + 2 * part) = v;
+                                ss = __fadd_rn(ss, __fmul_rn(y0, y0));
+                                ss = __fadd_rn(ss, __fmul_rn(y1, y1));
+                            }
                         }
                     }
-                    if (!last)
-                        p.SS[(size_t)(par ^ 1u) * p.n_own * 64 + (size_t)k_own * Mp + m] = ss;
+                    const float o1 = __shfl_xor_sync(0xffffffffu, ss, 1);
+                    const float pr2 = (part & 1) ? __fadd_rn(o1, ss) : __fadd_rn(ss, o1);
+                    const float o2 = __shfl_xor_sync(0xffffffffu, pr2, 2);
+                    if (!last && part == 0 && m < M)
+                        p.SS[(size_t)(par ^ 1u) * p.n_own * 64 + (size_t)k_own * Mp + m] = __fadd_rn(pr2, o2);
                 }
-                __threadfence();
+                if (tid == 0)
+                    ST_MARK(24);
+                fence_acq_rel_gpu();
+                if (tid == 0)
+                    ST_MARK(25);
                 compute_sync();
-                if (tid == 0 && !last)
-                    red_release_gpu(cnt_R, 1);
+                if (tid == 0) {
+                    ST_MARK(12);
+                    if (!last)
+                        red_release_gpu(cnt_R, 1);
+                }
             }
         }
     }
@@ -610,13 +713,13 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
                     mbar_wait_for(bar(b), par, 20000000ull);
         }
         // drain what this CTA may still have in flight: weight copies, MMAs
-        if (warp == 4 && lane == 0) {
+        if (warp == W_PROD && lane == 0) {
             if (w_issued & 1u)
                 mbar_wait_for(bar(B_WFULL_GU), 0, 100000000ull), mbar_wait_for(bar(B_WFULL_GU), 1, 100000000ull);
             if (w_issued & 2u)
                 mbar_wait_for(bar(B_WFULL_D), 0, 100000000ull), mbar_wait_for(bar(B_WFULL_D), 1, 100000000ull);
         }
-        if (warp == 5 && lane == 0 && mma_issued) {
+        if (warp == W_MMA && lane == 0 && mma_issued) {
             mma_commit(bar(B_DRAIN));
             mbar_wait_for(bar(B_DRAIN), 0, 100000000ull);
         }
@@ -627,7 +730,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
         cluster_arrive();
         cluster_wait();
     }
-    if (warp == 5) {
+    if (warp == W_MMA) {
         __syncwarp();
         tmem_dealloc(tmem, 512);
     }
@@ -683,13 +786,13 @@ bool plan_stack(StackParams &p, int M, int d, int ff, int num_sms, size_t *smem_
         return false;
     const int FPC = ST_FEAT / S;
     const int Mp = (M + 3) & ~3;
-    const size_t rx = (size_t)(S - 1) * M * 2 * FPC * 4;
+    const size_t rx = (size_t)(S - 1) * M * (2 * FPC + 4) * 4;
     const size_t xs = rx;
     const size_t astage = (size_t)M * 512 + (size_t)n_own * Mp * 4;
     const size_t own = (size_t)G * nC * M * 32;
     size_t x = std::max(rx + std::max(xs, astage), own);
     x = (x + 1023) / 1024 * 1024;
-    const size_t total = 1024 + OFF_X + x + (size_t)G * 64 * 16 + 256 + N_BARS * 8 + 16;
+    const size_t total = 1024 + OFF_X + x + (size_t)G * 64 * 16 + 256 + 1024 + N_BARS * 8 + 16;
     if (total > smem_max_stack())
         return false;
     // over half an SM's shared memory: one CTA per SM, each holding all 512

@@ -214,10 +214,24 @@ class FFNPlan:
         """Whether the forward for M tokens is the one persistent stack kernel."""
         return N.frt_ffn_uses_stack_kernel(self.handle, M)
 
-    def debug_stack(self, residual, hidden=None, q_x_in=None, stream=None):
+    def stack_timeline(self, residual, hidden=None, stream=None):
+        """The forward through the persistent stack kernel (the product
+        instantiation) with its per-CTA, per-layer timeline: int64
+        [CTAs, L, 16] %globaltimer nanoseconds (diagnostics)."""
+        M, d, ff, L = residual.shape[0], self.d, self.ff, self.n_layers
+        dev = residual.device
+        out = torch.empty((M, d), dtype=torch.bfloat16, device=dev)
+        times = torch.zeros(((ff // 128) * (d // 256), L, 32), dtype=torch.int64, device=dev)
+        N.frt_ffn_debug_stack(self.handle, _bf16(residual, (M, d), "residual"),
+                              _bf16(hidden, (M, d), "hidden") if hidden is not None else None, _ptr(out), M,
+                              None, None, None, None, None, None, _ptr(times), _stream(stream))
+        return out, times
+
+    def debug_stack(self, residual, hidden=None, q_x_in=None, res_in=None, stream=None):
         """The forward through the persistent stack kernel with every layer's
-        intermediates dumped (diagnostics); q_x_in (uint8 [L, M, d]) replaces
-        each layer's own E4M3 codes of step A1 as the GEMMs' input."""
+        intermediates dumped (diagnostics).  q_x_in (uint8 [L, M, d])
+        replaces each layer's own E4M3 codes of step A1 as the GEMMs' input;
+        res_in (BF16 [L, M, d]) replaces the input of every layer >= 1."""
         M, d, ff, L = residual.shape[0], self.d, self.ff, self.n_layers
         dev = residual.device
         o = {
@@ -225,15 +239,17 @@ class FFNPlan:
             "q_x": torch.empty((L, M, d), dtype=torch.uint8, device=dev),
             "gu": torch.empty((L, M, 2 * ff), dtype=torch.bfloat16, device=dev),
             "q_h": torch.empty((L, M, ff), dtype=torch.uint8, device=dev),
-            "res": torch.empty((L, M, d), dtype=torch.bfloat16, device=dev),
+            "layer_out": torch.empty((L, M, d), dtype=torch.bfloat16, device=dev),
+            "times": torch.zeros(((ff // 128) * (d // 256), L, 32), dtype=torch.int64, device=dev),
         }
-        if q_x_in is not None and (q_x_in.dtype != torch.uint8 or tuple(q_x_in.shape) != (L, M, d)
-                                   or not q_x_in.is_contiguous()):
-            raise ValueError("q_x_in must be a contiguous uint8 [L, M, d] tensor")
+        for name, t, dt in (("q_x_in", q_x_in, torch.uint8), ("res_in", res_in, torch.bfloat16)):
+            if t is not None and (t.dtype != dt or tuple(t.shape) != (L, M, d) or not t.is_contiguous()):
+                raise ValueError("%s must be a contiguous [L, M, d] tensor of %s" % (name, dt))
         N.frt_ffn_debug_stack(self.handle, _bf16(residual, (M, d), "residual"),
                               _bf16(hidden, (M, d), "hidden") if hidden is not None else None, _ptr(o["out"]), M,
-                              _ptr(q_x_in) if q_x_in is not None else None, _ptr(o["q_x"]), _ptr(o["gu"]),
-                              _ptr(o["q_h"]), _ptr(o["res"]), _stream(stream))
+                              _ptr(q_x_in) if q_x_in is not None else None,
+                              _ptr(res_in) if res_in is not None else None, _ptr(o["q_x"]), _ptr(o["gu"]),
+                              _ptr(o["q_h"]), _ptr(o["layer_out"]), _ptr(o["times"]), _stream(stream))
         return o
 
     def weights(self, layer, device="cuda", stream=None):
