@@ -367,6 +367,20 @@ def run_ours(args, wl, world, rank, local):
     torch.cuda.synchronize()
     replay = lambda: plan.graph_replay(wl.M, stream)
 
+    if args.launch_list:
+        # profiling aid: warm replays, then the given number inside an NVTX
+        # range "replay" that ncu can select (--nvtx --nvtx-include "replay/")
+        timed_steps(stream, flush, replay, 0, args.warmup)
+        torch.cuda.nvtx.range_push("replay")
+        with torch.cuda.stream(stream):
+            for _ in range(args.launch_list):
+                replay()
+        torch.cuda.synchronize()
+        torch.cuda.nvtx.range_pop()
+        plan.device_status(stream)
+        plan.close()
+        return {"launch_list": wl.name, "replays": args.launch_list, "launches_per_replay": 3 * wl.L}
+
     # warm-up, then exactly K timed steps between barriers
     timed_steps(stream, flush, replay, 0, args.warmup)
     barrier(world)
@@ -767,6 +781,43 @@ def run_fp4(args, wl, world, rank, local):
     return line
 
 
+def run_fp8_gemm_peak(args, local):
+    """Diagnostic: this library's FP8 GEMM (tcgen05, tiled role, CTA pairs)
+    on 8192 x 8192 x 8192 E4M3 operands, timed with CUDA events -- the FP8
+    dense throughput a long contraction reaches here, beside the nominal
+    2 x bf16 proxy."""
+    from realtime_transformer_gb300.ffn import FFNPlan
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    n = 8192
+    plan = FFNPlan(256, 1024, "geglu_tanh", 64, 1)
+    g = torch.Generator(device=dev).manual_seed(7)
+    A = torch.randint(0, 0x7E, (n, n), generator=g, device=dev, dtype=torch.int32).to(torch.uint8)
+    B = torch.randint(0, 0x7E, (n, n), generator=g, device=dev, dtype=torch.int32).to(torch.uint8)
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            plan.gemm(A, B, path=2, stream=stream)
+        torch.cuda.synchronize()
+        sampler = ClockSampler(local)
+        sampler.start()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            plan.gemm(A, B, path=2, stream=stream)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    plan.device_status()
+    plan.close()
+    ms = e0.elapsed_time(e1) / args.steps
+    P = peaks()
+    tf = 2.0 * n ** 3 / (ms * 1e-3) / 1e12
+    return {"fp8_gemm_8192": {"tflops": tf, "ms": ms, "steps": args.steps,
+                              "vs_2x_bf16_burst": tf / (2.0 * P["bf16_tflops"]),
+                              "vs_2x_bf16_sustained": tf / (2.0 * P["bf16_tflops_sustained"]), "clocks": clocks}}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -783,6 +834,11 @@ def main():
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling aid: run a plan of this many layers of the workload's shape "
                          "(the line is then not the workload's bench line)")
+    ap.add_argument("--launch-list", type=int, default=0,
+                    help="profiling aid: after the warm-up, run this many graph replays of one workload inside an "
+                         "NVTX range \"replay\" and print no bench line")
+    ap.add_argument("--fp8-gemm-peak", action="store_true",
+                    help="diagnostic: time this library's FP8 GEMM on 8192^3 and print its TFLOP/s (no bench line)")
     ap.add_argument("--variant", choices=sorted(VARIANTS), default="plain",
                     help="FFN stack only: plain (the bench line), fold (norm weight folded into the gate/up "
                          "weights) or ada (AdaRMSNorm modulation)")
@@ -793,14 +849,17 @@ def main():
     WARM_L2 = args.warm_l2
     if args.warmup < 3:
         args.warmup = 3
-    all_ffn = args.config is None and args.sublayer == "ffn" and args.layers == 0 and args.variant == "plain"
+    all_ffn = (args.config is None and args.sublayer == "ffn" and args.layers == 0 and args.variant == "plain"
+               and not args.launch_list)
     wl = synthetic.WORKLOADS[args.config or (HEADLINE if args.sublayer == "ffn" else DEFAULT_CONFIG)]
     if args.layers > 0:
         wl = wl.with_(L=args.layers, name=wl.name + "_%dlayers" % args.layers)
     if args.variant != "plain" and (args.sublayer != "ffn" or args.impl != "ours"):
         ap.error("--variant applies to the FFN stack of this implementation only")
     world, rank, local = dist_setup(args.gpus)
-    if args.impl == "reference":
+    if args.fp8_gemm_peak:
+        line = run_fp8_gemm_peak(args, local)
+    elif args.impl == "reference":
         line = run_reference(args, wl, world, rank)
     elif args.sublayer == "qkv":
         line = run_qkv(args, wl, world, rank, local)

@@ -45,6 +45,7 @@ struct GemmParams {
     float *ws;              // split-K partials
     int *counters;          // split-K arrival counters, one per tile, for this launch's split count
     int pair;               // tiled role on CTA pairs (cta_group::2): 256-token MMAs, half a weight tile per CTA
+    int w_evict, x_evict;   // L2 priority of the weight / token tiles: 0 evict-first, 1 normal, 2 evict-last
     int cluster;            // 1: the splits of a tile are one thread-block cluster and exchange
                             //    partials in distributed shared memory (ws, counters unused)
     const uint16_t *gate;   // EPI_RESID with AdaRMSNorm: out = bf16(resid + gate * acc * alpha), BF16 gate

@@ -110,3 +110,40 @@ def test_cta_pair_matches_single_cta(plan, monkeypatch, M, N, K, splits):
     monkeypatch.delenv("FRT_FFN_PAIR", raising=False)
     c_pair = run(plan, A, B, 2, splits)
     assert np.array_equal(c_single, c_pair)
+
+
+@pytest.mark.parametrize("M,N,K,splits", [(512, 1024, 1024, 1), (768, 2048, 512, 0), (256, 768, 4096, 2)])
+@pytest.mark.parametrize("policy", ["normal", "last"])
+def test_weight_l2_priority_leaves_the_bits(plan, monkeypatch, M, N, K, splits, policy):
+    """The weight tiles' L2 priority (a tuning switch of the tiled role) only
+    changes what stays in L2, never the result."""
+    rng = np.random.default_rng(M + 3 * N + 7 * K)
+    A = rng.integers(0, 0x7E, (M, K)).astype(np.uint8)
+    B = rng.integers(0, 0x7E, (N, K)).astype(np.uint8)
+    monkeypatch.delenv("FRT_FFN_W_EVICT", raising=False)
+    c0 = run(plan, A, B, 2, splits)
+    monkeypatch.setenv("FRT_FFN_W_EVICT", policy)
+    assert np.array_equal(c0, run(plan, A, B, 2, splits))
+
+
+def test_large_tiled_gemm_matches_the_oracle_on_sampled_rows():
+    """8192 x 8192 x 8192 (token groups of the raster, CTA pairs, 8 waves):
+    sampled rows against the oracle (exact-sum inputs: bit for bit)."""
+    from realtime_transformer_gb300.ffn import FFNPlan
+    p = FFNPlan(256, 1024, "geglu_tanh", 64, 1)
+    try:
+        rng = np.random.default_rng(8192)
+        M = N = K = 8192
+        e = rng.integers(5, 7, (M, K))      # |v| < 1, multiples of 2^-5: sums over 8192 stay exact in fp32
+        A = ((rng.integers(0, 2, (M, K)) << 7) | (e << 3) | rng.integers(0, 8, (M, K))).astype(np.uint8)
+        e = rng.integers(5, 7, (N, K))
+        B = ((rng.integers(0, 2, (N, K)) << 7) | (e << 3) | rng.integers(0, 8, (N, K))).astype(np.uint8)
+        dev = torch.device("cuda")
+        C = p.gemm(torch.from_numpy(A).to(dev), torch.from_numpy(B).to(dev), path=2)
+        torch.cuda.synchronize()
+        p.device_status()
+        rows = np.array([0, 1, 127, 128, 4095, 4096, 8190, 8191])
+        got = C.index_select(0, torch.from_numpy(rows).to(dev)).cpu().numpy()
+        assert np.array_equal(got, oracle.gemm_e4m3(A[rows], B))
+    finally:
+        p.close()
