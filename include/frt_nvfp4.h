@@ -20,14 +20,20 @@
  * Readings (the pages give the loop, not the format or the AWQ rule): NVFP4
  * as NVIDIA publishes it; AWQ scales supplied by the caller (the oracle's
  * awq_scales gives the activation-magnitude rule c_k = mean|y_k|^alpha).
+ * Kernels: N2 and N3 run as one GEMM over [W_g'; W_u'] (stored interleaved in
+ * blocks of 64 rows, so a tile holds the gate and up rows of the same
+ * features) whose epilogue forms G and U as above, decodes them and
+ * requantises act(dec G) * dec U -- the same operations in the same order as
+ * two GEMMs and a combine kernel, without the round trip of G and U through
+ * memory; three kernels per layer, chained by programmatic dependent launch.
  *
  * Layouts: codes are packed two per byte, element 2i in the low nibble,
- * row-major [rows, K/2] (activations; the plan stores weights in the tiled
- * order of frt_fp4_debug_weights, one contiguous copy per pipeline stage); the block scales of GEMM operands (X, A and the
+ * row-major [rows, K/2]; the block scales of GEMM operands (X, A and the
  * weights) are stored in the tensor cores' TMEM-ready order: per 128-row tile
  * and 64-element K chunk a 512-byte block, byte (r % 32) * 16 + (r / 32) * 4 + j
  * for row r of the tile and 16-element group j of the chunk (tiles major,
- * chunks minor); the block scales of G and U are row-major [M, ff/16].
+ * chunks minor); the block scales of G and U (frt_fp4_debug_trace) are
+ * row-major [M, ff/16].
  *
  * Conventions: as frt_ffn.h (BF16 bit patterns, 16-byte aligned device
  * pointers, frt_ffn_last_error() for messages, one host thread and one stream
@@ -89,7 +95,7 @@ frt_status frt_fp4_set_scales(frt_fp4_plan_t plan, const float *act);
 /*
  * The stack on M tokens: residual_in [M, d] BF16, hidden_in [M, d] BF16 (added
  * at layer 0) or NULL, out [M, d] BF16 (may not alias the inputs).  M == 0
- * does nothing.  Five kernels per layer; no allocation.
+ * does nothing.  Three kernels per layer; no allocation.
  * Errors: INVALID_ARG, NOT_READY (weights or scales missing), SHAPE, CUDA.
  */
 frt_status frt_fp4_forward(frt_fp4_plan_t plan, const void *residual_in, const void *hidden_in, void *out, int M,
@@ -101,7 +107,9 @@ frt_status frt_fp4_forward(frt_fp4_plan_t plan, const void *residual_in, const v
  * [M, d] BF16 (only when hidden_in is given), x_codes [M, d/2] and x_sf
  * (TMEM-ready, ceil(M/128) * 128 * d/16 bytes), g/u codes [M, ff/2] and
  * row-major scales [M, ff/16], h_codes [M, ff/2] and h_sf (TMEM-ready,
- * ceil(M/128) * 128 * ff/16 bytes).  Synchronises `stream`.
+ * ceil(M/128) * 128 * ff/16 bytes).  G and U are written by the gate/up
+ * GEMM's epilogue as it forms them (the four g/u buffers: all or none).
+ * Synchronises `stream`.
  */
 frt_status frt_fp4_debug_trace(frt_fp4_plan_t plan, int layer, const void *residual_in, const void *hidden_in,
                                void *out, void *r_prime, void *x_codes, void *x_sf, void *g_codes, void *g_sf,
@@ -109,12 +117,9 @@ frt_status frt_fp4_debug_trace(frt_fp4_plan_t plan, int layer, const void *resid
 
 /*
  * Test/diagnostic: copy a layer's quantised weight (which: 0 gate, 1 up,
- * 2 down) -- codes (rows * K/2 bytes) in the plan's tiled layout and
- * TMEM-ready scales (rows * K/16 bytes).  Tiled layout: per 128-row tile and
- * 256-element K stage one 16 KB block (tiles major, stages minor) holding the
- * shared-memory image of a 128-byte-swizzled copy of that box: row r of the
- * tile at byte r * 128, its 16-byte chunk c at chunk c ^ (r % 8), element 2i
- * in the low nibble.
+ * 2 down) -- codes row-major [rows, K/2] and TMEM-ready scales (rows * K/16
+ * bytes) of that weight's own rows (gate and up taken out of the interleaved
+ * arena on the host).  Synchronises `stream`.
  */
 frt_status frt_fp4_debug_weights(frt_fp4_plan_t plan, int layer, int which, void *codes, void *sf,
                                  frt_stream_t stream);
@@ -123,12 +128,17 @@ frt_status frt_fp4_debug_weights(frt_fp4_plan_t plan, int layer, int which, void
  * Test/diagnostic: out[m][n] = alpha * sum_k A[m][k] B[n][k] over NVFP4
  * operands (codes [M, K/2] and [N, K/2]; TMEM-ready scales sized for
  * ceil(M/128) and N/128 tiles), fp32 [M, N] out.  N % 128 == 0, K % 256 == 0,
- * 1 <= M <= 65536.  Runs the role the plan's GEMMs run (the tiled role; the
- * weight-streaming role for M <= 64 when FRT_F4_SWAP=1).  splits: split-K factor (1 <= splits <= K / 256); above 1,
- * ws (fp32, tiles * splits * 128 * 128, tiles = N/128 * ceil(M/128) <= 4096)
- * and counters (tiles zeroed ints, left zeroed) are device scratch; the
- * partials are summed in split order.  err: a device int the kernel sets on a
- * timed-out wait.
+ * 1 <= M <= 65536.  Runs the role the plan's GEMMs run: weight-streaming
+ * (the weights as the 128-row operand) for M <= 64, else tiled; FRT_F4_SWAP=0
+ * forces the tiled role.  splits: the split-K factor asked for (1 <= splits
+ * <= K / 256; the planner may take fewer, never more); weight-streaming
+ * splits of a tile exchange partials inside a thread-block cluster, tiled
+ * ones through ws (fp32, tiles * splits * 128 * 128; tiles = N/128, or N/128
+ * * ceil(M/128) tiled; at most 2048) with one arrival counter per tile in
+ * counters (zeroed before the first call; each call advances a tile's counter
+ * by its split count, so counters may be reused only with the same splits).
+ * The partials are summed in split order.  err: a device int the kernel sets
+ * on a timed-out wait.
  */
 frt_status frt_nvfp4_gemm(const void *a_codes, const void *a_sf, const void *b_codes, const void *b_sf, int M, int N,
                           int K, float alpha, float *out, int splits, float *ws, int *counters, int *err,

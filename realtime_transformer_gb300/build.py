@@ -16,9 +16,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfrt_ffn.so")
-SOURCES = ["frt_ffn.cu", "k_elementwise.cu", "k_gemm_fp8.cu", "k_stack_fp8.cu", "frt_noalloc.cu", "frt_qkv.cu",
-           "k_nvfp4.cu", "frt_nvfp4.cu"]
-HEADERS = ["frt_internal.h", "frt_ptx.cuh", "frt_epi.cuh"]
+SOURCES = ["frt_ffn.cu", "k_elementwise.cu", "k_gemm_fp8.cu", "k_gemm_f4.cu", "k_stack_fp8.cu", "frt_noalloc.cu",
+           "frt_qkv.cu", "k_nvfp4.cu", "frt_nvfp4.cu"]
+HEADERS = ["frt_internal.h", "frt_ptx.cuh", "frt_epi.cuh", "frt_f4.cuh", "k_gemm_tc.cuh"]
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

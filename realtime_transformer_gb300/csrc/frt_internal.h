@@ -18,6 +18,12 @@ enum Epi : int {
     EPI_GATED = 3,  // out = q_h[m][f] = E4M3(act(g) * u * inv_s), g/u = bf16(acc * alpha) (interleaved rows)
     EPI_GATED_AMAX = 4,  // atomicMax(amax, |act(g) * u|) (calibration)
     EPI_ROPE = 5,   // tiled role: x = bf16(acc * alpha), split into Q/K/V heads, RoPE on Q and K (rope_* fields)
+    // NVFP4 operands (f4 launches), [W_gate; W_up] interleaved as for EPI_GATED:
+    // g = acc * alpha, u = acc * alpha_u; G = NVFP4(g, s_g), U = NVFP4(u, s_u);
+    // a = act(dec G) * dec U
+    EPI_F4_GATED = 6,    // out = codes of NVFP4(a, s_h) [m][f/2], TMEM-ready block scales into out_sf
+    EPI_F4_AMAX_GU = 7,  // atomicMax(amax[0], |g|), atomicMax(amax[1], |u|) (calibration)
+    EPI_F4_AMAX_H = 8,   // atomicMax(amax[2], |a|) (calibration)
 };
 
 // One GEMM launch: C[token][feature] = epilogue(sum_k X[token][k] W[feature][k]).
@@ -66,6 +72,15 @@ struct GemmParams {
     const float2 *rope_cs;  // (cos, sin) [m_tok, hd / 2] of each token's angles
     int rope_hd, rope_nq, rope_nkv;
     uint16_t *rope_q, *rope_k, *rope_v;
+    // NVFP4 operands (f4 launches): the E4M3 block scales of the weight and
+    // token operands in the TMEM-ready order (per 128-row tile and 64-element
+    // K chunk a 512-byte block, tiles major), rows counted as in the tensor maps
+    const uint8_t *sf_w, *sf_x;
+    // NVFP4 gated epilogues (alpha: the gate rows')
+    float alpha_u;
+    float s_g, inv6_g, s_u, inv6_u, s_h, inv6_h;  // tensor scales s and 1 / (6 s)
+    uint8_t *out_sf;        // EPI_F4_GATED: block scales of the output, TMEM-ready (K = ff)
+    uint8_t *dbg_gq, *dbg_gs, *dbg_uq, *dbg_us;  // optional: G and U codes [M, ff/2], row-major scales [M, ff/16]
 };
 
 struct GemmLaunch {
@@ -73,6 +88,7 @@ struct GemmLaunch {
     GemmParams p;
     int bn;                 // MMA N (Q tile rows)
     bool swap;
+    bool f4;                // NVFP4 operands (k_gemm_f4)
     int grid;
     size_t min_smem;        // dynamic shared memory floor (see plan_gemm)
 };
@@ -101,14 +117,18 @@ struct Tactic {
     bool no_pairs = false;
 };
 
-// Choose tiling / split-K for a GEMM of m_tok tokens x n_feat features x K
-// and fill the launch (tensor maps excluded).  swap: weight-streaming path;
-// tactic: null for the defaults.
+// Choose tiling / split-K for a GEMM of m_tok tokens x n_feat features and
+// K bytes per operand row (E4M3: K elements; NVFP4: K / 2 of 2 elements
+// each, a multiple of 128) and fill the launch (tensor maps excluded).
+// swap: weight-streaming path; tactic: null for the defaults; f4: NVFP4
+// operands (single-CTA tiles, N = 128 for the tiled role).
 void plan_gemm(GemmLaunch &g, bool swap, int m_tok, int n_feat, int K, int num_sms, int force_splits,
-               const Tactic *tactic = nullptr);
+               const Tactic *tactic = nullptr, bool f4 = false);
 size_t gemm_ws_floats(const GemmLaunch &g);
 int gemm_tiles(const GemmLaunch &g);
 cudaError_t launch_gemm(const GemmLaunch &g, cudaStream_t s, bool pdl);
+// The NVFP4 instantiations (k_gemm_f4.cu); launch_gemm hands f4 launches to it.
+cudaError_t launch_gemm_f4(const GemmLaunch &g, cudaStream_t s, bool pdl);
 
 cudaError_t launch_amax_bf16(const void *x, size_t n, unsigned *amax_word, cudaStream_t s);
 cudaError_t launch_quant_bf16(const void *x, size_t n, float inv_s, uint8_t *q, cudaStream_t s);
@@ -175,54 +195,17 @@ int stack_max_active_clusters(const StackParams &p, size_t smem);
 cudaError_t launch_stack(const StackParams &p, size_t smem, cudaStream_t s, bool debug);
 
 // ---------------------------------------------------------------- NVFP4 --
-// Epilogues of the block-scaled FP4 GEMM (k_nvfp4.cu).
-enum F4Epi : int {
-    F4_EPI_F32 = 0,    // out[m][n] = acc * alpha (fp32; diagnostics)
-    F4_EPI_AMAX = 1,   // atomicMax(amax, |acc * alpha|) (calibration)
-    F4_EPI_FP4 = 2,    // NVFP4 of acc * alpha: codes out[m][n/2], row-major block scales out_sf[m][n/16]
-    F4_EPI_RESID = 3,  // out[m][n] = bf16(resid[m][n] + acc * alpha)
-};
-
-// C[m][n] = epi(sum_k A[m][k] B[n][k]) over E2M1 operands with E4M3 block
-// scales; A rows a_row0.., B rows b_row0.. of their tensor maps (packed
-// bytes, box 128 bytes x 128 rows); sfa / sfb the TMEM-ready scales of the
-// A tiles and of the B tiles starting at b_row0.
-struct F4GemmParams {
-    const uint8_t *sfa, *sfb;
-    int a_row0, b_row0;
-    int M, K;               // valid rows of A; K % 256 == 0
-    int epi;                // F4Epi
-    float alpha;
-    float s_out, inv6_out;  // F4_EPI_FP4: tensor scale of the output and 1 / (6 s_out)
-    void *out;
-    int ldo;                // F32 / RESID: elements; FP4: bytes
-    uint8_t *out_sf;
-    int ldsf;
-    const uint16_t *resid;
-    int ldr;
-    unsigned *amax;
-    int *err;
-    int splits;             // split-K factor (grid z); > 1 needs ws and counters
-    const uint8_t *w_tiles; // weights in the tiled layout (one bulk copy per stage) or null (tensor map)
-    float *ws;              // fp32 partial tiles: [tiles][splits][128 x 128]
-    int *counters;          // one zeroed arrival counter per output tile (re-armed by the kernel)
-};
-
-// swap_n 0: tiled role (A = token tiles of 128 rows, B = weight tiles);
-// 16 / 32 / 64: weight-streaming role for M <= swap_n tokens (A = the weight
-// tiles, B = the tokens padded to swap_n rows; sfa the weights' scales).
-cudaError_t launch_f4_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const F4GemmParams &p, int n_cols,
-                           int swap_n, cudaStream_t s);
+// Elementwise kernels of the NVFP4 sublayer (k_nvfp4.cu); its GEMMs are f4
+// launches of the tensor-core GEMM (plan_gemm / launch_gemm).
 cudaError_t launch_f4_amax_w(const void *w, size_t rows, int K, const float *col, unsigned *amax_word,
                              cudaStream_t s);
+// ilv: 0 plain rows; 1 / 2 the gate / up rows of a [W_gate; W_up] arena
+// interleaved in blocks of 64 rows (q and sf: the layer's arena).
 cudaError_t launch_f4_quant_w(const void *w, int rows, int K, const float *col, float sc, float inv6, uint8_t *q,
-                              uint8_t *sf, bool tiled, cudaStream_t s);
+                              uint8_t *sf, int ilv, cudaStream_t s);
 cudaError_t launch_f4_norm_quant(const void *r, const void *h, const void *w, const float *awq_inv, int M, int d,
                                  float eps, float sc, float inv6, void *rprime, uint8_t *q, uint8_t *sf,
-                                 unsigned *amax_word, bool measure, cudaStream_t s);
-cudaError_t launch_f4_geglu(const uint8_t *gq, const uint8_t *gs, float s_g, const uint8_t *uq, const uint8_t *us,
-                            float s_u, int act, int M, int ff, float s_h, float inv6, uint8_t *hq, uint8_t *hsf,
-                            unsigned *amax_word, bool measure, cudaStream_t s);
+                                 unsigned *amax_word, bool measure, cudaStream_t s, bool pdl);
 
 }  // namespace frt
 

@@ -1,9 +1,11 @@
 // frt_nvfp4.cu -- the NVFP4 sublayer stack behind frt_nvfp4.h (itsolotime
-// FlashRT article, 7.2): per layer the norm + AWQ + FP4 quantise kernel, the
-// gate and up NVFP4 GEMMs with FP4 epilogues, the GeGLU FP4 -> FP4 kernel and
-// the down NVFP4 GEMM with the residual epilogue (kernels in k_nvfp4.cu).
-// Tensor maps of the fixed buffers are encoded once at plan creation and
-// passed as kernel parameters, so a forward can be captured into a graph.
+// FlashRT article, 7.2): per layer the norm + AWQ + FP4 quantise kernel
+// (k_nvfp4.cu), the gate/up NVFP4 GEMM whose epilogue quantises G and U to
+// NVFP4 and applies the FP4-to-FP4 gated activation, and the down NVFP4 GEMM
+// with the residual epilogue (f4 launches of the tensor-core GEMM,
+// k_gemm_tc.cuh), chained by programmatic dependent launch.  Tensor maps of
+// the fixed buffers are encoded once at plan creation (host and device
+// copies), so a forward can be captured into a graph.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -11,6 +13,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <map>
 #include <vector>
 
 #include "frt_internal.h"
@@ -66,36 +69,43 @@ float word_to_float(unsigned w) {
 
 struct frt_fp4_plan {
     int d = 0, ff = 0, act = 0, M_max = 0, L = 0, M_alloc = 0;
-    // weights: codes [L * rows, K/2], TMEM-ready scales rows * K/16 per layer
-    uint8_t *wg = nullptr, *wu = nullptr, *wd = nullptr;
-    uint8_t *sg = nullptr, *su = nullptr, *sd = nullptr;
+    // weights: codes row-major [L * rows, K/2], TMEM-ready scales rows * K/16
+    // per layer; gate and up as one [W_gate; W_up] arena interleaved in
+    // blocks of 64 rows (2 ff rows a layer), so a 128-row tile holds the gate
+    // and up rows of the same 64 features
+    uint8_t *wgu = nullptr, *wd = nullptr;
+    uint8_t *sgu = nullptr, *sd = nullptr;
     uint16_t *w_norm = nullptr;  // BF16 [L, d]
     float *awq_inv = nullptr;    // fp32 [L, d]: 1 / c
     // activations
     uint8_t *xq = nullptr, *xsf = nullptr;  // [M_alloc, d/2], TMEM-ready
-    uint8_t *gq = nullptr, *gs = nullptr;   // [M_alloc, ff/2], [M_alloc, ff/16]
-    uint8_t *uq = nullptr, *us = nullptr;
     uint8_t *hq = nullptr, *hsf = nullptr;  // [M_alloc, ff/2], TMEM-ready
     uint16_t *rp = nullptr;                 // r' of layer 0 [M_alloc, d]
     uint16_t *res[2] = {nullptr, nullptr};  // layer outputs between layers
     unsigned *amax = nullptr;               // [4]
     int *err = nullptr;
     int num_sms = 0;
-    float *ws = nullptr;                    // split-K partial tiles: num_sms x 128 x 128 fp32
-    int *counters = nullptr;                // split-K arrival counters, one per tile
+    float *ws = nullptr;                    // split-K partials of the down GEMM
+    size_t ws_floats = 0;
+    int *counters = nullptr;                // split-K arrival counters (SPLIT_COUNTERS)
     std::vector<float> s_wg, s_wu, s_wd, s_x, s_g, s_u, s_h;
-    CUtensorMap tm_wg, tm_wu, tm_wd, tm_xq, tm_hq;
-    CUtensorMap tm_xq_n[3], tm_hq_n[3];     // token operands of the weight-streaming role: boxes of 16 / 32 / 64 rows
+    // tensor maps of the fixed buffers (host copies for the kernel parameter,
+    // device copies the kernels read), keyed by (buffer, box rows)
+    std::map<std::pair<int, int>, std::pair<CUtensorMap, int>> tmaps;
+    CUtensorMap *tmap_dev = nullptr;
+    bool pdl = true;                        // programmatic dependent launch (FRT_FFN_NO_PDL=1 disables)
     std::vector<char> loaded, has_awq;
     bool scaled = false;
 };
 
 namespace {
 
+enum F4Buf : int { F_WGU = 0, F_WD = 1, F_XQ = 2, F_HQ = 3 };
+
 void free_fp4(frt_fp4_plan *P) {
-    void *ptrs[] = {P->wg, P->wu,  P->wd,  P->sg,  P->su,     P->sd,     P->w_norm, P->awq_inv, P->xq,
-                    P->xsf, P->gq, P->gs,  P->uq,  P->us,     P->hq,     P->hsf,    P->rp,      P->res[0],
-                    P->res[1], P->amax, P->err, P->ws, P->counters};
+    void *ptrs[] = {P->wgu, P->wd,  P->sgu,     P->sd,  P->w_norm, P->awq_inv, P->xq,       P->xsf,
+                    P->hq,  P->hsf, P->rp,      P->res[0], P->res[1], P->amax,  P->err,      P->ws,
+                    P->counters, P->tmap_dev};
     for (void *p : ptrs)
         if (p) cudaFree(p);
     delete P;
@@ -112,31 +122,48 @@ frt_status check_ready(frt_fp4_plan *P) {
 
 size_t wsf_bytes(size_t rows, size_t K) { return rows * K / 16; }
 
-constexpr int F4_MAX_TILES = 4096;
-
-// Split-K factor of a GEMM with `tiles` output tiles and K / 256 stages:
-// enough splits to put a CTA on most SMs, each split at least four stages
-// long (one CTA per SM: the kernel's shared memory allows no more).
-// Token tile of the weight-streaming role for M tokens (0: the tiled role).
+// The role of a GEMM on M tokens: weight-streaming for at most 64 tokens,
+// else tiled; FRT_F4_SWAP = 0 / 1 forces the tiled / weight-streaming role
+// (the latter for at most 64 tokens; read per launch).
 constexpr int F4_SWAP_MAX_TOKENS = 64;
-// The tiled role measured faster on every shape (the per-stage cost of the
-// block-scaled pipeline does not shrink with the narrower N), so the
-// weight-streaming role runs only when FRT_F4_SWAP=1 (read per launch).
-int f4_swap_n(int M) {
+bool f4_swap(int M) {
     const char *e = getenv("FRT_F4_SWAP");
-    if (M > F4_SWAP_MAX_TOKENS || !e || atoi(e) != 1)
-        return 0;
-    return M <= 16 ? 16 : M <= 32 ? 32 : 64;
+    if (e && e[0] == '0')
+        return false;
+    return M <= F4_SWAP_MAX_TOKENS;
 }
-int f4_swap_idx(int n) { return n == 16 ? 0 : n == 32 ? 1 : 2; }
 
-int f4_splits(int tiles, int KB, int num_sms) {
-    if (tiles > F4_MAX_TILES)
-        return 1;
-    int s = num_sms / tiles;
-    if (s > KB / 4)
-        s = KB / 4;
-    return s < 1 ? 1 : s;
+frt_status build_tmaps(frt_fp4_plan *P) {
+    const int combos[][2] = {{F_WGU, 128}, {F_WD, 128}, {F_XQ, 16}, {F_XQ, 32}, {F_XQ, 64},
+                             {F_XQ, 128},  {F_HQ, 16},  {F_HQ, 32}, {F_HQ, 64}, {F_HQ, 128}};
+    constexpr int N = sizeof(combos) / sizeof(combos[0]);
+    CUtensorMap host[N];
+    const uint64_t L = P->L, D = P->d, F = P->ff, MA = P->M_alloc;
+    for (int i = 0; i < N; ++i) {
+        const int buf = combos[i][0], box = combos[i][1];
+        cudaError_t e;
+        switch (buf) {
+        case F_WGU: e = encode_tmap_u8(&host[i], P->wgu, L * 2 * F, D / 2, box); break;
+        case F_WD: e = encode_tmap_u8(&host[i], P->wd, L * D, F / 2, box); break;
+        case F_XQ: e = encode_tmap_u8(&host[i], P->xq, MA, D / 2, box); break;
+        default: e = encode_tmap_u8(&host[i], P->hq, MA, F / 2, box); break;
+        }
+        if (e != cudaSuccess)
+            return ffail(FRT_ERR_CUDA, "cuTensorMapEncodeTiled failed for buffer %d box %d", buf, box);
+        P->tmaps[std::make_pair(buf, box)] = std::make_pair(host[i], i);
+    }
+    FCK(cudaMalloc(&P->tmap_dev, sizeof(CUtensorMap) * N));
+    FCK(cudaMemcpy(P->tmap_dev, host, sizeof(CUtensorMap) * N, cudaMemcpyHostToDevice));
+    return FRT_OK;
+}
+
+frt_status get_tmap(frt_fp4_plan *P, int buf, int box, CUtensorMap *out, const CUtensorMap **dev) {
+    auto it = P->tmaps.find(std::make_pair(buf, box));
+    if (it == P->tmaps.end())
+        return ffail(FRT_ERR_UNSUPPORTED, "no tensor map for buffer %d box %d", buf, box);
+    *out = it->second.first;
+    *dev = P->tmap_dev + it->second.second;
+    return FRT_OK;
 }
 
 }  // namespace
@@ -168,22 +195,19 @@ FRT_API frt_status frt_fp4_plan_create(int d, int ff, int act, int M_max, int n_
         v->assign(n_layers, 1.0f);
     P->loaded.assign(n_layers, 0);
     P->has_awq.assign(n_layers, 0);
+    if (const char *np = getenv("FRT_FFN_NO_PDL"))
+        P->pdl = !(np[0] == '1');
     const size_t L = n_layers, D = d, F = ff, MA = P->M_alloc;
-    cudaError_t e = cudaSuccess;
-    if (e == cudaSuccess) e = cudaMalloc(&P->wg, L * F * D / 2);
-    if (e == cudaSuccess) e = cudaMalloc(&P->wu, L * F * D / 2);
+    cudaError_t e = cudaDeviceGetAttribute(&P->num_sms, cudaDevAttrMultiProcessorCount, dev);
+    P->ws_floats = (size_t)P->num_sms * 128 * 256;
+    if (e == cudaSuccess) e = cudaMalloc(&P->wgu, L * 2 * F * D / 2);
     if (e == cudaSuccess) e = cudaMalloc(&P->wd, L * D * F / 2);
-    if (e == cudaSuccess) e = cudaMalloc(&P->sg, L * wsf_bytes(F, D));
-    if (e == cudaSuccess) e = cudaMalloc(&P->su, L * wsf_bytes(F, D));
+    if (e == cudaSuccess) e = cudaMalloc(&P->sgu, L * wsf_bytes(2 * F, D));
     if (e == cudaSuccess) e = cudaMalloc(&P->sd, L * wsf_bytes(D, F));
     if (e == cudaSuccess) e = cudaMalloc(&P->w_norm, L * D * 2);
     if (e == cudaSuccess) e = cudaMalloc(&P->awq_inv, L * D * 4);
     if (e == cudaSuccess) e = cudaMalloc(&P->xq, MA * D / 2);
     if (e == cudaSuccess) e = cudaMalloc(&P->xsf, MA * D / 16);
-    if (e == cudaSuccess) e = cudaMalloc(&P->gq, MA * F / 2);
-    if (e == cudaSuccess) e = cudaMalloc(&P->gs, MA * F / 16);
-    if (e == cudaSuccess) e = cudaMalloc(&P->uq, MA * F / 2);
-    if (e == cudaSuccess) e = cudaMalloc(&P->us, MA * F / 16);
     if (e == cudaSuccess) e = cudaMalloc(&P->hq, MA * F / 2);
     if (e == cudaSuccess) e = cudaMalloc(&P->hsf, MA * F / 16);
     if (e == cudaSuccess) e = cudaMalloc(&P->rp, MA * D * 2);
@@ -191,28 +215,20 @@ FRT_API frt_status frt_fp4_plan_create(int d, int ff, int act, int M_max, int n_
     if (e == cudaSuccess) e = cudaMalloc(&P->res[1], MA * D * 2);
     if (e == cudaSuccess) e = cudaMalloc(&P->amax, 16);
     if (e == cudaSuccess) e = cudaMalloc(&P->err, 4);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&P->num_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess) e = cudaMalloc(&P->ws, (size_t)P->num_sms * 128 * 128 * 4);
-    if (e == cudaSuccess) e = cudaMalloc(&P->counters, F4_MAX_TILES * 4);
-    if (e == cudaSuccess) e = cudaMemset(P->counters, 0, F4_MAX_TILES * 4);
-    // the GEMMs read operand rows (and their scales) up to M_alloc: padding stays zero
+    if (e == cudaSuccess) e = cudaMalloc(&P->ws, P->ws_floats * 4);
+    if (e == cudaSuccess) e = cudaMalloc(&P->counters, (size_t)SPLIT_COUNTERS * 4);
+    if (e == cudaSuccess) e = cudaMemset(P->counters, 0, (size_t)SPLIT_COUNTERS * 4);
+    // the GEMMs read operand rows (and their scales) up to the 128-row tile:
+    // padding starts at zero
     if (e == cudaSuccess) e = cudaMemset(P->xq, 0, MA * D / 2);
     if (e == cudaSuccess) e = cudaMemset(P->xsf, 0, MA * D / 16);
     if (e == cudaSuccess) e = cudaMemset(P->hq, 0, MA * F / 2);
     if (e == cudaSuccess) e = cudaMemset(P->hsf, 0, MA * F / 16);
     if (e == cudaSuccess) e = cudaMemset(P->err, 0, 4);
-    if (e == cudaSuccess) e = encode_tmap_u8(&P->tm_wg, P->wg, L * F, D / 2, 128);
-    if (e == cudaSuccess) e = encode_tmap_u8(&P->tm_wu, P->wu, L * F, D / 2, 128);
-    if (e == cudaSuccess) e = encode_tmap_u8(&P->tm_wd, P->wd, L * D, F / 2, 128);
-    if (e == cudaSuccess) e = encode_tmap_u8(&P->tm_xq, P->xq, MA, D / 2, 128);
-    if (e == cudaSuccess) e = encode_tmap_u8(&P->tm_hq, P->hq, MA, F / 2, 128);
-    for (int i = 0; i < 3; ++i) {
-        if (e == cudaSuccess) e = encode_tmap_u8(&P->tm_xq_n[i], P->xq, MA, D / 2, 16u << i);
-        if (e == cudaSuccess) e = encode_tmap_u8(&P->tm_hq_n[i], P->hq, MA, F / 2, 16u << i);
-    }
-    if (e != cudaSuccess) {
+    frt_status st = e == cudaSuccess ? build_tmaps(P) : fcuda_fail(e, "frt_fp4_plan_create");
+    if (st != FRT_OK) {
         free_fp4(P);
-        return fcuda_fail(e, "frt_fp4_plan_create");
+        return st;
     }
     *out = P;
     return FRT_OK;
@@ -262,12 +278,12 @@ FRT_API frt_status frt_fp4_load_weights(frt_fp4_plan_t P, int layer, const void 
     const float sg = scale_of(word_to_float(words[0]));
     const float su = scale_of(word_to_float(words[1]));
     const float sd = scale_of(word_to_float(words[2]));
-    FCK(launch_f4_quant_w(w_gate, (int)ff, (int)d, awq, sg, inv6_of(sg), P->wg + (size_t)layer * ff * d / 2,
-                          P->sg + (size_t)layer * wsf_bytes(ff, d), true, s));
-    FCK(launch_f4_quant_w(w_up, (int)ff, (int)d, awq, su, inv6_of(su), P->wu + (size_t)layer * ff * d / 2,
-                          P->su + (size_t)layer * wsf_bytes(ff, d), true, s));
+    uint8_t *q_gu = P->wgu + (size_t)layer * 2 * ff * d / 2;
+    uint8_t *s_gu = P->sgu + (size_t)layer * wsf_bytes(2 * ff, d);
+    FCK(launch_f4_quant_w(w_gate, (int)ff, (int)d, awq, sg, inv6_of(sg), q_gu, s_gu, 1, s));
+    FCK(launch_f4_quant_w(w_up, (int)ff, (int)d, awq, su, inv6_of(su), q_gu, s_gu, 2, s));
     FCK(launch_f4_quant_w(w_down, (int)d, (int)ff, nullptr, sd, inv6_of(sd), P->wd + (size_t)layer * d * ff / 2,
-                          P->sd + (size_t)layer * wsf_bytes(d, ff), true, s));
+                          P->sd + (size_t)layer * wsf_bytes(d, ff), 0, s));
     FCK(cudaStreamSynchronize(s));
     P->s_wg[layer] = sg;
     P->s_wu[layer] = su;
@@ -286,84 +302,103 @@ cudaError_t f4_norm(frt_fp4_plan *P, int l, const void *r, const void *h, int M,
     return launch_f4_norm_quant(r, h, P->w_norm + (size_t)l * P->d, P->has_awq[l] ? P->awq_inv + (size_t)l * P->d
                                                                                    : nullptr,
                                 M, P->d, F4_RMS_EPS, sx, inv6_of(sx), h ? P->rp : nullptr, P->xq, P->xsf,
-                                P->amax, measure, s);
+                                P->amax, measure, s, P->pdl);
 }
 
-// N2: the gate (up = false) or up GEMM; epi F4_EPI_FP4 (into G / U) or
-// F4_EPI_AMAX (into amax[0] / amax[1]).
-cudaError_t f4_gate_up(frt_fp4_plan *P, int l, bool up, int M, int epi, cudaStream_t s) {
-    const size_t d = P->d, ff = P->ff;
-    const int sw = f4_swap_n(M);
-    F4GemmParams p;
-    memset(&p, 0, sizeof p);
-    const uint8_t *wsf = (up ? P->su : P->sg) + (size_t)l * wsf_bytes(ff, d);
-    p.sfa = sw ? wsf : P->xsf;
-    p.sfb = sw ? P->xsf : wsf;
-    p.a_row0 = sw ? l * P->ff : 0;
-    p.b_row0 = sw ? 0 : l * P->ff;
-    p.M = M;
-    p.K = P->d;
+// Tensor maps and row offsets of one GEMM of layer l: the weight buffer
+// (rows_per_layer rows a layer) and the token buffer, in the launch's role.
+frt_status f4_maps(frt_fp4_plan *P, GemmLaunch &g, int wbuf, int xbuf, int l, int rows_per_layer) {
+    frt_status st;
+    if (g.swap) {
+        if ((st = get_tmap(P, wbuf, 128, &g.tmP, &g.p.gtm_p)) != FRT_OK) return st;
+        if ((st = get_tmap(P, xbuf, g.bn, &g.tmQ, &g.p.gtm_q)) != FRT_OK) return st;
+        g.p.p_row0 = l * rows_per_layer;
+        g.p.q_row0 = 0;
+    } else {
+        if ((st = get_tmap(P, xbuf, 128, &g.tmP, &g.p.gtm_p)) != FRT_OK) return st;
+        if ((st = get_tmap(P, wbuf, 128, &g.tmQ, &g.p.gtm_q)) != FRT_OK) return st;
+        g.p.p_row0 = 0;
+        g.p.q_row0 = l * rows_per_layer;
+    }
+    return FRT_OK;
+}
+
+// N2 + N3: the fused gate/up GEMM: G and U as NVFP4, act(dec G) * dec U
+// requantised into the A buffers (epi EPI_F4_GATED), or the calibration
+// amaxes (EPI_F4_AMAX_GU: amax[0], amax[1]; EPI_F4_AMAX_H: amax[2]).  dbg: G
+// and U codes and row-major scales (trace), or nulls.
+frt_status f4_gate_up(frt_fp4_plan *P, int l, int M, int epi, cudaStream_t s, uint8_t *const dbg[4]) {
+    GemmLaunch g;
+    memset(&g.p, 0, sizeof g.p);
+    plan_gemm(g, f4_swap(M), M, 2 * P->ff, P->d / 2, P->num_sms, 1, nullptr, true);
+    frt_status st = f4_maps(P, g, F_WGU, F_XQ, l, 2 * P->ff);
+    if (st != FRT_OK)
+        return st;
+    GemmParams &p = g.p;
     p.epi = epi;
-    p.alpha = P->s_x[l] * (up ? P->s_wu[l] : P->s_wg[l]);
-    p.s_out = up ? P->s_u[l] : P->s_g[l];
-    p.inv6_out = inv6_of(p.s_out);
-    p.out = up ? P->uq : P->gq;
+    p.alpha = P->s_x[l] * P->s_wg[l];
+    p.alpha_u = P->s_x[l] * P->s_wu[l];
+    p.s_g = P->s_g[l];
+    p.inv6_g = inv6_of(p.s_g);
+    p.s_u = P->s_u[l];
+    p.inv6_u = inv6_of(p.s_u);
+    p.s_h = P->s_h[l];
+    p.inv6_h = inv6_of(p.s_h);
+    p.out = P->hq;
     p.ldo = P->ff / 2;
-    p.out_sf = up ? P->us : P->gs;
-    p.ldsf = P->ff / 16;
-    p.amax = P->amax + (up ? 1 : 0);
+    p.out_sf = P->hsf;
+    p.ff = P->ff;
+    p.act = P->act;
+    p.amax = P->amax;
+    p.sf_w = P->sgu;
+    p.sf_x = P->xsf;
     p.err = P->err;
-    p.splits = f4_splits((P->ff / 128) * (sw ? 1 : (M + 127) / 128), P->d / 256, P->num_sms);
-    p.ws = P->ws;
-    p.counters = P->counters;
-    p.w_tiles = (up ? P->wu : P->wg) + (size_t)l * ff * d / 2;
-    const CUtensorMap &w = up ? P->tm_wu : P->tm_wg;
-    if (sw)
-        return launch_f4_gemm(w, P->tm_xq_n[f4_swap_idx(sw)], p, P->ff, sw, s);
-    return launch_f4_gemm(P->tm_xq, w, p, P->ff, 0, s);
-}
-
-// N3: A = NVFP4(act(G) * U) into the A buffers (measure: amax into amax[2]).
-cudaError_t f4_geglu(frt_fp4_plan *P, int l, int M, bool measure, cudaStream_t s) {
-    return launch_f4_geglu(P->gq, P->gs, P->s_g[l], P->uq, P->us, P->s_u[l], P->act, M, P->ff, P->s_h[l],
-                           inv6_of(P->s_h[l]), P->hq, P->hsf, P->amax + 2, measure, s);
+    if (dbg) {
+        p.dbg_gq = dbg[0];
+        p.dbg_gs = dbg[1];
+        p.dbg_uq = dbg[2];
+        p.dbg_us = dbg[3];
+    }
+    FCK(launch_gemm(g, s, P->pdl));
+    return FRT_OK;
 }
 
 // N4: out = bf16(resid + acc(A, W_d') * alpha).
-cudaError_t f4_down(frt_fp4_plan *P, int l, const void *resid, void *out, int M, cudaStream_t s) {
-    const int sw = f4_swap_n(M);
-    F4GemmParams p;
-    memset(&p, 0, sizeof p);
-    const uint8_t *wsf = P->sd + (size_t)l * wsf_bytes(P->d, P->ff);
-    p.sfa = sw ? wsf : P->hsf;
-    p.sfb = sw ? P->hsf : wsf;
-    p.a_row0 = sw ? l * P->d : 0;
-    p.b_row0 = sw ? 0 : l * P->d;
-    p.M = M;
-    p.K = P->ff;
-    p.epi = F4_EPI_RESID;
+frt_status f4_down(frt_fp4_plan *P, int l, const void *resid, void *out, int M, cudaStream_t s) {
+    GemmLaunch g;
+    memset(&g.p, 0, sizeof g.p);
+    int force = 0;
+    if (const char *e = getenv("FRT_F4_DOWN_SPLITS"))
+        force = atoi(e);
+    plan_gemm(g, f4_swap(M), M, P->d, P->ff / 2, P->num_sms, force, nullptr, true);
+    frt_status st = f4_maps(P, g, F_WD, F_HQ, l, P->d);
+    if (st != FRT_OK)
+        return st;
+    if (gemm_ws_floats(g) > P->ws_floats || (g.p.splits > 1 && gemm_tiles(g) > MAX_SPLIT_TILES))
+        return ffail(FRT_ERR_UNSUPPORTED, "split-K workspace too small for M=%d", M);
+    GemmParams &p = g.p;
+    p.epi = EPI_RESID;
     p.alpha = P->s_h[l] * P->s_wd[l];
     p.out = out;
     p.ldo = P->d;
-    p.resid = static_cast<const uint16_t *>(resid);
+    p.resid = resid;
     p.ldr = P->d;
-    p.err = P->err;
-    p.splits = f4_splits((P->d / 128) * (sw ? 1 : (M + 127) / 128), P->ff / 256, P->num_sms);
+    p.sf_w = P->sd;
+    p.sf_x = P->hsf;
     p.ws = P->ws;
-    p.counters = P->counters;
-    p.w_tiles = P->wd + (size_t)l * P->d * P->ff / 2;
-    if (sw)
-        return launch_f4_gemm(P->tm_wd, P->tm_hq_n[f4_swap_idx(sw)], p, P->d, sw, s);
-    return launch_f4_gemm(P->tm_hq, P->tm_wd, p, P->d, 0, s);
+    p.counters = split_counters(P->counters, p.splits);
+    p.err = P->err;
+    FCK(launch_gemm(g, s, P->pdl));
+    return FRT_OK;
 }
 
-frt_status f4_layer(frt_fp4_plan *P, int l, const void *r, const void *h, void *out, int M, cudaStream_t s) {
+frt_status f4_layer(frt_fp4_plan *P, int l, const void *r, const void *h, void *out, int M, cudaStream_t s,
+                    uint8_t *const dbg[4] = nullptr) {
     FCK(f4_norm(P, l, r, h, M, false, s));
-    FCK(f4_gate_up(P, l, false, M, F4_EPI_FP4, s));
-    FCK(f4_gate_up(P, l, true, M, F4_EPI_FP4, s));
-    FCK(f4_geglu(P, l, M, false, s));
-    FCK(f4_down(P, l, h ? static_cast<const void *>(P->rp) : r, out, M, s));
-    return FRT_OK;
+    frt_status st = f4_gate_up(P, l, M, EPI_F4_GATED, s, dbg);
+    if (st != FRT_OK)
+        return st;
+    return f4_down(P, l, h ? static_cast<const void *>(P->rp) : r, out, M, s);
 }
 
 frt_status check_call(frt_fp4_plan *P, const void *r, const void *h, const void *out, int M) {
@@ -424,17 +459,17 @@ FRT_API frt_status frt_fp4_calibrate(frt_fp4_plan_t P, const void *const *residu
         return fcuda_fail(e, "calibration scratch");
     }
     std::vector<const void *> cur(residual, residual + n_batches);
-    auto read_amax = [&](float *out, int n) -> cudaError_t {
+    auto read_amax = [&](float *out) -> cudaError_t {
         unsigned w[4];
         cudaError_t e2 = cudaMemcpyAsync(w, P->amax, 16, cudaMemcpyDeviceToHost, s);
         if (e2 == cudaSuccess)
             e2 = cudaStreamSynchronize(s);
-        for (int i = 0; i < n; ++i)
+        for (int i = 0; i < 4; ++i)
             out[i] = scale_of(word_to_float(w[i]));
         return e2;
     };
     st = FRT_OK;
-    for (int l = 0; l < P->L && st == FRT_OK; ++l) {
+    for (int l = 0; l < P->L && st == FRT_OK && e == cudaSuccess; ++l) {
         auto hid = [&](int b) -> const void * { return (l == 0 && hidden) ? hidden[b] : nullptr; };
         float sc[4];
         // s_x
@@ -442,43 +477,31 @@ FRT_API frt_status frt_fp4_calibrate(frt_fp4_plan_t P, const void *const *residu
         for (int b = 0; b < n_batches && e == cudaSuccess; ++b)
             e = f4_norm(P, l, cur[b], hid(b), M, true, s);
         if (e == cudaSuccess)
-            e = read_amax(sc, 1);
+            e = read_amax(sc);
         if (e != cudaSuccess)
             break;
         P->s_x[l] = sc[0];
-        // s_g, s_u
-        e = cudaMemsetAsync(P->amax, 0, 16, s);
-        for (int b = 0; b < n_batches && e == cudaSuccess; ++b) {
-            e = f4_norm(P, l, cur[b], hid(b), M, false, s);
-            if (e == cudaSuccess)
-                e = f4_gate_up(P, l, false, M, F4_EPI_AMAX, s);
-            if (e == cudaSuccess)
-                e = f4_gate_up(P, l, true, M, F4_EPI_AMAX, s);
+        // s_g and s_u, then s_h with G and U quantised by them
+        for (int pass = 0; pass < 2 && st == FRT_OK && e == cudaSuccess; ++pass) {
+            e = cudaMemsetAsync(P->amax, 0, 16, s);
+            for (int b = 0; b < n_batches && e == cudaSuccess && st == FRT_OK; ++b) {
+                e = f4_norm(P, l, cur[b], hid(b), M, false, s);
+                if (e == cudaSuccess)
+                    st = f4_gate_up(P, l, M, pass == 0 ? EPI_F4_AMAX_GU : EPI_F4_AMAX_H, s, nullptr);
+            }
+            if (e == cudaSuccess && st == FRT_OK)
+                e = read_amax(sc);
+            if (e != cudaSuccess || st != FRT_OK)
+                break;
+            if (pass == 0) {
+                P->s_g[l] = sc[0];
+                P->s_u[l] = sc[1];
+            } else {
+                P->s_h[l] = sc[2];
+            }
         }
-        if (e == cudaSuccess)
-            e = read_amax(sc, 2);
-        if (e != cudaSuccess)
-            break;
-        P->s_g[l] = sc[0];
-        P->s_u[l] = sc[1];
-        // s_h
-        e = cudaMemsetAsync(P->amax, 0, 16, s);
-        for (int b = 0; b < n_batches && e == cudaSuccess; ++b) {
-            e = f4_norm(P, l, cur[b], hid(b), M, false, s);
-            if (e == cudaSuccess)
-                e = f4_gate_up(P, l, false, M, F4_EPI_FP4, s);
-            if (e == cudaSuccess)
-                e = f4_gate_up(P, l, true, M, F4_EPI_FP4, s);
-            if (e == cudaSuccess)
-                e = f4_geglu(P, l, M, true, s);
-        }
-        if (e == cudaSuccess)
-            e = read_amax(sc, 3);
-        if (e != cudaSuccess)
-            break;
-        P->s_h[l] = sc[2];
         // the layer's outputs feed the next layer
-        if (l + 1 < P->L) {
+        if (l + 1 < P->L && e == cudaSuccess && st == FRT_OK) {
             uint16_t *dst = buf[l & 1];
             for (int b = 0; b < n_batches && st == FRT_OK; ++b)
                 st = f4_layer(P, l, cur[b], hid(b), dst + per * b, M, s);
@@ -541,8 +564,12 @@ FRT_API frt_status frt_fp4_debug_trace(frt_fp4_plan_t P, int layer, const void *
         return st;
     if (layer < 0 || layer >= P->L)
         return ffail(FRT_ERR_INVALID_ARG, "layer %d out of range [0, %d)", layer, P->L);
+    if ((g_codes || g_sf || u_codes || u_sf) && !(g_codes && g_sf && u_codes && u_sf))
+        return ffail(FRT_ERR_INVALID_ARG, "g/u codes and scales: all four or none");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    st = f4_layer(P, layer, residual_in, hidden_in, out, M, s);
+    uint8_t *const dbg[4] = {static_cast<uint8_t *>(g_codes), static_cast<uint8_t *>(g_sf),
+                             static_cast<uint8_t *>(u_codes), static_cast<uint8_t *>(u_sf)};
+    st = f4_layer(P, layer, residual_in, hidden_in, out, M, s, g_codes ? dbg : nullptr);
     if (st != FRT_OK)
         return st;
     const size_t d = P->d, ff = P->ff, m = (size_t)M, mt = (size_t)(M + 127) / 128 * 128;
@@ -550,15 +577,22 @@ FRT_API frt_status frt_fp4_debug_trace(frt_fp4_plan_t P, int layer, const void *
     if (r_prime && hidden_in) FCK(cudaMemcpyAsync(r_prime, P->rp, m * d * 2, k, s));
     if (x_codes) FCK(cudaMemcpyAsync(x_codes, P->xq, m * d / 2, k, s));
     if (x_sf) FCK(cudaMemcpyAsync(x_sf, P->xsf, mt * d / 16, k, s));
-    if (g_codes) FCK(cudaMemcpyAsync(g_codes, P->gq, m * ff / 2, k, s));
-    if (g_sf) FCK(cudaMemcpyAsync(g_sf, P->gs, m * ff / 16, k, s));
-    if (u_codes) FCK(cudaMemcpyAsync(u_codes, P->uq, m * ff / 2, k, s));
-    if (u_sf) FCK(cudaMemcpyAsync(u_sf, P->us, m * ff / 16, k, s));
     if (h_codes) FCK(cudaMemcpyAsync(h_codes, P->hq, m * ff / 2, k, s));
     if (h_sf) FCK(cudaMemcpyAsync(h_sf, P->hsf, mt * ff / 16, k, s));
     FCK(cudaStreamSynchronize(s));
     return FRT_OK;
 }
+
+namespace {
+
+// Byte offset of (row, 16-element group g) in the TMEM-ready scale order of
+// an operand with K elements per row (as the kernels' sf_offset).
+size_t sf_off(size_t row, size_t g, size_t K) {
+    const size_t r = row & 127;
+    return ((row >> 7) * (K >> 6) + (g >> 2)) * 512u + (r & 31) * 16 + (r >> 5) * 4 + (g & 3);
+}
+
+}  // namespace
 
 FRT_API frt_status frt_fp4_debug_weights(frt_fp4_plan_t P, int layer, int which, void *codes, void *sf,
                                          frt_stream_t stream) {
@@ -570,10 +604,26 @@ FRT_API frt_status frt_fp4_debug_weights(frt_fp4_plan_t P, int layer, int which,
         return ffail(FRT_ERR_NOT_READY, "weights of layer %d not loaded", layer);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const size_t d = P->d, ff = P->ff, n = d * ff;
-    const uint8_t *q = which == 0 ? P->wg : which == 1 ? P->wu : P->wd;
-    const uint8_t *f = which == 0 ? P->sg : which == 1 ? P->su : P->sd;
-    if (codes) FCK(cudaMemcpyAsync(codes, q + (size_t)layer * n / 2, n / 2, cudaMemcpyDeviceToDevice, s));
-    if (sf) FCK(cudaMemcpyAsync(sf, f + (size_t)layer * n / 16, n / 16, cudaMemcpyDeviceToDevice, s));
+    if (which == 2) {
+        if (codes) FCK(cudaMemcpyAsync(codes, P->wd + (size_t)layer * n / 2, n / 2, cudaMemcpyDeviceToDevice, s));
+        if (sf) FCK(cudaMemcpyAsync(sf, P->sd + (size_t)layer * n / 16, n / 16, cudaMemcpyDeviceToDevice, s));
+        FCK(cudaStreamSynchronize(s));
+        return FRT_OK;
+    }
+    // gate or up: pick its rows out of the layer's interleaved arena (host side)
+    std::vector<uint8_t> arena_q(2 * n / 2), arena_s(2 * n / 16), q(n / 2), f(n / 16);
+    FCK(cudaMemcpyAsync(arena_q.data(), P->wgu + (size_t)layer * 2 * n / 2, 2 * n / 2, cudaMemcpyDeviceToHost, s));
+    FCK(cudaMemcpyAsync(arena_s.data(), P->sgu + (size_t)layer * 2 * n / 16, 2 * n / 16, cudaMemcpyDeviceToHost, s));
+    FCK(cudaStreamSynchronize(s));
+    const size_t G = d / 16;
+    for (size_t j = 0; j < ff; ++j) {
+        const size_t src = (j / 64) * 128 + (which == 1 ? 64 : 0) + j % 64;
+        memcpy(&q[j * (d / 2)], &arena_q[src * (d / 2)], d / 2);
+        for (size_t g = 0; g < G; ++g)
+            f[sf_off(j, g, d)] = arena_s[sf_off(src, g, d)];
+    }
+    if (codes) FCK(cudaMemcpyAsync(codes, q.data(), n / 2, cudaMemcpyHostToDevice, s));
+    if (sf) FCK(cudaMemcpyAsync(sf, f.data(), n / 16, cudaMemcpyHostToDevice, s));
     FCK(cudaStreamSynchronize(s));
     return FRT_OK;
 }
@@ -587,32 +637,39 @@ FRT_API frt_status frt_nvfp4_gemm(const void *a_codes, const void *a_sf, const v
     if (M < 1 || M > 65536 || N < 128 || N % 128 || K < 256 || K % 256)
         return ffail(FRT_ERR_INVALID_ARG, "M=%d N=%d K=%d: need 1 <= M <= 65536, N %% 128 == 0, K %% 256 == 0", M,
                      N, K);
-    const int tiles = (N / 128) * (f4_swap_n(M) ? 1 : (M + 127) / 128);
-    if (splits < 1 || splits > K / 256 || (splits > 1 && (!ws || !counters || !al16(ws) || tiles > F4_MAX_TILES)))
+    const bool swap = f4_swap(M);
+    const int tiles = (N / 128) * (swap ? 1 : (M + 127) / 128);
+    if (splits < 1 || splits > K / 256 || (splits > 1 && (!ws || !counters || !al16(ws) || tiles > MAX_SPLIT_TILES)))
         return ffail(FRT_ERR_INVALID_ARG, "splits=%d: need 1 <= splits <= K / 256 and, above 1, ws and counters",
                      splits);
-    // the plan's choice of role: weight-streaming for at most 64 tokens
-    const int sw = f4_swap_n(M);
-    CUtensorMap ta, tb;
-    if (encode_tmap_u8(&ta, a_codes, (uint64_t)M, (uint64_t)K / 2, sw ? (uint32_t)sw : 128u) != cudaSuccess ||
-        encode_tmap_u8(&tb, b_codes, (uint64_t)N, (uint64_t)K / 2, 128) != cudaSuccess)
+    int dev = 0, sms = 0;
+    FCK(cudaGetDevice(&dev));
+    FCK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    GemmLaunch g;
+    memset(&g.p, 0, sizeof g.p);
+    plan_gemm(g, swap, M, N, K / 2, sms, splits, nullptr, true);
+    // swap: A (the tokens) is the narrow operand, B (the weights) the 128-row one
+    cudaError_t e1, e2;
+    if (swap) {
+        e1 = encode_tmap_u8(&g.tmP, b_codes, (uint64_t)N, (uint64_t)K / 2, 128);
+        e2 = encode_tmap_u8(&g.tmQ, a_codes, (uint64_t)M, (uint64_t)K / 2, (uint32_t)g.bn);
+    } else {
+        e1 = encode_tmap_u8(&g.tmP, a_codes, (uint64_t)M, (uint64_t)K / 2, 128);
+        e2 = encode_tmap_u8(&g.tmQ, b_codes, (uint64_t)N, (uint64_t)K / 2, 128);
+    }
+    if (e1 != cudaSuccess || e2 != cudaSuccess)
         return ffail(FRT_ERR_CUDA, "cuTensorMapEncodeTiled failed");
-    F4GemmParams p;
-    memset(&p, 0, sizeof p);
-    p.sfa = static_cast<const uint8_t *>(sw ? b_sf : a_sf);
-    p.sfb = static_cast<const uint8_t *>(sw ? a_sf : b_sf);
-    p.M = M;
-    p.K = K;
-    p.epi = F4_EPI_F32;
+    GemmParams &p = g.p;
+    p.sf_w = static_cast<const uint8_t *>(b_sf);
+    p.sf_x = static_cast<const uint8_t *>(a_sf);
+    p.epi = EPI_F32;
     p.alpha = alpha;
     p.out = out;
     p.ldo = N;
-    p.err = err;
-    p.splits = splits;
     p.ws = ws;
     p.counters = counters;
-    FCK(sw ? launch_f4_gemm(tb, ta, p, N, sw, static_cast<cudaStream_t>(stream))
-           : launch_f4_gemm(ta, tb, p, N, 0, static_cast<cudaStream_t>(stream)));
+    p.err = err;
+    FCK(launch_gemm(g, static_cast<cudaStream_t>(stream), false));
     return FRT_OK;
 }
 
@@ -625,6 +682,8 @@ FRT_API frt_status frt_fp4_device_status(frt_fp4_plan_t P, frt_stream_t stream) 
     FCK(cudaStreamSynchronize(s));
     if (err) {
         FCK(cudaMemset(P->err, 0, 4));
+        // a launch that gave up may have left split-K counters mid-generation
+        FCK(cudaMemset(P->counters, 0, (size_t)SPLIT_COUNTERS * 4));
         return ffail(FRT_ERR_DEVICE_TIMEOUT, "a kernel gave up a bounded wait (code %d)", err);
     }
     return FRT_OK;

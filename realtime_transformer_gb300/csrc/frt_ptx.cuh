@@ -364,6 +364,43 @@ __device__ __forceinline__ void mbar_arrive_cluster_release(uint32_t bar) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// ---------------------------------------------- block-scaled NVFP4 MMA --
+// Shared-memory descriptor of a 512-byte scale block: 32 rows of 16 bytes,
+// no swizzle, 8-row core matrices 128 bytes apart (leading and stride byte
+// offsets both 128, so either reading of the 16-byte-wide block agrees).
+__device__ __forceinline__ uint64_t smem_desc_sf(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)(128u >> 4) << 16;
+    d |= (uint64_t)(128u >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    return d;
+}
+
+__device__ __forceinline__ void tmem_cp_sf(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// D[tmem] (+)= (A * scale_A) (B * scale_B)^T, E2M1 operands with E4M3 scales
+// per 16 elements, K = 64.
+__device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa,
+                                         uint32_t sfb, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+        : "memory");
+}
+
+// Instruction descriptor of the block-scaled kinds: A and B E2M1 (format 1),
+// both K-major, N >> 3 at bit 17, scale format UE4M3 (bit 23 clear), M >> 4
+// at bit 24, scale-factor ids 0.
+__host__ __device__ constexpr uint32_t idesc_nvf4(int m, int n) {
+    return (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
 // ---------------------------------------------- programmatic dependent launch --
 // Block until the grids this grid depends on have completed and their memory
 // is visible.  A no-op when the launch had no programmatic dependency.

@@ -1,8 +1,9 @@
 """FP4Plan: torch-facing wrapper of the NVFP4 sublayer stack's C ABI
 (include/frt_nvfp4.h; itsolotime FlashRT article, 7.2): norm + AWQ + NVFP4
-quantise, gate and up NVFP4 GEMMs emitting FP4, GeGLU FP4 -> FP4, NVFP4 down
-GEMM + residual.  PyTorch supplies device memory and streams; every step runs
-in libfrt_ffn.so."""
+quantise, the gate/up NVFP4 GEMM that forms G and U as NVFP4 and applies the
+FP4 -> FP4 gated activation in its epilogue, NVFP4 down GEMM + residual.
+PyTorch supplies device memory and streams; every step runs in
+libfrt_ffn.so."""
 from __future__ import annotations
 
 import torch
@@ -84,7 +85,7 @@ class FP4Plan:
         return t
 
     def weights(self, layer, which, stream=None):
-        """which: 'gate', 'up' or 'down' -> (codes [rows, K/2], TMEM-ready scales)."""
+        """which: 'gate', 'up' or 'down' -> (codes row-major [rows, K/2], TMEM-ready scales)."""
         w = {"gate": 0, "up": 1, "down": 2}[which]
         rows, K = (self.ff, self.d) if w < 2 else (self.d, self.ff)
         dev = torch.device("cuda")
@@ -99,7 +100,8 @@ class FP4Plan:
 
 def nvfp4_gemm(a_codes, a_sf, b_codes, b_sf, M, N_, K, alpha=1.0, splits=1, stream=None):
     """Diagnostic block-scaled GEMM: fp32 [M, N] = alpha * A . B^T over NVFP4
-    operands, split-K into `splits` partials summed in split order."""
+    operands, split-K into at most `splits` partials summed in split order
+    (fresh zeroed arrival counters each call)."""
     dev = a_codes.device
     out = torch.empty((M, N_), dtype=torch.float32, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)

@@ -57,15 +57,6 @@ def sf_from_tmem(buf, rows, K):
     return np.asarray(buf, np.uint8)[_sf_index(rows, K)]
 
 
-def untile_weights(buf, rows, K):
-    """The plan's tiled weight layout -> row-major packed codes [rows, K/2]."""
-    t = np.asarray(buf, np.uint8).reshape(rows // 128, K // 256, 128, 8, 16)  # tile, stage, row, chunk, byte
-    r = np.arange(128)[:, None]
-    c = np.arange(8)[None, :]
-    t = t[:, :, r, c ^ (r % 8), :]                                             # undo the chunk swizzle
-    return t.transpose(0, 2, 1, 3, 4).reshape(rows, K // 2)
-
-
 def canon(codes):
     """E2M1 codes with -0 (8) read as +0."""
     c = np.asarray(codes, np.uint8)
@@ -131,21 +122,19 @@ def dev(a):
                                      (1, 256, 2048, 3), (50, 128, 4096, 8), (300, 256, 1024, 2)])
 def test_block_scaled_gemm_matches_the_exact_sum(M, N, K, S, swap, monkeypatch):
     from realtime_transformer_gb300.nvfp4 import nvfp4_gemm
-    if swap:
-        if M > 64:
-            pytest.skip("the weight-streaming role takes at most 64 tokens")
-        monkeypatch.setenv("FRT_F4_SWAP", "1")
+    if swap and M > 64:
+        pytest.skip("the weight-streaming role takes at most 64 tokens")
+    monkeypatch.setenv("FRT_F4_SWAP", "1" if swap else "0")
     rng = np.random.default_rng(M * 7 + N + K)
     qa = rng.integers(0, 16, (M, K)).astype(np.uint8)
     qb = rng.integers(0, 16, (N, K)).astype(np.uint8)
     sa = rng.integers(0x28, 0x48, (M, K // 16)).astype(np.uint8)
     sb = rng.integers(0x28, 0x48, (N, K // 16)).astype(np.uint8)
     alpha = 0.375
-    out, err, counters = nvfp4_gemm(dev(pack(qa)), dev(sf_to_tmem(sa)), dev(pack(qb)), dev(sf_to_tmem(sb)), M, N, K,
-                                    alpha, splits=S)
+    out, err, _ = nvfp4_gemm(dev(pack(qa)), dev(sf_to_tmem(sa)), dev(pack(qb)), dev(sf_to_tmem(sb)), M, N, K,
+                             alpha, splits=S)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
-    assert int(counters.abs().sum().item()) == 0, "split-K counters must be re-armed"
     ref = (oracle.nvfp4_gemm(qa, sa, qb, sb).astype(np.float64) * alpha)
     got = out.cpu().numpy().astype(np.float64)
     rms = np.sqrt((ref ** 2).mean())
@@ -232,7 +221,7 @@ def test_weight_preparation_is_bit_exact(layer_case):
                                    ("down", L.down, wl.d, wl.ff, s_w[2])]:
         codes, sf = plan.weights(0, which)
         assert np.float32(s) == np.float32(ref.s), which
-        assert np.array_equal(canon(unpack(untile_weights(codes.cpu().numpy(), rows, K))), canon(ref.q)), which
+        assert np.array_equal(canon(unpack(codes.cpu().numpy())), canon(ref.q)), which
         assert np.array_equal(sf_from_tmem(sf.cpu().numpy(), rows, K), ref.sb), which
 
 
@@ -283,6 +272,7 @@ def test_weight_streaming_role_matches_the_tiled_role(layer_case, monkeypatch):
     if c["wl"].M > 64:
         pytest.skip("the weight-streaming role takes at most 64 tokens")
     r, h = c["r"].cuda(), c["h"].cuda()
+    monkeypatch.setenv("FRT_F4_SWAP", "0")
     a = c["plan"].trace(0, r, h)
     monkeypatch.setenv("FRT_F4_SWAP", "1")
     b = c["plan"].trace(0, r, h)

@@ -17,7 +17,7 @@ import torch
 import oracle
 import synthetic
 from parity import bits, check_bf16, cosine
-from test_gpu_nvfp4 import check_nvfp4, canon, sf_from_tmem, unpack, untile_weights
+from test_gpu_nvfp4 import check_nvfp4, canon, sf_from_tmem, unpack
 
 pytestmark = pytest.mark.gpu
 
@@ -43,7 +43,7 @@ def test_full_size_nvfp4_layer(name):
                                          ("down", L.down, d, ff, s_w[2])]:
             codes, sf = plan.weights(0, which)
             assert np.float32(s) == np.float32(ref.s), which
-            assert np.array_equal(canon(unpack(untile_weights(codes.cpu().numpy(), rows_w, K))), canon(ref.q)), which
+            assert np.array_equal(canon(unpack(codes.cpu().numpy())), canon(ref.q)), which
             assert np.array_equal(sf_from_tmem(sf.cpu().numpy(), rows_w, K), ref.sb), which
             del codes, sf
         plan.set_scales([[sc.s_x, sc.s_g, sc.s_u, sc.s_h]])
