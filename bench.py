@@ -686,6 +686,22 @@ def run_fp4(args, wl, world, rank, local):
             plan.forward(r, h, out=out, stream=stream)
     torch.cuda.synchronize()
 
+    if args.launch_list:
+        # profiling aid: warm replays, then the given number inside an NVTX
+        # range "replay" that ncu can select (--nvtx --nvtx-include "replay/")
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize()
+        torch.cuda.nvtx.range_push("replay")
+        for _ in range(args.launch_list):
+            graph.replay()
+        torch.cuda.synchronize()
+        torch.cuda.nvtx.range_pop()
+        plan.device_status(stream)
+        plan.close()
+        return {"launch_list": wl.name, "sublayer": "ffn_nvfp4", "replays": args.launch_list,
+                "launches_per_replay": 3 * wl.L}
+
     def timed(fn, n, warm):
         for _ in range(warm):
             with torch.cuda.stream(stream):

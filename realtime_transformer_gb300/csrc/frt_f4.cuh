@@ -10,9 +10,11 @@
 // (dec(q) * dec(b)) * s.
 #pragma once
 
+#include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
 #include <cstdint>
+#include <cstring>
 
 namespace frt {
 namespace {
@@ -66,31 +68,35 @@ __device__ __forceinline__ uint32_t quant_block16(const float *v, float s, float
 // K elements per row in the TMEM-ready layout: per 128-row tile and 64-element
 // K chunk a 512-byte block (tiles major, chunks minor), byte
 // (r % 32) * 16 + (r / 32) * 4 + j holding row r of the tile, group j of the
-// chunk -- the order in which one tcgen05.cp of shape 32x128b with warpx4
-// replication puts a block where a kind::mxf4nvf4 MMA with scale_vec::4X
-// reads the scales of its 128 rows.
+// chunk: lane l of each TMEM lane quarter holds the block's 16 bytes at
+// 16 l (rows l, l + 32, l + 64, l + 96 in its 4 columns), the replicated
+// order in which a kind::mxf4nvf4 MMA with scale_vec::4X reads the scales of
+// its 128 rows.
 __device__ __forceinline__ size_t sf_offset(int row, int g, int K) {
     const int r = row & 127;
     return ((size_t)(row >> 7) * (size_t)(K >> 6) + (size_t)(g >> 2)) * 512u + (size_t)((r & 31) * 16 + (r >> 5) * 4 +
                                                                                         (g & 3));
 }
 
-// E2M1 code of one fp32 value (low nibble of a pair conversion with 0).
-__device__ __forceinline__ uint32_t e2m1_one(float x) {
-    uint32_t v;
-    asm("{\n\t.reg .b8 b;\n\tcvt.rn.satfinite.e2m1x2.f32 b, %2, %1;\n\tcvt.u32.u8 %0, b;\n\t}"
-        : "=r"(v)
-        : "f"(x), "f"(0.0f));
-    return v & 15u;
-}
-
-// The 16 values of a block: (dec(q_j) * dec(b)) * s.
+// The 16 values of a block: (dec(q_j) * dec(b)) * s.  dec(q_j) * dec(b) is
+// formed in f16 pairs: an E2M1 value (2 significant bits, 0.5 .. 6) times an
+// E4M3 scale (4 significant bits, 2^-9 .. 448) has at most 6 significant bits
+// and lies in [2^-10, 2688] (or is 0), so the f16 product is exact and equals
+// the fp32 one; only the multiplication by s rounds.
 __device__ __forceinline__ void dequant_block16(uint2 q, uint32_t b, float s, float *out) {
-    const float sb = e4m3_dec(b);
+    const __half sbh = __float2half_rn(e4m3_dec(b));  // exact: E4M3 values are f16 values
+    const __half2 sb2 = __halves2half2(sbh, sbh);
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        const uint32_t w = j < 8 ? q.x : q.y;
-        out[j] = __fmul_rn(__fmul_rn(e2m1_dec((w >> (4 * (j & 7))) & 15u), sb), s);
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t w = i < 4 ? q.x : q.y;
+        const uint32_t byte = (w >> (8 * (i & 3))) & 0xFFu;  // elements 2i (low nibble) and 2i + 1
+        uint32_t h2;
+        asm("{\n\t.reg .b8 c;\n\tcvt.u8.u32 c, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, c;\n\t}" : "=r"(h2) : "r"(byte));
+        __half2 v;
+        memcpy(&v, &h2, 4);
+        v = __hmul2(v, sb2);
+        out[2 * i] = __fmul_rn(__low2float(v), s);
+        out[2 * i + 1] = __fmul_rn(__high2float(v), s);
     }
 }
 

@@ -128,6 +128,8 @@ void plan_gemm(GemmLaunch &g, bool swap, int m_tok, int n_feat, int K, int num_s
     // per CTA and 7 pipeline stages instead of 4; 256-wide tiles on an even
     // number of token tiles
     p.pair = 0;
+    // (NVFP4 tiles stay on single CTAs: measured faster than pairs of
+    // 256 x 128 tiles, whose two CTAs' epilogues run in lockstep)
     if (!swap && !f4 && g.bn == 256 && p.n_tiles_p % 2 == 0 && !(tactic && tactic->no_pairs)) {
         const char *e = getenv("FRT_FFN_PAIR");
         if (!(e && e[0] == '0')) {

@@ -7,7 +7,7 @@
 // instantiate it: k_gemm_fp8.cu (E4M3) and k_gemm_f4.cu (NVFP4).
 #pragma once
 //
-// One persistent kernel template, 192 threads per CTA:
+// One persistent kernel template, 192 threads per CTA (320 with NVFP4 operands):
 //   warp 4      TMA producer: streams 128-byte-wide K slices of the two
 //               operands into a ring of shared-memory stages (128B swizzle);
 //   warp 5      MMA issuer: one thread issues tcgen05.mma (kind::f8f6f4,
@@ -15,7 +15,9 @@
 //               accumulator and commits to mbarriers;
 //   warps 0..3  epilogue: tcgen05.ld of the accumulator (one TMEM lane per
 //               thread), scale by alpha, gated activation + E4M3 requantise
-//               or residual add + BF16 store.
+//               or residual add + BF16 store;
+//   warps 6..9  (NVFP4 only) scale warps: each stage's E4M3 block scales
+//               from shared memory into TMEM (tcgen05.st) for the MMAs.
 // Split-K is cooperative (one unit per CTA): each split stages its fp32
 // partial, the S partials of a tile are exchanged -- over distributed shared
 // memory inside a thread-block cluster, or through a global workspace --
@@ -54,6 +56,7 @@ constexpr int BM = 128;        // MMA M = rows of the P tile = TMEM lanes
 constexpr int BK = 128;        // K bytes per stage = one 128-byte swizzle row
 constexpr int UK = 32;         // K of one tcgen05.mma for 8-bit operands
 constexpr int NTHREADS = 192;  // 4 epilogue warps + producer warp + MMA warp
+constexpr int NTHREADS_F4 = 320;  // NVFP4: and 4 scale warps (warps 6..9)
 constexpr int GATED_TOKENS = 4;  // tokens per step of the weight-streaming gated epilogue
 constexpr uint32_t SMEM_LIMIT = 232448;  // largest dynamic shared memory of one CTA (227 KB)
 
@@ -64,8 +67,10 @@ constexpr uint32_t SMEM_LIMIT = 232448;  // largest dynamic shared memory of one
 // TMEM-ready order: per 128 rows four 512-byte blocks (one per 64-element K
 // chunk), the P tile's 2 KB then the Q tile's 2 KB (a Q tile has at most 128
 // rows; the weight-streaming role's <= 64 tokens are the first rows of their
-// 128-row block).  The MMA thread moves a stage's scales into 32 TMEM
-// columns of their own (tcgen05.cp) before its MMAs read them.
+// 128-row block).  Four scale warps, one per TMEM lane quarter, write a
+// stage's scales into 32 TMEM columns of their own (tcgen05.st, each quarter
+// a copy: the replicated order kind::mxf4nvf4 reads) and signal the MMA
+// thread, so the tensor pipe issues MMAs only.
 template <int BN, bool SWAP = false, bool PAIR = false, bool F4 = false>
 struct Cfg {
     static_assert(!(PAIR && SWAP), "CTA pairs serve the tiled role");
@@ -75,10 +80,11 @@ struct Cfg {
     static constexpr uint32_t SF_BYTES = F4 ? 2 * 2048 : 0;  // block scales of a stage (P's, then Q's)
     static constexpr uint32_t STAGE_BYTES = P_BYTES + Q_BYTES + SF_BYTES;
     static constexpr int SF_COLS = 32;            // TMEM columns of a stage's block scales
+    static constexpr uint32_t BAR_BYTES = F4 ? 512 : 256;  // mbarriers and flags after the stages
     static constexpr int CH = BN < 32 ? 16 : 32;  // accumulator columns per tcgen05.ld
     static constexpr uint32_t XBUF_BYTES = SWAP ? BN * (128 + 4) * 4 : 0;  // gate/up exchange, whole tile
     static constexpr int STAGES_FIT =
-        (int)((SMEM_LIMIT - 1024 - 256 - XBUF_BYTES) / STAGE_BYTES);
+        (int)((SMEM_LIMIT - 1024 - BAR_BYTES - XBUF_BYTES) / STAGE_BYTES);
     static constexpr int STAGES_TMEM = F4 ? (512 - 2 * BN) / SF_COLS : 64;  // scale columns within TMEM
     static constexpr int STAGES_CAP = STAGES_FIT < STAGES_TMEM ? STAGES_FIT : STAGES_TMEM;
     static constexpr int STAGES = STAGES_CAP > 10 ? 10 : STAGES_CAP;  // most stages a launch may ask for
@@ -95,19 +101,19 @@ struct Cfg {
         const uint32_t need = 2u * BN + (uint32_t)(SF_COLS * stages);
         return need <= 32 ? 32u : need <= 64 ? 64u : need <= 128 ? 128u : need <= 256 ? 256u : 512u;
     }
-    static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + 256 + XBUF_BYTES;
+    static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + BAR_BYTES + XBUF_BYTES;
     // Shared memory of a launch with `stages` pipeline stages: a small
     // footprint lets the next kernel's CTAs share the SM and start streaming
     // their weights while this one runs.
     // (the gate/up exchange buffer only for the unsplit gated epilogue)
     static size_t smem_bytes(int stages, bool xbuf) {
-        return 1024 + (size_t)stages * STAGE_BYTES + 256 + (xbuf ? XBUF_BYTES : 0);
+        return 1024 + (size_t)stages * STAGE_BYTES + BAR_BYTES + (xbuf ? XBUF_BYTES : 0);
     }
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
     static_assert(Q_BYTES % 1024 == 0, "tiles must stay 1024-byte aligned");
     static_assert(STAGES >= 2, "pipeline needs two stages");
     static_assert(SMEM <= SMEM_LIMIT, "shared memory over the per-CTA limit");
-    static_assert((2 * STAGES + 9) * 8 + 24 <= 256, "mbarriers and flags fit their 256-byte block");
+    static_assert(((F4 ? 4 : 2) * STAGES + 9) * 8 + 24 <= BAR_BYTES, "mbarriers and flags fit their block");
 };
 
 struct Unit {
@@ -164,12 +170,15 @@ __device__ __forceinline__ Unit decode(const GemmParams &p, int u) {
 // ------------------------------------------------------------ producer --
 template <int BN, bool SWAP, bool PAIR, bool F4>
 __device__ void producer(const CUtensorMap *tmP, const CUtensorMap *tmQ, const GemmParams &p, uint8_t *sP,
-                         uint8_t *sQ, uint8_t *sSF, uint64_t *full, uint64_t *empty, volatile int *abort_f) {
+                         uint8_t *sQ, uint8_t *sSF, uint64_t *full, uint64_t *empty, uint64_t *sffull,
+                         volatile int *abort_f) {
     using C = Cfg<BN, SWAP, PAIR, F4>;
     // F4: a stage's 2 KB of block scales of the 128-row tile holding `row`
     // (K / 64 blocks of 512 bytes per 128 rows, tiles major); weight scales
-    // travel with the weight tile, token scales with the token tile, P's
-    // first in the stage's scale area
+    // are requested before the weight tile, token scales before the token
+    // tile (P's first in the stage's scale area), all completing on the
+    // stage's own scale barrier, so the scale warps can move them into TMEM
+    // while the operand tiles are still in flight
     const size_t sf_tile = (size_t)p.k_blocks * 2048u;
     const uint32_t sf_w_off = SWAP ? 0u : 2048u, sf_x_off = SWAP ? 2048u : 0u;
     // CTA pair: both CTAs' copies complete on the even CTA's stage barrier,
@@ -202,10 +211,15 @@ __device__ void producer(const CUtensorMap *tmP, const CUtensorMap *tmQ, const G
                 goto drain;
             {
                 const uint32_t fb = PAIR ? mapa_shared(smem_u32(&full[stage]), 0u) : smem_u32(&full[stage]);
-                if (!PAIR)
+                const uint32_t sfb = F4 ? smem_u32(&sffull[stage]) : 0u;
+                if constexpr (F4) {
+                    mbar_arrive_expect_tx(sfb, C::SF_BYTES);
+                    mbar_arrive_expect_tx(fb, C::P_BYTES + C::Q_BYTES);
+                } else if (!PAIR) {
                     mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
-                else if (rank == 0)
+                } else if (rank == 0) {
                     mbar_arrive_expect_tx(smem_u32(&full[stage]), 2u * C::STAGE_BYTES);
+                }
                 issued |= 1u << stage;
                 issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
                 const uint32_t dP = smem_u32(sP + (size_t)stage * C::P_BYTES);
@@ -214,23 +228,23 @@ __device__ void producer(const CUtensorMap *tmP, const CUtensorMap *tmQ, const G
                 const uint32_t dX = SWAP ? dQ : dP;
                 const CUtensorMap *mW = SWAP ? tmP : tmQ;
                 const CUtensorMap *mX = SWAP ? tmQ : tmP;
+                if constexpr (F4)
+                    bulk_load(smem_u32(sSF + (size_t)stage * C::SF_BYTES + sf_w_off),
+                              p.sf_w + (size_t)(wrow / BM) * sf_tile + (size_t)kb * 2048u, 2048u, sfb);
                 if constexpr (PAIR) {
                     // this CTA's half of the weight tile
                     tma_load_2d_pair(dW, mW, fb, kb * BK, wrow + (int)rank * (BN / 2), pol_w);
                 } else {
                     tma_load_2d(dW, mW, fb, kb * BK, wrow, pol_w);
                 }
-                if constexpr (F4)
-                    bulk_load(smem_u32(sSF + (size_t)stage * C::SF_BYTES + sf_w_off),
-                              p.sf_w + (size_t)(wrow / BM) * sf_tile + (size_t)kb * 2048u, 2048u, fb);
                 if (waited) {
+                    if constexpr (F4)
+                        bulk_load(smem_u32(sSF + (size_t)stage * C::SF_BYTES + sf_x_off),
+                                  p.sf_x + (size_t)(xrow / BM) * sf_tile + (size_t)kb * 2048u, 2048u, sfb);
                     if constexpr (PAIR)
                         tma_load_2d_pair(dX, mX, fb, kb * BK, xrow, pol_x);
                     else
                         tma_load_2d(dX, mX, fb, kb * BK, xrow, pol_x);
-                    if constexpr (F4)
-                        bulk_load(smem_u32(sSF + (size_t)stage * C::SF_BYTES + sf_x_off),
-                                  p.sf_x + (size_t)(xrow / BM) * sf_tile + (size_t)kb * 2048u, 2048u, fb);
                 } else {
                     if (n_def == 0) {
                         def_kb = kb;
@@ -247,14 +261,14 @@ __device__ void producer(const CUtensorMap *tmP, const CUtensorMap *tmQ, const G
                                 PAIR ? mapa_shared(smem_u32(&full[st]), 0u) : smem_u32(&full[st]);
                             const uint32_t dst = SWAP ? smem_u32(sQ + (size_t)st * C::Q_BYTES)
                                                       : smem_u32(sP + (size_t)st * C::P_BYTES);
+                            if constexpr (F4)
+                                bulk_load(smem_u32(sSF + (size_t)st * C::SF_BYTES + sf_x_off),
+                                          p.sf_x + (size_t)(def_row / BM) * sf_tile + (size_t)(def_kb + i) * 2048u,
+                                          2048u, smem_u32(&sffull[st]));
                             if constexpr (PAIR)
                                 tma_load_2d_pair(dst, mX, fbi, (def_kb + i) * BK, def_row, pol_x);
                             else
                                 tma_load_2d(dst, mX, fbi, (def_kb + i) * BK, def_row, pol_x);
-                            if constexpr (F4)
-                                bulk_load(smem_u32(sSF + (size_t)st * C::SF_BYTES + sf_x_off),
-                                          p.sf_x + (size_t)(def_row / BM) * sf_tile + (size_t)(def_kb + i) * 2048u,
-                                          2048u, fbi);
                             if (++st == NS)
                                 st = 0;
                         }
@@ -275,16 +289,19 @@ drain:
     // Give copies in flight a bounded time to land before the CTA exits (a
     // pair's odd CTA has no armed stage barrier of its own; the pair's
     // closing cluster barrier holds it until the even one is done).
-    if (!PAIR || rank == 0)
-        for (int s = 0; s < NS; ++s)
-            if (issued & (1u << s))
+    for (int s = 0; s < NS; ++s)
+        if (issued & (1u << s)) {
+            if (!PAIR || rank == 0)
                 mbar_wait_for(smem_u32(&full[s]), (issued_par >> s) & 1u, 100000000ull);
+            if constexpr (F4)
+                mbar_wait_for(smem_u32(&sffull[s]), (issued_par >> s) & 1u, 100000000ull);
+        }
 }
 
 // ---------------------------------------------------------- MMA issuer --
 template <int BN, bool SWAP, bool PAIR, bool F4>
-__device__ void mma_issuer(const GemmParams &p, uint8_t *sP, uint8_t *sQ, uint8_t *sSF, uint64_t *full,
-                           uint64_t *empty, uint64_t *tfull, uint64_t *tempty, uint64_t *drain_bar,
+__device__ void mma_issuer(const GemmParams &p, uint8_t *sP, uint8_t *sQ, uint64_t *full, uint64_t *empty,
+                           uint64_t *sfull, uint64_t *tfull, uint64_t *tempty, uint64_t *drain_bar,
                            uint32_t tmem_base, volatile int *abort_f) {
     using C = Cfg<BN, SWAP, PAIR, F4>;
     // a pair's MMAs (issued by the even CTA only) cover 256 token rows
@@ -313,19 +330,14 @@ __device__ void mma_issuer(const GemmParams &p, uint8_t *sP, uint8_t *sQ, uint8_
                 const uint32_t aP = smem_u32(sP + (size_t)stage * C::P_BYTES);
                 const uint32_t aQ = smem_u32(sQ + (size_t)stage * C::Q_BYTES);
                 if constexpr (F4) {
-                    // the stage's block scales into its own TMEM columns (after
-                    // the accumulators): per 64-element chunk j the P tile's
-                    // block at +4j, the Q tile's at +16+4j; a tcgen05.cp and
-                    // the later MMAs of this thread run in issue order, and
-                    // the columns are rewritten only once the stage's MMAs
-                    // have completed (the producer waited for that)
+                    // the stage's block scales, in its own TMEM columns after
+                    // the accumulators (per 64-element chunk j the P tile's at
+                    // +4j, the Q tile's at +16+4j), once the scale warps have
+                    // written them
+                    if (!mbar_wait(smem_u32(&sfull[stage]), phase, abort_f, p.err))
+                        goto drain;
+                    tc_fence_after();
                     const uint32_t t_sf = tmem_base + (uint32_t)(2 * BN + C::SF_COLS * stage);
-                    const uint32_t s_sf = smem_u32(sSF + (size_t)stage * C::SF_BYTES);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        tmem_cp_sf(t_sf + 4 * j, smem_desc_sf(s_sf + 512 * j));
-                        tmem_cp_sf(t_sf + 16 + 4 * j, smem_desc_sf(s_sf + 2048 + 512 * j));
-                    }
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
                         mma_nvf4(dt, smem_desc_k128(aP + k * UK), smem_desc_k128(aQ + k * UK), idesc, t_sf + 4 * k,
@@ -372,6 +384,55 @@ drain:
         else
             mma_commit(smem_u32(drain_bar));
         mbar_wait_for(smem_u32(drain_bar), 0, 100000000ull);
+    }
+}
+
+// -------------------------------------------------------- scale warps --
+// NVFP4: warps 6..9, one per TMEM lane quarter (warp id % 4).  For each stage
+// in the MMA thread's order: wait until its scale copies have landed, read its
+// eight 512-byte scale blocks (lane l: bytes 16 l .. 16 l + 15 of each, i.e.
+// rows l, l + 32, l + 64, l + 96 of the block's 128), write them to this
+// quarter's lanes of the stage's 32 scale columns (block j at columns 4 j ..
+// 4 j + 3), wait for the stores, and count the warp in on the stage's
+// scales-ready barrier.  The columns of a stage are rewritten only after its
+// refill, i.e. after the MMAs that read them completed.
+template <int BN, bool SWAP>
+__device__ void scale_feeder(const GemmParams &p, uint8_t *sSF, uint64_t *sffull, uint64_t *sfull,
+                             uint32_t tmem_base, volatile int *abort_f) {
+    using C = Cfg<BN, SWAP, false, true>;
+    const int lane = threadIdx.x & 31;
+    const uint32_t quarter = (threadIdx.x >> 5) & 3u;
+    const uint32_t t_lane = tmem_base + ((quarter * 32u) << 16);
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
+        const Unit w = decode(p, u);
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
+            // every lane waits itself (the blocks were written by the async proxy)
+            const bool ok = mbar_wait(smem_u32(&sffull[stage]), phase, abort_f, p.err);
+            if (!__all_sync(0xffffffffu, ok))
+                return;
+            const uint8_t *src = sSF + (size_t)stage * C::SF_BYTES + lane * 16;
+            uint32_t v[32];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint4 q = *reinterpret_cast<const uint4 *>(src + 512 * j);
+                v[4 * j] = q.x;
+                v[4 * j + 1] = q.y;
+                v[4 * j + 2] = q.z;
+                v[4 * j + 3] = q.w;
+            }
+            tmem_st_x32(t_lane + (uint32_t)(2 * BN + C::SF_COLS * stage), v);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(smem_u32(&sfull[stage]));
+            if (++stage == p.stages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
     }
 }
 
@@ -650,44 +711,64 @@ __host__ __device__ __forceinline__ bool f4_gated(int epi) {
     return epi == EPI_F4_GATED || epi == EPI_F4_AMAX_GU || epi == EPI_F4_AMAX_H;
 }
 
-// One block of 16 features f0 .. f0+15 of token m: g and u (acc * alpha
-// applied, fp32) -> G = NVFP4(g, s_g), U = NVFP4(u, s_u) -> a = act(dec G)
-// dec U -> NVFP4(a, s_h) (codes at out[m][f0/2], the block scale TMEM-ready
-// in out_sf), or the calibration amaxes: |g| into am0 and |u| into am1
-// (EPI_F4_AMAX_GU), |a| into am0 (EPI_F4_AMAX_H).
-__device__ __forceinline__ void f4_gated_block(const GemmParams &p, int m, int f0, const float (&g)[16],
-                                               const float (&u)[16], float &am0, float &am1) {
+// NB consecutive blocks of 16 features f0 .. f0 + 16 NB - 1 of token m: g
+// and u (acc * alpha applied, fp32) -> G = NVFP4(g, s_g), U = NVFP4(u, s_u)
+// -> a = act(dec G) dec U -> NVFP4(a, s_h) (codes at out[m][f0/2], the block
+// scales TMEM-ready in out_sf), or the calibration amaxes: |g| into am0 and
+// |u| into am1 (EPI_F4_AMAX_GU), |a| into am0 (EPI_F4_AMAX_H).  Each step
+// runs over all NB blocks, so their chains interleave.
+template <int NB>
+__device__ __forceinline__ void f4_gated_blocks(const GemmParams &p, int m, int f0, const float (&g)[16 * NB],
+                                                const float (&u)[16 * NB], float &am0, float &am1) {
     if (p.epi == EPI_F4_AMAX_GU) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
+        for (int j = 0; j < 16 * NB; ++j) {
             am0 = fmaxf(am0, fabsf(g[j]));
             am1 = fmaxf(am1, fabsf(u[j]));
         }
         return;
     }
-    uint2 qg, qu;
-    const uint32_t bg = quant_block16(g, p.s_g, p.inv6_g, qg);
-    const uint32_t bu = quant_block16(u, p.s_u, p.inv6_u, qu);
-    if (p.dbg_gq) {
-        *reinterpret_cast<uint2 *>(p.dbg_gq + (size_t)m * (p.ff / 2) + f0 / 2) = qg;
-        *reinterpret_cast<uint2 *>(p.dbg_uq + (size_t)m * (p.ff / 2) + f0 / 2) = qu;
-        p.dbg_gs[(size_t)m * (p.ff / 16) + f0 / 16] = (uint8_t)bg;
-        p.dbg_us[(size_t)m * (p.ff / 16) + f0 / 16] = (uint8_t)bu;
+    uint2 qg[NB], qu[NB];
+    uint32_t bg[NB], bu[NB];
+#pragma unroll
+    for (int k = 0; k < NB; ++k) {
+        bg[k] = quant_block16(g + 16 * k, p.s_g, p.inv6_g, qg[k]);
+        bu[k] = quant_block16(u + 16 * k, p.s_u, p.inv6_u, qu[k]);
     }
-    float gd[16], ud[16], a[16];
-    dequant_block16(qg, bg, p.s_g, gd);
-    dequant_block16(qu, bu, p.s_u, ud);
-    gated_run<16>(p.act, gd, ud, a);
+    if (p.dbg_gq) {
+#pragma unroll
+        for (int k = 0; k < NB; ++k) {
+            const int f = f0 + 16 * k;
+            *reinterpret_cast<uint2 *>(p.dbg_gq + (size_t)m * (p.ff / 2) + f / 2) = qg[k];
+            *reinterpret_cast<uint2 *>(p.dbg_uq + (size_t)m * (p.ff / 2) + f / 2) = qu[k];
+            p.dbg_gs[(size_t)m * (p.ff / 16) + f / 16] = (uint8_t)bg[k];
+            p.dbg_us[(size_t)m * (p.ff / 16) + f / 16] = (uint8_t)bu[k];
+        }
+    }
+    float gd[16 * NB], ud[16 * NB], a[16 * NB];
+#pragma unroll
+    for (int k = 0; k < NB; ++k) {
+        dequant_block16(qg[k], bg[k], p.s_g, gd + 16 * k);
+        dequant_block16(qu[k], bu[k], p.s_u, ud + 16 * k);
+    }
+    gated_run<16 * NB>(p.act, gd, ud, a);
     if (p.epi == EPI_F4_AMAX_H) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
+        for (int j = 0; j < 16 * NB; ++j)
             am0 = fmaxf(am0, fabsf(a[j]));
         return;
     }
-    uint2 qh;
-    const uint32_t bh = quant_block16(a, p.s_h, p.inv6_h, qh);
-    *reinterpret_cast<uint2 *>(static_cast<uint8_t *>(p.out) + (size_t)m * p.ldo + f0 / 2) = qh;
-    p.out_sf[sf_offset(m, f0 / 16, p.ff)] = (uint8_t)bh;
+    uint2 qh[NB];
+    uint32_t bh[NB];
+#pragma unroll
+    for (int k = 0; k < NB; ++k)
+        bh[k] = quant_block16(a + 16 * k, p.s_h, p.inv6_h, qh[k]);
+#pragma unroll
+    for (int k = 0; k < NB; ++k) {
+        const int f = f0 + 16 * k;
+        *reinterpret_cast<uint2 *>(static_cast<uint8_t *>(p.out) + (size_t)m * p.ldo + f / 2) = qh[k];
+        p.out_sf[sf_offset(m, f / 16, p.ff)] = (uint8_t)bh[k];
+    }
 }
 
 // The calibration amaxes of an NVFP4 gated epilogue into amax[0..2].
@@ -739,7 +820,7 @@ __device__ __forceinline__ void f4_gated_swap_tile(const GemmParams &p, const Un
             g[j] = gv.x; g[j + 1] = gv.y; g[j + 2] = gv.z; g[j + 3] = gv.w;
             u[j] = uv.x; u[j + 1] = uv.y; u[j + 2] = uv.z; u[j + 3] = uv.w;
         }
-        f4_gated_block(p, m0 + c, fbase + 16 * b, g, u, am0, am1);
+        f4_gated_blocks<1>(p, m0 + c, fbase + 16 * b, g, u, am0, am1);
     }
     named_bar_sync(1, 128);
 }
@@ -758,22 +839,23 @@ __device__ __forceinline__ void consume_unit(const GemmParams &p, const Unit &w,
             // NVFP4 gated, tiled: TMEM lanes are tokens; columns [128q, 128q+64)
             // are gate and [128q+64, 128q+128) the up rows of the same 64
             // features, a block of 16 features per step
+            // two blocks of 16 features a step
             const int m = w.tp * BM + r;
             float am0 = 0.0f, am1 = 0.0f;
 #pragma unroll 1
             for (int c0 = 0; c0 < BN; c0 += 128) {
 #pragma unroll 1
-                for (int sub = 0; sub < 64; sub += 16) {
-                    float g[16], u[16];
-                    tmem_load_chunk<16>(tbase + c0 + sub, g);
-                    tmem_load_chunk<16>(tbase + c0 + 64 + sub, u);
+                for (int sub = 0; sub < 64; sub += 32) {
+                    float g[32], u[32];
+                    tmem_load_chunk<32>(tbase + c0 + sub, g);
+                    tmem_load_chunk<32>(tbase + c0 + 64 + sub, u);
                     if (m < p.m_tok) {
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
+                        for (int j = 0; j < 32; ++j) {
                             g[j] = __fmul_rn(g[j], p.alpha);
                             u[j] = __fmul_rn(u[j], p.alpha_u);
                         }
-                        f4_gated_block(p, m, w.tq * (BN / 2) + c0 / 2 + sub, g, u, am0, am1);
+                        f4_gated_blocks<2>(p, m, w.tq * (BN / 2) + c0 / 2 + sub, g, u, am0, am1);
                     }
                 }
             }
@@ -1499,11 +1581,13 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmP, const CUtensor
     uint64_t *free_bar = red_bar + 1;    // cluster split-K: every other CTA's stages are free
     uint64_t *data_bar = free_bar + 1;   // cluster split-K: this CTA's slice of every partial landed
     uint64_t *sent_bar = data_bar + 1;   // cluster split-K: every copy out of this CTA landed
-    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(sent_bar + 1);
+    uint64_t *sfull = sent_bar + 1;      // F4: a stage's scales are in TMEM (4 scale warps)
+    uint64_t *sffull = sfull + (F4 ? NS : 0);  // F4: a stage's scale copies landed in shared memory
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(sffull + (F4 ? NS : 0));
     volatile int *abort_f = reinterpret_cast<volatile int *>(tmem_holder + 1);
     volatile int *s_ok = abort_f + 1;    // [2]
     volatile int *s_last = s_ok + 2;     // [2]
-    float *xbuf = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(bars) + 256);
+    float *xbuf = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(bars) + C::BAR_BYTES);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -1521,6 +1605,11 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmP, const CUtensor
         mbar_init(smem_u32(free_bar), p.cluster ? (uint32_t)(p.splits - 1) : 1u);
         mbar_init(smem_u32(data_bar), 1);
         mbar_init(smem_u32(sent_bar), p.cluster ? (uint32_t)(p.splits - 1) : 1u);
+        if constexpr (F4)
+            for (int s = 0; s < NS; ++s) {
+                mbar_init(smem_u32(&sfull[s]), 4u);
+                mbar_init(smem_u32(&sffull[s]), 1u);
+            }
         *abort_f = 0;
         fence_mbar_init();
     }
@@ -1563,7 +1652,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmP, const CUtensor
                                  data_bar, sent_bar, reinterpret_cast<float *>(smem));
     } else if (warp == 4) {
         if (lane == 0)
-            producer<BN, SWAP, PAIR, F4>(mapP, mapQ, p, sP, sQ, sSF, full, empty, abort_f);
+            producer<BN, SWAP, PAIR, F4>(mapP, mapQ, p, sP, sQ, sSF, full, empty, sffull, abort_f);
         __syncwarp();
         if (p.cluster) {
             cluster_wait();
@@ -1581,10 +1670,16 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmP, const CUtensor
                     mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(sent_bar), (uint32_t)lane));
             }
         }
-    } else {
+    } else if (warp == 5) {
         if (lane == 0 && (!PAIR || (blockIdx.x & 1u) == 0))
-            mma_issuer<BN, SWAP, PAIR, F4>(p, sP, sQ, sSF, full, empty, tfull, tempty, drain_bar, tmem_base,
+            mma_issuer<BN, SWAP, PAIR, F4>(p, sP, sQ, full, empty, sfull, tfull, tempty, drain_bar, tmem_base,
                                            abort_f);
+        __syncwarp();
+        if (p.cluster)
+            cluster_wait();
+    } else {
+        if constexpr (F4)
+            scale_feeder<BN, SWAP>(p, sSF, sffull, sfull, tmem_base, abort_f);
         __syncwarp();
         if (p.cluster)
             cluster_wait();
@@ -1615,9 +1710,10 @@ __global__ void __launch_bounds__(NTHREADS, SWAP ? 2 : 1)
     gemm_body<BN, SWAP, PAIR, ROLE, false>(tmP, tmQ, p);
 }
 
-// NVFP4 operands (E2M1 codes, E4M3 block scales): single CTAs, N <= 128.
+// NVFP4 operands (E2M1 codes, E4M3 block scales): single CTAs, N <= 128,
+// with the four scale warps.
 template <int BN, bool SWAP, int ROLE>
-__global__ void __launch_bounds__(NTHREADS, SWAP ? 2 : 1)
+__global__ void __launch_bounds__(NTHREADS_F4, 1)
     k_gemm_f4(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmQ,
               const __grid_constant__ GemmParams p) {
     gemm_body<BN, SWAP, false, ROLE, true>(tmP, tmQ, p);
@@ -1661,7 +1757,7 @@ cudaError_t run(const GemmLaunch &g, cudaStream_t s, bool pdl) {
     const bool xbuf = SWAP && g.p.splits == 1 &&
                       (g.p.epi == EPI_GATED || g.p.epi == EPI_GATED_AMAX || f4_gated(g.p.epi));
     const unsigned cluster = PAIR ? 2u : g.p.cluster ? (unsigned)g.p.splits : 1u;
-    return launch_ex(kernel_of<BN, SWAP, PAIR, ROLE, F4>(), dim3((unsigned)g.grid), dim3(NTHREADS),
+    return launch_ex(kernel_of<BN, SWAP, PAIR, ROLE, F4>(), dim3((unsigned)g.grid), dim3(F4 ? NTHREADS_F4 : NTHREADS),
                      std::max(C::smem_bytes(g.p.stages, xbuf), g.min_smem), s, pdl, cluster, g.tmP, g.tmQ, g.p);
 }
 

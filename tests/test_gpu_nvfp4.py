@@ -119,7 +119,8 @@ def dev(a):
 
 @pytest.mark.parametrize("swap", [False, True], ids=["tiled", "weight_streaming"])
 @pytest.mark.parametrize("M,N,K,S", [(1, 128, 256, 1), (50, 256, 512, 1), (128, 128, 2048, 1), (300, 384, 1024, 1),
-                                     (1, 256, 2048, 3), (50, 128, 4096, 8), (300, 256, 1024, 2)])
+                                     (1, 256, 2048, 3), (50, 128, 4096, 8), (300, 256, 1024, 2),
+                                     (256, 256, 1024, 1), (500, 384, 512, 2)])
 def test_block_scaled_gemm_matches_the_exact_sum(M, N, K, S, swap, monkeypatch):
     from realtime_transformer_gb300.nvfp4 import nvfp4_gemm
     if swap and M > 64:
@@ -142,7 +143,8 @@ def test_block_scaled_gemm_matches_the_exact_sum(M, N, K, S, swap, monkeypatch):
     assert cosine(got, ref) > 0.9999999
 
 
-@pytest.mark.parametrize("M,swap", [(130, "0"), (40, "0"), (40, "1")])  # "1": the weight-streaming role
+# "1": the weight-streaming role; "0": the tiled role (130, 256: several token tiles)
+@pytest.mark.parametrize("M,swap", [(130, "0"), (256, "0"), (40, "0"), (40, "1")])
 def test_gemm_scale_placement_one_block_at_a_time(M, swap, monkeypatch):
     """Only one (row, K-group) scale of A nonzero: the product picks exactly
     that row's 16 elements of K -- pins the TMEM-ready layout end to end."""
