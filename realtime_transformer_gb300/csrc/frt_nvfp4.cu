@@ -134,8 +134,8 @@ bool f4_swap(int M) {
 }
 
 frt_status build_tmaps(frt_fp4_plan *P) {
-    const int combos[][2] = {{F_WGU, 128}, {F_WD, 128}, {F_XQ, 16}, {F_XQ, 32}, {F_XQ, 64},
-                             {F_XQ, 128},  {F_HQ, 16},  {F_HQ, 32}, {F_HQ, 64}, {F_HQ, 128}};
+    const int combos[][2] = {{F_WGU, 128}, {F_WGU, 256}, {F_WD, 128}, {F_WD, 256}, {F_XQ, 16},  {F_XQ, 32},
+                             {F_XQ, 64},   {F_XQ, 128},  {F_HQ, 16},  {F_HQ, 32}, {F_HQ, 64}, {F_HQ, 128}};
     constexpr int N = sizeof(combos) / sizeof(combos[0]);
     CUtensorMap host[N];
     const uint64_t L = P->L, D = P->d, F = P->ff, MA = P->M_alloc;
@@ -316,7 +316,7 @@ frt_status f4_maps(frt_fp4_plan *P, GemmLaunch &g, int wbuf, int xbuf, int l, in
         g.p.q_row0 = 0;
     } else {
         if ((st = get_tmap(P, xbuf, 128, &g.tmP, &g.p.gtm_p)) != FRT_OK) return st;
-        if ((st = get_tmap(P, wbuf, 128, &g.tmQ, &g.p.gtm_q)) != FRT_OK) return st;
+        if ((st = get_tmap(P, wbuf, g.bn, &g.tmQ, &g.p.gtm_q)) != FRT_OK) return st;
         g.p.p_row0 = 0;
         g.p.q_row0 = l * rows_per_layer;
     }
@@ -655,7 +655,7 @@ FRT_API frt_status frt_nvfp4_gemm(const void *a_codes, const void *a_sf, const v
         e2 = encode_tmap_u8(&g.tmQ, a_codes, (uint64_t)M, (uint64_t)K / 2, (uint32_t)g.bn);
     } else {
         e1 = encode_tmap_u8(&g.tmP, a_codes, (uint64_t)M, (uint64_t)K / 2, 128);
-        e2 = encode_tmap_u8(&g.tmQ, b_codes, (uint64_t)N, (uint64_t)K / 2, 128);
+        e2 = encode_tmap_u8(&g.tmQ, b_codes, (uint64_t)N, (uint64_t)K / 2, (uint32_t)g.bn);
     }
     if (e1 != cudaSuccess || e2 != cudaSuccess)
         return ffail(FRT_ERR_CUDA, "cuTensorMapEncodeTiled failed");

@@ -2,7 +2,8 @@
 // (k_gemm_tc.cuh): the fused gate/up GEMM with the FP4-to-FP4 gated
 // activation and the down GEMM + residual of the NVFP4 encoder FFN
 // (itsolotime FlashRT article, 7.2), in the weight-streaming role (<= 64
-// tokens; BN = 16 / 32 / 64) and the tiled role (BN = 128).
+// tokens; BN = 16 / 32 / 64) and the tiled role (BN = 256, one accumulator;
+// or 128, two).
 #include "k_gemm_tc.cuh"
 
 namespace frt {
@@ -29,6 +30,8 @@ cudaError_t launch_gemm_f4(const GemmLaunch &g, cudaStream_t s, bool pdl) {
     }
     if (g.bn == 128)
         return run<128, false, false, ROLE_ANY, true>(g, s, pdl);
+    if (g.bn == 256)
+        return run<256, false, false, ROLE_ANY, true>(g, s, pdl);
     return cudaErrorInvalidValue;
 }
 

@@ -60,7 +60,7 @@ StageInfo stage_info_for(int bn, bool swap, bool pair = false, bool f4 = false) 
         if (swap)
             return bn == 16 ? stage_info<16, true, false, true>()
                             : (bn == 32 ? stage_info<32, true, false, true>() : stage_info<64, true, false, true>());
-        return stage_info<128, false, false, true>();
+        return bn == 256 ? stage_info<256, false, false, true>() : stage_info<128, false, false, true>();
     }
     if (swap)
         return bn == 16 ? stage_info<16, true>() : (bn == 32 ? stage_info<32, true>() : stage_info<64, true>());
@@ -96,8 +96,10 @@ void plan_gemm(GemmLaunch &g, bool swap, int m_tok, int n_feat, int K, int num_s
         p.n_tiles_p = (n_feat + BM - 1) / BM;
         p.n_tiles_q = (m_tok + g.bn - 1) / g.bn;
     } else {
-        // NVFP4 tiles: N = 128 (its TMEM holds the stages' block scales too)
-        g.bn = (n_feat % 256 == 0 && !f4) ? 256 : 128;
+        // NVFP4: FRT_F4_BN=128 keeps 128-wide tiles (two accumulators)
+        // where 256 would fit (one accumulator beside the stages' scales)
+        const char *fb = f4 ? getenv("FRT_F4_BN") : nullptr;
+        g.bn = (n_feat % 256 == 0 && !(fb && atoi(fb) == 128)) ? 256 : 128;
         p.n_tiles_p = (m_tok + BM - 1) / BM;
         p.n_tiles_q = (n_feat + g.bn - 1) / g.bn;
     }
@@ -172,6 +174,11 @@ void plan_gemm(GemmLaunch &g, bool swap, int m_tok, int n_feat, int K, int num_s
     int cohabit = (int)((COHABIT_SMEM - fixed) / si.stage_bytes);
     cohabit = std::max(2, std::min(cohabit, si.max_stages));
     p.stages = kb_cta <= 2 * cohabit ? std::min(cohabit, std::max(2, kb_cta)) : si.max_stages;
+    // CTA pairs: 5 of the 7 stages that fit measured fastest on the long
+    // prefill shape (1237 against 1286 us a layer; 4: 1316, 6: 1257), the
+    // VLA prefix shape alike at 5 to 7
+    if (p.pair)
+        p.stages = std::min(p.stages, 5);
     if (const char *e = getenv("FRT_FFN_STAGES")) {
         const int v = atoi(e);
         if (v >= 2)

@@ -65,27 +65,32 @@ constexpr uint32_t SMEM_LIMIT = 232448;  // largest dynamic shared memory of one
 // F4: NVFP4 operands.  A stage's 128 bytes of K then hold 256 E2M1 elements,
 // and the stage also carries both operands' E4M3 block scales in the
 // TMEM-ready order: per 128 rows four 512-byte blocks (one per 64-element K
-// chunk), the P tile's 2 KB then the Q tile's 2 KB (a Q tile has at most 128
-// rows; the weight-streaming role's <= 64 tokens are the first rows of their
-// 128-row block).  Four scale warps, one per TMEM lane quarter, write a
+// chunk), the P tile's 2 KB then the Q tile's 2 KB per 128 of its rows (the
+// weight-streaming role's <= 64 tokens are the first rows of their 128-row
+// block).  In TMEM a chunk's scales take 4 columns per 128 rows (row r at
+// lane r % 32 of every lane quarter, column r / 32).  A 256-row Q tile
+// leaves room for one accumulator only (the epilogue of a tile then runs
+// between its MMAs and the next tile's).  Four scale warps, one per TMEM lane quarter, write a
 // stage's scales into 32 TMEM columns of their own (tcgen05.st, each quarter
 // a copy: the replicated order kind::mxf4nvf4 reads) and signal the MMA
 // thread, so the tensor pipe issues MMAs only.
 template <int BN, bool SWAP = false, bool PAIR = false, bool F4 = false>
 struct Cfg {
     static_assert(!(PAIR && SWAP), "CTA pairs serve the tiled role");
-    static_assert(!(F4 && (PAIR || BN > 128)), "NVFP4 tiles: single CTAs, N <= 128");
+    static_assert(!(F4 && PAIR), "NVFP4 tiles: single CTAs");
     static constexpr uint32_t P_BYTES = BM * BK;
     static constexpr uint32_t Q_BYTES = (PAIR ? BN / 2 : BN) * BK;
-    static constexpr uint32_t SF_BYTES = F4 ? 2 * 2048 : 0;  // block scales of a stage (P's, then Q's)
+    static constexpr int SF_QB = F4 ? (BN + 127) / 128 : 0;  // 128-row scale blocks of the Q tile
+    static constexpr uint32_t SF_BYTES = F4 ? 2048u * (1 + SF_QB) : 0;  // block scales of a stage (P's, then Q's)
     static constexpr uint32_t STAGE_BYTES = P_BYTES + Q_BYTES + SF_BYTES;
-    static constexpr int SF_COLS = 32;            // TMEM columns of a stage's block scales
+    static constexpr int SF_COLS = 16 + 16 * SF_QB;  // TMEM columns of a stage's block scales (F4)
+    static constexpr int ACC_BUFS = (F4 && BN > 128) ? 1 : 2;  // TMEM accumulators
     static constexpr uint32_t BAR_BYTES = F4 ? 512 : 256;  // mbarriers and flags after the stages
     static constexpr int CH = BN < 32 ? 16 : 32;  // accumulator columns per tcgen05.ld
     static constexpr uint32_t XBUF_BYTES = SWAP ? BN * (128 + 4) * 4 : 0;  // gate/up exchange, whole tile
     static constexpr int STAGES_FIT =
         (int)((SMEM_LIMIT - 1024 - BAR_BYTES - XBUF_BYTES) / STAGE_BYTES);
-    static constexpr int STAGES_TMEM = F4 ? (512 - 2 * BN) / SF_COLS : 64;  // scale columns within TMEM
+    static constexpr int STAGES_TMEM = F4 ? (512 - ACC_BUFS * BN) / SF_COLS : 64;  // scale columns within TMEM
     static constexpr int STAGES_CAP = STAGES_FIT < STAGES_TMEM ? STAGES_FIT : STAGES_TMEM;
     static constexpr int STAGES = STAGES_CAP > 10 ? 10 : STAGES_CAP;  // most stages a launch may ask for
     static constexpr uint32_t TMEM_COLS = (2 * BN <= 32)    ? 32
@@ -93,12 +98,12 @@ struct Cfg {
                                           : (2 * BN <= 128) ? 128
                                           : (2 * BN <= 256) ? 256
                                                             : 512;
-    // TMEM columns of a launch with `stages` stages: the two accumulators,
-    // then (F4) the stages' scale columns; a power of two
+    // TMEM columns of a launch with `stages` stages: the accumulators, then
+    // (F4) the stages' scale columns; a power of two
     __host__ __device__ static uint32_t tmem_cols(int stages) {
         if (!F4)
             return TMEM_COLS;
-        const uint32_t need = 2u * BN + (uint32_t)(SF_COLS * stages);
+        const uint32_t need = (uint32_t)(ACC_BUFS * BN) + (uint32_t)(SF_COLS * stages);
         return need <= 32 ? 32u : need <= 64 ? 64u : need <= 128 ? 128u : need <= 256 ? 256u : 512u;
     }
     static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + BAR_BYTES + XBUF_BYTES;
@@ -228,9 +233,13 @@ __device__ void producer(const CUtensorMap *tmP, const CUtensorMap *tmQ, const G
                 const uint32_t dX = SWAP ? dQ : dP;
                 const CUtensorMap *mW = SWAP ? tmP : tmQ;
                 const CUtensorMap *mX = SWAP ? tmQ : tmP;
-                if constexpr (F4)
-                    bulk_load(smem_u32(sSF + (size_t)stage * C::SF_BYTES + sf_w_off),
-                              p.sf_w + (size_t)(wrow / BM) * sf_tile + (size_t)kb * 2048u, 2048u, sfb);
+                if constexpr (F4) {
+                    constexpr int WB = SWAP ? 1 : C::SF_QB;  // 128-row blocks of the weight tile
+#pragma unroll
+                    for (int i = 0; i < WB; ++i)
+                        bulk_load(smem_u32(sSF + (size_t)stage * C::SF_BYTES + sf_w_off + 2048u * i),
+                                  p.sf_w + (size_t)(wrow / BM + i) * sf_tile + (size_t)kb * 2048u, 2048u, sfb);
+                }
                 if constexpr (PAIR) {
                     // this CTA's half of the weight tile
                     tma_load_2d_pair(dW, mW, fb, kb * BK, wrow + (int)rank * (BN / 2), pol_w);
@@ -337,11 +346,11 @@ __device__ void mma_issuer(const GemmParams &p, uint8_t *sP, uint8_t *sQ, uint64
                     if (!mbar_wait(smem_u32(&sfull[stage]), phase, abort_f, p.err))
                         goto drain;
                     tc_fence_after();
-                    const uint32_t t_sf = tmem_base + (uint32_t)(2 * BN + C::SF_COLS * stage);
+                    const uint32_t t_sf = tmem_base + (uint32_t)(C::ACC_BUFS * BN + C::SF_COLS * stage);
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
                         mma_nvf4(dt, smem_desc_k128(aP + k * UK), smem_desc_k128(aQ + k * UK), idesc, t_sf + 4 * k,
-                                 t_sf + 16 + 4 * k, (kb > w.kb0 || k > 0) ? 1u : 0u);
+                                 t_sf + 16 + 4 * C::SF_QB * k, (kb > w.kb0 || k > 0) ? 1u : 0u);
                 } else {
 #pragma unroll
                 for (int k = 0; k < BK / UK; ++k) {
@@ -371,7 +380,7 @@ __device__ void mma_issuer(const GemmParams &p, uint8_t *sP, uint8_t *sQ, uint64
             mma_commit_pair(smem_u32(&tfull[abuf]), 0x3);
         else
             mma_commit(smem_u32(&tfull[abuf]));
-        if (++abuf == 2) {
+        if (++abuf == C::ACC_BUFS) {
             abuf = 0;
             aphase ^= 1u;
         }
@@ -390,11 +399,11 @@ drain:
 // -------------------------------------------------------- scale warps --
 // NVFP4: warps 6..9, one per TMEM lane quarter (warp id % 4).  For each stage
 // in the MMA thread's order: wait until its scale copies have landed, read its
-// eight 512-byte scale blocks (lane l: bytes 16 l .. 16 l + 15 of each, i.e.
-// rows l, l + 32, l + 64, l + 96 of the block's 128), write them to this
-// quarter's lanes of the stage's 32 scale columns (block j at columns 4 j ..
-// 4 j + 3), wait for the stores, and count the warp in on the stage's
-// scales-ready barrier.  The columns of a stage are rewritten only after its
+// 512-byte scale blocks (lane l: bytes 16 l .. 16 l + 15 of each, i.e. rows
+// l, l + 32, l + 64, l + 96 of the block's 128), write them to this quarter's
+// lanes of the stage's scale columns (P's chunk j at columns 4 j .. 4 j + 3;
+// the Q tile's chunk j from 16 + 4 QB j, its 128-row blocks i at + 4 i), wait
+// for the stores, and count the warp in on the stage's scales-ready barrier.  The columns of a stage are rewritten only after its
 // refill, i.e. after the MMAs that read them completed.
 template <int BN, bool SWAP>
 __device__ void scale_feeder(const GemmParams &p, uint8_t *sSF, uint64_t *sffull, uint64_t *sfull,
@@ -413,16 +422,23 @@ __device__ void scale_feeder(const GemmParams &p, uint8_t *sSF, uint64_t *sffull
             if (!__all_sync(0xffffffffu, ok))
                 return;
             const uint8_t *src = sSF + (size_t)stage * C::SF_BYTES + lane * 16;
-            uint32_t v[32];
+            constexpr int QB = C::SF_QB;
+            uint32_t v[C::SF_COLS];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint4 q = *reinterpret_cast<const uint4 *>(src + 512 * j);
-                v[4 * j] = q.x;
-                v[4 * j + 1] = q.y;
-                v[4 * j + 2] = q.z;
-                v[4 * j + 3] = q.w;
+            for (int b = 0; b < 4 + 4 * QB; ++b) {
+                // smem block b: P's chunk b (b < 4), else the Q tile's 128-row
+                // block i = (b - 4) / 4, chunk j = (b - 4) % 4
+                const int col = b < 4 ? 4 * b : 16 + 4 * QB * ((b - 4) % 4) + 4 * ((b - 4) / 4);
+                const uint4 q = *reinterpret_cast<const uint4 *>(src + 512 * b);
+                v[col] = q.x;
+                v[col + 1] = q.y;
+                v[col + 2] = q.z;
+                v[col + 3] = q.w;
             }
-            tmem_st_x32(t_lane + (uint32_t)(2 * BN + C::SF_COLS * stage), v);
+            const uint32_t t_st = t_lane + (uint32_t)(C::ACC_BUFS * BN + C::SF_COLS * stage);
+            tmem_st_x32(t_st, *reinterpret_cast<const uint32_t(*)[32]>(&v[0]));
+            if constexpr (C::SF_COLS == 48)
+                tmem_st_x16(t_st + 32, *reinterpret_cast<const uint32_t(*)[16]>(&v[32]));
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -1549,7 +1565,7 @@ __device__ void epilogue(const GemmParams &p, uint64_t *tfull, uint64_t *tempty,
             if (!coop_split_unit<BN, SWAP>(p, w, tbase, &tempty[abuf], red_bar, red, abort_f, &s_last[abuf]))
                 break;
         }
-        if (++abuf == 2) {
+        if (++abuf == (F4 ? Cfg<BN, SWAP, PAIR, F4>::ACC_BUFS : 2)) {
             abuf = 0;
             aphase ^= 1u;
         }

@@ -143,14 +143,17 @@ def test_block_scaled_gemm_matches_the_exact_sum(M, N, K, S, swap, monkeypatch):
     assert cosine(got, ref) > 0.9999999
 
 
-# "1": the weight-streaming role; "0": the tiled role (130, 256: several token tiles)
-@pytest.mark.parametrize("M,swap", [(130, "0"), (256, "0"), (40, "0"), (40, "1")])
-def test_gemm_scale_placement_one_block_at_a_time(M, swap, monkeypatch):
+# "1": the weight-streaming role; "0": the tiled role (130, 256: several token
+# tiles; N = 256: 256-row weight tiles, whose second 128 rows have scale
+# columns of their own)
+@pytest.mark.parametrize("M,swap,N", [(130, "0", 128), (256, "0", 128), (40, "0", 128), (40, "1", 128),
+                                      (130, "0", 256), (40, "1", 256)])
+def test_gemm_scale_placement_one_block_at_a_time(M, swap, N, monkeypatch):
     """Only one (row, K-group) scale of A nonzero: the product picks exactly
     that row's 16 elements of K -- pins the TMEM-ready layout end to end."""
     from realtime_transformer_gb300.nvfp4 import nvfp4_gemm
     monkeypatch.setenv("FRT_F4_SWAP", swap)
-    N, K = 128, 512
+    K = 512
     rng = np.random.default_rng(9)
     qa = rng.integers(0, 16, (M, K)).astype(np.uint8)
     qb = rng.integers(0, 16, (N, K)).astype(np.uint8)
@@ -168,7 +171,9 @@ def test_gemm_scale_placement_one_block_at_a_time(M, swap, monkeypatch):
         assert np.array_equal(got, ref), (m, g)
         assert np.count_nonzero(got[np.arange(M) != m]) == 0
     sa = np.full((M, K // 16), 0x38, np.uint8)
-    for (n, g) in [(0, 3), (64, 12), (127, 30)]:
+    for (n, g) in [(0, 3), (64, 12), (127, 30), (128, 1), (200, 22), (255, 31)]:
+        if n >= N:
+            continue
         sb = np.zeros((N, K // 16), np.uint8)
         sb[n, g] = 0x38
         out, err, _ = nvfp4_gemm(dev(pack(qa)), dev(sf_to_tmem(sa)), dev(pack(qb)), dev(sf_to_tmem(sb)), M, N, K,
