@@ -116,6 +116,23 @@ frt_status frt_fp4_debug_trace(frt_fp4_plan_t plan, int layer, const void *resid
                                void *u_codes, void *u_sf, void *h_codes, void *h_sf, int M, frt_stream_t stream);
 
 /*
+ * Test/diagnostic: layer `layer` step by step, each GEMM optionally started
+ * from caller-supplied quantised inputs (so that a test can feed the
+ * oracle's X and A and compare every row of each step alone): x_codes_in
+ * [M, d/2] with x_sf_in (TMEM-ready, ceil(M/128) * 128 * d/16 bytes) replace
+ * the norm's X for the gate/up GEMM; h_codes_in [M, ff/2] with h_sf_in
+ * (TMEM-ready) replace the gate/up epilogue's A for the down GEMM; either
+ * pair may be NULL (the kernels' own).  Copies out G and U (as
+ * frt_fp4_debug_trace; all four or none), A as the gate/up GEMM produced it
+ * (h_codes, h_sf; before any injection) and the layer output (out).
+ * Synchronises `stream`.
+ */
+frt_status frt_fp4_debug_trace_from(frt_fp4_plan_t plan, int layer, const void *residual_in, const void *hidden_in,
+                                   const void *x_codes_in, const void *x_sf_in, const void *h_codes_in,
+                                   const void *h_sf_in, void *out, void *g_codes, void *g_sf, void *u_codes,
+                                   void *u_sf, void *h_codes, void *h_sf, int M, frt_stream_t stream);
+
+/*
  * Test/diagnostic: copy a layer's quantised weight (which: 0 gate, 1 up,
  * 2 down) -- codes row-major [rows, K/2] and TMEM-ready scales (rows * K/16
  * bytes) of that weight's own rows (gate and up taken out of the interleaved

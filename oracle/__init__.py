@@ -761,6 +761,13 @@ def _nvfp4_awq_divide(y, awq):
     return (y * inv[None, :]).astype(np.float32)
 
 
+def nvfp4_gated_act(g4, u4, s_g, s_u, act):
+    """The combine step of the NVFP4 encoder FFN (itsolotime FlashRT article,
+    7.2): act(dec G) * dec U in fp32 from G and U as (E2M1 codes, row-major
+    block-scale codes) with tensor scales s_g, s_u."""
+    return _nvfp4_gated(g4, u4, s_g, s_u, act)
+
+
 def _nvfp4_gated(g4, u4, s_g, s_u, act):
     gd = nvfp4_decode(g4[0], g4[1], s_g)
     ud = nvfp4_decode(u4[0], u4[1], s_u)

@@ -80,6 +80,7 @@ SIGNATURES = {
     "frt_fp4_forward": (_I, [_P, _P, _P, _P, _I, _P]),
     "frt_fp4_debug_trace": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P]),
     "frt_fp4_debug_weights": (_I, [_P, _I, _I, _P, _P, _P]),
+    "frt_fp4_debug_trace_from": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P]),
     "frt_nvfp4_gemm": (_I, [_P, _P, _P, _P, _I, _I, _I, _F, _P, _I, _P, _P, _P, _P]),
     "frt_fp4_device_status": (_I, [_P, _P]),
 }
@@ -376,6 +377,12 @@ def frt_fp4_debug_trace(plan, layer, residual_in, hidden_in, out, r_prime, x_cod
                         u_sf, h_codes, h_sf, M, stream) -> None:
     _check(lib().frt_fp4_debug_trace(plan, layer, residual_in, hidden_in, out, r_prime, x_codes, x_sf, g_codes,
                                      g_sf, u_codes, u_sf, h_codes, h_sf, M, stream))
+
+
+def frt_fp4_debug_trace_from(plan, layer, residual_in, hidden_in, x_codes_in, x_sf_in, h_codes_in, h_sf_in, out,
+                             g_codes, g_sf, u_codes, u_sf, h_codes, h_sf, M, stream) -> None:
+    _check(lib().frt_fp4_debug_trace_from(plan, layer, residual_in, hidden_in, x_codes_in, x_sf_in, h_codes_in,
+                                          h_sf_in, out, g_codes, g_sf, u_codes, u_sf, h_codes, h_sf, M, stream))
 
 
 def frt_fp4_debug_weights(plan, layer, which, codes, sf, stream) -> None:

@@ -583,6 +583,46 @@ FRT_API frt_status frt_fp4_debug_trace(frt_fp4_plan_t P, int layer, const void *
     return FRT_OK;
 }
 
+FRT_API frt_status frt_fp4_debug_trace_from(frt_fp4_plan_t P, int layer, const void *residual_in,
+                                           const void *hidden_in, const void *x_codes_in, const void *x_sf_in,
+                                           const void *h_codes_in, const void *h_sf_in, void *out, void *g_codes,
+                                           void *g_sf, void *u_codes, void *u_sf, void *h_codes, void *h_sf, int M,
+                                           frt_stream_t stream) {
+    frt_status st = check_call(P, residual_in, hidden_in, out, M);
+    if (st != FRT_OK || M == 0)
+        return st;
+    if (layer < 0 || layer >= P->L)
+        return ffail(FRT_ERR_INVALID_ARG, "layer %d out of range [0, %d)", layer, P->L);
+    if ((g_codes || g_sf || u_codes || u_sf) && !(g_codes && g_sf && u_codes && u_sf))
+        return ffail(FRT_ERR_INVALID_ARG, "g/u codes and scales: all four or none");
+    if (!x_codes_in != !x_sf_in || !h_codes_in != !h_sf_in)
+        return ffail(FRT_ERR_INVALID_ARG, "injected codes and scales come in pairs");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t d = P->d, ff = P->ff, m = (size_t)M, mt = (size_t)(M + 127) / 128 * 128;
+    const cudaMemcpyKind k = cudaMemcpyDeviceToDevice;
+    uint8_t *const dbg[4] = {static_cast<uint8_t *>(g_codes), static_cast<uint8_t *>(g_sf),
+                             static_cast<uint8_t *>(u_codes), static_cast<uint8_t *>(u_sf)};
+    FCK(f4_norm(P, layer, residual_in, hidden_in, M, false, s));
+    if (x_codes_in) {
+        FCK(cudaMemcpyAsync(P->xq, x_codes_in, m * d / 2, k, s));
+        FCK(cudaMemcpyAsync(P->xsf, x_sf_in, mt * d / 16, k, s));
+    }
+    st = f4_gate_up(P, layer, M, EPI_F4_GATED, s, g_codes ? dbg : nullptr);
+    if (st != FRT_OK)
+        return st;
+    if (h_codes) FCK(cudaMemcpyAsync(h_codes, P->hq, m * ff / 2, k, s));
+    if (h_sf) FCK(cudaMemcpyAsync(h_sf, P->hsf, mt * ff / 16, k, s));
+    if (h_codes_in) {
+        FCK(cudaMemcpyAsync(P->hq, h_codes_in, m * ff / 2, k, s));
+        FCK(cudaMemcpyAsync(P->hsf, h_sf_in, mt * ff / 16, k, s));
+    }
+    st = f4_down(P, layer, hidden_in ? static_cast<const void *>(P->rp) : residual_in, out, M, s);
+    if (st != FRT_OK)
+        return st;
+    FCK(cudaStreamSynchronize(s));
+    return FRT_OK;
+}
+
 namespace {
 
 // Byte offset of (row, 16-element group g) in the TMEM-ready scale order of

@@ -84,6 +84,35 @@ class FP4Plan:
             del t["r_prime"]
         return t
 
+    def trace_from(self, layer, residual, hidden=None, x=None, h=None, stream=None):
+        """One layer step by step: x = (codes [M, d/2] uint8, TMEM-ready scales) replaces the norm's X for
+        the gate/up GEMM, h = (codes [M, ff/2], TMEM-ready scales) the gate/up output A for the down GEMM
+        (None: the kernels' own).  Returns g/u codes and row-major scales, h as the gate/up GEMM produced
+        it, and the layer output."""
+        M, d, ff = residual.shape[0], self.d, self.ff
+        dev = residual.device
+        mt = (M + 127) // 128 * 128
+        u8 = lambda *s: torch.empty(s, dtype=torch.uint8, device=dev)
+        t = {"out": torch.empty_like(residual), "g_codes": u8(M, ff // 2), "g_sf": u8(M, ff // 16),
+             "u_codes": u8(M, ff // 2), "u_sf": u8(M, ff // 16), "h_codes": u8(M, ff // 2), "h_sf": u8(mt * ff // 16)}
+
+        def pair(v, kk, what):
+            if v is None:
+                return None, None
+            codes, sf = v
+            if codes.dtype != torch.uint8 or sf.dtype != torch.uint8 or tuple(codes.shape) != (M, kk // 2) or \
+                    sf.numel() != mt * kk // 16 or not codes.is_contiguous() or not sf.is_contiguous():
+                raise ValueError("%s: uint8 codes (%d, %d) and %d scale bytes" % (what, M, kk // 2, mt * kk // 16))
+            return codes.data_ptr(), sf.data_ptr()
+
+        xc, xs = pair(x, d, "x")
+        hc, hs = pair(h, ff, "h")
+        N.frt_fp4_debug_trace_from(self.handle, layer, _bf16(residual, (M, d), "residual"),
+                                   _bf16(hidden, (M, d), "hidden") if hidden is not None else None, xc, xs, hc, hs,
+                                   *[t[k].data_ptr() for k in ("out", "g_codes", "g_sf", "u_codes", "u_sf",
+                                                               "h_codes", "h_sf")], M, _stream(stream))
+        return t
+
     def weights(self, layer, which, stream=None):
         """which: 'gate', 'up' or 'down' -> (codes row-major [rows, K/2], TMEM-ready scales)."""
         w = {"gate": 0, "up": 1, "down": 2}[which]

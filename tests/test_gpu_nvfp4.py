@@ -6,9 +6,10 @@ accumulation; weight preparation bit-exact; activation codes and block scales
 identical wherever the oracle's value before rounding is not at a rounding
 tie, E2M1 codes compared with +0 and -0 equal (FP4 values lie on a coarse
 grid, so exact ties are common, and a last-ulp difference -- accumulation
-order, tanhf -- may take the other side; both roundings are valid there and
-must be one step apart); layer outputs under the FP8 path's contract on rows
-whose quantised activations agree."""
+order, the activation's hardware approximations -- may take the other side;
+both roundings are valid there and must be one step apart), every step on
+every row from the oracle's own input to it; layer outputs under the FP8
+path's contract."""
 import numpy as np
 import pytest
 import torch
@@ -233,37 +234,39 @@ def test_weight_preparation_is_bit_exact(layer_case):
 
 
 def test_layer_matches_oracle(layer_case):
+    """Every step on every row, each started from the oracle's own input to
+    that step (the GPU GEMMs fed the oracle's X and A through
+    frt_fp4_debug_trace_from; the combine checked on the GPU's own G and U);
+    then the kernels' own path through the whole layer."""
     c = layer_case
-    wl, plan = c["wl"], c["plan"]
+    wl, plan, sc = c["wl"], c["plan"], c["sc"]
     r, h = c["r"].cuda(), c["h"].cuda()
+    ref = oracle.ffn_layer_nvfp4(bits(c["r"]), bits(c["h"]), c["L"], sc, wl.act_id, trace=True)
+    M, d, ff = wl.M, wl.d, wl.ff
     tr = plan.trace(0, r, h)
     torch.cuda.synchronize()
     plan.device_status()
-    ref = oracle.ffn_layer_nvfp4(bits(c["r"]), bits(c["h"]), c["L"], c["sc"], wl.act_id, trace=True)
-    M, d, ff = wl.M, wl.d, wl.ff
+    # N1: r' bit for bit, X under the tie-aware code contract
     assert np.array_equal(bits(tr["r_prime"]), ref.r_prime)
-    # N1: the normalised activation
-    xq = unpack(tr["x_codes"].cpu().numpy())
-    xs = sf_from_tmem(tr["x_sf"].cpu().numpy(), M, d)
-    rows = check_nvfp4(xq, xs, ref.x[0], ref.x[1], ref.y, c["sc"].s_x, "x")
-    assert rows.mean() >= 0.5
-    # N2: gate and up, on rows whose X agrees
-    gq, uq = unpack(tr["g_codes"].cpu().numpy()), unpack(tr["u_codes"].cpu().numpy())
-    gs, us = tr["g_sf"].cpu().numpy(), tr["u_sf"].cpu().numpy()
-    rows_g = check_nvfp4(gq[rows], gs[rows], ref.g[0][rows], ref.g[1][rows], ref.g_f32[rows], c["sc"].s_g, "gate")
-    rows_u = check_nvfp4(uq[rows], us[rows], ref.u[0][rows], ref.u[1][rows], ref.u_f32[rows], c["sc"].s_u, "up")
-    sel = np.nonzero(rows)[0]
-    rows[sel[~(rows_g & rows_u)]] = False
-    assert rows.mean() >= 0.25
-    # N3: the gated activation, on rows whose G and U agree
-    hq = unpack(tr["h_codes"].cpu().numpy())
-    hs = sf_from_tmem(tr["h_sf"].cpu().numpy(), M, ff)
-    rows_h = check_nvfp4(hq[rows], hs[rows], ref.h[0][rows], ref.h[1][rows], ref.a[rows], c["sc"].s_h, "h")
-    sel = np.nonzero(rows)[0]
-    rows[sel[~rows_h]] = False
-    # N4: the output, on rows whose every quantised activation agrees
-    if rows.any():
-        check_bf16(bits(tr["out"])[rows], ref.out[rows], "out")
+    check_nvfp4(unpack(tr["x_codes"].cpu().numpy()), sf_from_tmem(tr["x_sf"].cpu().numpy(), M, d), ref.x[0],
+                ref.x[1], ref.y, sc.s_x, "x")
+    tf = plan.trace_from(0, r, h, x=(dev(pack(ref.x[0])), dev(sf_to_tmem(ref.x[1]))),
+                         h=(dev(pack(ref.h[0])), dev(sf_to_tmem(ref.h[1]))))
+    torch.cuda.synchronize()
+    plan.device_status()
+    # N2 from the oracle's X: G and U
+    gq, gs = unpack(tf["g_codes"].cpu().numpy()), tf["g_sf"].cpu().numpy()
+    uq, us = unpack(tf["u_codes"].cpu().numpy()), tf["u_sf"].cpu().numpy()
+    check_nvfp4(gq, gs, ref.g[0], ref.g[1], ref.g_f32, sc.s_g, "gate")
+    check_nvfp4(uq, us, ref.u[0], ref.u[1], ref.u_f32, sc.s_u, "up")
+    # N3 on the GPU's own G and U: the oracle's combine of those codes
+    a = oracle.nvfp4_gated_act((gq, gs), (uq, us), sc.s_g, sc.s_u, wl.act_id)
+    h_ref = oracle.nvfp4_quantize(a, sc.s_h)
+    check_nvfp4(unpack(tf["h_codes"].cpu().numpy()), sf_from_tmem(tf["h_sf"].cpu().numpy(), M, ff), h_ref[0],
+                h_ref[1], a, sc.s_h, "h")
+    # N4 from the oracle's A: the output under the FP8 path's contract
+    check_bf16(bits(tf["out"]), ref.out, "out")
+    # the kernels' own path through the layer
     got_all = oracle.bf16_decode(bits(tr["out"]))
     assert cosine(got_all, oracle.bf16_decode(ref.out)) > 0.9999
     # the stack entry point (one layer) computes what the trace computes

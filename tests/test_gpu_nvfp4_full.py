@@ -6,10 +6,10 @@ whose GEMMs take other tilings and split-K factors than the small cases.
 Rows are independent once the scales are fixed, so the oracle runs the layer
 on sampled rows (spread over the token tiles, the first and last included)
 while the GPU runs all of them.  Weight preparation is compared bit for bit;
-the quantised activations under the tie-aware NVFP4 contract of the small
-cases (tests/test_gpu_nvfp4.py), the output on rows whose quantised
-activations agree under the FP8 path's contract, and all sampled rows'
-outputs under its cosine bound."""
+every step on every sampled row, from the oracle's own input to that step
+(its X and A fed to the GPU GEMMs on those rows), under the contract of the
+small cases (tests/test_gpu_nvfp4.py); the kernels' own path under the
+cosine bound."""
 import numpy as np
 import pytest
 import torch
@@ -17,9 +17,13 @@ import torch
 import oracle
 import synthetic
 from parity import bits, check_bf16, cosine
-from test_gpu_nvfp4 import check_nvfp4, canon, sf_from_tmem, unpack
+from test_gpu_nvfp4 import _sf_index as sf_index, check_nvfp4, canon, pack, sf_from_tmem, unpack
 
 pytestmark = pytest.mark.gpu
+
+
+def dev_u8(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
 
 @pytest.mark.parametrize("name", ["vla_prefix", "llm_decode", "long_prefill"])
@@ -56,27 +60,30 @@ def test_full_size_nvfp4_layer(name):
         assert np.array_equal(bits(tr["r_prime"])[rows], ref.r_prime)
         xq = unpack(tr["x_codes"].cpu().numpy())[rows]
         xs = sf_from_tmem(tr["x_sf"].cpu().numpy(), M, d)[rows]
-        ok = check_nvfp4(xq, xs, ref.x[0], ref.x[1], ref.y, sc.s_x, name + " x")
-        gq = unpack(tr["g_codes"].cpu().numpy())[rows]
-        uq = unpack(tr["u_codes"].cpu().numpy())[rows]
-        gs, us = tr["g_sf"].cpu().numpy()[rows], tr["u_sf"].cpu().numpy()[rows]
-        if ok.any():
-            ok_g = check_nvfp4(gq[ok], gs[ok], ref.g[0][ok], ref.g[1][ok], ref.g_f32[ok], sc.s_g, name + " gate")
-            ok_u = check_nvfp4(uq[ok], us[ok], ref.u[0][ok], ref.u[1][ok], ref.u_f32[ok], sc.s_u, name + " up")
-            sel = np.nonzero(ok)[0]
-            ok[sel[~(ok_g & ok_u)]] = False
-        if ok.any():
-            hq = unpack(tr["h_codes"].cpu().numpy())[rows]
-            hs = sf_from_tmem(tr["h_sf"].cpu().numpy(), M, ff)[rows]
-            ok_h = check_nvfp4(hq[ok], hs[ok], ref.h[0][ok], ref.h[1][ok], ref.a[ok], sc.s_h, name + " h")
-            sel = np.nonzero(ok)[0]
-            ok[sel[~ok_h]] = False
-        got = bits(tr["out"])[rows]
-        if ok.any():
-            check_bf16(got[ok], ref.out[ok], name + " out")
-        c = cosine(oracle.bf16_decode(got), oracle.bf16_decode(ref.out))
-        print("%s NVFP4 layer: rows %s, %d with every quantised activation identical, out cosine %.7f" % (
-            name, list(rows), int(ok.sum()), c))
+        check_nvfp4(xq, xs, ref.x[0], ref.x[1], ref.y, sc.s_x, name + " x")
+        # the GEMMs from the oracle's X and A on the sampled rows (the GPU's own elsewhere)
+        x_codes, x_sf = tr["x_codes"].cpu().numpy().copy(), tr["x_sf"].cpu().numpy().copy()
+        h_codes, h_sf = tr["h_codes"].cpu().numpy().copy(), tr["h_sf"].cpu().numpy().copy()
+        x_codes[rows] = pack(ref.x[0])
+        x_sf[sf_index(M, d)[rows]] = ref.x[1]
+        h_codes[rows] = pack(ref.h[0])
+        h_sf[sf_index(M, ff)[rows]] = ref.h[1]
+        tf = plan.trace_from(0, r, h, x=(dev_u8(x_codes), dev_u8(x_sf)), h=(dev_u8(h_codes), dev_u8(h_sf)))
+        torch.cuda.synchronize()
+        plan.device_status()
+        gq, gs = unpack(tf["g_codes"].cpu().numpy())[rows], tf["g_sf"].cpu().numpy()[rows]
+        uq, us = unpack(tf["u_codes"].cpu().numpy())[rows], tf["u_sf"].cpu().numpy()[rows]
+        check_nvfp4(gq, gs, ref.g[0], ref.g[1], ref.g_f32, sc.s_g, name + " gate")
+        check_nvfp4(uq, us, ref.u[0], ref.u[1], ref.u_f32, sc.s_u, name + " up")
+        a = oracle.nvfp4_gated_act((gq, gs), (uq, us), sc.s_g, sc.s_u, wl.act_id)
+        h_ref = oracle.nvfp4_quantize(a, sc.s_h)
+        check_nvfp4(unpack(tf["h_codes"].cpu().numpy())[rows], sf_from_tmem(tf["h_sf"].cpu().numpy(), M, ff)[rows],
+                    h_ref[0], h_ref[1], a, sc.s_h, name + " h")
+        check_bf16(bits(tf["out"])[rows], ref.out, name + " out")
+        # the kernels' own path
+        c = cosine(oracle.bf16_decode(bits(tr["out"])[rows]), oracle.bf16_decode(ref.out))
+        print("%s NVFP4 layer: rows %s, every step on every sampled row; own-path out cosine %.7f" % (
+            name, list(rows), c))
         assert c > 0.9999, c
     finally:
         plan.close()
