@@ -96,10 +96,15 @@ void plan_gemm(GemmLaunch &g, bool swap, int m_tok, int n_feat, int K, int num_s
         p.n_tiles_p = (n_feat + BM - 1) / BM;
         p.n_tiles_q = (m_tok + g.bn - 1) / g.bn;
     } else {
-        // NVFP4: FRT_F4_BN=128 keeps 128-wide tiles (two accumulators)
-        // where 256 would fit (one accumulator beside the stages' scales)
+        // NVFP4: 256-wide tiles have one accumulator (beside the stages'
+        // scales), so a tile's epilogue runs between its MMAs and the next
+        // tile's; with at most 8 k-blocks a tile that costs more than the
+        // doubled MACs a k-block gain, and 128-wide tiles (two accumulators)
+        // are used (measured: VLA prefix 92.2 against 95.9 us/layer; long
+        // prefill, 20 k-blocks, 1164 against 1337 with 128-wide gate/up
+        // tiles).  FRT_F4_BN=128 keeps 128 everywhere.
         const char *fb = f4 ? getenv("FRT_F4_BN") : nullptr;
-        g.bn = (n_feat % 256 == 0 && !(fb && atoi(fb) == 128)) ? 256 : 128;
+        g.bn = (n_feat % 256 == 0 && !(fb && atoi(fb) == 128) && !(f4 && p.k_blocks <= 8)) ? 256 : 128;
         p.n_tiles_p = (m_tok + BM - 1) / BM;
         p.n_tiles_q = (n_feat + g.bn - 1) / g.bn;
     }
