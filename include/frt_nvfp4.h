@@ -162,8 +162,22 @@ frt_status frt_nvfp4_gemm(const void *a_codes, const void *a_sf, const void *b_c
                           frt_stream_t stream);
 
 /* Synchronise `stream` and report a kernel that gave up a bounded wait
- * (DEVICE_TIMEOUT; the plan's error word is then cleared). */
+ * (DEVICE_TIMEOUT; the plan's error word and split-K counters are then
+ * cleared). */
 frt_status frt_fp4_device_status(frt_fp4_plan_t plan, frt_stream_t stream);
+
+/*
+ * Test hook for the failure path (no counterpart in the pages): launch layer
+ * 0's gate/up GEMM for M tokens (the weight-streaming role for M <= 64, else
+ * the tiled one) whose MMA thread first waits for a barrier phase that
+ * nothing completes.  The bounded wait gives up after about 2 s, sets the
+ * plan's error word, and every role of the kernel -- the scale warps
+ * included -- drains its copies, frees its tensor memory and exits; the call
+ * then returns what frt_fp4_device_status reports -- DEVICE_TIMEOUT -- and the
+ * plan (and the CUDA context) stay usable.  Overwrites the plan's activation
+ * scratch.  Errors: INVALID_ARG, SHAPE, CUDA, DEVICE_TIMEOUT.
+ */
+frt_status frt_fp4_debug_stall(frt_fp4_plan_t plan, int M, frt_stream_t stream);
 
 #ifdef __cplusplus
 }

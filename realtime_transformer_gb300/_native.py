@@ -83,6 +83,7 @@ SIGNATURES = {
     "frt_fp4_debug_trace_from": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P]),
     "frt_nvfp4_gemm": (_I, [_P, _P, _P, _P, _I, _I, _I, _F, _P, _I, _P, _P, _P, _P]),
     "frt_fp4_device_status": (_I, [_P, _P]),
+    "frt_fp4_debug_stall": (_I, [_P, _I, _P]),
 }
 
 
@@ -396,3 +397,7 @@ def frt_nvfp4_gemm(a_codes, a_sf, b_codes, b_sf, M, N, K, alpha, out, splits, ws
 
 def frt_fp4_device_status(plan, stream) -> None:
     _check(lib().frt_fp4_device_status(plan, stream))
+
+
+def frt_fp4_debug_stall(plan, M, stream) -> None:
+    _check(lib().frt_fp4_debug_stall(plan, M, stream))

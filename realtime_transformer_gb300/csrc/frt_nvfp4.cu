@@ -327,7 +327,8 @@ frt_status f4_maps(frt_fp4_plan *P, GemmLaunch &g, int wbuf, int xbuf, int l, in
 // requantised into the A buffers (epi EPI_F4_GATED), or the calibration
 // amaxes (EPI_F4_AMAX_GU: amax[0], amax[1]; EPI_F4_AMAX_H: amax[2]).  dbg: G
 // and U codes and row-major scales (trace), or nulls.
-frt_status f4_gate_up(frt_fp4_plan *P, int l, int M, int epi, cudaStream_t s, uint8_t *const dbg[4]) {
+frt_status f4_gate_up(frt_fp4_plan *P, int l, int M, int epi, cudaStream_t s, uint8_t *const dbg[4],
+                      bool stall = false) {
     GemmLaunch g;
     memset(&g.p, 0, sizeof g.p);
     plan_gemm(g, f4_swap(M), M, 2 * P->ff, P->d / 2, P->num_sms, 1, nullptr, true);
@@ -359,7 +360,8 @@ frt_status f4_gate_up(frt_fp4_plan *P, int l, int M, int epi, cudaStream_t s, ui
         p.dbg_uq = dbg[2];
         p.dbg_us = dbg[3];
     }
-    FCK(launch_gemm(g, s, P->pdl));
+    p.stall_test = stall ? 1 : 0;
+    FCK(launch_gemm(g, s, P->pdl && !stall));
     return FRT_OK;
 }
 
@@ -711,6 +713,18 @@ FRT_API frt_status frt_nvfp4_gemm(const void *a_codes, const void *a_sf, const v
     p.err = err;
     FCK(launch_gemm(g, static_cast<cudaStream_t>(stream), false));
     return FRT_OK;
+}
+
+FRT_API frt_status frt_fp4_debug_stall(frt_fp4_plan_t P, int M, frt_stream_t stream) {
+    if (!P)
+        return ffail(FRT_ERR_INVALID_ARG, "null plan");
+    if (M < 1 || M > P->M_max)
+        return ffail(M < 1 ? FRT_ERR_INVALID_ARG : FRT_ERR_SHAPE, "M=%d outside [1, M_max=%d]", M, P->M_max);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const frt_status st = f4_gate_up(P, 0, M, EPI_F4_GATED, s, nullptr, true);
+    if (st != FRT_OK)
+        return st;
+    return frt_fp4_device_status(P, stream);
 }
 
 FRT_API frt_status frt_fp4_device_status(frt_fp4_plan_t P, frt_stream_t stream) {

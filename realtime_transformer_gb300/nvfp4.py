@@ -126,6 +126,10 @@ class FP4Plan:
     def device_status(self, stream=None):
         N.frt_fp4_device_status(self.handle, _stream(stream))
 
+    def debug_stall(self, M, stream=None):
+        """Test hook: a gate/up GEMM whose bounded wait gives up; raises FrtError(DEVICE_TIMEOUT)."""
+        N.frt_fp4_debug_stall(self.handle, M, _stream(stream))
+
 
 def nvfp4_gemm(a_codes, a_sf, b_codes, b_sf, M, N_, K, alpha=1.0, splits=1, stream=None):
     """Diagnostic block-scaled GEMM: fp32 [M, N] = alpha * A . B^T over NVFP4

@@ -7,6 +7,7 @@ import pytest
 import torch
 
 import oracle
+import synthetic
 
 pytestmark = pytest.mark.gpu
 
@@ -33,3 +34,30 @@ def test_bounded_wait_gives_up_and_plan_recovers():
     plan.device_status()
     assert np.array_equal(C.cpu().numpy(), oracle.gemm_e4m3(A, B))
     plan.close()
+
+
+@pytest.mark.parametrize("M", [8, 300], ids=["weight_streaming", "tiled"])
+def test_nvfp4_bounded_wait_gives_up_and_plan_recovers(M):
+    """The NVFP4 GEMM (with its scale warps and per-stage scale barriers)
+    gives up the same way, and the plan then computes the same bits."""
+    from realtime_transformer_gb300.nvfp4 import FP4Plan
+    from realtime_transformer_gb300._native import FrtError
+    wl = synthetic.WORKLOADS["tiny"].with_(M=M, d=512, ff=1024)
+    lw = synthetic.layer_weights(wl, 0, device=torch.device("cuda"))
+    r, h = synthetic.inputs(wl, device=torch.device("cuda"))
+    plan = FP4Plan(wl.d, wl.ff, wl.act, wl.M, 1)
+    try:
+        plan.load_weights(0, lw["w_norm"], lw["w_gate"], lw["w_up"], lw["w_down"])
+        plan.set_scales([[0.002, 0.01, 0.01, 0.004]])
+        before = plan.forward(r, h)
+        torch.cuda.synchronize()
+        with pytest.raises(FrtError) as err:
+            plan.debug_stall(M)
+        assert err.value.name == "FRT_ERR_DEVICE_TIMEOUT"
+        plan.device_status()  # the flag was cleared by the report
+        after = plan.forward(r, h)
+        torch.cuda.synchronize()
+        plan.device_status()
+        assert torch.equal(before, after)
+    finally:
+        plan.close()
