@@ -333,6 +333,64 @@ def timed_steps(stream, flush, fn, n, warm):
     return [e0.elapsed_time(e1) for e0, e1 in evs]
 
 
+L2_BYTES = 129 * 1024 * 1024
+
+
+def pipelined_e2e(stream, dev, replay, io, out, h_io, h_o, steps, warmup):
+    """End to end as a serving loop runs it, for steps whose inputs exceed L2
+    (so no flush is needed between them): step i+1's inputs are copied from
+    pinned host memory into one of two device staging buffers on a copy stream
+    while step i computes, and step i's output goes back to pinned host memory
+    while step i+1 computes; a step copies its staged inputs into the graph's
+    input buffer and its output into a staging buffer (device to device).  One
+    pair of events brackets all `steps` steps, every host-to-device and
+    device-to-host copy included.  Returns seconds for the steps."""
+    cs = torch.cuda.Stream(device=dev)
+    st_in = [torch.empty_like(io) for _ in range(2)]
+    st_out = [torch.empty_like(out) for _ in range(2)]
+
+    def run(n):
+        in_ready, in_free = [torch.cuda.Event() for _ in range(2)], [torch.cuda.Event() for _ in range(2)]
+        out_ready, out_free = [torch.cuda.Event() for _ in range(2)], [torch.cuda.Event() for _ in range(2)]
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        for b in range(2):
+            in_free[b].record(stream)
+            out_free[b].record(cs)
+        e0.record(cs)
+
+        def h2d(i):
+            b = i % 2
+            cs.wait_event(in_free[b])
+            with torch.cuda.stream(cs):
+                st_in[b].copy_(h_io, non_blocking=True)
+            in_ready[b].record(cs)
+
+        h2d(0)
+        for i in range(n):
+            b = i % 2
+            if i + 1 < n:
+                h2d(i + 1)
+            stream.wait_event(in_ready[b])
+            with torch.cuda.stream(stream):
+                io.copy_(st_in[b])
+                in_free[b].record(stream)
+                replay()
+                stream.wait_event(out_free[b])
+                st_out[b].copy_(out)
+                out_ready[b].record(stream)
+            cs.wait_event(out_ready[b])
+            with torch.cuda.stream(cs):
+                h_o.copy_(st_out[b], non_blocking=True)
+            out_free[b].record(cs)
+        e1.record(cs)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / 1000.0
+
+    run(warmup)
+    return run(steps)
+
+
 def run_ours(args, wl, world, rank, local):
     """One workload: the stack graph-replayed K times (CUDA events, L2 flushed
     between steps), end to end through the C ABI with pinned host buffers,
@@ -408,8 +466,16 @@ def run_ours(args, wl, world, rank, local):
         plan.graph_replay(wl.M, stream)
         h_o.copy_(out, non_blocking=True)
 
-    e2e_ms = timed_steps(stream, flush, e2e_step, args.steps, args.warmup)
-    e2e_s = reduce_max(sum(e2e_ms) / 1000.0, world, dev)
+    # steps whose inputs exceed L2: the serving loop's overlap of the copies
+    # with the previous and next steps' compute; else one step at a time, L2
+    # flushed before each
+    e2e_pipelined = io.numel() * io.element_size() > L2_BYTES and not WARM_L2
+    if e2e_pipelined:
+        e2e_s = reduce_max(pipelined_e2e(stream, dev, replay, io, out, h_io, h_o, args.steps, args.warmup), world,
+                           dev)
+    else:
+        e2e_ms = timed_steps(stream, flush, e2e_step, args.steps, args.warmup)
+        e2e_s = reduce_max(sum(e2e_ms) / 1000.0, world, dev)
     h2d = h_io.numel() * 2
     d2h = h_o.numel() * 2
 
@@ -478,7 +544,12 @@ def run_ours(args, wl, world, rank, local):
         "roofline": roof, "step_roofline": step_roof,
         "kernels_us_in_stack": {k: v / launches for k, v in kern_total.items()},
         "e2e": {"value": world * wl.M * args.steps / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": 1000.0 * e2e_s / args.steps},
+                "d2h_bytes_per_step": d2h, "ms_per_step": 1000.0 * e2e_s / args.steps,
+                "timing": ("all steps between one pair of events; step i+1's inputs copied in (pinned host -> "
+                           "device staging) and step i-1's output read back while step i computes, as a serving "
+                           "loop overlaps them; inputs larger than L2, no flush") if e2e_pipelined else
+                          ("per step, L2 flushed before each: host-to-device copy, graph replay, device-to-host "
+                           "copy in order on one stream")},
         "gpu_launches": args.steps * n_k, "clocks": clocks, "wall_s_timed_region": t_wall,
     }
     sc = plan.scales()
