@@ -94,6 +94,12 @@ def test_nvfp4_entry_points_check_arguments_before_any_cuda_call(native):
     assert L.frt_fp4_forward(None, None, None, None, 1, None) == 1
     assert L.frt_fp4_set_scales(None, None) == 1
     assert L.frt_fp4_device_status(None, None) == 1
+    assert L.frt_fp4_debug_stall(None, 8, None) == 1
+    assert L.frt_fp4_debug_trace_from(None, 0, None, None, None, None, None, None, None, None, None, None, None,
+                                      None, None, 8, None) == 1
+    assert L.frt_fp4_debug_trace(None, 0, None, None, None, None, None, None, None, None, None, None, None, None,
+                                 8, None) == 1
+    assert L.frt_fp4_debug_weights(None, 0, 0, None, None, None) == 1
     assert L.frt_fp4_plan_destroy(None) == 0
     # the diagnostic GEMM rejects shapes its tiles do not cover
     assert L.frt_nvfp4_gemm(None, None, None, None, 8, 128, 256, ctypes.c_float(1.0), None, 1, None, None, None,
