@@ -129,6 +129,14 @@ void plan_gemm(GemmLaunch &g, bool swap, int m_tok, int n_feat, int K, int num_s
     p.splits = (p.k_blocks + p.kb_per_split - 1) / p.kb_per_split;
     p.total_units = tiles * p.splits;
     g.grid = std::min(p.total_units, num_sms);
+    // persistent weight-streaming launches: the fewest CTAs that keep the
+    // number of waves (272 tiles on 152 SMs: 136 CTAs of two tiles instead of
+    // 120 of two and 32 of one, the same makespan), which leaves the other SMs
+    // to the next kernel's early start (decode layer: 48.5 against 49.0 us)
+    if (swap && p.splits == 1 && p.total_units > num_sms) {
+        const int waves = (p.total_units + num_sms - 1) / num_sms;
+        g.grid = (p.total_units + waves - 1) / waves;
+    }
     // tiled role on CTA pairs (FRT_FFN_PAIR=0 disables): 256-token tiles
     // computed by two CTAs with cta_group::2 MMAs, each staging its own 128
     // tokens and half of the 256-row weight tile -- half the weight traffic
