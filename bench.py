@@ -46,7 +46,10 @@ STEP_NAMES = ["norm_quant", "gemm_gate_up_act", "gemm_down"]
 KERNEL_SOURCES = {"norm_quant": ["k_elementwise.cu", "frt_ptx.cuh"],
                   "gemm_gate_up_act": ["k_gemm_tc.cuh", "k_gemm_fp8.cu", "frt_ptx.cuh", "frt_epi.cuh", "frt_f4.cuh"],
                   "gemm_down": ["k_gemm_tc.cuh", "k_gemm_fp8.cu", "frt_ptx.cuh", "frt_epi.cuh", "frt_f4.cuh"],
-                  "ffn_stack": ["k_stack_fp8.cu", "frt_ptx.cuh", "frt_epi.cuh"]}
+                  "ffn_stack": ["k_stack_fp8.cu", "frt_ptx.cuh", "frt_epi.cuh"],
+                  "nvfp4_norm_quant": ["k_nvfp4.cu", "frt_ptx.cuh", "frt_f4.cuh"],
+                  "nvfp4_gemm": ["k_gemm_tc.cuh", "k_gemm_f4.cu", "frt_ptx.cuh", "frt_epi.cuh", "frt_f4.cuh"]}
+FP4_STEP_NAMES = ["nvfp4_norm_quant", "nvfp4_gemm_gate_up", "nvfp4_gemm_down"]
 
 
 # ----------------------------------------------------------------- helpers --
@@ -96,6 +99,19 @@ def fp4_layer_bytes_flops(wl, M):
     return 3 * wl.d * wl.ff // 2 + 3 * wl.d * wl.ff // 16 + 4 * M * wl.d, 6.0 * M * wl.d * wl.ff
 
 
+def fp4_kernel_bytes_flops(wl, M, step):
+    """Algorithmic bytes and FLOPs of one launch of one NVFP4 step, for M
+    tokens (codes half a byte an element, E4M3 block scales one byte per 16)."""
+    d, ff = wl.d, wl.ff
+    if step == 0:   # residual + norm weight in, X codes and scales out
+        return 2 * M * d + 2 * d + M * d // 2 + M * d // 16, 0
+    if step == 1:   # [W_g; W_u] codes + scales and X in, A codes and scales out
+        return (2 * ff * d // 2 + 2 * ff * d // 16 + M * d // 2 + M * d // 16 + M * ff // 2 + M * ff // 16,
+                4.0 * M * d * ff)
+    # W_d codes + scales and A in, residual in, out
+    return d * ff // 2 + d * ff // 16 + M * ff // 2 + M * ff // 16 + 4 * M * d, 2.0 * M * d * ff
+
+
 def source_code_only(text):
     """The code of a CUDA/C++ source without its comments and blank lines
     (string literals in these sources hold no comment markers)."""
@@ -114,23 +130,26 @@ def source_hash(names):
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel, workload):
+def profiled_traffic(kernel, workload, index=0):
     """dram read+write bytes per launch recorded from an ncu capture in
-    profiles/, if the kernel source has not changed since."""
+    profiles/ (the index-th kernel of the summary), if the kernel source has
+    not changed since."""
     path = os.path.join(ROOT, "profiles", "ncu_%s_%s.md" % (kernel, workload))
     if not os.path.exists(path):
         return None
-    rec = {}
+    rec, traffic = {}, []
     with open(path) as f:
         for line in f:
             if ":" in line and line.startswith("- "):
                 k, v = line[2:].split(":", 1)
                 rec[k.strip()] = v.strip().strip("`")
+                if k.strip() == "traffic_bytes_per_launch":
+                    traffic.append(v.strip())
     if rec.get("source_sha256_16") != source_hash(KERNEL_SOURCES[kernel]):
         return None
     try:
-        return int(float(rec["traffic_bytes_per_launch"]))
-    except (KeyError, ValueError):
+        return int(float(traffic[index]))
+    except (IndexError, ValueError):
         return None
 
 
@@ -821,26 +840,46 @@ def run_fp4(args, wl, world, rank, local):
     e2e_ms = timed(e2e_step, args.steps, args.warmup)
     e2e_s = reduce_max(sum(e2e_ms) / 1000.0, world, dev)
 
-    # roofline of one layer (its three kernels together): FP4 weights and their
-    # scales + the residual stream in and out, against HBM or the FP4 tensor
-    # peak by intensity (the sustained bf16 figure for steps of a millisecond
-    # and more, as the FP8 arm)
-    layer_s = ms_step / 1000.0 / wl.L
-    nbytes, flops = fp4_layer_bytes_flops(wl, wl.M)
+    # against HBM or the FP4 tensor peak by intensity (the sustained bf16
+    # figure for steps of a millisecond and more, as the FP8 arm)
     long_step = ms_step >= 1.0
     fp4_peak = 6.0 * (P["bf16_tflops_sustained"] if long_step else P["bf16_tflops"])
-    if flops / nbytes > fp4_peak * 1e12 / (P["hbm_gbs"] * 1e9):
-        ach = flops / layer_s / 1e12
-        roof = {"bound": "tensor", "achieved": ach, "peak": fp4_peak, "unit": "TFLOP/s", "frac": ach / fp4_peak,
-                "peak_note": "FP4 dense = 6 x measured bf16 %s (%s; nominal 13.5 / 2.25)" % (
-                    "sustained" if long_step else "burst", P["src"])}
-    else:
-        ach = nbytes / layer_s / 1e9
-        roof = {"bound": "hbm", "achieved": ach, "peak": P["hbm_gbs"], "unit": "GB/s", "frac": ach / P["hbm_gbs"],
+
+    def roofline(nbytes, flops, secs):
+        if flops / nbytes > fp4_peak * 1e12 / (P["hbm_gbs"] * 1e9):
+            ach = flops / secs / 1e12
+            return {"bound": "tensor", "achieved": ach, "peak": fp4_peak, "unit": "TFLOP/s", "frac": ach / fp4_peak,
+                    "peak_note": "FP4 dense = 6 x measured bf16 %s (%s; nominal 13.5 / 2.25)" % (
+                        "sustained" if long_step else "burst", P["src"])}
+        ach = nbytes / secs / 1e9
+        return {"bound": "hbm", "achieved": ach, "peak": P["hbm_gbs"], "unit": "GB/s", "frac": ach / P["hbm_gbs"],
                 "peak_note": "%s HBM copy bandwidth" % P["src"]}
-    roof.update({"kernel": "nvfp4 layer (norm_quant + gate/up GEMM with the gated FP4 epilogue + down GEMM, "
-                           "graph-replayed)",
-                 "us_per_launch": 1e6 * layer_s, "algorithmic_bytes": nbytes, "traffic": None})
+
+    # the dominant kernel: each launch's in-stack share of a replay (stamped
+    # replays of the same forward, L2 flushed before each)
+    n_prof = 20
+    shares = []
+    for _ in range(n_prof):
+        if not WARM_L2:
+            with torch.cuda.stream(stream):
+                flush.zero_()
+        shares.append(plan.forward_profile(r, h, out=out, n_replays=1, stream=stream))
+    med = [statistics.median(sh[k] for sh in shares) for k in range(3 * wl.L)]
+    kern_total = {FP4_STEP_NAMES[st]: sum(med[3 * l + st] for l in range(wl.L)) for st in range(3)}
+    dom = max(kern_total, key=kern_total.get)
+    nbytes, flops = fp4_kernel_bytes_flops(wl, wl.M, FP4_STEP_NAMES.index(dom))
+    roof = roofline(nbytes, flops, kern_total[dom] / wl.L * 1e-6)
+    roof.update({"kernel": dom, "us_per_launch": kern_total[dom] / wl.L,
+                 "timing": "in-stack share of each launch (%%globaltimer stamps, median of %d profiled replays): "
+                           "%d x us_per_launch = %.1f us of a %.1f us step" % (
+                               n_prof, wl.L, kern_total[dom], 1000.0 * ms_step),
+                 "algorithmic_bytes": nbytes, "flops": flops,
+                 "traffic": (profiled_traffic("nvfp4_gemm", wl.name, index=FP4_STEP_NAMES.index(dom) - 1)
+                             if dom != "nvfp4_norm_quant" else None)})
+    # the layer (its three kernels together): FP4 weights and their scales +
+    # the residual stream in and out
+    layer_s = ms_step / 1000.0 / wl.L
+    step_roof = roofline(*fp4_layer_bytes_flops(wl, wl.M), layer_s)
     line = {
         "metric": "NVFP4 FFN stack tokens/s (graph-replayed, %s)" % wl.name, "value": value, "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -848,7 +887,8 @@ def run_fp4(args, wl, world, rank, local):
         "dtype": "nvfp4 (e2m1 + e4m3 block scales, fp32 accumulate, bf16 residual)", "data": "synthetic",
         "config": dict(config_of(wl), weights="NVFP4 (E2M1, E4M3 scale per 16, fp32 per tensor)",
                        activations="NVFP4, calibrated per-tensor scales", graph="one CUDA graph per stack"),
-        "roofline": roof,
+        "roofline": roof, "step_roofline": step_roof,
+        "kernels_us_in_stack": {k: v / wl.L for k, v in kern_total.items()},
         "e2e": {"value": world * wl.M * args.steps / e2e_s, "unit": "tokens/s",
                 "h2d_bytes_per_step": h_io.numel() * 2, "d2h_bytes_per_step": h_out.numel() * 2,
                 "ms_per_step": 1000.0 * e2e_s / args.steps},

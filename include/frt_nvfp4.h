@@ -102,6 +102,27 @@ frt_status frt_fp4_forward(frt_fp4_plan_t plan, const void *residual_in, const v
                            frt_stream_t stream);
 
 /*
+ * Measurement: where the time of the stack goes, kernel by kernel, when it
+ * runs as one replayed graph ("FlashRT docs/architecture.md", 7).  Captures
+ * frt_fp4_forward on these buffers into a graph with every launch recording
+ * %globaltimer at its CTAs' starts and ends, replays it n_replays times
+ * (synchronising after each), and writes to kernel_us[k] the median over
+ * replays of launch k's share of the replay: from its first CTA's start, or
+ * the end of the launches before it if later, to its last CTA's end -- so the
+ * shares of launches that overlap (programmatic dependent launch) do not
+ * overlap.  Launch k = 3 l + s for layer l and step s (0 norm + quantise,
+ * 1 gate/up GEMM with the gated FP4 epilogue, 2 down GEMM with the residual);
+ * kernel_us must hold 3 n_layers floats and *n_kernels (may be NULL)
+ * receives that count.  The replays write `out` like frt_fp4_forward.  The
+ * graph is freed before returning.  `stream` must not be the legacy default
+ * stream (a graph is captured on it).  Synchronises.
+ * Errors: INVALID_ARG (M < 1, counts, default stream), NOT_READY, SHAPE,
+ * CUDA, DEVICE_TIMEOUT.
+ */
+frt_status frt_fp4_forward_profile(frt_fp4_plan_t plan, const void *residual_in, const void *hidden_in, void *out,
+                                   int M, int n_replays, float *kernel_us, int *n_kernels, frt_stream_t stream);
+
+/*
  * Test/diagnostic: layer `layer` alone on its input, with the same kernels,
  * copying the intermediates to caller buffers (any may be NULL): r_prime
  * [M, d] BF16 (only when hidden_in is given), x_codes [M, d/2] and x_sf

@@ -78,6 +78,7 @@ SIGNATURES = {
     "frt_fp4_get_scales": (_I, [_P, _FP, _FP]),
     "frt_fp4_set_scales": (_I, [_P, _FP]),
     "frt_fp4_forward": (_I, [_P, _P, _P, _P, _I, _P]),
+    "frt_fp4_forward_profile": (_I, [_P, _P, _P, _P, _I, _I, _FP, ctypes.POINTER(ctypes.c_int), _P]),
     "frt_fp4_debug_trace": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P]),
     "frt_fp4_debug_weights": (_I, [_P, _I, _I, _P, _P, _P]),
     "frt_fp4_debug_trace_from": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P]),
@@ -372,6 +373,15 @@ def frt_fp4_set_scales(plan, act) -> None:
 
 def frt_fp4_forward(plan, residual_in, hidden_in, out, M, stream) -> None:
     _check(lib().frt_fp4_forward(plan, residual_in, hidden_in, out, M, stream))
+
+
+def frt_fp4_forward_profile(plan, residual_in, hidden_in, out, M, n_replays, n_slots, stream) -> list[float]:
+    """Per-launch shares (us) of a replayed graph of the NVFP4 forward (median of n_replays)."""
+    buf = (ctypes.c_float * n_slots)()
+    n = ctypes.c_int(0)
+    _check(lib().frt_fp4_forward_profile(plan, residual_in, hidden_in, out, M, n_replays, buf, ctypes.byref(n),
+                                         stream))
+    return [float(buf[i]) for i in range(n.value)]
 
 
 def frt_fp4_debug_trace(plan, layer, residual_in, hidden_in, out, r_prime, x_codes, x_sf, g_codes, g_sf, u_codes,

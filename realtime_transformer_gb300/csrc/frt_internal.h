@@ -205,7 +205,8 @@ cudaError_t launch_f4_quant_w(const void *w, int rows, int K, const float *col, 
                               uint8_t *sf, int ilv, cudaStream_t s);
 cudaError_t launch_f4_norm_quant(const void *r, const void *h, const void *w, const float *awq_inv, int M, int d,
                                  float eps, float sc, float inv6, void *rprime, uint8_t *q, uint8_t *sf,
-                                 unsigned *amax_word, bool measure, cudaStream_t s, bool pdl);
+                                 unsigned *amax_word, bool measure, cudaStream_t s, bool pdl,
+                                 unsigned long long *stamp = nullptr);  // profiling stamps (null: off)
 
 }  // namespace frt
 

@@ -8,6 +8,7 @@
 // copies), so a forward can be captured into a graph.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -94,6 +95,10 @@ struct frt_fp4_plan {
     std::map<std::pair<int, int>, std::pair<CUtensorMap, int>> tmaps;
     CUtensorMap *tmap_dev = nullptr;
     bool pdl = true;                        // programmatic dependent launch (FRT_FFN_NO_PDL=1 disables)
+    // profiling: while set, launch 3 l + s of a forward (s: 0 norm, 1 gate/up,
+    // 2 down) records its CTAs' %globaltimer span at stamps[2 (3 l + s)]
+    unsigned long long *stamps = nullptr;
+    bool profiling = false;
     std::vector<char> loaded, has_awq;
     bool scaled = false;
 };
@@ -105,7 +110,7 @@ enum F4Buf : int { F_WGU = 0, F_WD = 1, F_XQ = 2, F_HQ = 3 };
 void free_fp4(frt_fp4_plan *P) {
     void *ptrs[] = {P->wgu, P->wd,  P->sgu,     P->sd,  P->w_norm, P->awq_inv, P->xq,       P->xsf,
                     P->hq,  P->hsf, P->rp,      P->res[0], P->res[1], P->amax,  P->err,      P->ws,
-                    P->counters, P->tmap_dev};
+                    P->counters, P->tmap_dev, P->stamps};
     for (void *p : ptrs)
         if (p) cudaFree(p);
     delete P;
@@ -218,6 +223,7 @@ FRT_API frt_status frt_fp4_plan_create(int d, int ff, int act, int M_max, int n_
     if (e == cudaSuccess) e = cudaMalloc(&P->ws, P->ws_floats * 4);
     if (e == cudaSuccess) e = cudaMalloc(&P->counters, (size_t)SPLIT_COUNTERS * 4);
     if (e == cudaSuccess) e = cudaMemset(P->counters, 0, (size_t)SPLIT_COUNTERS * 4);
+    if (e == cudaSuccess) e = cudaMalloc(&P->stamps, L * 3 * 2 * sizeof(unsigned long long));
     // the GEMMs read operand rows (and their scales) up to the 128-row tile:
     // padding starts at zero
     if (e == cudaSuccess) e = cudaMemset(P->xq, 0, MA * D / 2);
@@ -295,6 +301,11 @@ FRT_API frt_status frt_fp4_load_weights(frt_fp4_plan_t P, int layer, const void 
 
 namespace {
 
+// Layer l's step s stamp pair while profiling, else null.
+unsigned long long *f4_stamp(const frt_fp4_plan *P, int l, int s) {
+    return P->profiling ? P->stamps + 2 * ((size_t)3 * l + s) : nullptr;
+}
+
 // N1: norm (+ AWQ) + NVFP4 quantise of layer l's input into the X buffers
 // (measure: the amax of y into amax[0] instead).  With h, r' goes to P->rp.
 cudaError_t f4_norm(frt_fp4_plan *P, int l, const void *r, const void *h, int M, bool measure, cudaStream_t s) {
@@ -302,7 +313,7 @@ cudaError_t f4_norm(frt_fp4_plan *P, int l, const void *r, const void *h, int M,
     return launch_f4_norm_quant(r, h, P->w_norm + (size_t)l * P->d, P->has_awq[l] ? P->awq_inv + (size_t)l * P->d
                                                                                    : nullptr,
                                 M, P->d, F4_RMS_EPS, sx, inv6_of(sx), h ? P->rp : nullptr, P->xq, P->xsf,
-                                P->amax, measure, s, P->pdl);
+                                P->amax, measure, s, P->pdl, f4_stamp(P, l, 0));
 }
 
 // Tensor maps and row offsets of one GEMM of layer l: the weight buffer
@@ -361,6 +372,7 @@ frt_status f4_gate_up(frt_fp4_plan *P, int l, int M, int epi, cudaStream_t s, ui
         p.dbg_us = dbg[3];
     }
     p.stall_test = stall ? 1 : 0;
+    p.stamp = f4_stamp(P, l, 1);
     FCK(launch_gemm(g, s, P->pdl && !stall));
     return FRT_OK;
 }
@@ -390,6 +402,7 @@ frt_status f4_down(frt_fp4_plan *P, int l, const void *resid, void *out, int M, 
     p.ws = P->ws;
     p.counters = split_counters(P->counters, p.splits);
     p.err = P->err;
+    p.stamp = f4_stamp(P, l, 2);
     FCK(launch_gemm(g, s, P->pdl));
     return FRT_OK;
 }
@@ -433,6 +446,65 @@ FRT_API frt_status frt_fp4_forward(frt_fp4_plan_t P, const void *residual_in, co
         cur = dst;
     }
     return FRT_OK;
+}
+
+FRT_API frt_status frt_fp4_forward_profile(frt_fp4_plan_t P, const void *residual_in, const void *hidden_in,
+                                           void *out, int M, int n_replays, float *kernel_us, int *n_kernels,
+                                           frt_stream_t stream) {
+    frt_status st = check_call(P, residual_in, hidden_in, out, M);
+    if (st != FRT_OK)
+        return st;
+    if (M < 1 || !kernel_us || n_replays < 1 || n_replays > 10000)
+        return ffail(FRT_ERR_INVALID_ARG, "need M >= 1, kernel_us and 1 <= n_replays <= 10000");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (!s)
+        return ffail(FRT_ERR_INVALID_ARG, "profiling captures a graph: needs a stream other than the default");
+    // the forward captured once with every launch stamping its pair
+    FCK(cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal));
+    P->profiling = true;
+    st = frt_fp4_forward(P, residual_in, hidden_in, out, M, stream);
+    P->profiling = false;
+    cudaGraph_t graph = nullptr;
+    cudaError_t e = cudaStreamEndCapture(s, &graph);
+    if (st != FRT_OK || e != cudaSuccess) {
+        if (graph)
+            cudaGraphDestroy(graph);
+        return st != FRT_OK ? st : fcuda_fail(e, "profiling capture");
+    }
+    cudaGraphExec_t exec = nullptr;
+    e = cudaGraphInstantiate(&exec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (e != cudaSuccess)
+        return fcuda_fail(e, "profiling graph instantiate");
+    const int nk = 3 * P->L;
+    std::vector<unsigned long long> h(2 * (size_t)nk);
+    std::vector<std::vector<float>> dur(nk);
+    for (int i = 0; i < n_replays && e == cudaSuccess; ++i) {
+        if ((e = cudaMemsetAsync(P->stamps, 0, h.size() * sizeof(unsigned long long), s)) != cudaSuccess) break;
+        if ((e = cudaGraphLaunch(exec, s)) != cudaSuccess) break;
+        if ((e = cudaMemcpyAsync(h.data(), P->stamps, h.size() * sizeof(unsigned long long), cudaMemcpyDeviceToHost,
+                                 s)) != cudaSuccess) break;
+        if ((e = cudaStreamSynchronize(s)) != cudaSuccess) break;
+        // launch k's share: from its first CTA's start, or the end of the
+        // launches before it if later, to its last CTA's end
+        unsigned long long prev_end = 0;
+        for (int k = 0; k < nk; ++k) {
+            const unsigned long long t0 = ~h[2 * k], t1 = h[2 * k + 1];
+            const unsigned long long from = std::max(t0, prev_end);
+            dur[k].push_back(t1 > from ? (float)(t1 - from) * 1e-3f : 0.0f);
+            prev_end = std::max(prev_end, t1);
+        }
+    }
+    cudaGraphExecDestroy(exec);
+    if (e != cudaSuccess)
+        return fcuda_fail(e, "profiling replays");
+    for (int k = 0; k < nk; ++k) {
+        std::sort(dur[k].begin(), dur[k].end());
+        kernel_us[k] = dur[k][dur[k].size() / 2];
+    }
+    if (n_kernels)
+        *n_kernels = nk;
+    return frt_fp4_device_status(P, stream);
 }
 
 FRT_API frt_status frt_fp4_calibrate(frt_fp4_plan_t P, const void *const *residual, const void *const *hidden,

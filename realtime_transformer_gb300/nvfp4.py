@@ -66,6 +66,18 @@ class FP4Plan:
                           _bf16(out, (M, self.d), "out"), M, _stream(stream))
         return out
 
+    def forward_profile(self, residual, hidden=None, out=None, n_replays=20, stream=None):
+        """Per-launch shares (us) of the forward replayed as one graph: index
+        3 l + s for layer l and step s (0 norm, 1 gate/up, 2 down); the
+        median of n_replays.  Needs a stream other than the legacy default."""
+        M = residual.shape[0]
+        if out is None:
+            out = torch.empty_like(residual)
+        return N.frt_fp4_forward_profile(self.handle, _bf16(residual, (M, self.d), "residual"),
+                                         _bf16(hidden, (M, self.d), "hidden") if hidden is not None else None,
+                                         _bf16(out, (M, self.d), "out"), M, n_replays, 3 * self.n_layers,
+                                         _stream(stream))
+
     def trace(self, layer, residual, hidden=None, stream=None):
         """One layer with its intermediates: codes are packed uint8 (two per
         byte), x_sf / h_sf in the TMEM-ready layout, g_sf / u_sf row-major."""

@@ -95,6 +95,7 @@ def test_nvfp4_entry_points_check_arguments_before_any_cuda_call(native):
     assert L.frt_fp4_set_scales(None, None) == 1
     assert L.frt_fp4_device_status(None, None) == 1
     assert L.frt_fp4_debug_stall(None, 8, None) == 1
+    assert L.frt_fp4_forward_profile(None, None, None, None, 8, 1, None, None, None) == 1
     assert L.frt_fp4_debug_trace_from(None, 0, None, None, None, None, None, None, None, None, None, None, None,
                                       None, None, 8, None) == 1
     assert L.frt_fp4_debug_trace(None, 0, None, None, None, None, None, None, None, None, None, None, None, None,

@@ -314,6 +314,42 @@ def test_forward_can_be_captured_in_a_cuda_graph(layer_case):
     assert torch.equal(out, eager)
 
 
+def test_forward_profile_splits_the_stack_and_computes_the_forward():
+    """The stamped replays: one share per launch (3 per layer), each positive,
+    together at most the replay's span; the profiled graph writes the same
+    output as the eager forward."""
+    from realtime_transformer_gb300.nvfp4 import FP4Plan
+    wl = synthetic.WORKLOADS["tiny"].with_(L=3, M=40)
+    plan = FP4Plan(wl.d, wl.ff, wl.act, wl.M, wl.L)
+    try:
+        for l in range(wl.L):
+            w = synthetic.layer_weights(wl, l, device=torch.device("cuda"))
+            plan.load_weights(l, w["w_norm"], w["w_gate"], w["w_up"], w["w_down"])
+        plan.set_scales([[0.02, 0.05, 0.05, 0.01]] * wl.L)
+        r, h = (t.cuda() for t in synthetic.inputs(wl))
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            eager = plan.forward(r, h, stream=s)
+            s.synchronize()
+            out = torch.zeros_like(eager)
+            shares = plan.forward_profile(r, h, out=out, n_replays=5, stream=s)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            for _ in range(10):
+                plan.forward(r, h, out=out, stream=s)
+            e1.record(s)
+        s.synchronize()
+        assert torch.equal(out, eager)
+        assert len(shares) == 3 * wl.L
+        assert all(x > 0.0 for x in shares), shares
+        # the eager forward's time bounds the replayed graph's stamped span
+        assert sum(shares) <= e0.elapsed_time(e1) * 1000.0 / 10 + 5.0, (sum(shares), shares)
+        with pytest.raises(Exception):
+            plan.forward_profile(r, h, out=out, n_replays=0, stream=s)
+    finally:
+        plan.close()
+
+
 def test_gpu_calibration_and_stack_match_oracle():
     from realtime_transformer_gb300.nvfp4 import FP4Plan
     wl = synthetic.WORKLOADS["tiny"].with_(L=3, M=40)
