@@ -61,6 +61,27 @@ def test_nvfp4_layer_bytes():
     assert f == 6.0 * 5120 * 17408
 
 
+def test_nvfp4_kernel_bytes_add_up_to_the_layer():
+    """The NVFP4 launches' algorithmic bytes: the two GEMMs carry all the
+    weight codes and scales and the residual stream; without the activations
+    passed between them (A written by one, read by the other; X read from the
+    norm) they are the layer's bytes.  The norm reads the residual and its
+    weight and writes X."""
+    for name in ("llm_decode", "vla_action_expert", "long_prefill"):
+        wl = synthetic.WORKLOADS[name]
+        M, d, ff = wl.M, wl.d, wl.ff
+        n, g, w = (bench.fp4_kernel_bytes_flops(wl, M, s) for s in range(3))
+        x = M * d // 2 + M * d // 16     # X codes + scales: written by the norm, read by the gate/up GEMM
+        a = M * ff // 2 + M * ff // 16   # A codes + scales: written by the gate/up GEMM, read by the down GEMM
+        layer_b, layer_f = bench.fp4_layer_bytes_flops(wl, M)
+        assert g[0] + w[0] - x - 2 * a == layer_b
+        assert n[0] == 2 * M * d + 2 * d + x
+        assert n[1] + g[1] + w[1] == layer_f
+    # the decode gate/up figure the profile summary divides by
+    wl = synthetic.WORKLOADS["llm_decode"]
+    assert bench.fp4_kernel_bytes_flops(wl, 1, 1)[0] == 100282752
+    assert bench.fp4_kernel_bytes_flops(wl, 1, 2)[0] == 50165312
+
 
 def test_l2_note_states_the_flush(monkeypatch):
     assert bench.l2_note().startswith("flushed")
