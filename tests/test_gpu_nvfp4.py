@@ -191,6 +191,8 @@ CASES = {
     "tiny": synthetic.WORKLOADS["tiny"],
     "action_expert": synthetic.WORKLOADS["vla_action_expert"].with_(L=1),
     "ragged": synthetic.WORKLOADS["tiny"].with_(name="ragged", M=300, d=512, ff=1024, act="swiglu", seed=5),
+    # one token, as decode: the weight-streaming role's 16-token tile with 15 padding rows
+    "m1_swiglu": synthetic.WORKLOADS["tiny"].with_(name="m1_swiglu", M=1, d=1024, ff=2048, act="swiglu", seed=6),
 }
 
 
